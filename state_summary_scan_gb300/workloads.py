@@ -1,0 +1,136 @@
+"""Seeded synthetic workloads for chunkwise gated linear attention.
+
+This module only draws random inputs; it holds none of the method's
+arithmetic.  Both the fp64 oracle (through the tests and the bench's CPU leg)
+and the CUDA path are fed from the tensors it returns, so the two sides always
+see identical values.
+
+Recipe (one torch CPU generator, seed 0, fixed draw order):
+  1. packed workloads only: sequence lengths ~ U{512, ..., 8192}, drawn until
+     their sum reaches T, the last one cut so the sum is exactly T;
+  2. q ~ N(0, 1)                                   [B, T, H, Dk]
+  3. k ~ N(0, 1), L2-normalised per (token, head)  [B, T, H, Dk]
+  4. v ~ N(0, 1)                                   [B, T, H, Dv]
+  5. g = logsigmoid(N(0, 1) + c), fp32             [B, T, H]
+  6. dO ~ N(0, 1)                                  [B, T, H, Dv]
+All draws are fp32; q, k, v and dO are then rounded to the workload dtype.
+The gate shift c is 3 for the tiny case, 4 for the 4k/32k/packed cases and 5
+for the 256k case, so a segment's summed gate lies between about -45 and -62.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    T: int
+    H: int
+    Dk: int
+    Dv: int
+    dtype: str            # "f32" or "bf16": storage type of q, k, v, o, dO, dq, dk, dv
+    num_segments: int
+    chunk: int
+    gate_shift: float
+    packed: bool = False
+    backward: bool = True
+    seed: int = 0
+
+    @property
+    def seg_len(self) -> int:
+        return self.T // self.num_segments
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.Dk)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", B=1, T=256, H=2, Dk=32, Dv=32, dtype="f32",
+                     num_segments=4, chunk=64, gate_shift=3.0),
+    "fwd4k": Workload("fwd4k", B=2, T=4096, H=8, Dk=128, Dv=128, dtype="bf16",
+                      num_segments=8, chunk=64, gate_shift=4.0, backward=False),
+    "32k": Workload("32k", B=1, T=32768, H=16, Dk=128, Dv=128, dtype="bf16",
+                    num_segments=16, chunk=64, gate_shift=4.0),
+    "packed64k": Workload("packed64k", B=1, T=65536, H=32, Dk=128, Dv=128, dtype="bf16",
+                          num_segments=32, chunk=64, gate_shift=4.0, packed=True),
+    "256k": Workload("256k", B=1, T=262144, H=16, Dk=128, Dv=256, dtype="bf16",
+                     num_segments=64, chunk=64, gate_shift=5.0),
+}
+
+
+def draw_lengths(gen: torch.Generator, total: int, lo: int = 512, hi: int = 8192) -> list:
+    """Sequence lengths ~ U{lo..hi} until they cover `total`; the last is cut."""
+    lengths = []
+    acc = 0
+    while acc < total:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=gen).item())
+        n = min(n, total - acc)
+        lengths.append(n)
+        acc += n
+    return lengths
+
+
+def cu_seqlens_from_lengths(lengths) -> torch.Tensor:
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+@dataclasses.dataclass
+class Inputs:
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    g: torch.Tensor
+    dO: Optional[torch.Tensor]
+    cu_seqlens: Optional[torch.Tensor]   # int32 [N+1] for packed workloads, else None
+
+
+def make_inputs(w: Workload, with_grad: Optional[bool] = None,
+                gate_shift: Optional[float] = None) -> Inputs:
+    """Draw the workload's inputs on the CPU (deterministic for a given seed)."""
+    if with_grad is None:
+        with_grad = w.backward
+    c = w.gate_shift if gate_shift is None else gate_shift
+    gen = torch.Generator("cpu").manual_seed(w.seed)
+    cu = None
+    if w.packed:
+        cu = cu_seqlens_from_lengths(draw_lengths(gen, w.T))
+    dt = w.torch_dtype
+    q = torch.randn(w.B, w.T, w.H, w.Dk, generator=gen, dtype=torch.float32)
+    k = torch.randn(w.B, w.T, w.H, w.Dk, generator=gen, dtype=torch.float32)
+    k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+    v = torch.randn(w.B, w.T, w.H, w.Dv, generator=gen, dtype=torch.float32)
+    g = torch.nn.functional.logsigmoid(
+        torch.randn(w.B, w.T, w.H, generator=gen, dtype=torch.float32) + c)
+    dO = None
+    if with_grad:
+        dO = torch.randn(w.B, w.T, w.H, w.Dv, generator=gen, dtype=torch.float32).to(dt)
+    return Inputs(q=q.to(dt), k=k.to(dt), v=v.to(dt), g=g.contiguous(), dO=dO, cu_seqlens=cu)
+
+
+def random_cu_seqlens(gen: torch.Generator, T: int, max_len: int) -> torch.Tensor:
+    """Random packing of T tokens into sequences of length 1..max_len (test helper)."""
+    lengths = []
+    acc = 0
+    while acc < T:
+        n = int(torch.randint(1, max_len + 1, (1,), generator=gen).item())
+        n = min(n, T - acc)
+        lengths.append(n)
+        acc += n
+    return cu_seqlens_from_lengths(lengths)
