@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark: fwd+bwd tokens/s of chunkwise gated linear attention on one GB300.
+
+One step = the whole path on one batch of the workload: forward_prepare,
+compose_prefix, forward_apply, backward_prepare, compose_suffix,
+backward_apply (forward only for forward-only workloads), all through the
+C ABI on the current stream, inputs resident in HBM.
+
+Prints ONE JSON line (rank 0).  Besides the step throughput it reports:
+  roofline      the dominant kernel's algorithmic bytes per launch over its
+                CUDA-event launch time, against the measured HBM copy peak;
+  path_roofline the whole step against max(flops / bf16 peak, bytes / HBM peak);
+  e2e           the same metric with pinned host buffers copied in and out
+                inside every timed step;
+  cpu_baseline  the fp64 CPU oracle timed on a bounded sample of the workload;
+  clocks        nvidia-smi samples taken during the timed region.
+
+--impl reference times the fp64 CPU oracle itself as the reference arm.
+Multi-GPU (torchrun): independent replicas, one per GPU, weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from state_summary_scan_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "fwd+bwd tokens/sec on 1 GB300; % of bf16 tensor/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 2 ** 20
+PHASES_FWD = ("forward_prepare", "compose_prefix", "forward_apply")
+PHASES_BWD = ("backward_prepare", "compose_suffix", "backward_apply")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ accounting
+
+def kernel_bytes(w, phase):
+    """Algorithmic bytes of one launch: each input read once, each output
+    written once (tokens: [B,T,H] rows; summaries: [nseg,B,H] states)."""
+    e = 4 if w.dtype == "f32" else 2
+    ntok = w.B * w.T * w.H
+    nsum = w.num_segments * w.B * w.H
+    st = 4 * w.Dk * w.Dv
+    Dk, Dv = w.Dk, w.Dv
+    if phase == "forward_prepare":
+        return ntok * (e * (Dk + Dv) + 4) + nsum * (st + 4)
+    if phase == "compose_prefix":
+        return nsum * (2 * st + 4)
+    if phase == "forward_apply":
+        return ntok * (e * (2 * Dk + Dv) + 4 + e * Dv) + nsum * st
+    if phase == "backward_prepare":
+        return ntok * (e * (2 * Dk + 2 * Dv) + 4 + e * Dk + 4) + nsum * 2 * st
+    if phase == "compose_suffix":
+        return nsum * (2 * st + 4)
+    if phase == "backward_apply":
+        return ntok * (e * (2 * Dk + 2 * Dv) + 4 + 4 + e * (Dk + Dv) + 4) + nsum * 2 * st
+    raise KeyError(phase)
+
+
+def path_roofline(w, peaks):
+    """Roofline of one step of the method (chunk C): algorithmic flops and
+    bytes per token and head, plus summary traffic per segment, row and head."""
+    e = 4 if w.dtype == "f32" else 2
+    C, Dk, Dv = w.chunk, w.Dk, w.Dv
+    ntok = w.B * w.T * w.H
+    nsum = w.num_segments * w.B * w.H
+    flops = ntok * (C * (Dk + Dv) + 4 * Dk * Dv)
+    byts = ntok * (e * (2 * Dk + Dv) + 4 + e * Dv) + nsum * (16 * Dk * Dv + 8)
+    if w.backward:
+        flops += ntok * (C * (3 * Dk + 2 * Dv) + 8 * Dk * Dv)
+        byts += ntok * (2 * e * (2 * Dk + Dv) + e * Dv + 8) + nsum * (16 * Dk * Dv + 8)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    return dict(flops=flops, bytes=byts, t_tc_us=t_tc * 1e6, t_hbm_us=t_hbm * 1e6,
+                bound="hbm" if t_hbm >= t_tc else "tensor", t_roofline_us=max(t_tc, t_hbm) * 1e6)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample_run(w, inp, ntok, threads=0):
+    """fp64 oracle fwd (+bwd) on the first ntok tokens of every row and head."""
+    import oracle
+    cores = oracle.set_threads(threads)
+    sl = slice(0, ntok)
+    q, k, v, g = inp.q[:, sl], inp.k[:, sl], inp.v[:, sl], inp.g[:, sl]
+    si = None
+    if inp.cu_seqlens is not None:
+        md = oracle.packed_metadata(inp.cu_seqlens, w.T, oracle.equal_segments(w.T, w.num_segments))
+        si = md["seq_idx"][:ntok]
+    args = [oracle._f64(x) for x in (q, k, v, g)]
+    dO = oracle._f64(inp.dO[:, sl]) if w.backward else None
+    t0 = time.perf_counter()
+    oracle.forward(*args, w.scale, si)
+    if w.backward:
+        oracle.backward(*args, dO, w.scale, si)
+    return time.perf_counter() - t0, cores
+
+
+def calibrate_oracle(w, inp, target_s):
+    """Number of tokens (per row) whose oracle run takes about target_s."""
+    ntok = 64
+    dt, _ = oracle_sample_run(w, inp, ntok)
+    per_tok = max(dt / ntok, 1e-9)
+    n = int(target_s / per_tok)
+    return max(64, min(w.T, n - n % 64))
+
+
+def cpu_baseline(w, inp, target_s=12.0):
+    ntok = calibrate_oracle(w, inp, target_s)
+    dt, cores = oracle_sample_run(w, inp, ntok)
+    value = w.B * ntok / dt
+    return {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle {'fwd+bwd' if w.backward else 'fwd'} on the first {ntok} of "
+                      f"{w.T} tokens of all {w.B} rows x {w.H} heads, {dt:.1f} s wall",
+            "seconds": dt}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, rank, world, local_rank):
+    from state_summary_scan_gb300 import _capi as C
+    from state_summary_scan_gb300 import api
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    inp = make_inputs(w)
+    q, k, v, g = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.g))
+    dO = inp.dO.to(dev) if w.backward else None
+    plan = api.make_plan(w.B, w.T, w.H, w.Dk, w.Dv, w.num_segments, w.chunk, w.scale,
+                         q.dtype, inp.cu_seqlens, dev, w.backward)
+    o = torch.empty_like(v)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg = torch.empty_like(g)
+    s = plan.spec
+    stream = torch.cuda.current_stream(dev)
+    phases = PHASES_FWD + (PHASES_BWD if w.backward else ())
+
+    def calls(q, k, v, g, dO, o, dq, dk, dv, dg):
+        return {
+            "forward_prepare": lambda: C.rm_cp_forward_prepare(s, k, v, g, plan.M, plan.dS, plan.ws, stream),
+            "compose_prefix": lambda: C.rm_cp_compose_prefix(s, plan.M, plan.dS, plan.S_in, stream),
+            "forward_apply": lambda: C.rm_cp_forward_apply(s, q, k, v, g, plan.S_in, o, plan.ws, stream),
+            "backward_prepare": lambda: C.rm_cp_backward_prepare(s, q, k, v, g, plan.S_in, dO, plan.gamma,
+                                                                 dq, plan.ws, stream),
+            "compose_suffix": lambda: C.rm_cp_compose_suffix(s, plan.M, plan.gamma, plan.dS_out, stream),
+            "backward_apply": lambda: C.rm_cp_backward_apply(s, q, k, v, g, dO, plan.S_in, plan.dS_out,
+                                                             dk, dv, dg, plan.ws, stream),
+        }
+
+    fns = calls(q, k, v, g, dO, o, dq, dk, dv, dg)
+
+    def step(events=None):
+        for i, ph in enumerate(phases):
+            if events is not None:
+                events[i].record(stream)
+            fns[ph]()
+        if events is not None:
+            events[len(phases)].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
+          for _ in range(args.steps)]
+    l0 = C.rm_cp_launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = C.rm_cp_launch_count() - l0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tok_per_step = w.B * w.T
+    value = world * tok_per_step / (ms_per_step / 1e3)
+
+    phase_ms = {ph: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                for j, ph in enumerate(phases)}
+    dom = max(phase_ms, key=phase_ms.get)
+    dom_bytes = kernel_bytes(w, dom)
+    achieved = dom_bytes / (phase_ms[dom] / 1e3) / 1e9
+    traffic = load_traffic(args.workload, dom)
+    roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "traffic": traffic, "algorithmic_bytes": dom_bytes, "launch_us": phase_ms[dom] * 1e3,
+            "peak_source": peak_src}
+    pr = path_roofline(w, peaks)
+    path = {"bound": pr["bound"], "t_roofline_us": pr["t_roofline_us"],
+            "t_measured_us": ms_per_step * 1e3, "frac": pr["t_roofline_us"] / (ms_per_step * 1e3),
+            "flops": pr["flops"], "bytes": pr["bytes"], "peak_source": peak_src,
+            "phases_us": {ph: round(t * 1e3, 2) for ph, t in phase_ms.items()},
+            "phase_frac_of_hbm": {ph: round(kernel_bytes(w, ph) / (phase_ms[ph] / 1e3) / 1e9
+                                            / peaks["hbm_gbs"], 4) for ph in phases}}
+
+    # ---- end to end: pinned host buffers in, results out, every step
+    e2e = None
+    if not args.no_e2e:
+        hin = [t.pin_memory() for t in (inp.q, inp.k, inp.v, inp.g) + ((inp.dO,) if w.backward else ())]
+        outs = [o] + ([dq, dk, dv, dg] if w.backward else [])
+        hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+        dins = [torch.empty_like(t, device=dev) for t in hin]
+        fns_e2e = calls(*(dins[:4]), dins[4] if w.backward else None, o, dq, dk, dv, dg)
+
+        def e2e_step():
+            for d_, h_ in zip(dins, hin):
+                d_.copy_(h_, non_blocking=True)
+            for ph in phases:
+                fns_e2e[ph]()
+            for h_, d_ in zip(hout, outs):
+                h_.copy_(d_, non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 3))):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, args.steps // 2)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(b) / n_e2e
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * tok_per_step / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
+               "ms_per_step": e_ms}
+
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, g) + ((dO,) if dO is not None else ()))
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp, args.cpu_seconds)
+
+    path_kind = C.rm_cp_path(s)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if (w.dtype == "bf16" and path_kind == 1) else "f32",
+        "data": "synthetic (seeded: q,k,v,dO ~ N(0,1), k L2-normalised, g = logsigmoid(N(0,1)+c))",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
+                   "num_segments": w.num_segments, "chunk": w.chunk, "storage": w.dtype,
+                   "mode": "fwd+bwd" if w.backward else "fwd", "packed": w.packed,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB > 129 MiB), no flush",
+                   "kernel_path": "tcgen05" if path_kind == 1 else "simt-fp32"},
+        "roofline": roof, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(launches), "clocks": clk,
+    }
+    return line
+
+
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm, timed per step on host cores."""
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    budget = max(2.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    ntok = calibrate_oracle(w, inp, budget)
+    for _ in range(args.warmup):
+        oracle_sample_run(w, inp, ntok)
+    times = []
+    cores = 1
+    for _ in range(args.steps):
+        dt, cores = oracle_sample_run(w, inp, ntok)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = w.B * ntok / (ms / 1e3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
+                   "num_segments": w.num_segments, "chunk": w.chunk,
+                   "mode": "fwd+bwd" if w.backward else "fwd"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"fp64 oracle on the first {ntok} of {w.T} tokens of all "
+                                   f"{w.B} rows x {w.H} heads per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def load_traffic(workload, kernel):
+    """DRAM bytes per launch from a committed ncu capture, if one matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        table = json.load(f)
+    entry = table.get(workload, {}).get(kernel)
+    return None if entry is None else entry.get("bytes_per_launch")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        line = run_ours(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

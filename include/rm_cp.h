@@ -1,0 +1,240 @@
+/*
+ * rm_cp.h -- C ABI of the GB300 (sm_103a) chunkwise gated linear attention
+ * library, organised around per-segment affine state summaries.
+ *
+ * Method, per batch row b and head h (q_t, k_t in R^Dk, v_t in R^Dv, g_t a
+ * scalar gate, alpha_t = exp(g_t), or 0 when token t starts a sequence):
+ *     S_t = alpha_t S_{t-1} + k_t v_t^T,      o_t = scale * S_t^T q_t.
+ * The sequence axis is cut into num_segments equal contiguous segments, the
+ * "shards" of the Megatron-Core API docs page
+ * "core.ssm.context_parallel.chunkwise"; here all of them live on one GPU and
+ * no collective is involved.  The six compute calls follow that page's
+ * LinearAttentionCPBackend protocol and its two drivers:
+ *
+ *   forward   rm_cp_forward_prepare  -> (M, delta_S) per segment   [cp_forward_prepare]
+ *             rm_cp_compose_prefix   -> S_in per segment            [chunkwise_cp_forward]
+ *             rm_cp_forward_apply    -> o                           [cp_forward_apply]
+ *   backward  rm_cp_backward_prepare -> gamma per segment (+ dq)    [cp_backward_prepare]
+ *             rm_cp_compose_suffix   -> dS_out per segment          [chunkwise_cp_backward]
+ *             rm_cp_backward_apply   -> dk, dv, dg                  [cp_backward_apply]
+ *
+ * Conventions for every call:
+ *   - Layouts are contiguous row-major: q, k, dq, dk [B,T,H,Dk]; v, o, dO, dv
+ *     [B,T,H,Dv]; g, dg [B,T,H] (fp32); summaries [nseg,B,H,Dk,Dv] (fp32);
+ *     M [nseg,B,H] (fp32).  Segment j covers tokens [j*L, (j+1)*L) of every
+ *     row, L = T / num_segments.
+ *   - q, k, v, o, dO, dq, dk, dv have the problem's dtype (RM_F32 or RM_BF16;
+ *     bf16 results are rounded to nearest even from fp32).  g, dg, M and all
+ *     summaries are always fp32.
+ *   - Every pointer passed to a compute call is a DEVICE pointer, 16-byte
+ *     aligned, owned by the caller.  The library never allocates, frees or
+ *     synchronises; it only enqueues kernels on the given stream (0 = the
+ *     legacy default stream).  Outputs are fully overwritten.
+ *   - All validation happens on the host before anything is launched.  On a
+ *     non-OK status nothing was enqueued; rm_cp_last_error() returns a
+ *     thread-local description.  Launch failures map to RM_ERR_CUDA.  Kernels
+ *     contain no traps and no inter-block waits.
+ *   - Calls are thread-safe; concurrent calls on different streams may not
+ *     share output buffers.
+ */
+#ifndef RM_CP_H
+#define RM_CP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without requiring cuda_runtime.h */
+typedef struct CUstream_st* rm_stream_t;
+
+typedef enum {
+    RM_OK = 0,
+    RM_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad enum          */
+    RM_ERR_SHAPE = 2,       /* T % num_segments, (T/nseg) % chunk, size overflow  */
+    RM_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned                   */
+    RM_ERR_UNSUPPORTED = 4, /* head dims outside the supported set                */
+    RM_ERR_METADATA = 5,    /* cu_seqlens not 0 = cu[0] < ... < cu[n] = T          */
+    RM_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed               */
+    RM_ERR_TIMEOUT = 7      /* reserved for bounded device-side waits             */
+} rm_status;
+
+typedef enum { RM_F32 = 0, RM_BF16 = 1 } rm_dtype;
+
+/*
+ * Problem description shared by all calls.
+ *   B, T, H, Dk, Dv  batch rows, tokens per row, heads, key and value dims.
+ *                    Supported: Dk in {16, 32, 64, 128}; Dv a multiple of 8
+ *                    in [8, 256].
+ *   num_segments     contiguous segments per row; T % num_segments == 0.
+ *   chunk            the chunk length of the chunkwise form; the segment
+ *                    length must be a multiple of it.  The result does not
+ *                    depend on it beyond rounding: kernels block the
+ *                    sequence axis in tiles of their own.
+ *   scale            output scale (commonly 1/sqrt(Dk)); passed explicitly.
+ *   seq_idx          NULL: every row is one sequence.  Otherwise a device
+ *                    int32 [T] array of non-decreasing sequence ids
+ *                    (PackedSequenceCPMetadata.local_seq_idx, concatenated
+ *                    over segments), applied to every row; token t starts a
+ *                    sequence when t == 0 or seq_idx[t] != seq_idx[t-1].
+ *   preceding_start  NULL (all prefixes start at segment 0) or device int32
+ *                    [num_segments]: inclusive first segment of segment j's
+ *                    forward-summary prefix (preceding_rank_start).
+ *   following_stop   NULL (all suffixes end at num_segments) or device int32
+ *                    [num_segments]: exclusive end of segment j's
+ *                    backward-summary suffix (following_rank_stop).
+ * Out-of-range metadata values are clamped on the device to [0, j] and
+ * [j+1, num_segments]; rm_cp_build_packed_metadata produces valid ones.
+ */
+typedef struct {
+    int32_t B, T, H, Dk, Dv;
+    int32_t num_segments;
+    int32_t chunk;
+    float scale;
+    rm_dtype dtype;
+    const int32_t* seq_idx;
+    const int32_t* preceding_start;
+    const int32_t* following_stop;
+} rm_cp_problem;
+
+/*
+ * Host helper: rank-local packed-sequence metadata for every segment
+ * (PackedSequenceCPMetadata / build_packed_sequence_cp_metadata on the
+ * Megatron-Core page).  All arrays are HOST memory owned by the caller.
+ *   cu_seqlens_host       [num_seqs+1], 0 = cu[0] < cu[1] < ... < cu[num_seqs] = T
+ *   seq_idx_host          out [T]: i for cu[i] <= t < cu[i+1]
+ *   local_cu_seqlens_host out, concatenated per segment: 0, every sequence
+ *                         start strictly inside the segment (relative to the
+ *                         segment start), then L.  Capacity needed:
+ *                         num_seqs + 2*num_segments entries.
+ *   local_cu_offsets_host out [num_segments+1]: segment j's entries are
+ *                         [off[j], off[j+1]).
+ *   preceding_start_host  out [num_segments]: segment holding the start of
+ *                         the sequence that holds segment j's first token.
+ *   following_stop_host   out [num_segments]: 1 + segment holding the last
+ *                         token of the sequence that holds segment j's last
+ *                         token.
+ * Errors: RM_ERR_INVALID_ARG (null pointer, non-positive sizes),
+ * RM_ERR_SHAPE (T % num_segments), RM_ERR_METADATA (bad cu_seqlens).
+ */
+rm_status rm_cp_build_packed_metadata(const int32_t* cu_seqlens_host, int32_t num_seqs,
+                                      int32_t T, int32_t num_segments,
+                                      int32_t* seq_idx_host,
+                                      int32_t* local_cu_seqlens_host,
+                                      int32_t* local_cu_offsets_host,
+                                      int32_t* preceding_start_host,
+                                      int32_t* following_stop_host);
+
+/* Validate a problem without launching anything (RM_OK if every call accepts it). */
+rm_status rm_cp_validate(const rm_cp_problem* p);
+
+/*
+ * Bytes of device workspace the calls need for this problem (0 if none; 0
+ * also for an invalid problem).  The SAME workspace must be passed, unchanged
+ * in between, to rm_cp_backward_prepare and the rm_cp_backward_apply that
+ * follows it: the first leaves per-token partial gate gradients there for the
+ * second.  The forward calls accept NULL.
+ */
+size_t rm_cp_workspace_size(const rm_cp_problem* p);
+
+/*
+ * cp_forward_prepare ("compute the local state summary with zero incoming
+ * state"), for every segment at once.
+ *   k [B,T,H,Dk], v [B,T,H,Dv] (dtype), g [B,T,H] fp32       in
+ *   M [nseg,B,H] fp32: exp(sum of the segment's gates), or 0 when one of its
+ *     tokens starts a sequence (its first token included)     out
+ *   dS [nseg,B,H,Dk,Dv] fp32: the segment's end state from S_in = 0   out
+ *   ws: unused (may be NULL).
+ */
+rm_status rm_cp_forward_prepare(const rm_cp_problem* p, const void* k, const void* v,
+                                const float* g, float* M, float* dS, void* ws,
+                                rm_stream_t stream);
+
+/*
+ * chunkwise_cp_forward's causal prefix: for every segment j,
+ *   S_in[j] = sum_{i in [pre_j, j)} (M_{i+1} ... M_{j-1}) dS_i,
+ * i.e. the summaries of segments pre_j .. j-1 (CPForwardUnpackedSummary:
+ * S_out = M S_in + delta_S) applied in order to a zero state.
+ *   M [nseg,B,H], dS [nseg,B,H,Dk,Dv] fp32 in;  S_in [nseg,B,H,Dk,Dv] fp32 out.
+ */
+rm_status rm_cp_compose_prefix(const rm_cp_problem* p, const float* M, const float* dS,
+                               float* S_in, rm_stream_t stream);
+
+/*
+ * cp_forward_apply ("compose the preceding summaries and compute the local
+ * output"): o_t for every token, each segment starting from its S_in.
+ *   q, k [B,T,H,Dk], v [B,T,H,Dv] (dtype), g fp32, S_in fp32   in
+ *   o [B,T,H,Dv] (dtype)                                        out
+ *   ws: unused (may be NULL).
+ */
+rm_status rm_cp_forward_apply(const rm_cp_problem* p, const void* q, const void* k,
+                              const void* v, const float* g, const float* S_in, void* o,
+                              void* ws, rm_stream_t stream);
+
+/*
+ * cp_backward_prepare ("compute local gamma with zero outgoing-state
+ * gradient"), for every segment, for the loss L = sum_t dO_t . o_t:
+ *   gamma_j = dL_j / dS_in[j] = sum over tokens t of segment j that belong to
+ *             the sequence open at its first token a of
+ *             (alpha_a ... alpha_t) * scale * q_t dO_t^T.
+ * dq depends only on forward-direction states, all known once S_in is, so
+ * this call also writes dq_t = scale * S_t dO_t and leaves q_t . dq_t per
+ * token in the workspace for rm_cp_backward_apply.
+ *   q, k [B,T,H,Dk], v, dO [B,T,H,Dv] (dtype), g fp32, S_in fp32   in
+ *   gamma [nseg,B,H,Dk,Dv] fp32, dq [B,T,H,Dk] (dtype)             out
+ *   ws: device workspace of rm_cp_workspace_size bytes             out
+ */
+rm_status rm_cp_backward_prepare(const rm_cp_problem* p, const void* q, const void* k,
+                                 const void* v, const float* g, const float* S_in,
+                                 const void* dO, float* gamma, void* dq, void* ws,
+                                 rm_stream_t stream);
+
+/*
+ * chunkwise_cp_backward's reverse-causal suffix: for every segment j,
+ *   dS_out[j] = sum_{i in (j, fol_j)} (M_{j+1} ... M_{i-1}) gamma_i,
+ * i.e. CPBackwardUnpackedSummary dS_in = M^T dS_out + gamma (M is a scalar
+ * per row and head here) applied from segment fol_j - 1 down to j + 1.
+ *   M [nseg,B,H], gamma [nseg,B,H,Dk,Dv] fp32 in;  dS_out fp32 out.
+ */
+rm_status rm_cp_compose_suffix(const rm_cp_problem* p, const float* M, const float* gamma,
+                               float* dS_out, rm_stream_t stream);
+
+/*
+ * cp_backward_apply ("compose the reverse-causal suffix and finish the local
+ * input gradients"): dk, dv and dg of every token, each segment's adjoint
+ * starting from dS_out[j] at its last token.
+ *   dk_t = D_t v_t, dv_t = D_t^T k_t with D_t = scale q_t dO_t^T + alpha_{t+1} D_{t+1};
+ *   dg_t = sum_{r >= t, same sequence} (q_r . dq_r - k_r . dk_r), exactly 0 at
+ *          sequence starts; the part beyond the segment is <S_out, dS_out>,
+ *          with S_out read as S_in[j+1] (equal to the segment's end state
+ *          whenever dS_out[j] is not zero).
+ *   q, k [B,T,H,Dk], v, dO [B,T,H,Dv] (dtype), g, S_in, dS_out fp32   in
+ *   ws: the workspace rm_cp_backward_prepare filled                    in
+ *   dk [B,T,H,Dk], dv [B,T,H,Dv] (dtype), dg [B,T,H] fp32             out
+ */
+rm_status rm_cp_backward_apply(const rm_cp_problem* p, const void* q, const void* k,
+                               const void* v, const float* g, const void* dO,
+                               const float* S_in, const float* dS_out, void* dk, void* dv,
+                               float* dg, void* ws, rm_stream_t stream);
+
+/* Name of a status code (static string). */
+const char* rm_cp_status_string(rm_status s);
+
+/* Thread-local detail for the last non-OK status returned on this thread. */
+const char* rm_cp_last_error(void);
+
+/* Number of kernels this library has enqueued in this process so far (all
+ * devices, all threads).  A diagnostic for counting launches per step. */
+uint64_t rm_cp_launch_count(void);
+
+/* Which kernel family a problem runs on: 0 = generic SIMT fp32 path,
+ * 1 = tensor-core (tcgen05) path.  -1 for an invalid problem. */
+int32_t rm_cp_path(const rm_cp_problem* p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RM_CP_H */

@@ -1,0 +1,111 @@
+"""PyTorch-facing entry points: buffer allocation and the call sequence.
+
+The work is the six C-ABI calls, issued in the order of the Megatron-Core
+page "core.ssm.context_parallel.chunkwise" (chunkwise_cp_forward:
+prepare -> prefix -> apply; chunkwise_cp_backward: prepare -> suffix ->
+apply).  PyTorch only provides device memory and the stream.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+from . import _capi as C
+
+
+@dataclasses.dataclass
+class Plan:
+    """Problem description plus every intermediate buffer of one step."""
+    spec: C.ProblemSpec
+    M: torch.Tensor          # [nseg,B,H] fp32
+    dS: torch.Tensor         # [nseg,B,H,Dk,Dv] fp32 (forward summaries)
+    S_in: torch.Tensor       # [nseg,B,H,Dk,Dv] fp32
+    gamma: torch.Tensor      # [nseg,B,H,Dk,Dv] fp32 (backward summaries)
+    dS_out: torch.Tensor     # [nseg,B,H,Dk,Dv] fp32
+    ws: torch.Tensor         # uint8 workspace
+    metadata: Optional[dict] = None   # host metadata of a packed problem
+
+
+def make_plan(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch.bfloat16,
+              cu_seqlens=None, device="cuda", backward=True) -> Plan:
+    if scale is None:
+        scale = 1.0 / math.sqrt(Dk)
+    meta = None
+    seq_idx = pre = fol = None
+    if cu_seqlens is not None:
+        meta = C.rm_cp_build_packed_metadata(cu_seqlens, T, num_segments)
+        seq_idx = meta["seq_idx"].to(device)
+        pre = meta["preceding_start"].to(device)
+        fol = meta["following_stop"].to(device)
+    spec = C.ProblemSpec(B, T, H, Dk, Dv, num_segments, chunk, scale, dtype, seq_idx, pre, fol)
+    C.rm_cp_validate(spec)
+    f32 = dict(dtype=torch.float32, device=device)
+    ssz = (num_segments, B, H, Dk, Dv)
+    M = torch.empty((num_segments, B, H), **f32)
+    dS = torch.empty(ssz, **f32)
+    S_in = torch.empty(ssz, **f32)
+    gamma = torch.empty(ssz if backward else (0,), **f32)
+    dS_out = torch.empty(ssz if backward else (0,), **f32)
+    ws = torch.empty(max(C.rm_cp_workspace_size(spec), 16), dtype=torch.uint8, device=device)
+    return Plan(spec, M, dS, S_in, gamma, dS_out, ws, meta)
+
+
+def plan_like(q: torch.Tensor, v: torch.Tensor, num_segments: int, chunk: int = 64,
+              scale=None, cu_seqlens=None, backward=True) -> Plan:
+    B, T, H, Dk = q.shape
+    return make_plan(B, T, H, Dk, v.shape[-1], num_segments, chunk, scale, q.dtype, cu_seqlens,
+                     q.device, backward)
+
+
+def forward(plan: Plan, q, k, v, g, o=None, stream=None) -> torch.Tensor:
+    """o = chunkwise gated linear attention; fills plan.M, plan.dS, plan.S_in."""
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    C.rm_cp_forward_prepare(plan.spec, k, v, g, plan.M, plan.dS, plan.ws, stream)
+    C.rm_cp_compose_prefix(plan.spec, plan.M, plan.dS, plan.S_in, stream)
+    C.rm_cp_forward_apply(plan.spec, q, k, v, g, plan.S_in, o, plan.ws, stream)
+    return o
+
+
+def backward(plan: Plan, q, k, v, g, dO, grads=None, stream=None):
+    """(dq, dk, dv, dg) of sum(dO * o); needs plan.M and plan.S_in from forward."""
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                 torch.empty(g.shape, dtype=torch.float32, device=g.device))
+    dq, dk, dv, dg = grads
+    C.rm_cp_backward_prepare(plan.spec, q, k, v, g, plan.S_in, dO, plan.gamma, dq, plan.ws, stream)
+    C.rm_cp_compose_suffix(plan.spec, plan.M, plan.gamma, plan.dS_out, stream)
+    C.rm_cp_backward_apply(plan.spec, q, k, v, g, dO, plan.S_in, plan.dS_out, dk, dv, dg, plan.ws,
+                           stream)
+    return dq, dk, dv, dg
+
+
+class ChunkwiseGatedLinearAttention(torch.autograd.Function):
+    """Autograd adapter; the saved context is (q, k, v, g) plus the plan, whose
+    S_in and M carry the forward's composed summaries into backward."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, num_segments, chunk, scale, cu_seqlens):
+        q, k, v, g = (t.contiguous() for t in (q, k, v, g))
+        plan = plan_like(q, v, num_segments, chunk, scale, cu_seqlens)
+        o = forward(plan, q, k, v, g)
+        ctx.plan = plan
+        ctx.save_for_backward(q, k, v, g)
+        return o
+
+    @staticmethod
+    def backward(ctx, dO):
+        q, k, v, g = ctx.saved_tensors
+        dq, dk, dv, dg = backward(ctx.plan, q, k, v, g, dO.contiguous())
+        return dq, dk, dv, dg, None, None, None, None
+
+
+def chunkwise_gla(q, k, v, g, num_segments: int, chunk: int = 64, scale=None, cu_seqlens=None):
+    """Differentiable chunkwise gated linear attention.
+
+    q, k [B,T,H,Dk], v [B,T,H,Dv] (fp32 or bf16, CUDA), g [B,T,H] fp32 log-gates.
+    cu_seqlens (host int32 [N+1]) packs several sequences along T."""
+    return ChunkwiseGatedLinearAttention.apply(q, k, v, g, num_segments, chunk, scale, cu_seqlens)

@@ -1,0 +1,46 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace rmcp {
+
+enum class Op { kForwardPrepare, kForwardApply, kBackwardPrepare, kBackwardApply };
+
+// Device pointers of one call; unused ones are null.
+struct Ptrs {
+    const void* q = nullptr;
+    const void* k = nullptr;
+    const void* v = nullptr;
+    const float* g = nullptr;
+    const void* dO = nullptr;
+    const float* S_in = nullptr;
+    const float* dS_out = nullptr;
+    float* M = nullptr;
+    float* sum_out = nullptr;  // dS (forward prepare) or gamma (backward prepare)
+    void* out0 = nullptr;      // o / dq / dk
+    void* out1 = nullptr;      // dv
+    float* dg = nullptr;
+    float* ws_f32 = nullptr;   // per-token q.dq [B,T,H]
+};
+
+// adds n to the process-wide launch counter (rm_cp_launch_count)
+void note_launch(int n);
+
+// generic fp32 SIMT path (simt_kernels.cu)
+bool generic_supports(const Dims& d);
+rm_status launch_generic(Op op, const Dims& d, rm_dtype dt, const Ptrs& p, cudaStream_t s);
+
+// summary scans (compose_kernels.cu)
+rm_status launch_compose_prefix(const Dims& d, const float* M, const float* dS, float* S_in,
+                                cudaStream_t s);
+rm_status launch_compose_suffix(const Dims& d, const float* M, const float* gamma,
+                                float* dS_out, cudaStream_t s);
+
+// tensor-core path (tc_kernels.cu)
+bool tc_supports(const Dims& d, rm_dtype dt);
+rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s);
+
+}  // namespace rmcp

@@ -1,0 +1,159 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/rm_cp.h declares, validates problems before any
+launch, and builds packed-sequence metadata bit-exactly like the oracle's
+brute-force definition."""
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_summary_scan_gb300 import _capi as C
+from state_summary_scan_gb300.workloads import WORKLOADS, make_inputs, random_cu_seqlens
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def declared_entry_points():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(rm_cp_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = C.load()
+    declared = declared_entry_points()
+    assert len(declared) >= 12
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(C.EXPORTS) <= set(declared)
+
+
+def test_status_strings():
+    lib = C.load()
+    for code, name in C.STATUS_NAMES.items():
+        assert lib.rm_cp_status_string(code).decode() == name
+
+
+def spec(**kw):
+    base = dict(B=1, T=256, H=2, Dk=32, Dv=32, num_segments=4, chunk=64, scale=0.17, dtype=0)
+    base.update(kw)
+    return C.ProblemSpec(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=250), 2),                   # T % num_segments
+    (dict(chunk=48), 2),                # segment length % chunk
+    (dict(B=0), 1), (dict(T=0), 1), (dict(H=-1), 1), (dict(num_segments=0), 1),
+    (dict(dtype=7), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(Dk=48), 4), (dict(Dk=256), 4), (dict(Dv=12), 4), (dict(Dv=264), 4),
+])
+def test_validation_rejects_bad_problems(kw, status):
+    with pytest.raises(C.RmCpError) as e:
+        C.rm_cp_validate(spec(**kw))
+    assert e.value.status == status
+    assert C.rm_cp_workspace_size(spec(**kw)) == 0
+    assert C.rm_cp_path(spec(**kw)) == -1
+
+
+def test_validation_accepts_every_workload():
+    for w in WORKLOADS.values():
+        s = spec(B=w.B, T=w.T, H=w.H, Dk=w.Dk, Dv=w.Dv, num_segments=w.num_segments,
+                 chunk=w.chunk, scale=w.scale, dtype=0 if w.dtype == "f32" else 1)
+        C.rm_cp_validate(s)
+        assert C.rm_cp_workspace_size(s) >= w.B * w.T * w.H * 4
+
+
+def test_compute_calls_reject_null_and_misaligned_pointers_before_launch():
+    """These return from host validation; no CUDA call is reached."""
+    lib = C.load()
+    s = spec()
+    rc = lib.rm_cp_forward_prepare(s.ref, None, None, None, None, None, None, None)
+    assert rc == 1 and b"k is NULL" in lib.rm_cp_last_error()
+    odd = ctypes.c_void_p(0x1008)
+    ok = ctypes.c_void_p(0x1000)
+    rc = lib.rm_cp_forward_apply(s.ref, ok, ok, ok, ok, ok, odd, None, None)
+    assert rc == 3 and b"o is not 16-byte aligned" in lib.rm_cp_last_error()
+    rc = lib.rm_cp_backward_prepare(s.ref, ok, ok, ok, ok, ok, ok, ok, ok, None, None)
+    assert rc == 1 and b"ws is NULL" in lib.rm_cp_last_error()
+    bad = spec(T=100)
+    rc = lib.rm_cp_compose_prefix(bad.ref, ok, ok, ok, None)
+    assert rc == 2
+
+
+def test_metadata_builder_matches_golden():
+    for case in json.load(open(os.path.join(GOLDEN, "packed_metadata.json"))):
+        md = C.rm_cp_build_packed_metadata(case["cu_seqlens"], case["T"], case["num_segments"])
+        assert md["seq_idx"].tolist() == case["seq_idx"]
+        off = md["local_cu_offsets"].tolist()
+        loc = md["local_cu_seqlens"].tolist()
+        assert [loc[off[j]:off[j + 1]] for j in range(case["num_segments"])] == case["local_cu_seqlens"]
+        assert md["preceding_start"].tolist() == case["preceding_start"]
+        assert md["following_stop"].tolist() == case["following_stop"]
+
+
+def check_builder_against_oracle(cu, T, nseg):
+    md = C.rm_cp_build_packed_metadata(cu, T, nseg)
+    ref = oracle.packed_metadata(cu, T, oracle.equal_segments(T, nseg))
+    assert np.array_equal(md["seq_idx"].numpy(), ref["seq_idx"])
+    off = md["local_cu_offsets"].numpy()
+    loc = md["local_cu_seqlens"].numpy()
+    for j in range(nseg):
+        assert np.array_equal(loc[off[j]:off[j + 1]], ref["local_cu_seqlens"][j])
+    assert np.array_equal(md["preceding_start"].numpy(), ref["preceding_start"])
+    assert np.array_equal(md["following_stop"].numpy(), ref["following_stop"])
+
+
+def test_metadata_builder_bit_exact_random():
+    gen = torch.Generator().manual_seed(123)
+    for trial in range(300):
+        nseg = int(torch.randint(1, 9, (1,), generator=gen))
+        L = int(torch.randint(1, 12, (1,), generator=gen))
+        T = nseg * L
+        cu = random_cu_seqlens(gen, T, max_len=int(torch.randint(1, 2 * T + 1, (1,), generator=gen)))
+        check_builder_against_oracle(cu.tolist(), T, nseg)
+
+
+def test_metadata_builder_packed_workload():
+    w = WORKLOADS["packed64k"]
+    gen = torch.Generator("cpu").manual_seed(w.seed)
+    from state_summary_scan_gb300.workloads import draw_lengths, cu_seqlens_from_lengths
+    cu = cu_seqlens_from_lengths(draw_lengths(gen, w.T))
+    check_builder_against_oracle(cu.tolist(), w.T, w.num_segments)
+    # the workload's segments are not aligned to sequences: some boundary falls
+    # inside a sequence and some sequence spans at least three segments
+    md = oracle.packed_metadata(cu, w.T, oracle.equal_segments(w.T, w.num_segments))
+    pre, fol = md["preceding_start"], md["following_stop"]
+    assert any(pre[j] < j for j in range(w.num_segments))
+    assert any(fol[j] - pre[j] >= 3 for j in range(w.num_segments))
+
+
+def test_metadata_builder_rejects_bad_cu_seqlens():
+    for cu in ([1, 8], [0, 7], [0, 3, 3, 8], [0, 5, 4, 8]):
+        with pytest.raises(C.RmCpError) as e:
+            C.rm_cp_build_packed_metadata(cu, 8, 2)
+        assert e.value.status == 5
+    with pytest.raises(C.RmCpError) as e:
+        C.rm_cp_build_packed_metadata([0, 9], 9, 2)
+    assert e.value.status == 2
+
+
+def test_workload_recipe_is_deterministic_and_shaped():
+    w = WORKLOADS["tiny"]
+    a = make_inputs(w)
+    b = make_inputs(w)
+    for x, y in zip((a.q, a.k, a.v, a.g, a.dO), (b.q, b.k, b.v, b.g, b.dO)):
+        assert torch.equal(x, y)
+    assert a.q.shape == (1, 256, 2, 32) and a.q.dtype == torch.float32
+    assert torch.allclose(a.k.norm(dim=-1), torch.ones(1, 256, 2), atol=1e-5)
+    assert (a.g < 0).all()
