@@ -229,8 +229,12 @@ const char* rm_cp_last_error(void);
  * devices, all threads).  A diagnostic for counting launches per step. */
 uint64_t rm_cp_launch_count(void);
 
-/* Which kernel family a problem runs on: 0 = generic SIMT fp32 path,
- * 1 = tensor-core (tcgen05) path.  -1 for an invalid problem. */
+/* Which kernel family a problem runs on: 0 = generic SIMT fp32 path for
+ * every call, 1 = tensor-core (tcgen05) path for every call, 2 = tensor-core
+ * path for some calls and the generic path for the others.  -1 for an
+ * invalid problem.  The tensor-core path serves bf16 storage with Dk = 128,
+ * Dv in {128, 256} and segment lengths that are multiples of 64 (its
+ * backward calls need Dv = 128). */
 int32_t rm_cp_path(const rm_cp_problem* p);
 
 #ifdef __cplusplus

@@ -41,6 +41,7 @@ rm_status launch_compose_suffix(const Dims& d, const float* M, const float* gamm
 
 // tensor-core path (tc_kernels.cu)
 bool tc_supports(const Dims& d, rm_dtype dt);
+bool tc_supports_op(Op op, const Dims& d, rm_dtype dt);
 rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s);
 
 }  // namespace rmcp

@@ -95,8 +95,9 @@ size_t workspace_bytes(const rmcp::Dims& d) {
 rm_status launch(rmcp::Op op, const rm_cp_problem* p, const rmcp::Dims& d, const rmcp::Ptrs& ptrs,
                  rm_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    rm_status st = rmcp::tc_supports(d, p->dtype) ? rmcp::launch_tc(op, d, ptrs, s)
-                                                  : rmcp::launch_generic(op, d, p->dtype, ptrs, s);
+    rm_status st = rmcp::tc_supports_op(op, d, p->dtype)
+                       ? rmcp::launch_tc(op, d, ptrs, s)
+                       : rmcp::launch_generic(op, d, p->dtype, ptrs, s);
     if (st == RM_ERR_CUDA) {
         cudaError_t e = cudaGetLastError();
         return fail(RM_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
@@ -135,7 +136,11 @@ rm_status rm_cp_validate(const rm_cp_problem* p) {
 int32_t rm_cp_path(const rm_cp_problem* p) {
     rmcp::Dims d;
     if (check_problem(p, &d) != RM_OK) return -1;
-    return rmcp::tc_supports(d, p->dtype) ? 1 : 0;
+    int n = 0;
+    for (rmcp::Op op : {rmcp::Op::kForwardPrepare, rmcp::Op::kForwardApply,
+                        rmcp::Op::kBackwardPrepare, rmcp::Op::kBackwardApply})
+        n += rmcp::tc_supports_op(op, d, p->dtype) ? 1 : 0;
+    return n == 4 ? 1 : (n == 0 ? 0 : 2);
 }
 
 size_t rm_cp_workspace_size(const rm_cp_problem* p) {

@@ -162,3 +162,48 @@ def test_deterministic():
     b = run_gpu(q, k, v, g, dO, 4, 64, 0.1)
     for key in a:
         assert torch.equal(a[key], b[key]), key
+
+
+# ------------------------------------------------------------------ tensor-core path
+
+def test_workloads_take_the_tensor_core_path():
+    from state_summary_scan_gb300 import _capi as C
+    for name, expect in (("fwd4k", 1), ("32k", 1), ("packed64k", 1), ("256k", 2), ("tiny", 0)):
+        w = WORKLOADS[name]
+        s = C.ProblemSpec(w.B, w.T, w.H, w.Dk, w.Dv, w.num_segments, w.chunk, w.scale,
+                          w.torch_dtype)
+        assert C.rm_cp_path(s) == expect, name
+
+
+@pytest.mark.parametrize("Dv", [128, 256])
+def test_tc_single_and_many_segments(Dv):
+    check_case(1, 512, 2, 128, Dv, torch.bfloat16, nseg=1, chunk=64)
+    check_case(2, 512, 2, 128, Dv, torch.bfloat16, nseg=8, chunk=64)
+
+
+@pytest.mark.parametrize("Dv", [128, 256])
+def test_tc_packed_ragged_resets(Dv):
+    # starts at chunk positions 0, 1, 63, a segment start (256), length-1
+    # sequences, and a sequence across three segments
+    cu = [0, 1, 2, 63, 64, 65, 129, 256, 257, 300, 511, 512, 700, 1024]
+    check_case(1, 1024, 2, 128, Dv, torch.bfloat16, nseg=4, chunk=64, cu=cu)
+
+
+def test_tc_every_token_starts_a_sequence():
+    cu = list(range(0, 257))
+    check_case(1, 256, 2, 128, 128, torch.bfloat16, nseg=2, chunk=64, cu=cu)
+
+
+def test_tc_zero_gate():
+    check_case(1, 512, 2, 128, 128, torch.bfloat16, nseg=4, chunk=64, gate=0.0)
+
+
+def test_tc_strong_decay():
+    import oracle
+    q, k, v, g, dO = synth(1, 256, 2, 128, 128, torch.bfloat16, gate=-30.0)
+    scale = 1.0 / math.sqrt(128)
+    gpu = run_gpu(q, k, v, g, dO, 2, 64, scale)
+    ref = run_oracle(q, k, v, g, dO, 2, scale)
+    compare(select_heads(gpu, None), ref, 2e-2, ("o", "M", "dS", "S_in", "dq", "dk", "dv"))
+    ref["dg"] = oracle.backward(q, k, v, g, dO, scale, direct=True)[3]
+    compare(select_heads(gpu, None), ref, 2e-2, ("dg",))
