@@ -219,6 +219,27 @@ rm_status rm_cp_backward_apply(const rm_cp_problem* p, const void* q, const void
                                const float* S_in, const float* dS_out, void* dk, void* dv,
                                float* dg, void* ws, rm_stream_t stream);
 
+/*
+ * Failure detection.  Every wait inside the tensor-core kernels (on a TMA
+ * copy or on tensor-core completion) is bounded (200 ms); a wait that runs
+ * out sets a device-side flag, and the kernel finishes its remaining work
+ * with bounded waits and frees its tensor memory instead of hanging.
+ *
+ * rm_cp_device_status reads (and, if clear != 0, resets) that flag.  It
+ * enqueues one tiny kernel and a copy on `stream`, then SYNCHRONISES the
+ * stream (the only call of this library that does).  dev_scratch is a device
+ * int32 the call may overwrite.  Returns RM_ERR_TIMEOUT if a wait ran out
+ * since the flag was last cleared, RM_OK otherwise, RM_ERR_CUDA on a CUDA error.
+ *
+ * rm_cp_selftest_wait_timeout enqueues a one-thread kernel that waits on a
+ * barrier nothing ever completes, with a bound of limit_us microseconds
+ * (1 <= limit_us <= 1000000): it exercises the timeout path above without
+ * faulting or hanging the device.  Returns RM_ERR_INVALID_ARG for an
+ * out-of-range limit.
+ */
+rm_status rm_cp_device_status(int32_t* dev_scratch, int32_t clear, rm_stream_t stream);
+rm_status rm_cp_selftest_wait_timeout(uint32_t limit_us, rm_stream_t stream);
+
 /* Name of a status code (static string). */
 const char* rm_cp_status_string(rm_status s);
 

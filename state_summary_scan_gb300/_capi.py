@@ -27,6 +27,7 @@ EXPORTS = (
     "rm_cp_forward_prepare", "rm_cp_compose_prefix", "rm_cp_forward_apply",
     "rm_cp_backward_prepare", "rm_cp_compose_suffix", "rm_cp_backward_apply",
     "rm_cp_status_string", "rm_cp_last_error", "rm_cp_path", "rm_cp_launch_count",
+    "rm_cp_device_status", "rm_cp_selftest_wait_timeout",
 )
 
 
@@ -66,6 +67,8 @@ _SIGS = {
     "rm_cp_last_error": (ctypes.c_char_p, []),
     "rm_cp_path": (ctypes.c_int32, [_PP]),
     "rm_cp_launch_count": (ctypes.c_uint64, []),
+    "rm_cp_device_status": (_S, [_P, ctypes.c_int32, _P]),
+    "rm_cp_selftest_wait_timeout": (_S, [ctypes.c_uint32, _P]),
 }
 
 _lock = threading.Lock()
@@ -152,6 +155,15 @@ def rm_cp_path(p: ProblemSpec) -> int:
 
 def rm_cp_launch_count() -> int:
     return int(load().rm_cp_launch_count())
+
+
+def rm_cp_device_status(dev_scratch: torch.Tensor, clear: bool = True, stream=None) -> int:
+    """Returns the status code (0 = RM_OK, 7 = RM_ERR_TIMEOUT); synchronises the stream."""
+    return int(load().rm_cp_device_status(_ptr(dev_scratch), int(clear), _stream(stream)))
+
+
+def rm_cp_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    _check(load().rm_cp_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def rm_cp_workspace_size(p: ProblemSpec) -> int:

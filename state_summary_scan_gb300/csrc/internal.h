@@ -43,5 +43,7 @@ rm_status launch_compose_suffix(const Dims& d, const float* M, const float* gamm
 bool tc_supports(const Dims& d, rm_dtype dt);
 bool tc_supports_op(Op op, const Dims& d, rm_dtype dt);
 rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s);
+rm_status tc_selftest_wait(uint32_t limit_us, cudaStream_t s);
+rm_status tc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cudaStream_t s);
 
 }  // namespace rmcp

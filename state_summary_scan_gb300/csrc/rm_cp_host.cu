@@ -128,6 +128,25 @@ const char* rm_cp_last_error(void) { return g_last_error; }
 
 uint64_t rm_cp_launch_count(void) { return rmcp::g_launches.load(std::memory_order_relaxed); }
 
+rm_status rm_cp_device_status(int32_t* dev_scratch, int32_t clear, rm_stream_t stream) {
+    RM_NEED(dev_scratch);
+    int flag = 0;
+    rm_status st = rmcp::tc_read_timeout_flag(&flag, clear, dev_scratch,
+                                              reinterpret_cast<cudaStream_t>(stream));
+    if (st != RM_OK)
+        return fail(st, "device status read failed: %s", cudaGetErrorString(cudaGetLastError()));
+    if (flag) return fail(RM_ERR_TIMEOUT, "a bounded device-side wait ran out");
+    return RM_OK;
+}
+
+rm_status rm_cp_selftest_wait_timeout(uint32_t limit_us, rm_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(RM_ERR_INVALID_ARG, "limit_us must be in [1, 1000000]");
+    rm_status st = rmcp::tc_selftest_wait(limit_us, reinterpret_cast<cudaStream_t>(stream));
+    if (st != RM_OK) return fail(st, "self-test launch failed");
+    return RM_OK;
+}
+
 rm_status rm_cp_validate(const rm_cp_problem* p) {
     rmcp::Dims d;
     return check_problem(p, &d);

@@ -20,8 +20,8 @@
 namespace rmcp {
 namespace tc {
 
-constexpr int kChunk = 64;                 // tokens per chunk
-constexpr uint32_t kSpinLimit = 1u << 22;  // bounded mbarrier waits (each try can suspend)
+constexpr int kChunk = 64;                       // tokens per chunk
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // bound of every mbarrier wait
 
 // set by a kernel whose bounded wait ran out (the kernel then finishes
 // without waiting further; its outputs are not valid)
@@ -52,12 +52,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Waits for the phase with the given parity; false (and the flag set) on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    atomicExch(&g_timeout_flag, 1);
-    return false;
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Waits for the phase with the given parity for at most limit_ns; on
+// timeout sets g_timeout_flag and returns false.  Kernels keep walking their
+// loop after a timeout (every later wait is bounded too), so that every copy
+// they issued has been waited for before they free tensor memory and exit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > limit_ns) {
+            atomicExch(&g_timeout_flag, 1);
+            return false;
+        }
+    }
+    return true;
 }
 
 // ------------------------------------------------------------------ TMA

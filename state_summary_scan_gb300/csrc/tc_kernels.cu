@@ -762,6 +762,22 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// Failure-detection self test: waits on an mbarrier that nothing arrives on,
+// with the given bound, so that the timeout path and its host-side status can
+// be exercised without faulting or hanging the device.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    mbar_fence_init();
+    mbar_wait(b, 0, limit_ns);
+}
+
+__global__ void read_flag_kernel(int* out, int clear) {
+    *out = g_timeout_flag;
+    if (clear) g_timeout_flag = 0;
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -806,6 +822,23 @@ constexpr size_t kRevSmem = 26 * kTileBytes + 1024;   // 2 stages x 8 + Q~ K~ (4
 }  // namespace
 
 }  // namespace tc
+
+rm_status tc_selftest_wait(uint32_t limit_us, cudaStream_t s) {
+    tc::selftest_wait_kernel<<<1, 1, 0, s>>>(uint64_t(limit_us) * 1000ull);
+    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    note_launch(1);
+    return RM_OK;
+}
+
+rm_status tc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cudaStream_t s) {
+    tc::read_flag_kernel<<<1, 1, 0, s>>>(dev_scratch, clear);
+    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    note_launch(1);
+    if (cudaMemcpyAsync(host_flag, dev_scratch, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return RM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RM_ERR_CUDA;
+    return RM_OK;
+}
 
 bool tc_supports(const Dims& d, rm_dtype dt) {
     return dt == RM_BF16 && d.Dk == 128 && (d.Dv == 128 || d.Dv == 256) && d.L % tc::kChunk == 0 &&

@@ -89,6 +89,9 @@ def test_compute_calls_reject_null_and_misaligned_pointers_before_launch():
     bad = spec(T=100)
     rc = lib.rm_cp_compose_prefix(bad.ref, ok, ok, ok, None)
     assert rc == 2
+    assert lib.rm_cp_selftest_wait_timeout(0, None) == 1
+    assert lib.rm_cp_selftest_wait_timeout(2000000, None) == 1
+    assert lib.rm_cp_device_status(None, 1, None) == 1
 
 
 def test_metadata_builder_matches_golden():
