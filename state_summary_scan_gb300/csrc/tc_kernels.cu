@@ -35,6 +35,8 @@ namespace tc {
 namespace {
 
 constexpr uint32_t kTileBytes = kChunk * 64 * 2;  // one [64 rows][64 cols] bf16 block: 8 KB
+constexpr int kThreads = 256;                     // 8 warps: two per tensor-memory lane quadrant
+constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     const uint32_t a = smem_u32(p);
@@ -48,11 +50,142 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
         tma_load_3d(smem_u32(dst + (c / 64) * kTileBytes), map, col0 + c, h, row, bar);
 }
 
+// Thread geometry.  Warp w reads tensor-memory lanes [32 (w % 4), +32); the
+// two warps of a quadrant split the columns (grp = w / 4).  In the M = 64
+// accumulators a chunk row tau lives in lane 32 (tau / 16) + tau % 16, i.e.
+// lanes 0-15 of its quadrant; lanes 16-31 take over half of those rows'
+// columns through a shuffle, so every thread works on 1/4 of a token row.
+struct Geo {
+    int tid, warp, lane, qd, grp;
+    bool hi;       // lane >= 16
+    int tau;       // token row of the M = 64 tiles handled by this thread
+    int srow;      // state row of the M = 128 tiles (= 32 qd + lane)
+    uint32_t tl;   // tensor-memory lane offset of the warp
+};
+__device__ __forceinline__ Geo geo() {
+    Geo g;
+    g.tid = threadIdx.x;
+    g.warp = g.tid >> 5;
+    g.lane = g.tid & 31;
+    g.qd = g.warp & 3;
+    g.grp = g.warp >> 2;
+    g.hi = g.lane >= 16;
+    g.tau = 16 * g.qd + (g.lane & 15);
+    g.srow = 32 * g.qd + g.lane;
+    g.tl = uint32_t(32 * g.qd) << 16;
+    return g;
+}
+
+// Columns [col + 16 hi, +16) of row tau of an M = 64 accumulator (col absolute).
+__device__ __forceinline__ void tok16(uint32_t tmem, const Geo& g, int col, float* x) {
+    float v[32];
+    tmem_ld32(tmem + g.tl + col, v);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const float up = __shfl_sync(kFull, v[16 + e], (g.lane + 16) & 31);
+        x[e] = g.hi ? up : v[e];
+    }
+}
+
+// Columns [64 grp, +64) of state row srow of an M = 128 accumulator at column col.
+__device__ __forceinline__ void state_cols64(uint32_t tmem, const Geo& g, int col, float* x) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32_nowait(tmem + g.tl + col + 64 * g.grp, r0);
+    tmem_ld32_nowait(tmem + g.tl + col + 64 * g.grp + 32, r1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        x[e] = __uint_as_float(r0[e]);
+        x[32 + e] = __uint_as_float(r1[e]);
+    }
+}
+
+// S[e] = W S[e] + acc[srow][64 grp + e] for e < 64, accumulator at column col;
+// then row srow's columns [64 grp, +64) are written as bf16 into a [128][128] tile.
+__device__ __forceinline__ void state_update(uint32_t tmem, const Geo& g, int col, float W, float* S,
+                                             uint8_t* tile);
+
+// Writes columns [64 grp, +64) of state row i as bf16 into a [128][128] tile.
+__device__ __forceinline__ void store_state_half(uint8_t* tile, int i, int grp, const float* s) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(tile + sw_chunk(128, i, 8 * grp + c)) = pack8(s + c * 8);
+}
+
+__device__ __forceinline__ void state_update(uint32_t tmem, const Geo& g, int col, float W, float* S,
+                                             uint8_t* tile) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        float y[32];
+        tmem_ld32(tmem + g.tl + col + 64 * g.grp + 32 * hf, y);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) S[32 * hf + e] = fmaf(W, S[32 * hf + e], y[e]);
+    }
+    store_state_half(tile, g.srow, g.grp, S);
+}
+
+// Physical 16-byte chunks [4 h4, 4 h4 + 4) of row r of block blk of a [64][128]
+// tile, each thread of the CTA taking one such quarter row.
+__device__ __forceinline__ uint8_t* quarter_row(uint8_t* tile, int tid, int* r) {
+    *r = tid >> 2;
+    return tile + ((tid >> 1) & 1) * kTileBytes + (tid >> 2) * 128 + (tid & 1) * 64;
+}
+__device__ __forceinline__ void scale_quarter(uint8_t* p, float w) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint4* q = reinterpret_cast<uint4*>(p + c * 16);
+        float x[8];
+        unpack8(*q, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] *= w;
+        *q = pack8(x);
+    }
+}
+__device__ __forceinline__ void scale_quarter_to(const uint8_t* src, uint8_t* dst, float w) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float x[8];
+        unpack8(*reinterpret_cast<const uint4*>(src + c * 16), x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] *= w;
+        *reinterpret_cast<uint4*>(dst + c * 16) = pack8(x);
+    }
+}
+
+// Decay mask for this thread's 16 columns c0..c0+15 of row tau:
+// gam[e] = exp(b_tau - b_s) if s <= tau (s < tau when strict) in tau's sequence.
+__device__ __forceinline__ void decay_row16(const GateSmem& gs, int tau, int c0, bool strict, float* gam) {
+    const float bt = gs.b[tau];
+    const int lt = gs.lid[tau];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const int s = c0 + e;
+        const bool keep = (strict ? s < tau : s <= tau) && gs.lid[s] == lt;
+        gam[e] = keep ? __expf(bt - gs.b[s]) : 0.f;
+    }
+}
+// Writes 16 bf16 values (columns c0..c0+15, c0 % 16 == 0) of row tau of a [64][64] tile.
+__device__ __forceinline__ void store_row16(uint8_t* tile, int tau, int c0, const float* y) {
+    *reinterpret_cast<uint4*>(tile + sw_chunk(64, tau, c0 >> 3)) = pack8(y);
+    *reinterpret_cast<uint4*>(tile + sw_chunk(64, tau, (c0 >> 3) + 1)) = pack8(y + 8);
+}
+
+// 16 values (columns c0..c0+15, c0 % 8 == 0) of row t of a [64][128] bf16 tile.
+__device__ __forceinline__ void tile_row_get16(const uint8_t* tile, int t, int c0, float* x) {
+    unpack8(*reinterpret_cast<const uint4*>(tile + sw_chunk(64, t, c0 >> 3)), x);
+    unpack8(*reinterpret_cast<const uint4*>(tile + sw_chunk(64, t, (c0 >> 3) + 1)), x + 8);
+}
+
+__device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v) {
+    *reinterpret_cast<uint4*>(dst) = pack8(v);
+    *reinterpret_cast<uint4*>(dst + 8) = pack8(v + 8);
+}
+
 // ===========================================================================
 // sum_t w_t x_t y_t^T over one segment (x: Dk = 128 columns, y: DV columns)
 // ===========================================================================
 template <int DV, bool GAMMA>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     tc_outer_kernel(const Dims d, const __grid_constant__ CUtensorMap mx,
                     const __grid_constant__ CUtensorMap my, const float* __restrict__ g,
                     float* __restrict__ M, float* __restrict__ out) {
@@ -68,12 +201,12 @@ __global__ void __launch_bounds__(128, 1)
     __shared__ __align__(8) uint64_t done_bar;
     __shared__ uint32_t tmem_slot;
 
+    const Geo G = geo();
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
 
-    if (tid == 0) {
+    if (G.tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
@@ -81,7 +214,7 @@ __global__ void __launch_bounds__(128, 1)
         mbar_init(smem_u32(&done_bar), 1);
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), DV);
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), DV);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -97,36 +230,35 @@ __global__ void __launch_bounds__(128, 1)
         load_tile(st, &mx, 0, 128, h, row, bar);
         load_tile(st + XBYTES, &my, 0, DV, h, row, bar);
     };
-    if (tid == 0)
+    if (G.tid == 0)
         for (int it = 0; it < STAGES && it < nch; ++it) issue(it, it);
 
     float run = 0.f;  // sum of the gates of the chunks already walked
     int seen = 0;     // a sequence starts in the chunks already walked
     GateRegs gr;
-    if (warp == 0) gr = gate_load(d, g, b, h, a0 + chunk_of(0) * kChunk, lane);
+    if (G.warp == 0) gr = gate_load(d, g, b, h, a0 + chunk_of(0) * kChunk, G.lane);
     for (int it = 0; it < nch; ++it) {
         const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (warp == 0) {
-            gate_prep(gr, &gs, lane);
-            if (it + 1 < nch) gr = gate_load(d, g, b, h, a0 + chunk_of(it + 1) * kChunk, lane);
+        if (G.warp == 0) {
+            gate_prep(gr, &gs, G.lane);
+            if (it + 1 < nch) gr = gate_load(d, g, b, h, a0 + chunk_of(it + 1) * kChunk, G.lane);
         }
-        mbar_wait(smem_u32(&full_bar[s]), ph);
+        mbar_wait(smem_u32(&full_bar[s]), (it / STAGES) & 1);
         __syncthreads();
         {
-            // row weight w_t, applied to x_t in place
-            const int r = tid >> 1, blk = tid & 1;
+            int r;
+            uint8_t* p = quarter_row(smem + s * SBYTES, G.tid, &r);
             float w;
             if (GAMMA)  // scale * alpha_a ... alpha_t: no start in [a, t]
                 w = (!seen && !gs.first && gs.lid[r] == 0) ? d.scale * expf(run + gs.b[r]) : 0.f;
             else        // alpha_{t+1} ... alpha_end: no start in (t, end]
                 w = (!seen && gs.lid[r] == gs.lid[kChunk - 1]) ? expf(run + gs.btot - gs.b[r]) : 0.f;
-            scale_row128(smem + s * SBYTES + blk * kTileBytes + r * 128, w);
+            scale_quarter(p, w);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (G.tid == 0) {
             tc_fence_after();
             const uint32_t xa = smem_u32(smem + s * SBYTES), ya = xa + XBYTES;
             constexpr uint32_t idesc = idesc_bf16(128, DV, 1, 1);
@@ -135,81 +267,42 @@ __global__ void __launch_bounds__(128, 1)
                 mma_bf16(tmem, sdesc(xa + k * 2048, kTileBytes, 1024),
                          sdesc(ya + k * 2048, kTileBytes, 1024), idesc, (it > 0 || k > 0) ? 1u : 0u);
             mma_commit(smem_u32(&empty_bar[s]));
-            if (it + STAGES < nch) {
-                mbar_wait(smem_u32(&empty_bar[s]), ph);
-                issue(it + STAGES, s);
+            // refill the stage the previous chunk's products have finished with
+            const int prev = it - 1;
+            if (prev >= 0 && prev + STAGES < nch) {
+                const int ps = prev % STAGES;
+                mbar_wait(smem_u32(&empty_bar[ps]), (prev / STAGES) & 1);
+                issue(prev + STAGES, ps);
             }
         }
         run += gs.btot;
         seen |= gs.any;
         __syncthreads();
     }
-    if (tid == 0) mma_commit(smem_u32(&done_bar));
+    if (G.tid == 0) mma_commit(smem_u32(&done_bar));
     mbar_wait(smem_u32(&done_bar), 0);
     tc_fence_after();
-    float* dst = out + sum_off(d, seg, b, h) + int64_t(warp * 32 + lane) * DV;
+    {
+        float* dst = out + sum_off(d, seg, b, h) + int64_t(G.srow) * DV;
 #pragma unroll 1
-    for (int c = 0; c < DV; c += 32) {
-        float v[32];
-        tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + c, v);
+        for (int c = G.grp * (DV / 2); c < (G.grp + 1) * (DV / 2); c += 64) {
+            float v[64];
+            state_cols64(tmem, G, c - 64 * G.grp, v);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            for (int i = 0; i < 64; i += 4)
+                *reinterpret_cast<float4*>(dst + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
     }
-    if (!GAMMA && tid == 0) M[(int64_t(seg) * d.B + b) * d.H + h] = seen ? 0.f : expf(run);
+    if (!GAMMA && G.tid == 0) M[(int64_t(seg) * d.B + b) * d.H + h] = seen ? 0.f : expf(run);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, DV);
-}
-
-// ---------------------------------------------------------------------------
-// helpers shared by the sweeps
-// ---------------------------------------------------------------------------
-
-// Writes row i (128 fp32 values) of a state as bf16 into a [128][128] tile.
-__device__ __forceinline__ void store_state_row(uint8_t* tile, int i, const float* s) {
-#pragma unroll
-    for (int ch = 0; ch < 16; ++ch)
-        *reinterpret_cast<uint4*>(tile + sw_chunk(128, i, ch)) = pack8(s + ch * 8);
-}
-
-// Masked score row: out[s] = scale * x[s] * exp(b_t - b_s) for s <= t (s < t if
-// strict) in t's sequence, else 0; written as bf16 row t of a [64][64] tile.
-// diag receives x[t].
-__device__ __forceinline__ void masked_row(uint8_t* tile, const GateSmem& gs, int t, const float* x,
-                                           float scale, bool strict, float* diag) {
-    const float bt = gs.b[t];
-    const int lt = gs.lid[t];
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        float y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int s = ch * 8 + e;
-            const bool keep = (strict ? s < t : s <= t) && gs.lid[s] == lt;
-            y[e] = keep ? scale * x[s] * expf(bt - gs.b[s]) : 0.f;
-            if (s == t) *diag = x[s];
-        }
-        *reinterpret_cast<uint4*>(tile + sw_chunk(64, t, ch)) = pack8(y);
-    }
-}
-
-// 32 values of row t of a [64][128] bf16 tile, columns [col0, col0 + 32)
-__device__ __forceinline__ void tile_row_get32(const uint8_t* tile, int t, int col0, float* x) {
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch)
-        unpack8(*reinterpret_cast<const uint4*>(tile + sw_chunk(64, t, (col0 >> 3) + ch)), x + ch * 8);
-}
-
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
-#pragma unroll
-    for (int i = 0; i < 32; i += 8) *reinterpret_cast<uint4*>(dst + i) = pack8(v + i);
+    if (G.warp == 0) tmem_dealloc(tmem, DV);
 }
 
 // ===========================================================================
 // forward sweep: o for one (segment, row, head, 128-wide value block)
 // ===========================================================================
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     tc_fwd_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                         const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                         const float* __restrict__ g, const float* __restrict__ S_in,
@@ -228,38 +321,35 @@ __global__ void __launch_bounds__(128, 1)
     __shared__ __align__(8) uint64_t mma_bar;
     __shared__ uint32_t tmem_slot;
 
+    const Geo G = geo();
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H, vb = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tau = warp * 16 + lane;  // token row of the M = 64 tiles (lanes 0-15)
-    const bool tok = lane < 16;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     const uint32_t fb = smem_u32(&full_bar), mb = smem_u32(&mma_bar);
 
-    if (tid == 0) {
+    if (G.tid == 0) {
         mbar_init(fb, 1);
         mbar_init(mb, 1);
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
 
-    // fp32 master state row i = tid, columns [128 vb, 128 vb + 128)
-    float S[128];
+    // fp32 master state: row srow, columns [128 vb + 64 grp, +64)
+    float S[64];
     {
-        const float* src = S_in + sum_off(d, seg, b, h) + int64_t(tid) * d.Dv + vb * 128;
+        const float* src = S_in + sum_off(d, seg, b, h) + int64_t(G.srow) * d.Dv + vb * 128 + 64 * G.grp;
 #pragma unroll
-        for (int j = 0; j < 128; j += 4) {
+        for (int j = 0; j < 64; j += 4) {
             const float4 x = *reinterpret_cast<const float4*>(src + j);
             S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
         }
-        store_state_row(Sb, tid, S);
+        store_state_half(Sb, G.srow, G.grp, S);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    const uint32_t t_lane = uint32_t(warp * 32) << 16;
     auto issue = [&](int c) {
         const int row = b * d.T + a0 + c * kChunk;
         mbar_expect_tx(fb, 6 * kTileBytes);
@@ -267,25 +357,25 @@ __global__ void __launch_bounds__(128, 1)
         load_tile(Ks, &mk, 0, 128, h, row, fb);
         load_tile(Vs, &mv, vb * 128, 128, h, row, fb);
     };
-    if (tid == 0) issue(0);
+    if (G.tid == 0) issue(0);
     GateRegs gr;
-    if (warp == 0) gr = gate_load(d, g, b, h, a0, lane);
+    if (G.warp == 0) gr = gate_load(d, g, b, h, a0, G.lane);
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
         const int t0 = a0 + c * kChunk;
-        if (warp == 0) {
-            gate_prep(gr, &gs, lane);
-            if (c + 1 < nch) gr = gate_load(d, g, b, h, t0 + kChunk, lane);
+        if (G.warp == 0) {
+            gate_prep(gr, &gs, G.lane);
+            if (c + 1 < nch) gr = gate_load(d, g, b, h, t0 + kChunk, G.lane);
         }
         mbar_wait(fb, c & 1);
         __syncthreads();
         const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks), va = smem_u32(Vs);
         const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb);
-        if (tid == 0) {
+        if (G.tid == 0) {
             tc_fence_after();
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
+            for (int s = 0; s < 8; ++s) {  // scores = Q K^T
                 const uint32_t off = (s >> 2) * kTileBytes + (s & 3) * 32;
                 mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, s > 0);
             }
@@ -295,19 +385,22 @@ __global__ void __launch_bounds__(128, 1)
         mph ^= 1;
         tc_fence_after();
         {
-            float x[64];
-            tmem_ld32(tmem + t_lane, x);
-            tmem_ld32(tmem + t_lane + 32, x + 32);
-            float dummy;
-            if (tok) masked_row(Ps, gs, tau, x, d.scale, false, &dummy);
-            const int r = tid >> 1, blk = tid & 1;
-            scale_row128(Qs + blk * kTileBytes + r * 128, d.scale * gs.win[r]);
-            scale_row128(Ks + blk * kTileBytes + r * 128, gs.wout[r]);
+            float x[16], gam[16];
+            tok16(tmem, G, 32 * G.grp, x);
+            const int c0 = 32 * G.grp + 16 * G.hi;
+            decay_row16(gs, G.tau, c0, false, gam);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] *= d.scale * gam[e];
+            store_row16(Ps, G.tau, c0, x);
+            int r;
+            uint8_t* pq = quarter_row(Qs, G.tid, &r);
+            scale_quarter(pq, d.scale * gs.win[r]);
+            scale_quarter(quarter_row(Ks, G.tid, &r), gs.wout[r]);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (G.tid == 0) {
             tc_fence_after();
             constexpr uint32_t id_o = idesc_bf16(64, 128, 0, 1);
             constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
@@ -327,37 +420,30 @@ __global__ void __launch_bounds__(128, 1)
         }
         mbar_wait(mb, mph);
         mph ^= 1;
-        if (tid == 0 && c + 1 < nch) issue(c + 1);
+        if (G.tid == 0 && c + 1 < nch) issue(c + 1);
         tc_fence_after();
         {
-            __nv_bfloat16* orow = o + (((int64_t)b * d.T + t0 + tau) * d.H + h) * d.Dv + vb * 128;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                float x[32];
-                tmem_ld32(tmem + t_lane + cb * 32, x);
-                if (tok) store_bf16x32(orow + cb * 32, x);
-            }
-            const float W = gs.W;
+            __nv_bfloat16* orow = o + (((int64_t)b * d.T + t0 + G.tau) * d.H + h) * d.Dv + vb * 128;
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                float x[32];
-                tmem_ld32(tmem + t_lane + 128 + cb * 32, x);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) S[cb * 32 + e] = fmaf(W, S[cb * 32 + e], x[e]);
+            for (int k = 0; k < 2; ++k) {
+                float x[16];
+                const int col = 64 * G.grp + 32 * k;
+                tok16(tmem, G, col, x);
+                store_bf16x16(orow + col + 16 * G.hi, x);
             }
-            store_state_row(Sb, tid, S);
+            state_update(tmem, G, 128, gs.W, S, Sb);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
     }
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (G.warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ===========================================================================
 // forward sweep of the backward: dq and q.dq' for one (segment, row, head), Dv = 128
 // ===========================================================================
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     tc_dq_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                  const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                  const __grid_constant__ CUtensorMap mdo, const float* __restrict__ g,
@@ -377,37 +463,36 @@ __global__ void __launch_bounds__(128, 1)
     __shared__ __align__(8) uint64_t full_bar;
     __shared__ __align__(8) uint64_t mma_bar;
     __shared__ uint32_t tmem_slot;
+    __shared__ float diag_s[kChunk];
+    __shared__ float apart[2][kChunk];
 
+    const Geo G = geo();
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tau = warp * 16 + lane;
-    const bool tok = lane < 16;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     const uint32_t fb = smem_u32(&full_bar), mb = smem_u32(&mma_bar);
 
-    if (tid == 0) {
+    if (G.tid == 0) {
         mbar_init(fb, 1);
         mbar_init(mb, 1);
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
-    float S[128];
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
+    float S[64];
     {
-        const float* src = S_in + sum_off(d, seg, b, h) + int64_t(tid) * 128;
+        const float* src = S_in + sum_off(d, seg, b, h) + int64_t(G.srow) * 128 + 64 * G.grp;
 #pragma unroll
-        for (int j = 0; j < 128; j += 4) {
+        for (int j = 0; j < 64; j += 4) {
             const float4 x = *reinterpret_cast<const float4*>(src + j);
             S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
         }
-        store_state_row(Sb, tid, S);
+        store_state_half(Sb, G.srow, G.grp, S);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    const uint32_t t_lane = uint32_t(warp * 32) << 16;
     auto issue = [&](int c) {
         const int row = b * d.T + a0 + c * kChunk;
         mbar_expect_tx(fb, 8 * kTileBytes);
@@ -416,21 +501,21 @@ __global__ void __launch_bounds__(128, 1)
         load_tile(Vs, &mv, 0, 128, h, row, fb);
         load_tile(Ds, &mdo, 0, 128, h, row, fb);
     };
-    if (tid == 0) issue(0);
+    if (G.tid == 0) issue(0);
     GateRegs gr;
-    if (warp == 0) gr = gate_load(d, g, b, h, a0, lane);
+    if (G.warp == 0) gr = gate_load(d, g, b, h, a0, G.lane);
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
         const int t0 = a0 + c * kChunk;
-        if (warp == 0) {
-            gate_prep(gr, &gs, lane);
-            if (c + 1 < nch) gr = gate_load(d, g, b, h, t0 + kChunk, lane);
+        if (G.warp == 0) {
+            gate_prep(gr, &gs, G.lane);
+            if (c + 1 < nch) gr = gate_load(d, g, b, h, t0 + kChunk, G.lane);
         }
         mbar_wait(fb, c & 1);
         __syncthreads();
         const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks), va = smem_u32(Vs), da = smem_u32(Ds);
         const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb);
-        if (tid == 0) {
+        if (G.tid == 0) {
             tc_fence_after();
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
 #pragma unroll
@@ -443,20 +528,25 @@ __global__ void __launch_bounds__(128, 1)
         mbar_wait(mb, mph);
         mph ^= 1;
         tc_fence_after();
-        float diag = 0.f;  // dO_t . v_t
         {
-            float x[64];
-            tmem_ld32(tmem + t_lane, x);
-            tmem_ld32(tmem + t_lane + 32, x + 32);
-            if (tok) masked_row(Ps, gs, tau, x, d.scale, true, &diag);
-            const int r = tid >> 1, blk = tid & 1;
-            scale_row128(Ds + blk * kTileBytes + r * 128, d.scale * gs.win[r]);
-            scale_row128(Vs + blk * kTileBytes + r * 128, gs.wout[r]);
+            float x[16], gam[16];
+            tok16(tmem, G, 32 * G.grp, x);
+            const int c0 = 32 * G.grp + 16 * G.hi;
+            decay_row16(gs, G.tau, c0, true, gam);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                if (c0 + e == G.tau) diag_s[G.tau] = x[e];  // dO_t . v_t
+                x[e] *= d.scale * gam[e];
+            }
+            store_row16(Ps, G.tau, c0, x);
+            int r;
+            scale_quarter(quarter_row(Ds, G.tid, &r), d.scale * gs.win[r]);
+            scale_quarter(quarter_row(Vs, G.tid, &r), gs.wout[r]);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (G.tid == 0) {
             tc_fence_after();
             constexpr uint32_t id_a = idesc_bf16(64, 128, 0, 1);
             constexpr uint32_t id_b = idesc_bf16(64, 128, 0, 0);
@@ -479,47 +569,42 @@ __global__ void __launch_bounds__(128, 1)
         mph ^= 1;
         tc_fence_after();
         {
-            const int64_t tok_off = ((int64_t)b * d.T + t0 + tau) * d.H + h;
+            __nv_bfloat16* drow = dq + (((int64_t)b * d.T + t0 + G.tau) * d.H + h) * 128;
+            const float cd = d.scale * diag_s[G.tau];
             float a = 0.f;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                float x[32];
-                tmem_ld32(tmem + t_lane + cb * 32, x);
-                if (tok) {
-                    float qv[32], kv[32];
-                    tile_row_get32(Qs, tau, cb * 32, qv);
-                    tile_row_get32(Ks, tau, cb * 32, kv);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        a = fmaf(qv[e], x[e], a);
-                        x[e] = fmaf(d.scale * diag, kv[e], x[e]);
-                    }
-                    store_bf16x32(dq + tok_off * 128 + cb * 32, x);
+            for (int k = 0; k < 2; ++k) {
+                float x[16], qv[16], kv[16];
+                const int col = 64 * G.grp + 32 * k;
+                tok16(tmem, G, col, x);
+                const int c0 = col + 16 * G.hi;
+                tile_row_get16(Qs, G.tau, c0, qv);
+                tile_row_get16(Ks, G.tau, c0, kv);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    a = fmaf(qv[e], x[e], a);
+                    x[e] = fmaf(cd, kv[e], x[e]);
                 }
+                store_bf16x16(drow + c0, x);
             }
-            if (tok) qdq[tok_off] = a;
-            const float W = gs.W;
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                float x[32];
-                tmem_ld32(tmem + t_lane + 128 + cb * 32, x);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) S[cb * 32 + e] = fmaf(W, S[cb * 32 + e], x[e]);
-            }
-            store_state_row(Sb, tid, S);
+            a += __shfl_xor_sync(kFull, a, 16);
+            if (!G.hi) apart[G.grp][G.tau] = a;
+            state_update(tmem, G, 128, gs.W, S, Sb);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0 && c + 1 < nch) issue(c + 1);
+        if (G.tid < kChunk)
+            qdq[((int64_t)b * d.T + t0 + G.tid) * d.H + h] = apart[0][G.tid] + apart[1][G.tid];
+        if (G.tid == 0 && c + 1 < nch) issue(c + 1);
     }
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (G.warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ===========================================================================
 // reverse sweep of the backward: dk, dv, dg for one (segment, row, head), Dv = 128
 // ===========================================================================
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     tc_rev_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                   const __grid_constant__ CUtensorMap mdo, const float* __restrict__ g,
@@ -541,35 +626,34 @@ __global__ void __launch_bounds__(128, 1)
     __shared__ __align__(8) uint64_t full_bar[2];
     __shared__ __align__(8) uint64_t mma_bar;
     __shared__ uint32_t tmem_slot;
-    __shared__ float cbuf[kChunk];
-    __shared__ float dgbuf[kChunk];
-    __shared__ float red[4];
-    __shared__ float carry_s;
+    __shared__ float diag_s[kChunk];
+    __shared__ float bpart[2][kChunk];
+    __shared__ float red[8];
 
+    const Geo G = geo();
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tau = warp * 16 + lane;
-    const bool tok = lane < 16;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     const uint32_t mb = smem_u32(&mma_bar);
 
-    if (tid == 0) {
+    if (G.tid == 0) {
         mbar_init(smem_u32(&full_bar[0]), 1);
         mbar_init(smem_u32(&full_bar[1]), 1);
         mbar_init(mb, 1);
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
-    // E (adjoint arriving at the last state of the current chunk) starts as dS_out;
-    // ext = <S_out, dS_out> with S_out read as S_in[seg+1]
-    float E[128];
-    float ext = 0.f;
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
+    // E (adjoint arriving at the last state of the current chunk) starts as
+    // dS_out; ext = <S_out, dS_out> with S_out read as S_in[seg+1]
+    float E[64];
     {
-        const float* src = dS_out + sum_off(d, seg, b, h) + int64_t(tid) * 128;
-        const float* so = seg + 1 < d.nseg ? S_in + sum_off(d, seg + 1, b, h) + int64_t(tid) * 128 : nullptr;
+        const float* src = dS_out + sum_off(d, seg, b, h) + int64_t(G.srow) * 128 + 64 * G.grp;
+        const float* so = seg + 1 < d.nseg
+                              ? S_in + sum_off(d, seg + 1, b, h) + int64_t(G.srow) * 128 + 64 * G.grp
+                              : nullptr;
+        float ext = 0.f;
 #pragma unroll
-        for (int j = 0; j < 128; j += 4) {
+        for (int j = 0; j < 64; j += 4) {
             const float4 x = *reinterpret_cast<const float4*>(src + j);
             E[j] = x.x; E[j + 1] = x.y; E[j + 2] = x.z; E[j + 3] = x.w;
             if (so) {
@@ -578,52 +662,59 @@ __global__ void __launch_bounds__(128, 1)
                 ext = fmaf(x.z, y.z, ext); ext = fmaf(x.w, y.w, ext);
             }
         }
-        store_state_row(Eb, tid, E);
+        store_state_half(Eb, G.srow, G.grp, E);
         ext = warp_sum(ext);
-        if (lane == 0) red[warp] = ext;
+        if (G.lane == 0) red[G.warp] = ext;
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) carry_s = red[0] + red[1] + red[2] + red[3];
+    // running gate-gradient sum carried from later chunks (held by warp 0)
+    float carry = 0.f;
+    if (G.warp == 0) {
+#pragma unroll
+        for (int w = 0; w < 8; ++w) carry += red[w];
+    }
     const uint32_t tmem = tmem_slot;
-    const uint32_t t_lane = uint32_t(warp * 32) << 16;
-    auto stage_ptr = [&](int s) { return smem + s * STAGE; };
     auto issue = [&](int it, int s) {
         const int c = nch - 1 - it;
         const int row = b * d.T + a0 + c * kChunk;
         const uint32_t bar = smem_u32(&full_bar[s]);
-        uint8_t* st = stage_ptr(s);
+        uint8_t* st = smem + s * STAGE;
         mbar_expect_tx(bar, STAGE);
         load_tile(st, &mq, 0, 128, h, row, bar);
         load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
         load_tile(st + 4 * kTileBytes, &mv, 0, 128, h, row, bar);
         load_tile(st + 6 * kTileBytes, &mdo, 0, 128, h, row, bar);
     };
-    if (tid == 0) {
+    if (G.tid == 0) {
         issue(0, 0);
         if (nch > 1) issue(1, 1);
     }
     GateRegs gr;
-    if (warp == 0) gr = gate_load(d, g, b, h, a0 + (nch - 1) * kChunk, lane);
+    if (G.warp == 0) gr = gate_load(d, g, b, h, a0 + (nch - 1) * kChunk, G.lane);
     uint32_t mph = 0;
     for (int it = 0; it < nch; ++it) {
         const int c = nch - 1 - it;
         const int t0 = a0 + c * kChunk;
         const int s = it & 1;
-        uint8_t* Qs = stage_ptr(s);
+        uint8_t* Qs = smem + s * STAGE;
         uint8_t* Ks = Qs + 2 * kTileBytes;
         uint8_t* Vs = Qs + 4 * kTileBytes;
         uint8_t* Ds = Qs + 6 * kTileBytes;
-        if (warp == 0) {
-            gate_prep(gr, &gs, lane);
-            if (it + 1 < nch) gr = gate_load(d, g, b, h, t0 - kChunk, lane);
+        // warp 0 lane l scans tokens 63 - 2l and 62 - 2l; fetch their q.dq' early
+        float qd0 = 0.f, qd1 = 0.f;
+        if (G.warp == 0) {
+            gate_prep(gr, &gs, G.lane);
+            if (it + 1 < nch) gr = gate_load(d, g, b, h, t0 - kChunk, G.lane);
+            qd0 = __ldg(qdq + ((int64_t)b * d.T + t0 + 63 - 2 * G.lane) * d.H + h);
+            qd1 = __ldg(qdq + ((int64_t)b * d.T + t0 + 62 - 2 * G.lane) * d.H + h);
         }
         mbar_wait(smem_u32(&full_bar[s]), (it >> 1) & 1);
         __syncthreads();
         const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks), va = smem_u32(Vs), da = smem_u32(Ds);
-        if (tid == 0) {
+        if (G.tid == 0) {
             tc_fence_after();
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
 #pragma unroll
@@ -637,39 +728,32 @@ __global__ void __launch_bounds__(128, 1)
         mbar_wait(mb, mph);
         mph ^= 1;
         tc_fence_after();
-        float diag = 0.f;
         {
-            float x[64];
-            tmem_ld32(tmem + t_lane, x);
-            tmem_ld32(tmem + t_lane + 32, x + 32);
-            float dummy;
-            if (tok) masked_row(PA, gs, tau, x, d.scale, false, &dummy);
-            tmem_ld32(tmem + t_lane + 64, x);
-            tmem_ld32(tmem + t_lane + 96, x + 32);
-            if (tok) masked_row(PD, gs, tau, x, d.scale, true, &diag);
-            const int r = tid >> 1, blk = tid & 1;
-            const uint32_t ro = blk * kTileBytes + r * 128;
-            // Q~ = scale win Q and K~ = wout K into their own tiles; V~ = wout V in place
+            float xa[16], xd[16], gam[16];
+            tok16(tmem, G, 32 * G.grp, xa);
+            tok16(tmem, G, 64 + 32 * G.grp, xd);
+            const int c0 = 32 * G.grp + 16 * G.hi;
+            decay_row16(gs, G.tau, c0, false, gam);
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                float xq[8], xk[8];
-                unpack8(*reinterpret_cast<const uint4*>(Qs + ro + ch * 16), xq);
-                unpack8(*reinterpret_cast<const uint4*>(Ks + ro + ch * 16), xk);
-                const float wq = d.scale * gs.win[r], wk = gs.wout[r];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    xq[e] *= wq;
-                    xk[e] *= wk;
-                }
-                *reinterpret_cast<uint4*>(Qt + ro + ch * 16) = pack8(xq);
-                *reinterpret_cast<uint4*>(Kt + ro + ch * 16) = pack8(xk);
+            for (int e = 0; e < 16; ++e) {
+                const int sidx = c0 + e;
+                if (sidx == G.tau) diag_s[G.tau] = xd[e];  // dO_t . v_t
+                xa[e] *= d.scale * gam[e];
+                xd[e] = sidx < G.tau ? xd[e] * d.scale * gam[e] : 0.f;
             }
-            scale_row128(Vs + ro, gs.wout[r]);
+            store_row16(PA, G.tau, c0, xa);
+            store_row16(PD, G.tau, c0, xd);
+            // Q~ = scale win Q and K~ = wout K into their own tiles; V~ = wout V in place
+            int r;
+            const uint32_t qoff = uint32_t(quarter_row(Qs, G.tid, &r) - Qs);
+            scale_quarter_to(Qs + qoff, Qt + qoff, d.scale * gs.win[r]);
+            scale_quarter_to(Ks + qoff, Kt + qoff, gs.wout[r]);
+            scale_quarter(Vs + qoff, gs.wout[r]);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (G.tid == 0) {
             tc_fence_after();
             const uint32_t pa = smem_u32(PA), pd = smem_u32(PD), ea = smem_u32(Eb);
             const uint32_t qta = smem_u32(Qt), kta = smem_u32(Kt);
@@ -703,63 +787,78 @@ __global__ void __launch_bounds__(128, 1)
         mph ^= 1;
         tc_fence_after();
         {
-            const int64_t tok_off = ((int64_t)b * d.T + t0 + tau) * d.H + h;
+            const int64_t tok = ((int64_t)b * d.T + t0 + G.tau) * d.H + h;
+            const float cd = d.scale * diag_s[G.tau];
             float bk = 0.f;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                float x[32];
-                tmem_ld32(tmem + t_lane + 128 + cb * 32, x);
-                if (tok) {
-                    float qv[32], kv[32];
-                    tile_row_get32(Qs, tau, cb * 32, qv);
-                    tile_row_get32(Ks, tau, cb * 32, kv);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        bk = fmaf(kv[e], x[e], bk);
-                        x[e] = fmaf(d.scale * diag, qv[e], x[e]);
-                    }
-                    store_bf16x32(dk + tok_off * 128 + cb * 32, x);
+            for (int k = 0; k < 2; ++k) {
+                float x[16], qv[16], kv[16];
+                const int col = 64 * G.grp + 32 * k;
+                const int c0 = col + 16 * G.hi;
+                tok16(tmem, G, 128 + col, x);
+                tile_row_get16(Qs, G.tau, c0, qv);
+                tile_row_get16(Ks, G.tau, c0, kv);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    bk = fmaf(kv[e], x[e], bk);
+                    x[e] = fmaf(cd, qv[e], x[e]);
                 }
+                store_bf16x16(dk + tok * 128 + c0, x);
+                tok16(tmem, G, 256 + col, x);
+                store_bf16x16(dv + tok * 128 + c0, x);
             }
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                float x[32];
-                tmem_ld32(tmem + t_lane + 256 + cb * 32, x);
-                if (tok) store_bf16x32(dv + tok_off * 128 + cb * 32, x);
-            }
-            if (tok) cbuf[tau] = qdq[tok_off] - bk;
-            const float W = gs.W;
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                float x[32];
-                tmem_ld32(tmem + t_lane + 384 + cb * 32, x);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) E[cb * 32 + e] = fmaf(W, E[cb * 32 + e], x[e]);
-            }
-            store_state_row(Eb, tid, E);
+            bk += __shfl_xor_sync(kFull, bk, 16);
+            if (!G.hi) bpart[G.grp][G.tau] = bk;
+            state_update(tmem, G, 384, gs.W, E, Eb);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
-            // gate gradient of the chunk, newest token first: sums restart where
-            // a sequence starts; tokens that start one get exactly 0
-            float run = carry_s;
-            for (int t = kChunk - 1; t >= 0; --t) {
-                if (t + 1 < kChunk && gs.lid[t + 1] != gs.lid[t]) run = 0.f;
-                run += cbuf[t];
-                const bool start = t == 0 ? gs.first != 0 : gs.lid[t] != gs.lid[t - 1];
-                dgbuf[t] = start ? 0.f : run;
+        if (G.warp == 0) {
+            // gate gradient of the chunk: reverse running sums of q.dq' - k.dk'
+            // restarting where a sequence starts, plus the carry from later
+            // chunks for the sequence open at the chunk's end.  Lane l holds
+            // tokens t0 = 63 - 2l and t1 = 62 - 2l; a segmented warp scan runs
+            // over the lanes in that (reverse) order.
+            const int tA = 63 - 2 * G.lane, tB = 62 - 2 * G.lane;
+            const float cA = qd0 - (bpart[0][tA] + bpart[1][tA]);
+            const float cB = qd1 - (bpart[0][tB] + bpart[1][tB]);
+            // head: token t + 1 starts a sequence, so t starts a new reverse run
+            const bool hA = tA < 63 && gs.lid[tA + 1] != gs.lid[tA];
+            const bool hB = gs.lid[tB + 1] != gs.lid[tB];
+            float v = hB ? cB : cA + cB;  // pair summary
+            bool f = hA || hB;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float vp = __shfl_up_sync(kFull, v, o);
+                const bool fp = __shfl_up_sync(kFull, f, o);
+                if (G.lane >= o) {
+                    if (!f) v += vp;
+                    f = f || fp;
+                }
             }
-            carry_s = gs.first ? 0.f : run;
-            if (it + 2 < nch) issue(it + 2, s);
+            // exclusive prefix for this lane, with the carry as the leftmost element
+            float vx = __shfl_up_sync(kFull, v, 1);
+            bool fx = __shfl_up_sync(kFull, f, 1);
+            if (G.lane == 0) {
+                vx = 0.f;
+                fx = false;
+            }
+            const float X = fx ? vx : carry + vx;
+            const float sA = cA + (hA ? 0.f : X);
+            const float sB = cB + (hB ? 0.f : sA);
+            const bool stA = gs.lid[tA] != gs.lid[tA - 1];  // tA >= 1
+            const bool stB = tB == 0 ? gs.first != 0 : gs.lid[tB] != gs.lid[tB - 1];
+            dg[((int64_t)b * d.T + t0 + tA) * d.H + h] = stA ? 0.f : sA;
+            dg[((int64_t)b * d.T + t0 + tB) * d.H + h] = stB ? 0.f : sB;
+            const float last = __shfl_sync(kFull, sB, 31);  // value at token 0
+            carry = gs.first ? 0.f : last;
+            if (G.tid == 0 && it + 2 < nch) issue(it + 2, s);
         }
-        __syncthreads();
-        if (tid < kChunk) dg[((int64_t)b * d.T + t0 + tid) * d.H + h] = dgbuf[tid];
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (G.warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // Failure-detection self test: waits on an mbarrier that nothing arrives on,
@@ -862,11 +961,11 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             if (d.Dv == 128) {
                 auto fn = tc_outer_kernel<128, false>;
                 if (!set_smem(fn, kOuterSmem)) return RM_ERR_CUDA;
-                fn<<<grid, 128, kOuterSmem, s>>>(d, mk, mv, p.g, p.M, p.sum_out);
+                fn<<<grid, kThreads, kOuterSmem, s>>>(d, mk, mv, p.g, p.M, p.sum_out);
             } else {
                 auto fn = tc_outer_kernel<256, false>;
                 if (!set_smem(fn, kOuterSmem)) return RM_ERR_CUDA;
-                fn<<<grid, 128, kOuterSmem, s>>>(d, mk, mv, p.g, p.M, p.sum_out);
+                fn<<<grid, kThreads, kOuterSmem, s>>>(d, mk, mv, p.g, p.M, p.sum_out);
             }
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(1);
@@ -877,7 +976,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 !make_map(&mv, p.v, d, d.Dv))
                 return RM_ERR_CUDA;
             if (!set_smem(tc_fwd_apply_kernel, kFwdSmem)) return RM_ERR_CUDA;
-            tc_fwd_apply_kernel<<<dim3(d.nseg, d.B * d.H, d.Dv / 128), 128, kFwdSmem, s>>>(
+            tc_fwd_apply_kernel<<<dim3(d.nseg, d.B * d.H, d.Dv / 128), kThreads, kFwdSmem, s>>>(
                 d, mq, mk, mv, p.g, p.S_in, static_cast<__nv_bfloat16*>(p.out0));
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(1);
@@ -889,9 +988,9 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 return RM_ERR_CUDA;
             auto fo = tc_outer_kernel<128, true>;
             if (!set_smem(fo, kOuterSmem) || !set_smem(tc_dq_kernel, kDqSmem)) return RM_ERR_CUDA;
-            fo<<<grid, 128, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
+            fo<<<grid, kThreads, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
-            tc_dq_kernel<<<grid, 128, kDqSmem, s>>>(d, mq, mk, mv, mdo, p.g, p.S_in,
+            tc_dq_kernel<<<grid, kThreads, kDqSmem, s>>>(d, mq, mk, mv, mdo, p.g, p.S_in,
                                                     static_cast<__nv_bfloat16*>(p.out0), p.ws_f32);
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(2);
@@ -902,7 +1001,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 !make_map(&mv, p.v, d, 128) || !make_map(&mdo, p.dO, d, 128))
                 return RM_ERR_CUDA;
             if (!set_smem(tc_rev_kernel, kRevSmem)) return RM_ERR_CUDA;
-            tc_rev_kernel<<<grid, 128, kRevSmem, s>>>(
+            tc_rev_kernel<<<grid, kThreads, kRevSmem, s>>>(
                 d, mq, mk, mv, mdo, p.g, p.S_in, p.dS_out, p.ws_f32,
                 static_cast<__nv_bfloat16*>(p.out0), static_cast<__nv_bfloat16*>(p.out1), p.dg);
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
