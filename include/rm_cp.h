@@ -254,8 +254,7 @@ uint64_t rm_cp_launch_count(void);
  * every call, 1 = tensor-core (tcgen05) path for every call, 2 = tensor-core
  * path for some calls and the generic path for the others.  -1 for an
  * invalid problem.  The tensor-core path serves bf16 storage with Dk = 128,
- * Dv in {128, 256} and segment lengths that are multiples of 64 (its
- * backward calls need Dv = 128). */
+ * Dv in {128, 256} and segment lengths that are multiples of 64. */
 int32_t rm_cp_path(const rm_cp_problem* p);
 
 #ifdef __cplusplus

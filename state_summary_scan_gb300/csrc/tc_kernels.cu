@@ -124,6 +124,42 @@ __device__ __forceinline__ void state_update(uint32_t tmem, const Geo& g, int co
     store_state_half(tile, g.srow, g.grp, S);
 }
 
+// State rows of width DV split over the two column groups: thread (srow, grp)
+// owns columns 128 h + 64 grp + [0, 64) for h < DV / 128, stored in S[64 h + e].
+template <int DV>
+__device__ __forceinline__ void load_state_rows(const float* __restrict__ src, const Geo& g, float* S,
+                                                uint8_t* tile) {
+#pragma unroll
+    for (int hh = 0; hh < DV / 128; ++hh) {
+        const float* p = src + int64_t(g.srow) * DV + 128 * hh + 64 * g.grp;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(p + j);
+            S[64 * hh + j] = x.x; S[64 * hh + j + 1] = x.y; S[64 * hh + j + 2] = x.z; S[64 * hh + j + 3] = x.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(tile + sw_chunk(128, g.srow, 16 * hh + 8 * g.grp + c)) =
+                pack8(S + 64 * hh + c * 8);
+    }
+}
+// S[64 hh + e] = W S[64 hh + e] + acc[srow][col + 64 grp + e] (accumulator holding
+// state columns [128 hh, +128) at column col); writes those columns as bf16.
+__device__ __forceinline__ void state_update_half(uint32_t tmem, const Geo& g, int col, int hh, float W,
+                                                  float* S, uint8_t* tile) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        float y[32];
+        tmem_ld32(tmem + g.tl + col + 64 * g.grp + 32 * hf, y);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) S[64 * hh + 32 * hf + e] = fmaf(W, S[64 * hh + 32 * hf + e], y[e]);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(tile + sw_chunk(128, g.srow, 16 * hh + 8 * g.grp + c)) =
+            pack8(S + 64 * hh + c * 8);
+}
+
 // Physical 16-byte chunks [4 h4, 4 h4 + 4) of row r of block blk of a [64][128]
 // tile, each thread of the CTA taking one such quarter row.
 __device__ __forceinline__ uint8_t* quarter_row(uint8_t* tile, int tid, int* r) {
@@ -441,16 +477,20 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ===========================================================================
-// forward sweep of the backward: dq and q.dq' for one (segment, row, head), Dv = 128
+// forward sweep of the backward: dq and q.dq' for one (segment, row, head)
 // ===========================================================================
-__global__ void __launch_bounds__(kThreads, 2)
+template <int DV>
+__global__ void __launch_bounds__(kThreads, DV == 128 ? 2 : 1)
     tc_dq_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                  const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                  const __grid_constant__ CUtensorMap mdo, const float* __restrict__ g,
                  const float* __restrict__ S_in, __nv_bfloat16* __restrict__ dq,
                  float* __restrict__ qdq) {
+    constexpr int NV = DV / 64;  // 64-column blocks of v and dO
     constexpr uint32_t OFF_Q = 0, OFF_K = 2 * kTileBytes, OFF_V = 4 * kTileBytes;
-    constexpr uint32_t OFF_DO = 6 * kTileBytes, OFF_P = 8 * kTileBytes, OFF_S = 9 * kTileBytes;
+    constexpr uint32_t OFF_DO = OFF_V + NV * kTileBytes, OFF_P = OFF_DO + NV * kTileBytes;
+    constexpr uint32_t OFF_S = OFF_P + kTileBytes;  // S tile [128][DV]: 2 NV blocks
+    constexpr uint32_t TCOLS = DV == 128 ? 256 : 512;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint8_t* Qs = smem + OFF_Q;
@@ -477,17 +517,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_init(mb, 1);
         mbar_fence_init();
     }
-    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
-    float S[64];
-    {
-        const float* src = S_in + sum_off(d, seg, b, h) + int64_t(G.srow) * 128 + 64 * G.grp;
-#pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(src + j);
-            S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
-        }
-        store_state_half(Sb, G.srow, G.grp, S);
-    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), TCOLS);
+    float S[DV / 2];
+    load_state_rows<DV>(S_in + sum_off(d, seg, b, h), G, S, Sb);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -495,11 +527,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t tmem = tmem_slot;
     auto issue = [&](int c) {
         const int row = b * d.T + a0 + c * kChunk;
-        mbar_expect_tx(fb, 8 * kTileBytes);
+        mbar_expect_tx(fb, (4 + 2 * NV) * kTileBytes);
         load_tile(Qs, &mq, 0, 128, h, row, fb);
         load_tile(Ks, &mk, 0, 128, h, row, fb);
-        load_tile(Vs, &mv, 0, 128, h, row, fb);
-        load_tile(Ds, &mdo, 0, 128, h, row, fb);
+        load_tile(Vs, &mv, 0, DV, h, row, fb);
+        load_tile(Ds, &mdo, 0, DV, h, row, fb);
     };
     if (G.tid == 0) issue(0);
     GateRegs gr;
@@ -519,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc_fence_after();
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {  // dA = dO V^T
+            for (int s = 0; s < DV / 16; ++s) {  // dA = dO V^T
                 const uint32_t off = (s >> 2) * kTileBytes + (s & 3) * 32;
                 mma_bf16(tmem, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, s > 0);
             }
@@ -539,9 +571,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 x[e] *= d.scale * gam[e];
             }
             store_row16(Ps, G.tau, c0, x);
-            int r;
-            scale_quarter(quarter_row(Ds, G.tid, &r), d.scale * gs.win[r]);
-            scale_quarter(quarter_row(Vs, G.tid, &r), gs.wout[r]);
+#pragma unroll
+            for (int pr = 0; pr < NV / 2; ++pr) {
+                int r;
+                scale_quarter(quarter_row(Ds + 2 * pr * kTileBytes, G.tid, &r), d.scale * gs.win[r]);
+                scale_quarter(quarter_row(Vs + 2 * pr * kTileBytes, G.tid, &r), gs.wout[r]);
+            }
         }
         fence_async_smem();
         tc_fence_before();
@@ -550,13 +585,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc_fence_after();
             constexpr uint32_t id_a = idesc_bf16(64, 128, 0, 1);
             constexpr uint32_t id_b = idesc_bf16(64, 128, 0, 0);
-            constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
+            constexpr uint32_t id_s = idesc_bf16(128, DV, 1, 1);
 #pragma unroll
             for (int k = 0; k < 4; ++k)  // dq' = P K  (strictly causal part)
                 mma_bf16(tmem, sdesc(pa + k * 32, 16, 1024), sdesc(ka + k * 2048, kTileBytes, 1024),
                          id_a, k > 0);
 #pragma unroll
-            for (int s = 0; s < 8; ++s)  // dq' += dO~ S_prev^T
+            for (int s = 0; s < DV / 16; ++s)  // dq' += dO~ S_prev^T
                 mma_bf16(tmem, sdesc(da + (s >> 2) * kTileBytes + (s & 3) * 32, 16, 1024),
                          sdesc(sa + (s >> 2) * 2 * kTileBytes + (s & 3) * 32, 16, 1024), id_b, 1);
 #pragma unroll
@@ -589,7 +624,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             a += __shfl_xor_sync(kFull, a, 16);
             if (!G.hi) apart[G.grp][G.tau] = a;
-            state_update(tmem, G, 128, gs.W, S, Sb);
+#pragma unroll
+            for (int hh = 0; hh < DV / 128; ++hh)
+                state_update_half(tmem, G, 128 + 128 * hh, hh, gs.W, S, Sb);
         }
         fence_async_smem();
         tc_fence_before();
@@ -598,12 +635,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             qdq[((int64_t)b * d.T + t0 + G.tid) * d.H + h] = apart[0][G.tid] + apart[1][G.tid];
         if (G.tid == 0 && c + 1 < nch) issue(c + 1);
     }
-    if (G.warp == 0) tmem_dealloc(tmem, 256);
+    if (G.warp == 0) tmem_dealloc(tmem, TCOLS);
 }
 
 // ===========================================================================
-// reverse sweep of the backward: dk, dv, dg for one (segment, row, head), Dv = 128
+// reverse sweep of the backward: dk, dv, dg for one (segment, row, head).
+// Dv = 256 processes dv and the adjoint update in two 128-column halves
+// (tensor memory holds one half at a time) and single-buffers its inputs.
 // ===========================================================================
+template <int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_rev_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
@@ -611,10 +651,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const float* __restrict__ S_in, const float* __restrict__ dS_out,
                   const float* __restrict__ qdq, __nv_bfloat16* __restrict__ dk,
                   __nv_bfloat16* __restrict__ dv, float* __restrict__ dg) {
-    constexpr uint32_t STAGE = 8 * kTileBytes;  // Q | K | V | dO
-    constexpr uint32_t OFF_QT = 2 * STAGE, OFF_KT = OFF_QT + 2 * kTileBytes;
+    constexpr int NV = DV / 64;
+    constexpr int NH = DV / 128;
+    constexpr int STAGES = DV == 128 ? 2 : 1;
+    constexpr uint32_t STAGE = (4 + 2 * NV) * kTileBytes;  // Q | K | V | dO
+    constexpr uint32_t OFF_QT = STAGES * STAGE, OFF_KT = OFF_QT + 2 * kTileBytes;
     constexpr uint32_t OFF_PA = OFF_KT + 2 * kTileBytes, OFF_PD = OFF_PA + kTileBytes;
-    constexpr uint32_t OFF_E = OFF_PD + kTileBytes;  // E tile: 32 KB
+    constexpr uint32_t OFF_E = OFF_PD + kTileBytes;  // E tile [128][DV]: 2 NV blocks
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint8_t* Qt = smem + OFF_QT;
@@ -623,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* PD = smem + OFF_PD;
     uint8_t* Eb = smem + OFF_E;
     __shared__ GateSmem gs;
-    __shared__ __align__(8) uint64_t full_bar[2];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
     __shared__ __align__(8) uint64_t mma_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ float diag_s[kChunk];
@@ -637,32 +680,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t mb = smem_u32(&mma_bar);
 
     if (G.tid == 0) {
-        mbar_init(smem_u32(&full_bar[0]), 1);
-        mbar_init(smem_u32(&full_bar[1]), 1);
+        for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
         mbar_init(mb, 1);
         mbar_fence_init();
     }
     if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
     // E (adjoint arriving at the last state of the current chunk) starts as
     // dS_out; ext = <S_out, dS_out> with S_out read as S_in[seg+1]
-    float E[64];
+    float E[DV / 2];
+    load_state_rows<DV>(dS_out + sum_off(d, seg, b, h), G, E, Eb);
     {
-        const float* src = dS_out + sum_off(d, seg, b, h) + int64_t(G.srow) * 128 + 64 * G.grp;
-        const float* so = seg + 1 < d.nseg
-                              ? S_in + sum_off(d, seg + 1, b, h) + int64_t(G.srow) * 128 + 64 * G.grp
-                              : nullptr;
         float ext = 0.f;
+        if (seg + 1 < d.nseg) {
+            const float* so = S_in + sum_off(d, seg + 1, b, h) + int64_t(G.srow) * DV + 64 * G.grp;
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(src + j);
-            E[j] = x.x; E[j + 1] = x.y; E[j + 2] = x.z; E[j + 3] = x.w;
-            if (so) {
-                const float4 y = *reinterpret_cast<const float4*>(so + j);
-                ext = fmaf(x.x, y.x, ext); ext = fmaf(x.y, y.y, ext);
-                ext = fmaf(x.z, y.z, ext); ext = fmaf(x.w, y.w, ext);
-            }
+            for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+                for (int j = 0; j < 64; j += 4) {
+                    const float4 y = *reinterpret_cast<const float4*>(so + 128 * hh + j);
+                    ext = fmaf(E[64 * hh + j], y.x, ext);
+                    ext = fmaf(E[64 * hh + j + 1], y.y, ext);
+                    ext = fmaf(E[64 * hh + j + 2], y.z, ext);
+                    ext = fmaf(E[64 * hh + j + 3], y.w, ext);
+                }
         }
-        store_state_half(Eb, G.srow, G.grp, E);
         ext = warp_sum(ext);
         if (G.lane == 0) red[G.warp] = ext;
     }
@@ -685,24 +726,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar, STAGE);
         load_tile(st, &mq, 0, 128, h, row, bar);
         load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
-        load_tile(st + 4 * kTileBytes, &mv, 0, 128, h, row, bar);
-        load_tile(st + 6 * kTileBytes, &mdo, 0, 128, h, row, bar);
+        load_tile(st + 4 * kTileBytes, &mv, 0, DV, h, row, bar);
+        load_tile(st + (4 + NV) * kTileBytes, &mdo, 0, DV, h, row, bar);
     };
-    if (G.tid == 0) {
-        issue(0, 0);
-        if (nch > 1) issue(1, 1);
-    }
+    if (G.tid == 0)
+        for (int it = 0; it < STAGES && it < nch; ++it) issue(it, it);
     GateRegs gr;
     if (G.warp == 0) gr = gate_load(d, g, b, h, a0 + (nch - 1) * kChunk, G.lane);
     uint32_t mph = 0;
     for (int it = 0; it < nch; ++it) {
         const int c = nch - 1 - it;
         const int t0 = a0 + c * kChunk;
-        const int s = it & 1;
+        const int s = it % STAGES;
         uint8_t* Qs = smem + s * STAGE;
         uint8_t* Ks = Qs + 2 * kTileBytes;
         uint8_t* Vs = Qs + 4 * kTileBytes;
-        uint8_t* Ds = Qs + 6 * kTileBytes;
+        uint8_t* Ds = Qs + (4 + NV) * kTileBytes;
         // warp 0 lane l scans tokens 63 - 2l and 62 - 2l; fetch their q.dq' early
         float qd0 = 0.f, qd1 = 0.f;
         if (G.warp == 0) {
@@ -711,16 +750,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             qd0 = __ldg(qdq + ((int64_t)b * d.T + t0 + 63 - 2 * G.lane) * d.H + h);
             qd1 = __ldg(qdq + ((int64_t)b * d.T + t0 + 62 - 2 * G.lane) * d.H + h);
         }
-        mbar_wait(smem_u32(&full_bar[s]), (it >> 1) & 1);
+        mbar_wait(smem_u32(&full_bar[s]), (it / STAGES) & 1);
         __syncthreads();
         const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks), va = smem_u32(Vs), da = smem_u32(Ds);
         if (G.tid == 0) {
             tc_fence_after();
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 8; ++k) {  // A = Q K^T
                 const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
                 mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, k > 0);
+            }
+#pragma unroll
+            for (int k = 0; k < DV / 16; ++k) {  // dA = dO V^T
+                const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
                 mma_bf16(tmem + 64, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
             }
             mma_commit(mb);
@@ -748,82 +791,102 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t qoff = uint32_t(quarter_row(Qs, G.tid, &r) - Qs);
             scale_quarter_to(Qs + qoff, Qt + qoff, d.scale * gs.win[r]);
             scale_quarter_to(Ks + qoff, Kt + qoff, gs.wout[r]);
-            scale_quarter(Vs + qoff, gs.wout[r]);
+#pragma unroll
+            for (int pr = 0; pr < NV / 2; ++pr) scale_quarter(Vs + 2 * pr * kTileBytes + qoff, gs.wout[r]);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (G.tid == 0) {
-            tc_fence_after();
-            const uint32_t pa = smem_u32(PA), pd = smem_u32(PD), ea = smem_u32(Eb);
-            const uint32_t qta = smem_u32(Qt), kta = smem_u32(Kt);
-            constexpr uint32_t id_mm = idesc_bf16(64, 128, 1, 1);
-            constexpr uint32_t id_kk = idesc_bf16(64, 128, 0, 0);
-            constexpr uint32_t id_km = idesc_bf16(64, 128, 0, 1);
-            constexpr uint32_t id_e = idesc_bf16(128, 128, 1, 1);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // dk' = PdA^T Q
-                mma_bf16(tmem + 128, sdesc(pd + k * 2048, kTileBytes, 1024),
-                         sdesc(qa + k * 2048, kTileBytes, 1024), id_mm, k > 0);
+        for (int hh = 0; hh < NH; ++hh) {
+            if (G.tid == 0) {
+                tc_fence_after();
+                const uint32_t pa = smem_u32(PA), pd = smem_u32(PD), ea = smem_u32(Eb);
+                const uint32_t qta = smem_u32(Qt), kta = smem_u32(Kt);
+                constexpr uint32_t id_mm = idesc_bf16(64, 128, 1, 1);
+                constexpr uint32_t id_kk = idesc_bf16(64, 128, 0, 0);
+                constexpr uint32_t id_km = idesc_bf16(64, 128, 0, 1);
+                constexpr uint32_t id_e = idesc_bf16(128, 128, 1, 1);
+                if (hh == 0) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k)  // dk' += V~ E^T
-                mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                         sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, 1);
+                    for (int k = 0; k < 4; ++k)  // dk' = PdA^T Q
+                        mma_bf16(tmem + 128, sdesc(pd + k * 2048, kTileBytes, 1024),
+                                 sdesc(qa + k * 2048, kTileBytes, 1024), id_mm, k > 0);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // dv = PA^T dO
-                mma_bf16(tmem + 256, sdesc(pa + k * 2048, kTileBytes, 1024),
-                         sdesc(da + k * 2048, kTileBytes, 1024), id_mm, k > 0);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)  // dv += K~ E
-                mma_bf16(tmem + 256, sdesc(kta + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                         sdesc(ea + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // dE = Q~^T dO
-                mma_bf16(tmem + 384, sdesc(qta + k * 2048, kTileBytes, 1024),
-                         sdesc(da + k * 2048, kTileBytes, 1024), id_e, k > 0);
-            mma_commit(mb);
-        }
-        mbar_wait(mb, mph);
-        mph ^= 1;
-        tc_fence_after();
-        {
-            const int64_t tok = ((int64_t)b * d.T + t0 + G.tau) * d.H + h;
-            const float cd = d.scale * diag_s[G.tau];
-            float bk = 0.f;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                float x[16], qv[16], kv[16];
-                const int col = 64 * G.grp + 32 * k;
-                const int c0 = col + 16 * G.hi;
-                tok16(tmem, G, 128 + col, x);
-                tile_row_get16(Qs, G.tau, c0, qv);
-                tile_row_get16(Ks, G.tau, c0, kv);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    bk = fmaf(kv[e], x[e], bk);
-                    x[e] = fmaf(cd, qv[e], x[e]);
+                    for (int k = 0; k < DV / 16; ++k)  // dk' += V~ E^T
+                        mma_bf16(tmem + 128,
+                                 sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                                 sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024),
+                                 id_kk, 1);
                 }
-                store_bf16x16(dk + tok * 128 + c0, x);
-                tok16(tmem, G, 256 + col, x);
-                store_bf16x16(dv + tok * 128 + c0, x);
+                const uint32_t dah = da + 2 * hh * kTileBytes;      // dO columns [128 hh, +128)
+                const uint32_t eah = ea + 2 * hh * 2 * kTileBytes;  // E columns [128 hh, +128)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // dv = PA^T dO
+                    mma_bf16(tmem + 256, sdesc(pa + k * 2048, kTileBytes, 1024),
+                             sdesc(dah + k * 2048, kTileBytes, 1024), id_mm, k > 0);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)  // dv += K~ E
+                    mma_bf16(tmem + 256, sdesc(kta + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                             sdesc(eah + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // dE = Q~^T dO
+                    mma_bf16(tmem + 384, sdesc(qta + k * 2048, kTileBytes, 1024),
+                             sdesc(dah + k * 2048, kTileBytes, 1024), id_e, k > 0);
+                mma_commit(mb);
             }
-            bk += __shfl_xor_sync(kFull, bk, 16);
-            if (!G.hi) bpart[G.grp][G.tau] = bk;
-            state_update(tmem, G, 384, gs.W, E, Eb);
+            mbar_wait(mb, mph);
+            mph ^= 1;
+            // single-buffered inputs: once the last products of the chunk are
+            // done and the Q/K rows have been read, refill for the next chunk
+            if (STAGES == 1 && hh == NH - 1 && NH > 1 && G.tid == 0 && it + 1 < nch) issue(it + 1, 0);
+            tc_fence_after();
+            {
+                const int64_t tok = ((int64_t)b * d.T + t0 + G.tau) * d.H + h;
+                if (hh == 0) {
+                    const float cd = d.scale * diag_s[G.tau];
+                    float bk = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        float x[16], qv[16], kv[16];
+                        const int col = 64 * G.grp + 32 * k;
+                        const int c0 = col + 16 * G.hi;
+                        tok16(tmem, G, 128 + col, x);
+                        tile_row_get16(Qs, G.tau, c0, qv);
+                        tile_row_get16(Ks, G.tau, c0, kv);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            bk = fmaf(kv[e], x[e], bk);
+                            x[e] = fmaf(cd, qv[e], x[e]);
+                        }
+                        store_bf16x16(dk + tok * 128 + c0, x);
+                    }
+                    bk += __shfl_xor_sync(kFull, bk, 16);
+                    if (!G.hi) bpart[G.grp][G.tau] = bk;
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    float x[16];
+                    const int col = 64 * G.grp + 32 * k;
+                    tok16(tmem, G, 256 + col, x);
+                    store_bf16x16(dv + tok * DV + 128 * hh + col + 16 * G.hi, x);
+                }
+                state_update_half(tmem, G, 384, hh, gs.W, E, Eb);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
         if (G.warp == 0) {
             // gate gradient of the chunk: reverse running sums of q.dq' - k.dk'
             // restarting where a sequence starts, plus the carry from later
             // chunks for the sequence open at the chunk's end.  Lane l holds
-            // tokens t0 = 63 - 2l and t1 = 62 - 2l; a segmented warp scan runs
-            // over the lanes in that (reverse) order.
+            // tokens 63 - 2l and 62 - 2l; a segmented warp scan runs over the
+            // lanes in that (reverse) order.
             const int tA = 63 - 2 * G.lane, tB = 62 - 2 * G.lane;
             const float cA = qd0 - (bpart[0][tA] + bpart[1][tA]);
             const float cB = qd1 - (bpart[0][tB] + bpart[1][tB]);
-            // head: token t + 1 starts a sequence, so t starts a new reverse run
+            // head: token t + 1 starts a sequence, so t begins a new reverse run
             const bool hA = tA < 63 && gs.lid[tA + 1] != gs.lid[tA];
             const bool hB = gs.lid[tB + 1] != gs.lid[tB];
             float v = hB ? cB : cA + cB;  // pair summary
@@ -853,7 +916,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             dg[((int64_t)b * d.T + t0 + tB) * d.H + h] = stB ? 0.f : sB;
             const float last = __shfl_sync(kFull, sB, 31);  // value at token 0
             carry = gs.first ? 0.f : last;
-            if (G.tid == 0 && it + 2 < nch) issue(it + 2, s);
+            if (STAGES == 2 && G.tid == 0 && it + 2 < nch) issue(it + 2, s);
+            if (STAGES == 1 && NH == 1 && G.tid == 0 && it + 1 < nch) issue(it + 1, 0);
         }
     }
     tc_fence_before();
@@ -915,8 +979,12 @@ bool set_smem(K kernel, size_t bytes) {
 
 constexpr size_t kOuterSmem = 96 * 1024 + 1024;
 constexpr size_t kFwdSmem = 11 * kTileBytes + 1024;   // Q K V P (7 tiles) + S (4 tiles)
-constexpr size_t kDqSmem = 13 * kTileBytes + 1024;    // Q K V dO P (9) + S (4)
-constexpr size_t kRevSmem = 26 * kTileBytes + 1024;   // 2 stages x 8 + Q~ K~ (4) + PA PdA (2) + E (4)
+// Q K (4 tiles) + V dO (2 NV) + P (1) + S (2 NV)
+constexpr size_t dq_smem(int dv) { return size_t(5 + 4 * (dv / 64)) * kTileBytes + 1024; }
+// stages x (4 + 2 NV) + Q~ K~ (4) + PA PdA (2) + E (2 NV): 26 tiles for Dv 128 and 256
+constexpr size_t rev_smem(int dv) {
+    return size_t((dv == 128 ? 2 : 1) * (4 + 2 * (dv / 64)) + 6 + 2 * (dv / 64)) * kTileBytes + 1024;
+}
 
 }  // namespace
 
@@ -945,9 +1013,8 @@ bool tc_supports(const Dims& d, rm_dtype dt) {
 }
 
 bool tc_supports_op(Op op, const Dims& d, rm_dtype dt) {
-    if (!tc_supports(d, dt)) return false;
-    if (op == Op::kBackwardPrepare || op == Op::kBackwardApply) return d.Dv == 128;
-    return true;
+    (void)op;
+    return tc_supports(d, dt);
 }
 
 rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
@@ -984,26 +1051,45 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
         }
         case Op::kBackwardPrepare: {
             if (!make_map(&mq, p.q, d, 128) || !make_map(&mk, p.k, d, 128) ||
-                !make_map(&mv, p.v, d, 128) || !make_map(&mdo, p.dO, d, 128))
+                !make_map(&mv, p.v, d, d.Dv) || !make_map(&mdo, p.dO, d, d.Dv))
                 return RM_ERR_CUDA;
-            auto fo = tc_outer_kernel<128, true>;
-            if (!set_smem(fo, kOuterSmem) || !set_smem(tc_dq_kernel, kDqSmem)) return RM_ERR_CUDA;
-            fo<<<grid, kThreads, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
-            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
-            tc_dq_kernel<<<grid, kThreads, kDqSmem, s>>>(d, mq, mk, mv, mdo, p.g, p.S_in,
-                                                    static_cast<__nv_bfloat16*>(p.out0), p.ws_f32);
+            auto* dqo = static_cast<__nv_bfloat16*>(p.out0);
+            if (d.Dv == 128) {
+                auto fo = tc_outer_kernel<128, true>;
+                auto fq = tc_dq_kernel<128>;
+                if (!set_smem(fo, kOuterSmem) || !set_smem(fq, dq_smem(128))) return RM_ERR_CUDA;
+                fo<<<grid, kThreads, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
+                if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+                fq<<<grid, kThreads, dq_smem(128), s>>>(d, mq, mk, mv, mdo, p.g, p.S_in, dqo, p.ws_f32);
+            } else {
+                auto fo = tc_outer_kernel<256, true>;
+                auto fq = tc_dq_kernel<256>;
+                if (!set_smem(fo, kOuterSmem) || !set_smem(fq, dq_smem(256))) return RM_ERR_CUDA;
+                fo<<<grid, kThreads, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
+                if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+                fq<<<grid, kThreads, dq_smem(256), s>>>(d, mq, mk, mv, mdo, p.g, p.S_in, dqo, p.ws_f32);
+            }
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(2);
             return RM_OK;
         }
         case Op::kBackwardApply: {
             if (!make_map(&mq, p.q, d, 128) || !make_map(&mk, p.k, d, 128) ||
-                !make_map(&mv, p.v, d, 128) || !make_map(&mdo, p.dO, d, 128))
+                !make_map(&mv, p.v, d, d.Dv) || !make_map(&mdo, p.dO, d, d.Dv))
                 return RM_ERR_CUDA;
-            if (!set_smem(tc_rev_kernel, kRevSmem)) return RM_ERR_CUDA;
-            tc_rev_kernel<<<grid, kThreads, kRevSmem, s>>>(
-                d, mq, mk, mv, mdo, p.g, p.S_in, p.dS_out, p.ws_f32,
-                static_cast<__nv_bfloat16*>(p.out0), static_cast<__nv_bfloat16*>(p.out1), p.dg);
+            auto* dko = static_cast<__nv_bfloat16*>(p.out0);
+            auto* dvo = static_cast<__nv_bfloat16*>(p.out1);
+            if (d.Dv == 128) {
+                auto fr = tc_rev_kernel<128>;
+                if (!set_smem(fr, rev_smem(128))) return RM_ERR_CUDA;
+                fr<<<grid, kThreads, rev_smem(128), s>>>(d, mq, mk, mv, mdo, p.g, p.S_in, p.dS_out,
+                                                          p.ws_f32, dko, dvo, p.dg);
+            } else {
+                auto fr = tc_rev_kernel<256>;
+                if (!set_smem(fr, rev_smem(256))) return RM_ERR_CUDA;
+                fr<<<grid, kThreads, rev_smem(256), s>>>(d, mq, mk, mv, mdo, p.g, p.S_in, p.dS_out,
+                                                          p.ws_f32, dko, dvo, p.dg);
+            }
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(1);
             return RM_OK;
