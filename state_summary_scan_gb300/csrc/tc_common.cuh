@@ -215,15 +215,18 @@ __device__ __forceinline__ void scale_row128(uint8_t* row, float w) {
 //   first    = the chunk's position 0 starts a sequence
 // so that, inside the chunk, tokens s <= t are in the same sequence iff
 // lid[s] == lid[t], and alpha_{s+1} ... alpha_t = exp(b[t] - b[s]) then.
-struct GateSmem {
+struct alignas(16) GateSmem {
     float b[kChunk];
     float win[kChunk];   // alpha_0 ... alpha_tau (decay from the chunk's incoming state)
     float wout[kChunk];  // alpha_{tau+1} ... alpha_63 (decay to the chunk's last state)
+    float ep[kChunk];    // exp(b[tau] - b[63])
+    float en[kChunk];    // exp(b[63] - b[tau])
     int lid[kChunk];
     float btot;          // b[63]
     float W;             // alpha_0 ... alpha_63
     int first;           // position 0 starts a sequence
     int any;             // some position of the chunk starts a sequence
+    int fast;            // every |b[tau] - b[63]| < 60: exp(b_t - b_s) = ep[t] en[s] in fp32
 };
 
 struct GateRegs {
@@ -272,13 +275,21 @@ __device__ __forceinline__ void gate_prep(const GateRegs& r, GateSmem* gs, int l
     gs->lid[2 * lane + 1] = l1;
     gs->win[2 * lane] = (!first && l0 == 0) ? expf(b0) : 0.f;
     gs->win[2 * lane + 1] = (!first && l1 == 0) ? expf(b1) : 0.f;
-    gs->wout[2 * lane] = (l0 == ltot) ? expf(btot - b0) : 0.f;
-    gs->wout[2 * lane + 1] = (l1 == ltot) ? expf(btot - b1) : 0.f;
+    const float en0 = expf(btot - b0), en1 = expf(btot - b1);
+    gs->en[2 * lane] = en0;
+    gs->en[2 * lane + 1] = en1;
+    gs->ep[2 * lane] = expf(b0 - btot);
+    gs->ep[2 * lane + 1] = expf(b1 - btot);
+    gs->wout[2 * lane] = (l0 == ltot) ? en0 : 0.f;
+    gs->wout[2 * lane + 1] = (l1 == ltot) ? en1 : 0.f;
+    const float dev = fmaxf(fabsf(btot - b0), fabsf(btot - b1));
+    const bool fast = __all_sync(0xffffffffu, dev < 60.f);
     if (lane == 0) {
         gs->btot = btot;
         gs->W = (!first && ltot == 0) ? expf(btot) : 0.f;
         gs->first = first;
         gs->any = (first || ltot > 0) ? 1 : 0;
+        gs->fast = fast ? 1 : 0;
     }
 }
 

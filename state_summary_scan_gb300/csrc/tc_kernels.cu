@@ -160,44 +160,67 @@ __device__ __forceinline__ void state_update_half(uint32_t tmem, const Geo& g, i
             pack8(S + 64 * hh + c * 8);
 }
 
-// Physical 16-byte chunks [4 h4, 4 h4 + 4) of row r of block blk of a [64][128]
-// tile, each thread of the CTA taking one such quarter row.
-__device__ __forceinline__ uint8_t* quarter_row(uint8_t* tile, int tid, int* r) {
-    *r = tid >> 2;
-    return tile + ((tid >> 1) & 1) * kTileBytes + (tid >> 2) * 128 + (tid & 1) * 64;
+// Row scaling of a [64][128] bf16 tile (2 blocks x 64 rows x 8 chunks of 16
+// bytes = 1024 chunks): the CTA's 256 threads take 4 chunks each, eight
+// consecutive threads covering the eight chunks of one 128-byte row so that a
+// warp's 16-byte accesses hit distinct banks.  Chunk k (k < 4) of a thread is
+// n = tid + 256 k: block n >> 9, row (n >> 3) & 63, chunk n & 7.
+__device__ __forceinline__ uint32_t scale_off(int tid, int k, int* r) {
+    const int n = tid + 256 * k;
+    *r = (n >> 3) & 63;
+    return uint32_t((n >> 9) * kTileBytes + ((n >> 3) & 63) * 128 + (n & 7) * 16);
 }
-__device__ __forceinline__ void scale_quarter(uint8_t* p, float w) {
+__device__ __forceinline__ void scale_chunk(const uint8_t* src, uint8_t* dst, float w) {
+    float x[8];
+    unpack8(*reinterpret_cast<const uint4*>(src), x);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint4* q = reinterpret_cast<uint4*>(p + c * 16);
-        float x[8];
-        unpack8(*q, x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] *= w;
-        *q = pack8(x);
-    }
+    for (int i = 0; i < 8; ++i) x[i] *= w;
+    *reinterpret_cast<uint4*>(dst) = pack8(x);
 }
-__device__ __forceinline__ void scale_quarter_to(const uint8_t* src, uint8_t* dst, float w) {
+// dst row r = w[r] * src row r for the [64][128] tile (dst may equal src)
+__device__ __forceinline__ void scale_tile(const uint8_t* src, uint8_t* dst, const float* w, float mul,
+                                           int tid) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        float x[8];
-        unpack8(*reinterpret_cast<const uint4*>(src + c * 16), x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] *= w;
-        *reinterpret_cast<uint4*>(dst + c * 16) = pack8(x);
+    for (int k = 0; k < 4; ++k) {
+        int r;
+        const uint32_t off = scale_off(tid, k, &r);
+        scale_chunk(src + off, dst + off, mul * w[r]);
     }
 }
 
 // Decay mask for this thread's 16 columns c0..c0+15 of row tau:
 // gam[e] = exp(b_tau - b_s) if s <= tau (s < tau when strict) in tau's sequence.
+// When the chunk's decays are moderate the exponential factors through the
+// chunk end, exp(b_tau - b_63) exp(b_63 - b_s), and costs one multiply.
 __device__ __forceinline__ void decay_row16(const GateSmem& gs, int tau, int c0, bool strict, float* gam) {
-    const float bt = gs.b[tau];
     const int lt = gs.lid[tau];
+    float bb[16], en[16];
+    int ll[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        const int s = c0 + e;
-        const bool keep = (strict ? s < tau : s <= tau) && gs.lid[s] == lt;
-        gam[e] = keep ? __expf(bt - gs.b[s]) : 0.f;
+    for (int e = 0; e < 16; e += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(&gs.b[c0 + e]);
+        const float4 y = *reinterpret_cast<const float4*>(&gs.en[c0 + e]);
+        const int4 z = *reinterpret_cast<const int4*>(&gs.lid[c0 + e]);
+        bb[e] = x.x; bb[e + 1] = x.y; bb[e + 2] = x.z; bb[e + 3] = x.w;
+        en[e] = y.x; en[e + 1] = y.y; en[e + 2] = y.z; en[e + 3] = y.w;
+        ll[e] = z.x; ll[e + 1] = z.y; ll[e + 2] = z.z; ll[e + 3] = z.w;
+    }
+    if (gs.fast) {
+        const float et = gs.ep[tau];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int s = c0 + e;
+            const bool keep = (strict ? s < tau : s <= tau) && ll[e] == lt;
+            gam[e] = keep ? et * en[e] : 0.f;
+        }
+    } else {
+        const float bt = gs.b[tau];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int s = c0 + e;
+            const bool keep = (strict ? s < tau : s <= tau) && ll[e] == lt;
+            gam[e] = keep ? __expf(bt - bb[e]) : 0.f;
+        }
     }
 }
 // Writes 16 bf16 values (columns c0..c0+15, c0 % 16 == 0) of row tau of a [64][64] tile.
@@ -282,14 +305,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(smem_u32(&full_bar[s]), (it / STAGES) & 1);
         __syncthreads();
         {
-            int r;
-            uint8_t* p = quarter_row(smem + s * SBYTES, G.tid, &r);
-            float w;
-            if (GAMMA)  // scale * alpha_a ... alpha_t: no start in [a, t]
-                w = (!seen && !gs.first && gs.lid[r] == 0) ? d.scale * expf(run + gs.b[r]) : 0.f;
-            else        // alpha_{t+1} ... alpha_end: no start in (t, end]
-                w = (!seen && gs.lid[r] == gs.lid[kChunk - 1]) ? expf(run + gs.btot - gs.b[r]) : 0.f;
-            scale_quarter(p, w);
+            // row weight w_t, applied to x_t in place
+            uint8_t* xt = smem + s * SBYTES;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                int r;
+                const uint32_t off = scale_off(G.tid, k, &r);
+                float w;
+                if (GAMMA)  // scale * alpha_a ... alpha_t: no start in [a, t]
+                    w = (!seen && !gs.first && gs.lid[r] == 0) ? d.scale * expf(run + gs.b[r]) : 0.f;
+                else        // alpha_{t+1} ... alpha_end: no start in (t, end]
+                    w = (!seen && gs.lid[r] == gs.lid[kChunk - 1]) ? expf(run + gs.btot - gs.b[r]) : 0.f;
+                scale_chunk(xt + off, xt + off, w);
+            }
         }
         fence_async_smem();
         tc_fence_before();
@@ -428,10 +456,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int e = 0; e < 16; ++e) x[e] *= d.scale * gam[e];
             store_row16(Ps, G.tau, c0, x);
-            int r;
-            uint8_t* pq = quarter_row(Qs, G.tid, &r);
-            scale_quarter(pq, d.scale * gs.win[r]);
-            scale_quarter(quarter_row(Ks, G.tid, &r), gs.wout[r]);
+            scale_tile(Qs, Qs, gs.win, d.scale, G.tid);
+            scale_tile(Ks, Ks, gs.wout, 1.f, G.tid);
         }
         fence_async_smem();
         tc_fence_before();
@@ -573,9 +599,10 @@ __global__ void __launch_bounds__(kThreads, DV == 128 ? 2 : 1)
             store_row16(Ps, G.tau, c0, x);
 #pragma unroll
             for (int pr = 0; pr < NV / 2; ++pr) {
-                int r;
-                scale_quarter(quarter_row(Ds + 2 * pr * kTileBytes, G.tid, &r), d.scale * gs.win[r]);
-                scale_quarter(quarter_row(Vs + 2 * pr * kTileBytes, G.tid, &r), gs.wout[r]);
+                uint8_t* dp = Ds + 2 * pr * kTileBytes;
+                uint8_t* vp = Vs + 2 * pr * kTileBytes;
+                scale_tile(dp, dp, gs.win, d.scale, G.tid);
+                scale_tile(vp, vp, gs.wout, 1.f, G.tid);
             }
         }
         fence_async_smem();
@@ -787,12 +814,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_row16(PA, G.tau, c0, xa);
             store_row16(PD, G.tau, c0, xd);
             // Q~ = scale win Q and K~ = wout K into their own tiles; V~ = wout V in place
-            int r;
-            const uint32_t qoff = uint32_t(quarter_row(Qs, G.tid, &r) - Qs);
-            scale_quarter_to(Qs + qoff, Qt + qoff, d.scale * gs.win[r]);
-            scale_quarter_to(Ks + qoff, Kt + qoff, gs.wout[r]);
+            scale_tile(Qs, Qt, gs.win, d.scale, G.tid);
+            scale_tile(Ks, Kt, gs.wout, 1.f, G.tid);
 #pragma unroll
-            for (int pr = 0; pr < NV / 2; ++pr) scale_quarter(Vs + 2 * pr * kTileBytes + qoff, gs.wout[r]);
+            for (int pr = 0; pr < NV / 2; ++pr) {
+                uint8_t* vp = Vs + 2 * pr * kTileBytes;
+                scale_tile(vp, vp, gs.wout, 1.f, G.tid);
+            }
         }
         fence_async_smem();
         tc_fence_before();
