@@ -369,10 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(kThreads, 2)
     tc_fwd_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                         const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                        const float* __restrict__ g, const float* __restrict__ S_in,
-                        __nv_bfloat16* __restrict__ o) {
+                        const __grid_constant__ CUtensorMap mo, const float* __restrict__ g,
+                        const float* __restrict__ S_in) {
     constexpr uint32_t OFF_Q = 0, OFF_K = 2 * kTileBytes, OFF_V = 4 * kTileBytes;
     constexpr uint32_t OFF_P = 6 * kTileBytes, OFF_S = 7 * kTileBytes;  // S tile: 32 KB
+    constexpr uint32_t OFF_O = 11 * kTileBytes;                          // o staging: 16 KB
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint8_t* Qs = smem + OFF_Q;
@@ -380,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t* Vs = smem + OFF_V;
     uint8_t* Ps = smem + OFF_P;
     uint8_t* Sb = smem + OFF_S;
+    uint8_t* Os = smem + OFF_O;
     __shared__ GateSmem gs;
     __shared__ __align__(8) uint64_t full_bar;
     __shared__ __align__(8) uint64_t mma_bar;
@@ -436,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks), va = smem_u32(Vs);
         const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb);
         if (G.tid == 0) {
+            bulk_wait_read();  // the previous chunk's o store has left the staging tile
             tc_fence_after();
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
 #pragma unroll
@@ -485,20 +488,26 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (G.tid == 0 && c + 1 < nch) issue(c + 1);
         tc_fence_after();
         {
-            __nv_bfloat16* orow = o + (((int64_t)b * d.T + t0 + G.tau) * d.H + h) * d.Dv + vb * 128;
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 float x[16];
                 const int col = 64 * G.grp + 32 * k;
                 tok16(tmem, G, col, x);
-                store_bf16x16(orow + col + 16 * G.hi, x);
+                store_row16(Os, G.tau, col + 16 * G.hi, x);
             }
             state_update(tmem, G, 128, gs.W, S, Sb);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        if (G.tid == 0) {  // o rows of the chunk: one bulk tensor store per 64 columns
+            const int row = b * d.T + t0;
+            tma_store_3d(&mo, smem_u32(Os), vb * 128, h, row);
+            tma_store_3d(&mo, smem_u32(Os + kTileBytes), vb * 128 + 64, h, row);
+            bulk_commit();
+        }
     }
+    if (G.tid == 0) bulk_wait_all();
     if (G.warp == 0) tmem_dealloc(tmem, 256);
 }
 
@@ -509,8 +518,8 @@ template <int DV>
 __global__ void __launch_bounds__(kThreads, DV == 128 ? 2 : 1)
     tc_dq_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                  const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                 const __grid_constant__ CUtensorMap mdo, const float* __restrict__ g,
-                 const float* __restrict__ S_in, __nv_bfloat16* __restrict__ dq,
+                 const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdq,
+                 const float* __restrict__ g, const float* __restrict__ S_in,
                  float* __restrict__ qdq) {
     constexpr int NV = DV / 64;  // 64-column blocks of v and dO
     constexpr uint32_t OFF_Q = 0, OFF_K = 2 * kTileBytes, OFF_V = 4 * kTileBytes;
@@ -577,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, DV == 128 ? 2 : 1)
             tc_fence_after();
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
 #pragma unroll
-            for (int s = 0; s < DV / 16; ++s) {  // dA = dO V^T
+            for (int s = 0; s < DV / 16; ++s) {  // dA = dO V^T (dO~ tile doubles as dq staging)
                 const uint32_t off = (s >> 2) * kTileBytes + (s & 3) * 32;
                 mma_bf16(tmem, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, s > 0);
             }
@@ -631,7 +640,6 @@ __global__ void __launch_bounds__(kThreads, DV == 128 ? 2 : 1)
         mph ^= 1;
         tc_fence_after();
         {
-            __nv_bfloat16* drow = dq + (((int64_t)b * d.T + t0 + G.tau) * d.H + h) * 128;
             const float cd = d.scale * diag_s[G.tau];
             float a = 0.f;
 #pragma unroll
@@ -647,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, DV == 128 ? 2 : 1)
                     a = fmaf(qv[e], x[e], a);
                     x[e] = fmaf(cd, kv[e], x[e]);
                 }
-                store_bf16x16(drow + c0, x);
+                store_row16(Ds, G.tau, c0, x);  // dO~ is dead: stage dq there
             }
             a += __shfl_xor_sync(kFull, a, 16);
             if (!G.hi) apart[G.grp][G.tau] = a;
@@ -660,8 +668,18 @@ __global__ void __launch_bounds__(kThreads, DV == 128 ? 2 : 1)
         __syncthreads();
         if (G.tid < kChunk)
             qdq[((int64_t)b * d.T + t0 + G.tid) * d.H + h] = apart[0][G.tid] + apart[1][G.tid];
-        if (G.tid == 0 && c + 1 < nch) issue(c + 1);
+        if (G.tid == 0) {
+            const int row = b * d.T + t0;
+            tma_store_3d(&mdq, smem_u32(Ds), 0, h, row);
+            tma_store_3d(&mdq, smem_u32(Ds + kTileBytes), 64, h, row);
+            bulk_commit();
+            if (c + 1 < nch) {
+                bulk_wait_read();  // the staging tile is refilled by the next load
+                issue(c + 1);
+            }
+        }
     }
+    if (G.tid == 0) bulk_wait_all();
     if (G.warp == 0) tmem_dealloc(tmem, TCOLS);
 }
 
@@ -674,10 +692,15 @@ template <int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_rev_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                  const __grid_constant__ CUtensorMap mdo, const float* __restrict__ g,
+                  const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdk,
+                  const __grid_constant__ CUtensorMap mdv, const float* __restrict__ g,
                   const float* __restrict__ S_in, const float* __restrict__ dS_out,
                   const float* __restrict__ qdq, __nv_bfloat16* __restrict__ dk,
                   __nv_bfloat16* __restrict__ dv, float* __restrict__ dg) {
+    // Dv = 128 stages dk and dv in the Q~ and K~ tiles (dead once the chunk's
+    // products are done) and writes them with bulk tensor stores; Dv = 256
+    // still needs those tiles for its second half and stores rows directly.
+    constexpr bool kStage = DV == 128;
     constexpr int NV = DV / 64;
     constexpr int NH = DV / 128;
     constexpr int STAGES = DV == 128 ? 2 : 1;
@@ -781,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks), va = smem_u32(Vs), da = smem_u32(Ds);
         if (G.tid == 0) {
+            if (kStage) bulk_wait_read();  // last chunk's dk/dv have left the Q~/K~ tiles
             tc_fence_after();
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
 #pragma unroll
@@ -887,7 +911,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             bk = fmaf(kv[e], x[e], bk);
                             x[e] = fmaf(cd, qv[e], x[e]);
                         }
-                        store_bf16x16(dk + tok * 128 + c0, x);
+                        if (kStage)
+                            store_row16(Qt, G.tau, c0, x);
+                        else
+                            store_bf16x16(dk + tok * 128 + c0, x);
                     }
                     bk += __shfl_xor_sync(kFull, bk, 16);
                     if (!G.hi) bpart[G.grp][G.tau] = bk;
@@ -897,7 +924,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float x[16];
                     const int col = 64 * G.grp + 32 * k;
                     tok16(tmem, G, 256 + col, x);
-                    store_bf16x16(dv + tok * DV + 128 * hh + col + 16 * G.hi, x);
+                    if (kStage)
+                        store_row16(Kt, G.tau, col + 16 * G.hi, x);
+                    else
+                        store_bf16x16(dv + tok * DV + 128 * hh + col + 16 * G.hi, x);
                 }
                 state_update_half(tmem, G, 384, hh, gs.W, E, Eb);
             }
@@ -944,10 +974,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             dg[((int64_t)b * d.T + t0 + tB) * d.H + h] = stB ? 0.f : sB;
             const float last = __shfl_sync(kFull, sB, 31);  // value at token 0
             carry = gs.first ? 0.f : last;
+            if (kStage && G.tid == 0) {
+                const int row = b * d.T + t0;
+                tma_store_3d(&mdk, smem_u32(Qt), 0, h, row);
+                tma_store_3d(&mdk, smem_u32(Qt + kTileBytes), 64, h, row);
+                tma_store_3d(&mdv, smem_u32(Kt), 0, h, row);
+                tma_store_3d(&mdv, smem_u32(Kt + kTileBytes), 64, h, row);
+                bulk_commit();
+            }
             if (STAGES == 2 && G.tid == 0 && it + 2 < nch) issue(it + 2, s);
             if (STAGES == 1 && NH == 1 && G.tid == 0 && it + 1 < nch) issue(it + 1, 0);
         }
     }
+    if (G.tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (G.warp == 0) tmem_dealloc(tmem, 512);
@@ -1006,7 +1045,7 @@ bool set_smem(K kernel, size_t bytes) {
 }
 
 constexpr size_t kOuterSmem = 96 * 1024 + 1024;
-constexpr size_t kFwdSmem = 11 * kTileBytes + 1024;   // Q K V P (7 tiles) + S (4 tiles)
+constexpr size_t kFwdSmem = 13 * kTileBytes + 1024;   // Q K V P (7 tiles) + S (4) + o staging (2)
 // Q K (4 tiles) + V dO (2 NV) + P (1) + S (2 NV)
 constexpr size_t dq_smem(int dv) { return size_t(5 + 4 * (dv / 64)) * kTileBytes + 1024; }
 // stages x (4 + 2 NV) + Q~ K~ (4) + PA PdA (2) + E (2 NV): 26 tiles for Dv 128 and 256
@@ -1067,12 +1106,13 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             return RM_OK;
         }
         case Op::kForwardApply: {
+            CUtensorMap mo;
             if (!make_map(&mq, p.q, d, 128) || !make_map(&mk, p.k, d, 128) ||
-                !make_map(&mv, p.v, d, d.Dv))
+                !make_map(&mv, p.v, d, d.Dv) || !make_map(&mo, p.out0, d, d.Dv))
                 return RM_ERR_CUDA;
             if (!set_smem(tc_fwd_apply_kernel, kFwdSmem)) return RM_ERR_CUDA;
             tc_fwd_apply_kernel<<<dim3(d.nseg, d.B * d.H, d.Dv / 128), kThreads, kFwdSmem, s>>>(
-                d, mq, mk, mv, p.g, p.S_in, static_cast<__nv_bfloat16*>(p.out0));
+                d, mq, mk, mv, mo, p.g, p.S_in);
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(1);
             return RM_OK;
@@ -1081,21 +1121,22 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             if (!make_map(&mq, p.q, d, 128) || !make_map(&mk, p.k, d, 128) ||
                 !make_map(&mv, p.v, d, d.Dv) || !make_map(&mdo, p.dO, d, d.Dv))
                 return RM_ERR_CUDA;
-            auto* dqo = static_cast<__nv_bfloat16*>(p.out0);
+            CUtensorMap mdq;
+            if (!make_map(&mdq, p.out0, d, 128)) return RM_ERR_CUDA;
             if (d.Dv == 128) {
                 auto fo = tc_outer_kernel<128, true>;
                 auto fq = tc_dq_kernel<128>;
                 if (!set_smem(fo, kOuterSmem) || !set_smem(fq, dq_smem(128))) return RM_ERR_CUDA;
                 fo<<<grid, kThreads, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
                 if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
-                fq<<<grid, kThreads, dq_smem(128), s>>>(d, mq, mk, mv, mdo, p.g, p.S_in, dqo, p.ws_f32);
+                fq<<<grid, kThreads, dq_smem(128), s>>>(d, mq, mk, mv, mdo, mdq, p.g, p.S_in, p.ws_f32);
             } else {
                 auto fo = tc_outer_kernel<256, true>;
                 auto fq = tc_dq_kernel<256>;
                 if (!set_smem(fo, kOuterSmem) || !set_smem(fq, dq_smem(256))) return RM_ERR_CUDA;
                 fo<<<grid, kThreads, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
                 if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
-                fq<<<grid, kThreads, dq_smem(256), s>>>(d, mq, mk, mv, mdo, p.g, p.S_in, dqo, p.ws_f32);
+                fq<<<grid, kThreads, dq_smem(256), s>>>(d, mq, mk, mv, mdo, mdq, p.g, p.S_in, p.ws_f32);
             }
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(2);
@@ -1107,15 +1148,17 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 return RM_ERR_CUDA;
             auto* dko = static_cast<__nv_bfloat16*>(p.out0);
             auto* dvo = static_cast<__nv_bfloat16*>(p.out1);
+            CUtensorMap mdk, mdv;
+            if (!make_map(&mdk, p.out0, d, 128) || !make_map(&mdv, p.out1, d, d.Dv)) return RM_ERR_CUDA;
             if (d.Dv == 128) {
                 auto fr = tc_rev_kernel<128>;
                 if (!set_smem(fr, rev_smem(128))) return RM_ERR_CUDA;
-                fr<<<grid, kThreads, rev_smem(128), s>>>(d, mq, mk, mv, mdo, p.g, p.S_in, p.dS_out,
+                fr<<<grid, kThreads, rev_smem(128), s>>>(d, mq, mk, mv, mdo, mdk, mdv, p.g, p.S_in, p.dS_out,
                                                           p.ws_f32, dko, dvo, p.dg);
             } else {
                 auto fr = tc_rev_kernel<256>;
                 if (!set_smem(fr, rev_smem(256))) return RM_ERR_CUDA;
-                fr<<<grid, kThreads, rev_smem(256), s>>>(d, mq, mk, mv, mdo, p.g, p.S_in, p.dS_out,
+                fr<<<grid, kThreads, rev_smem(256), s>>>(d, mq, mk, mv, mdo, mdk, mdv, p.g, p.S_in, p.dS_out,
                                                           p.ws_f32, dko, dvo, p.dg);
             }
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
