@@ -240,6 +240,35 @@ rm_status rm_cp_backward_apply(const rm_cp_problem* p, const void* q, const void
 rm_status rm_cp_device_status(int32_t* dev_scratch, int32_t clear, rm_stream_t stream);
 rm_status rm_cp_selftest_wait_timeout(uint32_t limit_us, rm_stream_t stream);
 
+/*
+ * The whole backward in one call, with no device allocation and no
+ * workspace argument: rm_cp_backward_prepare, rm_cp_compose_suffix and
+ * rm_cp_backward_apply, in that order on `stream`, with the per-token
+ * scratch they pass between each other taken from a fixed array that the
+ * library itself holds in device memory.  The paper has no counterpart to
+ * this call; it exists for callers that cannot allocate device memory, such
+ * as a custom operator reached through a plugin interface with a fixed
+ * signature and no workspace, or a deployment whose device memory is
+ * planned up front and must not grow after start-up.
+ *   Inputs, outputs and their layouts are those of the three calls it
+ *   replaces: q, k, v, dO (dtype), g fp32, S_in and M from the forward;
+ *   gamma and dS_out [nseg,B,H,Dk,Dv] fp32 are written as by those calls;
+ *   dq, dk, dv (dtype), dg fp32 out.
+ *   Limit: B * T * H <= 4,194,304 (16 MiB of fp32 scratch, held on every
+ *   device that loads the library until the process exits); larger
+ *   problems get RM_ERR_SHAPE and must use the workspace form.
+ *   The first call on a device looks the array's device address up (once
+ *   per device, with that device current); make that first call before any
+ *   stream capture.  Every call shares the one array: calls whose work
+ *   overlaps on the GPU (other streams, other host threads) race on it and
+ *   must be serialised by the caller.  Nothing in the array needs clearing:
+ *   each call writes every entry it later reads.
+ */
+rm_status rm_cp_backward_noalloc(const rm_cp_problem* p, const void* q, const void* k,
+                                 const void* v, const float* g, const float* S_in,
+                                 const float* M, const void* dO, float* gamma, float* dS_out,
+                                 void* dq, void* dk, void* dv, float* dg, rm_stream_t stream);
+
 /* Name of a status code (static string). */
 const char* rm_cp_status_string(rm_status s);
 

@@ -27,7 +27,7 @@ EXPORTS = (
     "rm_cp_forward_prepare", "rm_cp_compose_prefix", "rm_cp_forward_apply",
     "rm_cp_backward_prepare", "rm_cp_compose_suffix", "rm_cp_backward_apply",
     "rm_cp_status_string", "rm_cp_last_error", "rm_cp_path", "rm_cp_launch_count",
-    "rm_cp_device_status", "rm_cp_selftest_wait_timeout",
+    "rm_cp_device_status", "rm_cp_selftest_wait_timeout", "rm_cp_backward_noalloc",
 )
 
 
@@ -69,6 +69,7 @@ _SIGS = {
     "rm_cp_launch_count": (ctypes.c_uint64, []),
     "rm_cp_device_status": (_S, [_P, ctypes.c_int32, _P]),
     "rm_cp_selftest_wait_timeout": (_S, [ctypes.c_uint32, _P]),
+    "rm_cp_backward_noalloc": (_S, [_PP] + [_P] * 14),
 }
 
 _lock = threading.Lock()
@@ -216,3 +217,10 @@ def rm_cp_backward_apply(p, q, k, v, g, dO, S_in, dS_out, dk, dv, dg, ws, stream
     _check(load().rm_cp_backward_apply(p.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(dO),
                                        _ptr(S_in), _ptr(dS_out), _ptr(dk), _ptr(dv), _ptr(dg),
                                        _ptr(ws), _stream(stream)))
+
+
+def rm_cp_backward_noalloc(p, q, k, v, g, S_in, M, dO, gamma, dS_out, dq, dk, dv, dg, stream=None):
+    """The whole backward with the library's own fixed scratch (no workspace)."""
+    _check(load().rm_cp_backward_noalloc(p.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S_in),
+                                         _ptr(M), _ptr(dO), _ptr(gamma), _ptr(dS_out), _ptr(dq),
+                                         _ptr(dk), _ptr(dv), _ptr(dg), _stream(stream)))

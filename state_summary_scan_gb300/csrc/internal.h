@@ -33,6 +33,13 @@ void note_launch(int n);
 bool generic_supports(const Dims& d);
 rm_status launch_generic(Op op, const Dims& d, rm_dtype dt, const Ptrs& p, cudaStream_t s);
 
+// host-side checks and launches of rm_cp_host.cu, for other entry points
+rm_status api_check_problem(const rm_cp_problem* p, Dims* d);
+rm_status api_need(const void* ptr, const char* name);
+rm_status api_fail(rm_status s, const char* msg);
+rm_status api_launch(Op op, const rm_cp_problem* p, const Dims& d, const Ptrs& ptrs,
+                     rm_stream_t stream);
+
 // summary scans (compose_kernels.cu)
 rm_status launch_compose_prefix(const Dims& d, const float* M, const float* dS, float* S_in,
                                 cudaStream_t s);

@@ -108,6 +108,17 @@ rm_status launch(rmcp::Op op, const rm_cp_problem* p, const rmcp::Dims& d, const
 
 }  // namespace
 
+namespace rmcp {
+// host-side checks and launches shared with noalloc.cu
+rm_status api_check_problem(const rm_cp_problem* p, Dims* d) { return check_problem(p, d); }
+rm_status api_need(const void* ptr, const char* name) { return need(ptr, name); }
+rm_status api_fail(rm_status s, const char* msg) { return fail(s, "%s", msg); }
+rm_status api_launch(Op op, const rm_cp_problem* p, const Dims& d, const Ptrs& ptrs,
+                     rm_stream_t stream) {
+    return launch(op, p, d, ptrs, stream);
+}
+}  // namespace rmcp
+
 extern "C" {
 
 const char* rm_cp_status_string(rm_status s) {

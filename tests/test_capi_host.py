@@ -92,6 +92,11 @@ def test_compute_calls_reject_null_and_misaligned_pointers_before_launch():
     assert lib.rm_cp_selftest_wait_timeout(0, None) == 1
     assert lib.rm_cp_selftest_wait_timeout(2000000, None) == 1
     assert lib.rm_cp_device_status(None, 1, None) == 1
+    # the allocation-free backward rejects problems beyond its fixed scratch
+    big = spec(B=1, T=2 ** 21, H=4, num_segments=2 ** 10)   # 8M token-heads > 4M
+    args = [ok] * 13
+    rc = lib.rm_cp_backward_noalloc(big.ref, *args, None)
+    assert rc == 2 and b"fixed scratch" in lib.rm_cp_last_error()
 
 
 def test_metadata_builder_matches_golden():
