@@ -992,6 +992,306 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (G.warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// Gate gradient of one chunk (warp 0): reverse running sums of q.dq' - k.dk'
+// that restart where a sequence starts, plus the carry from later chunks for
+// the sequence open at the chunk's end.  Lane l holds tokens 63 - 2l and
+// 62 - 2l; a segmented warp scan runs over the lanes in that (reverse) order.
+// bp[grp][t] are the two column groups' partials of k.dk'; qd0/qd1 are q.dq'
+// of the lane's tokens; dgc points at dg of the chunk's token 0 (stride H).
+// Returns the carry into the previous chunk.
+__device__ __forceinline__ float dg_scan(const GateSmem& gs, const float (*bp)[kChunk], float qd0,
+                                         float qd1, float carry, int lane, float* dgc, int H) {
+    const int tA = 63 - 2 * lane, tB = 62 - 2 * lane;
+    const float cA = qd0 - (bp[0][tA] + bp[1][tA]);
+    const float cB = qd1 - (bp[0][tB] + bp[1][tB]);
+    const bool hA = tA < 63 && gs.lid[tA + 1] != gs.lid[tA];  // t + 1 starts a sequence
+    const bool hB = gs.lid[tB + 1] != gs.lid[tB];
+    float v = hB ? cB : cA + cB;  // pair summary
+    bool f = hA || hB;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float vp = __shfl_up_sync(kFull, v, o);
+        const bool fp = __shfl_up_sync(kFull, f, o);
+        if (lane >= o) {
+            if (!f) v += vp;
+            f = f || fp;
+        }
+    }
+    float vx = __shfl_up_sync(kFull, v, 1);
+    bool fx = __shfl_up_sync(kFull, f, 1);
+    if (lane == 0) {
+        vx = 0.f;
+        fx = false;
+    }
+    const float X = fx ? vx : carry + vx;
+    const float sA = cA + (hA ? 0.f : X);
+    const float sB = cB + (hB ? 0.f : sA);
+    const bool stA = gs.lid[tA] != gs.lid[tA - 1];  // tA >= 1
+    const bool stB = tB == 0 ? gs.first != 0 : gs.lid[tB] != gs.lid[tB - 1];
+    dgc[int64_t(tA) * H] = stA ? 0.f : sA;
+    dgc[int64_t(tB) * H] = stB ? 0.f : sB;
+    const float last = __shfl_sync(kFull, sB, 31);  // value at token 0
+    return gs.first ? 0.f : last;
+}
+
+// ===========================================================================
+// reverse sweep for Dv = 128, warp-specialised and software-pipelined.
+// Warps 0-7 form the epilogues (score masks, tile scaling, dk/dv rows, the
+// adjoint update); warp 8 issues every TMA copy and MMA and the bulk stores;
+// warp 9 prepares the gate tables and runs each chunk's gate-gradient scan.
+// Per chunk the CTA meets twice: S1 (scaled operands ready -> output
+// products) and S2 (outputs staged -> stores, refill, scan).  The next
+// chunk's score products are issued right behind this chunk's output
+// products, dk and dv are staged in the chunk's own (dead) V~ and dO tiles.
+// ===========================================================================
+constexpr int kRevThreads = kThreads + 64;
+
+__global__ void __launch_bounds__(kRevThreads, 1)
+    tc_rev128_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                     const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                     const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdk,
+                     const __grid_constant__ CUtensorMap mdv, const float* __restrict__ g,
+                     const float* __restrict__ S_in, const float* __restrict__ dS_out,
+                     const float* __restrict__ qdq, float* __restrict__ dg) {
+    constexpr int DV = 128;
+    constexpr uint32_t STAGE = 8 * kTileBytes;  // Q | K | V | dO
+    constexpr uint32_t OFF_QT = 2 * STAGE, OFF_KT = OFF_QT + 2 * kTileBytes;
+    constexpr uint32_t OFF_PA = OFF_KT + 2 * kTileBytes, OFF_PD = OFF_PA + kTileBytes;
+    constexpr uint32_t OFF_E = OFF_PD + kTileBytes;  // E tile [128][128]
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint8_t* Qt = smem + OFF_QT;
+    uint8_t* Kt = smem + OFF_KT;
+    uint8_t* PA = smem + OFF_PA;
+    uint8_t* PD = smem + OFF_PD;
+    uint8_t* Eb = smem + OFF_E;
+    __shared__ GateSmem gsb[2];  // gate tables of the current and the next chunk
+    __shared__ __align__(8) uint64_t full_bar[2];
+    // one barrier per commit stream: the score products and the output
+    // products each commit once per chunk, and each is waited on before the
+    // stream's next commit can be issued, so no waiter can miss a phase
+    __shared__ __align__(8) uint64_t score_bar;
+    __shared__ __align__(8) uint64_t out_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ float diag_s[kChunk];
+    __shared__ float bpart[2][2][kChunk];  // [chunk parity][column group][token]
+    __shared__ float red[8];
+
+    const Geo G = geo();
+    const bool epi = G.warp < 8;
+    const bool ctl = G.warp == 8;
+    const bool scn = G.warp == 9;
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+    const uint32_t sbar = smem_u32(&score_bar), obar = smem_u32(&out_bar);
+
+    if (G.tid == 0) {
+        mbar_init(smem_u32(&full_bar[0]), 1);
+        mbar_init(smem_u32(&full_bar[1]), 1);
+        mbar_init(sbar, 1);
+        mbar_init(obar, 1);
+        mbar_fence_init();
+    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
+    auto issue = [&](int it, int s) {
+        const int row = b * d.T + a0 + (nch - 1 - it) * kChunk;
+        const uint32_t bar = smem_u32(&full_bar[s]);
+        uint8_t* st = smem + s * STAGE;
+        mbar_expect_tx(bar, STAGE);
+        load_tile(st, &mq, 0, 128, h, row, bar);
+        load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
+        load_tile(st + 4 * kTileBytes, &mv, 0, DV, h, row, bar);
+        load_tile(st + 6 * kTileBytes, &mdo, 0, DV, h, row, bar);
+    };
+    // E (adjoint arriving at the last state of the current chunk) starts as
+    // dS_out; ext = <S_out, dS_out> with S_out read as S_in[seg+1]
+    float E[DV / 2];
+    GateRegs gr;
+    if (epi) {
+        load_state_rows<DV>(dS_out + sum_off(d, seg, b, h), G, E, Eb);
+        float ext = 0.f;
+        if (seg + 1 < d.nseg) {
+            const float* so = S_in + sum_off(d, seg + 1, b, h) + int64_t(G.srow) * DV + 64 * G.grp;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+                const float4 y = *reinterpret_cast<const float4*>(so + j);
+                ext = fmaf(E[j], y.x, ext);
+                ext = fmaf(E[j + 1], y.y, ext);
+                ext = fmaf(E[j + 2], y.z, ext);
+                ext = fmaf(E[j + 3], y.w, ext);
+            }
+        }
+        ext = warp_sum(ext);
+        if (G.lane == 0) red[G.warp] = ext;
+    } else if (scn) {
+        gr = gate_load(d, g, b, h, a0 + (nch - 1) * kChunk, G.lane);
+        gate_prep(gr, &gsb[0], G.lane);
+        if (nch > 1) gr = gate_load(d, g, b, h, a0 + (nch - 2) * kChunk, G.lane);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    float carry = 0.f;  // gate-gradient sum carried from later chunks (warp 9)
+    if (scn) {
+#pragma unroll
+        for (int w = 0; w < 8; ++w) carry += red[w];
+    }
+    // score products A = Q K^T and dA = dO V^T of the chunk in stage s
+    auto issue_scores = [&](int s) {
+        const uint32_t qa = smem_u32(smem + s * STAGE), ka = qa + 2 * kTileBytes;
+        const uint32_t va = qa + 4 * kTileBytes, da = qa + 6 * kTileBytes;
+        constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
+            mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, k > 0);
+            mma_bf16(tmem + 64, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+        }
+        mma_commit(sbar);
+    };
+    if (ctl && G.lane == 0) {
+        issue(0, 0);
+        if (nch > 1) issue(1, 1);
+        mbar_wait(smem_u32(&full_bar[0]), 0);
+        tc_fence_after();
+        issue_scores(0);
+    }
+    uint32_t sph = 0, oph = 0;
+    for (int it = 0; it < nch; ++it) {
+        const int c = nch - 1 - it;
+        const int t0 = a0 + c * kChunk;
+        const int s = it & 1;
+        const GateSmem& gs = gsb[it & 1];
+        uint8_t* Qs = smem + s * STAGE;
+        uint8_t* Ks = Qs + 2 * kTileBytes;
+        uint8_t* Vs = Qs + 4 * kTileBytes;
+        uint8_t* Ds = Qs + 6 * kTileBytes;
+        float qd0 = 0.f, qd1 = 0.f;
+        if (scn) {  // q.dq' of this lane's two scan tokens
+            qd0 = __ldg(qdq + ((int64_t)b * d.T + t0 + 63 - 2 * G.lane) * d.H + h);
+            qd1 = __ldg(qdq + ((int64_t)b * d.T + t0 + 62 - 2 * G.lane) * d.H + h);
+        }
+        if (epi) {
+            mbar_wait(sbar, sph);  // this chunk's score products
+            sph ^= 1;
+            mbar_wait(smem_u32(&full_bar[s]), (it >> 1) & 1);  // its tiles, for the scaling
+            tc_fence_after();
+            float xa[16], xd[16], gam[16];
+            tok16(tmem, G, 32 * G.grp, xa);
+            tok16(tmem, G, 64 + 32 * G.grp, xd);
+            const int c0 = 32 * G.grp + 16 * G.hi;
+            decay_row16(gs, G.tau, c0, false, gam);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int sidx = c0 + e;
+                if (sidx == G.tau) diag_s[G.tau] = xd[e];  // dO_t . v_t
+                xa[e] *= d.scale * gam[e];
+                xd[e] = sidx < G.tau ? xd[e] * d.scale * gam[e] : 0.f;
+            }
+            store_row16(PA, G.tau, c0, xa);
+            store_row16(PD, G.tau, c0, xd);
+            scale_tile(Qs, Qt, gs.win, d.scale, G.tid);
+            scale_tile(Ks, Kt, gs.wout, 1.f, G.tid);
+            scale_tile(Vs, Vs, gs.wout, 1.f, G.tid);
+            fence_async_smem();
+            tc_fence_before();
+        }
+        __syncthreads();  // S1
+        if (ctl && G.lane == 0) {
+            tc_fence_after();
+            const uint32_t qa = smem_u32(Qs), va = smem_u32(Vs), da = smem_u32(Ds);
+            const uint32_t pa = smem_u32(PA), pd = smem_u32(PD), ea = smem_u32(Eb);
+            const uint32_t qta = smem_u32(Qt), kta = smem_u32(Kt);
+            constexpr uint32_t id_mm = idesc_bf16(64, 128, 1, 1);
+            constexpr uint32_t id_kk = idesc_bf16(64, 128, 0, 0);
+            constexpr uint32_t id_km = idesc_bf16(64, 128, 0, 1);
+            constexpr uint32_t id_e = idesc_bf16(128, 128, 1, 1);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // dk' = PdA^T Q
+                mma_bf16(tmem + 128, sdesc(pd + k * 2048, kTileBytes, 1024),
+                         sdesc(qa + k * 2048, kTileBytes, 1024), id_mm, k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)  // dk' += V~ E^T
+                mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                         sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, 1);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // dv = PA^T dO
+                mma_bf16(tmem + 256, sdesc(pa + k * 2048, kTileBytes, 1024),
+                         sdesc(da + k * 2048, kTileBytes, 1024), id_mm, k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)  // dv += K~ E
+                mma_bf16(tmem + 256, sdesc(kta + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                         sdesc(ea + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // dE = Q~^T dO
+                mma_bf16(tmem + 384, sdesc(qta + k * 2048, kTileBytes, 1024),
+                         sdesc(da + k * 2048, kTileBytes, 1024), id_e, k > 0);
+            mma_commit(obar);
+            // the next chunk's score products queue right behind: their
+            // accumulator columns were read before S1
+            if (it + 1 < nch) {
+                mbar_wait(smem_u32(&full_bar[s ^ 1]), ((it + 1) >> 1) & 1);
+                issue_scores(s ^ 1);
+            }
+        } else if (scn && it + 1 < nch) {
+            // gate tables of the next chunk, into the buffer scanned last time
+            gate_prep(gr, &gsb[(it + 1) & 1], G.lane);
+            if (it + 2 < nch) gr = gate_load(d, g, b, h, t0 - 2 * kChunk, G.lane);
+        } else if (epi) {
+            mbar_wait(obar, oph);  // this chunk's output products
+            oph ^= 1;
+            tc_fence_after();
+            float bk = 0.f;
+            const float cd = d.scale * diag_s[G.tau];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                float x[16], qv[16], kv[16];
+                const int col = 64 * G.grp + 32 * k;
+                const int c0 = col + 16 * G.hi;
+                tok16(tmem, G, 128 + col, x);
+                tile_row_get16(Qs, G.tau, c0, qv);
+                tile_row_get16(Ks, G.tau, c0, kv);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    bk = fmaf(kv[e], x[e], bk);
+                    x[e] = fmaf(cd, qv[e], x[e]);
+                }
+                store_row16(Vs, G.tau, c0, x);  // V~ is dead: stage dk there
+                tok16(tmem, G, 256 + col, x);
+                store_row16(Ds, G.tau, c0, x);  // dO is dead: stage dv there
+            }
+            bk += __shfl_xor_sync(kFull, bk, 16);
+            if (!G.hi) bpart[it & 1][G.grp][G.tau] = bk;
+            state_update_half(tmem, G, 384, 0, gs.W, E, Eb);
+            fence_async_smem();
+            tc_fence_before();
+        }
+        __syncthreads();  // S2
+        if (ctl && G.lane == 0) {
+            const int row = b * d.T + t0;
+            tma_store_3d(&mdk, smem_u32(Vs), 0, h, row);
+            tma_store_3d(&mdk, smem_u32(Vs + kTileBytes), 64, h, row);
+            tma_store_3d(&mdv, smem_u32(Ds), 0, h, row);
+            tma_store_3d(&mdv, smem_u32(Ds + kTileBytes), 64, h, row);
+            bulk_commit();
+            if (it + 2 < nch) {
+                bulk_wait_read();  // the staging tiles are refilled by the next load
+                issue(it + 2, s);
+            }
+        } else if (scn) {
+            carry = dg_scan(gs, bpart[it & 1], qd0, qd1, carry, G.lane,
+                            dg + ((int64_t)b * d.T + t0) * d.H + h, d.H);
+        }
+    }
+    if (ctl && G.lane == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // Failure-detection self test: waits on an mbarrier that nothing arrives on,
 // with the given bound, so that the timeout path and its host-side status can
 // be exercised without faulting or hanging the device.
@@ -1151,10 +1451,10 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             CUtensorMap mdk, mdv;
             if (!make_map(&mdk, p.out0, d, 128) || !make_map(&mdv, p.out1, d, d.Dv)) return RM_ERR_CUDA;
             if (d.Dv == 128) {
-                auto fr = tc_rev_kernel<128>;
+                auto fr = tc_rev128_kernel;
                 if (!set_smem(fr, rev_smem(128))) return RM_ERR_CUDA;
-                fr<<<grid, kThreads, rev_smem(128), s>>>(d, mq, mk, mv, mdo, mdk, mdv, p.g, p.S_in, p.dS_out,
-                                                          p.ws_f32, dko, dvo, p.dg);
+                fr<<<grid, kRevThreads, rev_smem(128), s>>>(d, mq, mk, mv, mdo, mdk, mdv, p.g, p.S_in, p.dS_out,
+                                                          p.ws_f32, p.dg);
             } else {
                 auto fr = tc_rev_kernel<256>;
                 if (!set_smem(fr, rev_smem(256))) return RM_ERR_CUDA;
