@@ -36,6 +36,7 @@ namespace {
 
 constexpr uint32_t kTileBytes = kChunk * 64 * 2;  // one [64 rows][64 cols] bf16 block: 8 KB
 constexpr int kThreads = 256;                     // 8 warps: two per tensor-memory lane quadrant
+constexpr int kRevThreads = kThreads + 64;        // + a control warp and a gate/scan warp
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -683,6 +684,231 @@ __global__ void __launch_bounds__(kThreads, DV == 128 ? 2 : 1)
     if (G.warp == 0) tmem_dealloc(tmem, TCOLS);
 }
 
+// dst = f * src for a [64][128] bf16 tile (uniform factor), 4 chunks per thread
+__device__ __forceinline__ void copy_scaled_tile(const uint8_t* src, uint8_t* dst, float f, int tid) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        int r;
+        const uint32_t off = scale_off(tid, k, &r);
+        scale_chunk(src + off, dst + off, f);
+    }
+}
+
+// ===========================================================================
+// forward sweep of the backward for Dv = 128, warp-specialised, with gamma:
+// dq, q.dq' per token, and gamma = sum_t (alpha_a..alpha_t) scale q_t dO_t^T
+// accumulated in tensor memory over the segment (one pass over q, k, v, dO).
+// Warps 0-7: epilogues; warp 8: TMA copies, MMAs, bulk stores; warp 9: gate
+// tables and the per-token q.dq' writes.  Two CTA-wide meetings per chunk
+// (S1: operands scaled; S2: outputs staged); the next chunk's dO V^T runs
+// right behind this chunk's output products.
+// ===========================================================================
+__global__ void __launch_bounds__(kRevThreads, 1)
+    tc_dqg128_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                     const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                     const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdq,
+                     const float* __restrict__ g, const float* __restrict__ S_in,
+                     float* __restrict__ gamma, float* __restrict__ qdq) {
+    constexpr uint32_t STAGE = 8 * kTileBytes;  // Q | K | V | dO
+    constexpr uint32_t OFF_P = 2 * STAGE, OFF_S = OFF_P + kTileBytes;  // S tile 32 KB
+    constexpr uint32_t OFF_QH = OFF_S + 4 * kTileBytes;               // (prefix decay) Q
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint8_t* Ps = smem + OFF_P;
+    uint8_t* Sb = smem + OFF_S;
+    uint8_t* Qh = smem + OFF_QH;
+    __shared__ GateSmem gsb[2];
+    __shared__ __align__(8) uint64_t full_bar[2];
+    __shared__ __align__(8) uint64_t score_bar;  // one commit per chunk: dA = dO V^T
+    __shared__ __align__(8) uint64_t out_bar;    // one commit per chunk: dq', dS, gamma
+    __shared__ uint32_t tmem_slot;
+    __shared__ float diag_s[kChunk];
+    __shared__ float apart[2][2][kChunk];  // [chunk parity][column group][token]
+
+    const Geo G = geo();
+    const bool epi = G.warp < 8;
+    const bool ctl = G.warp == 8;
+    const bool gat = G.warp == 9;
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+    const uint32_t sbar = smem_u32(&score_bar), obar = smem_u32(&out_bar);
+
+    if (G.tid == 0) {
+        mbar_init(smem_u32(&full_bar[0]), 1);
+        mbar_init(smem_u32(&full_bar[1]), 1);
+        mbar_init(sbar, 1);
+        mbar_init(obar, 1);
+        mbar_fence_init();
+    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
+    auto issue = [&](int c, int s) {
+        const int row = b * d.T + a0 + c * kChunk;
+        const uint32_t bar = smem_u32(&full_bar[s]);
+        uint8_t* st = smem + s * STAGE;
+        mbar_expect_tx(bar, STAGE);
+        load_tile(st, &mq, 0, 128, h, row, bar);
+        load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
+        load_tile(st + 4 * kTileBytes, &mv, 0, 128, h, row, bar);
+        load_tile(st + 6 * kTileBytes, &mdo, 0, 128, h, row, bar);
+    };
+    float S[64];
+    GateRegs gr;
+    if (epi) {
+        load_state_rows<128>(S_in + sum_off(d, seg, b, h), G, S, Sb);
+    } else if (gat) {
+        gr = gate_load(d, g, b, h, a0, G.lane);
+        gate_prep(gr, &gsb[0], G.lane);
+        if (nch > 1) gr = gate_load(d, g, b, h, a0 + kChunk, G.lane);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    auto issue_scores = [&](int s) {  // dA = dO V^T of the chunk in stage s
+        const uint32_t st = smem_u32(smem + s * STAGE);
+        const uint32_t va = st + 4 * kTileBytes, da = st + 6 * kTileBytes;
+        constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
+            mma_bf16(tmem, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+        }
+        mma_commit(sbar);
+    };
+    if (ctl && G.lane == 0) {
+        issue(0, 0);
+        if (nch > 1) issue(1, 1);
+        mbar_wait(smem_u32(&full_bar[0]), 0);
+        tc_fence_after();
+        issue_scores(0);
+    }
+    uint32_t sph = 0, oph = 0;
+    float P = 1.f;  // alpha product from the segment start to this chunk's start (epilogue warps)
+    for (int c = 0; c < nch; ++c) {
+        const int t0 = a0 + c * kChunk;
+        const int s = c & 1;
+        const GateSmem& gs = gsb[c & 1];
+        uint8_t* Qs = smem + s * STAGE;
+        uint8_t* Ks = Qs + 2 * kTileBytes;
+        uint8_t* Vs = Qs + 4 * kTileBytes;
+        uint8_t* Ds = Qs + 6 * kTileBytes;
+        if (epi) {
+            mbar_wait(sbar, sph);  // this chunk's dA
+            sph ^= 1;
+            mbar_wait(smem_u32(&full_bar[s]), (c >> 1) & 1);
+            tc_fence_after();
+            float x[16], gam[16];
+            tok16(tmem, G, 32 * G.grp, x);
+            const int c0 = 32 * G.grp + 16 * G.hi;
+            decay_row16(gs, G.tau, c0, true, gam);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                if (c0 + e == G.tau) diag_s[G.tau] = x[e];  // dO_t . v_t
+                x[e] *= d.scale * gam[e];
+            }
+            store_row16(Ps, G.tau, c0, x);
+            copy_scaled_tile(Qs, Qh, P, G.tid);            // gamma's A operand
+            scale_tile(Ds, Ds, gs.win, d.scale, G.tid);     // dO~
+            scale_tile(Vs, Vs, gs.wout, 1.f, G.tid);        // V~
+            P *= gs.W;
+            fence_async_smem();
+            tc_fence_before();
+        }
+        __syncthreads();  // S1
+        if (ctl && G.lane == 0) {
+            tc_fence_after();
+            const uint32_t ka = smem_u32(Ks), va = smem_u32(Vs), da = smem_u32(Ds);
+            const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb), qh = smem_u32(Qh);
+            constexpr uint32_t id_a = idesc_bf16(64, 128, 0, 1);
+            constexpr uint32_t id_b = idesc_bf16(64, 128, 0, 0);
+            constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // dq' = P K  (strictly causal part)
+                mma_bf16(tmem + 128, sdesc(pa + k * 32, 16, 1024), sdesc(ka + k * 2048, kTileBytes, 1024),
+                         id_a, k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)  // dq' += dO~ S_prev^T
+                mma_bf16(tmem + 128, sdesc(da + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                         sdesc(sa + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_b, 1);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // dS = K^T V~
+                mma_bf16(tmem + 256, sdesc(ka + k * 2048, kTileBytes, 1024),
+                         sdesc(va + k * 2048, kTileBytes, 1024), id_s, k > 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // gamma += (P Q)^T dO~
+                mma_bf16(tmem + 384, sdesc(qh + k * 2048, kTileBytes, 1024),
+                         sdesc(da + k * 2048, kTileBytes, 1024), id_s, (c > 0 || k > 0) ? 1u : 0u);
+            mma_commit(obar);
+            if (c + 1 < nch) {
+                mbar_wait(smem_u32(&full_bar[s ^ 1]), ((c + 1) >> 1) & 1);
+                issue_scores(s ^ 1);
+            }
+        } else if (gat && c + 1 < nch) {
+            gate_prep(gr, &gsb[(c + 1) & 1], G.lane);
+            if (c + 2 < nch) gr = gate_load(d, g, b, h, t0 + 2 * kChunk, G.lane);
+        } else if (epi) {
+            mbar_wait(obar, oph);  // this chunk's dq', dS and gamma products
+            oph ^= 1;
+            tc_fence_after();
+            const float cd = d.scale * diag_s[G.tau];
+            float a = 0.f;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                float x[16], qv[16], kv[16];
+                const int col = 64 * G.grp + 32 * k;
+                const int cc = col + 16 * G.hi;
+                tok16(tmem, G, 128 + col, x);
+                tile_row_get16(Qs, G.tau, cc, qv);
+                tile_row_get16(Ks, G.tau, cc, kv);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    a = fmaf(qv[e], x[e], a);
+                    x[e] = fmaf(cd, kv[e], x[e]);
+                }
+                store_row16(Ds, G.tau, cc, x);  // dO~ is dead: stage dq there
+            }
+            a += __shfl_xor_sync(kFull, a, 16);
+            if (!G.hi) apart[c & 1][G.grp][G.tau] = a;
+            state_update(tmem, G, 256, gs.W, S, Sb);
+            fence_async_smem();
+            tc_fence_before();
+        }
+        __syncthreads();  // S2
+        if (ctl && G.lane == 0) {
+            const int row = b * d.T + t0;
+            tma_store_3d(&mdq, smem_u32(Ds), 0, h, row);
+            tma_store_3d(&mdq, smem_u32(Ds + kTileBytes), 64, h, row);
+            bulk_commit();
+            if (c + 2 < nch) {
+                bulk_wait_read();  // the staging tile is refilled by the next load
+                issue(c + 2, s);
+            }
+        } else if (gat) {
+            const int64_t base = ((int64_t)b * d.T + t0) * d.H + h;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = 2 * G.lane + u;
+                qdq[base + int64_t(t) * d.H] = apart[c & 1][0][t] + apart[c & 1][1][t];
+            }
+        }
+    }
+    if (epi) {  // gamma rows (all products have completed: last out_bar wait)
+        tc_fence_after();
+        float* dst = gamma + sum_off(d, seg, b, h) + int64_t(G.srow) * 128 + 64 * G.grp;
+        float v[64];
+        state_cols64(tmem, G, 384, v);
+#pragma unroll
+        for (int i = 0; i < 64; i += 4)
+            *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    }
+    if (ctl && G.lane == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // ===========================================================================
 // reverse sweep of the backward: dk, dv, dg for one (segment, row, head).
 // Dv = 256 processes dv and the adjoint update in two 128-column halves
@@ -1044,7 +1270,6 @@ __device__ __forceinline__ float dg_scan(const GateSmem& gs, const float (*bp)[k
 // chunk's score products are issued right behind this chunk's output
 // products, dk and dv are staged in the chunk's own (dead) V~ and dO tiles.
 // ===========================================================================
-constexpr int kRevThreads = kThreads + 64;
 
 __global__ void __launch_bounds__(kRevThreads, 1)
     tc_rev128_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
@@ -1348,6 +1573,8 @@ constexpr size_t kOuterSmem = 96 * 1024 + 1024;
 constexpr size_t kFwdSmem = 13 * kTileBytes + 1024;   // Q K V P (7 tiles) + S (4) + o staging (2)
 // Q K (4 tiles) + V dO (2 NV) + P (1) + S (2 NV)
 constexpr size_t dq_smem(int dv) { return size_t(5 + 4 * (dv / 64)) * kTileBytes + 1024; }
+// 2 stages x 8 + P (1) + S (4) + prefix-decayed Q (2)
+constexpr size_t kDqg128Smem = 23 * kTileBytes + 1024;
 // stages x (4 + 2 NV) + Q~ K~ (4) + PA PdA (2) + E (2 NV): 26 tiles for Dv 128 and 256
 constexpr size_t rev_smem(int dv) {
     return size_t((dv == 128 ? 2 : 1) * (4 + 2 * (dv / 64)) + 6 + 2 * (dv / 64)) * kTileBytes + 1024;
@@ -1424,12 +1651,13 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             CUtensorMap mdq;
             if (!make_map(&mdq, p.out0, d, 128)) return RM_ERR_CUDA;
             if (d.Dv == 128) {
-                auto fo = tc_outer_kernel<128, true>;
-                auto fq = tc_dq_kernel<128>;
-                if (!set_smem(fo, kOuterSmem) || !set_smem(fq, dq_smem(128))) return RM_ERR_CUDA;
-                fo<<<grid, kThreads, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
+                auto fq = tc_dqg128_kernel;
+                if (!set_smem(fq, kDqg128Smem)) return RM_ERR_CUDA;
+                fq<<<grid, kRevThreads, kDqg128Smem, s>>>(d, mq, mk, mv, mdo, mdq, p.g, p.S_in, p.sum_out,
+                                                          p.ws_f32);
                 if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
-                fq<<<grid, kThreads, dq_smem(128), s>>>(d, mq, mk, mv, mdo, mdq, p.g, p.S_in, p.ws_f32);
+                note_launch(1);
+                return RM_OK;
             } else {
                 auto fo = tc_outer_kernel<256, true>;
                 auto fq = tc_dq_kernel<256>;
