@@ -42,6 +42,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// one arrival (release, CTA scope) without a transaction count
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -96,6 +100,10 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // the smem sources of all committed bulk stores may be overwritten
 __device__ __forceinline__ void bulk_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed bulk store but the most recent group has finished reading
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // all committed bulk stores have completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -238,11 +246,17 @@ struct alignas(16) GateSmem {
     float ep[kChunk];    // exp(b[tau] - b[63])
     float en[kChunk];    // exp(b[63] - b[tau])
     int lid[kChunk];
+    float nb[kChunk];    // exp(-b[tau])
     float btot;          // b[63]
+    float emb;           // exp(-b[63])
     float W;             // alpha_0 ... alpha_63
     int first;           // position 0 starts a sequence
     int any;             // some position of the chunk starts a sequence
     int fast;            // every |b[tau] - b[63]| < 60: exp(b_t - b_s) = ep[t] en[s] in fp32
+    // no sequence starts in the chunk and every |b[tau]| < 60 (with fast): the
+    // decay weights can move from the operand tiles into the score masks and
+    // onto the output rows, with every factor within e^(+-60)
+    int fact;
 };
 
 struct GateRegs {
@@ -298,10 +312,15 @@ __device__ __forceinline__ void gate_prep(const GateRegs& r, GateSmem* gs, int l
     gs->ep[2 * lane + 1] = expf(b1 - btot);
     gs->wout[2 * lane] = (l0 == ltot) ? en0 : 0.f;
     gs->wout[2 * lane + 1] = (l1 == ltot) ? en1 : 0.f;
+    gs->nb[2 * lane] = expf(-b0);
+    gs->nb[2 * lane + 1] = expf(-b1);
     const float dev = fmaxf(fabsf(btot - b0), fabsf(btot - b1));
     const bool fast = __all_sync(0xffffffffu, dev < 60.f);
+    const bool small = __all_sync(0xffffffffu, fmaxf(fabsf(b0), fabsf(b1)) < 60.f);
     if (lane == 0) {
         gs->btot = btot;
+        gs->emb = expf(-btot);
+        gs->fact = (fast && small && !first && ltot == 0) ? 1 : 0;
         gs->W = (!first && ltot == 0) ? expf(btot) : 0.f;
         gs->first = first;
         gs->any = (first || ltot > 0) ? 1 : 0;

@@ -37,6 +37,7 @@ namespace {
 constexpr uint32_t kTileBytes = kChunk * 64 * 2;  // one [64 rows][64 cols] bf16 block: 8 KB
 constexpr int kThreads = 256;                     // 8 warps: two per tensor-memory lane quadrant
 constexpr int kRevThreads = kThreads + 64;        // + a control warp and a gate/scan warp
+constexpr int kRev3Threads = kThreads + 96;       // + an MMA warp, a gate/scan warp and a copy warp
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -1261,17 +1262,31 @@ __device__ __forceinline__ float dg_scan(const GateSmem& gs, const float (*bp)[k
 }
 
 // ===========================================================================
-// reverse sweep for Dv = 128, warp-specialised and software-pipelined.
-// Warps 0-7 form the epilogues (score masks, tile scaling, dk/dv rows, the
-// adjoint update); warp 8 issues every TMA copy and MMA and the bulk stores;
-// warp 9 prepares the gate tables and runs each chunk's gate-gradient scan.
-// Per chunk the CTA meets twice: S1 (scaled operands ready -> output
-// products) and S2 (outputs staged -> stores, refill, scan).  The next
-// chunk's score products are issued right behind this chunk's output
-// products, dk and dv are staged in the chunk's own (dead) V~ and dO tiles.
+// reverse sweep for Dv = 128, warp-specialised, paced by mbarriers instead of
+// CTA-wide barriers so that the tensor products overlap the epilogues:
+//   warps 0-7 (epilogues), per chunk:
+//     E1  score masks PA, PdA; V~ in place          -> pv_ready
+//         K~ and Q~ copies                            -> kq_ready
+//     E2  dk rows (staged in the dead V~ tile)        -> dk_staged
+//         dv rows (in the K~ tile), adjoint E          -> dv_staged, b_ready
+//   warp 8 (one thread) issues the tensor products: dk' = PdA^T Q + V~ E^T
+//     at pv_ready, dv = PA^T dO + K~ E and dE = Q~^T dO at kq_ready, then
+//     the next chunk's scores.  Chunks without sequence starts and with
+//     moderate decays are "factored": their weights sit in the score masks,
+//     on dO and on the output rows, so V E^T and K E need no epilogue work
+//     and are issued as soon as the adjoint of the chunk after is in place.
+//   warp 10 (one thread): the bulk stores of dk and dv, the refill of the
+//     stage with the chunk after next as its tiles die (Q, K, dO at
+//     dv_staged, V once the dk store has read it), and stg_free once the dv
+//     store has read the K~ tile.
+//   warp 9: the gate-gradient scan of a chunk once its b' rows are in, and
+//     the gate tables two chunks ahead.
+// Every barrier completes once per chunk (or once per two chunks for the
+// parity-indexed pairs) and each waiter is paced so that it cannot fall a
+// full phase behind.
 // ===========================================================================
 
-__global__ void __launch_bounds__(kRevThreads, 1)
+__global__ void __launch_bounds__(kRev3Threads, 1)
     tc_rev128_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                      const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdk,
@@ -1290,15 +1305,16 @@ __global__ void __launch_bounds__(kRevThreads, 1)
     uint8_t* PA = smem + OFF_PA;
     uint8_t* PD = smem + OFF_PD;
     uint8_t* Eb = smem + OFF_E;
-    __shared__ GateSmem gsb[2];  // gate tables of the current and the next chunk
+    __shared__ GateSmem gsb[2];  // gate tables by chunk parity
     __shared__ __align__(8) uint64_t full_bar[2];
-    // one barrier per commit stream: the score products and the output
-    // products each commit once per chunk, and each is waited on before the
-    // stream's next commit can be issued, so no waiter can miss a phase
-    __shared__ __align__(8) uint64_t score_bar;
-    __shared__ __align__(8) uint64_t out_bar;
+    __shared__ __align__(8) uint64_t score_bar, dk_done, dve_done;  // tensor-core commits
+    __shared__ __align__(8) uint64_t pv_ready, kq_ready, dk_staged, dv_staged;  // epilogue -> warp 8
+    __shared__ __align__(8) uint64_t b_ready[2];     // epilogue -> warp 9, by chunk parity
+    __shared__ __align__(8) uint64_t scan_done[2];   // warp 9 -> epilogue (b' rows free)
+    __shared__ __align__(8) uint64_t gate_ready[2];  // warp 9 -> epilogue (gate tables)
+    __shared__ __align__(8) uint64_t stg_free;       // warp 8 -> epilogue: dv store has read K~
     __shared__ uint32_t tmem_slot;
-    __shared__ float diag_s[kChunk];
+    __shared__ float diag_s[2][kChunk];  // dO_t . v_t by chunk parity
     __shared__ float bpart[2][2][kChunk];  // [chunk parity][column group][token]
     __shared__ float red[8];
 
@@ -1306,16 +1322,26 @@ __global__ void __launch_bounds__(kRevThreads, 1)
     const bool epi = G.warp < 8;
     const bool ctl = G.warp == 8;
     const bool scn = G.warp == 9;
+    const bool tma = G.warp == 10;
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
-    const uint32_t sbar = smem_u32(&score_bar), obar = smem_u32(&out_bar);
 
     if (G.tid == 0) {
-        mbar_init(smem_u32(&full_bar[0]), 1);
-        mbar_init(smem_u32(&full_bar[1]), 1);
-        mbar_init(sbar, 1);
-        mbar_init(obar, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&full_bar[i]), 1);
+            mbar_init(smem_u32(&b_ready[i]), 8);
+            mbar_init(smem_u32(&scan_done[i]), 1);
+            mbar_init(smem_u32(&gate_ready[i]), 1);
+        }
+        mbar_init(smem_u32(&score_bar), 1);
+        mbar_init(smem_u32(&dk_done), 1);
+        mbar_init(smem_u32(&dve_done), 1);
+        mbar_init(smem_u32(&pv_ready), 8);
+        mbar_init(smem_u32(&kq_ready), 8);
+        mbar_init(smem_u32(&dk_staged), 8);
+        mbar_init(smem_u32(&dv_staged), 8);
+        mbar_init(smem_u32(&stg_free), 1);
         mbar_fence_init();
     }
     if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
@@ -1349,169 +1375,316 @@ __global__ void __launch_bounds__(kRevThreads, 1)
         }
         ext = warp_sum(ext);
         if (G.lane == 0) red[G.warp] = ext;
-    } else if (scn) {
+    } else if (scn) {  // gate tables of the first two chunks; registers for the third
         gr = gate_load(d, g, b, h, a0 + (nch - 1) * kChunk, G.lane);
         gate_prep(gr, &gsb[0], G.lane);
-        if (nch > 1) gr = gate_load(d, g, b, h, a0 + (nch - 2) * kChunk, G.lane);
+        if (nch > 1) {
+            gr = gate_load(d, g, b, h, a0 + (nch - 2) * kChunk, G.lane);
+            gate_prep(gr, &gsb[1], G.lane);
+        }
+        if (nch > 2) gr = gate_load(d, g, b, h, a0 + (nch - 3) * kChunk, G.lane);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    float carry = 0.f;  // gate-gradient sum carried from later chunks (warp 9)
-    if (scn) {
+
+    if (ctl) {
+        if (G.lane == 0) {
+            // score products A = Q K^T and dA = dO V^T of the chunk in stage s
+            auto issue_scores = [&](int s) {
+                const uint32_t qa = smem_u32(smem + s * STAGE), ka = qa + 2 * kTileBytes;
+                const uint32_t va = qa + 4 * kTileBytes, da = qa + 6 * kTileBytes;
+                constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
 #pragma unroll
-        for (int w = 0; w < 8; ++w) carry += red[w];
-    }
-    // score products A = Q K^T and dA = dO V^T of the chunk in stage s
-    auto issue_scores = [&](int s) {
-        const uint32_t qa = smem_u32(smem + s * STAGE), ka = qa + 2 * kTileBytes;
-        const uint32_t va = qa + 4 * kTileBytes, da = qa + 6 * kTileBytes;
-        constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
-            mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, k > 0);
-            mma_bf16(tmem + 64, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
-        }
-        mma_commit(sbar);
-    };
-    if (ctl && G.lane == 0) {
-        issue(0, 0);
-        if (nch > 1) issue(1, 1);
-        mbar_wait(smem_u32(&full_bar[0]), 0);
-        tc_fence_after();
-        issue_scores(0);
-    }
-    uint32_t sph = 0, oph = 0;
-    for (int it = 0; it < nch; ++it) {
-        const int c = nch - 1 - it;
-        const int t0 = a0 + c * kChunk;
-        const int s = it & 1;
-        const GateSmem& gs = gsb[it & 1];
-        uint8_t* Qs = smem + s * STAGE;
-        uint8_t* Ks = Qs + 2 * kTileBytes;
-        uint8_t* Vs = Qs + 4 * kTileBytes;
-        uint8_t* Ds = Qs + 6 * kTileBytes;
-        float qd0 = 0.f, qd1 = 0.f;
-        if (scn) {  // q.dq' of this lane's two scan tokens
-            qd0 = __ldg(qdq + ((int64_t)b * d.T + t0 + 63 - 2 * G.lane) * d.H + h);
-            qd1 = __ldg(qdq + ((int64_t)b * d.T + t0 + 62 - 2 * G.lane) * d.H + h);
-        }
-        if (epi) {
-            mbar_wait(sbar, sph);  // this chunk's score products
-            sph ^= 1;
-            mbar_wait(smem_u32(&full_bar[s]), (it >> 1) & 1);  // its tiles, for the scaling
-            tc_fence_after();
-            float xa[16], xd[16], gam[16];
-            tok16(tmem, G, 32 * G.grp, xa);
-            tok16(tmem, G, 64 + 32 * G.grp, xd);
-            const int c0 = 32 * G.grp + 16 * G.hi;
-            decay_row16(gs, G.tau, c0, false, gam);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int sidx = c0 + e;
-                if (sidx == G.tau) diag_s[G.tau] = xd[e];  // dO_t . v_t
-                xa[e] *= d.scale * gam[e];
-                xd[e] = sidx < G.tau ? xd[e] * d.scale * gam[e] : 0.f;
-            }
-            store_row16(PA, G.tau, c0, xa);
-            store_row16(PD, G.tau, c0, xd);
-            scale_tile(Qs, Qt, gs.win, d.scale, G.tid);
-            scale_tile(Ks, Kt, gs.wout, 1.f, G.tid);
-            scale_tile(Vs, Vs, gs.wout, 1.f, G.tid);
-            fence_async_smem();
-            tc_fence_before();
-        }
-        __syncthreads();  // S1
-        if (ctl && G.lane == 0) {
-            tc_fence_after();
-            const uint32_t qa = smem_u32(Qs), va = smem_u32(Vs), da = smem_u32(Ds);
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
+                    mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, k > 0);
+                    mma_bf16(tmem + 64, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+                }
+                mma_commit(smem_u32(&score_bar));
+            };
             const uint32_t pa = smem_u32(PA), pd = smem_u32(PD), ea = smem_u32(Eb);
             const uint32_t qta = smem_u32(Qt), kta = smem_u32(Kt);
             constexpr uint32_t id_mm = idesc_bf16(64, 128, 1, 1);
             constexpr uint32_t id_kk = idesc_bf16(64, 128, 0, 0);
             constexpr uint32_t id_km = idesc_bf16(64, 128, 0, 1);
             constexpr uint32_t id_e = idesc_bf16(128, 128, 1, 1);
+            // The E-side products of a factored chunk, dk' = V E^T and
+            // dv = K E, use unscaled tiles and the adjoint of the chunk after
+            // it: they are issued as soon as that adjoint is in the E tile,
+            // ahead of the chunk's score masks.
+            auto issue_e_side = [&](int s) {
+                const uint32_t qa = smem_u32(smem + s * STAGE);
+                const uint32_t ka = qa + 2 * kTileBytes, va = qa + 4 * kTileBytes;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // dk' = PdA^T Q
-                mma_bf16(tmem + 128, sdesc(pd + k * 2048, kTileBytes, 1024),
-                         sdesc(qa + k * 2048, kTileBytes, 1024), id_mm, k > 0);
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                             sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, k > 0);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)  // dk' += V~ E^T
-                mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                         sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, 1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // dv = PA^T dO
-                mma_bf16(tmem + 256, sdesc(pa + k * 2048, kTileBytes, 1024),
-                         sdesc(da + k * 2048, kTileBytes, 1024), id_mm, k > 0);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)  // dv += K~ E
-                mma_bf16(tmem + 256, sdesc(kta + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                         sdesc(ea + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // dE = Q~^T dO
-                mma_bf16(tmem + 384, sdesc(qta + k * 2048, kTileBytes, 1024),
-                         sdesc(da + k * 2048, kTileBytes, 1024), id_e, k > 0);
-            mma_commit(obar);
-            // the next chunk's score products queue right behind: their
-            // accumulator columns were read before S1
-            if (it + 1 < nch) {
-                mbar_wait(smem_u32(&full_bar[s ^ 1]), ((it + 1) >> 1) & 1);
-                issue_scores(s ^ 1);
-            }
-        } else if (scn && it + 1 < nch) {
-            // gate tables of the next chunk, into the buffer scanned last time
-            gate_prep(gr, &gsb[(it + 1) & 1], G.lane);
-            if (it + 2 < nch) gr = gate_load(d, g, b, h, t0 - 2 * kChunk, G.lane);
-        } else if (epi) {
-            mbar_wait(obar, oph);  // this chunk's output products
-            oph ^= 1;
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16(tmem + 256, sdesc(ka + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                             sdesc(ea + k * 2048, 2 * kTileBytes, 1024), id_km, k > 0);
+            };
+            mbar_wait(smem_u32(&full_bar[0]), 0);
             tc_fence_after();
-            float bk = 0.f;
-            const float cd = d.scale * diag_s[G.tau];
+            issue_scores(0);
+            // factored chunks keep K, Q and V unscaled (the weights sit in the
+            // score masks, on dO and on the output rows)
+            bool fact = gsb[0].fact != 0;
+            if (fact) issue_e_side(0);
+            for (int it = 0; it < nch; ++it) {
+                const int s = it & 1;
+                const uint32_t ph = it & 1;
+                const uint32_t qa = smem_u32(smem + s * STAGE);
+                const uint32_t va = qa + 4 * kTileBytes, da = qa + 6 * kTileBytes;
+                mbar_wait(smem_u32(&pv_ready), ph);
+                tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                float x[16], qv[16], kv[16];
-                const int col = 64 * G.grp + 32 * k;
-                const int c0 = col + 16 * G.hi;
-                tok16(tmem, G, 128 + col, x);
-                tile_row_get16(Qs, G.tau, c0, qv);
-                tile_row_get16(Ks, G.tau, c0, kv);
+                for (int k = 0; k < 4; ++k)  // dk' (+)= PdA^T Q
+                    mma_bf16(tmem + 128, sdesc(pd + k * 2048, kTileBytes, 1024),
+                             sdesc(qa + k * 2048, kTileBytes, 1024), id_mm, (fact || k > 0) ? 1u : 0u);
+                if (!fact) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)  // dk' += V~ E^T
+                        mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                                 sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, 1);
+                }
+                mma_commit(smem_u32(&dk_done));
+                mbar_wait(smem_u32(&kq_ready), ph);
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // dv (+)= PA^T dO
+                    mma_bf16(tmem + 256, sdesc(pa + k * 2048, kTileBytes, 1024),
+                             sdesc(da + k * 2048, kTileBytes, 1024), id_mm, (fact || k > 0) ? 1u : 0u);
+                if (!fact) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)  // dv += K~ E
+                        mma_bf16(tmem + 256, sdesc(kta + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                                 sdesc(ea + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
+                }
+                const uint32_t qx = fact ? qa : qta;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // dE = Q~^T dO
+                    mma_bf16(tmem + 384, sdesc(qx + k * 2048, kTileBytes, 1024),
+                             sdesc(da + k * 2048, kTileBytes, 1024), id_e, k > 0);
+                mma_commit(smem_u32(&dve_done));
+                // the next chunk's scores: their accumulator columns were read
+                // before pv_ready, their tiles were loaded into the other stage
+                if (it + 1 < nch) {
+                    mbar_wait(smem_u32(&full_bar[s ^ 1]), ((it + 1) >> 1) & 1);
+                    tc_fence_after();
+                    issue_scores(s ^ 1);
+                }
+                // the adjoint of this chunk is in the E tile and its dk', dv
+                // rows have been read: the next chunk's E-side products
+                if (it + 1 < nch) {
+                    mbar_wait(smem_u32(&dv_staged), ph);
+                    if (it + 1 >= 2) mbar_wait(smem_u32(&gate_ready[(it + 1) & 1]), ((it - 1) >> 1) & 1);
+                    fact = gsb[(it + 1) & 1].fact != 0;
+                    if (fact) {
+                        tc_fence_after();
+                        issue_e_side(s ^ 1);
+                    }
+                }
+            }
+        }
+    } else if (tma) {
+        if (G.lane == 0) {
+            issue(0, 0);
+            if (nch > 1) issue(1, 1);
+            const uint32_t kta = smem_u32(Kt);
+            for (int it = 0; it < nch; ++it) {
+                const int s = it & 1;
+                const uint32_t ph = it & 1;
+                const int row = b * d.T + a0 + (nch - 1 - it) * kChunk;
+                uint8_t* st = smem + s * STAGE;
+                uint8_t* Vs = st + 4 * kTileBytes;
+                mbar_wait(smem_u32(&dk_staged), ph);
+                tma_store_3d(&mdk, smem_u32(Vs), 0, h, row);
+                tma_store_3d(&mdk, smem_u32(Vs + kTileBytes), 64, h, row);
+                bulk_commit();
+                // dv_staged: the output products are done and the dk rows have
+                // read Q and K, so Q, K and dO of this stage are dead; V is
+                // dead once the dk store has read it
+                mbar_wait(smem_u32(&dv_staged), ph);
+                tma_store_3d(&mdv, kta, 0, h, row);
+                tma_store_3d(&mdv, kta + kTileBytes, 64, h, row);
+                bulk_commit();
+                if (it + 2 < nch) {
+                    const int nrow = b * d.T + a0 + (nch - 3 - it) * kChunk;
+                    const uint32_t fb = smem_u32(&full_bar[s]);
+                    mbar_expect_tx(fb, STAGE);
+                    load_tile(st, &mq, 0, 128, h, nrow, fb);
+                    load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, nrow, fb);
+                    load_tile(st + 6 * kTileBytes, &mdo, 0, DV, h, nrow, fb);
+                    bulk_wait_read1();  // the dk store has read V's tile
+                    load_tile(Vs, &mv, 0, DV, h, nrow, fb);
+                }
+                bulk_wait_read();  // the dv store has read the K~ tile
+                mbar_arrive(smem_u32(&stg_free));
+            }
+            bulk_wait_all();
+        }
+    } else if (scn) {
+        float carry = 0.f;  // gate-gradient sum carried from later chunks
+#pragma unroll
+        for (int w = 0; w < 8; ++w) carry += red[w];
+        for (int it = 0; it < nch; ++it) {
+            const int c = nch - 1 - it;
+            const int t0 = a0 + c * kChunk;
+            const int p = it & 1;
+            const float qd0 = __ldg(qdq + ((int64_t)b * d.T + t0 + 63 - 2 * G.lane) * d.H + h);
+            const float qd1 = __ldg(qdq + ((int64_t)b * d.T + t0 + 62 - 2 * G.lane) * d.H + h);
+            mbar_wait(smem_u32(&b_ready[p]), (it >> 1) & 1);
+            carry = dg_scan(gsb[p], bpart[p], qd0, qd1, carry, G.lane,
+                            dg + ((int64_t)b * d.T + t0) * d.H + h, d.H);
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&scan_done[p]));
+            if (it + 2 < nch) {  // the tables of chunk it + 2 replace this chunk's
+                gate_prep(gr, &gsb[p], G.lane);
+                if (it + 3 < nch) gr = gate_load(d, g, b, h, t0 - 3 * kChunk, G.lane);
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&gate_ready[p]));
+            }
+        }
+    } else {  // epilogue warps
+        uint32_t sph = 0, kph = 0, vph = 0;
+        for (int it = 0; it < nch; ++it) {
+            const int s = it & 1;
+            const int p = it & 1;
+            const GateSmem& gs = gsb[p];
+            uint8_t* Qs = smem + s * STAGE;
+            uint8_t* Ks = Qs + 2 * kTileBytes;
+            uint8_t* Vs = Qs + 4 * kTileBytes;
+            uint8_t* Ds = Qs + 6 * kTileBytes;
+            // ---- E1
+            if (it >= 2) mbar_wait(smem_u32(&gate_ready[p]), ((it - 2) >> 1) & 1);
+            mbar_wait(smem_u32(&score_bar), sph);
+            sph ^= 1;
+            mbar_wait(smem_u32(&full_bar[s]), (it >> 1) & 1);  // its tiles, for the scaling
+            tc_fence_after();
+            const bool fact = gs.fact != 0;
+            if (fact) {
+                // dk = wout (Pd^T Q + V E^T) with Pd = scale ep_t dA (s < t);
+                // dv = wout (Pa^T dO~ + K E) with Pa = e^(-b_63) A (s <= t);
+                // dE = Q^T dO~, dO~ = scale win dO
+                float xa[16], xd[16];
+                tok16(tmem, G, 32 * G.grp, xa);
+                tok16(tmem, G, 64 + 32 * G.grp, xd);
+                const int c0 = 32 * G.grp + 16 * G.hi;
+                const float fd = d.scale * gs.ep[G.tau], fa = gs.emb;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    bk = fmaf(kv[e], x[e], bk);
-                    x[e] = fmaf(cd, qv[e], x[e]);
+                    const int sidx = c0 + e;
+                    if (sidx == G.tau) diag_s[p][G.tau] = xd[e];  // dO_t . v_t
+                    xa[e] = sidx <= G.tau ? xa[e] * fa : 0.f;
+                    xd[e] = sidx < G.tau ? xd[e] * fd : 0.f;
                 }
-                store_row16(Vs, G.tau, c0, x);  // V~ is dead: stage dk there
-                tok16(tmem, G, 256 + col, x);
-                store_row16(Ds, G.tau, c0, x);  // dO is dead: stage dv there
+                store_row16(PA, G.tau, c0, xa);
+                store_row16(PD, G.tau, c0, xd);
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&pv_ready));
+                scale_tile(Ds, Ds, gs.win, d.scale, G.tid);
+                fence_async_smem();
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&kq_ready));
+            } else {
+                {
+                    float xa[16], xd[16], gam[16];
+                    tok16(tmem, G, 32 * G.grp, xa);
+                    tok16(tmem, G, 64 + 32 * G.grp, xd);
+                    const int c0 = 32 * G.grp + 16 * G.hi;
+                    decay_row16(gs, G.tau, c0, false, gam);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int sidx = c0 + e;
+                        if (sidx == G.tau) diag_s[p][G.tau] = xd[e];  // dO_t . v_t
+                        xa[e] *= d.scale * gam[e];
+                        xd[e] = sidx < G.tau ? xd[e] * d.scale * gam[e] : 0.f;
+                    }
+                    store_row16(PA, G.tau, c0, xa);
+                    store_row16(PD, G.tau, c0, xd);
+                }
+                scale_tile(Vs, Vs, gs.wout, 1.f, G.tid);
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&pv_ready));
+                if (it >= 1) mbar_wait(smem_u32(&stg_free), (it - 1) & 1);  // K~ tile free
+                scale_tile(Ks, Kt, gs.wout, 1.f, G.tid);
+                scale_tile(Qs, Qt, gs.win, d.scale, G.tid);
+                fence_async_smem();
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&kq_ready));
             }
-            bk += __shfl_xor_sync(kFull, bk, 16);
-            if (!G.hi) bpart[it & 1][G.grp][G.tau] = bk;
+            // ---- E2: dk rows
+            mbar_wait(smem_u32(&dk_done), kph);
+            kph ^= 1;
+            if (it >= 2) mbar_wait(smem_u32(&scan_done[p]), ((it - 2) >> 1) & 1);
+            // the copy warp has stored the previous chunk (K~ tile free); this
+            // also keeps dk_staged and dv_staged within one phase of it
+            if (it >= 1) mbar_wait(smem_u32(&stg_free), (it - 1) & 1);
+            // diag_s of this chunk comes from the other warp of the quadrant:
+            // every epilogue warp arrived on pv_ready after writing it
+            mbar_wait(smem_u32(&pv_ready), it & 1);
+            tc_fence_after();
+            {
+                float bk = 0.f;
+                const float cd = d.scale * diag_s[p][G.tau];
+                const float wr = fact ? gs.wout[G.tau] : 1.f;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    float x[16], qv[16], kv[16];
+                    const int col = 64 * G.grp + 32 * k;
+                    const int c0 = col + 16 * G.hi;
+                    tok16(tmem, G, 128 + col, x);
+                    tile_row_get16(Qs, G.tau, c0, qv);
+                    tile_row_get16(Ks, G.tau, c0, kv);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        x[e] *= wr;
+                        bk = fmaf(kv[e], x[e], bk);
+                        x[e] = fmaf(cd, qv[e], x[e]);
+                    }
+                    store_row16(Vs, G.tau, c0, x);  // V~ is dead: stage dk there
+                }
+                bk += __shfl_xor_sync(kFull, bk, 16);
+                if (!G.hi) bpart[p][G.grp][G.tau] = bk;
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&dk_staged));
+            // ---- E2: dv rows and the adjoint update
+            mbar_wait(smem_u32(&dve_done), vph);
+            vph ^= 1;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                float x[16];
+                const int col = 64 * G.grp + 32 * k;
+                tok16(tmem, G, 256 + col, x);
+                if (fact) {
+                    const float wr = gs.wout[G.tau];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) x[e] *= wr;
+                }
+                store_row16(Kt, G.tau, col + 16 * G.hi, x);  // K~ is dead: stage dv there
+            }
             state_update_half(tmem, G, 384, 0, gs.W, E, Eb);
             fence_async_smem();
             tc_fence_before();
-        }
-        __syncthreads();  // S2
-        if (ctl && G.lane == 0) {
-            const int row = b * d.T + t0;
-            tma_store_3d(&mdk, smem_u32(Vs), 0, h, row);
-            tma_store_3d(&mdk, smem_u32(Vs + kTileBytes), 64, h, row);
-            tma_store_3d(&mdv, smem_u32(Ds), 0, h, row);
-            tma_store_3d(&mdv, smem_u32(Ds + kTileBytes), 64, h, row);
-            bulk_commit();
-            if (it + 2 < nch) {
-                bulk_wait_read();  // the staging tiles are refilled by the next load
-                issue(it + 2, s);
+            __syncwarp();
+            if (G.lane == 0) {
+                mbar_arrive(smem_u32(&dv_staged));
+                mbar_arrive(smem_u32(&b_ready[p]));
             }
-        } else if (scn) {
-            carry = dg_scan(gs, bpart[it & 1], qd0, qd1, carry, G.lane,
-                            dg + ((int64_t)b * d.T + t0) * d.H + h, d.H);
         }
     }
-    if (ctl && G.lane == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (G.warp == 0) tmem_dealloc(tmem, 512);
@@ -1681,7 +1854,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             if (d.Dv == 128) {
                 auto fr = tc_rev128_kernel;
                 if (!set_smem(fr, rev_smem(128))) return RM_ERR_CUDA;
-                fr<<<grid, kRevThreads, rev_smem(128), s>>>(d, mq, mk, mv, mdo, mdk, mdv, p.g, p.S_in, p.dS_out,
+                fr<<<grid, kRev3Threads, rev_smem(128), s>>>(d, mq, mk, mv, mdo, mdk, mdv, p.g, p.S_in, p.dS_out,
                                                           p.ws_f32, p.dg);
             } else {
                 auto fr = tc_rev_kernel<256>;
