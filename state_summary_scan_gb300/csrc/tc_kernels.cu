@@ -126,6 +126,19 @@ __device__ __forceinline__ void state_update(uint32_t tmem, const Geo& g, int co
     store_state_half(tile, g.srow, g.grp, S);
 }
 
+// S[e] = W (S[e] + acc[srow][64 grp + e]): the update of a factored chunk
+__device__ __forceinline__ void state_update_scaled(uint32_t tmem, const Geo& g, int col, float W, float* S,
+                                                    uint8_t* tile) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        float y[32];
+        tmem_ld32(tmem + g.tl + col + 64 * g.grp + 32 * hf, y);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) S[32 * hf + e] = W * (S[32 * hf + e] + y[e]);
+    }
+    store_state_half(tile, g.srow, g.grp, S);
+}
+
 // State rows of width DV split over the two column groups: thread (srow, grp)
 // owns columns 128 h + 64 grp + [0, 64) for h < DV / 128, stored in S[64 h + e].
 template <int DV>
@@ -384,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t* Ps = smem + OFF_P;
     uint8_t* Sb = smem + OFF_S;
     uint8_t* Os = smem + OFF_O;
-    __shared__ GateSmem gs;
+    __shared__ GateSmem gsb[2];  // gate tables by chunk parity, built one chunk ahead
     __shared__ __align__(8) uint64_t full_bar;
     __shared__ __align__(8) uint64_t mma_bar;
     __shared__ uint32_t tmem_slot;
@@ -427,15 +440,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     };
     if (G.tid == 0) issue(0);
     GateRegs gr;
-    if (G.warp == 0) gr = gate_load(d, g, b, h, a0, G.lane);
+    if (G.warp == 0) {
+        gr = gate_load(d, g, b, h, a0, G.lane);
+        gate_prep(gr, &gsb[0], G.lane);
+        if (nch > 1) gr = gate_load(d, g, b, h, a0 + kChunk, G.lane);
+    }
+    __syncthreads();
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
         const int t0 = a0 + c * kChunk;
-        if (G.warp == 0) {
-            gate_prep(gr, &gs, G.lane);
-            if (c + 1 < nch) gr = gate_load(d, g, b, h, t0 + kChunk, G.lane);
-        }
+        const GateSmem& gs = gsb[c & 1];
+        // Chunks without sequence starts and with moderate decays take the
+        // decays as K^ = exp(-b) K (in place, before the scores):
+        //   o_t = scale win_t (sum_{s<=t} (q_t . k^_s) v_s + q_t S_prev),
+        //   S   = W (S_prev + K^T^ V),
+        // so the score mask has no exponentials and Q is not scaled.
+        const bool fact = gs.fact != 0;
         mbar_wait(fb, c & 1);
+        if (fact) {
+            scale_tile(Ks, Ks, gs.nb, 1.f, G.tid);
+            fence_async_smem();
+        }
         __syncthreads();
         const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks), va = smem_u32(Vs);
         const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb);
@@ -453,7 +478,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_wait(mb, mph);
         mph ^= 1;
         tc_fence_after();
-        {
+        if (fact) {
+            float x[16];
+            tok16(tmem, G, 32 * G.grp, x);
+            const int c0 = 32 * G.grp + 16 * G.hi;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = c0 + e <= G.tau ? x[e] : 0.f;
+            store_row16(Ps, G.tau, c0, x);
+        } else {
             float x[16], gam[16];
             tok16(tmem, G, 32 * G.grp, x);
             const int c0 = 32 * G.grp + 16 * G.hi;
@@ -485,19 +517,29 @@ __global__ void __launch_bounds__(kThreads, 2)
                          sdesc(va + k * 2048, kTileBytes, 1024), id_s, k > 0);
             mma_commit(mb);
         }
+        if (G.warp == 0 && c + 1 < nch) {  // the next chunk's gate tables
+            gate_prep(gr, &gsb[(c + 1) & 1], G.lane);
+            if (c + 2 < nch) gr = gate_load(d, g, b, h, t0 + 2 * kChunk, G.lane);
+        }
         mbar_wait(mb, mph);
         mph ^= 1;
         if (G.tid == 0 && c + 1 < nch) issue(c + 1);
         tc_fence_after();
         {
+            const float wr = fact ? d.scale * gs.win[G.tau] : 1.f;
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 float x[16];
                 const int col = 64 * G.grp + 32 * k;
                 tok16(tmem, G, col, x);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] *= wr;
                 store_row16(Os, G.tau, col + 16 * G.hi, x);
             }
-            state_update(tmem, G, 128, gs.W, S, Sb);
+            if (fact)
+                state_update_scaled(tmem, G, 128, gs.W, S, Sb);
+            else
+                state_update(tmem, G, 128, gs.W, S, Sb);
         }
         fence_async_smem();
         tc_fence_before();
@@ -800,19 +842,36 @@ __global__ void __launch_bounds__(kRevThreads, 1)
             sph ^= 1;
             mbar_wait(smem_u32(&full_bar[s]), (c >> 1) & 1);
             tc_fence_after();
-            float x[16], gam[16];
+            // Factored chunks (no sequence start, moderate decays) take the
+            // decays as K^ = exp(-b) K:  dq'_t = scale win_t (sum_{s<t}
+            // (dO_t . v_s) k^_s + dO_t S_prev^T),  dS = W K^T^ V,  and gamma's
+            // row weights go on its copy of Q; dO and V stay unscaled.
+            const bool fact = gs.fact != 0;
+            float x[16];
             tok16(tmem, G, 32 * G.grp, x);
             const int c0 = 32 * G.grp + 16 * G.hi;
-            decay_row16(gs, G.tau, c0, true, gam);
+            if (fact) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                if (c0 + e == G.tau) diag_s[G.tau] = x[e];  // dO_t . v_t
-                x[e] *= d.scale * gam[e];
+                for (int e = 0; e < 16; ++e) {
+                    if (c0 + e == G.tau) diag_s[G.tau] = x[e];  // dO_t . v_t
+                    x[e] = c0 + e < G.tau ? x[e] : 0.f;
+                }
+                store_row16(Ps, G.tau, c0, x);
+                scale_tile(Qs, Qh, gs.win, P * d.scale, G.tid);  // gamma's A operand
+                scale_tile(Ks, Ks, gs.nb, 1.f, G.tid);           // K^
+            } else {
+                float gam[16];
+                decay_row16(gs, G.tau, c0, true, gam);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    if (c0 + e == G.tau) diag_s[G.tau] = x[e];  // dO_t . v_t
+                    x[e] *= d.scale * gam[e];
+                }
+                store_row16(Ps, G.tau, c0, x);
+                copy_scaled_tile(Qs, Qh, P, G.tid);            // gamma's A operand
+                scale_tile(Ds, Ds, gs.win, d.scale, G.tid);     // dO~
+                scale_tile(Vs, Vs, gs.wout, 1.f, G.tid);        // V~
             }
-            store_row16(Ps, G.tau, c0, x);
-            copy_scaled_tile(Qs, Qh, P, G.tid);            // gamma's A operand
-            scale_tile(Ds, Ds, gs.win, d.scale, G.tid);     // dO~
-            scale_tile(Vs, Vs, gs.wout, 1.f, G.tid);        // V~
             P *= gs.W;
             fence_async_smem();
             tc_fence_before();
@@ -853,7 +912,10 @@ __global__ void __launch_bounds__(kRevThreads, 1)
             mbar_wait(obar, oph);  // this chunk's dq', dS and gamma products
             oph ^= 1;
             tc_fence_after();
-            const float cd = d.scale * diag_s[G.tau];
+            const bool fact = gs.fact != 0;
+            // factored: dq' = scale win_t acc and k_t = win_t k^_t
+            const float wr = fact ? d.scale * gs.win[G.tau] : 1.f;
+            const float cd = d.scale * diag_s[G.tau] * (fact ? gs.win[G.tau] : 1.f);
             float a = 0.f;
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
@@ -865,14 +927,18 @@ __global__ void __launch_bounds__(kRevThreads, 1)
                 tile_row_get16(Ks, G.tau, cc, kv);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
+                    x[e] *= wr;
                     a = fmaf(qv[e], x[e], a);
                     x[e] = fmaf(cd, kv[e], x[e]);
                 }
-                store_row16(Ds, G.tau, cc, x);  // dO~ is dead: stage dq there
+                store_row16(Ds, G.tau, cc, x);  // dO is dead: stage dq there
             }
             a += __shfl_xor_sync(kFull, a, 16);
             if (!G.hi) apart[c & 1][G.grp][G.tau] = a;
-            state_update(tmem, G, 256, gs.W, S, Sb);
+            if (fact)
+                state_update_scaled(tmem, G, 256, gs.W, S, Sb);
+            else
+                state_update(tmem, G, 256, gs.W, S, Sb);
             fence_async_smem();
             tc_fence_before();
         }
@@ -1273,11 +1339,12 @@ __device__ __forceinline__ float dg_scan(const GateSmem& gs, const float (*bp)[k
 //     at pv_ready, dv = PA^T dO + K~ E and dE = Q~^T dO at kq_ready, then
 //     the next chunk's scores.  Chunks without sequence starts and with
 //     moderate decays are "factored": their weights sit in the score masks,
-//     on dO and on the output rows, so V E^T and K E need no epilogue work
-//     and are issued as soon as the adjoint of the chunk after is in place.
+//     on dO and on the output rows, so V E^T and K E need no epilogue work:
+//     V E^T is issued as soon as the adjoint of the chunk after is in place,
+//     K E right behind the chunk's dk' products.
 //   warp 10 (one thread): the bulk stores of dk and dv, the refill of the
 //     stage with the chunk after next as its tiles die (Q, K, dO at
-//     dv_staged, V once the dk store has read it), and stg_free once the dv
+//     in_dead, V once the dk store has read it), and stg_free once the dv
 //     store has read the K~ tile.
 //   warp 9: the gate-gradient scan of a chunk once its b' rows are in, and
 //     the gate tables two chunks ahead.
@@ -1312,7 +1379,8 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
     __shared__ __align__(8) uint64_t b_ready[2];     // epilogue -> warp 9, by chunk parity
     __shared__ __align__(8) uint64_t scan_done[2];   // warp 9 -> epilogue (b' rows free)
     __shared__ __align__(8) uint64_t gate_ready[2];  // warp 9 -> epilogue (gate tables)
-    __shared__ __align__(8) uint64_t stg_free;       // warp 8 -> epilogue: dv store has read K~
+    __shared__ __align__(8) uint64_t stg_free;       // copy warp -> epilogue: dv store has read K~
+    __shared__ __align__(8) uint64_t in_dead;        // epilogue -> copy warp: Q, K, dO of the stage dead
     __shared__ uint32_t tmem_slot;
     __shared__ float diag_s[2][kChunk];  // dO_t . v_t by chunk parity
     __shared__ float bpart[2][2][kChunk];  // [chunk parity][column group][token]
@@ -1342,6 +1410,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
         mbar_init(smem_u32(&dk_staged), 8);
         mbar_init(smem_u32(&dv_staged), 8);
         mbar_init(smem_u32(&stg_free), 1);
+        mbar_init(smem_u32(&in_dead), 8);
         mbar_fence_init();
     }
     if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
@@ -1415,13 +1484,15 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             // dv = K E, use unscaled tiles and the adjoint of the chunk after
             // it: they are issued as soon as that adjoint is in the E tile,
             // ahead of the chunk's score masks.
-            auto issue_e_side = [&](int s) {
-                const uint32_t qa = smem_u32(smem + s * STAGE);
-                const uint32_t ka = qa + 2 * kTileBytes, va = qa + 4 * kTileBytes;
+            auto issue_ve = [&](int s) {  // dk' = V E^T
+                const uint32_t va = smem_u32(smem + s * STAGE) + 4 * kTileBytes;
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
                              sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, k > 0);
+            };
+            auto issue_ke = [&](int s) {  // dv = K E
+                const uint32_t ka = smem_u32(smem + s * STAGE) + 2 * kTileBytes;
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_bf16(tmem + 256, sdesc(ka + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
@@ -1433,7 +1504,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             // factored chunks keep K, Q and V unscaled (the weights sit in the
             // score masks, on dO and on the output rows)
             bool fact = gsb[0].fact != 0;
-            if (fact) issue_e_side(0);
+            if (fact) issue_ve(0);
             for (int it = 0; it < nch; ++it) {
                 const int s = it & 1;
                 const uint32_t ph = it & 1;
@@ -1452,6 +1523,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                                  sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, 1);
                 }
                 mma_commit(smem_u32(&dk_done));
+                if (fact) issue_ke(s);  // E-side of dv, behind the dk' products
                 mbar_wait(smem_u32(&kq_ready), ph);
                 tc_fence_after();
 #pragma unroll
@@ -1485,7 +1557,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                     fact = gsb[(it + 1) & 1].fact != 0;
                     if (fact) {
                         tc_fence_after();
-                        issue_e_side(s ^ 1);
+                        issue_ve(s ^ 1);
                     }
                 }
             }
@@ -1505,20 +1577,23 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 tma_store_3d(&mdk, smem_u32(Vs), 0, h, row);
                 tma_store_3d(&mdk, smem_u32(Vs + kTileBytes), 64, h, row);
                 bulk_commit();
-                // dv_staged: the output products are done and the dk rows have
+                // in_dead: the output products are done and the dk rows have
                 // read Q and K, so Q, K and dO of this stage are dead; V is
                 // dead once the dk store has read it
+                const int nrow = b * d.T + a0 + (nch - 3 - it) * kChunk;
+                const uint32_t fb = smem_u32(&full_bar[s]);
+                mbar_wait(smem_u32(&in_dead), ph);
+                if (it + 2 < nch) {
+                    mbar_expect_tx(fb, STAGE);
+                    load_tile(st, &mq, 0, 128, h, nrow, fb);
+                    load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, nrow, fb);
+                    load_tile(st + 6 * kTileBytes, &mdo, 0, DV, h, nrow, fb);
+                }
                 mbar_wait(smem_u32(&dv_staged), ph);
                 tma_store_3d(&mdv, kta, 0, h, row);
                 tma_store_3d(&mdv, kta + kTileBytes, 64, h, row);
                 bulk_commit();
                 if (it + 2 < nch) {
-                    const int nrow = b * d.T + a0 + (nch - 3 - it) * kChunk;
-                    const uint32_t fb = smem_u32(&full_bar[s]);
-                    mbar_expect_tx(fb, STAGE);
-                    load_tile(st, &mq, 0, 128, h, nrow, fb);
-                    load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, nrow, fb);
-                    load_tile(st + 6 * kTileBytes, &mdo, 0, DV, h, nrow, fb);
                     bulk_wait_read1();  // the dk store has read V's tile
                     load_tile(Vs, &mv, 0, DV, h, nrow, fb);
                 }
@@ -1662,6 +1737,8 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             // ---- E2: dv rows and the adjoint update
             mbar_wait(smem_u32(&dve_done), vph);
             vph ^= 1;
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&in_dead));  // after the dk rows and the products
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
