@@ -738,15 +738,25 @@ __device__ __forceinline__ void copy_scaled_tile(const uint8_t* src, uint8_t* ds
 }
 
 // ===========================================================================
-// forward sweep of the backward for Dv = 128, warp-specialised, with gamma:
-// dq, q.dq' per token, and gamma = sum_t (alpha_a..alpha_t) scale q_t dO_t^T
-// accumulated in tensor memory over the segment (one pass over q, k, v, dO).
-// Warps 0-7: epilogues; warp 8: TMA copies, MMAs, bulk stores; warp 9: gate
-// tables and the per-token q.dq' writes.  Two CTA-wide meetings per chunk
-// (S1: operands scaled; S2: outputs staged); the next chunk's dO V^T runs
-// right behind this chunk's output products.
+// forward sweep of the backward for Dv = 128: dq, q.dq' per token and
+// gamma = sum_t (alpha_a..alpha_t) scale q_t dO_t^T, accumulated in tensor
+// memory over the segment (one pass over q, k, v, dO).  Warp-specialised and
+// paced by mbarriers:
+//   warps 0-7 (epilogues), per chunk:
+//     E1  score mask P; K^ in place (factored) or dO~, V~ (general) -> p_ready
+//         gamma's copy of Q with its row weights                   -> q_ready
+//     E2  dq rows into their staging tile, q.dq' partials           -> dq_staged
+//         state update into the S tile                              -> in_dead, a_ready
+//   warp 8 (one thread): dq' = P K + dO S^T (in factored chunks dO S^T is
+//     issued as soon as the previous state is in the S tile), dS = K^T V,
+//     gamma += Qh^T dO, then the next chunk's dO V^T.
+//   warp 9: per-token q.dq' sums and the gate tables two chunks ahead.
+//   warp 10 (one thread): TMA loads (a stage is refilled once its chunk is
+//     done) and the dq stores.
+// Every barrier completes once per chunk (parity-indexed pairs once per two
+// chunks), and each waiter is paced so that it cannot fall a phase behind.
 // ===========================================================================
-__global__ void __launch_bounds__(kRevThreads, 1)
+__global__ void __launch_bounds__(kRev3Threads, 1)
     tc_dqg128_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                      const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdq,
@@ -754,91 +764,205 @@ __global__ void __launch_bounds__(kRevThreads, 1)
                      float* __restrict__ gamma, float* __restrict__ qdq) {
     constexpr uint32_t STAGE = 8 * kTileBytes;  // Q | K | V | dO
     constexpr uint32_t OFF_P = 2 * STAGE, OFF_S = OFF_P + kTileBytes;  // S tile 32 KB
-    constexpr uint32_t OFF_QH = OFF_S + 4 * kTileBytes;               // (prefix decay) Q
+    constexpr uint32_t OFF_QH = OFF_S + 4 * kTileBytes;               // gamma's Q
+    constexpr uint32_t OFF_DQ = OFF_QH + 2 * kTileBytes;              // dq staging
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint8_t* Ps = smem + OFF_P;
     uint8_t* Sb = smem + OFF_S;
     uint8_t* Qh = smem + OFF_QH;
+    uint8_t* DQ = smem + OFF_DQ;
     __shared__ GateSmem gsb[2];
     __shared__ __align__(8) uint64_t full_bar[2];
-    __shared__ __align__(8) uint64_t score_bar;  // one commit per chunk: dA = dO V^T
-    __shared__ __align__(8) uint64_t out_bar;    // one commit per chunk: dq', dS, gamma
+    __shared__ __align__(8) uint64_t score_bar, dq_done, st_done;          // tensor-core commits
+    __shared__ __align__(8) uint64_t p_ready, q_ready, dq_staged, in_dead;  // epilogue -> warps 8, 10
+    __shared__ __align__(8) uint64_t a_ready[2];     // epilogue -> warps 8, 9: chunk done
+    __shared__ __align__(8) uint64_t a_done[2];      // warp 9 -> epilogue: q.dq' partials read
+    __shared__ __align__(8) uint64_t gate_ready[2];  // warp 9 -> epilogue, warp 8: gate tables
+    __shared__ __align__(8) uint64_t stg_free;       // warp 10 -> epilogue: dq store has read DQ
     __shared__ uint32_t tmem_slot;
-    __shared__ float diag_s[kChunk];
+    __shared__ float diag_s[2][kChunk];  // dO_t . v_t by chunk parity
     __shared__ float apart[2][2][kChunk];  // [chunk parity][column group][token]
 
     const Geo G = geo();
     const bool epi = G.warp < 8;
     const bool ctl = G.warp == 8;
     const bool gat = G.warp == 9;
+    const bool cpy = G.warp == 10;
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
-    const uint32_t sbar = smem_u32(&score_bar), obar = smem_u32(&out_bar);
 
     if (G.tid == 0) {
-        mbar_init(smem_u32(&full_bar[0]), 1);
-        mbar_init(smem_u32(&full_bar[1]), 1);
-        mbar_init(sbar, 1);
-        mbar_init(obar, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&full_bar[i]), 1);
+            mbar_init(smem_u32(&a_ready[i]), 8);
+            mbar_init(smem_u32(&a_done[i]), 1);
+            mbar_init(smem_u32(&gate_ready[i]), 1);
+        }
+        mbar_init(smem_u32(&score_bar), 1);
+        mbar_init(smem_u32(&dq_done), 1);
+        mbar_init(smem_u32(&st_done), 1);
+        mbar_init(smem_u32(&p_ready), 8);
+        mbar_init(smem_u32(&q_ready), 8);
+        mbar_init(smem_u32(&dq_staged), 8);
+        mbar_init(smem_u32(&in_dead), 8);
+        mbar_init(smem_u32(&stg_free), 1);
         mbar_fence_init();
     }
     if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
-    auto issue = [&](int c, int s) {
-        const int row = b * d.T + a0 + c * kChunk;
-        const uint32_t bar = smem_u32(&full_bar[s]);
-        uint8_t* st = smem + s * STAGE;
-        mbar_expect_tx(bar, STAGE);
-        load_tile(st, &mq, 0, 128, h, row, bar);
-        load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
-        load_tile(st + 4 * kTileBytes, &mv, 0, 128, h, row, bar);
-        load_tile(st + 6 * kTileBytes, &mdo, 0, 128, h, row, bar);
-    };
     float S[64];
     GateRegs gr;
     if (epi) {
         load_state_rows<128>(S_in + sum_off(d, seg, b, h), G, S, Sb);
-    } else if (gat) {
+    } else if (gat) {  // gate tables of the first two chunks; registers for the third
         gr = gate_load(d, g, b, h, a0, G.lane);
         gate_prep(gr, &gsb[0], G.lane);
-        if (nch > 1) gr = gate_load(d, g, b, h, a0 + kChunk, G.lane);
+        if (nch > 1) {
+            gr = gate_load(d, g, b, h, a0 + kChunk, G.lane);
+            gate_prep(gr, &gsb[1], G.lane);
+        }
+        if (nch > 2) gr = gate_load(d, g, b, h, a0 + 2 * kChunk, G.lane);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    auto issue_scores = [&](int s) {  // dA = dO V^T of the chunk in stage s
-        const uint32_t st = smem_u32(smem + s * STAGE);
-        const uint32_t va = st + 4 * kTileBytes, da = st + 6 * kTileBytes;
-        constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
+
+    if (ctl) {
+        if (G.lane == 0) {
+            const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb), qh = smem_u32(Qh);
+            constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
+            constexpr uint32_t id_a = idesc_bf16(64, 128, 0, 1);
+            constexpr uint32_t id_b = idesc_bf16(64, 128, 0, 0);
+            constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
+            auto issue_scores = [&](int s) {  // dA = dO V^T of the chunk in stage s
+                const uint32_t st = smem_u32(smem + s * STAGE);
+                const uint32_t va = st + 4 * kTileBytes, da = st + 6 * kTileBytes;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
-            mma_bf16(tmem, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
+                    mma_bf16(tmem, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+                }
+                mma_commit(smem_u32(&score_bar));
+            };
+            // dq' (+)= dO S_prev^T: first in a factored chunk, after P K otherwise
+            auto issue_state_side = [&](int s, bool first) {
+                const uint32_t da = smem_u32(smem + s * STAGE) + 6 * kTileBytes;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16(tmem + 128, sdesc(da + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                             sdesc(sa + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_b,
+                             (first && k == 0) ? 0u : 1u);
+            };
+            mbar_wait(smem_u32(&full_bar[0]), 0);
+            tc_fence_after();
+            issue_scores(0);
+            bool fact = gsb[0].fact != 0;
+            if (fact) issue_state_side(0, true);
+            for (int c = 0; c < nch; ++c) {
+                const int s = c & 1;
+                const uint32_t ph = c & 1;
+                const uint32_t st = smem_u32(smem + s * STAGE);
+                const uint32_t ka = st + 2 * kTileBytes, va = st + 4 * kTileBytes, da = st + 6 * kTileBytes;
+                mbar_wait(smem_u32(&p_ready), ph);
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // dq' (+)= P K  (strictly causal part)
+                    mma_bf16(tmem + 128, sdesc(pa + k * 32, 16, 1024), sdesc(ka + k * 2048, kTileBytes, 1024),
+                             id_a, (fact || k > 0) ? 1u : 0u);
+                if (!fact) issue_state_side(s, false);
+                mma_commit(smem_u32(&dq_done));
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // dS = K^T V  (K^ or V~ carry the weights)
+                    mma_bf16(tmem + 256, sdesc(ka + k * 2048, kTileBytes, 1024),
+                             sdesc(va + k * 2048, kTileBytes, 1024), id_s, k > 0);
+                mbar_wait(smem_u32(&q_ready), ph);
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // gamma += Qh^T dO
+                    mma_bf16(tmem + 384, sdesc(qh + k * 2048, kTileBytes, 1024),
+                             sdesc(da + k * 2048, kTileBytes, 1024), id_s, (c > 0 || k > 0) ? 1u : 0u);
+                mma_commit(smem_u32(&st_done));
+                if (c + 1 < nch) {
+                    mbar_wait(smem_u32(&full_bar[s ^ 1]), ((c + 1) >> 1) & 1);
+                    tc_fence_after();
+                    issue_scores(s ^ 1);
+                    // the state after this chunk is in the S tile once its
+                    // epilogue is done: the next factored chunk's dO S^T
+                    mbar_wait(smem_u32(&a_ready[s]), (c >> 1) & 1);
+                    if (c + 1 >= 2) mbar_wait(smem_u32(&gate_ready[s ^ 1]), ((c - 1) >> 1) & 1);
+                    fact = gsb[s ^ 1].fact != 0;
+                    if (fact) {
+                        tc_fence_after();
+                        issue_state_side(s ^ 1, true);
+                    }
+                }
+            }
         }
-        mma_commit(sbar);
-    };
-    if (ctl && G.lane == 0) {
-        issue(0, 0);
-        if (nch > 1) issue(1, 1);
-        mbar_wait(smem_u32(&full_bar[0]), 0);
-        tc_fence_after();
-        issue_scores(0);
-    }
-    uint32_t sph = 0, oph = 0;
-    float P = 1.f;  // alpha product from the segment start to this chunk's start (epilogue warps)
-    for (int c = 0; c < nch; ++c) {
-        const int t0 = a0 + c * kChunk;
-        const int s = c & 1;
-        const GateSmem& gs = gsb[c & 1];
-        uint8_t* Qs = smem + s * STAGE;
-        uint8_t* Ks = Qs + 2 * kTileBytes;
-        uint8_t* Vs = Qs + 4 * kTileBytes;
-        uint8_t* Ds = Qs + 6 * kTileBytes;
-        if (epi) {
-            mbar_wait(sbar, sph);  // this chunk's dA
+    } else if (cpy) {
+        if (G.lane == 0) {
+            auto issue = [&](int c, int s) {
+                const int row = b * d.T + a0 + c * kChunk;
+                const uint32_t bar = smem_u32(&full_bar[s]);
+                uint8_t* st = smem + s * STAGE;
+                mbar_expect_tx(bar, STAGE);
+                load_tile(st, &mq, 0, 128, h, row, bar);
+                load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
+                load_tile(st + 4 * kTileBytes, &mv, 0, 128, h, row, bar);
+                load_tile(st + 6 * kTileBytes, &mdo, 0, 128, h, row, bar);
+            };
+            issue(0, 0);
+            if (nch > 1) issue(1, 1);
+            for (int c = 0; c < nch; ++c) {
+                const uint32_t ph = c & 1;
+                const int row = b * d.T + a0 + c * kChunk;
+                mbar_wait(smem_u32(&dq_staged), ph);
+                tma_store_3d(&mdq, smem_u32(DQ), 0, h, row);
+                tma_store_3d(&mdq, smem_u32(DQ + kTileBytes), 64, h, row);
+                bulk_commit();
+                mbar_wait(smem_u32(&in_dead), ph);  // every read of the chunk's stage is done
+                if (c + 2 < nch) issue(c + 2, c & 1);
+                bulk_wait_read();
+                mbar_arrive(smem_u32(&stg_free));
+            }
+            bulk_wait_all();
+        }
+    } else if (gat) {
+        for (int c = 0; c < nch; ++c) {
+            const int p = c & 1;
+            const int t0 = a0 + c * kChunk;
+            mbar_wait(smem_u32(&a_ready[p]), (c >> 1) & 1);
+            const int64_t base = ((int64_t)b * d.T + t0) * d.H + h;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = 2 * G.lane + u;
+                qdq[base + int64_t(t) * d.H] = apart[p][0][t] + apart[p][1][t];
+            }
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&a_done[p]));
+            if (c + 2 < nch) {  // the tables of chunk c + 2 replace this chunk's
+                gate_prep(gr, &gsb[p], G.lane);
+                if (c + 3 < nch) gr = gate_load(d, g, b, h, t0 + 3 * kChunk, G.lane);
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&gate_ready[p]));
+            }
+        }
+    } else {  // epilogue warps
+        uint32_t sph = 0, dph = 0, tph = 0;
+        float P = 1.f;  // alpha product from the segment start to this chunk's start
+        for (int c = 0; c < nch; ++c) {
+            const int s = c & 1;
+            const int p = c & 1;
+            const GateSmem& gs = gsb[p];
+            uint8_t* Qs = smem + s * STAGE;
+            uint8_t* Ks = Qs + 2 * kTileBytes;
+            uint8_t* Vs = Qs + 4 * kTileBytes;
+            uint8_t* Ds = Qs + 6 * kTileBytes;
+            // ---- E1
+            if (c >= 2) mbar_wait(smem_u32(&gate_ready[p]), ((c - 2) >> 1) & 1);
+            mbar_wait(smem_u32(&score_bar), sph);
             sph ^= 1;
             mbar_wait(smem_u32(&full_bar[s]), (c >> 1) & 1);
             tc_fence_after();
@@ -847,121 +971,98 @@ __global__ void __launch_bounds__(kRevThreads, 1)
             // (dO_t . v_s) k^_s + dO_t S_prev^T),  dS = W K^T^ V,  and gamma's
             // row weights go on its copy of Q; dO and V stay unscaled.
             const bool fact = gs.fact != 0;
-            float x[16];
-            tok16(tmem, G, 32 * G.grp, x);
-            const int c0 = 32 * G.grp + 16 * G.hi;
-            if (fact) {
+            {
+                float x[16];
+                tok16(tmem, G, 32 * G.grp, x);
+                const int c0 = 32 * G.grp + 16 * G.hi;
+                if (fact) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    if (c0 + e == G.tau) diag_s[G.tau] = x[e];  // dO_t . v_t
-                    x[e] = c0 + e < G.tau ? x[e] : 0.f;
+                    for (int e = 0; e < 16; ++e) {
+                        if (c0 + e == G.tau) diag_s[p][G.tau] = x[e];  // dO_t . v_t
+                        x[e] = c0 + e < G.tau ? x[e] : 0.f;
+                    }
+                } else {
+                    float gam[16];
+                    decay_row16(gs, G.tau, c0, true, gam);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        if (c0 + e == G.tau) diag_s[p][G.tau] = x[e];  // dO_t . v_t
+                        x[e] *= d.scale * gam[e];
+                    }
                 }
                 store_row16(Ps, G.tau, c0, x);
-                scale_tile(Qs, Qh, gs.win, P * d.scale, G.tid);  // gamma's A operand
-                scale_tile(Ks, Ks, gs.nb, 1.f, G.tid);           // K^
-            } else {
-                float gam[16];
-                decay_row16(gs, G.tau, c0, true, gam);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    if (c0 + e == G.tau) diag_s[G.tau] = x[e];  // dO_t . v_t
-                    x[e] *= d.scale * gam[e];
-                }
-                store_row16(Ps, G.tau, c0, x);
-                copy_scaled_tile(Qs, Qh, P, G.tid);            // gamma's A operand
-                scale_tile(Ds, Ds, gs.win, d.scale, G.tid);     // dO~
-                scale_tile(Vs, Vs, gs.wout, 1.f, G.tid);        // V~
             }
-            P *= gs.W;
+            if (fact) {
+                scale_tile(Ks, Ks, gs.nb, 1.f, G.tid);  // K^
+            } else {
+                scale_tile(Ds, Ds, gs.win, d.scale, G.tid);  // dO~
+                scale_tile(Vs, Vs, gs.wout, 1.f, G.tid);     // V~
+            }
             fence_async_smem();
             tc_fence_before();
-        }
-        __syncthreads();  // S1
-        if (ctl && G.lane == 0) {
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&p_ready));
+            if (fact)
+                scale_tile(Qs, Qh, gs.win, P * d.scale, G.tid);  // gamma's A operand
+            else
+                copy_scaled_tile(Qs, Qh, P, G.tid);
+            fence_async_smem();
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&q_ready));
+            P *= gs.W;
+            // ---- E2: dq rows
+            mbar_wait(smem_u32(&dq_done), dph);
+            dph ^= 1;
+            if (c >= 1) mbar_wait(smem_u32(&stg_free), (c - 1) & 1);      // DQ tile free
+            if (c >= 2) mbar_wait(smem_u32(&a_done[p]), ((c - 2) >> 1) & 1);  // apart[p] free
+            // diag_s of this chunk comes from the other warp of the quadrant:
+            // every epilogue warp arrived on p_ready after writing it
+            mbar_wait(smem_u32(&p_ready), c & 1);
             tc_fence_after();
-            const uint32_t ka = smem_u32(Ks), va = smem_u32(Vs), da = smem_u32(Ds);
-            const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb), qh = smem_u32(Qh);
-            constexpr uint32_t id_a = idesc_bf16(64, 128, 0, 1);
-            constexpr uint32_t id_b = idesc_bf16(64, 128, 0, 0);
-            constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
+            {
+                // factored: dq' = scale win_t acc and k_t = win_t k^_t
+                const float wr = fact ? d.scale * gs.win[G.tau] : 1.f;
+                const float cd = d.scale * diag_s[p][G.tau] * (fact ? gs.win[G.tau] : 1.f);
+                float a = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // dq' = P K  (strictly causal part)
-                mma_bf16(tmem + 128, sdesc(pa + k * 32, 16, 1024), sdesc(ka + k * 2048, kTileBytes, 1024),
-                         id_a, k > 0);
+                for (int k = 0; k < 2; ++k) {
+                    float x[16], qv[16], kv[16];
+                    const int col = 64 * G.grp + 32 * k;
+                    const int cc = col + 16 * G.hi;
+                    tok16(tmem, G, 128 + col, x);
+                    tile_row_get16(Qs, G.tau, cc, qv);
+                    tile_row_get16(Ks, G.tau, cc, kv);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)  // dq' += dO~ S_prev^T
-                mma_bf16(tmem + 128, sdesc(da + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                         sdesc(sa + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_b, 1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // dS = K^T V~
-                mma_bf16(tmem + 256, sdesc(ka + k * 2048, kTileBytes, 1024),
-                         sdesc(va + k * 2048, kTileBytes, 1024), id_s, k > 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // gamma += (P Q)^T dO~
-                mma_bf16(tmem + 384, sdesc(qh + k * 2048, kTileBytes, 1024),
-                         sdesc(da + k * 2048, kTileBytes, 1024), id_s, (c > 0 || k > 0) ? 1u : 0u);
-            mma_commit(obar);
-            if (c + 1 < nch) {
-                mbar_wait(smem_u32(&full_bar[s ^ 1]), ((c + 1) >> 1) & 1);
-                issue_scores(s ^ 1);
-            }
-        } else if (gat && c + 1 < nch) {
-            gate_prep(gr, &gsb[(c + 1) & 1], G.lane);
-            if (c + 2 < nch) gr = gate_load(d, g, b, h, t0 + 2 * kChunk, G.lane);
-        } else if (epi) {
-            mbar_wait(obar, oph);  // this chunk's dq', dS and gamma products
-            oph ^= 1;
-            tc_fence_after();
-            const bool fact = gs.fact != 0;
-            // factored: dq' = scale win_t acc and k_t = win_t k^_t
-            const float wr = fact ? d.scale * gs.win[G.tau] : 1.f;
-            const float cd = d.scale * diag_s[G.tau] * (fact ? gs.win[G.tau] : 1.f);
-            float a = 0.f;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                float x[16], qv[16], kv[16];
-                const int col = 64 * G.grp + 32 * k;
-                const int cc = col + 16 * G.hi;
-                tok16(tmem, G, 128 + col, x);
-                tile_row_get16(Qs, G.tau, cc, qv);
-                tile_row_get16(Ks, G.tau, cc, kv);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    x[e] *= wr;
-                    a = fmaf(qv[e], x[e], a);
-                    x[e] = fmaf(cd, kv[e], x[e]);
+                    for (int e = 0; e < 16; ++e) {
+                        x[e] *= wr;
+                        a = fmaf(qv[e], x[e], a);
+                        x[e] = fmaf(cd, kv[e], x[e]);
+                    }
+                    store_row16(DQ, G.tau, cc, x);
                 }
-                store_row16(Ds, G.tau, cc, x);  // dO is dead: stage dq there
+                a += __shfl_xor_sync(kFull, a, 16);
+                if (!G.hi) apart[p][G.grp][G.tau] = a;
             }
-            a += __shfl_xor_sync(kFull, a, 16);
-            if (!G.hi) apart[c & 1][G.grp][G.tau] = a;
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&dq_staged));
+            // ---- E2: state update
+            mbar_wait(smem_u32(&st_done), tph);
+            tph ^= 1;
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&in_dead));  // the stage's last reader is done
+            tc_fence_after();
             if (fact)
                 state_update_scaled(tmem, G, 256, gs.W, S, Sb);
             else
                 state_update(tmem, G, 256, gs.W, S, Sb);
             fence_async_smem();
             tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&a_ready[p]));
         }
-        __syncthreads();  // S2
-        if (ctl && G.lane == 0) {
-            const int row = b * d.T + t0;
-            tma_store_3d(&mdq, smem_u32(Ds), 0, h, row);
-            tma_store_3d(&mdq, smem_u32(Ds + kTileBytes), 64, h, row);
-            bulk_commit();
-            if (c + 2 < nch) {
-                bulk_wait_read();  // the staging tile is refilled by the next load
-                issue(c + 2, s);
-            }
-        } else if (gat) {
-            const int64_t base = ((int64_t)b * d.T + t0) * d.H + h;
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int t = 2 * G.lane + u;
-                qdq[base + int64_t(t) * d.H] = apart[c & 1][0][t] + apart[c & 1][1][t];
-            }
-        }
-    }
-    if (epi) {  // gamma rows (all products have completed: last out_bar wait)
+        // gamma rows (every product has completed: the last st_done wait)
         tc_fence_after();
         float* dst = gamma + sum_off(d, seg, b, h) + int64_t(G.srow) * 128 + 64 * G.grp;
         float v[64];
@@ -970,7 +1071,6 @@ __global__ void __launch_bounds__(kRevThreads, 1)
         for (int i = 0; i < 64; i += 4)
             *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     }
-    if (ctl && G.lane == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (G.warp == 0) tmem_dealloc(tmem, 512);
@@ -1823,8 +1923,8 @@ constexpr size_t kOuterSmem = 96 * 1024 + 1024;
 constexpr size_t kFwdSmem = 13 * kTileBytes + 1024;   // Q K V P (7 tiles) + S (4) + o staging (2)
 // Q K (4 tiles) + V dO (2 NV) + P (1) + S (2 NV)
 constexpr size_t dq_smem(int dv) { return size_t(5 + 4 * (dv / 64)) * kTileBytes + 1024; }
-// 2 stages x 8 + P (1) + S (4) + prefix-decayed Q (2)
-constexpr size_t kDqg128Smem = 23 * kTileBytes + 1024;
+// 2 stages x 8 + P (1) + S (4) + gamma's Q (2) + dq staging (2)
+constexpr size_t kDqg128Smem = 25 * kTileBytes + 1024;
 // stages x (4 + 2 NV) + Q~ K~ (4) + PA PdA (2) + E (2 NV): 26 tiles for Dv 128 and 256
 constexpr size_t rev_smem(int dv) {
     return size_t((dv == 128 ? 2 : 1) * (4 + 2 * (dv / 64)) + 6 + 2 * (dv / 64)) * kTileBytes + 1024;
@@ -1903,7 +2003,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             if (d.Dv == 128) {
                 auto fq = tc_dqg128_kernel;
                 if (!set_smem(fq, kDqg128Smem)) return RM_ERR_CUDA;
-                fq<<<grid, kRevThreads, kDqg128Smem, s>>>(d, mq, mk, mv, mdo, mdq, p.g, p.S_in, p.sum_out,
+                fq<<<grid, kRev3Threads, kDqg128Smem, s>>>(d, mq, mk, mv, mdo, mdq, p.g, p.S_in, p.sum_out,
                                                           p.ws_f32);
                 if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
                 note_launch(1);
