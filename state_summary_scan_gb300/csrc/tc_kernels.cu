@@ -89,6 +89,21 @@ __device__ __forceinline__ void tok16(uint32_t tmem, const Geo& g, int col, floa
     }
 }
 
+// tok16 of two column blocks with the two tensor-memory loads in flight together
+__device__ __forceinline__ void tok16x2(uint32_t tmem, const Geo& g, int col0, int col1, float* x0, float* x1) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32_nowait(tmem + g.tl + col0, r0);
+    tmem_ld32_nowait(tmem + g.tl + col1, r1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const float u0 = __shfl_sync(kFull, __uint_as_float(r0[16 + e]), (g.lane + 16) & 31);
+        const float u1 = __shfl_sync(kFull, __uint_as_float(r1[16 + e]), (g.lane + 16) & 31);
+        x0[e] = g.hi ? u0 : __uint_as_float(r0[e]);
+        x1[e] = g.hi ? u1 : __uint_as_float(r1[e]);
+    }
+}
+
 // Columns [64 grp, +64) of state row srow of an M = 128 accumulator at column col.
 __device__ __forceinline__ void state_cols64(uint32_t tmem, const Geo& g, int col, float* x) {
     uint32_t r0[32], r1[32];
@@ -137,6 +152,24 @@ __device__ __forceinline__ void state_update_scaled(uint32_t tmem, const Geo& g,
         for (int e = 0; e < 32; ++e) S[32 * hf + e] = W * (S[32 * hf + e] + y[e]);
     }
     store_state_half(tile, g.srow, g.grp, S);
+}
+
+// state_update_half with both 32-column loads in flight together
+__device__ __forceinline__ void state_update_half2(uint32_t tmem, const Geo& g, int col, int hh, float W,
+                                                   float* S, uint8_t* tile) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32_nowait(tmem + g.tl + col + 64 * g.grp, r0);
+    tmem_ld32_nowait(tmem + g.tl + col + 64 * g.grp + 32, r1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        S[64 * hh + e] = fmaf(W, S[64 * hh + e], __uint_as_float(r0[e]));
+        S[64 * hh + 32 + e] = fmaf(W, S[64 * hh + 32 + e], __uint_as_float(r1[e]));
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(tile + sw_chunk(128, g.srow, 16 * hh + 8 * g.grp + c)) =
+            pack8(S + 64 * hh + c * 8);
 }
 
 // State rows of width DV split over the two column groups: thread (srow, grp)
@@ -403,7 +436,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ uint32_t tmem_slot;
 
     const Geo G = geo();
-    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H, vb = blockIdx.z;
+    // the value blocks of one (segment, head) are adjacent in the grid, so
+    // they run together and the second one's q and k reads hit L2
+    const int nvb = d.Dv / 128;
+    const int seg = blockIdx.x / nvb, vb = blockIdx.x % nvb, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     const uint32_t fb = smem_u32(&full_bar), mb = smem_u32(&mma_bar);
@@ -1746,8 +1782,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 // dv = wout (Pa^T dO~ + K E) with Pa = e^(-b_63) A (s <= t);
                 // dE = Q^T dO~, dO~ = scale win dO
                 float xa[16], xd[16];
-                tok16(tmem, G, 32 * G.grp, xa);
-                tok16(tmem, G, 64 + 32 * G.grp, xd);
+                tok16x2(tmem, G, 32 * G.grp, 64 + 32 * G.grp, xa, xd);
                 const int c0 = 32 * G.grp + 16 * G.hi;
                 const float fd = d.scale * gs.ep[G.tau], fa = gs.emb;
 #pragma unroll
@@ -1770,8 +1805,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             } else {
                 {
                     float xa[16], xd[16], gam[16];
-                    tok16(tmem, G, 32 * G.grp, xa);
-                    tok16(tmem, G, 64 + 32 * G.grp, xd);
+                    tok16x2(tmem, G, 32 * G.grp, 64 + 32 * G.grp, xa, xd);
                     const int c0 = 32 * G.grp + 16 * G.hi;
                     decay_row16(gs, G.tau, c0, false, gam);
 #pragma unroll
@@ -1811,12 +1845,14 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 float bk = 0.f;
                 const float cd = d.scale * diag_s[p][G.tau];
                 const float wr = fact ? gs.wout[G.tau] : 1.f;
+                float xx[2][16];
+                tok16x2(tmem, G, 128 + 64 * G.grp, 128 + 64 * G.grp + 32, xx[0], xx[1]);
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    float x[16], qv[16], kv[16];
+                    float qv[16], kv[16];
+                    float* x = xx[k];
                     const int col = 64 * G.grp + 32 * k;
                     const int c0 = col + 16 * G.hi;
-                    tok16(tmem, G, 128 + col, x);
                     tile_row_get16(Qs, G.tau, c0, qv);
                     tile_row_get16(Ks, G.tau, c0, kv);
 #pragma unroll
@@ -1840,19 +1876,18 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             __syncwarp();
             if (G.lane == 0) mbar_arrive(smem_u32(&in_dead));  // after the dk rows and the products
             tc_fence_after();
+            {
+                float xx[2][16];
+                tok16x2(tmem, G, 256 + 64 * G.grp, 256 + 64 * G.grp + 32, xx[0], xx[1]);
+                const float wr = fact ? gs.wout[G.tau] : 1.f;
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                float x[16];
-                const int col = 64 * G.grp + 32 * k;
-                tok16(tmem, G, 256 + col, x);
-                if (fact) {
-                    const float wr = gs.wout[G.tau];
+                for (int k = 0; k < 2; ++k) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) x[e] *= wr;
+                    for (int e = 0; e < 16; ++e) xx[k][e] *= wr;
+                    store_row16(Kt, G.tau, 64 * G.grp + 32 * k + 16 * G.hi, xx[k]);  // K~ is dead: stage dv there
                 }
-                store_row16(Kt, G.tau, col + 16 * G.hi, x);  // K~ is dead: stage dv there
             }
-            state_update_half(tmem, G, 384, 0, gs.W, E, Eb);
+            state_update_half2(tmem, G, 384, 0, gs.W, E, Eb);
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -1988,7 +2023,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 !make_map(&mv, p.v, d, d.Dv) || !make_map(&mo, p.out0, d, d.Dv))
                 return RM_ERR_CUDA;
             if (!set_smem(tc_fwd_apply_kernel, kFwdSmem)) return RM_ERR_CUDA;
-            tc_fwd_apply_kernel<<<dim3(d.nseg, d.B * d.H, d.Dv / 128), kThreads, kFwdSmem, s>>>(
+            tc_fwd_apply_kernel<<<dim3(d.nseg * (d.Dv / 128), d.B * d.H), kThreads, kFwdSmem, s>>>(
                 d, mq, mk, mv, mo, p.g, p.S_in);
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(1);
