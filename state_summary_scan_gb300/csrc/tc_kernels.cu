@@ -10,8 +10,9 @@
 // state, W = whole-chunk decay), and the backward mirrors it.  Every product
 // above is a tcgen05.mma with bf16 operands in 128-byte-swizzled shared memory
 // (loaded by TMA) and fp32 accumulators in tensor memory; the fp32 master
-// state lives in registers, one state row per thread, and is re-quantised to
-// a bf16 shared-memory copy for the next chunk's products.
+// state lives in registers, one state row per thread (in tensor memory for
+// the Dv = 256 reverse sweep), and is re-quantised to a bf16 shared-memory
+// copy for the next chunk's products.
 //
 // Kernels (one CTA per (segment, row, head[, value block])):
 //   tc_outer_kernel     sum_t w_t x_t y_t^T over a segment: delta_S of
@@ -19,9 +20,12 @@
 //                       segment end) and gamma of cp_backward_prepare (x = q,
 //                       y = dO, w = scale * decay from the segment start)
 //   tc_fwd_apply_kernel the forward sweep from S_in: o
-//   tc_dq_kernel        the forward sweep of the backward: dq and, per token,
-//                       q.dq minus its same-token term (for the gate gradient)
-//   tc_rev_kernel       the reverse sweep from dS_out: dk, dv, dg
+//   tc_dqg128_kernel    the forward sweep of the backward for Dv = 128: dq,
+//                       per token q.dq minus its same-token term (for the
+//                       gate gradient), and gamma
+//   tc_dq_kernel        the same for Dv = 256, without gamma
+//   tc_rev128_kernel    the reverse sweep from dS_out: dk, dv, dg (Dv = 128)
+//   tc_rev256_kernel    the same for Dv = 256
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -1112,315 +1116,6 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
     if (G.warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// ===========================================================================
-// reverse sweep of the backward: dk, dv, dg for one (segment, row, head).
-// Dv = 256 processes dv and the adjoint update in two 128-column halves
-// (tensor memory holds one half at a time) and single-buffers its inputs.
-// ===========================================================================
-template <int DV>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_rev_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
-                  const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                  const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdk,
-                  const __grid_constant__ CUtensorMap mdv, const float* __restrict__ g,
-                  const float* __restrict__ S_in, const float* __restrict__ dS_out,
-                  const float* __restrict__ qdq, __nv_bfloat16* __restrict__ dk,
-                  __nv_bfloat16* __restrict__ dv, float* __restrict__ dg) {
-    // Dv = 128 stages dk and dv in the Q~ and K~ tiles (dead once the chunk's
-    // products are done) and writes them with bulk tensor stores; Dv = 256
-    // still needs those tiles for its second half and stores rows directly.
-    constexpr bool kStage = DV == 128;
-    constexpr int NV = DV / 64;
-    constexpr int NH = DV / 128;
-    constexpr int STAGES = DV == 128 ? 2 : 1;
-    constexpr uint32_t STAGE = (4 + 2 * NV) * kTileBytes;  // Q | K | V | dO
-    constexpr uint32_t OFF_QT = STAGES * STAGE, OFF_KT = OFF_QT + 2 * kTileBytes;
-    constexpr uint32_t OFF_PA = OFF_KT + 2 * kTileBytes, OFF_PD = OFF_PA + kTileBytes;
-    constexpr uint32_t OFF_E = OFF_PD + kTileBytes;  // E tile [128][DV]: 2 NV blocks
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = align1024(smem_raw);
-    uint8_t* Qt = smem + OFF_QT;
-    uint8_t* Kt = smem + OFF_KT;
-    uint8_t* PA = smem + OFF_PA;
-    uint8_t* PD = smem + OFF_PD;
-    uint8_t* Eb = smem + OFF_E;
-    __shared__ GateSmem gs;
-    __shared__ __align__(8) uint64_t full_bar[STAGES];
-    __shared__ __align__(8) uint64_t mma_bar;
-    __shared__ uint32_t tmem_slot;
-    __shared__ float diag_s[kChunk];
-    __shared__ float bpart[2][kChunk];
-    __shared__ float red[8];
-
-    const Geo G = geo();
-    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
-    const int nch = d.L / kChunk;
-    const int a0 = seg * d.L;
-    const uint32_t mb = smem_u32(&mma_bar);
-
-    if (G.tid == 0) {
-        for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
-        mbar_init(mb, 1);
-        mbar_fence_init();
-    }
-    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
-    // E (adjoint arriving at the last state of the current chunk) starts as
-    // dS_out; ext = <S_out, dS_out> with S_out read as S_in[seg+1]
-    float E[DV / 2];
-    load_state_rows<DV>(dS_out + sum_off(d, seg, b, h), G, E, Eb);
-    {
-        float ext = 0.f;
-        if (seg + 1 < d.nseg) {
-            const float* so = S_in + sum_off(d, seg + 1, b, h) + int64_t(G.srow) * DV + 64 * G.grp;
-#pragma unroll
-            for (int hh = 0; hh < NH; ++hh)
-#pragma unroll
-                for (int j = 0; j < 64; j += 4) {
-                    const float4 y = *reinterpret_cast<const float4*>(so + 128 * hh + j);
-                    ext = fmaf(E[64 * hh + j], y.x, ext);
-                    ext = fmaf(E[64 * hh + j + 1], y.y, ext);
-                    ext = fmaf(E[64 * hh + j + 2], y.z, ext);
-                    ext = fmaf(E[64 * hh + j + 3], y.w, ext);
-                }
-        }
-        ext = warp_sum(ext);
-        if (G.lane == 0) red[G.warp] = ext;
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // running gate-gradient sum carried from later chunks (held by warp 0)
-    float carry = 0.f;
-    if (G.warp == 0) {
-#pragma unroll
-        for (int w = 0; w < 8; ++w) carry += red[w];
-    }
-    const uint32_t tmem = tmem_slot;
-    auto issue = [&](int it, int s) {
-        const int c = nch - 1 - it;
-        const int row = b * d.T + a0 + c * kChunk;
-        const uint32_t bar = smem_u32(&full_bar[s]);
-        uint8_t* st = smem + s * STAGE;
-        mbar_expect_tx(bar, STAGE);
-        load_tile(st, &mq, 0, 128, h, row, bar);
-        load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
-        load_tile(st + 4 * kTileBytes, &mv, 0, DV, h, row, bar);
-        load_tile(st + (4 + NV) * kTileBytes, &mdo, 0, DV, h, row, bar);
-    };
-    if (G.tid == 0)
-        for (int it = 0; it < STAGES && it < nch; ++it) issue(it, it);
-    GateRegs gr;
-    if (G.warp == 0) gr = gate_load(d, g, b, h, a0 + (nch - 1) * kChunk, G.lane);
-    uint32_t mph = 0;
-    for (int it = 0; it < nch; ++it) {
-        const int c = nch - 1 - it;
-        const int t0 = a0 + c * kChunk;
-        const int s = it % STAGES;
-        uint8_t* Qs = smem + s * STAGE;
-        uint8_t* Ks = Qs + 2 * kTileBytes;
-        uint8_t* Vs = Qs + 4 * kTileBytes;
-        uint8_t* Ds = Qs + (4 + NV) * kTileBytes;
-        // warp 0 lane l scans tokens 63 - 2l and 62 - 2l; fetch their q.dq' early
-        float qd0 = 0.f, qd1 = 0.f;
-        if (G.warp == 0) {
-            gate_prep(gr, &gs, G.lane);
-            if (it + 1 < nch) gr = gate_load(d, g, b, h, t0 - kChunk, G.lane);
-            qd0 = __ldg(qdq + ((int64_t)b * d.T + t0 + 63 - 2 * G.lane) * d.H + h);
-            qd1 = __ldg(qdq + ((int64_t)b * d.T + t0 + 62 - 2 * G.lane) * d.H + h);
-        }
-        mbar_wait(smem_u32(&full_bar[s]), (it / STAGES) & 1);
-        __syncthreads();
-        const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks), va = smem_u32(Vs), da = smem_u32(Ds);
-        if (G.tid == 0) {
-            if (kStage) bulk_wait_read();  // last chunk's dk/dv have left the Q~/K~ tiles
-            tc_fence_after();
-            constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {  // A = Q K^T
-                const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
-                mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, k > 0);
-            }
-#pragma unroll
-            for (int k = 0; k < DV / 16; ++k) {  // dA = dO V^T
-                const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
-                mma_bf16(tmem + 64, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
-            }
-            mma_commit(mb);
-        }
-        mbar_wait(mb, mph);
-        mph ^= 1;
-        tc_fence_after();
-        {
-            float xa[16], xd[16], gam[16];
-            tok16(tmem, G, 32 * G.grp, xa);
-            tok16(tmem, G, 64 + 32 * G.grp, xd);
-            const int c0 = 32 * G.grp + 16 * G.hi;
-            decay_row16(gs, G.tau, c0, false, gam);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int sidx = c0 + e;
-                if (sidx == G.tau) diag_s[G.tau] = xd[e];  // dO_t . v_t
-                xa[e] *= d.scale * gam[e];
-                xd[e] = sidx < G.tau ? xd[e] * d.scale * gam[e] : 0.f;
-            }
-            store_row16(PA, G.tau, c0, xa);
-            store_row16(PD, G.tau, c0, xd);
-            // Q~ = scale win Q and K~ = wout K into their own tiles; V~ = wout V in place
-            scale_tile(Qs, Qt, gs.win, d.scale, G.tid);
-            scale_tile(Ks, Kt, gs.wout, 1.f, G.tid);
-#pragma unroll
-            for (int pr = 0; pr < NV / 2; ++pr) {
-                uint8_t* vp = Vs + 2 * pr * kTileBytes;
-                scale_tile(vp, vp, gs.wout, 1.f, G.tid);
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-#pragma unroll
-        for (int hh = 0; hh < NH; ++hh) {
-            if (G.tid == 0) {
-                tc_fence_after();
-                const uint32_t pa = smem_u32(PA), pd = smem_u32(PD), ea = smem_u32(Eb);
-                const uint32_t qta = smem_u32(Qt), kta = smem_u32(Kt);
-                constexpr uint32_t id_mm = idesc_bf16(64, 128, 1, 1);
-                constexpr uint32_t id_kk = idesc_bf16(64, 128, 0, 0);
-                constexpr uint32_t id_km = idesc_bf16(64, 128, 0, 1);
-                constexpr uint32_t id_e = idesc_bf16(128, 128, 1, 1);
-                if (hh == 0) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)  // dk' = PdA^T Q
-                        mma_bf16(tmem + 128, sdesc(pd + k * 2048, kTileBytes, 1024),
-                                 sdesc(qa + k * 2048, kTileBytes, 1024), id_mm, k > 0);
-#pragma unroll
-                    for (int k = 0; k < DV / 16; ++k)  // dk' += V~ E^T
-                        mma_bf16(tmem + 128,
-                                 sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                                 sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024),
-                                 id_kk, 1);
-                }
-                const uint32_t dah = da + 2 * hh * kTileBytes;      // dO columns [128 hh, +128)
-                const uint32_t eah = ea + 2 * hh * 2 * kTileBytes;  // E columns [128 hh, +128)
-#pragma unroll
-                for (int k = 0; k < 4; ++k)  // dv = PA^T dO
-                    mma_bf16(tmem + 256, sdesc(pa + k * 2048, kTileBytes, 1024),
-                             sdesc(dah + k * 2048, kTileBytes, 1024), id_mm, k > 0);
-#pragma unroll
-                for (int k = 0; k < 8; ++k)  // dv += K~ E
-                    mma_bf16(tmem + 256, sdesc(kta + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                             sdesc(eah + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)  // dE = Q~^T dO
-                    mma_bf16(tmem + 384, sdesc(qta + k * 2048, kTileBytes, 1024),
-                             sdesc(dah + k * 2048, kTileBytes, 1024), id_e, k > 0);
-                mma_commit(mb);
-            }
-            mbar_wait(mb, mph);
-            mph ^= 1;
-            // single-buffered inputs: once the last products of the chunk are
-            // done and the Q/K rows have been read, refill for the next chunk
-            if (STAGES == 1 && hh == NH - 1 && NH > 1 && G.tid == 0 && it + 1 < nch) issue(it + 1, 0);
-            tc_fence_after();
-            {
-                const int64_t tok = ((int64_t)b * d.T + t0 + G.tau) * d.H + h;
-                if (hh == 0) {
-                    const float cd = d.scale * diag_s[G.tau];
-                    float bk = 0.f;
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        float x[16], qv[16], kv[16];
-                        const int col = 64 * G.grp + 32 * k;
-                        const int c0 = col + 16 * G.hi;
-                        tok16(tmem, G, 128 + col, x);
-                        tile_row_get16(Qs, G.tau, c0, qv);
-                        tile_row_get16(Ks, G.tau, c0, kv);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            bk = fmaf(kv[e], x[e], bk);
-                            x[e] = fmaf(cd, qv[e], x[e]);
-                        }
-                        if (kStage)
-                            store_row16(Qt, G.tau, c0, x);
-                        else
-                            store_bf16x16(dk + tok * 128 + c0, x);
-                    }
-                    bk += __shfl_xor_sync(kFull, bk, 16);
-                    if (!G.hi) bpart[G.grp][G.tau] = bk;
-                }
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    float x[16];
-                    const int col = 64 * G.grp + 32 * k;
-                    tok16(tmem, G, 256 + col, x);
-                    if (kStage)
-                        store_row16(Kt, G.tau, col + 16 * G.hi, x);
-                    else
-                        store_bf16x16(dv + tok * DV + 128 * hh + col + 16 * G.hi, x);
-                }
-                state_update_half(tmem, G, 384, hh, gs.W, E, Eb);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-        }
-        if (G.warp == 0) {
-            // gate gradient of the chunk: reverse running sums of q.dq' - k.dk'
-            // restarting where a sequence starts, plus the carry from later
-            // chunks for the sequence open at the chunk's end.  Lane l holds
-            // tokens 63 - 2l and 62 - 2l; a segmented warp scan runs over the
-            // lanes in that (reverse) order.
-            const int tA = 63 - 2 * G.lane, tB = 62 - 2 * G.lane;
-            const float cA = qd0 - (bpart[0][tA] + bpart[1][tA]);
-            const float cB = qd1 - (bpart[0][tB] + bpart[1][tB]);
-            // head: token t + 1 starts a sequence, so t begins a new reverse run
-            const bool hA = tA < 63 && gs.lid[tA + 1] != gs.lid[tA];
-            const bool hB = gs.lid[tB + 1] != gs.lid[tB];
-            float v = hB ? cB : cA + cB;  // pair summary
-            bool f = hA || hB;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float vp = __shfl_up_sync(kFull, v, o);
-                const bool fp = __shfl_up_sync(kFull, f, o);
-                if (G.lane >= o) {
-                    if (!f) v += vp;
-                    f = f || fp;
-                }
-            }
-            // exclusive prefix for this lane, with the carry as the leftmost element
-            float vx = __shfl_up_sync(kFull, v, 1);
-            bool fx = __shfl_up_sync(kFull, f, 1);
-            if (G.lane == 0) {
-                vx = 0.f;
-                fx = false;
-            }
-            const float X = fx ? vx : carry + vx;
-            const float sA = cA + (hA ? 0.f : X);
-            const float sB = cB + (hB ? 0.f : sA);
-            const bool stA = gs.lid[tA] != gs.lid[tA - 1];  // tA >= 1
-            const bool stB = tB == 0 ? gs.first != 0 : gs.lid[tB] != gs.lid[tB - 1];
-            dg[((int64_t)b * d.T + t0 + tA) * d.H + h] = stA ? 0.f : sA;
-            dg[((int64_t)b * d.T + t0 + tB) * d.H + h] = stB ? 0.f : sB;
-            const float last = __shfl_sync(kFull, sB, 31);  // value at token 0
-            carry = gs.first ? 0.f : last;
-            if (kStage && G.tid == 0) {
-                const int row = b * d.T + t0;
-                tma_store_3d(&mdk, smem_u32(Qt), 0, h, row);
-                tma_store_3d(&mdk, smem_u32(Qt + kTileBytes), 64, h, row);
-                tma_store_3d(&mdv, smem_u32(Kt), 0, h, row);
-                tma_store_3d(&mdv, smem_u32(Kt + kTileBytes), 64, h, row);
-                bulk_commit();
-            }
-            if (STAGES == 2 && G.tid == 0 && it + 2 < nch) issue(it + 2, s);
-            if (STAGES == 1 && NH == 1 && G.tid == 0 && it + 1 < nch) issue(it + 1, 0);
-        }
-    }
-    if (G.tid == 0) bulk_wait_all();
-    tc_fence_before();
-    __syncthreads();
-    if (G.warp == 0) tmem_dealloc(tmem, 512);
-}
-
 // Gate gradient of one chunk (warp 0): reverse running sums of q.dq' - k.dk'
 // that restart where a sequence starts, plus the carry from later chunks for
 // the sequence open at the chunk's end.  Lane l holds tokens 63 - 2l and
@@ -1902,6 +1597,448 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
     if (G.warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// ===========================================================================
+// reverse sweep for Dv = 256, warp-specialised like the Dv = 128 sweep.  At
+// Dv = 256 the fp32 adjoint E (128 x 256) would take 128 registers a thread,
+// so it lives in tensor memory instead, where dE = Q~^T dO accumulates into
+// it; the epilogue scales it by W before each chunk's dE and snapshots it to
+// the bf16 E tile that the next chunk's products read.
+// Tensor memory: [0,128) the scores, then dv for one 128-column half at a
+// time; [128,256) dk'; [256,512) E.
+// Shared memory: Q|K by chunk parity (2 x 32 KB), V and dO (32 KB each,
+// refilled as soon as their last reader is done), E as bf16 (64 KB), PA, PD.
+//   warps 0-7 (epilogues), per chunk:
+//     E1  score masks; factored: dO~ in place, E *= W  -> pv_ready, kq_ready
+//                      general: V~ in place           -> pv_ready
+//     E2  dk rows                                     -> v_dead
+//         general: K~, Q~ in place, E *= W            -> kq_ready
+//         dv rows of half 0                           -> dv0_read
+//         dv rows of half 1                           -> in_dead, dv1_read
+//         E snapshot                                  -> e_ready, b_ready
+//   warp 8 (one thread): the tensor products; in factored chunks V E^T and
+//     K E need no epilogue work, V E^T is issued as soon as E is in place.
+//   warp 9: the gate-gradient scan and the gate tables two chunks ahead.
+//   warp 10 (one thread): V, dO and Q|K loads as the tiles die.
+// ===========================================================================
+__global__ void __launch_bounds__(kRev3Threads, 1)
+    tc_rev256_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                     const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                     const __grid_constant__ CUtensorMap mdo, const float* __restrict__ g,
+                     const float* __restrict__ S_in, const float* __restrict__ dS_out,
+                     const float* __restrict__ qdq, __nv_bfloat16* __restrict__ dk,
+                     __nv_bfloat16* __restrict__ dv, float* __restrict__ dg) {
+    constexpr int DV = 256;
+    constexpr uint32_t QKB = 4 * kTileBytes;  // Q | K
+    constexpr uint32_t OFF_V = 2 * QKB, OFF_D = OFF_V + 4 * kTileBytes, OFF_E = OFF_D + 4 * kTileBytes;
+    constexpr uint32_t OFF_PA = OFF_E + 8 * kTileBytes, OFF_PD = OFF_PA + kTileBytes;
+    constexpr uint32_t TE = 256;  // tensor-memory column of E
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint8_t* Vs = smem + OFF_V;
+    uint8_t* Ds = smem + OFF_D;
+    uint8_t* Eb = smem + OFF_E;
+    uint8_t* PA = smem + OFF_PA;
+    uint8_t* PD = smem + OFF_PD;
+    __shared__ GateSmem gsb[2];
+    __shared__ __align__(8) uint64_t qk_full[2], v_full, d_full;
+    __shared__ __align__(8) uint64_t score_bar, dk_done, dv0_done, dv1_done;  // tensor-core commits
+    __shared__ __align__(8) uint64_t pv_ready, kq_ready, dv0_read, dv1_read, e_ready;  // epilogue -> warp 8
+    __shared__ __align__(8) uint64_t v_dead, in_dead;  // epilogue -> warp 10
+    __shared__ __align__(8) uint64_t b_ready[2], scan_done[2], gate_ready[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ float diag_s[2][kChunk];
+    __shared__ float bpart[2][2][kChunk];
+    __shared__ float red[8];
+
+    const Geo G = geo();
+    const bool epi = G.warp < 8;
+    const bool ctl = G.warp == 8;
+    const bool scn = G.warp == 9;
+    const bool cpy = G.warp == 10;
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+
+    if (G.tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&qk_full[i]), 1);
+            mbar_init(smem_u32(&b_ready[i]), 8);
+            mbar_init(smem_u32(&scan_done[i]), 1);
+            mbar_init(smem_u32(&gate_ready[i]), 1);
+        }
+        mbar_init(smem_u32(&v_full), 1);
+        mbar_init(smem_u32(&d_full), 1);
+        mbar_init(smem_u32(&score_bar), 1);
+        mbar_init(smem_u32(&dk_done), 1);
+        mbar_init(smem_u32(&dv0_done), 1);
+        mbar_init(smem_u32(&dv1_done), 1);
+        for (uint64_t* bar : {&pv_ready, &kq_ready, &dv0_read, &dv1_read, &e_ready, &v_dead, &in_dead})
+            mbar_init(smem_u32(bar), 8);
+        mbar_fence_init();
+    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
+    GateRegs gr;
+    if (scn) {  // gate tables of the first two chunks; registers for the third
+        gr = gate_load(d, g, b, h, a0 + (nch - 1) * kChunk, G.lane);
+        gate_prep(gr, &gsb[0], G.lane);
+        if (nch > 1) {
+            gr = gate_load(d, g, b, h, a0 + (nch - 2) * kChunk, G.lane);
+            gate_prep(gr, &gsb[1], G.lane);
+        }
+        if (nch > 2) gr = gate_load(d, g, b, h, a0 + (nch - 3) * kChunk, G.lane);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (epi) {
+        // E starts as dS_out: into tensor memory and the bf16 tile; thread
+        // (srow, grp) owns columns [128 grp, +128).  ext = <S_out, dS_out>,
+        // S_out read as S_in[seg + 1].
+        const float* src = dS_out + sum_off(d, seg, b, h) + int64_t(G.srow) * DV + 128 * G.grp;
+        const float* so = S_in + sum_off(d, seg + 1, b, h) + int64_t(G.srow) * DV + 128 * G.grp;
+        float ext = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src + 32 * j + i);
+                r[i] = __float_as_uint(x.x); r[i + 1] = __float_as_uint(x.y);
+                r[i + 2] = __float_as_uint(x.z); r[i + 3] = __float_as_uint(x.w);
+                if (seg + 1 < d.nseg) {
+                    const float4 y = *reinterpret_cast<const float4*>(so + 32 * j + i);
+                    ext = fmaf(x.x, y.x, ext); ext = fmaf(x.y, y.y, ext);
+                    ext = fmaf(x.z, y.z, ext); ext = fmaf(x.w, y.w, ext);
+                }
+            }
+            tmem_st32(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(Eb + sw_chunk(128, G.srow, 16 * G.grp + 4 * j + c)) = pack8(f + 8 * c);
+        }
+        tmem_wait_st();
+        ext = warp_sum(ext);
+        if (G.lane == 0) red[G.warp] = ext;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (ctl) {
+        if (G.lane == 0) {
+            const uint32_t pa = smem_u32(PA), pd = smem_u32(PD), ea = smem_u32(Eb);
+            const uint32_t va = smem_u32(Vs), da = smem_u32(Ds);
+            constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
+            constexpr uint32_t id_mm = idesc_bf16(64, 128, 1, 1);
+            constexpr uint32_t id_kk = idesc_bf16(64, 128, 0, 0);
+            constexpr uint32_t id_km = idesc_bf16(64, 128, 0, 1);
+            constexpr uint32_t id_e = idesc_bf16(128, 256, 1, 1);
+            auto issue_scores = [&](int p) {  // A = Q K^T, dA = dO V^T
+                const uint32_t qa = smem_u32(smem + p * QKB), ka = qa + 2 * kTileBytes;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
+                    mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
+                    mma_bf16(tmem + 64, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+                }
+                mma_commit(smem_u32(&score_bar));
+            };
+            auto issue_ve = [&](bool first) {  // dk' (+)= V E^T
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                             sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk,
+                             (first && k == 0) ? 0u : 1u);
+            };
+            auto issue_dv = [&](int hh, uint32_t kx, bool fact) {  // dv_hh = PA^T dO_hh + K E_hh
+                const uint32_t dah = da + 2 * hh * kTileBytes, eah = ea + 4 * hh * kTileBytes;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(tmem, sdesc(pa + k * 2048, kTileBytes, 1024), sdesc(dah + k * 2048, kTileBytes, 1024),
+                             id_mm, k > 0);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16(tmem, sdesc(kx + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                             sdesc(eah + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
+                (void)fact;
+            };
+            mbar_wait(smem_u32(&qk_full[0]), 0);
+            mbar_wait(smem_u32(&v_full), 0);
+            mbar_wait(smem_u32(&d_full), 0);
+            tc_fence_after();
+            issue_scores(0);
+            bool fact = gsb[0].fact != 0;
+            if (fact) issue_ve(true);
+            for (int it = 0; it < nch; ++it) {
+                const int p = it & 1;
+                const uint32_t ph = it & 1;
+                const uint32_t qa = smem_u32(smem + p * QKB), ka = qa + 2 * kTileBytes;
+                mbar_wait(smem_u32(&pv_ready), ph);
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // dk' (+)= PdA^T Q
+                    mma_bf16(tmem + 128, sdesc(pd + k * 2048, kTileBytes, 1024),
+                             sdesc(qa + k * 2048, kTileBytes, 1024), id_mm, (fact || k > 0) ? 1u : 0u);
+                if (!fact) issue_ve(false);  // V~ E^T
+                mma_commit(smem_u32(&dk_done));
+                mbar_wait(smem_u32(&kq_ready), ph);  // dO~ or K~, Q~ in place; E scaled by W
+                tc_fence_after();
+                issue_dv(0, ka, fact);
+                mma_commit(smem_u32(&dv0_done));
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // E += Q~^T dO (all 256 columns)
+                    mma_bf16(tmem + TE, sdesc(qa + k * 2048, kTileBytes, 1024), sdesc(da + k * 2048, kTileBytes, 1024),
+                             id_e, 1u);
+                mbar_wait(smem_u32(&dv0_read), ph);
+                tc_fence_after();
+                issue_dv(1, ka, fact);
+                mma_commit(smem_u32(&dv1_done));
+                if (it + 1 < nch) {
+                    mbar_wait(smem_u32(&dv1_read), ph);
+                    mbar_wait(smem_u32(&qk_full[p ^ 1]), ((it + 1) >> 1) & 1);
+                    mbar_wait(smem_u32(&v_full), (it + 1) & 1);
+                    mbar_wait(smem_u32(&d_full), (it + 1) & 1);
+                    tc_fence_after();
+                    issue_scores(p ^ 1);
+                    // E of the chunk before is in the bf16 tile: the next chunk's V E^T
+                    mbar_wait(smem_u32(&e_ready), ph);
+                    if (it + 1 >= 2) mbar_wait(smem_u32(&gate_ready[p ^ 1]), ((it - 1) >> 1) & 1);
+                    fact = gsb[p ^ 1].fact != 0;
+                    if (fact) {
+                        tc_fence_after();
+                        issue_ve(true);
+                    }
+                }
+            }
+        }
+    } else if (cpy) {
+        if (G.lane == 0) {
+            auto load_qk = [&](int it, int p) {
+                const int row = b * d.T + a0 + (nch - 1 - it) * kChunk;
+                const uint32_t bar = smem_u32(&qk_full[p]);
+                uint8_t* st = smem + p * QKB;
+                mbar_expect_tx(bar, QKB);
+                load_tile(st, &mq, 0, 128, h, row, bar);
+                load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
+            };
+            auto load_one = [&](int it, uint8_t* dst, const CUtensorMap* map, uint64_t* barp) {
+                const int row = b * d.T + a0 + (nch - 1 - it) * kChunk;
+                const uint32_t bar = smem_u32(barp);
+                mbar_expect_tx(bar, 4 * kTileBytes);
+                load_tile(dst, map, 0, DV, h, row, bar);
+            };
+            load_qk(0, 0);
+            load_one(0, Vs, &mv, &v_full);
+            load_one(0, Ds, &mdo, &d_full);
+            if (nch > 1) load_qk(1, 1);
+            for (int it = 0; it + 1 < nch; ++it) {
+                const uint32_t ph = it & 1;
+                mbar_wait(smem_u32(&v_dead), ph);  // dk' and the scores are done with V
+                load_one(it + 1, Vs, &mv, &v_full);
+                mbar_wait(smem_u32(&in_dead), ph);  // the chunk's last products are done
+                load_one(it + 1, Ds, &mdo, &d_full);
+                if (it + 2 < nch) load_qk(it + 2, it & 1);
+            }
+        }
+    } else if (scn) {
+        float carry = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) carry += red[w];
+        for (int it = 0; it < nch; ++it) {
+            const int c = nch - 1 - it;
+            const int t0 = a0 + c * kChunk;
+            const int p = it & 1;
+            const float qd0 = __ldg(qdq + ((int64_t)b * d.T + t0 + 63 - 2 * G.lane) * d.H + h);
+            const float qd1 = __ldg(qdq + ((int64_t)b * d.T + t0 + 62 - 2 * G.lane) * d.H + h);
+            mbar_wait(smem_u32(&b_ready[p]), (it >> 1) & 1);
+            carry = dg_scan(gsb[p], bpart[p], qd0, qd1, carry, G.lane,
+                            dg + ((int64_t)b * d.T + t0) * d.H + h, d.H);
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&scan_done[p]));
+            if (it + 2 < nch) {
+                gate_prep(gr, &gsb[p], G.lane);
+                if (it + 3 < nch) gr = gate_load(d, g, b, h, t0 - 3 * kChunk, G.lane);
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&gate_ready[p]));
+            }
+        }
+    } else {  // epilogue warps
+        uint32_t sph = 0, kph = 0, v0ph = 0, v1ph = 0;
+        // E *= W for this thread's 128 columns of the tensor-memory adjoint
+        auto scale_e = [&](float W) {
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+                tmem_ld32_nowait(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(W * __uint_as_float(r[i]));
+                tmem_st32(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
+            }
+            tmem_wait_st();
+        };
+        for (int it = 0; it < nch; ++it) {
+            const int c = nch - 1 - it;
+            const int t0 = a0 + c * kChunk;
+            const int p = it & 1;
+            const GateSmem& gs = gsb[p];
+            uint8_t* Qs = smem + p * QKB;
+            uint8_t* Ks = Qs + 2 * kTileBytes;
+            const int64_t tok = ((int64_t)b * d.T + t0 + G.tau) * d.H + h;
+            // ---- E1
+            if (it >= 2) mbar_wait(smem_u32(&gate_ready[p]), ((it - 2) >> 1) & 1);
+            mbar_wait(smem_u32(&score_bar), sph);
+            sph ^= 1;
+            mbar_wait(smem_u32(&qk_full[p]), (it >> 1) & 1);
+            mbar_wait(smem_u32(&v_full), it & 1);
+            mbar_wait(smem_u32(&d_full), it & 1);
+            tc_fence_after();
+            const bool fact = gs.fact != 0;
+            {
+                float xa[16], xd[16];
+                tok16x2(tmem, G, 32 * G.grp, 64 + 32 * G.grp, xa, xd);
+                const int c0 = 32 * G.grp + 16 * G.hi;
+                if (fact) {
+                    // dk = wout (Pd^T Q + V E^T) with Pd = scale ep_t dA (s < t);
+                    // dv = wout (Pa^T dO~ + K E) with Pa = e^(-b_63) A (s <= t);
+                    // dE = Q^T dO~, dO~ = scale win dO
+                    const float fd = d.scale * gs.ep[G.tau], fa = gs.emb;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int sidx = c0 + e;
+                        if (sidx == G.tau) diag_s[p][G.tau] = xd[e];  // dO_t . v_t
+                        xa[e] = sidx <= G.tau ? xa[e] * fa : 0.f;
+                        xd[e] = sidx < G.tau ? xd[e] * fd : 0.f;
+                    }
+                } else {
+                    float gam[16];
+                    decay_row16(gs, G.tau, c0, false, gam);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int sidx = c0 + e;
+                        if (sidx == G.tau) diag_s[p][G.tau] = xd[e];  // dO_t . v_t
+                        xa[e] *= d.scale * gam[e];
+                        xd[e] = sidx < G.tau ? xd[e] * d.scale * gam[e] : 0.f;
+                    }
+                }
+                store_row16(PA, G.tau, c0, xa);
+                store_row16(PD, G.tau, c0, xd);
+            }
+            if (!fact) {  // V~ = wout V in place
+                scale_tile(Vs, Vs, gs.wout, 1.f, G.tid);
+                scale_tile(Vs + 2 * kTileBytes, Vs + 2 * kTileBytes, gs.wout, 1.f, G.tid);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&pv_ready));
+            if (fact) {
+                scale_tile(Ds, Ds, gs.win, d.scale, G.tid);
+                scale_tile(Ds + 2 * kTileBytes, Ds + 2 * kTileBytes, gs.win, d.scale, G.tid);
+                scale_e(gs.W);
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&kq_ready));
+            }
+            // ---- E2: dk rows
+            mbar_wait(smem_u32(&dk_done), kph);
+            kph ^= 1;
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&v_dead));
+            if (it >= 2) mbar_wait(smem_u32(&scan_done[p]), ((it - 2) >> 1) & 1);
+            mbar_wait(smem_u32(&pv_ready), it & 1);  // diag_s from the other warp of the quadrant
+            tc_fence_after();
+            const float wr = fact ? gs.wout[G.tau] : 1.f;
+            {
+                float bk = 0.f;
+                const float cd = d.scale * diag_s[p][G.tau];
+                float xx[2][16];
+                tok16x2(tmem, G, 128 + 64 * G.grp, 128 + 64 * G.grp + 32, xx[0], xx[1]);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    float qv[16], kv[16];
+                    float* x = xx[k];
+                    const int c0 = 64 * G.grp + 32 * k + 16 * G.hi;
+                    tile_row_get16(Qs, G.tau, c0, qv);
+                    tile_row_get16(Ks, G.tau, c0, kv);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        x[e] *= wr;
+                        bk = fmaf(kv[e], x[e], bk);
+                        x[e] = fmaf(cd, qv[e], x[e]);
+                    }
+                    store_bf16x16(dk + tok * 128 + c0, x);
+                }
+                bk += __shfl_xor_sync(kFull, bk, 16);
+                if (!G.hi) bpart[p][G.grp][G.tau] = bk;
+            }
+            if (!fact) {
+                // K~ = wout K and Q~ = scale win Q in place, once every epilogue
+                // warp has read its q, k rows
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                scale_tile(Ks, Ks, gs.wout, 1.f, G.tid);
+                scale_tile(Qs, Qs, gs.win, d.scale, G.tid);
+                scale_e(gs.W);
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&kq_ready));
+            }
+            // ---- E2: dv rows, half 0 then half 1
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                mbar_wait(smem_u32(hh == 0 ? &dv0_done : &dv1_done), hh == 0 ? v0ph : v1ph);
+                if (hh == 0) v0ph ^= 1; else v1ph ^= 1;
+                tc_fence_after();
+                if (hh == 1) {
+                    __syncwarp();
+                    if (G.lane == 0) mbar_arrive(smem_u32(&in_dead));
+                }
+                float xx[2][16];
+                tok16x2(tmem, G, 64 * G.grp, 64 * G.grp + 32, xx[0], xx[1]);
+                tc_fence_before();
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(hh == 0 ? &dv0_read : &dv1_read));
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) xx[k][e] *= wr;
+                    store_bf16x16(dv + tok * DV + 128 * hh + 64 * G.grp + 32 * k + 16 * G.hi, xx[k]);
+                }
+            }
+            // ---- E2: E snapshot (the chunk's products are done with the E tile)
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+                float f[32];
+                tmem_ld32(tmem + G.tl + TE + 128 * G.grp + 32 * j, f);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4*>(Eb + sw_chunk(128, G.srow, 16 * G.grp + 4 * j + cc)) = pack8(f + 8 * cc);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) {
+                mbar_arrive(smem_u32(&e_ready));
+                mbar_arrive(smem_u32(&b_ready[p]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // Failure-detection self test: waits on an mbarrier that nothing arrives on,
 // with the given bound, so that the timeout path and its host-side status can
 // be exercised without faulting or hanging the device.
@@ -2069,10 +2206,10 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 fr<<<grid, kRev3Threads, rev_smem(128), s>>>(d, mq, mk, mv, mdo, mdk, mdv, p.g, p.S_in, p.dS_out,
                                                           p.ws_f32, p.dg);
             } else {
-                auto fr = tc_rev_kernel<256>;
+                auto fr = tc_rev256_kernel;
                 if (!set_smem(fr, rev_smem(256))) return RM_ERR_CUDA;
-                fr<<<grid, kThreads, rev_smem(256), s>>>(d, mq, mk, mv, mdo, mdk, mdv, p.g, p.S_in, p.dS_out,
-                                                          p.ws_f32, dko, dvo, p.dg);
+                fr<<<grid, kRev3Threads, rev_smem(256), s>>>(d, mq, mk, mv, mdo, p.g, p.S_in, p.dS_out,
+                                                             p.ws_f32, dko, dvo, p.dg);
             }
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(1);
