@@ -23,7 +23,7 @@
 //   tc_dqg128_kernel    the forward sweep of the backward for Dv = 128: dq,
 //                       per token q.dq minus its same-token term (for the
 //                       gate gradient), and gamma
-//   tc_dq_kernel        the same for Dv = 256, without gamma
+//   tc_dq256_kernel     the same for Dv = 256, without gamma
 //   tc_rev128_kernel    the reverse sweep from dS_out: dk, dv, dg (Dv = 128)
 //   tc_rev256_kernel    the same for Dv = 256
 #include <cudaTypedefs.h>
@@ -593,178 +593,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (G.tid == 0) bulk_wait_all();
     if (G.warp == 0) tmem_dealloc(tmem, 256);
-}
-
-// ===========================================================================
-// forward sweep of the backward: dq and q.dq' for one (segment, row, head)
-// ===========================================================================
-template <int DV>
-__global__ void __launch_bounds__(kThreads, DV == 128 ? 2 : 1)
-    tc_dq_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
-                 const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                 const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdq,
-                 const float* __restrict__ g, const float* __restrict__ S_in,
-                 float* __restrict__ qdq) {
-    constexpr int NV = DV / 64;  // 64-column blocks of v and dO
-    constexpr uint32_t OFF_Q = 0, OFF_K = 2 * kTileBytes, OFF_V = 4 * kTileBytes;
-    constexpr uint32_t OFF_DO = OFF_V + NV * kTileBytes, OFF_P = OFF_DO + NV * kTileBytes;
-    constexpr uint32_t OFF_S = OFF_P + kTileBytes;  // S tile [128][DV]: 2 NV blocks
-    constexpr uint32_t TCOLS = DV == 128 ? 256 : 512;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = align1024(smem_raw);
-    uint8_t* Qs = smem + OFF_Q;
-    uint8_t* Ks = smem + OFF_K;
-    uint8_t* Vs = smem + OFF_V;
-    uint8_t* Ds = smem + OFF_DO;
-    uint8_t* Ps = smem + OFF_P;
-    uint8_t* Sb = smem + OFF_S;
-    __shared__ GateSmem gs;
-    __shared__ __align__(8) uint64_t full_bar;
-    __shared__ __align__(8) uint64_t mma_bar;
-    __shared__ uint32_t tmem_slot;
-    __shared__ float diag_s[kChunk];
-    __shared__ float apart[2][kChunk];
-
-    const Geo G = geo();
-    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
-    const int nch = d.L / kChunk;
-    const int a0 = seg * d.L;
-    const uint32_t fb = smem_u32(&full_bar), mb = smem_u32(&mma_bar);
-
-    if (G.tid == 0) {
-        mbar_init(fb, 1);
-        mbar_init(mb, 1);
-        mbar_fence_init();
-    }
-    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), TCOLS);
-    float S[DV / 2];
-    load_state_rows<DV>(S_in + sum_off(d, seg, b, h), G, S, Sb);
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_slot;
-    auto issue = [&](int c) {
-        const int row = b * d.T + a0 + c * kChunk;
-        mbar_expect_tx(fb, (4 + 2 * NV) * kTileBytes);
-        load_tile(Qs, &mq, 0, 128, h, row, fb);
-        load_tile(Ks, &mk, 0, 128, h, row, fb);
-        load_tile(Vs, &mv, 0, DV, h, row, fb);
-        load_tile(Ds, &mdo, 0, DV, h, row, fb);
-    };
-    if (G.tid == 0) issue(0);
-    GateRegs gr;
-    if (G.warp == 0) gr = gate_load(d, g, b, h, a0, G.lane);
-    uint32_t mph = 0;
-    for (int c = 0; c < nch; ++c) {
-        const int t0 = a0 + c * kChunk;
-        if (G.warp == 0) {
-            gate_prep(gr, &gs, G.lane);
-            if (c + 1 < nch) gr = gate_load(d, g, b, h, t0 + kChunk, G.lane);
-        }
-        mbar_wait(fb, c & 1);
-        __syncthreads();
-        const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks), va = smem_u32(Vs), da = smem_u32(Ds);
-        const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb);
-        if (G.tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
-#pragma unroll
-            for (int s = 0; s < DV / 16; ++s) {  // dA = dO V^T (dO~ tile doubles as dq staging)
-                const uint32_t off = (s >> 2) * kTileBytes + (s & 3) * 32;
-                mma_bf16(tmem, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, s > 0);
-            }
-            mma_commit(mb);
-        }
-        mbar_wait(mb, mph);
-        mph ^= 1;
-        tc_fence_after();
-        {
-            float x[16], gam[16];
-            tok16(tmem, G, 32 * G.grp, x);
-            const int c0 = 32 * G.grp + 16 * G.hi;
-            decay_row16(gs, G.tau, c0, true, gam);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                if (c0 + e == G.tau) diag_s[G.tau] = x[e];  // dO_t . v_t
-                x[e] *= d.scale * gam[e];
-            }
-            store_row16(Ps, G.tau, c0, x);
-#pragma unroll
-            for (int pr = 0; pr < NV / 2; ++pr) {
-                uint8_t* dp = Ds + 2 * pr * kTileBytes;
-                uint8_t* vp = Vs + 2 * pr * kTileBytes;
-                scale_tile(dp, dp, gs.win, d.scale, G.tid);
-                scale_tile(vp, vp, gs.wout, 1.f, G.tid);
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (G.tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id_a = idesc_bf16(64, 128, 0, 1);
-            constexpr uint32_t id_b = idesc_bf16(64, 128, 0, 0);
-            constexpr uint32_t id_s = idesc_bf16(128, DV, 1, 1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // dq' = P K  (strictly causal part)
-                mma_bf16(tmem, sdesc(pa + k * 32, 16, 1024), sdesc(ka + k * 2048, kTileBytes, 1024),
-                         id_a, k > 0);
-#pragma unroll
-            for (int s = 0; s < DV / 16; ++s)  // dq' += dO~ S_prev^T
-                mma_bf16(tmem, sdesc(da + (s >> 2) * kTileBytes + (s & 3) * 32, 16, 1024),
-                         sdesc(sa + (s >> 2) * 2 * kTileBytes + (s & 3) * 32, 16, 1024), id_b, 1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // dS = K^T V~
-                mma_bf16(tmem + 128, sdesc(ka + k * 2048, kTileBytes, 1024),
-                         sdesc(va + k * 2048, kTileBytes, 1024), id_s, k > 0);
-            mma_commit(mb);
-        }
-        mbar_wait(mb, mph);
-        mph ^= 1;
-        tc_fence_after();
-        {
-            const float cd = d.scale * diag_s[G.tau];
-            float a = 0.f;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                float x[16], qv[16], kv[16];
-                const int col = 64 * G.grp + 32 * k;
-                tok16(tmem, G, col, x);
-                const int c0 = col + 16 * G.hi;
-                tile_row_get16(Qs, G.tau, c0, qv);
-                tile_row_get16(Ks, G.tau, c0, kv);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    a = fmaf(qv[e], x[e], a);
-                    x[e] = fmaf(cd, kv[e], x[e]);
-                }
-                store_row16(Ds, G.tau, c0, x);  // dO~ is dead: stage dq there
-            }
-            a += __shfl_xor_sync(kFull, a, 16);
-            if (!G.hi) apart[G.grp][G.tau] = a;
-#pragma unroll
-            for (int hh = 0; hh < DV / 128; ++hh)
-                state_update_half(tmem, G, 128 + 128 * hh, hh, gs.W, S, Sb);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (G.tid < kChunk)
-            qdq[((int64_t)b * d.T + t0 + G.tid) * d.H + h] = apart[0][G.tid] + apart[1][G.tid];
-        if (G.tid == 0) {
-            const int row = b * d.T + t0;
-            tma_store_3d(&mdq, smem_u32(Ds), 0, h, row);
-            tma_store_3d(&mdq, smem_u32(Ds + kTileBytes), 64, h, row);
-            bulk_commit();
-            if (c + 1 < nch) {
-                bulk_wait_read();  // the staging tile is refilled by the next load
-                issue(c + 1);
-            }
-        }
-    }
-    if (G.tid == 0) bulk_wait_all();
-    if (G.warp == 0) tmem_dealloc(tmem, TCOLS);
 }
 
 // dst = f * src for a [64][128] bf16 tile (uniform factor), 4 chunks per thread
@@ -2039,6 +1867,366 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
     if (G.warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// ===========================================================================
+// forward sweep of the backward for Dv = 256: dq and q.dq' per token.  The
+// fp32 state S (128 x 256) lives in tensor memory, where dS accumulates; the
+// epilogue scales it by W (after dS in factored chunks, before it otherwise)
+// and snapshots it to the bf16 S tile for the next chunk's dO S^T.  Gamma
+// keeps its own pass at Dv = 256 (its accumulator would not fit beside S).
+// Tensor memory: [0,64) dA, [128,256) dq', [256,512) S.
+// Shared memory: Q|K by chunk parity (2 x 32 KB), V and dO (32 KB each), S as
+// bf16 (64 KB), P.  dS = K^T V is issued first once the chunk's operands are
+// ready, so V dies early and the next chunk's V load overlaps dq' and the dq
+// rows; dO dies with dq'.
+//   warps 0-7 (epilogues): E1 score mask, K^ (factored) or dO~, V~ and
+//     S *= W (general) -> p_ready;  E2 dq rows -> in_dead, state snapshot
+//     -> s_ready, a_ready.
+//   warp 8 (one thread): the tensor products.  warp 9: q.dq' sums and gate
+//   tables.  warp 10 (one thread): V at v_dead, dO at dq_done, Q|K at in_dead.
+// ===========================================================================
+__global__ void __launch_bounds__(kRev3Threads, 1)
+    tc_dq256_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                    const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                    const __grid_constant__ CUtensorMap mdo, const float* __restrict__ g,
+                    const float* __restrict__ S_in, __nv_bfloat16* __restrict__ dq,
+                    float* __restrict__ qdq) {
+    constexpr int DV = 256;
+    constexpr uint32_t QKB = 4 * kTileBytes;  // Q | K
+    constexpr uint32_t OFF_V = 2 * QKB, OFF_D = OFF_V + 4 * kTileBytes, OFF_S = OFF_D + 4 * kTileBytes;
+    constexpr uint32_t OFF_P = OFF_S + 8 * kTileBytes;
+    constexpr uint32_t TS = 256;  // tensor-memory column of S
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint8_t* Vs = smem + OFF_V;
+    uint8_t* Ds = smem + OFF_D;
+    uint8_t* Sb = smem + OFF_S;
+    uint8_t* Ps = smem + OFF_P;
+    __shared__ GateSmem gsb[2];
+    __shared__ __align__(8) uint64_t qk_full[2], v_full, d_full;
+    __shared__ __align__(8) uint64_t score_bar, v_dead, dq_done;  // tensor-core commits
+    __shared__ __align__(8) uint64_t p_ready, s_ready;           // epilogue -> warp 8
+    __shared__ __align__(8) uint64_t in_dead[2];                 // epilogue -> warp 10, by chunk parity
+    __shared__ __align__(8) uint64_t a_ready[2], a_done[2], gate_ready[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ float diag_s[2][kChunk];
+    __shared__ float apart[2][2][kChunk];
+
+    const Geo G = geo();
+    const bool epi = G.warp < 8;
+    const bool ctl = G.warp == 8;
+    const bool gat = G.warp == 9;
+    const bool cpy = G.warp == 10;
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+
+    if (G.tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&qk_full[i]), 1);
+            mbar_init(smem_u32(&a_ready[i]), 8);
+            mbar_init(smem_u32(&a_done[i]), 1);
+            mbar_init(smem_u32(&gate_ready[i]), 1);
+            mbar_init(smem_u32(&in_dead[i]), 8);
+        }
+        mbar_init(smem_u32(&v_full), 1);
+        mbar_init(smem_u32(&d_full), 1);
+        mbar_init(smem_u32(&score_bar), 1);
+        mbar_init(smem_u32(&v_dead), 1);
+        mbar_init(smem_u32(&dq_done), 1);
+        mbar_init(smem_u32(&p_ready), 8);
+        mbar_init(smem_u32(&s_ready), 8);
+        mbar_fence_init();
+    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
+    GateRegs gr;
+    if (gat) {  // gate tables of the first two chunks; registers for the third
+        gr = gate_load(d, g, b, h, a0, G.lane);
+        gate_prep(gr, &gsb[0], G.lane);
+        if (nch > 1) {
+            gr = gate_load(d, g, b, h, a0 + kChunk, G.lane);
+            gate_prep(gr, &gsb[1], G.lane);
+        }
+        if (nch > 2) gr = gate_load(d, g, b, h, a0 + 2 * kChunk, G.lane);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (epi) {  // S_in into tensor memory and the bf16 tile; thread (srow, grp) owns columns [128 grp, +128)
+        const float* src = S_in + sum_off(d, seg, b, h) + int64_t(G.srow) * DV + 128 * G.grp;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src + 32 * j + i);
+                f[i] = x.x; f[i + 1] = x.y; f[i + 2] = x.z; f[i + 3] = x.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i]);
+            tmem_st32(tmem + G.tl + TS + 128 * G.grp + 32 * j, r);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(Sb + sw_chunk(128, G.srow, 16 * G.grp + 4 * j + c)) = pack8(f + 8 * c);
+        }
+        tmem_wait_st();
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (ctl) {
+        if (G.lane == 0) {
+            const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb), va = smem_u32(Vs), da = smem_u32(Ds);
+            constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
+            constexpr uint32_t id_a = idesc_bf16(64, 128, 0, 1);
+            constexpr uint32_t id_b = idesc_bf16(64, 128, 0, 0);
+            constexpr uint32_t id_s = idesc_bf16(128, 256, 1, 1);
+            auto issue_scores = [&]() {  // dA = dO V^T
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
+                    mma_bf16(tmem, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+                }
+                mma_commit(smem_u32(&score_bar));
+            };
+            auto issue_state_side = [&](bool first) {  // dq' (+)= dO S_prev^T
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    mma_bf16(tmem + 128, sdesc(da + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                             sdesc(sa + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_b,
+                             (first && k == 0) ? 0u : 1u);
+            };
+            mbar_wait(smem_u32(&v_full), 0);
+            mbar_wait(smem_u32(&d_full), 0);
+            tc_fence_after();
+            issue_scores();
+            bool fact = gsb[0].fact != 0;
+            if (fact) issue_state_side(true);
+            for (int c = 0; c < nch; ++c) {
+                const int p = c & 1;
+                const uint32_t ph = c & 1;
+                const uint32_t ka = smem_u32(smem + p * QKB) + 2 * kTileBytes;
+                mbar_wait(smem_u32(&p_ready), ph);
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // S += K^T V  (K^ or V~ carry the weights)
+                    mma_bf16(tmem + TS, sdesc(ka + k * 2048, kTileBytes, 1024), sdesc(va + k * 2048, kTileBytes, 1024),
+                             id_s, 1u);
+                mma_commit(smem_u32(&v_dead));
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // dq' (+)= P K  (strictly causal part)
+                    mma_bf16(tmem + 128, sdesc(pa + k * 32, 16, 1024), sdesc(ka + k * 2048, kTileBytes, 1024),
+                             id_a, (fact || k > 0) ? 1u : 0u);
+                if (!fact) issue_state_side(false);  // dO~ S_prev^T
+                mma_commit(smem_u32(&dq_done));
+                if (c + 1 < nch) {
+                    mbar_wait(smem_u32(&v_full), (c + 1) & 1);
+                    mbar_wait(smem_u32(&d_full), (c + 1) & 1);
+                    tc_fence_after();
+                    issue_scores();
+                    // the state after this chunk is in the S tile: the next
+                    // factored chunk's dO S^T
+                    mbar_wait(smem_u32(&s_ready), ph);
+                    if (c + 1 >= 2) mbar_wait(smem_u32(&gate_ready[p ^ 1]), ((c - 1) >> 1) & 1);
+                    fact = gsb[p ^ 1].fact != 0;
+                    if (fact) {
+                        tc_fence_after();
+                        issue_state_side(true);
+                    }
+                }
+            }
+        }
+    } else if (cpy) {
+        if (G.lane == 0) {
+            auto load_qk = [&](int c, int p) {
+                const int row = b * d.T + a0 + c * kChunk;
+                const uint32_t bar = smem_u32(&qk_full[p]);
+                uint8_t* st = smem + p * QKB;
+                mbar_expect_tx(bar, QKB);
+                load_tile(st, &mq, 0, 128, h, row, bar);
+                load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
+            };
+            auto load_one = [&](int c, uint8_t* dst, const CUtensorMap* map, uint64_t* barp) {
+                const int row = b * d.T + a0 + c * kChunk;
+                const uint32_t bar = smem_u32(barp);
+                mbar_expect_tx(bar, 4 * kTileBytes);
+                load_tile(dst, map, 0, DV, h, row, bar);
+            };
+            load_one(0, Vs, &mv, &v_full);
+            load_one(0, Ds, &mdo, &d_full);
+            load_qk(0, 0);
+            if (nch > 1) load_qk(1, 1);
+            for (int c = 0; c + 1 < nch; ++c) {
+                const uint32_t ph = c & 1;
+                mbar_wait(smem_u32(&v_dead), ph);  // the scores and dS are done with V
+                load_one(c + 1, Vs, &mv, &v_full);
+                mbar_wait(smem_u32(&dq_done), ph);  // the scores and dq' are done with dO
+                load_one(c + 1, Ds, &mdo, &d_full);
+                // the dq rows are done with Q and K (parity-indexed: its next
+                // completion needs the Q|K this load brings)
+                mbar_wait(smem_u32(&in_dead[c & 1]), (c >> 1) & 1);
+                if (c + 2 < nch) load_qk(c + 2, c & 1);
+            }
+        }
+    } else if (gat) {
+        for (int c = 0; c < nch; ++c) {
+            const int p = c & 1;
+            const int t0 = a0 + c * kChunk;
+            mbar_wait(smem_u32(&a_ready[p]), (c >> 1) & 1);
+            const int64_t base = ((int64_t)b * d.T + t0) * d.H + h;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = 2 * G.lane + u;
+                qdq[base + int64_t(t) * d.H] = apart[p][0][t] + apart[p][1][t];
+            }
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&a_done[p]));
+            if (c + 2 < nch) {
+                gate_prep(gr, &gsb[p], G.lane);
+                if (c + 3 < nch) gr = gate_load(d, g, b, h, t0 + 3 * kChunk, G.lane);
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&gate_ready[p]));
+            }
+        }
+    } else {  // epilogue warps
+        uint32_t sph = 0, dph = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int p = c & 1;
+            const int t0 = a0 + c * kChunk;
+            const GateSmem& gs = gsb[p];
+            uint8_t* Qs = smem + p * QKB;
+            uint8_t* Ks = Qs + 2 * kTileBytes;
+            // ---- E1
+            if (c >= 2) mbar_wait(smem_u32(&gate_ready[p]), ((c - 2) >> 1) & 1);
+            mbar_wait(smem_u32(&score_bar), sph);
+            sph ^= 1;
+            mbar_wait(smem_u32(&qk_full[p]), (c >> 1) & 1);
+            mbar_wait(smem_u32(&v_full), c & 1);
+            mbar_wait(smem_u32(&d_full), c & 1);
+            tc_fence_after();
+            // Factored chunks take the decays as K^ = exp(-b) K:  dq'_t =
+            // scale win_t (sum_{s<t} (dO_t . v_s) k^_s + dO_t S_prev^T) and
+            // S = W (S_prev + K^T^ V); dO and V stay unscaled.
+            const bool fact = gs.fact != 0;
+            {
+                float x[16];
+                tok16(tmem, G, 32 * G.grp, x);
+                const int c0 = 32 * G.grp + 16 * G.hi;
+                if (fact) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        if (c0 + e == G.tau) diag_s[p][G.tau] = x[e];  // dO_t . v_t
+                        x[e] = c0 + e < G.tau ? x[e] : 0.f;
+                    }
+                } else {
+                    float gam[16];
+                    decay_row16(gs, G.tau, c0, true, gam);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        if (c0 + e == G.tau) diag_s[p][G.tau] = x[e];  // dO_t . v_t
+                        x[e] *= d.scale * gam[e];
+                    }
+                }
+                store_row16(Ps, G.tau, c0, x);
+            }
+            if (fact) {
+                scale_tile(Ks, Ks, gs.nb, 1.f, G.tid);  // K^
+            } else {
+                scale_tile(Ds, Ds, gs.win, d.scale, G.tid);  // dO~
+                scale_tile(Ds + 2 * kTileBytes, Ds + 2 * kTileBytes, gs.win, d.scale, G.tid);
+                scale_tile(Vs, Vs, gs.wout, 1.f, G.tid);  // V~
+                scale_tile(Vs + 2 * kTileBytes, Vs + 2 * kTileBytes, gs.wout, 1.f, G.tid);
+#pragma unroll 1
+                for (int j = 0; j < 4; ++j) {  // S *= W ahead of S += K^T V~
+                    uint32_t r[32];
+                    tmem_ld32_nowait(tmem + G.tl + TS + 128 * G.grp + 32 * j, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(gs.W * __uint_as_float(r[i]));
+                    tmem_st32(tmem + G.tl + TS + 128 * G.grp + 32 * j, r);
+                }
+                tmem_wait_st();
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&p_ready));
+            // ---- E2: dq rows
+            mbar_wait(smem_u32(&dq_done), dph);
+            dph ^= 1;
+            if (c >= 2) mbar_wait(smem_u32(&a_done[p]), ((c - 2) >> 1) & 1);  // apart[p] free
+            mbar_wait(smem_u32(&p_ready), c & 1);  // diag_s from the other warp of the quadrant
+            tc_fence_after();
+            {
+                // factored: dq' = scale win_t acc and k_t = win_t k^_t
+                const float wr = fact ? d.scale * gs.win[G.tau] : 1.f;
+                const float cd = d.scale * diag_s[p][G.tau] * (fact ? gs.win[G.tau] : 1.f);
+                const int64_t tok = ((int64_t)b * d.T + t0 + G.tau) * d.H + h;
+                float a = 0.f;
+                float xx[2][16];
+                tok16x2(tmem, G, 128 + 64 * G.grp, 128 + 64 * G.grp + 32, xx[0], xx[1]);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    float qv[16], kv[16];
+                    float* x = xx[k];
+                    const int cc = 64 * G.grp + 32 * k + 16 * G.hi;
+                    tile_row_get16(Qs, G.tau, cc, qv);
+                    tile_row_get16(Ks, G.tau, cc, kv);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        x[e] *= wr;
+                        a = fmaf(qv[e], x[e], a);
+                        x[e] = fmaf(cd, kv[e], x[e]);
+                    }
+                    store_bf16x16(dq + tok * 128 + cc, x);
+                }
+                a += __shfl_xor_sync(kFull, a, 16);
+                if (!G.hi) apart[p][G.grp][G.tau] = a;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&in_dead[p]));
+            // ---- E2: state snapshot (dS has accumulated: it precedes dq' in
+            // the commit that dq_done tracks)
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+                float f[32];
+                tmem_ld32_nowait(tmem + G.tl + TS + 128 * G.grp + 32 * j, r);
+                tmem_wait_ld();
+                if (fact) {  // S = W (S_prev + K^T^ V)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        f[i] = gs.W * __uint_as_float(r[i]);
+                        r[i] = __float_as_uint(f[i]);
+                    }
+                    tmem_st32(tmem + G.tl + TS + 128 * G.grp + 32 * j, r);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4*>(Sb + sw_chunk(128, G.srow, 16 * G.grp + 4 * j + cc)) = pack8(f + 8 * cc);
+            }
+            tmem_wait_st();
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) {
+                mbar_arrive(smem_u32(&s_ready));
+                mbar_arrive(smem_u32(&a_ready[p]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // Failure-detection self test: waits on an mbarrier that nothing arrives on,
 // with the given bound, so that the timeout path and its host-side status can
 // be exercised without faulting or hanging the device.
@@ -2094,7 +2282,8 @@ bool set_smem(K kernel, size_t bytes) {
 constexpr size_t kOuterSmem = 96 * 1024 + 1024;
 constexpr size_t kFwdSmem = 13 * kTileBytes + 1024;   // Q K V P (7 tiles) + S (4) + o staging (2)
 // Q K (4 tiles) + V dO (2 NV) + P (1) + S (2 NV)
-constexpr size_t dq_smem(int dv) { return size_t(5 + 4 * (dv / 64)) * kTileBytes + 1024; }
+// Q|K x 2 (8) + V (4) + dO (4) + S (8) + P (1)
+constexpr size_t kDq256Smem = 25 * kTileBytes + 1024;
 // 2 stages x 8 + P (1) + S (4) + gamma's Q (2) + dq staging (2)
 constexpr size_t kDqg128Smem = 25 * kTileBytes + 1024;
 // stages x (4 + 2 NV) + Q~ K~ (4) + PA PdA (2) + E (2 NV): 26 tiles for Dv 128 and 256
@@ -2182,11 +2371,12 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 return RM_OK;
             } else {
                 auto fo = tc_outer_kernel<256, true>;
-                auto fq = tc_dq_kernel<256>;
-                if (!set_smem(fo, kOuterSmem) || !set_smem(fq, dq_smem(256))) return RM_ERR_CUDA;
+                auto fq = tc_dq256_kernel;
+                if (!set_smem(fo, kOuterSmem) || !set_smem(fq, kDq256Smem)) return RM_ERR_CUDA;
                 fo<<<grid, kThreads, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
                 if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
-                fq<<<grid, kThreads, dq_smem(256), s>>>(d, mq, mk, mv, mdo, mdq, p.g, p.S_in, p.ws_f32);
+                fq<<<grid, kRev3Threads, kDq256Smem, s>>>(d, mq, mk, mv, mdo, p.g, p.S_in,
+                                                          static_cast<__nv_bfloat16*>(p.out0), p.ws_f32);
             }
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(2);
