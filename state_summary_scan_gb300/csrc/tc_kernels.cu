@@ -2227,6 +2227,330 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
     if (G.warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// ===========================================================================
+// forward sweep, warp-specialised: o for one (segment, row, head, 128-wide
+// value block).  The fp32 state block S (128 x 128) lives in tensor memory,
+// where dS accumulates; the epilogue scales it by W and snapshots it to the
+// bf16 state tile that the next chunk's Q S reads.
+// Factored chunks (no sequence start, every |b| < 60) take the decays as
+// V^ = exp(-b) V in place:
+//   o_t = scale win_t (sum_{s<=t} (q_t . k_s) v^_s + q_t S_prev),
+//   S   = W (S_prev + K^T V^),
+// so the score mask is plain causal, Q and K stay unscaled, and Q S_prev is
+// issued as soon as the previous state is in place.  Other chunks scale Q~ and
+// K~ in place and pre-scale S by W.
+// Tensor memory: [0,64) scores, [64,192) O, [256,384) S.
+// Shared memory: Q|K and V double-buffered by chunk parity, P, S (bf16), o
+// staging (written by bulk tensor stores).
+//   warps 0-7: E1 score mask (+ V^, or Q~, K~, S *= W) -> p_ready;
+//              E2 o rows -> o_read, o_staged; state snapshot -> s_ready,
+//              in_dead, g_free
+//   warp 8 (one thread): the tensor products; warp 9: gate tables;
+//   warp 10 (one thread): loads (a stage refilled once its chunk is done)
+//              and the o stores.
+// ===========================================================================
+__global__ void __launch_bounds__(kRev3Threads, 1)
+    tc_fwd2_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                   const __grid_constant__ CUtensorMap mo, const float* __restrict__ g,
+                   const float* __restrict__ S_in) {
+    constexpr uint32_t QKB = 4 * kTileBytes;  // Q | K
+    constexpr uint32_t VB = 2 * kTileBytes;   // V block (128 columns)
+    constexpr uint32_t OFF_V = 2 * QKB, OFF_P = OFF_V + 2 * VB, OFF_S = OFF_P + kTileBytes;
+    constexpr uint32_t OFF_O = OFF_S + 4 * kTileBytes;
+    constexpr uint32_t TO = 64, TS = 256;  // tensor-memory columns of O and S
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint8_t* Ps = smem + OFF_P;
+    uint8_t* Sb = smem + OFF_S;
+    uint8_t* Os = smem + OFF_O;
+    __shared__ GateSmem gsb[2];
+    __shared__ __align__(8) uint64_t qk_full[2], v_full[2];
+    __shared__ __align__(8) uint64_t score_bar, o_done, s_done;            // tensor-core commits
+    __shared__ __align__(8) uint64_t p_ready, s_ready, o_read, o_staged;   // epilogue -> warps 8, 10
+    __shared__ __align__(8) uint64_t in_dead[2], g_free[2], gate_ready[2];
+    __shared__ __align__(8) uint64_t stg_free;                             // warp 10 -> epilogue
+    __shared__ uint32_t tmem_slot;
+
+    const Geo G = geo();
+    const bool epi = G.warp < 8;
+    const bool ctl = G.warp == 8;
+    const bool gat = G.warp == 9;
+    const bool cpy = G.warp == 10;
+    const int nvb = d.Dv / 128;
+    const int seg = blockIdx.x / nvb, vb = blockIdx.x % nvb, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+
+    if (G.tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&qk_full[i]), 1);
+            mbar_init(smem_u32(&v_full[i]), 1);
+            mbar_init(smem_u32(&in_dead[i]), 8);
+            mbar_init(smem_u32(&g_free[i]), 8);
+            mbar_init(smem_u32(&gate_ready[i]), 1);
+        }
+        mbar_init(smem_u32(&score_bar), 1);
+        mbar_init(smem_u32(&o_done), 1);
+        mbar_init(smem_u32(&s_done), 1);
+        mbar_init(smem_u32(&p_ready), 8);
+        mbar_init(smem_u32(&s_ready), 8);
+        mbar_init(smem_u32(&o_read), 8);
+        mbar_init(smem_u32(&o_staged), 8);
+        mbar_init(smem_u32(&stg_free), 1);
+        mbar_fence_init();
+    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
+    GateRegs gr;
+    if (gat) {  // gate tables of the first two chunks; registers for the third
+        gr = gate_load(d, g, b, h, a0, G.lane);
+        gate_prep(gr, &gsb[0], G.lane);
+        if (nch > 1) {
+            gr = gate_load(d, g, b, h, a0 + kChunk, G.lane);
+            gate_prep(gr, &gsb[1], G.lane);
+        }
+        if (nch > 2) gr = gate_load(d, g, b, h, a0 + 2 * kChunk, G.lane);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (epi) {  // S_in block into tensor memory and the bf16 tile: row srow, columns [64 grp, +64)
+        const float* src = S_in + sum_off(d, seg, b, h) + int64_t(G.srow) * d.Dv + vb * 128 + 64 * G.grp;
+        float f[64];
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src + j);
+            f[j] = x.x; f[j + 1] = x.y; f[j + 2] = x.z; f[j + 3] = x.w;
+        }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[32 * hf + i]);
+            tmem_st32(tmem + G.tl + TS + 64 * G.grp + 32 * hf, r);
+        }
+        tmem_wait_st();
+        store_state_half(Sb, G.srow, G.grp, f);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (ctl) {
+        if (G.lane == 0) {
+            const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb);
+            constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
+            constexpr uint32_t id_o = idesc_bf16(64, 128, 0, 1);
+            constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
+            auto issue_scores = [&](int p) {  // scores = Q K^T
+                const uint32_t qa = smem_u32(smem + p * QKB), ka = qa + 2 * kTileBytes;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
+                    mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, k > 0);
+                }
+                mma_commit(smem_u32(&score_bar));
+            };
+            auto issue_qs = [&](int p, bool first) {  // O (+)= Q S_prev
+                const uint32_t qa = smem_u32(smem + p * QKB);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16(tmem + TO, sdesc(qa + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                             sdesc(sa + k * 2048, 2 * kTileBytes, 1024), id_o, (first && k == 0) ? 0u : 1u);
+            };
+            mbar_wait(smem_u32(&qk_full[0]), 0);
+            tc_fence_after();
+            issue_scores(0);
+            bool fact = gsb[0].fact != 0;
+            if (fact) issue_qs(0, true);
+            for (int c = 0; c < nch; ++c) {
+                const int p = c & 1;
+                const uint32_t ph = c & 1;
+                const uint32_t qa = smem_u32(smem + p * QKB), ka = qa + 2 * kTileBytes;
+                const uint32_t va = smem_u32(smem + OFF_V + p * VB);
+                mbar_wait(smem_u32(&p_ready), ph);
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // O (+)= P V
+                    mma_bf16(tmem + TO, sdesc(pa + k * 32, 16, 1024), sdesc(va + k * 2048, kTileBytes, 1024), id_o,
+                             (fact || k > 0) ? 1u : 0u);
+                if (!fact) issue_qs(p, false);  // O += Q~ S_prev
+                mma_commit(smem_u32(&o_done));
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // S += K^T V  (V^ or K~ carry the weights)
+                    mma_bf16(tmem + TS, sdesc(ka + k * 2048, kTileBytes, 1024), sdesc(va + k * 2048, kTileBytes, 1024),
+                             id_s, 1u);
+                mma_commit(smem_u32(&s_done));
+                if (c + 1 < nch) {
+                    mbar_wait(smem_u32(&qk_full[p ^ 1]), ((c + 1) >> 1) & 1);
+                    tc_fence_after();
+                    issue_scores(p ^ 1);
+                    // the next factored chunk's Q S once the state is in its
+                    // tile and this chunk's o rows have left tensor memory
+                    mbar_wait(smem_u32(&o_read), ph);
+                    mbar_wait(smem_u32(&s_ready), ph);
+                    if (c + 1 >= 2) mbar_wait(smem_u32(&gate_ready[p ^ 1]), ((c - 1) >> 1) & 1);
+                    fact = gsb[p ^ 1].fact != 0;
+                    if (fact) {
+                        tc_fence_after();
+                        issue_qs(p ^ 1, true);
+                    }
+                }
+            }
+        }
+    } else if (cpy) {
+        if (G.lane == 0) {
+            auto load = [&](int c, int p) {
+                const int row = b * d.T + a0 + c * kChunk;
+                uint8_t* st = smem + p * QKB;
+                const uint32_t qb = smem_u32(&qk_full[p]), vbar = smem_u32(&v_full[p]);
+                mbar_expect_tx(qb, QKB);
+                load_tile(st, &mq, 0, 128, h, row, qb);
+                load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, qb);
+                mbar_expect_tx(vbar, VB);
+                load_tile(smem + OFF_V + p * VB, &mv, vb * 128, 128, h, row, vbar);
+            };
+            load(0, 0);
+            if (nch > 1) load(1, 1);
+            for (int c = 0; c < nch; ++c) {
+                const int p = c & 1;
+                const int row = b * d.T + a0 + c * kChunk;
+                mbar_wait(smem_u32(&o_staged), c & 1);
+                tma_store_3d(&mo, smem_u32(Os), vb * 128, h, row);
+                tma_store_3d(&mo, smem_u32(Os + kTileBytes), vb * 128 + 64, h, row);
+                bulk_commit();
+                mbar_wait(smem_u32(&in_dead[p]), (c >> 1) & 1);  // every read of the stage is done
+                if (c + 2 < nch) load(c + 2, p);
+                bulk_wait_read();
+                mbar_arrive(smem_u32(&stg_free));
+            }
+            bulk_wait_all();
+        }
+    } else if (gat) {
+        for (int c = 0; c + 2 < nch; ++c) {
+            const int p = c & 1;
+            mbar_wait(smem_u32(&g_free[p]), (c >> 1) & 1);
+            gate_prep(gr, &gsb[p], G.lane);
+            if (c + 3 < nch) gr = gate_load(d, g, b, h, a0 + (c + 3) * kChunk, G.lane);
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&gate_ready[p]));
+        }
+    } else {  // epilogue warps
+        uint32_t sph = 0, oph = 0, tph = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int p = c & 1;
+            const GateSmem& gs = gsb[p];
+            uint8_t* Qs = smem + p * QKB;
+            uint8_t* Ks = Qs + 2 * kTileBytes;
+            uint8_t* Vs = smem + OFF_V + p * VB;
+            // ---- E1
+            if (c >= 2) mbar_wait(smem_u32(&gate_ready[p]), ((c - 2) >> 1) & 1);
+            mbar_wait(smem_u32(&score_bar), sph);
+            sph ^= 1;
+            mbar_wait(smem_u32(&qk_full[p]), (c >> 1) & 1);
+            mbar_wait(smem_u32(&v_full[p]), (c >> 1) & 1);
+            tc_fence_after();
+            const bool fact = gs.fact != 0;
+            {
+                float x[16];
+                tok16(tmem, G, 32 * G.grp, x);
+                const int c0 = 32 * G.grp + 16 * G.hi;
+                if (fact) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) x[e] = c0 + e <= G.tau ? x[e] : 0.f;
+                } else {
+                    float gam[16];
+                    decay_row16(gs, G.tau, c0, false, gam);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) x[e] *= d.scale * gam[e];
+                }
+                store_row16(Ps, G.tau, c0, x);
+            }
+            if (fact) {
+                scale_tile(Vs, Vs, gs.nb, 1.f, G.tid);  // V^
+            } else {
+                scale_tile(Qs, Qs, gs.win, d.scale, G.tid);  // Q~
+                scale_tile(Ks, Ks, gs.wout, 1.f, G.tid);     // K~
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {  // S *= W ahead of S += K~^T V
+                    uint32_t r[32];
+                    tmem_ld32_nowait(tmem + G.tl + TS + 64 * G.grp + 32 * hf, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(gs.W * __uint_as_float(r[i]));
+                    tmem_st32(tmem + G.tl + TS + 64 * G.grp + 32 * hf, r);
+                }
+                tmem_wait_st();
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&p_ready));
+            // ---- E2: o rows
+            mbar_wait(smem_u32(&o_done), oph);
+            oph ^= 1;
+            if (c >= 1) mbar_wait(smem_u32(&stg_free), (c - 1) & 1);  // o staging free
+            tc_fence_after();
+            {
+                float xx[2][16];
+                tok16x2(tmem, G, TO + 64 * G.grp, TO + 64 * G.grp + 32, xx[0], xx[1]);
+                tc_fence_before();
+                __syncwarp();
+                if (G.lane == 0) mbar_arrive(smem_u32(&o_read));
+                const float wr = fact ? d.scale * gs.win[G.tau] : 1.f;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) xx[k][e] *= wr;
+                    store_row16(Os, G.tau, 64 * G.grp + 32 * k + 16 * G.hi, xx[k]);
+                }
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&o_staged));
+            // ---- E2: state snapshot
+            mbar_wait(smem_u32(&s_done), tph);
+            tph ^= 1;
+            tc_fence_after();
+            {
+                float f[64];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t r[32];
+                    tmem_ld32_nowait(tmem + G.tl + TS + 64 * G.grp + 32 * hf, r);
+                    tmem_wait_ld();
+                    if (fact) {  // S = W (S_prev + K^T V^)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            f[32 * hf + i] = gs.W * __uint_as_float(r[i]);
+                            r[i] = __float_as_uint(f[32 * hf + i]);
+                        }
+                        tmem_st32(tmem + G.tl + TS + 64 * G.grp + 32 * hf, r);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) f[32 * hf + i] = __uint_as_float(r[i]);
+                    }
+                }
+                tmem_wait_st();
+                store_state_half(Sb, G.srow, G.grp, f);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) {
+                mbar_arrive(smem_u32(&s_ready));
+                mbar_arrive(smem_u32(&in_dead[p]));
+                mbar_arrive(smem_u32(&g_free[p]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // Failure-detection self test: waits on an mbarrier that nothing arrives on,
 // with the given bound, so that the timeout path and its host-side status can
 // be exercised without faulting or hanging the device.
@@ -2280,7 +2604,9 @@ bool set_smem(K kernel, size_t bytes) {
 }
 
 constexpr size_t kOuterSmem = 96 * 1024 + 1024;
-constexpr size_t kFwdSmem = 13 * kTileBytes + 1024;   // Q K V P (7 tiles) + S (4) + o staging (2)
+constexpr size_t kFwdSmem = 13 * kTileBytes + 1024;
+// Q|K x 2 (8) + V x 2 (4) + P (1) + S (4) + o staging (2)
+constexpr size_t kFwd2Smem = 19 * kTileBytes + 1024;   // Q K V P (7 tiles) + S (4) + o staging (2)
 // Q K (4 tiles) + V dO (2 NV) + P (1) + S (2 NV)
 // Q|K x 2 (8) + V (4) + dO (4) + S (8) + P (1)
 constexpr size_t kDq256Smem = 25 * kTileBytes + 1024;
@@ -2348,8 +2674,8 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             if (!make_map(&mq, p.q, d, 128) || !make_map(&mk, p.k, d, 128) ||
                 !make_map(&mv, p.v, d, d.Dv) || !make_map(&mo, p.out0, d, d.Dv))
                 return RM_ERR_CUDA;
-            if (!set_smem(tc_fwd_apply_kernel, kFwdSmem)) return RM_ERR_CUDA;
-            tc_fwd_apply_kernel<<<dim3(d.nseg * (d.Dv / 128), d.B * d.H), kThreads, kFwdSmem, s>>>(
+            if (!set_smem(tc_fwd2_kernel, kFwd2Smem)) return RM_ERR_CUDA;
+            tc_fwd2_kernel<<<dim3(d.nseg * (d.Dv / 128), d.B * d.H), kRev3Threads, kFwd2Smem, s>>>(
                 d, mq, mk, mv, mo, p.g, p.S_in);
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(1);
