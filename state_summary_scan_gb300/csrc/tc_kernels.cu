@@ -19,7 +19,7 @@
 //                       cp_forward_prepare (x = k, y = v, w = decay to the
 //                       segment end) and gamma of cp_backward_prepare (x = q,
 //                       y = dO, w = scale * decay from the segment start)
-//   tc_fwd_apply_kernel the forward sweep from S_in: o
+//   tc_fwd2_kernel      the forward sweep from S_in: o
 //   tc_dqg128_kernel    the forward sweep of the backward for Dv = 128: dq,
 //                       per token q.dq minus its same-token term (for the
 //                       gate gradient), and gamma
@@ -413,186 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (G.warp == 0) tmem_dealloc(tmem, DV);
-}
-
-// ===========================================================================
-// forward sweep: o for one (segment, row, head, 128-wide value block)
-// ===========================================================================
-__global__ void __launch_bounds__(kThreads, 2)
-    tc_fwd_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
-                        const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                        const __grid_constant__ CUtensorMap mo, const float* __restrict__ g,
-                        const float* __restrict__ S_in) {
-    constexpr uint32_t OFF_Q = 0, OFF_K = 2 * kTileBytes, OFF_V = 4 * kTileBytes;
-    constexpr uint32_t OFF_P = 6 * kTileBytes, OFF_S = 7 * kTileBytes;  // S tile: 32 KB
-    constexpr uint32_t OFF_O = 11 * kTileBytes;                          // o staging: 16 KB
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = align1024(smem_raw);
-    uint8_t* Qs = smem + OFF_Q;
-    uint8_t* Ks = smem + OFF_K;
-    uint8_t* Vs = smem + OFF_V;
-    uint8_t* Ps = smem + OFF_P;
-    uint8_t* Sb = smem + OFF_S;
-    uint8_t* Os = smem + OFF_O;
-    __shared__ GateSmem gsb[2];  // gate tables by chunk parity, built one chunk ahead
-    __shared__ __align__(8) uint64_t full_bar;
-    __shared__ __align__(8) uint64_t mma_bar;
-    __shared__ uint32_t tmem_slot;
-
-    const Geo G = geo();
-    // the value blocks of one (segment, head) are adjacent in the grid, so
-    // they run together and the second one's q and k reads hit L2
-    const int nvb = d.Dv / 128;
-    const int seg = blockIdx.x / nvb, vb = blockIdx.x % nvb, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
-    const int nch = d.L / kChunk;
-    const int a0 = seg * d.L;
-    const uint32_t fb = smem_u32(&full_bar), mb = smem_u32(&mma_bar);
-
-    if (G.tid == 0) {
-        mbar_init(fb, 1);
-        mbar_init(mb, 1);
-        mbar_fence_init();
-    }
-    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
-
-    // fp32 master state: row srow, columns [128 vb + 64 grp, +64)
-    float S[64];
-    {
-        const float* src = S_in + sum_off(d, seg, b, h) + int64_t(G.srow) * d.Dv + vb * 128 + 64 * G.grp;
-#pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(src + j);
-            S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
-        }
-        store_state_half(Sb, G.srow, G.grp, S);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_slot;
-    auto issue = [&](int c) {
-        const int row = b * d.T + a0 + c * kChunk;
-        mbar_expect_tx(fb, 6 * kTileBytes);
-        load_tile(Qs, &mq, 0, 128, h, row, fb);
-        load_tile(Ks, &mk, 0, 128, h, row, fb);
-        load_tile(Vs, &mv, vb * 128, 128, h, row, fb);
-    };
-    if (G.tid == 0) issue(0);
-    GateRegs gr;
-    if (G.warp == 0) {
-        gr = gate_load(d, g, b, h, a0, G.lane);
-        gate_prep(gr, &gsb[0], G.lane);
-        if (nch > 1) gr = gate_load(d, g, b, h, a0 + kChunk, G.lane);
-    }
-    __syncthreads();
-    uint32_t mph = 0;
-    for (int c = 0; c < nch; ++c) {
-        const int t0 = a0 + c * kChunk;
-        const GateSmem& gs = gsb[c & 1];
-        // Chunks without sequence starts and with moderate decays take the
-        // decays as K^ = exp(-b) K (in place, before the scores):
-        //   o_t = scale win_t (sum_{s<=t} (q_t . k^_s) v_s + q_t S_prev),
-        //   S   = W (S_prev + K^T^ V),
-        // so the score mask has no exponentials and Q is not scaled.
-        const bool fact = gs.fact != 0;
-        mbar_wait(fb, c & 1);
-        if (fact) {
-            scale_tile(Ks, Ks, gs.nb, 1.f, G.tid);
-            fence_async_smem();
-        }
-        __syncthreads();
-        const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks), va = smem_u32(Vs);
-        const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb);
-        if (G.tid == 0) {
-            bulk_wait_read();  // the previous chunk's o store has left the staging tile
-            tc_fence_after();
-            constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {  // scores = Q K^T
-                const uint32_t off = (s >> 2) * kTileBytes + (s & 3) * 32;
-                mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, s > 0);
-            }
-            mma_commit(mb);
-        }
-        mbar_wait(mb, mph);
-        mph ^= 1;
-        tc_fence_after();
-        if (fact) {
-            float x[16];
-            tok16(tmem, G, 32 * G.grp, x);
-            const int c0 = 32 * G.grp + 16 * G.hi;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] = c0 + e <= G.tau ? x[e] : 0.f;
-            store_row16(Ps, G.tau, c0, x);
-        } else {
-            float x[16], gam[16];
-            tok16(tmem, G, 32 * G.grp, x);
-            const int c0 = 32 * G.grp + 16 * G.hi;
-            decay_row16(gs, G.tau, c0, false, gam);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] *= d.scale * gam[e];
-            store_row16(Ps, G.tau, c0, x);
-            scale_tile(Qs, Qs, gs.win, d.scale, G.tid);
-            scale_tile(Ks, Ks, gs.wout, 1.f, G.tid);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (G.tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id_o = idesc_bf16(64, 128, 0, 1);
-            constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // O = P V
-                mma_bf16(tmem, sdesc(pa + k * 32, 16, 1024), sdesc(va + k * 2048, kTileBytes, 1024),
-                         id_o, k > 0);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)  // O += Q~ S_prev
-                mma_bf16(tmem, sdesc(qa + (s >> 2) * kTileBytes + (s & 3) * 32, 16, 1024),
-                         sdesc(sa + s * 2048, 2 * kTileBytes, 1024), id_o, 1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // dS = K~^T V
-                mma_bf16(tmem + 128, sdesc(ka + k * 2048, kTileBytes, 1024),
-                         sdesc(va + k * 2048, kTileBytes, 1024), id_s, k > 0);
-            mma_commit(mb);
-        }
-        if (G.warp == 0 && c + 1 < nch) {  // the next chunk's gate tables
-            gate_prep(gr, &gsb[(c + 1) & 1], G.lane);
-            if (c + 2 < nch) gr = gate_load(d, g, b, h, t0 + 2 * kChunk, G.lane);
-        }
-        mbar_wait(mb, mph);
-        mph ^= 1;
-        if (G.tid == 0 && c + 1 < nch) issue(c + 1);
-        tc_fence_after();
-        {
-            const float wr = fact ? d.scale * gs.win[G.tau] : 1.f;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                float x[16];
-                const int col = 64 * G.grp + 32 * k;
-                tok16(tmem, G, col, x);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) x[e] *= wr;
-                store_row16(Os, G.tau, col + 16 * G.hi, x);
-            }
-            if (fact)
-                state_update_scaled(tmem, G, 128, gs.W, S, Sb);
-            else
-                state_update(tmem, G, 128, gs.W, S, Sb);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (G.tid == 0) {  // o rows of the chunk: one bulk tensor store per 64 columns
-            const int row = b * d.T + t0;
-            tma_store_3d(&mo, smem_u32(Os), vb * 128, h, row);
-            tma_store_3d(&mo, smem_u32(Os + kTileBytes), vb * 128 + 64, h, row);
-            bulk_commit();
-        }
-    }
-    if (G.tid == 0) bulk_wait_all();
-    if (G.warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // dst = f * src for a [64][128] bf16 tile (uniform factor), 4 chunks per thread
@@ -2604,15 +2424,14 @@ bool set_smem(K kernel, size_t bytes) {
 }
 
 constexpr size_t kOuterSmem = 96 * 1024 + 1024;
-constexpr size_t kFwdSmem = 13 * kTileBytes + 1024;
 // Q|K x 2 (8) + V x 2 (4) + P (1) + S (4) + o staging (2)
-constexpr size_t kFwd2Smem = 19 * kTileBytes + 1024;   // Q K V P (7 tiles) + S (4) + o staging (2)
-// Q K (4 tiles) + V dO (2 NV) + P (1) + S (2 NV)
+constexpr size_t kFwd2Smem = 19 * kTileBytes + 1024;
 // Q|K x 2 (8) + V (4) + dO (4) + S (8) + P (1)
 constexpr size_t kDq256Smem = 25 * kTileBytes + 1024;
 // 2 stages x 8 + P (1) + S (4) + gamma's Q (2) + dq staging (2)
 constexpr size_t kDqg128Smem = 25 * kTileBytes + 1024;
-// stages x (4 + 2 NV) + Q~ K~ (4) + PA PdA (2) + E (2 NV): 26 tiles for Dv 128 and 256
+// Dv = 128: 2 stages x 8 + Q~ K~ (4) + PA PdA (2) + E (4);
+// Dv = 256: Q|K x 2 (8) + V (4) + dO (4) + E (8) + PA PdA (2): 26 tiles either way
 constexpr size_t rev_smem(int dv) {
     return size_t((dv == 128 ? 2 : 1) * (4 + 2 * (dv / 64)) + 6 + 2 * (dv / 64)) * kTileBytes + 1024;
 }
