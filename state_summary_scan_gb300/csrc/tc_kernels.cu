@@ -965,14 +965,14 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             // ahead of the chunk's score masks.
             auto issue_ve = [&](int s) {  // dk' = V E^T
                 const uint32_t va = smem_u32(smem + s * STAGE) + 4 * kTileBytes;
-#pragma unroll
+#pragma unroll 1
                 for (int k = 0; k < 8; ++k)
                     mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
                              sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, k > 0);
             };
             auto issue_ke = [&](int s) {  // dv = K E
                 const uint32_t ka = smem_u32(smem + s * STAGE) + 2 * kTileBytes;
-#pragma unroll
+#pragma unroll 1
                 for (int k = 0; k < 8; ++k)
                     mma_bf16(tmem + 256, sdesc(ka + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
                              sdesc(ea + k * 2048, 2 * kTileBytes, 1024), id_km, k > 0);
@@ -991,12 +991,12 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 const uint32_t va = qa + 4 * kTileBytes, da = qa + 6 * kTileBytes;
                 mbar_wait(smem_u32(&pv_ready), ph);
                 tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                 for (int k = 0; k < 4; ++k)  // dk' (+)= PdA^T Q
                     mma_bf16(tmem + 128, sdesc(pd + k * 2048, kTileBytes, 1024),
                              sdesc(qa + k * 2048, kTileBytes, 1024), id_mm, (fact || k > 0) ? 1u : 0u);
                 if (!fact) {
-#pragma unroll
+#pragma unroll 1
                     for (int k = 0; k < 8; ++k)  // dk' += V~ E^T
                         mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
                                  sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, 1);
@@ -1005,18 +1005,18 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 if (fact) issue_ke(s);  // E-side of dv, behind the dk' products
                 mbar_wait(smem_u32(&kq_ready), ph);
                 tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                 for (int k = 0; k < 4; ++k)  // dv (+)= PA^T dO
                     mma_bf16(tmem + 256, sdesc(pa + k * 2048, kTileBytes, 1024),
                              sdesc(da + k * 2048, kTileBytes, 1024), id_mm, (fact || k > 0) ? 1u : 0u);
                 if (!fact) {
-#pragma unroll
+#pragma unroll 1
                     for (int k = 0; k < 8; ++k)  // dv += K~ E
                         mma_bf16(tmem + 256, sdesc(kta + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
                                  sdesc(ea + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
                 }
                 const uint32_t qx = fact ? qa : qta;
-#pragma unroll
+#pragma unroll 1
                 for (int k = 0; k < 4; ++k)  // dE = Q~^T dO
                     mma_bf16(tmem + 384, sdesc(qx + k * 2048, kTileBytes, 1024),
                              sdesc(da + k * 2048, kTileBytes, 1024), id_e, k > 0);
@@ -2069,26 +2069,30 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
 //   warp 10 (one thread): loads (a stage refilled once its chunk is done)
 //              and the o stores.
 // ===========================================================================
-__global__ void __launch_bounds__(kRev3Threads, 1)
+template <bool TWO>
+__global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
     tc_fwd2_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                    const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                    const __grid_constant__ CUtensorMap mo, const float* __restrict__ g,
                    const float* __restrict__ S_in) {
     constexpr uint32_t QKB = 4 * kTileBytes;  // Q | K
     constexpr uint32_t VB = 2 * kTileBytes;   // V block (128 columns)
-    constexpr uint32_t OFF_V = 2 * QKB, OFF_P = OFF_V + 2 * VB, OFF_S = OFF_P + kTileBytes;
+    constexpr int NST = TWO ? 1 : 2;          // input stages
+    constexpr uint32_t OFF_V = NST * QKB, OFF_P = OFF_V + NST * VB, OFF_S = OFF_P + kTileBytes;
     constexpr uint32_t OFF_O = OFF_S + 4 * kTileBytes;
-    constexpr uint32_t TO = 64, TS = 256;  // tensor-memory columns of O and S
+    // tensor-memory columns of O and S; two CTAs a SM share the 512 columns,
+    // so there O aliases the scores (issued after the scores were read)
+    constexpr uint32_t TO = TWO ? 0 : 64, TS = TWO ? 128 : 256, TCOLS = TWO ? 256 : 512;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint8_t* Ps = smem + OFF_P;
     uint8_t* Sb = smem + OFF_S;
     uint8_t* Os = smem + OFF_O;
     __shared__ GateSmem gsb[2];
-    __shared__ __align__(8) uint64_t qk_full[2], v_full[2];
+    __shared__ __align__(8) uint64_t qk_full[NST], v_full[NST];
     __shared__ __align__(8) uint64_t score_bar, o_done, s_done;            // tensor-core commits
     __shared__ __align__(8) uint64_t p_ready, s_ready, o_read, o_staged;   // epilogue -> warps 8, 10
-    __shared__ __align__(8) uint64_t in_dead[2], g_free[2], gate_ready[2];
+    __shared__ __align__(8) uint64_t in_dead[NST], g_free[2], gate_ready[2];
     __shared__ __align__(8) uint64_t stg_free;                             // warp 10 -> epilogue
     __shared__ uint32_t tmem_slot;
 
@@ -2103,10 +2107,12 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
     const int a0 = seg * d.L;
 
     if (G.tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NST; ++i) {
             mbar_init(smem_u32(&qk_full[i]), 1);
             mbar_init(smem_u32(&v_full[i]), 1);
             mbar_init(smem_u32(&in_dead[i]), 8);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&g_free[i]), 8);
             mbar_init(smem_u32(&gate_ready[i]), 1);
         }
@@ -2120,7 +2126,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
         mbar_init(smem_u32(&stg_free), 1);
         mbar_fence_init();
     }
-    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), TCOLS);
     GateRegs gr;
     if (gat) {  // gate tables of the first two chunks; registers for the third
         gr = gate_load(d, g, b, h, a0, G.lane);
@@ -2184,19 +2190,20 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             tc_fence_after();
             issue_scores(0);
             bool fact = gsb[0].fact != 0;
-            if (fact) issue_qs(0, true);
+            if (!TWO && fact) issue_qs(0, true);
             for (int c = 0; c < nch; ++c) {
                 const int p = c & 1;
+                const int st = TWO ? 0 : p;
                 const uint32_t ph = c & 1;
-                const uint32_t qa = smem_u32(smem + p * QKB), ka = qa + 2 * kTileBytes;
-                const uint32_t va = smem_u32(smem + OFF_V + p * VB);
+                const uint32_t qa = smem_u32(smem + st * QKB), ka = qa + 2 * kTileBytes;
+                const uint32_t va = smem_u32(smem + OFF_V + st * VB);
                 mbar_wait(smem_u32(&p_ready), ph);
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // O (+)= P V
                     mma_bf16(tmem + TO, sdesc(pa + k * 32, 16, 1024), sdesc(va + k * 2048, kTileBytes, 1024), id_o,
-                             (fact || k > 0) ? 1u : 0u);
-                if (!fact) issue_qs(p, false);  // O += Q~ S_prev
+                             ((!TWO && fact) || k > 0) ? 1u : 0u);
+                if (TWO || !fact) issue_qs(st, false);  // O += Q S_prev (Q~ in general chunks)
                 mma_commit(smem_u32(&o_done));
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // S += K^T V  (V^ or K~ carry the weights)
@@ -2204,6 +2211,15 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                              id_s, 1u);
                 mma_commit(smem_u32(&s_done));
                 if (c + 1 < nch) {
+                    if (TWO) {
+                        mbar_wait(smem_u32(&o_read), ph);  // the scores overwrite O
+                        mbar_wait(smem_u32(&qk_full[0]), (c + 1) & 1);
+                        tc_fence_after();
+                        issue_scores(0);
+                        if (c + 1 >= 2) mbar_wait(smem_u32(&gate_ready[p ^ 1]), ((c - 1) >> 1) & 1);
+                        fact = gsb[p ^ 1].fact != 0;
+                        continue;
+                    }
                     mbar_wait(smem_u32(&qk_full[p ^ 1]), ((c + 1) >> 1) & 1);
                     tc_fence_after();
                     issue_scores(p ^ 1);
@@ -2233,16 +2249,24 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 load_tile(smem + OFF_V + p * VB, &mv, vb * 128, 128, h, row, vbar);
             };
             load(0, 0);
-            if (nch > 1) load(1, 1);
+            if (!TWO && nch > 1) load(1, 1);
             for (int c = 0; c < nch; ++c) {
                 const int p = c & 1;
                 const int row = b * d.T + a0 + c * kChunk;
+                if (TWO && c + 1 < nch) {
+                    // one stage: every product of the chunk has read it once
+                    // S += K^T V is done (the scores of the next chunk come later)
+                    mbar_wait(smem_u32(&s_done), c & 1);
+                    load(c + 1, 0);
+                }
                 mbar_wait(smem_u32(&o_staged), c & 1);
                 tma_store_3d(&mo, smem_u32(Os), vb * 128, h, row);
                 tma_store_3d(&mo, smem_u32(Os + kTileBytes), vb * 128 + 64, h, row);
                 bulk_commit();
-                mbar_wait(smem_u32(&in_dead[p]), (c >> 1) & 1);  // every read of the stage is done
-                if (c + 2 < nch) load(c + 2, p);
+                if (!TWO) {
+                    mbar_wait(smem_u32(&in_dead[p]), (c >> 1) & 1);  // every read of the stage is done
+                    if (c + 2 < nch) load(c + 2, p);
+                }
                 bulk_wait_read();
                 mbar_arrive(smem_u32(&stg_free));
             }
@@ -2261,16 +2285,17 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
         uint32_t sph = 0, oph = 0, tph = 0;
         for (int c = 0; c < nch; ++c) {
             const int p = c & 1;
+            const int st = TWO ? 0 : p;
             const GateSmem& gs = gsb[p];
-            uint8_t* Qs = smem + p * QKB;
+            uint8_t* Qs = smem + st * QKB;
             uint8_t* Ks = Qs + 2 * kTileBytes;
-            uint8_t* Vs = smem + OFF_V + p * VB;
+            uint8_t* Vs = smem + OFF_V + st * VB;
             // ---- E1
             if (c >= 2) mbar_wait(smem_u32(&gate_ready[p]), ((c - 2) >> 1) & 1);
             mbar_wait(smem_u32(&score_bar), sph);
             sph ^= 1;
-            mbar_wait(smem_u32(&qk_full[p]), (c >> 1) & 1);
-            mbar_wait(smem_u32(&v_full[p]), (c >> 1) & 1);
+            mbar_wait(smem_u32(&qk_full[st]), TWO ? (c & 1) : ((c >> 1) & 1));
+            mbar_wait(smem_u32(&v_full[st]), TWO ? (c & 1) : ((c >> 1) & 1));
             tc_fence_after();
             const bool fact = gs.fact != 0;
             {
@@ -2361,14 +2386,14 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             __syncwarp();
             if (G.lane == 0) {
                 mbar_arrive(smem_u32(&s_ready));
-                mbar_arrive(smem_u32(&in_dead[p]));
+                if (!TWO) mbar_arrive(smem_u32(&in_dead[p]));
                 mbar_arrive(smem_u32(&g_free[p]));
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (G.warp == 0) tmem_dealloc(tmem, 512);
+    if (G.warp == 0) tmem_dealloc(tmem, TCOLS);
 }
 
 // Failure-detection self test: waits on an mbarrier that nothing arrives on,
@@ -2417,6 +2442,19 @@ bool make_map(CUtensorMap* m, const void* base, const Dims& d, int D) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// multiprocessors of the current device (cached per device)
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 template <typename K>
 bool set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) ==
@@ -2426,6 +2464,8 @@ bool set_smem(K kernel, size_t bytes) {
 constexpr size_t kOuterSmem = 96 * 1024 + 1024;
 // Q|K x 2 (8) + V x 2 (4) + P (1) + S (4) + o staging (2)
 constexpr size_t kFwd2Smem = 19 * kTileBytes + 1024;
+// two CTAs a SM: Q|K (4) + V (2) + P (1) + S (4) + o staging (2)
+constexpr size_t kFwd2TwoSmem = 13 * kTileBytes + 1024;
 // Q|K x 2 (8) + V (4) + dO (4) + S (8) + P (1)
 constexpr size_t kDq256Smem = 25 * kTileBytes + 1024;
 // 2 stages x 8 + P (1) + S (4) + gamma's Q (2) + dq staging (2)
@@ -2493,8 +2533,15 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             if (!make_map(&mq, p.q, d, 128) || !make_map(&mk, p.k, d, 128) ||
                 !make_map(&mv, p.v, d, d.Dv) || !make_map(&mo, p.out0, d, d.Dv))
                 return RM_ERR_CUDA;
-            if (!set_smem(tc_fwd2_kernel, kFwd2Smem)) return RM_ERR_CUDA;
-            tc_fwd2_kernel<<<dim3(d.nseg * (d.Dv / 128), d.B * d.H), kRev3Threads, kFwd2Smem, s>>>(
+            // more CTAs than SMs: two a SM (single-stage, 256 tensor-memory
+            // columns) so that each hides the other's latencies; otherwise one
+            // a SM with two stages
+            const dim3 fgrid(d.nseg * (d.Dv / 128), d.B * d.H);
+            const bool two = int64_t(fgrid.x) * fgrid.y > sm_count();
+            auto ff = two ? tc_fwd2_kernel<true> : tc_fwd2_kernel<false>;
+            const size_t fsm = two ? kFwd2TwoSmem : kFwd2Smem;
+            if (!set_smem(ff, fsm)) return RM_ERR_CUDA;
+            ff<<<fgrid, kRev3Threads, fsm, s>>>(
                 d, mq, mk, mv, mo, p.g, p.S_in);
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
             note_launch(1);
