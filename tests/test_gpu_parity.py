@@ -207,3 +207,30 @@ def test_tc_strong_decay():
     compare(select_heads(gpu, None), ref, 2e-2, ("o", "M", "dS", "S_in", "dq", "dk", "dv"))
     ref["dg"] = oracle.backward(q, k, v, g, dO, scale, direct=True)[3]
     compare(select_heads(gpu, None), ref, 2e-2, ("dg",))
+
+
+# ------------------------------------------------------------------ wide grids
+# More CTAs than SMs select the forward sweep that runs two CTAs a SM; these
+# cases put 16 x 16 = 256 (segment, head) sweeps on the GPU with the chunk
+# kinds that take its general path (sequence starts, strong decay).
+
+def test_tc_wide_grid_packed_resets():
+    T = 2048
+    cu = [0, 1, 100, 128, 129, 700, 1024, 1025, 1500, 1999, 2048]
+    check_case(1, T, 16, 128, 128, torch.bfloat16, nseg=16, chunk=64, cu=cu)
+
+
+def test_tc_wide_grid_strong_decay():
+    import oracle
+    q, k, v, g, dO = synth(1, 2048, 16, 128, 128, torch.bfloat16, gate=-30.0)
+    scale = 1.0 / math.sqrt(128)
+    gpu = run_gpu(q, k, v, g, dO, 16, 64, scale)
+    ref = run_oracle(q, k, v, g, dO, 16, scale)
+    compare(select_heads(gpu, None), ref, 2e-2, ("o", "M", "dS", "S_in", "dq", "dk", "dv"))
+    ref["dg"] = oracle.backward(q, k, v, g, dO, scale, direct=True)[3]
+    compare(select_heads(gpu, None), ref, 2e-2, ("dg",))
+
+
+def test_tc_wide_grid_value_blocks():
+    # Dv = 256: two value blocks per (segment, head) -> 512 forward CTAs
+    check_case(1, 1024, 16, 128, 256, torch.bfloat16, nseg=16, chunk=64, seed=5)
