@@ -1249,24 +1249,27 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
 // reverse sweep for Dv = 256, warp-specialised like the Dv = 128 sweep.  At
 // Dv = 256 the fp32 adjoint E (128 x 256) would take 128 registers a thread,
 // so it lives in tensor memory instead, where dE = Q~^T dO accumulates into
-// it; the epilogue scales it by W before each chunk's dE and snapshots it to
-// the bf16 E tile that the next chunk's products read.
-// Tensor memory: [0,128) the scores, then dv for one 128-column half at a
-// time; [128,256) dk'; [256,512) E.
+// it; the epilogue snapshots it to the bf16 E tile that the next chunk's
+// products read and, in the same pass, scales the tensor-memory copy by W of
+// that chunk ahead of its dE.
+// Tensor memory: [0,128) the scores, then dv half 0; [128,256) dk', then dv
+// half 1; [256,512) E.
 // Shared memory: Q|K by chunk parity (2 x 32 KB), V and dO (32 KB each,
 // refilled as soon as their last reader is done), E as bf16 (64 KB), PA, PD.
 //   warps 0-7 (epilogues), per chunk:
-//     E1  score masks; factored: dO~ in place, E *= W  -> pv_ready, kq_ready
+//     E1  score masks; factored: dO~ in place          -> pv_ready, kq_ready
 //                      general: V~ in place           -> pv_ready
 //     E2  dk rows                                     -> v_dead
-//         general: K~, Q~ in place, E *= W            -> kq_ready
+//         general: K~, Q~ in place                    -> kq_ready
+//         (dk' read                                   -> dk_read)
 //         dv rows of half 0                           -> dv0_read
-//         dv rows of half 1                           -> in_dead, dv1_read
-//         E snapshot                                  -> e_ready, b_ready
+//         dv rows of half 1                           -> in_dead
+//         E snapshot (and E *= W of the next chunk)   -> e_ready, b_ready
 //   warp 8 (one thread): the tensor products; in factored chunks V E^T and
 //     K E need no epilogue work, V E^T is issued as soon as E is in place.
 //   warp 9: the gate-gradient scan and the gate tables two chunks ahead.
-//   warp 10 (one thread): V, dO and Q|K loads as the tiles die.
+//   warp 10 (one thread): V, dO and Q|K loads as the tiles die (dO at the
+//     commit of the chunk's last products).
 // ===========================================================================
 __global__ void __launch_bounds__(kRev3Threads, 1)
     tc_rev256_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
@@ -1290,7 +1293,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
     __shared__ GateSmem gsb[2];
     __shared__ __align__(8) uint64_t qk_full[2], v_full, d_full;
     __shared__ __align__(8) uint64_t score_bar, dk_done, dv0_done, dv1_done;  // tensor-core commits
-    __shared__ __align__(8) uint64_t pv_ready, kq_ready, dv0_read, dv1_read, e_ready;  // epilogue -> warp 8
+    __shared__ __align__(8) uint64_t pv_ready, kq_ready, dk_read, dv0_read, e_ready;  // epilogue -> warp 8
     __shared__ __align__(8) uint64_t v_dead, in_dead;  // epilogue -> warp 10
     __shared__ __align__(8) uint64_t b_ready[2], scan_done[2], gate_ready[2];
     __shared__ uint32_t tmem_slot;
@@ -1320,7 +1323,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
         mbar_init(smem_u32(&dk_done), 1);
         mbar_init(smem_u32(&dv0_done), 1);
         mbar_init(smem_u32(&dv1_done), 1);
-        for (uint64_t* bar : {&pv_ready, &kq_ready, &dv0_read, &dv1_read, &e_ready, &v_dead, &in_dead})
+        for (uint64_t* bar : {&pv_ready, &kq_ready, &dk_read, &dv0_read, &e_ready, &v_dead, &in_dead})
             mbar_init(smem_u32(bar), 8);
         mbar_fence_init();
     }
@@ -1345,6 +1348,9 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
         // S_out read as S_in[seg + 1].
         const float* src = dS_out + sum_off(d, seg, b, h) + int64_t(G.srow) * DV + 128 * G.grp;
         const float* so = S_in + sum_off(d, seg + 1, b, h) + int64_t(G.srow) * DV + 128 * G.grp;
+        // the tensor-memory E is kept scaled by W of the chunk about to
+        // accumulate into it (the bf16 tile holds it unscaled)
+        const float W0 = gsb[0].W;
         float ext = 0.f;
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
@@ -1360,10 +1366,13 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                     ext = fmaf(x.z, y.z, ext); ext = fmaf(x.w, y.w, ext);
                 }
             }
-            tmem_st32(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
             float f[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
+            for (int i = 0; i < 32; ++i) {
+                f[i] = __uint_as_float(r[i]);
+                r[i] = __float_as_uint(W0 * f[i]);
+            }
+            tmem_st32(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 *reinterpret_cast<uint4*>(Eb + sw_chunk(128, G.srow, 16 * G.grp + 4 * j + c)) = pack8(f + 8 * c);
@@ -1407,17 +1416,19 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                              sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk,
                              (first && k == 0) ? 0u : 1u);
             };
-            auto issue_dv = [&](int hh, uint32_t kx, bool fact) {  // dv_hh = PA^T dO_hh + K E_hh
+            // dv_hh = PA^T dO_hh + K E_hh, half 0 into the scores' columns, half 1
+            // into dk''s (free once the dk rows have been read)
+            auto issue_dv = [&](int hh, uint32_t kx) {
                 const uint32_t dah = da + 2 * hh * kTileBytes, eah = ea + 4 * hh * kTileBytes;
+                const uint32_t acc = tmem + 128 * hh;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem, sdesc(pa + k * 2048, kTileBytes, 1024), sdesc(dah + k * 2048, kTileBytes, 1024),
+                    mma_bf16(acc, sdesc(pa + k * 2048, kTileBytes, 1024), sdesc(dah + k * 2048, kTileBytes, 1024),
                              id_mm, k > 0);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_bf16(tmem, sdesc(kx + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                    mma_bf16(acc, sdesc(kx + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
                              sdesc(eah + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
-                (void)fact;
             };
             mbar_wait(smem_u32(&qk_full[0]), 0);
             mbar_wait(smem_u32(&v_full), 0);
@@ -1440,18 +1451,18 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 mma_commit(smem_u32(&dk_done));
                 mbar_wait(smem_u32(&kq_ready), ph);  // dO~ or K~, Q~ in place; E scaled by W
                 tc_fence_after();
-                issue_dv(0, ka, fact);
+                issue_dv(0, ka);
                 mma_commit(smem_u32(&dv0_done));
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // E += Q~^T dO (all 256 columns)
                     mma_bf16(tmem + TE, sdesc(qa + k * 2048, kTileBytes, 1024), sdesc(da + k * 2048, kTileBytes, 1024),
                              id_e, 1u);
-                mbar_wait(smem_u32(&dv0_read), ph);
+                mbar_wait(smem_u32(&dk_read), ph);  // dk' columns read: dv half 1 goes there
                 tc_fence_after();
-                issue_dv(1, ka, fact);
+                issue_dv(1, ka);
                 mma_commit(smem_u32(&dv1_done));
                 if (it + 1 < nch) {
-                    mbar_wait(smem_u32(&dv1_read), ph);
+                    mbar_wait(smem_u32(&dv0_read), ph);  // the scores overwrite dv half 0
                     mbar_wait(smem_u32(&qk_full[p ^ 1]), ((it + 1) >> 1) & 1);
                     mbar_wait(smem_u32(&v_full), (it + 1) & 1);
                     mbar_wait(smem_u32(&d_full), (it + 1) & 1);
@@ -1492,8 +1503,9 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 const uint32_t ph = it & 1;
                 mbar_wait(smem_u32(&v_dead), ph);  // dk' and the scores are done with V
                 load_one(it + 1, Vs, &mv, &v_full);
-                mbar_wait(smem_u32(&in_dead), ph);  // the chunk's last products are done
+                mbar_wait(smem_u32(&dv1_done), ph);  // the chunk's last products (dO's readers) are done
                 load_one(it + 1, Ds, &mdo, &d_full);
+                mbar_wait(smem_u32(&in_dead), ph);  // ... and the dk rows have read Q and K
                 if (it + 2 < nch) load_qk(it + 2, it & 1);
             }
         }
@@ -1521,19 +1533,6 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
         }
     } else {  // epilogue warps
         uint32_t sph = 0, kph = 0, v0ph = 0, v1ph = 0;
-        // E *= W for this thread's 128 columns of the tensor-memory adjoint
-        auto scale_e = [&](float W) {
-#pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                tmem_ld32_nowait(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(W * __uint_as_float(r[i]));
-                tmem_st32(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
-            }
-            tmem_wait_st();
-        };
         for (int it = 0; it < nch; ++it) {
             const int c = nch - 1 - it;
             const int t0 = a0 + c * kChunk;
@@ -1592,7 +1591,6 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             if (fact) {
                 scale_tile(Ds, Ds, gs.win, d.scale, G.tid);
                 scale_tile(Ds + 2 * kTileBytes, Ds + 2 * kTileBytes, gs.win, d.scale, G.tid);
-                scale_e(gs.W);
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
@@ -1630,13 +1628,15 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 bk += __shfl_xor_sync(kFull, bk, 16);
                 if (!G.hi) bpart[p][G.grp][G.tau] = bk;
             }
+            tc_fence_before();
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&dk_read));
             if (!fact) {
                 // K~ = wout K and Q~ = scale win Q in place, once every epilogue
                 // warp has read its q, k rows
                 asm volatile("bar.sync 1, 256;" ::: "memory");
                 scale_tile(Ks, Ks, gs.wout, 1.f, G.tid);
                 scale_tile(Qs, Qs, gs.win, d.scale, G.tid);
-                scale_e(gs.W);
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
@@ -1653,10 +1653,12 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                     if (G.lane == 0) mbar_arrive(smem_u32(&in_dead));
                 }
                 float xx[2][16];
-                tok16x2(tmem, G, 64 * G.grp, 64 * G.grp + 32, xx[0], xx[1]);
-                tc_fence_before();
-                __syncwarp();
-                if (G.lane == 0) mbar_arrive(smem_u32(hh == 0 ? &dv0_read : &dv1_read));
+                tok16x2(tmem, G, 128 * hh + 64 * G.grp, 128 * hh + 64 * G.grp + 32, xx[0], xx[1]);
+                if (hh == 0) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (G.lane == 0) mbar_arrive(smem_u32(&dv0_read));
+                }
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
 #pragma unroll
@@ -1664,15 +1666,31 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                     store_bf16x16(dv + tok * DV + 128 * hh + 64 * G.grp + 32 * k + 16 * G.hi, xx[k]);
                 }
             }
-            // ---- E2: E snapshot (the chunk's products are done with the E tile)
+            // ---- E2: E snapshot (the chunk's products are done with the E tile);
+            // the tensor-memory copy is scaled by W of the next chunk, ahead
+            // of that chunk's dE
+            float Wn = 1.f;
+            if (it + 1 < nch) {
+                if (it + 1 >= 2) mbar_wait(smem_u32(&gate_ready[p ^ 1]), ((it - 1) >> 1) & 1);
+                Wn = gsb[p ^ 1].W;
+            }
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
                 float f[32];
-                tmem_ld32(tmem + G.tl + TE + 128 * G.grp + 32 * j, f);
+                tmem_ld32_nowait(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    f[i] = __uint_as_float(r[i]);
+                    r[i] = __float_as_uint(Wn * f[i]);
+                }
+                if (it + 1 < nch) tmem_st32(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
                     *reinterpret_cast<uint4*>(Eb + sw_chunk(128, G.srow, 16 * G.grp + 4 * j + cc)) = pack8(f + 8 * cc);
             }
+            tmem_wait_st();
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
