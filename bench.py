@@ -186,6 +186,24 @@ def cpu_baseline(w, inp, target_s=12.0):
             "seconds": dt}
 
 
+# ------------------------------------------------------------------ replicas
+
+def replica_time(ms_local: float, world: int, device) -> float:
+    """Max over ranks of a per-rank time (the slowest replica sets the step);
+    a no-op on one process.  Uses whatever backend the process group has
+    (NCCL with a CUDA device, gloo with the CPU)."""
+    if world <= 1:
+        return float(ms_local)
+    t = torch.tensor([float(ms_local)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, tokens_per_step: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every replica processes tokens_per_step per step."""
+    return world * tokens_per_step / (ms_per_step / 1e3)
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_ours(args, rank, world, local_rank):
@@ -253,14 +271,10 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    total_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = replica_time(start.elapsed_time(end), world, dev)
     ms_per_step = total_ms / args.steps
     tok_per_step = w.B * w.T
-    value = world * tok_per_step / (ms_per_step / 1e3)
+    value = replica_throughput(world, tok_per_step, ms_per_step)
 
     phase_ms = {ph: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
                 for j, ph in enumerate(phases)}
@@ -308,12 +322,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = a.elapsed_time(b) / n_e2e
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * tok_per_step / (e_ms / 1e3), "unit": "tokens/s",
+        e_ms = replica_time(a.elapsed_time(b) / n_e2e, world, dev)
+        e2e = {"value": replica_throughput(world, tok_per_step, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
                "ms_per_step": e_ms}
