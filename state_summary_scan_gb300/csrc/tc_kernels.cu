@@ -1675,20 +1675,27 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 Wn = gsb[p ^ 1].W;
             }
 #pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                float f[32];
-                tmem_ld32_nowait(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
+            for (int j = 0; j < 4; j += 2) {  // two 32-column loads in flight at a time
+                uint32_t r0[32], r1[32];
+                tmem_ld32_nowait(tmem + G.tl + TE + 128 * G.grp + 32 * j, r0);
+                tmem_ld32_nowait(tmem + G.tl + TE + 128 * G.grp + 32 * (j + 1), r1);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    f[i] = __uint_as_float(r[i]);
-                    r[i] = __float_as_uint(Wn * f[i]);
+                for (int cc = 0; cc < 4; ++cc) {
+                    *reinterpret_cast<uint4*>(Eb + sw_chunk(128, G.srow, 16 * G.grp + 4 * j + cc)) =
+                        pack8(reinterpret_cast<const float*>(r0) + 8 * cc);
+                    *reinterpret_cast<uint4*>(Eb + sw_chunk(128, G.srow, 16 * G.grp + 4 * (j + 1) + cc)) =
+                        pack8(reinterpret_cast<const float*>(r1) + 8 * cc);
                 }
-                if (it + 1 < nch) tmem_st32(tmem + G.tl + TE + 128 * G.grp + 32 * j, r);
+                if (it + 1 < nch) {
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4*>(Eb + sw_chunk(128, G.srow, 16 * G.grp + 4 * j + cc)) = pack8(f + 8 * cc);
+                    for (int i = 0; i < 32; ++i) {
+                        r0[i] = __float_as_uint(Wn * __uint_as_float(r0[i]));
+                        r1[i] = __float_as_uint(Wn * __uint_as_float(r1[i]));
+                    }
+                    tmem_st32(tmem + G.tl + TE + 128 * G.grp + 32 * j, r0);
+                    tmem_st32(tmem + G.tl + TE + 128 * G.grp + 32 * (j + 1), r1);
+                }
             }
             tmem_wait_st();
             fence_async_smem();
@@ -2029,26 +2036,31 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             if (G.lane == 0) mbar_arrive(smem_u32(&in_dead[p]));
             // ---- E2: state snapshot (dS has accumulated: it precedes dq' in
             // the commit that dq_done tracks)
+            {  // two 32-column loads in flight at a time
+                const float Wf = fact ? gs.W : 1.f;  // S = W (S_prev + K^T^ V) in factored chunks
 #pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                float f[32];
-                tmem_ld32_nowait(tmem + G.tl + TS + 128 * G.grp + 32 * j, r);
-                tmem_wait_ld();
-                if (fact) {  // S = W (S_prev + K^T^ V)
+                for (int j = 0; j < 4; j += 2) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32_nowait(tmem + G.tl + TS + 128 * G.grp + 32 * j, r0);
+                    tmem_ld32_nowait(tmem + G.tl + TS + 128 * G.grp + 32 * (j + 1), r1);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        f[i] = gs.W * __uint_as_float(r[i]);
-                        r[i] = __float_as_uint(f[i]);
+                        r0[i] = __float_as_uint(Wf * __uint_as_float(r0[i]));
+                        r1[i] = __float_as_uint(Wf * __uint_as_float(r1[i]));
                     }
-                    tmem_st32(tmem + G.tl + TS + 128 * G.grp + 32 * j, r);
-                } else {
+                    if (fact) {
+                        tmem_st32(tmem + G.tl + TS + 128 * G.grp + 32 * j, r0);
+                        tmem_st32(tmem + G.tl + TS + 128 * G.grp + 32 * (j + 1), r1);
+                    }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
+                    for (int cc = 0; cc < 4; ++cc) {
+                        *reinterpret_cast<uint4*>(Sb + sw_chunk(128, G.srow, 16 * G.grp + 4 * j + cc)) =
+                            pack8(reinterpret_cast<const float*>(r0) + 8 * cc);
+                        *reinterpret_cast<uint4*>(Sb + sw_chunk(128, G.srow, 16 * G.grp + 4 * (j + 1) + cc)) =
+                            pack8(reinterpret_cast<const float*>(r1) + 8 * cc);
+                    }
                 }
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4*>(Sb + sw_chunk(128, G.srow, 16 * G.grp + 4 * j + cc)) = pack8(f + 8 * cc);
             }
             tmem_wait_st();
             fence_async_smem();
