@@ -234,18 +234,6 @@ __device__ __forceinline__ void unpack8(uint4 u, float* x) {
         x[2 * i + 1] = f.y;
     }
 }
-// Multiplies the 64 bf16 values of one 128-byte tile row by w (rounded to bf16).
-__device__ __forceinline__ void scale_row128(uint8_t* row, float w) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint4* p = reinterpret_cast<uint4*>(row + c * 16);
-        float x[8];
-        unpack8(*p, x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] *= w;
-        *p = pack8(x);
-    }
-}
 
 // ------------------------------------------------------------------ gates
 // Per-chunk gate quantities (chunk-local, tau = 0..63):

@@ -40,7 +40,6 @@ namespace {
 
 constexpr uint32_t kTileBytes = kChunk * 64 * 2;  // one [64 rows][64 cols] bf16 block: 8 KB
 constexpr int kThreads = 256;                     // 8 warps: two per tensor-memory lane quadrant
-constexpr int kRevThreads = kThreads + 64;        // + a control warp and a gate/scan warp
 constexpr int kRev3Threads = kThreads + 96;       // + an MMA warp, a gate/scan warp and a copy warp
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -158,7 +157,9 @@ __device__ __forceinline__ void state_update_scaled(uint32_t tmem, const Geo& g,
     store_state_half(tile, g.srow, g.grp, S);
 }
 
-// state_update_half with both 32-column loads in flight together
+// S[64 hh + e] = W S[64 hh + e] + acc[srow][col + 64 grp + e] (accumulator
+// holding state columns [128 hh, +128) at column col), with both 32-column
+// tensor-memory loads in flight together; writes those columns as bf16.
 __device__ __forceinline__ void state_update_half2(uint32_t tmem, const Geo& g, int col, int hh, float W,
                                                    float* S, uint8_t* tile) {
     uint32_t r0[32], r1[32];
@@ -194,22 +195,6 @@ __device__ __forceinline__ void load_state_rows(const float* __restrict__ src, c
             *reinterpret_cast<uint4*>(tile + sw_chunk(128, g.srow, 16 * hh + 8 * g.grp + c)) =
                 pack8(S + 64 * hh + c * 8);
     }
-}
-// S[64 hh + e] = W S[64 hh + e] + acc[srow][col + 64 grp + e] (accumulator holding
-// state columns [128 hh, +128) at column col); writes those columns as bf16.
-__device__ __forceinline__ void state_update_half(uint32_t tmem, const Geo& g, int col, int hh, float W,
-                                                  float* S, uint8_t* tile) {
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-        float y[32];
-        tmem_ld32(tmem + g.tl + col + 64 * g.grp + 32 * hf, y);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) S[64 * hh + 32 * hf + e] = fmaf(W, S[64 * hh + 32 * hf + e], y[e]);
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(tile + sw_chunk(128, g.srow, 16 * hh + 8 * g.grp + c)) =
-            pack8(S + 64 * hh + c * 8);
 }
 
 // Row scaling of a [64][128] bf16 tile (2 blocks x 64 rows x 8 chunks of 16
