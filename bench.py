@@ -186,6 +186,17 @@ def cpu_baseline(w, inp, target_s=12.0):
             "seconds": dt}
 
 
+def workload_of(args):
+    """The chosen workload; --T keeps its segment length and shrinks T (a
+    smaller case of the same kernels for profiling captures, named as such)."""
+    w = WORKLOADS[args.workload]
+    if args.T:
+        if args.T % w.seg_len or w.packed:
+            raise SystemExit(f"--T must be a multiple of {w.seg_len} (and the workload not packed)")
+        w = w.replace(T=args.T, num_segments=args.T // w.seg_len, name=f"{w.name}-T{args.T}")
+    return w
+
+
 # ------------------------------------------------------------------ replicas
 
 def replica_time(ms_local: float, world: int, device) -> float:
@@ -212,7 +223,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     peaks, peak_src = load_peaks()
     inp = make_inputs(w)
     q, k, v, g = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.g))
@@ -281,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
     dom = max(phase_ms, key=phase_ms.get)
     dom_bytes = kernel_bytes(w, dom)
     achieved = dom_bytes / (phase_ms[dom] / 1e3) / 1e9
-    traffic = load_traffic(args.workload, dom)
+    traffic = load_traffic(w.name, dom)
     roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
             "traffic": traffic, "algorithmic_bytes": dom_bytes, "launch_us": phase_ms[dom] * 1e3,
@@ -354,7 +365,7 @@ def run_ours(args, rank, world, local_rank):
 
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm, timed per step on host cores."""
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     inp = make_inputs(w)
     budget = max(2.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
     ntok = calibrate_oracle(w, inp, budget)
@@ -403,6 +414,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--T", type=int, default=0,
+                    help="shorter T with the same segment length (profiling captures of a smaller case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
