@@ -15,7 +15,8 @@
 // copy for the next chunk's products.
 //
 // Kernels (one CTA per (segment, row, head[, value block])):
-//   tc_outer_kernel     sum_t w_t x_t y_t^T over a segment: delta_S of
+//   tc_outer2_kernel    (Dv = 128, barrier-paced) and tc_outer_kernel (Dv = 256):
+//                       sum_t w_t x_t y_t^T over a segment: delta_S of
 //                       cp_forward_prepare (x = k, y = v, w = decay to the
 //                       segment end) and gamma of cp_backward_prepare (x = q,
 //                       y = dO, w = scale * decay from the segment start)
@@ -2411,6 +2412,158 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
     if (G.warp == 0) tmem_dealloc(tmem, TCOLS);
 }
 
+// ===========================================================================
+// sum_t w_t x_t y_t^T over a segment (delta_S of forward prepare: x = k, y = v,
+// w = decay to the segment end, chunks walked from the last one; gamma of
+// backward prepare: x = q, y = dO, w = scale * decay from the segment start),
+// paced by mbarriers: warps 0-7 scale each chunk's x rows by w in place as soon
+// as it lands (xready), warp 8 (one thread) issues the chunk's products and the
+// stage refills, warp 9 builds the gate tables two chunks ahead.  The scaling
+// of one chunk overlaps the products of the one before.
+// ===========================================================================
+template <int DV, bool GAMMA>
+__global__ void __launch_bounds__(kThreads + 64, 2)
+    tc_outer2_kernel(const Dims d, const __grid_constant__ CUtensorMap mx,
+                     const __grid_constant__ CUtensorMap my, const float* __restrict__ g,
+                     float* __restrict__ M, float* __restrict__ out) {
+    constexpr int NS = DV == 128 ? 3 : 2;
+    constexpr uint32_t XBYTES = 2 * kTileBytes;
+    constexpr uint32_t YBYTES = (DV / 64) * kTileBytes;
+    constexpr uint32_t SBYTES = XBYTES + YBYTES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    __shared__ GateSmem gsb[2];
+    __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS], xready[NS];
+    __shared__ __align__(8) uint64_t done_bar, gate_ready[2], g_free[2];
+    __shared__ uint32_t tmem_slot;
+
+    const Geo G = geo();
+    const bool epi = G.warp < 8;
+    const bool ctl = G.warp == 8;
+    const bool gat = G.warp == 9;
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+    // gamma walks forward from the segment start, delta_S backward from its end
+    auto chunk_of = [&](int it) { return GAMMA ? it : nch - 1 - it; };
+
+    if (G.tid == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(smem_u32(&full_bar[i]), 1);
+            mbar_init(smem_u32(&empty_bar[i]), 1);
+            mbar_init(smem_u32(&xready[i]), 8);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&gate_ready[i]), 1);
+            mbar_init(smem_u32(&g_free[i]), 8);
+        }
+        mbar_init(smem_u32(&done_bar), 1);
+        mbar_fence_init();
+    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), DV);
+    GateRegs gr;
+    if (gat) {
+        gr = gate_load(d, g, b, h, a0 + chunk_of(0) * kChunk, G.lane);
+        gate_prep(gr, &gsb[0], G.lane);
+        if (nch > 1) {
+            gr = gate_load(d, g, b, h, a0 + chunk_of(1) * kChunk, G.lane);
+            gate_prep(gr, &gsb[1], G.lane);
+        }
+        if (nch > 2) gr = gate_load(d, g, b, h, a0 + chunk_of(2) * kChunk, G.lane);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (ctl) {
+        if (G.lane == 0) {
+            auto issue = [&](int it, int s) {
+                const int row = b * d.T + a0 + chunk_of(it) * kChunk;
+                const uint32_t bar = smem_u32(&full_bar[s]);
+                uint8_t* st = smem + s * SBYTES;
+                mbar_expect_tx(bar, SBYTES);
+                load_tile(st, &mx, 0, 128, h, row, bar);
+                load_tile(st + XBYTES, &my, 0, DV, h, row, bar);
+            };
+            for (int it = 0; it < NS && it < nch; ++it) issue(it, it);
+            constexpr uint32_t idesc = idesc_bf16(128, DV, 1, 1);
+            for (int it = 0; it < nch; ++it) {
+                const int s = it % NS;
+                mbar_wait(smem_u32(&xready[s]), (it / NS) & 1);
+                tc_fence_after();
+                const uint32_t xa = smem_u32(smem + s * SBYTES), ya = xa + XBYTES;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(tmem, sdesc(xa + k * 2048, kTileBytes, 1024), sdesc(ya + k * 2048, kTileBytes, 1024),
+                             idesc, (it > 0 || k > 0) ? 1u : 0u);
+                mma_commit(smem_u32(&empty_bar[s]));
+                // refill the stage the previous chunk's products have finished with
+                const int prev = it - 1;
+                if (prev >= 0 && prev + NS < nch) {
+                    const int ps = prev % NS;
+                    mbar_wait(smem_u32(&empty_bar[ps]), (prev / NS) & 1);
+                    issue(prev + NS, ps);
+                }
+            }
+            mma_commit(smem_u32(&done_bar));
+        }
+    } else if (gat) {
+        for (int it = 0; it + 2 < nch; ++it) {
+            const int p = it & 1;
+            mbar_wait(smem_u32(&g_free[p]), (it >> 1) & 1);
+            gate_prep(gr, &gsb[p], G.lane);
+            if (it + 3 < nch) gr = gate_load(d, g, b, h, a0 + chunk_of(it + 3) * kChunk, G.lane);
+            __syncwarp();
+            if (G.lane == 0) mbar_arrive(smem_u32(&gate_ready[p]));
+        }
+    } else {  // epilogue warps
+        float run = 0.f;  // sum of the gates of the chunks already walked
+        int seen = 0;     // a sequence starts in the chunks already walked
+        for (int it = 0; it < nch; ++it) {
+            const int s = it % NS, p = it & 1;
+            const GateSmem& gs = gsb[p];
+            if (it >= 2) mbar_wait(smem_u32(&gate_ready[p]), ((it - 2) >> 1) & 1);
+            mbar_wait(smem_u32(&full_bar[s]), (it / NS) & 1);
+            uint8_t* xt = smem + s * SBYTES;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                int r;
+                const uint32_t off = scale_off(G.tid, k, &r);
+                float w;
+                if (GAMMA)  // scale * alpha_a ... alpha_t: no start in [a, t]
+                    w = (!seen && !gs.first && gs.lid[r] == 0) ? d.scale * expf(run + gs.b[r]) : 0.f;
+                else        // alpha_{t+1} ... alpha_end: no start in (t, end]
+                    w = (!seen && gs.lid[r] == gs.lid[kChunk - 1]) ? expf(run + gs.btot - gs.b[r]) : 0.f;
+                scale_chunk(xt + off, xt + off, w);
+            }
+            run += gs.btot;
+            seen |= gs.any;
+            fence_async_smem();
+            __syncwarp();
+            if (G.lane == 0) {
+                mbar_arrive(smem_u32(&xready[s]));
+                mbar_arrive(smem_u32(&g_free[p]));
+            }
+        }
+        mbar_wait(smem_u32(&done_bar), 0);
+        tc_fence_after();
+        float* dst = out + sum_off(d, seg, b, h) + int64_t(G.srow) * DV;
+#pragma unroll 1
+        for (int c = G.grp * (DV / 2); c < (G.grp + 1) * (DV / 2); c += 64) {
+            float v[64];
+            state_cols64(tmem, G, c - 64 * G.grp, v);
+#pragma unroll
+            for (int i = 0; i < 64; i += 4)
+                *reinterpret_cast<float4*>(dst + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
+        if (!GAMMA && G.tid == 0) M[(int64_t(seg) * d.B + b) * d.H + h] = seen ? 0.f : expf(run);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, DV);
+}
+
 // Failure-detection self test: waits on an mbarrier that nothing arrives on,
 // with the given bound, so that the timeout path and its host-side status can
 // be exercised without faulting or hanging the device.
@@ -2531,10 +2684,12 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
         case Op::kForwardPrepare: {
             if (!make_map(&mk, p.k, d, 128) || !make_map(&mv, p.v, d, d.Dv)) return RM_ERR_CUDA;
             if (d.Dv == 128) {
-                auto fn = tc_outer_kernel<128, false>;
+                auto fn = tc_outer2_kernel<128, false>;
                 if (!set_smem(fn, kOuterSmem)) return RM_ERR_CUDA;
-                fn<<<grid, kThreads, kOuterSmem, s>>>(d, mk, mv, p.g, p.M, p.sum_out);
+                fn<<<grid, kThreads + 64, kOuterSmem, s>>>(d, mk, mv, p.g, p.M, p.sum_out);
             } else {
+                // at Dv = 256 (two stages) the barrier-paced variant measured
+                // no faster than the original one
                 auto fn = tc_outer_kernel<256, false>;
                 if (!set_smem(fn, kOuterSmem)) return RM_ERR_CUDA;
                 fn<<<grid, kThreads, kOuterSmem, s>>>(d, mk, mv, p.g, p.M, p.sum_out);
