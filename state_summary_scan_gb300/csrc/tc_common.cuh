@@ -198,6 +198,13 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
            (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
+// The descriptor of the address `bytes` past that of d: one 32-bit add on the
+// start-address field (shared-memory addresses stay below 256 KB, so the
+// 14-bit field cannot carry into the next one).  Building descriptors this way
+// keeps the issuing thread at about one add per operand and MMA.
+__device__ __forceinline__ uint64_t desc_plus(uint64_t d, uint32_t bytes) {
+    return (uint64_t(uint32_t(d >> 32)) << 32) | uint32_t(uint32_t(d) + (bytes >> 4));
+}
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 D, dense.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) |

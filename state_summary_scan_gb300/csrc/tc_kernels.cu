@@ -926,21 +926,28 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
 
     if (ctl) {
         if (G.lane == 0) {
+            // Descriptors of the shared-memory operands: the three layouts
+            // (K-major, MN-major with 64-column blocks one or two tiles apart)
+            // at the start of shared memory; every operand is an offset from it.
+            const uint32_t sb0 = smem_u32(smem);
+            const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, kTileBytes, 1024);
+            const uint64_t DM2 = sdesc(sb0, 2 * kTileBytes, 1024);
             // score products A = Q K^T and dA = dO V^T of the chunk in stage s
             auto issue_scores = [&](int s) {
-                const uint32_t qa = smem_u32(smem + s * STAGE), ka = qa + 2 * kTileBytes;
-                const uint32_t va = qa + 4 * kTileBytes, da = qa + 6 * kTileBytes;
+                const uint64_t q = desc_plus(DK, s * STAGE), kk = desc_plus(q, 2 * kTileBytes);
+                const uint64_t v = desc_plus(q, 4 * kTileBytes), o = desc_plus(q, 6 * kTileBytes);
                 constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
-                    mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, k > 0);
-                    mma_bf16(tmem + 64, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+                    mma_bf16(tmem, desc_plus(q, off), desc_plus(kk, off), id1, k > 0);
+                    mma_bf16(tmem + 64, desc_plus(o, off), desc_plus(v, off), id1, k > 0);
                 }
                 mma_commit(smem_u32(&score_bar));
             };
-            const uint32_t pa = smem_u32(PA), pd = smem_u32(PD), ea = smem_u32(Eb);
-            const uint32_t qta = smem_u32(Qt), kta = smem_u32(Kt);
+            const uint64_t pa = desc_plus(DM, OFF_PA), pd = desc_plus(DM, OFF_PD);
+            const uint64_t ek = desc_plus(DK, OFF_E), em = desc_plus(DM2, OFF_E);
+            const uint64_t qt = desc_plus(DM, OFF_QT), kt = desc_plus(DK, OFF_KT);
             constexpr uint32_t id_mm = idesc_bf16(64, 128, 1, 1);
             constexpr uint32_t id_kk = idesc_bf16(64, 128, 0, 0);
             constexpr uint32_t id_km = idesc_bf16(64, 128, 0, 1);
@@ -949,19 +956,20 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             // dv = K E, use unscaled tiles and the adjoint of the chunk after
             // it: they are issued as soon as that adjoint is in the E tile,
             // ahead of the chunk's score masks.
-            auto issue_ve = [&](int s) {  // dk' = V E^T
-                const uint32_t va = smem_u32(smem + s * STAGE) + 4 * kTileBytes;
-#pragma unroll 1
-                for (int k = 0; k < 8; ++k)
-                    mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                             sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, k > 0);
+            auto issue_ve = [&](int s, uint32_t acc) {  // dk' (+)= V~ E^T
+                const uint64_t v = desc_plus(DK, s * STAGE + 4 * kTileBytes);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
+                    mma_bf16(tmem + 128, desc_plus(v, off), desc_plus(ek, 2 * off - (k & 3) * 32), id_kk,
+                             (acc || k > 0) ? 1u : 0u);
+                }
             };
-            auto issue_ke = [&](int s) {  // dv = K E
-                const uint32_t ka = smem_u32(smem + s * STAGE) + 2 * kTileBytes;
-#pragma unroll 1
+            auto issue_ke = [&](uint64_t kk, uint32_t acc) {  // dv (+)= K E
+#pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_bf16(tmem + 256, sdesc(ka + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                             sdesc(ea + k * 2048, 2 * kTileBytes, 1024), id_km, k > 0);
+                    mma_bf16(tmem + 256, desc_plus(kk, (k >> 2) * kTileBytes + (k & 3) * 32),
+                             desc_plus(em, k * 2048), id_km, (acc || k > 0) ? 1u : 0u);
             };
             mbar_wait(smem_u32(&full_bar[0]), 0);
             tc_fence_after();
@@ -969,43 +977,31 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             // factored chunks keep K, Q and V unscaled (the weights sit in the
             // score masks, on dO and on the output rows)
             bool fact = gsb[0].fact != 0;
-            if (fact) issue_ve(0);
+            if (fact) issue_ve(0, 0);
             for (int it = 0; it < nch; ++it) {
                 const int s = it & 1;
                 const uint32_t ph = it & 1;
-                const uint32_t qa = smem_u32(smem + s * STAGE);
-                const uint32_t va = qa + 4 * kTileBytes, da = qa + 6 * kTileBytes;
+                const uint64_t q = desc_plus(DM, s * STAGE), o = desc_plus(DM, s * STAGE + 6 * kTileBytes);
                 mbar_wait(smem_u32(&pv_ready), ph);
                 tc_fence_after();
-#pragma unroll 1
+#pragma unroll
                 for (int k = 0; k < 4; ++k)  // dk' (+)= PdA^T Q
-                    mma_bf16(tmem + 128, sdesc(pd + k * 2048, kTileBytes, 1024),
-                             sdesc(qa + k * 2048, kTileBytes, 1024), id_mm, (fact || k > 0) ? 1u : 0u);
-                if (!fact) {
-#pragma unroll 1
-                    for (int k = 0; k < 8; ++k)  // dk' += V~ E^T
-                        mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                                 sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk, 1);
-                }
+                    mma_bf16(tmem + 128, desc_plus(pd, k * 2048), desc_plus(q, k * 2048), id_mm,
+                             (fact || k > 0) ? 1u : 0u);
+                if (!fact) issue_ve(s, 1);  // dk' += V~ E^T
                 mma_commit(smem_u32(&dk_done));
-                if (fact) issue_ke(s);  // E-side of dv, behind the dk' products
+                if (fact) issue_ke(desc_plus(DK, s * STAGE + 2 * kTileBytes), 0);  // behind the dk' products
                 mbar_wait(smem_u32(&kq_ready), ph);
                 tc_fence_after();
-#pragma unroll 1
+#pragma unroll
                 for (int k = 0; k < 4; ++k)  // dv (+)= PA^T dO
-                    mma_bf16(tmem + 256, sdesc(pa + k * 2048, kTileBytes, 1024),
-                             sdesc(da + k * 2048, kTileBytes, 1024), id_mm, (fact || k > 0) ? 1u : 0u);
-                if (!fact) {
-#pragma unroll 1
-                    for (int k = 0; k < 8; ++k)  // dv += K~ E
-                        mma_bf16(tmem + 256, sdesc(kta + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                                 sdesc(ea + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
-                }
-                const uint32_t qx = fact ? qa : qta;
-#pragma unroll 1
+                    mma_bf16(tmem + 256, desc_plus(pa, k * 2048), desc_plus(o, k * 2048), id_mm,
+                             (fact || k > 0) ? 1u : 0u);
+                if (!fact) issue_ke(kt, 1);  // dv += K~ E
+                const uint64_t qx = fact ? q : qt;
+#pragma unroll
                 for (int k = 0; k < 4; ++k)  // dE = Q~^T dO
-                    mma_bf16(tmem + 384, sdesc(qx + k * 2048, kTileBytes, 1024),
-                             sdesc(da + k * 2048, kTileBytes, 1024), id_e, k > 0);
+                    mma_bf16(tmem + 384, desc_plus(qx, k * 2048), desc_plus(o, k * 2048), id_e, k > 0);
                 mma_commit(smem_u32(&dve_done));
                 // the next chunk's scores: their accumulator columns were read
                 // before pv_ready, their tiles were loaded into the other stage
@@ -1022,7 +1018,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                     fact = gsb[(it + 1) & 1].fact != 0;
                     if (fact) {
                         tc_fence_after();
-                        issue_ve(s ^ 1);
+                        issue_ve(s ^ 1, 0);
                     }
                 }
             }
