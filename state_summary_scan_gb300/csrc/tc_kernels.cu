@@ -506,28 +506,32 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
 
     if (ctl) {
         if (G.lane == 0) {
-            const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb), qh = smem_u32(Qh);
+            // operand descriptors as offsets from those of the start of
+            // shared memory (K-major; MN-major with blocks one tile apart)
+            const uint32_t sb0 = smem_u32(smem);
+            const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, kTileBytes, 1024);
+            const uint64_t pa = desc_plus(DK, OFF_P), sa = desc_plus(DK, OFF_S), qh = desc_plus(DM, OFF_QH);
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
             constexpr uint32_t id_a = idesc_bf16(64, 128, 0, 1);
             constexpr uint32_t id_b = idesc_bf16(64, 128, 0, 0);
             constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
             auto issue_scores = [&](int s) {  // dA = dO V^T of the chunk in stage s
-                const uint32_t st = smem_u32(smem + s * STAGE);
-                const uint32_t va = st + 4 * kTileBytes, da = st + 6 * kTileBytes;
+                const uint64_t v = desc_plus(DK, s * STAGE + 4 * kTileBytes);
+                const uint64_t o = desc_plus(DK, s * STAGE + 6 * kTileBytes);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
-                    mma_bf16(tmem, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+                    mma_bf16(tmem, desc_plus(o, off), desc_plus(v, off), id1, k > 0);
                 }
                 mma_commit(smem_u32(&score_bar));
             };
             // dq' (+)= dO S_prev^T: first in a factored chunk, after P K otherwise
             auto issue_state_side = [&](int s, bool first) {
-                const uint32_t da = smem_u32(smem + s * STAGE) + 6 * kTileBytes;
+                const uint64_t o = desc_plus(DK, s * STAGE + 6 * kTileBytes);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_bf16(tmem + 128, sdesc(da + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                             sdesc(sa + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_b,
+                    mma_bf16(tmem + 128, desc_plus(o, (k >> 2) * kTileBytes + (k & 3) * 32),
+                             desc_plus(sa, (k >> 2) * 2 * kTileBytes + (k & 3) * 32), id_b,
                              (first && k == 0) ? 0u : 1u);
             };
             mbar_wait(smem_u32(&full_bar[0]), 0);
@@ -538,26 +542,26 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             for (int c = 0; c < nch; ++c) {
                 const int s = c & 1;
                 const uint32_t ph = c & 1;
-                const uint32_t st = smem_u32(smem + s * STAGE);
-                const uint32_t ka = st + 2 * kTileBytes, va = st + 4 * kTileBytes, da = st + 6 * kTileBytes;
+                const uint64_t km = desc_plus(DM, s * STAGE + 2 * kTileBytes);
+                const uint64_t vm = desc_plus(DM, s * STAGE + 4 * kTileBytes);
+                const uint64_t om = desc_plus(DM, s * STAGE + 6 * kTileBytes);
                 mbar_wait(smem_u32(&p_ready), ph);
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // dq' (+)= P K  (strictly causal part)
-                    mma_bf16(tmem + 128, sdesc(pa + k * 32, 16, 1024), sdesc(ka + k * 2048, kTileBytes, 1024),
-                             id_a, (fact || k > 0) ? 1u : 0u);
+                    mma_bf16(tmem + 128, desc_plus(pa, k * 32), desc_plus(km, k * 2048), id_a,
+                             (fact || k > 0) ? 1u : 0u);
                 if (!fact) issue_state_side(s, false);
                 mma_commit(smem_u32(&dq_done));
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // dS = K^T V  (K^ or V~ carry the weights)
-                    mma_bf16(tmem + 256, sdesc(ka + k * 2048, kTileBytes, 1024),
-                             sdesc(va + k * 2048, kTileBytes, 1024), id_s, k > 0);
+                    mma_bf16(tmem + 256, desc_plus(km, k * 2048), desc_plus(vm, k * 2048), id_s, k > 0);
                 mbar_wait(smem_u32(&q_ready), ph);
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // gamma += Qh^T dO
-                    mma_bf16(tmem + 384, sdesc(qh + k * 2048, kTileBytes, 1024),
-                             sdesc(da + k * 2048, kTileBytes, 1024), id_s, (c > 0 || k > 0) ? 1u : 0u);
+                    mma_bf16(tmem + 384, desc_plus(qh, k * 2048), desc_plus(om, k * 2048), id_s,
+                             (c > 0 || k > 0) ? 1u : 0u);
                 mma_commit(smem_u32(&st_done));
                 if (c + 1 < nch) {
                     mbar_wait(smem_u32(&full_bar[s ^ 1]), ((c + 1) >> 1) & 1);
@@ -1370,47 +1374,50 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
 
     if (ctl) {
         if (G.lane == 0) {
-            const uint32_t pa = smem_u32(PA), pd = smem_u32(PD), ea = smem_u32(Eb);
-            const uint32_t va = smem_u32(Vs), da = smem_u32(Ds);
+            const uint32_t sb0 = smem_u32(smem);
+            const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, kTileBytes, 1024);
+            const uint64_t DM2 = sdesc(sb0, 2 * kTileBytes, 1024);
+            const uint64_t pa = desc_plus(DM, OFF_PA), pd = desc_plus(DM, OFF_PD);
+            const uint64_t ek = desc_plus(DK, OFF_E), em = desc_plus(DM2, OFF_E);
+            const uint64_t vk = desc_plus(DK, OFF_V), dk16 = desc_plus(DK, OFF_D), dm = desc_plus(DM, OFF_D);
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
             constexpr uint32_t id_mm = idesc_bf16(64, 128, 1, 1);
             constexpr uint32_t id_kk = idesc_bf16(64, 128, 0, 0);
             constexpr uint32_t id_km = idesc_bf16(64, 128, 0, 1);
             constexpr uint32_t id_e = idesc_bf16(128, 256, 1, 1);
             auto issue_scores = [&](int p) {  // A = Q K^T, dA = dO V^T
-                const uint32_t qa = smem_u32(smem + p * QKB), ka = qa + 2 * kTileBytes;
+                const uint64_t q = desc_plus(DK, p * QKB), kk = desc_plus(q, 2 * kTileBytes);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
-                    mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, k > 0);
+                    mma_bf16(tmem, desc_plus(q, off), desc_plus(kk, off), id1, k > 0);
                 }
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
-                    mma_bf16(tmem + 64, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+                    mma_bf16(tmem + 64, desc_plus(dk16, off), desc_plus(vk, off), id1, k > 0);
                 }
                 mma_commit(smem_u32(&score_bar));
             };
             auto issue_ve = [&](bool first) {  // dk' (+)= V E^T
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
-                    mma_bf16(tmem + 128, sdesc(va + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                             sdesc(ea + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_kk,
+                    mma_bf16(tmem + 128, desc_plus(vk, (k >> 2) * kTileBytes + (k & 3) * 32),
+                             desc_plus(ek, (k >> 2) * 2 * kTileBytes + (k & 3) * 32), id_kk,
                              (first && k == 0) ? 0u : 1u);
             };
             // dv_hh = PA^T dO_hh + K E_hh, half 0 into the scores' columns, half 1
             // into dk''s (free once the dk rows have been read)
-            auto issue_dv = [&](int hh, uint32_t kx) {
-                const uint32_t dah = da + 2 * hh * kTileBytes, eah = ea + 4 * hh * kTileBytes;
+            auto issue_dv = [&](int hh, uint64_t kx) {
+                const uint64_t dah = desc_plus(dm, 2 * hh * kTileBytes), eah = desc_plus(em, 4 * hh * kTileBytes);
                 const uint32_t acc = tmem + 128 * hh;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16(acc, sdesc(pa + k * 2048, kTileBytes, 1024), sdesc(dah + k * 2048, kTileBytes, 1024),
-                             id_mm, k > 0);
+                    mma_bf16(acc, desc_plus(pa, k * 2048), desc_plus(dah, k * 2048), id_mm, k > 0);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_bf16(acc, sdesc(kx + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                             sdesc(eah + k * 2048, 2 * kTileBytes, 1024), id_km, 1);
+                    mma_bf16(acc, desc_plus(kx, (k >> 2) * kTileBytes + (k & 3) * 32), desc_plus(eah, k * 2048),
+                             id_km, 1);
             };
             mbar_wait(smem_u32(&qk_full[0]), 0);
             mbar_wait(smem_u32(&v_full), 0);
@@ -1422,26 +1429,25 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             for (int it = 0; it < nch; ++it) {
                 const int p = it & 1;
                 const uint32_t ph = it & 1;
-                const uint32_t qa = smem_u32(smem + p * QKB), ka = qa + 2 * kTileBytes;
+                const uint64_t qm = desc_plus(DM, p * QKB), kx = desc_plus(DK, p * QKB + 2 * kTileBytes);
                 mbar_wait(smem_u32(&pv_ready), ph);
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // dk' (+)= PdA^T Q
-                    mma_bf16(tmem + 128, sdesc(pd + k * 2048, kTileBytes, 1024),
-                             sdesc(qa + k * 2048, kTileBytes, 1024), id_mm, (fact || k > 0) ? 1u : 0u);
+                    mma_bf16(tmem + 128, desc_plus(pd, k * 2048), desc_plus(qm, k * 2048), id_mm,
+                             (fact || k > 0) ? 1u : 0u);
                 if (!fact) issue_ve(false);  // V~ E^T
                 mma_commit(smem_u32(&dk_done));
                 mbar_wait(smem_u32(&kq_ready), ph);  // dO~ or K~, Q~ in place; E scaled by W
                 tc_fence_after();
-                issue_dv(0, ka);
+                issue_dv(0, kx);
                 mma_commit(smem_u32(&dv0_done));
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // E += Q~^T dO (all 256 columns)
-                    mma_bf16(tmem + TE, sdesc(qa + k * 2048, kTileBytes, 1024), sdesc(da + k * 2048, kTileBytes, 1024),
-                             id_e, 1u);
+                    mma_bf16(tmem + TE, desc_plus(qm, k * 2048), desc_plus(dm, k * 2048), id_e, 1u);
                 mbar_wait(smem_u32(&dk_read), ph);  // dk' columns read: dv half 1 goes there
                 tc_fence_after();
-                issue_dv(1, ka);
+                issue_dv(1, kx);
                 mma_commit(smem_u32(&dv1_done));
                 if (it + 1 < nch) {
                     mbar_wait(smem_u32(&dv0_read), ph);  // the scores overwrite dv half 0
@@ -1806,7 +1812,10 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
 
     if (ctl) {
         if (G.lane == 0) {
-            const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb), va = smem_u32(Vs), da = smem_u32(Ds);
+            const uint32_t sb0 = smem_u32(smem);
+            const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, kTileBytes, 1024);
+            const uint64_t pa = desc_plus(DK, OFF_P), sa = desc_plus(DK, OFF_S);
+            const uint64_t vk = desc_plus(DK, OFF_V), vm = desc_plus(DM, OFF_V), dk16 = desc_plus(DK, OFF_D);
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
             constexpr uint32_t id_a = idesc_bf16(64, 128, 0, 1);
             constexpr uint32_t id_b = idesc_bf16(64, 128, 0, 0);
@@ -1815,15 +1824,15 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
-                    mma_bf16(tmem, sdesc(da + off, 16, 1024), sdesc(va + off, 16, 1024), id1, k > 0);
+                    mma_bf16(tmem, desc_plus(dk16, off), desc_plus(vk, off), id1, k > 0);
                 }
                 mma_commit(smem_u32(&score_bar));
             };
             auto issue_state_side = [&](bool first) {  // dq' (+)= dO S_prev^T
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
-                    mma_bf16(tmem + 128, sdesc(da + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                             sdesc(sa + (k >> 2) * 2 * kTileBytes + (k & 3) * 32, 16, 1024), id_b,
+                    mma_bf16(tmem + 128, desc_plus(dk16, (k >> 2) * kTileBytes + (k & 3) * 32),
+                             desc_plus(sa, (k >> 2) * 2 * kTileBytes + (k & 3) * 32), id_b,
                              (first && k == 0) ? 0u : 1u);
             };
             mbar_wait(smem_u32(&v_full), 0);
@@ -1835,18 +1844,17 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
             for (int c = 0; c < nch; ++c) {
                 const int p = c & 1;
                 const uint32_t ph = c & 1;
-                const uint32_t ka = smem_u32(smem + p * QKB) + 2 * kTileBytes;
+                const uint64_t km = desc_plus(DM, p * QKB + 2 * kTileBytes);
                 mbar_wait(smem_u32(&p_ready), ph);
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // S += K^T V  (K^ or V~ carry the weights)
-                    mma_bf16(tmem + TS, sdesc(ka + k * 2048, kTileBytes, 1024), sdesc(va + k * 2048, kTileBytes, 1024),
-                             id_s, 1u);
+                    mma_bf16(tmem + TS, desc_plus(km, k * 2048), desc_plus(vm, k * 2048), id_s, 1u);
                 mma_commit(smem_u32(&v_dead));
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // dq' (+)= P K  (strictly causal part)
-                    mma_bf16(tmem + 128, sdesc(pa + k * 32, 16, 1024), sdesc(ka + k * 2048, kTileBytes, 1024),
-                             id_a, (fact || k > 0) ? 1u : 0u);
+                    mma_bf16(tmem + 128, desc_plus(pa, k * 32), desc_plus(km, k * 2048), id_a,
+                             (fact || k > 0) ? 1u : 0u);
                 if (!fact) issue_state_side(false);  // dO~ S_prev^T
                 mma_commit(smem_u32(&dq_done));
                 if (c + 1 < nch) {
@@ -2178,25 +2186,27 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
 
     if (ctl) {
         if (G.lane == 0) {
-            const uint32_t pa = smem_u32(Ps), sa = smem_u32(Sb);
+            const uint32_t sb0 = smem_u32(smem);
+            const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, kTileBytes, 1024);
+            const uint64_t pa = desc_plus(DK, OFF_P), sa = desc_plus(sdesc(sb0, 2 * kTileBytes, 1024), OFF_S);
             constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
             constexpr uint32_t id_o = idesc_bf16(64, 128, 0, 1);
             constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
             auto issue_scores = [&](int p) {  // scores = Q K^T
-                const uint32_t qa = smem_u32(smem + p * QKB), ka = qa + 2 * kTileBytes;
+                const uint64_t q = desc_plus(DK, p * QKB), kk = desc_plus(q, 2 * kTileBytes);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
-                    mma_bf16(tmem, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id1, k > 0);
+                    mma_bf16(tmem, desc_plus(q, off), desc_plus(kk, off), id1, k > 0);
                 }
                 mma_commit(smem_u32(&score_bar));
             };
             auto issue_qs = [&](int p, bool first) {  // O (+)= Q S_prev
-                const uint32_t qa = smem_u32(smem + p * QKB);
+                const uint64_t q = desc_plus(DK, p * QKB);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_bf16(tmem + TO, sdesc(qa + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                             sdesc(sa + k * 2048, 2 * kTileBytes, 1024), id_o, (first && k == 0) ? 0u : 1u);
+                    mma_bf16(tmem + TO, desc_plus(q, (k >> 2) * kTileBytes + (k & 3) * 32), desc_plus(sa, k * 2048),
+                             id_o, (first && k == 0) ? 0u : 1u);
             };
             mbar_wait(smem_u32(&qk_full[0]), 0);
             tc_fence_after();
@@ -2207,20 +2217,19 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
                 const int p = c & 1;
                 const int st = TWO ? 0 : p;
                 const uint32_t ph = c & 1;
-                const uint32_t qa = smem_u32(smem + st * QKB), ka = qa + 2 * kTileBytes;
-                const uint32_t va = smem_u32(smem + OFF_V + st * VB);
+                const uint64_t km = desc_plus(DM, st * QKB + 2 * kTileBytes);
+                const uint64_t vm = desc_plus(DM, OFF_V + st * VB);
                 mbar_wait(smem_u32(&p_ready), ph);
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // O (+)= P V
-                    mma_bf16(tmem + TO, sdesc(pa + k * 32, 16, 1024), sdesc(va + k * 2048, kTileBytes, 1024), id_o,
+                    mma_bf16(tmem + TO, desc_plus(pa, k * 32), desc_plus(vm, k * 2048), id_o,
                              ((!TWO && fact) || k > 0) ? 1u : 0u);
                 if (TWO || !fact) issue_qs(st, false);  // O += Q S_prev (Q~ in general chunks)
                 mma_commit(smem_u32(&o_done));
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // S += K^T V  (V^ or K~ carry the weights)
-                    mma_bf16(tmem + TS, sdesc(ka + k * 2048, kTileBytes, 1024), sdesc(va + k * 2048, kTileBytes, 1024),
-                             id_s, 1u);
+                    mma_bf16(tmem + TS, desc_plus(km, k * 2048), desc_plus(vm, k * 2048), id_s, 1u);
                 mma_commit(smem_u32(&s_done));
                 if (c + 1 < nch) {
                     if (TWO) {
