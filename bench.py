@@ -237,7 +237,7 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     phases = PHASES_FWD + (PHASES_BWD if w.backward else ())
 
-    def calls(q, k, v, g, dO, o, dq, dk, dv, dg, stream=stream):
+    def calls(q, k, v, g, dO, o, dq, dk, dv, dg):
         return {
             "forward_prepare": lambda: C.rm_cp_forward_prepare(s, k, v, g, plan.M, plan.dS, plan.ws, stream),
             "compose_prefix": lambda: C.rm_cp_compose_prefix(s, plan.M, plan.dS, plan.S_in, stream),
@@ -305,55 +305,26 @@ def run_ours(args, rank, world, local_rank):
             "phase_frac_of_hbm": {ph: round(kernel_bytes(w, ph) / (phase_ms[ph] / 1e3) / 1e9
                                             / peaks["hbm_gbs"], 4) for ph in phases}}
 
-    # ---- end to end: pinned host buffers in, results out, every step.  Two
-    # device buffer sets and three streams: the host->device copy of step i+1
-    # and the device->host copy of step i-1 run while step i's kernels do, as
-    # a training loop that prefetches its next batch would; every step's
-    # copies are inside the timed region.
+    # ---- end to end through rm_cp_step_host: pinned host buffers in, results
+    # out, every step.  Two device buffer sets and two copy streams: the
+    # host->device copy of step i+1 and the device->host copy of step i-1 run
+    # while step i's kernels do, as a training loop that prefetches its next
+    # batch would; every step's copies are inside the timed region.
     e2e = None
     if not args.no_e2e:
-        hin = [t.pin_memory() for t in (inp.q, inp.k, inp.v, inp.g) + ((inp.dO,) if w.backward else ())]
-        outs0 = [o] + ([dq, dk, dv, dg] if w.backward else [])
-        hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs0]
-        sets = []
-        for j in range(2):
-            dins = [torch.empty_like(t, device=dev) for t in hin]
-            douts = outs0 if j == 0 else [torch.empty_like(t) for t in outs0]
-            dob = douts + [None] * (5 - len(douts))
-            fn = calls(*(dins[:4]), dins[4] if w.backward else None, *dob, stream=stream)
-            sets.append((dins, douts, fn))
-        h2d = torch.cuda.Stream(dev)
-        d2h = torch.cuda.Stream(dev)
-        ev = lambda: torch.cuda.Event()  # noqa: E731
+        names_in = ("q", "k", "v", "g") + (("dO",) if w.backward else ())
+        host = {n: getattr(inp, n).pin_memory() for n in names_in}
+        outs0 = {"o": o}
+        if w.backward:
+            outs0.update(dq=dq, dk=dk, dv=dv, dg=dg)
+        host.update({n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in outs0.items()})
+        pipe = api.HostPipeline(plan, host, dev)
 
         def e2e_run(n):
-            """n pipelined steps; returns nothing, every stream joined at the end."""
-            in_ready = [ev() for _ in range(n)]
-            computed = [ev() for _ in range(n)]
-            out_read = [ev() for _ in range(n)]
-            h2d.wait_stream(stream)
-            d2h.wait_stream(stream)
-            for i in range(n):
-                dins, douts, fn = sets[i % 2]
-                with torch.cuda.stream(h2d):
-                    if i >= 2:
-                        h2d.wait_event(computed[i - 2])  # step i-2's kernels have read this set
-                    for d_, h_ in zip(dins, hin):
-                        d_.copy_(h_, non_blocking=True)
-                    in_ready[i].record(h2d)
-                stream.wait_event(in_ready[i])
-                if i >= 2:
-                    stream.wait_event(out_read[i - 2])  # step i-2's results have left this set
-                for ph in phases:
-                    fn[ph]()
-                computed[i].record(stream)
-                with torch.cuda.stream(d2h):
-                    d2h.wait_event(computed[i])
-                    for h_, d_ in zip(hout, douts):
-                        h_.copy_(d_, non_blocking=True)
-                    out_read[i].record(d2h)
-            stream.wait_stream(h2d)
-            stream.wait_stream(d2h)
+            pipe.begin(stream)
+            for _ in range(n):
+                pipe.step(stream)
+            pipe.join(stream)
 
         e2e_run(max(2, min(args.warmup, 3)))
         torch.cuda.synchronize(dev)
@@ -364,11 +335,12 @@ def run_ours(args, rank, world, local_rank):
         e2e_run(n_e2e)
         b.record(stream)
         torch.cuda.synchronize(dev)
+        pipe.close()
         e_ms = replica_time(a.elapsed_time(b) / n_e2e, world, dev)
         e2e = {"value": replica_throughput(world, tok_per_step, e_ms), "unit": "tokens/s",
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
-               "ms_per_step": e_ms,
+               "h2d_bytes_per_step": sum(host[n].numel() * host[n].element_size() for n in names_in),
+               "d2h_bytes_per_step": sum(host[n].numel() * host[n].element_size() for n in outs0),
+               "ms_per_step": e_ms, "call": "rm_cp_step_host",
                "pipeline": "2 device buffer sets; h2d of step i+1 and d2h of step i-1 overlap step i"}
 
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, g) + ((dO,) if dO is not None else ()))

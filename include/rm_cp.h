@@ -269,6 +269,84 @@ rm_status rm_cp_backward_noalloc(const rm_cp_problem* p, const void* q, const vo
                                  const float* M, const void* dO, float* gamma, float* dS_out,
                                  void* dq, void* dk, void* dv, float* dg, rm_stream_t stream);
 
+/*
+ * End to end from host memory: one step of the path (the three forward
+ * calls, and the three backward calls when host->dO is not NULL) with its
+ * inputs copied in from host buffers and its results copied back out, all
+ * enqueued without blocking the host.  The paper has no counterpart to this
+ * call; it is the step a training loop makes when its batches live in host
+ * memory, with the copies of one step overlapping the kernels of the next.
+ *
+ *   Streams: the host-to-device copies go on h2d, the compute calls on
+ *   compute, the device-to-host copies on d2h (one cudaMemcpyAsync per
+ *   tensor).  Each device buffer set carries three events (cudaEvent_t,
+ *   e.g. from rm_cp_event_create): `loaded` is recorded on h2d once the
+ *   inputs are in, `computed` on compute after the last kernel, `drained` on
+ *   d2h once the results are out.  Before reusing a set, h2d waits for the
+ *   set's previous `computed` (its kernels have read the old inputs) and
+ *   compute waits for its previous `drained` (its old results have left), so
+ *   consecutive calls that alternate between two sets overlap the copies of
+ *   one step with the kernels of another and never reuse a buffer early.
+ *   An event never recorded counts as complete.
+ *
+ *   host: host buffers, laid out as on the device; page-locked (pinned) for
+ *     the copies to run asynchronously.  q, k, v, g in; o out; for the
+ *     backward dO in and dq, dk, dv, dg out (all NULL for a forward step).
+ *   set:  device buffers of one step with the same fields, plus its events.
+ *   st:   device buffers the compute calls pass between each other, shared by
+ *     all sets (every compute call is on `compute`, so steps never overlap on
+ *     them): M, dS, S_in, and for the backward gamma, dS_out and the
+ *     workspace of rm_cp_workspace_size bytes.
+ *   Everything is validated before anything is enqueued; a CUDA error on
+ *   the copies or events returns RM_ERR_CUDA (work already enqueued stays).
+ */
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const void* dO;
+    void* o;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dg;
+} rm_cp_host_io;
+
+typedef struct {
+    void* q;
+    void* k;
+    void* v;
+    float* g;
+    void* dO;
+    void* o;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dg;
+    void* loaded;    /* cudaEvent_t */
+    void* computed;  /* cudaEvent_t */
+    void* drained;   /* cudaEvent_t */
+} rm_cp_step_set;
+
+typedef struct {
+    float* M;
+    float* dS;
+    float* S_in;
+    float* gamma;
+    float* dS_out;
+    void* ws;
+} rm_cp_step_state;
+
+rm_status rm_cp_step_host(const rm_cp_problem* p, const rm_cp_host_io* host,
+                          const rm_cp_step_set* set, const rm_cp_step_state* st,
+                          rm_stream_t compute, rm_stream_t h2d, rm_stream_t d2h);
+
+/* A CUDA event without timing (cudaEventDisableTiming) on the current device,
+ * for rm_cp_step_set; destroy it with rm_cp_event_destroy. */
+rm_status rm_cp_event_create(void** event);
+rm_status rm_cp_event_destroy(void* event);
+
 /* Name of a status code (static string). */
 const char* rm_cp_status_string(rm_status s);
 

@@ -28,6 +28,7 @@ EXPORTS = (
     "rm_cp_backward_prepare", "rm_cp_compose_suffix", "rm_cp_backward_apply",
     "rm_cp_status_string", "rm_cp_last_error", "rm_cp_path", "rm_cp_launch_count",
     "rm_cp_device_status", "rm_cp_selftest_wait_timeout", "rm_cp_backward_noalloc",
+    "rm_cp_step_host", "rm_cp_event_create", "rm_cp_event_destroy",
 )
 
 
@@ -47,6 +48,22 @@ class Problem(ctypes.Structure):
         ("seq_idx", ctypes.c_void_p), ("preceding_start", ctypes.c_void_p),
         ("following_stop", ctypes.c_void_p),
     ]
+
+
+class HostIO(ctypes.Structure):
+    """Mirror of rm_cp_host_io."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "g", "dO", "o", "dq", "dk", "dv", "dg")]
+
+
+class StepSet(ctypes.Structure):
+    """Mirror of rm_cp_step_set."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "g", "dO", "o", "dq", "dk", "dv", "dg",
+                                               "loaded", "computed", "drained")]
+
+
+class StepState(ctypes.Structure):
+    """Mirror of rm_cp_step_state."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("M", "dS", "S_in", "gamma", "dS_out", "ws")]
 
 
 _P = ctypes.c_void_p
@@ -70,6 +87,10 @@ _SIGS = {
     "rm_cp_device_status": (_S, [_P, ctypes.c_int32, _P]),
     "rm_cp_selftest_wait_timeout": (_S, [ctypes.c_uint32, _P]),
     "rm_cp_backward_noalloc": (_S, [_PP] + [_P] * 14),
+    "rm_cp_step_host": (_S, [_PP, ctypes.POINTER(HostIO), ctypes.POINTER(StepSet),
+                             ctypes.POINTER(StepState), _P, _P, _P]),
+    "rm_cp_event_create": (_S, [ctypes.POINTER(ctypes.c_void_p)]),
+    "rm_cp_event_destroy": (_S, [_P]),
 }
 
 _lock = threading.Lock()
@@ -224,3 +245,36 @@ def rm_cp_backward_noalloc(p, q, k, v, g, S_in, M, dO, gamma, dS_out, dq, dk, dv
     _check(load().rm_cp_backward_noalloc(p.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S_in),
                                          _ptr(M), _ptr(dO), _ptr(gamma), _ptr(dS_out), _ptr(dq),
                                          _ptr(dk), _ptr(dv), _ptr(dg), _stream(stream)))
+
+
+def rm_cp_event_create() -> int:
+    """A timing-free CUDA event on the current device (raw handle)."""
+    ev = ctypes.c_void_p()
+    _check(load().rm_cp_event_create(ctypes.byref(ev)))
+    return int(ev.value)
+
+
+def rm_cp_event_destroy(event: int) -> None:
+    _check(load().rm_cp_event_destroy(ctypes.c_void_p(event)))
+
+
+def _host_ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the C ABI must be contiguous")
+    return t.data_ptr()
+
+
+def rm_cp_step_host(p, host: dict, dev: dict, events, state: dict, compute=None, h2d=None, d2h=None):
+    """One step from host buffers.  host and dev map q, k, v, g, dO (inputs)
+    and o, dq, dk, dv, dg (outputs) to pinned host / device tensors (dO and
+    the gradients absent for a forward step); events = (loaded, computed,
+    drained) handles of this device set; state maps M, dS, S_in, gamma,
+    dS_out, ws to device tensors."""
+    names = ("q", "k", "v", "g", "dO", "o", "dq", "dk", "dv", "dg")
+    h = HostIO(*(_host_ptr(host.get(n)) for n in names))
+    d = StepSet(*(_host_ptr(dev.get(n)) for n in names), *(int(e) for e in events))
+    st = StepState(*(_host_ptr(state.get(n)) for n in ("M", "dS", "S_in", "gamma", "dS_out", "ws")))
+    _check(load().rm_cp_step_host(p.ref, ctypes.byref(h), ctypes.byref(d), ctypes.byref(st),
+                                  _stream(compute), _stream(h2d), _stream(d2h)))

@@ -109,3 +109,55 @@ def chunkwise_gla(q, k, v, g, num_segments: int, chunk: int = 64, scale=None, cu
     q, k [B,T,H,Dk], v [B,T,H,Dv] (fp32 or bf16, CUDA), g [B,T,H] fp32 log-gates.
     cu_seqlens (host int32 [N+1]) packs several sequences along T."""
     return ChunkwiseGatedLinearAttention.apply(q, k, v, g, num_segments, chunk, scale, cu_seqlens)
+
+
+class HostPipeline:
+    """Steps fed from host memory through rm_cp_step_host: two device buffer
+    sets used in turn, each with its three events, and two copy streams, so
+    that the copies of one step overlap the kernels of the next.  host maps
+    q, k, v, g (and dO) to pinned host inputs and o (and dq, dk, dv, dg) to
+    pinned host outputs."""
+
+    def __init__(self, plan: Plan, host: dict, device="cuda", nsets: int = 2):
+        self.plan = plan
+        self.host = host
+        self.backward = host.get("dO") is not None
+        names = ("q", "k", "v", "g", "o") + (("dO", "dq", "dk", "dv", "dg") if self.backward else ())
+        self.sets = []
+        for _ in range(nsets):
+            dev = {n: torch.empty(host[n].shape, dtype=host[n].dtype, device=device) for n in names}
+            events = tuple(C.rm_cp_event_create() for _ in range(3))
+            self.sets.append((dev, events))
+        self.h2d = torch.cuda.Stream(device)
+        self.d2h = torch.cuda.Stream(device)
+        self.state = dict(M=plan.M, dS=plan.dS, S_in=plan.S_in, ws=plan.ws)
+        if self.backward:
+            self.state.update(gamma=plan.gamma, dS_out=plan.dS_out)
+        self.n = 0
+
+    def begin(self, compute=None):
+        """Order the copy streams after everything already enqueued on compute."""
+        compute = compute if compute is not None else torch.cuda.current_stream()
+        self.h2d.wait_stream(compute)
+        self.d2h.wait_stream(compute)
+
+    def step(self, compute=None):
+        """Enqueue one step (copies in, the path, copies out); returns at once."""
+        compute = compute if compute is not None else torch.cuda.current_stream()
+        dev, events = self.sets[self.n % len(self.sets)]
+        C.rm_cp_step_host(self.plan.spec, self.host, dev, events, self.state, compute, self.h2d,
+                          self.d2h)
+        self.n += 1
+
+    def join(self, compute=None):
+        """Make compute wait for every copy enqueued so far."""
+        compute = compute if compute is not None else torch.cuda.current_stream()
+        compute.wait_stream(self.h2d)
+        compute.wait_stream(self.d2h)
+
+    def close(self):
+        torch.cuda.synchronize()
+        for _, events in self.sets:
+            for e in events:
+                C.rm_cp_event_destroy(e)
+        self.sets = []

@@ -92,6 +92,23 @@ def test_compute_calls_reject_null_and_misaligned_pointers_before_launch():
     assert lib.rm_cp_selftest_wait_timeout(0, None) == 1
     assert lib.rm_cp_selftest_wait_timeout(2000000, None) == 1
     assert lib.rm_cp_device_status(None, 1, None) == 1
+    # the host-fed step checks its argument structs before any CUDA call
+    rc = lib.rm_cp_step_host(s.ref, None, None, None, None, None, None)
+    assert rc == 1 and b"host is NULL" in lib.rm_cp_last_error()
+    hio = C.HostIO(*([0x1000] * 10))
+    rc = lib.rm_cp_step_host(s.ref, ctypes.byref(hio), None, None, None, None, None)
+    assert rc == 1 and b"set is NULL" in lib.rm_cp_last_error()
+    dset = C.StepSet(*([0x1000] * 10), 0x1008, None, 0x1018)
+    stt = C.StepState(*([0x1000] * 6))
+    rc = lib.rm_cp_step_host(s.ref, ctypes.byref(hio), ctypes.byref(dset), ctypes.byref(stt),
+                             None, None, None)
+    assert rc == 1 and b"set->computed is NULL" in lib.rm_cp_last_error()
+    dset = C.StepSet(*([0x1000] * 4), 0x1004, *([0x1000] * 5), 0x1008, 0x1010, 0x1018)
+    rc = lib.rm_cp_step_host(s.ref, ctypes.byref(hio), ctypes.byref(dset), ctypes.byref(stt),
+                             None, None, None)
+    assert rc == 3 and b"set->dO is not 16-byte aligned" in lib.rm_cp_last_error()
+    assert lib.rm_cp_event_create(None) == 1
+    assert lib.rm_cp_event_destroy(None) == 1
     # the allocation-free backward rejects problems beyond its fixed scratch
     big = spec(B=1, T=2 ** 21, H=4, num_segments=2 ** 10)   # 8M token-heads > 4M
     args = [ok] * 13

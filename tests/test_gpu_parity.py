@@ -234,3 +234,41 @@ def test_tc_wide_grid_strong_decay():
 def test_tc_wide_grid_value_blocks():
     # Dv = 256: two value blocks per (segment, head) -> 512 forward CTAs
     check_case(1, 1024, 16, 128, 256, torch.bfloat16, nseg=16, chunk=64, seed=5)
+
+
+# ------------------------------------------------------------------ from host memory
+
+@pytest.mark.parametrize("backward", [True, False])
+def test_step_host_pipeline_matches_device_path(backward):
+    """rm_cp_step_host on pinned host buffers, three steps on two alternating
+    device sets: every step's host results equal those of the device-buffer
+    calls bit for bit (same kernels, same order), and the oracle to tolerance."""
+    from state_summary_scan_gb300 import api
+    B, T, H, D, nseg = 1, 512, 2, 128, 4
+    q, k, v, g, dO = synth(B, T, H, D, D, torch.bfloat16, seed=7)
+    scale = 1.0 / math.sqrt(D)
+    ref_dev = run_gpu(q, k, v, g, dO if backward else None, nseg, 64, scale)
+    host = {n: t.contiguous().pin_memory() for n, t in
+            (("q", q), ("k", k), ("v", v), ("g", g)) + ((("dO", dO),) if backward else ())}
+    outs = {"o": v} if not backward else {"o": v, "dq": q, "dk": k, "dv": v, "dg": g}
+    results = []
+    plan = api.make_plan(B, T, H, D, D, nseg, 64, scale, torch.bfloat16, backward=backward)
+    outs_host = []
+    for _ in range(3):
+        outs_host.append({n: torch.full(t.shape, 7.0, dtype=t.dtype).pin_memory()
+                          for n, t in outs.items()})
+    pipe = api.HostPipeline(plan, dict(host, **outs_host[0]))
+    pipe.begin()
+    for i in range(3):
+        pipe.host = dict(host, **outs_host[i])  # each step into its own host outputs
+        pipe.step()
+    pipe.join()
+    torch.cuda.synchronize()
+    pipe.close()
+    for i in range(3):
+        for n in outs:
+            got = outs_host[i][n].to(torch.float64)
+            assert torch.equal(got, ref_dev[n]), (i, n)
+        results.append({n: outs_host[i][n].to(torch.float64).numpy() for n in outs})
+    ref = run_oracle(q, k, v, g, dO if backward else None, nseg, scale)
+    compare(results[-1], ref, 2e-2, tuple(outs))
