@@ -13,6 +13,10 @@ dS_in = M^T dS_out + gamma; LinearAttentionCPBackend prepare/apply;
 PackedSequenceCPMetadata) and the gated recurrence
 S_t = exp(g_t) S_{t-1} + k_t v_t^T, o_t = scale S_t^T q_t for the local work.
 
+ssd_forward / ssd_backward are the Mamba2 SSD scan (named by the
+context-parallel pages as the other user of exact state passing), written
+from the published SSD recurrence.
+
 Parity status: every function here is pinned by tests/test_oracle_pins.py
 (closed forms, finite differences, textbook special cases, segmentation and
 reset invariants, brute-force metadata); none is "parity unpinned".
@@ -65,6 +69,8 @@ _SIGS = {
     "oracle_backward_apply": (None, [_I, _I, _I, _I, _I, _I, _P, _D, _P, _P, _P, _P, _P, _P,
                                      _P, _P, _P, _P, _P, _P]),
     "oracle_packed_metadata": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "oracle_ssd_forward": (None, [_I] * 6 + [_P] * 8),
+    "oracle_ssd_backward": (None, [_I] * 6 + [_P] * 14),
 }
 
 
@@ -264,3 +270,39 @@ def segmented_backward(q, k, v, g, dO, scale, seg_starts, seq_idx=None,
     dS_out = compose_suffix(M, gamma, following_stop)
     grads = backward_apply(q, k, v, g, dO, S_in, dS_out, scale, seg_starts, seq_idx)
     return grads, dict(M=M, S_in=S_in, gamma=gamma, dS_out=dS_out)
+
+
+# ---------------------------------------------------------------- Mamba2 SSD
+
+def ssd_forward(x, dt, A, Bm, Cm, D=None, seq_idx=None):
+    """y [B,T,H,P] of the Mamba2 SSD scan h_t = exp(dt_t A_h) h_{t-1} +
+    dt_t B_t x_t^T, y_t = h_t^T C_t + D_h x_t (fp64; B_t, C_t shared by the
+    H / G heads of a group)."""
+    x, dt, A, Bm, Cm, D, si = (_f64(x), _f64(dt), _f64(A), _f64(Bm), _f64(Cm), _f64(D),
+                               _i32(seq_idx))
+    B, T, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    assert H % G == 0 and Cm.shape == Bm.shape and dt.shape == (B, T, H) and A.shape == (H,)
+    y = np.empty((B, T, H, P))
+    lib().oracle_ssd_forward(B, T, H, G, N, P, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
+                             _ptr(D), _ptr(si), _ptr(y))
+    return y
+
+
+def ssd_backward(x, dt, A, Bm, Cm, dy, D=None, seq_idx=None):
+    """(dx, ddt, dA, dB, dC, dD) of L = sum dy . y for ssd_forward (dD is zeros
+    of [H] when D is None)."""
+    x, dt, A, Bm, Cm, dy, D, si = (_f64(x), _f64(dt), _f64(A), _f64(Bm), _f64(Cm), _f64(dy),
+                                   _f64(D), _i32(seq_idx))
+    B, T, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    dx = np.empty((B, T, H, P))
+    ddt = np.empty((B, T, H))
+    dA = np.empty(H)
+    dB = np.empty((B, T, G, N))
+    dC = np.empty((B, T, G, N))
+    dD = np.empty(H)
+    lib().oracle_ssd_backward(B, T, H, G, N, P, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
+                              _ptr(D), _ptr(si), _ptr(dy), _ptr(dx), _ptr(ddt), _ptr(dA),
+                              _ptr(dB), _ptr(dC), _ptr(dD))
+    return dx, ddt, dA, dB, dC, dD

@@ -460,3 +460,154 @@ int oracle_packed_metadata(const int32_t* cu, int nseqs, int T, int nseg,
     local_off[nseg] = n;
     return 0;
 }
+
+/* ----------------------------------------------------------------------- */
+/* Mamba2 SSD state passing (the scan this state-summary machinery also     */
+/* serves): per row b and head h, with group gi = h / (H / G),              */
+/*   a_t = exp(dt_t A_h)  (0 when token t starts a sequence),               */
+/*   h_t = a_t h_{t-1} + dt_t B_t x_t^T           (N x P),                  */
+/*   y_t = h_t^T C_t + D_h x_t.                                             */
+/* x, y [B,T,H,P]; dt [B,T,H]; A, D [H]; Bm, Cm [B,T,G,N].                  */
+/* ----------------------------------------------------------------------- */
+
+#define SIDX_X(b, t, h) ((((i64)(b) * T + (t)) * H + (h)) * P)
+#define SIDX_BC(b, t, gi) ((((i64)(b) * T + (t)) * G + (gi)) * N)
+#define SIDX_DT(b, t, h) (((i64)(b) * T + (t)) * H + (h))
+
+static double ssd_decay(const double* dt, const double* A, const int32_t* seq_idx, int T,
+                        int H, int b, i64 t, int h) {
+    if (starts_sequence(seq_idx, t)) return 0.0;
+    return exp(dt[SIDX_DT(b, t, h)] * A[h]);
+}
+
+void oracle_ssd_forward(int B, int T, int H, int G, int N, int P, const double* x,
+                        const double* dt, const double* A, const double* Bm, const double* Cm,
+                        const double* D, const int32_t* seq_idx, double* y) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i64 bh = 0; bh < (i64)B * H; ++bh) {
+        const int b = (int)(bh / H), h = (int)(bh % H), gi = h / (H / G);
+        double* hs = (double*)calloc((size_t)N * P, sizeof(double));
+        for (i64 t = 0; t < T; ++t) {
+            const double a = ssd_decay(dt, A, seq_idx, T, H, b, t, h);
+            const double d = dt[SIDX_DT(b, t, h)];
+            const double* Bt = Bm + SIDX_BC(b, t, gi);
+            const double* Ct = Cm + SIDX_BC(b, t, gi);
+            const double* xt = x + SIDX_X(b, t, h);
+            for (int n = 0; n < N; ++n)
+                for (int p = 0; p < P; ++p)
+                    hs[(i64)n * P + p] = a * hs[(i64)n * P + p] + d * Bt[n] * xt[p];
+            double* yt = y + SIDX_X(b, t, h);
+            for (int p = 0; p < P; ++p) {
+                double acc = 0.0;
+                for (int n = 0; n < N; ++n) acc += hs[(i64)n * P + p] * Ct[n];
+                yt[p] = acc + (D ? D[h] * xt[p] : 0.0);
+            }
+        }
+        free(hs);
+    }
+}
+
+/* Backward of L = sum_t dy_t . y_t.  Tasks are (row, group) so that the heads
+ * of a group, which share B_t and C_t, add into dB and dC in a fixed order.
+ *   forward sweep:  dC_t += h_t dy_t;
+ *   reverse sweep:  adjoint Q_t = C_t dy_t^T + a_{t+1} Q_{t+1} (a_{t+1} = 0
+ *                   past the row or at a sequence start),
+ *                   dx_t = dt_t Q_t^T B_t + D_h dy_t,  dB_t += dt_t Q_t x_t,
+ *                   ddt_t = B_t . (Q_t x_t) + A_h e_t,  dA_h = sum_t dt_t e_t,
+ *                   dD_h = sum_t x_t . dy_t,
+ * where e_t = a_t <h_{t-1}, Q_t> is the gradient through the decay's exponent,
+ * taken as sum_{r >= t, same sequence} (C_r . dC^h_r - dt_r B_r . (Q_r x_r))
+ * (0 at a sequence start) so that no state has to be stored. */
+void oracle_ssd_backward(int B, int T, int H, int G, int N, int P, const double* x,
+                         const double* dt, const double* A, const double* Bm, const double* Cm,
+                         const double* D, const int32_t* seq_idx, const double* dy,
+                         double* dx, double* ddt, double* dA, double* dB, double* dC,
+                         double* dD) {
+    const int hpg = H / G;
+    memset(dB, 0, sizeof(double) * (size_t)B * T * G * N);
+    memset(dC, 0, sizeof(double) * (size_t)B * T * G * N);
+    double* dA_part = (double*)calloc((size_t)B * H, sizeof(double));
+    double* dD_part = (double*)calloc((size_t)B * H, sizeof(double));
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i64 bg = 0; bg < (i64)B * G; ++bg) {
+        const int b = (int)(bg / G), gi = (int)(bg % G);
+        double* hs = (double*)malloc(sizeof(double) * (size_t)N * P);
+        double* Q = (double*)malloc(sizeof(double) * (size_t)N * P);
+        double* cdc = (double*)malloc(sizeof(double) * (size_t)T);
+        double* dch = (double*)malloc(sizeof(double) * (size_t)N);
+        double* qx = (double*)malloc(sizeof(double) * (size_t)N);
+        for (int h = gi * hpg; h < (gi + 1) * hpg; ++h) {
+            memset(hs, 0, sizeof(double) * (size_t)N * P);
+            for (i64 t = 0; t < T; ++t) {
+                const double a = ssd_decay(dt, A, seq_idx, T, H, b, t, h);
+                const double d = dt[SIDX_DT(b, t, h)];
+                const double* Bt = Bm + SIDX_BC(b, t, gi);
+                const double* Ct = Cm + SIDX_BC(b, t, gi);
+                const double* xt = x + SIDX_X(b, t, h);
+                const double* dyt = dy + SIDX_X(b, t, h);
+                for (int n = 0; n < N; ++n)
+                    for (int p = 0; p < P; ++p)
+                        hs[(i64)n * P + p] = a * hs[(i64)n * P + p] + d * Bt[n] * xt[p];
+                for (int n = 0; n < N; ++n) {
+                    double acc = 0.0;
+                    for (int p = 0; p < P; ++p) acc += hs[(i64)n * P + p] * dyt[p];
+                    dch[n] = acc;
+                    dC[SIDX_BC(b, t, gi) + n] += acc;
+                }
+                cdc[t] = dot(Ct, dch, N);
+            }
+            memset(Q, 0, sizeof(double) * (size_t)N * P);
+            double run = 0.0, sa = 0.0, sd = 0.0;
+            for (i64 t = T - 1; t >= 0; --t) {
+                const double beta = (t + 1 < T) ? ssd_decay(dt, A, seq_idx, T, H, b, t + 1, h) : 0.0;
+                const double d = dt[SIDX_DT(b, t, h)];
+                const double* Bt = Bm + SIDX_BC(b, t, gi);
+                const double* Ct = Cm + SIDX_BC(b, t, gi);
+                const double* xt = x + SIDX_X(b, t, h);
+                const double* dyt = dy + SIDX_X(b, t, h);
+                for (int n = 0; n < N; ++n)
+                    for (int p = 0; p < P; ++p)
+                        Q[(i64)n * P + p] = Ct[n] * dyt[p] + beta * Q[(i64)n * P + p];
+                for (int n = 0; n < N; ++n) {
+                    double acc = 0.0;
+                    for (int p = 0; p < P; ++p) acc += Q[(i64)n * P + p] * xt[p];
+                    qx[n] = acc;
+                    dB[SIDX_BC(b, t, gi) + n] += d * acc;
+                }
+                double* dxt = dx + SIDX_X(b, t, h);
+                for (int p = 0; p < P; ++p) {
+                    double acc = 0.0;
+                    for (int n = 0; n < N; ++n) acc += Q[(i64)n * P + p] * Bt[n];
+                    dxt[p] = d * acc + (D ? D[h] * dyt[p] : 0.0);
+                }
+                const double bqx = dot(Bt, qx, N);
+                if (t + 1 < T && !starts_sequence(seq_idx, t + 1))
+                    run = (cdc[t] - d * bqx) + run;
+                else
+                    run = cdc[t] - d * bqx;
+                const double e = starts_sequence(seq_idx, t) ? 0.0 : run;
+                ddt[SIDX_DT(b, t, h)] = bqx + A[h] * e;
+                sa += d * e;
+                sd += dot(xt, dyt, P);
+            }
+            dA_part[(i64)b * H + h] = sa;
+            dD_part[(i64)b * H + h] = sd;
+        }
+        free(hs);
+        free(Q);
+        free(cdc);
+        free(dch);
+        free(qx);
+    }
+    for (int h = 0; h < H; ++h) {
+        double sa = 0.0, sd = 0.0;
+        for (int b = 0; b < B; ++b) {
+            sa += dA_part[(i64)b * H + h];
+            sd += dD_part[(i64)b * H + h];
+        }
+        dA[h] = sa;
+        dD[h] = sd;
+    }
+    free(dA_part);
+    free(dD_part);
+}

@@ -391,3 +391,108 @@ def test_metadata_rejects_bad_cu_seqlens():
     for cu in ([1, 8], [0, 7], [0, 3, 3, 8], [0, 5, 4, 8]):
         with pytest.raises(ValueError):
             oracle.packed_metadata(cu, 8, s)
+
+
+# ------------------------------------------------------------------ Mamba2 SSD scan
+# The oracle's ssd_forward / ssd_backward walk the token recurrence of the
+# Mamba2 SSD scan (the "Mamba2 ... exact CP linear scan" of the context-parallel
+# pages, restated from the published SSD formulation).  Pins: its quadratic
+# ("attention") form, the decay-free cumulative sum, the reset invariant and
+# central finite differences of every gradient.
+
+def _ssd_inputs(rng, B, T, H, G, N, P):
+    x = rng.standard_normal((B, T, H, P))
+    dt = np.abs(rng.standard_normal((B, T, H))) * 0.5 + 0.01
+    A = -np.abs(rng.standard_normal(H)) - 0.1
+    Bm = rng.standard_normal((B, T, G, N))
+    Cm = rng.standard_normal((B, T, G, N))
+    D = rng.standard_normal(H)
+    return x, dt, A, Bm, Cm, D
+
+
+def _ssd_quadratic(x, dt, A, Bm, Cm, D, seq_idx=None):
+    """y_t = sum_{s <= t, same sequence} exp(A sum_{r in (s, t]} dt_r) (C_t . B_s) dt_s x_s + D x_t."""
+    B, T, H, P = x.shape
+    G = Bm.shape[2]
+    y = np.zeros_like(x)
+    sid = np.zeros(T, dtype=np.int64) if seq_idx is None else np.asarray(seq_idx)
+    for b in range(B):
+        for h in range(H):
+            gi = h // (H // G)
+            cs = np.cumsum(dt[b, :, h] * A[h])
+            for t in range(T):
+                for s in range(t + 1):
+                    if sid[s] != sid[t]:
+                        continue
+                    y[b, t, h] += np.exp(cs[t] - cs[s]) * (Cm[b, t, gi] @ Bm[b, s, gi]) * dt[b, s, h] * x[b, s, h]
+                y[b, t, h] += D[h] * x[b, t, h]
+    return y
+
+
+def test_ssd_forward_matches_quadratic_form():
+    rng = np.random.default_rng(11)
+    x, dt, A, Bm, Cm, D = _ssd_inputs(rng, 2, 16, 4, 2, 5, 3)
+    np.testing.assert_allclose(oracle.ssd_forward(x, dt, A, Bm, Cm, D), _ssd_quadratic(x, dt, A, Bm, Cm, D),
+                               rtol=0, atol=1e-12)
+    si = np.array([0] * 5 + [1] * 7 + [2] * 4, dtype=np.int32)
+    x, dt, A, Bm, Cm, D = _ssd_inputs(rng, 1, 16, 2, 1, 4, 4)
+    np.testing.assert_allclose(oracle.ssd_forward(x, dt, A, Bm, Cm, D, si),
+                               _ssd_quadratic(x, dt, A, Bm, Cm, D, si), rtol=0, atol=1e-12)
+
+
+def test_ssd_without_decay_is_a_cumulative_sum():
+    rng = np.random.default_rng(12)
+    x, dt, A, Bm, Cm, _ = _ssd_inputs(rng, 1, 20, 2, 1, 3, 4)
+    A = np.zeros_like(A)
+    y = oracle.ssd_forward(x, dt, A, Bm, Cm)
+    for h in range(2):
+        hs = np.cumsum(dt[0, :, h, None, None] * Bm[0, :, 0, :, None] * x[0, :, h, None, :], axis=0)
+        np.testing.assert_allclose(y[0, :, h], np.einsum("tnp,tn->tp", hs, Cm[0, :, 0]), rtol=1e-12, atol=1e-12)
+
+
+def test_ssd_packed_equals_separate_runs():
+    rng = np.random.default_rng(13)
+    x, dt, A, Bm, Cm, D = _ssd_inputs(rng, 1, 18, 2, 1, 3, 2)
+    dy = rng.standard_normal(x.shape)
+    cut = [0, 7, 8, 18]
+    si = np.concatenate([np.full(cut[i + 1] - cut[i], i) for i in range(3)]).astype(np.int32)
+    y = oracle.ssd_forward(x, dt, A, Bm, Cm, D, si)
+    gr = oracle.ssd_backward(x, dt, A, Bm, Cm, dy, D, si)
+    dA = np.zeros(2)
+    dD = np.zeros(2)
+    for i in range(3):
+        sl = slice(cut[i], cut[i + 1])
+        ys = oracle.ssd_forward(x[:, sl], dt[:, sl], A, Bm[:, sl], Cm[:, sl], D)
+        assert np.array_equal(y[:, sl], ys)
+        gs = oracle.ssd_backward(x[:, sl], dt[:, sl], A, Bm[:, sl], Cm[:, sl], dy[:, sl], D)
+        for full, part in zip((gr[0], gr[1], gr[3], gr[4]), (gs[0], gs[1], gs[3], gs[4])):
+            assert np.array_equal(full[:, sl], part)
+        dA += gs[2]
+        dD += gs[5]
+    np.testing.assert_allclose(gr[2], dA, rtol=1e-12)
+    np.testing.assert_allclose(gr[5], dD, rtol=1e-12)
+
+
+@pytest.mark.parametrize("reset", [False, True])
+def test_ssd_gradients_match_finite_differences(reset):
+    rng = np.random.default_rng(14)
+    x, dt, A, Bm, Cm, D = _ssd_inputs(rng, 2, 10, 4, 2, 3, 2)
+    dy = rng.standard_normal(x.shape)
+    si = np.array([0, 0, 0, 1, 1, 2, 2, 2, 2, 2], dtype=np.int32) if reset else None
+    grads = oracle.ssd_backward(x, dt, A, Bm, Cm, dy, D, si)
+    base = dict(x=x, dt=dt, A=A, Bm=Bm, Cm=Cm, D=D)
+
+    def loss(**kw):
+        args = dict(base, **kw)
+        return float(np.sum(dy * oracle.ssd_forward(seq_idx=si, **args)))
+
+    eps = 1e-6
+    for name, gr in zip(("x", "dt", "A", "Bm", "Cm", "D"), grads):
+        arr = base[name]
+        fd = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            a1, a2 = arr.copy(), arr.copy()
+            a1[i] += eps
+            a2[i] -= eps
+            fd[i] = (loss(**{name: a1}) - loss(**{name: a2})) / (2 * eps)
+        assert np.max(np.abs(fd - gr)) <= 1e-7 * np.max(np.abs(fd)), name
