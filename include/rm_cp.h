@@ -347,6 +347,42 @@ rm_status rm_cp_step_host(const rm_cp_problem* p, const rm_cp_host_io* host,
 rm_status rm_cp_event_create(void** event);
 rm_status rm_cp_event_destroy(void* event);
 
+/*
+ * Mamba2 SSD scan on the same path.  The context-parallel pages name Mamba2
+ * as the other user of exact state passing; its scan, per row b and head h,
+ *     h_t = exp(dt_t A_h) h_{t-1} + dt_t B_t x_t^T,   y_t = h_t^T C_t + D_h x_t,
+ * with B_t, C_t [N] shared by the H / G heads of a group (head h uses group
+ * h / (H / G)), is the gated recurrence above with q = C, k = dt B, v = x,
+ * g = dt A and scale 1.  These three calls map the SSD arguments onto the six
+ * calls and map the results back; the problem passed to all of them has
+ * Dk = N, Dv = P and scale = 1 (any other scale is RM_ERR_INVALID_ARG here).
+ *   x, y, dy, dx [B,T,H,P] and Bm, Cm, dB, dC [B,T,G,N] have the problem's
+ *   dtype; dt, ddt [B,T,H], A, D, dA, dD [H] are fp32.  G >= 1 divides H.
+ *
+ * rm_ssd_map_inputs: q [B,T,H,N] = C of the head's group, k = dt B (rounded
+ *   to the dtype), g [B,T,H] = dt A (fp32).  v is x itself.
+ * rm_ssd_finish_forward: y = o + D_h x, in place over o (D may be NULL: o
+ *   is then y already and nothing is enqueued).
+ * rm_ssd_finish_backward: after the backward calls ran with dO = dy:
+ *   dx = dv + D_h dy (in place over dv; D may be NULL), dC = sum over the
+ *   group's heads of dq, dB = sum of dt dk, ddt = B . dk + A_h dg,
+ *   dA_h = sum over (b, t) of dt dg, dD_h = sum of x . dy (the gradient at
+ *   D = 0 when D is NULL).
+ *   Sums run in a fixed order: the results do not depend on the launch.
+ *   ws: device workspace of rm_ssd_workspace_size bytes.
+ */
+size_t rm_ssd_workspace_size(const rm_cp_problem* p);
+rm_status rm_ssd_map_inputs(const rm_cp_problem* p, int32_t G, const float* dt, const float* A,
+                            const void* Bm, const void* Cm, void* q, void* k, float* g,
+                            rm_stream_t stream);
+rm_status rm_ssd_finish_forward(const rm_cp_problem* p, const void* x, const float* D, void* o,
+                                rm_stream_t stream);
+rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, const void* x,
+                                 const float* dt, const float* A, const void* Bm,
+                                 const void* dy, const float* D, const void* dq, const void* dk,
+                                 void* dv, const float* dg, float* ddt, float* dA, void* dB,
+                                 void* dC, float* dD, void* ws, rm_stream_t stream);
+
 /* Name of a status code (static string). */
 const char* rm_cp_status_string(rm_status s);
 

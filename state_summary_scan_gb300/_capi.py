@@ -29,6 +29,7 @@ EXPORTS = (
     "rm_cp_status_string", "rm_cp_last_error", "rm_cp_path", "rm_cp_launch_count",
     "rm_cp_device_status", "rm_cp_selftest_wait_timeout", "rm_cp_backward_noalloc",
     "rm_cp_step_host", "rm_cp_event_create", "rm_cp_event_destroy",
+    "rm_ssd_workspace_size", "rm_ssd_map_inputs", "rm_ssd_finish_forward", "rm_ssd_finish_backward",
 )
 
 
@@ -91,6 +92,10 @@ _SIGS = {
                              ctypes.POINTER(StepState), _P, _P, _P]),
     "rm_cp_event_create": (_S, [ctypes.POINTER(ctypes.c_void_p)]),
     "rm_cp_event_destroy": (_S, [_P]),
+    "rm_ssd_workspace_size": (ctypes.c_size_t, [_PP]),
+    "rm_ssd_map_inputs": (_S, [_PP, ctypes.c_int32] + [_P] * 8),
+    "rm_ssd_finish_forward": (_S, [_PP, _P, _P, _P, _P]),
+    "rm_ssd_finish_backward": (_S, [_PP, ctypes.c_int32] + [_P] * 17),
 }
 
 _lock = threading.Lock()
@@ -278,3 +283,24 @@ def rm_cp_step_host(p, host: dict, dev: dict, events, state: dict, compute=None,
     st = StepState(*(_host_ptr(state.get(n)) for n in ("M", "dS", "S_in", "gamma", "dS_out", "ws")))
     _check(load().rm_cp_step_host(p.ref, ctypes.byref(h), ctypes.byref(d), ctypes.byref(st),
                                   _stream(compute), _stream(h2d), _stream(d2h)))
+
+
+def rm_ssd_workspace_size(p: ProblemSpec) -> int:
+    return int(load().rm_ssd_workspace_size(p.ref))
+
+
+def rm_ssd_map_inputs(p, G, dt, A, Bm, Cm, q, k, g, stream=None):
+    _check(load().rm_ssd_map_inputs(p.ref, int(G), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(q),
+                                    _ptr(k), _ptr(g), _stream(stream)))
+
+
+def rm_ssd_finish_forward(p, x, D, o, stream=None):
+    _check(load().rm_ssd_finish_forward(p.ref, _ptr(x), _ptr(D), _ptr(o), _stream(stream)))
+
+
+def rm_ssd_finish_backward(p, G, x, dt, A, Bm, dy, D, dq, dk, dv, dg, ddt, dA, dB, dC, dD, ws,
+                           stream=None):
+    _check(load().rm_ssd_finish_backward(p.ref, int(G), _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm),
+                                         _ptr(dy), _ptr(D), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                                         _ptr(ddt), _ptr(dA), _ptr(dB), _ptr(dC), _ptr(dD),
+                                         _ptr(ws), _stream(stream)))

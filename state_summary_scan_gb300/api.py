@@ -161,3 +161,48 @@ class HostPipeline:
             for e in events:
                 C.rm_cp_event_destroy(e)
         self.sets = []
+
+
+# ------------------------------------------------------------------ Mamba2 SSD
+
+@dataclasses.dataclass
+class SsdPlan:
+    """The path's plan (Dk = N, Dv = P, scale 1) plus the mapped inputs."""
+    core: Plan
+    G: int
+    q: torch.Tensor   # [B,T,H,N] = C of the head's group
+    k: torch.Tensor   # [B,T,H,N] = dt B
+    g: torch.Tensor   # [B,T,H] fp32 = dt A
+    ws: torch.Tensor  # workspace of rm_ssd_finish_backward
+
+
+def make_ssd_plan(B, T, H, G, N, P, num_segments, chunk=64, dtype=torch.bfloat16,
+                  cu_seqlens=None, device="cuda", backward=True) -> SsdPlan:
+    core = make_plan(B, T, H, N, P, num_segments, chunk, 1.0, dtype, cu_seqlens, device, backward)
+    q = torch.empty((B, T, H, N), dtype=dtype, device=device)
+    k = torch.empty_like(q)
+    g = torch.empty((B, T, H), dtype=torch.float32, device=device)
+    ws = torch.empty(max(C.rm_ssd_workspace_size(core.spec), 16), dtype=torch.uint8, device=device)
+    return SsdPlan(core, G, q, k, g, ws)
+
+
+def ssd_forward(sp: SsdPlan, x, dt, A, Bm, Cm, D=None, y=None, stream=None) -> torch.Tensor:
+    """y of the Mamba2 SSD scan through the six calls: q = C, k = dt B, v = x, g = dt A."""
+    C.rm_ssd_map_inputs(sp.core.spec, sp.G, dt, A, Bm, Cm, sp.q, sp.k, sp.g, stream)
+    y = forward(sp.core, sp.q, sp.k, x, sp.g, o=y, stream=stream)
+    C.rm_ssd_finish_forward(sp.core.spec, x, D, y, stream)
+    return y
+
+
+def ssd_backward(sp: SsdPlan, x, dt, A, Bm, dy, D=None, stream=None):
+    """(dx, ddt, dA, dB, dC, dD) of sum(dy * y); needs ssd_forward on sp first."""
+    dq, dk, dv, dg = backward(sp.core, sp.q, sp.k, x, sp.g, dy, stream=stream)
+    B, T, H, _ = x.shape
+    ddt = torch.empty((B, T, H), dtype=torch.float32, device=x.device)
+    dA = torch.empty(H, dtype=torch.float32, device=x.device)
+    dD = torch.empty(H, dtype=torch.float32, device=x.device)
+    dB = torch.empty(Bm.shape, dtype=Bm.dtype, device=x.device)
+    dC = torch.empty_like(dB)
+    C.rm_ssd_finish_backward(sp.core.spec, sp.G, x, dt, A, Bm, dy, D, dq, dk, dv, dg, ddt, dA, dB,
+                             dC, dD, sp.ws, stream)
+    return dv, ddt, dA, dB, dC, dD

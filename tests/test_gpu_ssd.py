@@ -1,0 +1,101 @@
+"""GPU parity of the Mamba2 SSD scan run on the gated-linear-attention path
+(rm_ssd_map_inputs -> the six calls -> rm_ssd_finish_forward / _backward)
+against the fp64 SSD oracle: y and the gradients of x, dt, A, B, C, D, each
+with max|gpu - ref| <= tol * max|ref| (2e-2 for bf16 storage, 1e-4 for fp32)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_summary_scan_gb300 import _capi as C
+from state_summary_scan_gb300 import api
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    C.load()
+
+
+def ssd_inputs(B, T, H, G, N, P, dtype, seed=0, with_D=True):
+    gen = torch.Generator().manual_seed(seed)
+    x = torch.randn(B, T, H, P, generator=gen)
+    dt = torch.nn.functional.softplus(torch.randn(B, T, H, generator=gen) - 2.0)
+    A = -(0.2 + 1.8 * torch.rand(H, generator=gen))
+    Bm = torch.randn(B, T, G, N, generator=gen) / N ** 0.5
+    Cm = torch.randn(B, T, G, N, generator=gen) / N ** 0.5
+    D = torch.randn(H, generator=gen) if with_D else None
+    dy = torch.randn(B, T, H, P, generator=gen)
+    return x.to(dtype), dt, A, Bm.to(dtype), Cm.to(dtype), D, dy.to(dtype)
+
+
+def check(B, T, H, G, N, P, dtype, nseg, cu=None, with_D=True, seed=0):
+    x, dt, A, Bm, Cm, D, dy = ssd_inputs(B, T, H, G, N, P, dtype, seed, with_D)
+    dev = "cuda"
+    xd, dtd, Ad, Bd, Cd, dyd = (t.to(dev).contiguous() for t in (x, dt, A, Bm, Cm, dy))
+    Dd = D.to(dev) if D is not None else None
+    sp = api.make_ssd_plan(B, T, H, G, N, P, nseg, 64 if T // nseg % 64 == 0 else 16, dtype, cu, dev)
+    y = api.ssd_forward(sp, xd, dtd, Ad, Bd, Cd, Dd)
+    grads = api.ssd_backward(sp, xd, dtd, Ad, Bd, dyd, Dd)
+    torch.cuda.synchronize()
+    si = None
+    if cu is not None:
+        si = np.concatenate([np.full(cu[i + 1] - cu[i], i) for i in range(len(cu) - 1)]).astype(np.int32)
+    ref_y = oracle.ssd_forward(x, dt, A, Bm, Cm, D, si)
+    ref = oracle.ssd_backward(x, dt, A, Bm, Cm, dy, D, si)
+    tol = 2e-2 if dtype == torch.bfloat16 else 1e-4
+    got = [y] + list(grads)
+    for name, a, b in zip(("y", "dx", "ddt", "dB", "dC", "dD"), got[:3] + got[4:],
+                          [ref_y] + list(ref[:2]) + list(ref[3:])):
+        a = a.detach().to("cpu", torch.float64).numpy()
+        assert a.shape == b.shape, (name, a.shape, b.shape)
+        assert np.all(np.isfinite(a)), name
+        scale = float(np.max(np.abs(b)))
+        err = float(np.max(np.abs(a - b)))
+        assert err <= tol * scale or (scale == 0.0 and err == 0.0), \
+            f"{name}: max|err| {err:.3e} > {tol:g} * max|ref| {scale:.3e}"
+    # dA_h = sum_t dt_t dg_t adds B*T signed terms (with heavy cancellation:
+    # sum |dt dg| reaches hundreds of times |dA|).  The path guarantees dg to
+    # tol * max|dg|, so dA is held to what that propagates to, per head:
+    # tol * max|dg| * sum_t dt_t, with dg of the gated recurrence on the
+    # mapped inputs (q = C, k = dt B, v = x, g = dt A, scale 1) in fp64.
+    hpg = H // G
+    q = np.stack([Cm[:, :, h // hpg].double().numpy() for h in range(H)], axis=2)
+    k = np.stack([dt[:, :, h, None].double().numpy() * Bm[:, :, h // hpg].double().numpy()
+                  for h in range(H)], axis=2)
+    dg_ref = oracle.backward(q, k, x, (dt * A).double(), dy, 1.0, si)[3]
+    dA = grads[2].detach().to("cpu", torch.float64).numpy()
+    bound = tol * np.abs(dg_ref).max() * dt.double().numpy().sum(axis=(0, 1))
+    assert np.all(np.abs(dA - ref[2]) <= bound), (dA, ref[2], bound)
+
+
+def test_ssd_tensor_core_groups():
+    check(1, 1024, 4, 2, 128, 128, torch.bfloat16, nseg=4)
+
+
+def test_ssd_tensor_core_wide_heads_no_D():
+    check(1, 512, 2, 1, 128, 256, torch.bfloat16, nseg=2, with_D=False, seed=1)
+
+
+def test_ssd_tensor_core_packed_resets():
+    cu = [0, 1, 63, 64, 300, 511, 512, 900, 1024]
+    check(1, 1024, 2, 1, 128, 128, torch.bfloat16, nseg=4, cu=cu, seed=2)
+
+
+def test_ssd_generic_fp32_one_group_per_head():
+    check(2, 256, 4, 4, 32, 16, torch.float32, nseg=4, seed=3)
+
+
+def test_ssd_rejects_bad_arguments():
+    sp = api.make_ssd_plan(1, 256, 4, 2, 32, 16, 4, 16, torch.float32, device="cuda")
+    t = torch.zeros(16, device="cuda")
+    with pytest.raises(C.RmCpError) as e:   # G does not divide H
+        C.rm_ssd_map_inputs(sp.core.spec, 3, t, t, t, t, t, t, t)
+    assert e.value.status == 1
+    bad = C.ProblemSpec(1, 256, 4, 32, 16, 4, 16, 0.5, torch.float32)  # scale != 1
+    with pytest.raises(C.RmCpError) as e:
+        C.rm_ssd_finish_forward(bad, t, t, t)
+    assert e.value.status == 1
