@@ -36,7 +36,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from state_summary_scan_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+from state_summary_scan_gb300.workloads import (SSD_WORKLOADS, WORKLOADS, make_inputs,  # noqa: E402
+                                                 make_ssd_inputs)
 
 METRIC = "fwd+bwd tokens/sec on 1 GB300; % of bf16 tensor/HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -367,8 +368,191 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# ------------------------------------------------------------------ Mamba2 SSD
+
+SSD_PHASES = ("ssd_map_inputs",) + PHASES_FWD + ("ssd_finish_forward",) + PHASES_BWD + (
+    "ssd_finish_backward",)
+
+
+def ssd_core_workload(w):
+    """The gated-recurrence problem the SSD scan runs as (Dk = N, Dv = P)."""
+    from state_summary_scan_gb300.workloads import Workload
+    return Workload(w.name, B=w.B, T=w.T, H=w.H, Dk=w.N, Dv=w.P, dtype=w.dtype,
+                    num_segments=w.num_segments, chunk=w.chunk, gate_shift=0.0)
+
+
+def ssd_kernel_bytes(w, phase):
+    """Algorithmic bytes of one launch (each input read once, each output
+    written once); the six path calls as for the gated recurrence."""
+    e = 4 if w.dtype == "f32" else 2
+    ntok = w.B * w.T * w.H
+    shared = 2 * e * w.N * w.B * w.T * w.G  # B and C, once per group
+    if phase == "ssd_map_inputs":
+        return ntok * (4 + 2 * e * w.N + 4) + shared + 4 * w.H
+    if phase == "ssd_finish_forward":
+        return ntok * 3 * e * w.P + 4 * w.H
+    if phase == "ssd_finish_backward":
+        return (ntok * (2 * e * w.N + 8 + 4 + 4 * e * w.P + 4 + 12) + e * w.N * w.B * w.T * w.G
+                + 2 * e * w.N * w.B * w.T * w.G + 12 * w.H)
+    return kernel_bytes(ssd_core_workload(w), phase)
+
+
+def ssd_path_roofline(w, peaks):
+    """The SSD scan's own step: read x, dt, B, C (B and C once per group), write
+    y; backward also reads dy and writes dx, ddt, dB, dC; the summary traffic
+    and the flops are those of the recurrence it runs as."""
+    e = 4 if w.dtype == "f32" else 2
+    core = path_roofline(ssd_core_workload(w), peaks)
+    ntok = w.B * w.T * w.H
+    nsum = w.num_segments * w.B * w.H
+    bc = w.B * w.T * w.G * e * w.N
+    byts = (ntok * (2 * e * w.P + 4) + 2 * bc + nsum * (16 * w.N * w.P + 8)
+            + ntok * (3 * e * w.P + 8) + 4 * bc + nsum * (16 * w.N * w.P + 8))
+    flops = core["flops"]
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    return dict(flops=flops, bytes=byts, bound="hbm" if t_hbm >= t_tc else "tensor",
+                t_roofline_us=max(t_tc, t_hbm) * 1e6)
+
+
+def ssd_cpu_baseline(w, inp, target_s=12.0):
+    import oracle
+    cores = oracle.set_threads(0)
+
+    def run(n):
+        sl = slice(0, n)
+        t0 = time.perf_counter()
+        oracle.ssd_forward(inp.x[:, sl], inp.dt[:, sl], inp.A, inp.Bm[:, sl], inp.Cm[:, sl], inp.D)
+        oracle.ssd_backward(inp.x[:, sl], inp.dt[:, sl], inp.A, inp.Bm[:, sl], inp.Cm[:, sl],
+                            inp.dy[:, sl], inp.D)
+        return time.perf_counter() - t0
+
+    per_tok = max(run(64) / 64, 1e-9)
+    n = max(64, min(w.T, int(target_s / per_tok) // 64 * 64))
+    dt = run(n)
+    return {"value": w.B * n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 SSD oracle fwd+bwd on the first {n} of {w.T} tokens of all {w.B} rows x "
+                      f"{w.H} heads, {dt:.1f} s wall", "seconds": dt}
+
+
+def run_ssd(args, rank, world, local_rank):
+    from state_summary_scan_gb300 import _capi as C
+    from state_summary_scan_gb300 import api
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = SSD_WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    inp = make_ssd_inputs(w)
+    x, dt, A, Bm, Cm, D, dy = (t.to(dev) for t in (inp.x, inp.dt, inp.A, inp.Bm, inp.Cm, inp.D, inp.dy))
+    sp = api.make_ssd_plan(w.B, w.T, w.H, w.G, w.N, w.P, w.num_segments, w.chunk, w.torch_dtype,
+                           device=dev)
+    plan, s = sp.core, sp.core.spec
+    y = torch.empty_like(x)
+    dq, dk, dv = torch.empty_like(sp.q), torch.empty_like(sp.k), torch.empty_like(x)
+    dg = torch.empty_like(sp.g)
+    ddt = torch.empty_like(dt)
+    dA = torch.empty_like(A)
+    dD = torch.empty_like(D)
+    dB, dC = torch.empty_like(Bm), torch.empty_like(Cm)
+    stream = torch.cuda.current_stream(dev)
+    fns = {
+        "ssd_map_inputs": lambda: C.rm_ssd_map_inputs(s, w.G, dt, A, Bm, Cm, sp.q, sp.k, sp.g, stream),
+        "forward_prepare": lambda: C.rm_cp_forward_prepare(s, sp.k, x, sp.g, plan.M, plan.dS, plan.ws, stream),
+        "compose_prefix": lambda: C.rm_cp_compose_prefix(s, plan.M, plan.dS, plan.S_in, stream),
+        "forward_apply": lambda: C.rm_cp_forward_apply(s, sp.q, sp.k, x, sp.g, plan.S_in, y, plan.ws, stream),
+        "ssd_finish_forward": lambda: C.rm_ssd_finish_forward(s, x, D, y, stream),
+        "backward_prepare": lambda: C.rm_cp_backward_prepare(s, sp.q, sp.k, x, sp.g, plan.S_in, dy,
+                                                             plan.gamma, dq, plan.ws, stream),
+        "compose_suffix": lambda: C.rm_cp_compose_suffix(s, plan.M, plan.gamma, plan.dS_out, stream),
+        "backward_apply": lambda: C.rm_cp_backward_apply(s, sp.q, sp.k, x, sp.g, dy, plan.S_in,
+                                                         plan.dS_out, dk, dv, dg, plan.ws, stream),
+        "ssd_finish_backward": lambda: C.rm_ssd_finish_backward(s, w.G, x, dt, A, Bm, dy, D, dq, dk, dv,
+                                                                dg, ddt, dA, dB, dC, dD, sp.ws, stream),
+    }
+
+    def step(events=None):
+        for i, ph in enumerate(SSD_PHASES):
+            if events is not None:
+                events[i].record(stream)
+            fns[ph]()
+        if events is not None:
+            events[len(SSD_PHASES)].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(SSD_PHASES) + 1)]
+          for _ in range(args.steps)]
+    l0 = C.rm_cp_launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = C.rm_cp_launch_count() - l0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms_per_step = replica_time(start.elapsed_time(end), world, dev) / args.steps
+    tok_per_step = w.B * w.T
+    value = replica_throughput(world, tok_per_step, ms_per_step)
+    phase_ms = {ph: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                for j, ph in enumerate(SSD_PHASES)}
+    dom = max(phase_ms, key=phase_ms.get)
+    dom_bytes = ssd_kernel_bytes(w, dom)
+    achieved = dom_bytes / (phase_ms[dom] / 1e3) / 1e9
+    roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(w.name, dom),
+            "algorithmic_bytes": dom_bytes, "launch_us": phase_ms[dom] * 1e3, "peak_source": peak_src}
+    pr = ssd_path_roofline(w, peaks)
+    path = {"bound": pr["bound"], "t_roofline_us": pr["t_roofline_us"], "t_measured_us": ms_per_step * 1e3,
+            "frac": pr["t_roofline_us"] / (ms_per_step * 1e3), "flops": pr["flops"], "bytes": pr["bytes"],
+            "peak_source": peak_src, "phases_us": {ph: round(t * 1e3, 2) for ph, t in phase_ms.items()},
+            "phase_frac_of_hbm": {ph: round(ssd_kernel_bytes(w, ph) / (phase_ms[ph] / 1e3) / 1e9
+                                            / peaks["hbm_gbs"], 4) for ph in SSD_PHASES}}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = ssd_cpu_baseline(w, inp, args.cpu_seconds)
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded Mamba2 SSD inputs)",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "G": w.G, "N": w.N, "P": w.P,
+                   "num_segments": w.num_segments, "chunk": w.chunk, "mode": "fwd+bwd",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2, no flush", "kernel_path": "tcgen05"},
+        "roofline": roof, "path_roofline": path, "cpu_baseline": cpu,
+        "e2e": None, "gpu_launches": int(launches), "clocks": clk,
+    }
+
+
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm, timed per step on host cores."""
+    if args.workload in SSD_WORKLOADS:
+        w = SSD_WORKLOADS[args.workload]
+        inp = make_ssd_inputs(w)
+        budget = max(2.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+        runs = [ssd_cpu_baseline(w, inp, budget) for _ in range(args.steps)]
+        value = statistics.mean(r["value"] for r in runs)
+        return {
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.B * w.T / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "G": w.G,
+                                            "N": w.N, "P": w.P, "num_segments": w.num_segments,
+                                            "mode": "fwd+bwd"},
+            "cpu_baseline": dict(runs[-1], value=value),
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0,
+        }
     w = workload_of(args)
     inp = make_inputs(w)
     budget = max(2.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -414,7 +598,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="32k", choices=sorted(WORKLOADS) + sorted(SSD_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -432,11 +616,14 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
+    if args.workload in SSD_WORKLOADS and args.T:
+        ap.error("--T applies to the gated-recurrence workloads only")
 
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        line = run_ours(args, rank, world, local_rank)
+        run = run_ssd if args.workload in SSD_WORKLOADS else run_ours
+        line = run(args, rank, world, local_rank)
         if rank == 0:
             print(json.dumps(line), flush=True)
     finally:

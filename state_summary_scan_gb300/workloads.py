@@ -134,3 +134,63 @@ def random_cu_seqlens(gen: torch.Generator, T: int, max_len: int) -> torch.Tenso
         lengths.append(n)
         acc += n
     return cu_seqlens_from_lengths(lengths)
+
+
+# ------------------------------------------------------------------ Mamba2 SSD
+# The pages name the Mamba2 SSD scan but give no workload for it; this one
+# has the 32k configuration's size and shape on the path (N = Dk = 128,
+# P = Dv = 128, 16 heads, 16 segments of 2048 tokens, bf16) with all heads in
+# one group.  Recipe (one torch CPU generator, seed 0, this draw order):
+#   x ~ N(0, 1) [B,T,H,P];  dt = softplus(N(0, 1) - 2) [B,T,H];
+#   A = -(0.2 + 1.8 U(0, 1)) [H];  B, C ~ N(0, 1) / sqrt(N) [B,T,G,N];
+#   D ~ N(0, 1) [H];  dy ~ N(0, 1) [B,T,H,P].
+# Per-token decays exp(dt A) then average about exp(-0.19), so a 64-token
+# chunk's summed gate lies between about -2 and -22.
+
+@dataclasses.dataclass(frozen=True)
+class SsdWorkload:
+    name: str
+    B: int
+    T: int
+    H: int
+    G: int
+    N: int
+    P: int
+    dtype: str
+    num_segments: int
+    chunk: int = 64
+    seed: int = 0
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+
+SSD_WORKLOADS = {
+    "ssd32k": SsdWorkload("ssd32k", B=1, T=32768, H=16, G=1, N=128, P=128, dtype="bf16",
+                          num_segments=16),
+}
+
+
+@dataclasses.dataclass
+class SsdInputs:
+    x: torch.Tensor
+    dt: torch.Tensor
+    A: torch.Tensor
+    Bm: torch.Tensor
+    Cm: torch.Tensor
+    D: torch.Tensor
+    dy: torch.Tensor
+
+
+def make_ssd_inputs(w: SsdWorkload) -> SsdInputs:
+    gen = torch.Generator("cpu").manual_seed(w.seed)
+    x = torch.randn(w.B, w.T, w.H, w.P, generator=gen)
+    dt = torch.nn.functional.softplus(torch.randn(w.B, w.T, w.H, generator=gen) - 2.0)
+    A = -(0.2 + 1.8 * torch.rand(w.H, generator=gen))
+    Bm = torch.randn(w.B, w.T, w.G, w.N, generator=gen) / math.sqrt(w.N)
+    Cm = torch.randn(w.B, w.T, w.G, w.N, generator=gen) / math.sqrt(w.N)
+    D = torch.randn(w.H, generator=gen)
+    dy = torch.randn(w.B, w.T, w.H, w.P, generator=gen)
+    d = w.torch_dtype
+    return SsdInputs(x.to(d), dt.contiguous(), A, Bm.to(d), Cm.to(d), D, dy.to(d))
