@@ -14,7 +14,7 @@ namespace rmcp {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRedBlocks = 128;  // blocks of the per-head reduction
+constexpr int kRedBlocks = 1024;  // blocks of the per-head reduction
 
 template <typename T>
 struct Vec;
@@ -228,18 +228,25 @@ __global__ void __launch_bounds__(kThreads) ssd_reduce_heads_kernel(
     }
 }
 
-__global__ void ssd_reduce_final_kernel(int H, const float* __restrict__ pa,
-                                        const float* __restrict__ pd, float* __restrict__ dA,
-                                        float* __restrict__ dD) {
-    const int h = threadIdx.x;
-    if (h >= H) return;
-    float a = 0.f, d = 0.f;
-    for (int r = 0; r < kRedBlocks; ++r) {
-        a += pa[r * H + h];
-        d += pd[r * H + h];
+// dA, dD from the block partials: warp w takes heads w, w + 8, ...; its lanes
+// add strided partials in a fixed order and a shuffle tree finishes the sum
+__global__ void __launch_bounds__(kThreads) ssd_reduce_final_kernel(
+    int H, const float* __restrict__ pa, const float* __restrict__ pd, float* __restrict__ dA,
+    float* __restrict__ dD) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int h = warp; h < H; h += kThreads / 32) {
+        float a = 0.f, d = 0.f;
+        for (int r = lane; r < kRedBlocks; r += 32) {
+            a += __ldg(pa + r * H + h);
+            d += __ldg(pd + r * H + h);
+        }
+        a = row_sum(a, 32);
+        d = row_sum(d, 32);
+        if (lane == 0) {
+            dA[h] = a;
+            dD[h] = d;
+        }
     }
-    dA[h] = a;
-    dD[h] = d;
 }
 
 int blocks_for(int64_t items) { return int((items + kThreads - 1) / kThreads); }
