@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kThreads) ssd_grad_bc_kernel(
         sc[e] = 0.f;
     }
     if (live) load16(Bm + btg * N + c * VE, bv);
+#pragma unroll 4
     for (int hh = 0; hh < hpg; ++hh) {
         const int h = gi * hpg + hh;
         float qv[VE], kv[VE];
@@ -228,24 +229,35 @@ __global__ void __launch_bounds__(kThreads) ssd_reduce_heads_kernel(
     }
 }
 
-// dA, dD from the block partials: warp w takes heads w, w + 8, ...; its lanes
-// add strided partials in a fixed order and a shuffle tree finishes the sum
+// dA, dD from the block partials: block h sums head h; thread t adds partials
+// t, t + 256, ... (independent loads), then warps and the block finish the
+// sum in a fixed order
 __global__ void __launch_bounds__(kThreads) ssd_reduce_final_kernel(
     int H, const float* __restrict__ pa, const float* __restrict__ pd, float* __restrict__ dA,
     float* __restrict__ dD) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int h = warp; h < H; h += kThreads / 32) {
-        float a = 0.f, d = 0.f;
-        for (int r = lane; r < kRedBlocks; r += 32) {
-            a += __ldg(pa + r * H + h);
-            d += __ldg(pd + r * H + h);
+    __shared__ float wa[kThreads / 32], wd[kThreads / 32];
+    const int h = blockIdx.x, tid = threadIdx.x;
+    float a = 0.f, d = 0.f;
+#pragma unroll
+    for (int r = tid; r < kRedBlocks; r += kThreads) {
+        a += __ldg(pa + r * H + h);
+        d += __ldg(pd + r * H + h);
+    }
+    a = row_sum(a, 32);
+    d = row_sum(d, 32);
+    if ((tid & 31) == 0) {
+        wa[tid >> 5] = a;
+        wd[tid >> 5] = d;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float sa = 0.f, sd = 0.f;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            sa += wa[w];
+            sd += wd[w];
         }
-        a = row_sum(a, 32);
-        d = row_sum(d, 32);
-        if (lane == 0) {
-            dA[h] = a;
-            dD[h] = d;
-        }
+        dA[h] = sa;
+        dD[h] = sd;
     }
 }
 
@@ -405,7 +417,7 @@ extern "C" rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, c
     }
     rmcp::ssd_reduce_heads_kernel<<<rmcp::kRedBlocks, rmcp::kThreads, 0, st>>>(
         bt, d.H, dt, dg, part, pa, pd);
-    rmcp::ssd_reduce_final_kernel<<<1, rmcp::kThreads, 0, st>>>(d.H, pa, pd, dA, dD);
+    rmcp::ssd_reduce_final_kernel<<<d.H, rmcp::kThreads, 0, st>>>(d.H, pa, pd, dA, dD);
     launches += 2;
     if (cudaGetLastError() != cudaSuccess) return api_fail(RM_ERR_CUDA, "rm_ssd_finish_backward: launch failed");
     rmcp::note_launch(launches);
