@@ -388,7 +388,7 @@ def ssd_kernel_bytes(w, phase):
     ntok = w.B * w.T * w.H
     shared = 2 * e * w.N * w.B * w.T * w.G  # B and C, once per group
     if phase == "ssd_map_inputs":
-        return ntok * (4 + 2 * e * w.N + 4) + shared + 4 * w.H
+        return ntok * (4 + e * w.N + 4) + shared // 2 + 4 * w.H
     if phase == "ssd_finish_forward":
         return ntok * 3 * e * w.P + 4 * w.H
     if phase == "ssd_finish_backward":
@@ -449,7 +449,7 @@ def run_ssd(args, rank, world, local_rank):
                            device=dev)
     plan, s = sp.core, sp.core.spec
     y = torch.empty_like(x)
-    dq, dk, dv = torch.empty_like(sp.q), torch.empty_like(sp.k), torch.empty_like(x)
+    dq, dk, dv = torch.empty_like(sp.k), torch.empty_like(sp.k), torch.empty_like(x)
     dg = torch.empty_like(sp.g)
     ddt = torch.empty_like(dt)
     dA = torch.empty_like(A)
@@ -457,15 +457,15 @@ def run_ssd(args, rank, world, local_rank):
     dB, dC = torch.empty_like(Bm), torch.empty_like(Cm)
     stream = torch.cuda.current_stream(dev)
     fns = {
-        "ssd_map_inputs": lambda: C.rm_ssd_map_inputs(s, w.G, dt, A, Bm, Cm, sp.q, sp.k, sp.g, stream),
+        "ssd_map_inputs": lambda: C.rm_ssd_map_inputs(s, w.G, dt, A, Bm, None, None, sp.k, sp.g, stream),
         "forward_prepare": lambda: C.rm_cp_forward_prepare(s, sp.k, x, sp.g, plan.M, plan.dS, plan.ws, stream),
         "compose_prefix": lambda: C.rm_cp_compose_prefix(s, plan.M, plan.dS, plan.S_in, stream),
-        "forward_apply": lambda: C.rm_cp_forward_apply(s, sp.q, sp.k, x, sp.g, plan.S_in, y, plan.ws, stream),
+        "forward_apply": lambda: C.rm_cp_forward_apply(s, Cm, sp.k, x, sp.g, plan.S_in, y, plan.ws, stream),
         "ssd_finish_forward": lambda: C.rm_ssd_finish_forward(s, x, D, y, stream),
-        "backward_prepare": lambda: C.rm_cp_backward_prepare(s, sp.q, sp.k, x, sp.g, plan.S_in, dy,
+        "backward_prepare": lambda: C.rm_cp_backward_prepare(s, Cm, sp.k, x, sp.g, plan.S_in, dy,
                                                              plan.gamma, dq, plan.ws, stream),
         "compose_suffix": lambda: C.rm_cp_compose_suffix(s, plan.M, plan.gamma, plan.dS_out, stream),
-        "backward_apply": lambda: C.rm_cp_backward_apply(s, sp.q, sp.k, x, sp.g, dy, plan.S_in,
+        "backward_apply": lambda: C.rm_cp_backward_apply(s, Cm, sp.k, x, sp.g, dy, plan.S_in,
                                                          plan.dS_out, dk, dv, dg, plan.ws, stream),
         "ssd_finish_backward": lambda: C.rm_ssd_finish_backward(s, w.G, x, dt, A, Bm, dy, D, dq, dk, dv,
                                                                 dg, ddt, dA, dB, dC, dD, sp.ws, stream),

@@ -85,6 +85,11 @@ typedef enum { RM_F32 = 0, RM_BF16 = 1 } rm_dtype;
  *   following_stop   NULL (all suffixes end at num_segments) or device int32
  *                    [num_segments]: exclusive end of segment j's
  *                    backward-summary suffix (following_rank_stop).
+ *   q_heads          0 (or H): q holds one row per head, [B,T,H,Dk].  Else
+ *                    a divisor of H: q is [B,T,q_heads,Dk] and head h reads
+ *                    q row h / (H / q_heads), i.e. consecutive heads share
+ *                    their queries (as the heads of a Mamba2 group share C).
+ *                    dq stays [B,T,H,Dk]: one gradient per head.
  * Out-of-range metadata values are clamped on the device to [0, j] and
  * [j+1, num_segments]; rm_cp_build_packed_metadata produces valid ones.
  */
@@ -97,6 +102,7 @@ typedef struct {
     const int32_t* seq_idx;
     const int32_t* preceding_start;
     const int32_t* following_stop;
+    int32_t q_heads;
 } rm_cp_problem;
 
 /*
@@ -359,8 +365,10 @@ rm_status rm_cp_event_destroy(void* event);
  *   x, y, dy, dx [B,T,H,P] and Bm, Cm, dB, dC [B,T,G,N] have the problem's
  *   dtype; dt, ddt [B,T,H], A, D, dA, dD [H] are fp32.  G >= 1 divides H.
  *
- * rm_ssd_map_inputs: q [B,T,H,N] = C of the head's group, k = dt B (rounded
- *   to the dtype), g [B,T,H] = dt A (fp32).  v is x itself.
+ * rm_ssd_map_inputs: k [B,T,H,N] = dt B (rounded to the dtype), g [B,T,H] =
+ *   dt A (fp32), and, when q is not NULL, q [B,T,H,N] = C of the head's group.
+ *   v is x itself.  With q NULL (and Cm unused) the problem passed to the six
+ *   calls sets q_heads = G and passes C itself as q: no copy of C per head.
  * rm_ssd_finish_forward: y = o + D_h x, in place over o (D may be NULL: o
  *   is then y already and nothing is enqueued).
  * rm_ssd_finish_backward: after the backward calls ran with dO = dy:

@@ -47,7 +47,7 @@ class Problem(ctypes.Structure):
         ("num_segments", ctypes.c_int32), ("chunk", ctypes.c_int32),
         ("scale", ctypes.c_float), ("dtype", ctypes.c_int),
         ("seq_idx", ctypes.c_void_p), ("preceding_start", ctypes.c_void_p),
-        ("following_stop", ctypes.c_void_p),
+        ("following_stop", ctypes.c_void_p), ("q_heads", ctypes.c_int32),
     ]
 
 
@@ -149,7 +149,7 @@ class ProblemSpec:
     def __init__(self, B, T, H, Dk, Dv, num_segments, chunk, scale, dtype,
                  seq_idx: Optional[torch.Tensor] = None,
                  preceding_start: Optional[torch.Tensor] = None,
-                 following_stop: Optional[torch.Tensor] = None):
+                 following_stop: Optional[torch.Tensor] = None, q_heads: int = 0):
         if isinstance(dtype, torch.dtype):
             dtype = RM_F32 if dtype == torch.float32 else RM_BF16 if dtype == torch.bfloat16 else -1
         self._keep = (seq_idx, preceding_start, following_stop)
@@ -160,7 +160,8 @@ class ProblemSpec:
                          float(scale), int(dtype),
                          None if seq_idx is None else seq_idx.data_ptr(),
                          None if preceding_start is None else preceding_start.data_ptr(),
-                         None if following_stop is None else following_stop.data_ptr())
+                         None if following_stop is None else following_stop.data_ptr(),
+                         int(q_heads))
 
     @property
     def ref(self):

@@ -30,7 +30,8 @@ class Plan:
 
 
 def make_plan(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch.bfloat16,
-              cu_seqlens=None, device="cuda", backward=True) -> Plan:
+              cu_seqlens=None, device="cuda", backward=True, q_heads=0) -> Plan:
+    """q_heads > 0: q is [B,T,q_heads,Dk], shared by H / q_heads consecutive heads."""
     if scale is None:
         scale = 1.0 / math.sqrt(Dk)
     meta = None
@@ -40,7 +41,8 @@ def make_plan(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch.b
         seq_idx = meta["seq_idx"].to(device)
         pre = meta["preceding_start"].to(device)
         fol = meta["following_stop"].to(device)
-    spec = C.ProblemSpec(B, T, H, Dk, Dv, num_segments, chunk, scale, dtype, seq_idx, pre, fol)
+    spec = C.ProblemSpec(B, T, H, Dk, Dv, num_segments, chunk, scale, dtype, seq_idx, pre, fol,
+                         q_heads=q_heads)
     C.rm_cp_validate(spec)
     f32 = dict(dtype=torch.float32, device=device)
     ssz = (num_segments, B, H, Dk, Dv)
@@ -167,10 +169,10 @@ class HostPipeline:
 
 @dataclasses.dataclass
 class SsdPlan:
-    """The path's plan (Dk = N, Dv = P, scale 1) plus the mapped inputs."""
+    """The path's plan (Dk = N, Dv = P, scale 1, q_heads = G: the heads of a
+    group read C itself as their queries) plus the mapped inputs."""
     core: Plan
     G: int
-    q: torch.Tensor   # [B,T,H,N] = C of the head's group
     k: torch.Tensor   # [B,T,H,N] = dt B
     g: torch.Tensor   # [B,T,H] fp32 = dt A
     ws: torch.Tensor  # workspace of rm_ssd_finish_backward
@@ -178,26 +180,29 @@ class SsdPlan:
 
 def make_ssd_plan(B, T, H, G, N, P, num_segments, chunk=64, dtype=torch.bfloat16,
                   cu_seqlens=None, device="cuda", backward=True) -> SsdPlan:
-    core = make_plan(B, T, H, N, P, num_segments, chunk, 1.0, dtype, cu_seqlens, device, backward)
-    q = torch.empty((B, T, H, N), dtype=dtype, device=device)
-    k = torch.empty_like(q)
+    core = make_plan(B, T, H, N, P, num_segments, chunk, 1.0, dtype, cu_seqlens, device, backward,
+                     q_heads=G)
+    k = torch.empty((B, T, H, N), dtype=dtype, device=device)
     g = torch.empty((B, T, H), dtype=torch.float32, device=device)
     ws = torch.empty(max(C.rm_ssd_workspace_size(core.spec), 16), dtype=torch.uint8, device=device)
-    return SsdPlan(core, G, q, k, g, ws)
+    return SsdPlan(core, G, k, g, ws)
 
 
 def ssd_forward(sp: SsdPlan, x, dt, A, Bm, Cm, D=None, y=None, stream=None) -> torch.Tensor:
-    """y of the Mamba2 SSD scan through the six calls: q = C, k = dt B, v = x, g = dt A."""
-    C.rm_ssd_map_inputs(sp.core.spec, sp.G, dt, A, Bm, Cm, sp.q, sp.k, sp.g, stream)
-    y = forward(sp.core, sp.q, sp.k, x, sp.g, o=y, stream=stream)
+    """y of the Mamba2 SSD scan through the six calls: q = C (shared by a
+    group's heads), k = dt B, v = x, g = dt A."""
+    C.rm_ssd_map_inputs(sp.core.spec, sp.G, dt, A, Bm, None, None, sp.k, sp.g, stream)
+    y = forward(sp.core, Cm, sp.k, x, sp.g, o=y, stream=stream)
     C.rm_ssd_finish_forward(sp.core.spec, x, D, y, stream)
     return y
 
 
-def ssd_backward(sp: SsdPlan, x, dt, A, Bm, dy, D=None, stream=None):
+def ssd_backward(sp: SsdPlan, x, dt, A, Bm, Cm, dy, D=None, stream=None):
     """(dx, ddt, dA, dB, dC, dD) of sum(dy * y); needs ssd_forward on sp first."""
-    dq, dk, dv, dg = backward(sp.core, sp.q, sp.k, x, sp.g, dy, stream=stream)
     B, T, H, _ = x.shape
+    grads = (torch.empty_like(sp.k), torch.empty_like(sp.k), torch.empty_like(x),
+             torch.empty((B, T, H), dtype=torch.float32, device=x.device))
+    dq, dk, dv, dg = backward(sp.core, Cm, sp.k, x, sp.g, dy, grads=grads, stream=stream)
     ddt = torch.empty((B, T, H), dtype=torch.float32, device=x.device)
     dA = torch.empty(H, dtype=torch.float32, device=x.device)
     dD = torch.empty(H, dtype=torch.float32, device=x.device)

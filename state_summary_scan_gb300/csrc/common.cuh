@@ -19,6 +19,8 @@ struct Dims {
     const int32_t* seq_idx;          // device [T] or nullptr
     const int32_t* preceding_start;  // device [nseg] or nullptr
     const int32_t* following_stop;   // device [nseg] or nullptr
+    int qh;     // query heads (rows of q per token)
+    int qdiv;   // H / qh: head h reads query row h / qdiv
 };
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
@@ -47,6 +49,10 @@ __device__ __forceinline__ bool same_sequence(const int32_t* seq_idx, int s, int
 
 __device__ __forceinline__ int64_t qk_off(const Dims& d, int b, int t, int h) {
     return ((int64_t(b) * d.T + t) * d.H + h) * d.Dk;
+}
+// q row of head h (heads share query rows when qh < H)
+__device__ __forceinline__ int64_t q_off(const Dims& d, int b, int t, int h) {
+    return ((int64_t(b) * d.T + t) * d.qh + h / d.qdiv) * d.Dk;
 }
 __device__ __forceinline__ int64_t v_off(const Dims& d, int b, int t, int h) {
     return ((int64_t(b) * d.T + t) * d.H + h) * d.Dv;

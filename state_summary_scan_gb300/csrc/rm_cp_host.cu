@@ -67,6 +67,10 @@ rm_status check_problem(const rm_cp_problem* p, rmcp::Dims* d) {
     d->seq_idx = p->seq_idx;
     d->preceding_start = p->preceding_start;
     d->following_stop = p->following_stop;
+    if (p->q_heads < 0 || (p->q_heads > 0 && p->H % p->q_heads != 0))
+        return fail(RM_ERR_INVALID_ARG, "q_heads=%d does not divide H=%d", p->q_heads, p->H);
+    d->qh = p->q_heads > 0 ? p->q_heads : p->H;
+    d->qdiv = p->H / d->qh;
     if (!rmcp::tc_supports(*d, p->dtype) && !rmcp::generic_supports(*d))
         return fail(RM_ERR_UNSUPPORTED,
                     "unsupported head dims Dk=%d Dv=%d (need Dk in {16,32,64,128}, Dv a multiple "

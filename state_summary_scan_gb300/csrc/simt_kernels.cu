@@ -69,8 +69,9 @@ __global__ void __launch_bounds__(128) simt_column_sweep(Dims d, const T* __rest
         for (int e = threadIdx.x; e < kTok * DK; e += blockDim.x) {
             const int tt = e / DK, i = e % DK;
             const int64_t off = qk_off(d, b, t0 + tt, h) + i;
-            vec_s[tt][i] = to_f32(MODE == kGamma ? q[off] : k[off]);
-            if (MODE == kApply) q_s[tt][i] = to_f32(q[off]);
+            const int64_t qo = q_off(d, b, t0 + tt, h) + i;
+            vec_s[tt][i] = to_f32(MODE == kGamma ? q[qo] : k[off]);
+            if (MODE == kApply) q_s[tt][i] = to_f32(q[qo]);
         }
         if (threadIdx.x < kTok) {
             const int t = t0 + threadIdx.x;
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(128) simt_dq_sweep(Dims d, const T* __restrict
 #pragma unroll
         for (int tt = 0; tt < kTok; ++tt) {
             kr[tt] = i < DK ? to_f32(k[qk_off(d, b, t0 + tt, h) + i]) : 0.f;
-            qr[tt] = i < DK ? to_f32(q[qk_off(d, b, t0 + tt, h) + i]) : 0.f;
+            qr[tt] = i < DK ? to_f32(q[q_off(d, b, t0 + tt, h) + i]) : 0.f;
         }
         __syncthreads();
 #pragma unroll 1
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(256) simt_reverse_sweep(Dims d, const T* __res
         for (int e = threadIdx.x; e < kTok * DK; e += blockDim.x) {
             const int tt = e / DK, i = e % DK;
             const int64_t off = qk_off(d, b, t0 + tt, h) + i;
-            q_s[e] = to_f32(q[off]);
+            q_s[e] = to_f32(q[q_off(d, b, t0 + tt, h) + i]);
             k_s[e] = to_f32(k[off]);
         }
         if (threadIdx.x < kTok) {

@@ -81,13 +81,16 @@ __global__ void __launch_bounds__(kThreads) ssd_map_inputs_kernel(
     const int64_t bt = btg / G;
     const int h = gi * hpg + hh;
     const float d = __ldg(dt + bt * H + h);
-    float bv[VE], cv[VE];
+    float bv[VE];
     load16(Bm + btg * N + c * VE, bv);
-    load16(Cm + btg * N + c * VE, cv);
 #pragma unroll
     for (int e = 0; e < VE; ++e) bv[e] *= d;
     const int64_t row = (bt * H + h) * N + c * VE;
-    store16(q + row, cv);
+    if (q != nullptr) {
+        float cv[VE];
+        load16(Cm + btg * N + c * VE, cv);
+        store16(q + row, cv);
+    }
     store16(k + row, bv);
     if (c == 0) g[bt * H + h] = d * __ldg(A + h);
 }
@@ -313,8 +316,10 @@ extern "C" rm_status rm_ssd_map_inputs(const rm_cp_problem* p, int32_t G, const 
     RM_NEED_SSD(dt);
     RM_NEED_SSD(A);
     RM_NEED_SSD(Bm);
-    RM_NEED_SSD(Cm);
-    RM_NEED_SSD(q);
+    if (q != nullptr) {
+        RM_NEED_SSD(Cm);
+        RM_NEED_SSD(q);
+    }
     RM_NEED_SSD(k);
     RM_NEED_SSD(g);
     auto st = reinterpret_cast<cudaStream_t>(stream);

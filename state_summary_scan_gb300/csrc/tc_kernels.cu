@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bar = smem_u32(&full_bar[s]);
         uint8_t* st = smem + s * SBYTES;
         mbar_expect_tx(bar, SBYTES);
-        load_tile(st, &mx, 0, 128, h, row, bar);
+        load_tile(st, &mx, 0, 128, GAMMA ? h / d.qdiv : h, row, bar);  // x = q or k
         load_tile(st + XBYTES, &my, 0, DV, h, row, bar);
     };
     if (G.tid == 0)
@@ -586,7 +586,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 const uint32_t bar = smem_u32(&full_bar[s]);
                 uint8_t* st = smem + s * STAGE;
                 mbar_expect_tx(bar, STAGE);
-                load_tile(st, &mq, 0, 128, h, row, bar);
+                load_tile(st, &mq, 0, 128, h / d.qdiv, row, bar);
                 load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
                 load_tile(st + 4 * kTileBytes, &mv, 0, 128, h, row, bar);
                 load_tile(st + 6 * kTileBytes, &mdo, 0, 128, h, row, bar);
@@ -888,7 +888,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
         const uint32_t bar = smem_u32(&full_bar[s]);
         uint8_t* st = smem + s * STAGE;
         mbar_expect_tx(bar, STAGE);
-        load_tile(st, &mq, 0, 128, h, row, bar);
+        load_tile(st, &mq, 0, 128, h / d.qdiv, row, bar);
         load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
         load_tile(st + 4 * kTileBytes, &mv, 0, DV, h, row, bar);
         load_tile(st + 6 * kTileBytes, &mdo, 0, DV, h, row, bar);
@@ -1050,7 +1050,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 mbar_wait(smem_u32(&in_dead), ph);
                 if (it + 2 < nch) {
                     mbar_expect_tx(fb, STAGE);
-                    load_tile(st, &mq, 0, 128, h, nrow, fb);
+                    load_tile(st, &mq, 0, 128, h / d.qdiv, nrow, fb);
                     load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, nrow, fb);
                     load_tile(st + 6 * kTileBytes, &mdo, 0, DV, h, nrow, fb);
                 }
@@ -1474,7 +1474,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 const uint32_t bar = smem_u32(&qk_full[p]);
                 uint8_t* st = smem + p * QKB;
                 mbar_expect_tx(bar, QKB);
-                load_tile(st, &mq, 0, 128, h, row, bar);
+                load_tile(st, &mq, 0, 128, h / d.qdiv, row, bar);
                 load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
             };
             auto load_one = [&](int it, uint8_t* dst, const CUtensorMap* map, uint64_t* barp) {
@@ -1881,7 +1881,7 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
                 const uint32_t bar = smem_u32(&qk_full[p]);
                 uint8_t* st = smem + p * QKB;
                 mbar_expect_tx(bar, QKB);
-                load_tile(st, &mq, 0, 128, h, row, bar);
+                load_tile(st, &mq, 0, 128, h / d.qdiv, row, bar);
                 load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, bar);
             };
             auto load_one = [&](int c, uint8_t* dst, const CUtensorMap* map, uint64_t* barp) {
@@ -2264,7 +2264,7 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
                 uint8_t* st = smem + p * QKB;
                 const uint32_t qb = smem_u32(&qk_full[p]), vbar = smem_u32(&v_full[p]);
                 mbar_expect_tx(qb, QKB);
-                load_tile(st, &mq, 0, 128, h, row, qb);
+                load_tile(st, &mq, 0, 128, h / d.qdiv, row, qb);
                 load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, qb);
                 mbar_expect_tx(vbar, VB);
                 load_tile(smem + OFF_V + p * VB, &mv, vb * 128, 128, h, row, vbar);
@@ -2488,7 +2488,7 @@ __global__ void __launch_bounds__(kThreads + 64, 2)
                 const uint32_t bar = smem_u32(&full_bar[s]);
                 uint8_t* st = smem + s * SBYTES;
                 mbar_expect_tx(bar, SBYTES);
-                load_tile(st, &mx, 0, 128, h, row, bar);
+                load_tile(st, &mx, 0, 128, GAMMA ? h / d.qdiv : h, row, bar);  // x = q or k
                 load_tile(st + XBYTES, &my, 0, DV, h, row, bar);
             };
             for (int it = 0; it < NS && it < nch; ++it) issue(it, it);
@@ -2603,11 +2603,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [B*T rows][H][D] bf16 viewed as a 3-D tensor; boxes of 64 tokens x 64 columns.
-bool make_map(CUtensorMap* m, const void* base, const Dims& d, int D) {
+bool make_map(CUtensorMap* m, const void* base, const Dims& d, int D, int heads = 0) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(d.H), cuuint64_t(d.B) * cuuint64_t(d.T)};
-    cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(d.H) * D * 2};
+    if (heads <= 0) heads = d.H;
+    cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(heads), cuuint64_t(d.B) * cuuint64_t(d.T)};
+    cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(heads) * D * 2};
     cuuint32_t box[3] = {64, 1, uint32_t(kChunk)};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
@@ -2705,7 +2706,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
         }
         case Op::kForwardApply: {
             CUtensorMap mo;
-            if (!make_map(&mq, p.q, d, 128) || !make_map(&mk, p.k, d, 128) ||
+            if (!make_map(&mq, p.q, d, 128, d.qh) || !make_map(&mk, p.k, d, 128) ||
                 !make_map(&mv, p.v, d, d.Dv) || !make_map(&mo, p.out0, d, d.Dv))
                 return RM_ERR_CUDA;
             // more CTAs than SMs: two a SM (single-stage, 256 tensor-memory
@@ -2723,7 +2724,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             return RM_OK;
         }
         case Op::kBackwardPrepare: {
-            if (!make_map(&mq, p.q, d, 128) || !make_map(&mk, p.k, d, 128) ||
+            if (!make_map(&mq, p.q, d, 128, d.qh) || !make_map(&mk, p.k, d, 128) ||
                 !make_map(&mv, p.v, d, d.Dv) || !make_map(&mdo, p.dO, d, d.Dv))
                 return RM_ERR_CUDA;
             CUtensorMap mdq;
@@ -2750,7 +2751,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             return RM_OK;
         }
         case Op::kBackwardApply: {
-            if (!make_map(&mq, p.q, d, 128) || !make_map(&mk, p.k, d, 128) ||
+            if (!make_map(&mq, p.q, d, 128, d.qh) || !make_map(&mk, p.k, d, 128) ||
                 !make_map(&mv, p.v, d, d.Dv) || !make_map(&mdo, p.dO, d, d.Dv))
                 return RM_ERR_CUDA;
             auto* dko = static_cast<__nv_bfloat16*>(p.out0);

@@ -57,6 +57,7 @@ def spec(**kw):
     (dict(dtype=7), 1),
     (dict(scale=float("nan")), 1),
     (dict(Dk=48), 4), (dict(Dk=256), 4), (dict(Dv=12), 4), (dict(Dv=264), 4),
+    (dict(q_heads=3), 1), (dict(q_heads=-1), 1),
 ])
 def test_validation_rejects_bad_problems(kw, status):
     with pytest.raises(C.RmCpError) as e:

@@ -272,3 +272,36 @@ def test_step_host_pipeline_matches_device_path(backward):
         results.append({n: outs_host[i][n].to(torch.float64).numpy() for n in outs})
     ref = run_oracle(q, k, v, g, dO if backward else None, nseg, scale)
     compare(results[-1], ref, 2e-2, tuple(outs))
+
+
+# ------------------------------------------------------------------ shared queries
+
+@pytest.mark.parametrize("dtype,Dk,Dv,chunk", [(torch.bfloat16, 128, 128, 64),
+                                               (torch.bfloat16, 128, 256, 64),
+                                               (torch.float32, 32, 16, 16)])
+def test_shared_queries(dtype, Dk, Dv, chunk):
+    """q_heads = 2 of H = 4: heads 0, 1 read query row 0 and heads 2, 3 row 1;
+    the oracle sees the same queries repeated per head.  dq stays per head."""
+    from state_summary_scan_gb300 import api
+    B, T, H, qh, nseg = 1, 512, 4, 2, 4
+    gen = torch.Generator().manual_seed(21)
+    q = torch.randn(B, T, qh, Dk, generator=gen)
+    k = torch.randn(B, T, H, Dk, generator=gen)
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn(B, T, H, Dv, generator=gen)
+    g = torch.nn.functional.logsigmoid(torch.randn(B, T, H, generator=gen) + 3.0)
+    dO = torch.randn(B, T, H, Dv, generator=gen)
+    q, k, v, dO = (t.to(dtype) for t in (q, k, v, dO))
+    scale = 1.0 / math.sqrt(Dk)
+    dev = "cuda"
+    qd, kd, vd, gd, dOd = (t.to(dev).contiguous() for t in (q, k, v, g, dO))
+    plan = api.make_plan(B, T, H, Dk, Dv, nseg, chunk, scale, dtype, device=dev, q_heads=qh)
+    o = api.forward(plan, qd, kd, vd, gd)
+    grads = (torch.empty_like(kd), torch.empty_like(kd), torch.empty_like(vd), torch.empty_like(gd))
+    dq, dk, dv, dg = api.backward(plan, qd, kd, vd, gd, dOd, grads=grads)
+    torch.cuda.synchronize()
+    gpu = dict(o=o, dq=dq, dk=dk, dv=dv, dg=dg, M=plan.M, dS=plan.dS, S_in=plan.S_in,
+               gamma=plan.gamma, dS_out=plan.dS_out)
+    gpu = {key: val.detach().to("cpu", torch.float64).numpy() for key, val in gpu.items()}
+    ref = run_oracle(q.repeat_interleave(H // qh, dim=2), k, v, g, dO, nseg, scale)
+    compare(gpu, ref, tol_for(dtype), ALL_KEYS)

@@ -39,7 +39,7 @@ def check(B, T, H, G, N, P, dtype, nseg, cu=None, with_D=True, seed=0):
     Dd = D.to(dev) if D is not None else None
     sp = api.make_ssd_plan(B, T, H, G, N, P, nseg, 64 if T // nseg % 64 == 0 else 16, dtype, cu, dev)
     y = api.ssd_forward(sp, xd, dtd, Ad, Bd, Cd, Dd)
-    grads = api.ssd_backward(sp, xd, dtd, Ad, Bd, dyd, Dd)
+    grads = api.ssd_backward(sp, xd, dtd, Ad, Bd, Cd, dyd, Dd)
     torch.cuda.synchronize()
     si = None
     if cu is not None:
