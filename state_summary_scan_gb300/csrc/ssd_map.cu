@@ -63,54 +63,51 @@ __device__ __forceinline__ float row_sum(float v, int width) {
     return v;
 }
 
-// q, k of every head and g; item = ((bt * G + gi) * hpg + hh) * NC + c
+// k (and q) of every head and g; block = one (row, token), its threads take
+// the H * NC (head, 16-byte chunk) items, NC = N / VEC a power of two
 template <typename T>
 __global__ void __launch_bounds__(kThreads) ssd_map_inputs_kernel(
-    int64_t items, int H, int G, int N, const float* __restrict__ dt, const float* __restrict__ A,
+    int H, int G, int N, int lnc, const float* __restrict__ dt, const float* __restrict__ A,
     const T* __restrict__ Bm, const T* __restrict__ Cm, T* __restrict__ q, T* __restrict__ k,
     float* __restrict__ g) {
     constexpr int VE = Vec<T>::n;
-    const int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x;
-    if (i >= items) return;
-    const int NC = N / VE, hpg = H / G;
-    const int c = int(i % NC);
-    const int64_t r = i / NC;
-    const int hh = int(r % hpg);
-    const int64_t btg = r / hpg;
-    const int gi = int(btg % G);
-    const int64_t bt = btg / G;
-    const int h = gi * hpg + hh;
-    const float d = __ldg(dt + bt * H + h);
-    float bv[VE];
-    load16(Bm + btg * N + c * VE, bv);
+    const int64_t bt = blockIdx.x;
+    const int hpg = H / G, nc = 1 << lnc;
+    for (int j = threadIdx.x; j < (H << lnc); j += kThreads) {
+        const int h = j >> lnc, c = j & (nc - 1), gi = h / hpg;
+        const float d = __ldg(dt + bt * H + h);
+        const int64_t src = (bt * G + gi) * N + c * VE;
+        float bv[VE];
+        load16(Bm + src, bv);
 #pragma unroll
-    for (int e = 0; e < VE; ++e) bv[e] *= d;
-    const int64_t row = (bt * H + h) * N + c * VE;
-    if (q != nullptr) {
-        float cv[VE];
-        load16(Cm + btg * N + c * VE, cv);
-        store16(q + row, cv);
+        for (int e = 0; e < VE; ++e) bv[e] *= d;
+        const int64_t row = (bt * H + h) * N + c * VE;
+        if (q != nullptr) {
+            float cv[VE];
+            load16(Cm + src, cv);
+            store16(q + row, cv);
+        }
+        store16(k + row, bv);
+        if (c == 0) g[bt * H + h] = d * __ldg(A + h);
     }
-    store16(k + row, bv);
-    if (c == 0) g[bt * H + h] = d * __ldg(A + h);
 }
 
-// y = o + D_h x over [B,T,H,P], in place
+// y = o + D_h x over [B,T,H,P], in place; block = one (row, token)
 template <typename T>
 __global__ void __launch_bounds__(kThreads) ssd_finish_forward_kernel(
-    int64_t items, int H, int P, const T* __restrict__ x, const float* __restrict__ D, T* o) {
+    int H, int lpc, const T* __restrict__ x, const float* __restrict__ D, T* o) {
     constexpr int VE = Vec<T>::n;
-    const int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x;
-    if (i >= items) return;
-    const int PC = P / VE;
-    const int h = int((i / PC) % H);
-    const float dh = __ldg(D + h);
-    float xv[VE], ov[VE];
-    load16(x + i * VE, xv);
-    load16(o + i * VE, ov);
+    const int64_t base = int64_t(blockIdx.x) * (int64_t(H) << lpc);
+    for (int j = threadIdx.x; j < (H << lpc); j += kThreads) {
+        const float dh = __ldg(D + (j >> lpc));
+        const int64_t i = base + j;
+        float xv[VE], ov[VE];
+        load16(x + i * VE, xv);
+        load16(o + i * VE, ov);
 #pragma unroll
-    for (int e = 0; e < VE; ++e) ov[e] = fmaf(dh, xv[e], ov[e]);
-    store16(o + i * VE, ov);
+        for (int e = 0; e < VE; ++e) ov[e] = fmaf(dh, xv[e], ov[e]);
+        store16(o + i * VE, ov);
+    }
 }
 
 // dC, dB of a (row, token, group) and ddt of its heads; item = (bt * G + gi) * NC + c.
@@ -122,13 +119,13 @@ __global__ void __launch_bounds__(kThreads) ssd_grad_bc_kernel(
     const T* __restrict__ Bm, const T* __restrict__ dq, const T* __restrict__ dk,
     const float* __restrict__ dg, float* __restrict__ ddt, T* __restrict__ dB, T* __restrict__ dC) {
     constexpr int VE = Vec<T>::n;
-    const int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x;
+    const int i = blockIdx.x * kThreads + threadIdx.x;  // items < 2^31 (checked on the host)
     const bool live = i < items;
     const int NC = N / VE, hpg = H / G;
-    const int c = int(i % NC);
-    const int64_t btg = live ? i / NC : 0;
-    const int gi = int(btg % G);
-    const int64_t bt = btg / G;
+    const int c = i & (NC - 1);
+    const int btg32 = live ? i / NC : 0;
+    const int gi = btg32 % G;
+    const int64_t btg = btg32, bt = btg32 / G;
     float bv[VE], sb[VE], sc[VE];
 #pragma unroll
     for (int e = 0; e < VE; ++e) {
@@ -168,33 +165,38 @@ __global__ void __launch_bounds__(kThreads) ssd_grad_bc_kernel(
 }
 
 // dx = dv + D_h dy in place over dv (D may be null), and part[row] = x . dy
-// per (row, token, head)
+// per (row, token, head); block = one (row, token), its threads take the
+// H * PC items (PC = P / VEC lanes per head row, a power of two up to 32).
+// The loop runs the same number of times in every lane of a warp (the row
+// sums shuffle across lanes); lanes past the end work on zeros.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) ssd_grad_x_kernel(
-    int64_t items, int H, int P, const T* __restrict__ x, const T* __restrict__ dy,
-    const float* __restrict__ D, T* dv, float* __restrict__ part) {
+    int H, int lpc, const T* __restrict__ x, const T* __restrict__ dy, const float* __restrict__ D,
+    T* dv, float* __restrict__ part) {
     constexpr int VE = Vec<T>::n;
-    const int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x;
-    const bool live = i < items;
-    const int PC = P / VE;
-    const int64_t row = live ? i / PC : 0;
-    const int h = int(row % H);
-    float xv[VE], yv[VE], vv[VE];
-    float s = 0.f;
-    if (live) {
-        load16(x + i * VE, xv);
-        load16(dy + i * VE, yv);
-        load16(dv + i * VE, vv);
-        const float dh = D != nullptr ? __ldg(D + h) : 0.f;
+    const int n = H << lpc, pc = 1 << lpc;
+    const int64_t base = int64_t(blockIdx.x) * n;
+    for (int j0 = 0; j0 < n; j0 += kThreads) {
+        const int j = j0 + threadIdx.x;
+        const bool live = j < n;
+        float s = 0.f;
+        if (live) {
+            const int64_t i = base + j;
+            float xv[VE], yv[VE], vv[VE];
+            load16(x + i * VE, xv);
+            load16(dy + i * VE, yv);
+            load16(dv + i * VE, vv);
+            const float dh = D != nullptr ? __ldg(D + (j >> lpc)) : 0.f;
 #pragma unroll
-        for (int e = 0; e < VE; ++e) {
-            vv[e] = fmaf(dh, yv[e], vv[e]);
-            s = fmaf(xv[e], yv[e], s);
+            for (int e = 0; e < VE; ++e) {
+                vv[e] = fmaf(dh, yv[e], vv[e]);
+                s = fmaf(xv[e], yv[e], s);
+            }
+            store16(dv + i * VE, vv);
         }
-        store16(dv + i * VE, vv);
+        s = row_sum(s, pc);
+        if (live && (j & (pc - 1)) == 0) part[(base >> lpc) + (j >> lpc)] = s;
     }
-    s = row_sum(s, PC);
-    if (live && int(i % PC) == 0) part[row] = s;
 }
 
 // per-head partial sums of dt dg and of part over the flattened [B*T, H]
@@ -265,6 +267,11 @@ __global__ void __launch_bounds__(kThreads) ssd_reduce_final_kernel(
 }
 
 int blocks_for(int64_t items) { return int((items + kThreads - 1) / kThreads); }
+int log2i(int n) {
+    int l = 0;
+    while ((1 << l) < n) ++l;
+    return l;
+}
 
 #define RM_NEED_SSD(ptr)                                     \
     do {                                                     \
@@ -288,6 +295,10 @@ rm_status check_ssd(const rm_cp_problem* p, int G, Dims* d) {
         return api_fail(RM_ERR_UNSUPPORTED,
                         "the SSD maps take N and P with N/v and P/v a power of two up to 32 "
                         "(v = 8 for bf16, 4 for fp32)");
+    // one block per (row, token); flat (row, token, group, lane) indices in int32
+    const double tokens = double(d->B) * d->T;
+    if (tokens > 2.0e9 || tokens * G * (d->Dk / ve) > 2.0e9)
+        return api_fail(RM_ERR_SHAPE, "B*T too large for the SSD maps");
     return RM_OK;
 }
 
@@ -325,15 +336,13 @@ extern "C" rm_status rm_ssd_map_inputs(const rm_cp_problem* p, int32_t G, const 
     auto st = reinterpret_cast<cudaStream_t>(stream);
     const int64_t bt = int64_t(d.B) * d.T;
     if (p->dtype == RM_BF16) {
-        const int64_t items = bt * d.H * (d.Dk / 8);
-        rmcp::ssd_map_inputs_kernel<__nv_bfloat16><<<rmcp::blocks_for(items), rmcp::kThreads, 0, st>>>(
-            items, d.H, G, d.Dk, dt, A, static_cast<const __nv_bfloat16*>(Bm),
+        rmcp::ssd_map_inputs_kernel<__nv_bfloat16><<<unsigned(bt), rmcp::kThreads, 0, st>>>(
+            d.H, G, d.Dk, rmcp::log2i(d.Dk / 8), dt, A, static_cast<const __nv_bfloat16*>(Bm),
             static_cast<const __nv_bfloat16*>(Cm), static_cast<__nv_bfloat16*>(q),
             static_cast<__nv_bfloat16*>(k), g);
     } else {
-        const int64_t items = bt * d.H * (d.Dk / 4);
-        rmcp::ssd_map_inputs_kernel<float><<<rmcp::blocks_for(items), rmcp::kThreads, 0, st>>>(
-            items, d.H, G, d.Dk, dt, A, static_cast<const float*>(Bm), static_cast<const float*>(Cm),
+        rmcp::ssd_map_inputs_kernel<float><<<unsigned(bt), rmcp::kThreads, 0, st>>>(
+            d.H, G, d.Dk, rmcp::log2i(d.Dk / 4), dt, A, static_cast<const float*>(Bm), static_cast<const float*>(Cm),
             static_cast<float*>(q), static_cast<float*>(k), g);
     }
     if (cudaGetLastError() != cudaSuccess) return api_fail(RM_ERR_CUDA, "rm_ssd_map_inputs: launch failed");
@@ -351,15 +360,13 @@ extern "C" rm_status rm_ssd_finish_forward(const rm_cp_problem* p, const void* x
     if (D == nullptr) return RM_OK;
     RM_NEED_SSD(D);
     auto st = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t rows = int64_t(d.B) * d.T * d.H;
+    const unsigned bt = unsigned(int64_t(d.B) * d.T);
     if (p->dtype == RM_BF16) {
-        const int64_t items = rows * (d.Dv / 8);
-        rmcp::ssd_finish_forward_kernel<__nv_bfloat16><<<rmcp::blocks_for(items), rmcp::kThreads, 0, st>>>(
-            items, d.H, d.Dv, static_cast<const __nv_bfloat16*>(x), D, static_cast<__nv_bfloat16*>(o));
+        rmcp::ssd_finish_forward_kernel<__nv_bfloat16><<<bt, rmcp::kThreads, 0, st>>>(
+            d.H, rmcp::log2i(d.Dv / 8), static_cast<const __nv_bfloat16*>(x), D, static_cast<__nv_bfloat16*>(o));
     } else {
-        const int64_t items = rows * (d.Dv / 4);
-        rmcp::ssd_finish_forward_kernel<float><<<rmcp::blocks_for(items), rmcp::kThreads, 0, st>>>(
-            items, d.H, d.Dv, static_cast<const float*>(x), D, static_cast<float*>(o));
+        rmcp::ssd_finish_forward_kernel<float><<<bt, rmcp::kThreads, 0, st>>>(
+            d.H, rmcp::log2i(d.Dv / 4), static_cast<const float*>(x), D, static_cast<float*>(o));
     }
     if (cudaGetLastError() != cudaSuccess) return api_fail(RM_ERR_CUDA, "rm_ssd_finish_forward: launch failed");
     rmcp::note_launch(1);
@@ -404,9 +411,9 @@ extern "C" rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, c
             nbc, d.H, G, d.Dk, dt, A, static_cast<const T*>(Bm), static_cast<const T*>(dq),
             static_cast<const T*>(dk), dg, ddt, static_cast<T*>(dB), static_cast<T*>(dC));
         ++launches;
-        const int64_t nx = rows * (d.Dv / 8);
-        rmcp::ssd_grad_x_kernel<T><<<rmcp::blocks_for(nx), rmcp::kThreads, 0, st>>>(
-            nx, d.H, d.Dv, static_cast<const T*>(x), static_cast<const T*>(dy), D, static_cast<T*>(dv), part);
+        rmcp::ssd_grad_x_kernel<T><<<unsigned(bt), rmcp::kThreads, 0, st>>>(
+            d.H, rmcp::log2i(d.Dv / 8), static_cast<const T*>(x), static_cast<const T*>(dy), D,
+            static_cast<T*>(dv), part);
         ++launches;
     } else {
         using T = float;
@@ -415,9 +422,9 @@ extern "C" rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, c
             nbc, d.H, G, d.Dk, dt, A, static_cast<const T*>(Bm), static_cast<const T*>(dq),
             static_cast<const T*>(dk), dg, ddt, static_cast<T*>(dB), static_cast<T*>(dC));
         ++launches;
-        const int64_t nx = rows * (d.Dv / 4);
-        rmcp::ssd_grad_x_kernel<T><<<rmcp::blocks_for(nx), rmcp::kThreads, 0, st>>>(
-            nx, d.H, d.Dv, static_cast<const T*>(x), static_cast<const T*>(dy), D, static_cast<T*>(dv), part);
+        rmcp::ssd_grad_x_kernel<T><<<unsigned(bt), rmcp::kThreads, 0, st>>>(
+            d.H, rmcp::log2i(d.Dv / 4), static_cast<const T*>(x), static_cast<const T*>(dy), D,
+            static_cast<T*>(dv), part);
         ++launches;
     }
     rmcp::ssd_reduce_heads_kernel<<<rmcp::kRedBlocks, rmcp::kThreads, 0, st>>>(
