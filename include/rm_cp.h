@@ -251,7 +251,7 @@ rm_status rm_cp_selftest_wait_timeout(uint32_t limit_us, rm_stream_t stream);
  * workspace argument: rm_cp_backward_prepare, rm_cp_compose_suffix and
  * rm_cp_backward_apply, in that order on `stream`, with the per-token
  * scratch they pass between each other taken from a fixed array that the
- * library itself holds in device memory.  The paper has no counterpart to
+ * library itself holds in device memory.  The Megatron-Core page has no counterpart to
  * this call; it exists for callers that cannot allocate device memory, such
  * as a custom operator reached through a plugin interface with a fixed
  * signature and no workspace, or a deployment whose device memory is
@@ -279,7 +279,7 @@ rm_status rm_cp_backward_noalloc(const rm_cp_problem* p, const void* q, const vo
  * End to end from host memory: one step of the path (the three forward
  * calls, and the three backward calls when host->dO is not NULL) with its
  * inputs copied in from host buffers and its results copied back out, all
- * enqueued without blocking the host.  The paper has no counterpart to this
+ * enqueued without blocking the host.  The Megatron-Core page has no counterpart to this
  * call; it is the step a training loop makes when its batches live in host
  * memory, with the copies of one step overlapping the kernels of the next.
  *

@@ -2443,8 +2443,7 @@ __global__ void __launch_bounds__(kThreads + 64, 2)
     __shared__ uint32_t tmem_slot;
 
     const Geo G = geo();
-    const bool epi = G.warp < 8;
-    const bool ctl = G.warp == 8;
+    const bool ctl = G.warp == 8;  // warps 0-7 scale, warp 8 issues, warp 9 prepares gates
     const bool gat = G.warp == 9;
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
     const int nch = d.L / kChunk;
