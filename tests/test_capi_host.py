@@ -183,3 +183,32 @@ def test_workload_recipe_is_deterministic_and_shaped():
     assert a.q.shape == (1, 256, 2, 32) and a.q.dtype == torch.float32
     assert torch.allclose(a.k.norm(dim=-1), torch.ones(1, 256, 2), atol=1e-5)
     assert (a.g < 0).all()
+
+
+def test_ssd_calls_validate_before_any_launch():
+    """The SSD maps check the problem, G and every pointer on the host."""
+    lib = C.load()
+    ok = ctypes.c_void_p(0x1000)
+    s = spec(T=256, H=4, Dk=32, Dv=16, chunk=16, scale=1.0)
+    # G must divide H
+    assert lib.rm_ssd_map_inputs(s.ref, 3, ok, ok, ok, ok, ok, ok, ok, None) == 1
+    assert b"G must divide H" in lib.rm_cp_last_error()
+    # the SSD scan runs the recurrence with scale 1
+    bad = spec(T=256, H=4, Dk=32, Dv=16, chunk=16, scale=0.5)
+    assert lib.rm_ssd_finish_forward(bad.ref, ok, ok, ok, None) == 1
+    assert b"scale = 1" in lib.rm_cp_last_error()
+    # rows must split into 16-byte vectors over a power-of-two number of lanes
+    odd = spec(T=256, H=4, Dk=32, Dv=24, chunk=16, scale=1.0, dtype=1)
+    assert lib.rm_ssd_finish_forward(odd.ref, ok, ok, ok, None) == 4
+    # null and misaligned device pointers
+    assert lib.rm_ssd_map_inputs(s.ref, 2, None, ok, ok, ok, ok, ok, ok, None) == 1
+    assert b"dt is NULL" in lib.rm_cp_last_error()
+    mis = ctypes.c_void_p(0x1004)
+    args = [ok] * 16  # x, dt, A, Bm, dy, D, dq, dk, dv, dg, ddt, dA, dB, dC, dD, ws
+    args[10] = mis  # ddt
+    assert lib.rm_ssd_finish_backward(s.ref, 2, *args, None) == 3
+    assert b"ddt is not 16-byte aligned" in lib.rm_cp_last_error()
+    # without D the forward finish has nothing to do and enqueues nothing
+    assert lib.rm_ssd_finish_forward(s.ref, ok, None, ok, None) == 0
+    assert lib.rm_ssd_workspace_size(s.ref) == 4 * (256 * 4 + 2 * 1024 * 4)
+    assert lib.rm_ssd_workspace_size(spec(T=250).ref) == 0
