@@ -13,6 +13,9 @@ dS_in = M^T dS_out + gamma; LinearAttentionCPBackend prepare/apply;
 PackedSequenceCPMetadata) and the gated recurrence
 S_t = exp(g_t) S_{t-1} + k_t v_t^T, o_t = scale S_t^T q_t for the local work.
 
+vg_forward / vg_backward / vg_forward_prepare / vg_compose_prefix are the
+same recurrence with one gate per key dimension (a diagonal transition M).
+
 ssd_forward / ssd_backward are the Mamba2 SSD scan (named by the
 context-parallel pages as the other user of exact state passing), written
 from the published SSD recurrence.
@@ -70,6 +73,9 @@ _SIGS = {
                                      _P, _P, _P, _P, _P, _P]),
     "oracle_packed_metadata": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "oracle_ssd_forward": (None, [_I] * 6 + [_P] * 8),
+    "oracle_vg_forward": (None, [_I] * 5 + [_D] + [_P] * 7),
+    "oracle_vg_backward": (None, [_I] * 5 + [_D] + [_P] * 6 + [_I] + [_P] * 4),
+    "oracle_vg_forward_prepare": (None, [_I] * 6 + [_P] * 7),
     "oracle_ssd_backward": (None, [_I] * 6 + [_P] * 14),
 }
 
@@ -306,3 +312,54 @@ def ssd_backward(x, dt, A, Bm, Cm, dy, D=None, seq_idx=None):
                               _ptr(D), _ptr(si), _ptr(dy), _ptr(dx), _ptr(ddt), _ptr(dA),
                               _ptr(dB), _ptr(dC), _ptr(dD))
     return dx, ddt, dA, dB, dC, dD
+
+
+# ---------------------------------------------------------------- vector gates
+
+def vg_forward(q, k, v, g, scale, seq_idx=None, S0=None):
+    """o [B,T,H,Dv] of S_t = diag(exp(g_t)) S_{t-1} + k_t v_t^T, o_t = scale S_t^T q_t
+    with g [B,T,H,Dk] (fp64).  S0 [B,H,Dk,Dv]: the state before token 0, which then
+    continues it (no reset at token 0)."""
+    q, k, v, g, si, S0 = _f64(q), _f64(k), _f64(v), _f64(g), _i32(seq_idx), _f64(S0)
+    B, T, H, Dk, Dv = _dims(q, v)
+    assert g.shape == (B, T, H, Dk)
+    o = np.empty((B, T, H, Dv))
+    lib().oracle_vg_forward(B, T, H, Dk, Dv, float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                            _ptr(si), _ptr(S0), _ptr(o))
+    return o
+
+
+def vg_backward(q, k, v, g, dO, scale, seq_idx=None, direct=False):
+    """(dq, dk, dv, dg [B,T,H,Dk]) of L = sum dO . o for vg_forward (S0 = 0)."""
+    q, k, v, g, dO, si = _f64(q), _f64(k), _f64(v), _f64(g), _f64(dO), _i32(seq_idx)
+    B, T, H, Dk, Dv = _dims(q, v)
+    dq, dk = np.empty((B, T, H, Dk)), np.empty((B, T, H, Dk))
+    dv, dg = np.empty((B, T, H, Dv)), np.empty((B, T, H, Dk))
+    lib().oracle_vg_backward(B, T, H, Dk, Dv, float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                             _ptr(si), _ptr(dO), int(bool(direct)), _ptr(dq), _ptr(dk), _ptr(dv),
+                             _ptr(dg))
+    return dq, dk, dv, dg
+
+
+def vg_forward_prepare(k, v, g, seg_starts, seq_idx=None):
+    """(M [nseg,B,H,Dk], dS [nseg,B,H,Dk,Dv]): each segment's diagonal transition
+    and its end state from a zero incoming state."""
+    k, v, g, si = _f64(k), _f64(v), _f64(g), _i32(seq_idx)
+    B, T, H, Dk, Dv = _dims(k, v)
+    seg = _seg(seg_starts, T)
+    nseg = len(seg) - 1
+    M = np.empty((nseg, B, H, Dk))
+    dS = np.empty((nseg, B, H, Dk, Dv))
+    lib().oracle_vg_forward_prepare(B, T, H, Dk, Dv, nseg, _ptr(seg), _ptr(k), _ptr(v), _ptr(g),
+                                    _ptr(si), _ptr(M), _ptr(dS))
+    return M, dS
+
+
+def vg_compose_prefix(M, dS):
+    """S_in[j]: segments [0, j) applied in order to a zero state, S <- diag(M_i) S + dS_i."""
+    S = np.zeros(dS.shape[1:])
+    out = np.empty_like(dS)
+    for j in range(dS.shape[0]):
+        out[j] = S
+        S = M[j][..., None] * S + dS[j]
+    return out

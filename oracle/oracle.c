@@ -611,3 +611,126 @@ void oracle_ssd_backward(int B, int T, int H, int G, int N, int P, const double*
     free(dA_part);
     free(dD_part);
 }
+
+/* ----------------------------------------------------------------------- */
+/* Vector (per key dimension) gates: the general transition of the summary  */
+/* algebra restricted to a diagonal M.  Per row b and head h, with g        */
+/* [B,T,H,Dk] fp32 and alpha_t[i] = exp(g_t[i]) (all 0 when token t starts  */
+/* a sequence):                                                             */
+/*   S_t = diag(alpha_t) S_{t-1} + k_t v_t^T,   o_t = scale S_t^T q_t.      */
+/* S0 [B,H,Dk,Dv] (may be NULL) is the state before the first token.        */
+/* ----------------------------------------------------------------------- */
+
+#define VG_IDX(b, t, h) ((((i64)(b) * T + (t)) * H + (h)) * Dk)
+
+static void vg_step(double* S, const double* g, int reset, const double* k, const double* v,
+                    int Dk, int Dv) {
+    for (int i = 0; i < Dk; ++i) {
+        const double a = reset ? 0.0 : exp(g[i]);
+        for (int j = 0; j < Dv; ++j) S[(i64)i * Dv + j] = a * S[(i64)i * Dv + j] + k[i] * v[j];
+    }
+}
+
+void oracle_vg_forward(int B, int T, int H, int Dk, int Dv, double scale, const double* q,
+                       const double* k, const double* v, const double* g, const int32_t* seq_idx,
+                       const double* S0, double* o) {
+    const i64 SZ = (i64)Dk * Dv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i64 bh = 0; bh < (i64)B * H; ++bh) {
+        const int b = (int)(bh / H), h = (int)(bh % H);
+        double* S = (double*)calloc((size_t)SZ, sizeof(double));
+        if (S0) memcpy(S, S0 + bh * SZ, sizeof(double) * (size_t)SZ);
+        for (i64 t = 0; t < T; ++t) {
+            vg_step(S, g + VG_IDX(b, t, h), starts_sequence(seq_idx, t) && (t > 0 || S0 == NULL),
+                    k + IDX_QK(b, t, h), v + IDX_V(b, t, h), Dk, Dv);
+            state_read(S, q + IDX_QK(b, t, h), scale, o + IDX_V(b, t, h), Dk, Dv);
+        }
+        free(S);
+    }
+}
+
+/* Backward of L = sum_t dO_t . o_t (S0 = 0).  dq_t = scale S_t dO_t;
+ * D_t = scale q_t dO_t^T + diag(alpha_{t+1}) D_{t+1}; dk_t = D_t v_t,
+ * dv_t = D_t^T k_t; per dimension i the gate gradient is
+ * dg_t[i] = sum_{r >= t, same sequence} (q_r[i] dq_r[i] - k_r[i] dk_r[i]),
+ * 0 at sequence starts; direct != 0 takes alpha_t[i] <S_{t-1}[i,:], D_t[i,:]>
+ * from stored states instead (small inputs only). */
+void oracle_vg_backward(int B, int T, int H, int Dk, int Dv, double scale, const double* q,
+                        const double* k, const double* v, const double* g,
+                        const int32_t* seq_idx, const double* dO, int direct, double* dq,
+                        double* dk, double* dv, double* dg) {
+    const i64 SZ = (i64)Dk * Dv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i64 bh = 0; bh < (i64)B * H; ++bh) {
+        const int b = (int)(bh / H), h = (int)(bh % H);
+        double* states = (double*)calloc((size_t)(direct ? T + 1 : 1) * SZ, sizeof(double));
+        double* S = states;
+        double* qdq = (double*)malloc(sizeof(double) * (size_t)T * Dk);
+        for (i64 t = 0; t < T; ++t) {
+            if (direct) {
+                memcpy(states + (t + 1) * SZ, states + t * SZ, sizeof(double) * (size_t)SZ);
+                S = states + (t + 1) * SZ;
+            }
+            vg_step(S, g + VG_IDX(b, t, h), starts_sequence(seq_idx, t), k + IDX_QK(b, t, h),
+                    v + IDX_V(b, t, h), Dk, Dv);
+            state_apply(S, dO + IDX_V(b, t, h), scale, dq + IDX_QK(b, t, h), Dk, Dv);
+            for (int i = 0; i < Dk; ++i) qdq[t * Dk + i] = q[IDX_QK(b, t, h) + i] * dq[IDX_QK(b, t, h) + i];
+        }
+        double* D = (double*)calloc((size_t)SZ, sizeof(double));
+        double* run = (double*)calloc((size_t)Dk, sizeof(double));
+        for (i64 t = T - 1; t >= 0; --t) {
+            const int next_reset = (t + 1 >= T) || starts_sequence(seq_idx, t + 1);
+            const double* gn = (t + 1 < T) ? g + VG_IDX(b, t + 1, h) : NULL;
+            const double* qt = q + IDX_QK(b, t, h);
+            const double* dOt = dO + IDX_V(b, t, h);
+            for (int i = 0; i < Dk; ++i) {
+                const double beta = next_reset ? 0.0 : exp(gn[i]);
+                for (int j = 0; j < Dv; ++j)
+                    D[(i64)i * Dv + j] = scale * qt[i] * dOt[j] + beta * D[(i64)i * Dv + j];
+            }
+            adjoint_read(D, k + IDX_QK(b, t, h), v + IDX_V(b, t, h), dk + IDX_QK(b, t, h),
+                         dv + IDX_V(b, t, h), Dk, Dv);
+            double* dgt = dg + VG_IDX(b, t, h);
+            const int start = starts_sequence(seq_idx, t);
+            for (int i = 0; i < Dk; ++i) {
+                if (direct) {
+                    double acc = 0.0;
+                    for (int j = 0; j < Dv; ++j) acc += states[t * SZ + (i64)i * Dv + j] * D[(i64)i * Dv + j];
+                    dgt[i] = start ? 0.0 : exp(g[VG_IDX(b, t, h) + i]) * acc;
+                } else {
+                    const double c = qdq[t * Dk + i] - k[IDX_QK(b, t, h) + i] * dk[IDX_QK(b, t, h) + i];
+                    run[i] = next_reset ? c : c + run[i];
+                    dgt[i] = start ? 0.0 : run[i];
+                }
+            }
+        }
+        free(run);
+        free(D);
+        free(qdq);
+        free(states);
+    }
+}
+
+/* cp_forward_prepare with vector gates: per (segment, row, head) the diagonal
+ * transition M [Dk] (prod of alpha over the segment, 0 where a token of it
+ * starts a sequence) and the local end state dS from S_in = 0. */
+void oracle_vg_forward_prepare(int B, int T, int H, int Dk, int Dv, int nseg,
+                               const int32_t* seg_starts, const double* k, const double* v,
+                               const double* g, const int32_t* seq_idx, double* M, double* dS) {
+    const i64 SZ = (i64)Dk * Dv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i64 task = 0; task < (i64)nseg * B * H; ++task) {
+        const int j = (int)(task / ((i64)B * H));
+        const int b = (int)((task / H) % B), h = (int)(task % H);
+        double* S = dS + task * SZ;
+        double* m = M + task * Dk;
+        memset(S, 0, sizeof(double) * (size_t)SZ);
+        for (int i = 0; i < Dk; ++i) m[i] = 1.0;
+        for (i64 t = seg_starts[j]; t < seg_starts[j + 1]; ++t) {
+            const int reset = starts_sequence(seq_idx, t);
+            const double* gt = g + VG_IDX(b, t, h);
+            for (int i = 0; i < Dk; ++i) m[i] = reset ? 0.0 : m[i] * exp(gt[i]);
+            vg_step(S, gt, reset, k + IDX_QK(b, t, h), v + IDX_V(b, t, h), Dk, Dv);
+        }
+    }
+}

@@ -496,3 +496,116 @@ def test_ssd_gradients_match_finite_differences(reset):
             a2[i] -= eps
             fd[i] = (loss(**{name: a1}) - loss(**{name: a2})) / (2 * eps)
         assert np.max(np.abs(fd - gr)) <= 1e-7 * np.max(np.abs(fd)), name
+
+
+# ------------------------------------------------------------------ vector gates
+# One gate per key dimension: S_t = diag(exp(g_t)) S_{t-1} + k_t v_t^T (the
+# diagonal case of the summary algebra's general transition M).  Pins: the
+# quadratic closed form, the reduction to scalar gates, finite differences of
+# every gradient, the direct gate gradient, the segmentation invariant and the
+# reset invariant.
+
+def _vg_inputs(rng, B, T, H, Dk, Dv):
+    q = rng.standard_normal((B, T, H, Dk))
+    k = rng.standard_normal((B, T, H, Dk))
+    v = rng.standard_normal((B, T, H, Dv))
+    g = -np.abs(rng.standard_normal((B, T, H, Dk))) * 0.5
+    return q, k, v, g
+
+
+def test_vg_forward_matches_quadratic_form():
+    rng = np.random.default_rng(31)
+    q, k, v, g = _vg_inputs(rng, 1, 14, 2, 3, 2)
+    si = np.array([0] * 4 + [1] * 6 + [2] * 4, dtype=np.int32)
+    for seq in (None, si):
+        o = oracle.vg_forward(q, k, v, g, 0.7, seq)
+        sid = np.zeros(14, dtype=np.int64) if seq is None else seq
+        G = np.cumsum(g, axis=1)
+        ref = np.zeros_like(o)
+        for h in range(2):
+            for t in range(14):
+                for s in range(t + 1):
+                    if sid[s] == sid[t]:
+                        w = np.sum(q[0, t, h] * k[0, s, h] * np.exp(G[0, t, h] - G[0, s, h]))
+                        ref[0, t, h] += 0.7 * w * v[0, s, h]
+        np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+
+
+def test_vg_equal_gates_reduce_to_scalar_gates():
+    """g_t[i] = g_t for every i is the scalar gate: same outputs and gradients,
+    and the scalar gate's gradient is the sum of the per-dimension ones."""
+    rng = np.random.default_rng(32)
+    q, k, v, g = _vg_inputs(rng, 2, 12, 2, 4, 3)
+    gs = g[..., 0]
+    gv = np.repeat(gs[..., None], 4, axis=-1)
+    dO = rng.standard_normal(v.shape)
+    np.testing.assert_allclose(oracle.vg_forward(q, k, v, gv, 0.5), oracle.forward(q, k, v, gs, 0.5),
+                               rtol=1e-12, atol=1e-12)
+    a = oracle.vg_backward(q, k, v, gv, dO, 0.5)
+    b = oracle.backward(q, k, v, gs, dO, 0.5)
+    for x, y in zip(a[:3], b[:3]):
+        np.testing.assert_allclose(x, y, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(a[3].sum(axis=-1), b[3], rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("reset", [False, True])
+def test_vg_gradients_match_finite_differences(reset):
+    rng = np.random.default_rng(33)
+    q, k, v, g = _vg_inputs(rng, 1, 10, 2, 3, 2)
+    dO = rng.standard_normal(v.shape)
+    si = np.array([0, 0, 0, 1, 1, 2, 2, 2, 2, 2], dtype=np.int32) if reset else None
+    grads = oracle.vg_backward(q, k, v, g, dO, 0.7, si)
+    direct = oracle.vg_backward(q, k, v, g, dO, 0.7, si, direct=True)
+    np.testing.assert_allclose(grads[3], direct[3], rtol=1e-10, atol=1e-12)
+    base = dict(q=q, k=k, v=v, g=g)
+    eps = 1e-6
+    for name, gr in zip(("q", "k", "v", "g"), grads):
+        arr = base[name]
+        fd = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            a1, a2 = arr.copy(), arr.copy()
+            a1[i] += eps
+            a2[i] -= eps
+            fd[i] = (np.sum(dO * oracle.vg_forward(**dict(base, **{name: a1}), scale=0.7, seq_idx=si))
+                     - np.sum(dO * oracle.vg_forward(**dict(base, **{name: a2}), scale=0.7, seq_idx=si))) / (2 * eps)
+        assert np.max(np.abs(fd - gr)) <= 1e-7 * np.max(np.abs(fd)), name
+    if reset:
+        assert np.all(grads[3][:, [0, 3, 5]] == 0.0)
+
+
+def test_vg_segmented_equals_monolithic():
+    """Summaries with a diagonal transition: prepare, compose, then each segment
+    from its incoming state gives the monolithic outputs."""
+    rng = np.random.default_rng(34)
+    q, k, v, g = _vg_inputs(rng, 2, 24, 2, 3, 2)
+    mono = oracle.vg_forward(q, k, v, g, 0.6)
+    for seg in ([0, 24], [0, 8, 16, 24], [0, 1, 7, 20, 24]):
+        seg = np.array(seg, dtype=np.int32)
+        M, dS = oracle.vg_forward_prepare(k, v, g, seg)
+        S_in = oracle.vg_compose_prefix(M, dS)
+        out = np.empty_like(mono)
+        for j in range(len(seg) - 1):
+            sl = slice(seg[j], seg[j + 1])
+            out[:, sl] = oracle.vg_forward(q[:, sl], k[:, sl], v[:, sl], g[:, sl], 0.6, S0=S_in[j])
+        np.testing.assert_allclose(out, mono, rtol=1e-12, atol=1e-12)
+        # M is the product of a segment's per-dimension decays, 0 for the segment
+        # holding the row's first token (a sequence start)
+        assert np.all(M[0] == 0.0)
+        for j in range(1, len(seg) - 1):
+            np.testing.assert_allclose(M[j], np.exp(g[:, seg[j]:seg[j + 1]].sum(axis=1)), rtol=1e-12)
+
+
+def test_vg_packed_equals_separate_runs():
+    rng = np.random.default_rng(35)
+    q, k, v, g = _vg_inputs(rng, 1, 15, 2, 3, 2)
+    dO = rng.standard_normal(v.shape)
+    cut = [0, 6, 7, 15]
+    si = np.concatenate([np.full(cut[i + 1] - cut[i], i) for i in range(3)]).astype(np.int32)
+    o = oracle.vg_forward(q, k, v, g, 0.5, si)
+    gr = oracle.vg_backward(q, k, v, g, dO, 0.5, si)
+    for i in range(3):
+        sl = slice(cut[i], cut[i + 1])
+        assert np.array_equal(o[:, sl], oracle.vg_forward(q[:, sl], k[:, sl], v[:, sl], g[:, sl], 0.5))
+        gs = oracle.vg_backward(q[:, sl], k[:, sl], v[:, sl], g[:, sl], dO[:, sl], 0.5)
+        for a, b in zip(gr, gs):
+            assert np.array_equal(a[:, sl], b)
