@@ -16,6 +16,9 @@ S_t = exp(g_t) S_{t-1} + k_t v_t^T, o_t = scale S_t^T q_t for the local work.
 vg_forward / vg_backward / vg_forward_prepare / vg_compose_prefix are the
 same recurrence with one gate per key dimension (a diagonal transition M).
 
+gdr_forward / gdr_backward / gdr_forward_prepare / gdr_compose_prefix are the
+gated delta rule, whose segment transitions are Dk x Dk matrices.
+
 ssd_forward / ssd_backward are the Mamba2 SSD scan (named by the
 context-parallel pages as the other user of exact state passing), written
 from the published SSD recurrence.
@@ -76,6 +79,9 @@ _SIGS = {
     "oracle_vg_forward": (None, [_I] * 5 + [_D] + [_P] * 7),
     "oracle_vg_backward": (None, [_I] * 5 + [_D] + [_P] * 6 + [_I] + [_P] * 4),
     "oracle_vg_forward_prepare": (None, [_I] * 6 + [_P] * 7),
+    "oracle_gdr_forward": (None, [_I] * 5 + [_D] + [_P] * 8),
+    "oracle_gdr_backward": (None, [_I] * 5 + [_D] + [_P] * 12),
+    "oracle_gdr_forward_prepare": (None, [_I] * 6 + [_P] * 8),
     "oracle_ssd_backward": (None, [_I] * 6 + [_P] * 14),
 }
 
@@ -362,4 +368,57 @@ def vg_compose_prefix(M, dS):
     for j in range(dS.shape[0]):
         out[j] = S
         S = M[j][..., None] * S + dS[j]
+    return out
+
+
+# ---------------------------------------------------------------- gated delta rule
+
+def gdr_forward(q, k, v, g, beta, scale, seq_idx=None, S0=None):
+    """o of S_t = exp(g_t)(I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
+    o_t = scale S_t^T q_t (fp64); g, beta [B,T,H].  S0 [B,H,Dk,Dv]: the state
+    before token 0, which then continues it (no reset at token 0)."""
+    q, k, v, g, be, si, S0 = (_f64(q), _f64(k), _f64(v), _f64(g), _f64(beta), _i32(seq_idx),
+                              _f64(S0))
+    B, T, H, Dk, Dv = _dims(q, v)
+    o = np.empty((B, T, H, Dv))
+    lib().oracle_gdr_forward(B, T, H, Dk, Dv, float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                             _ptr(be), _ptr(si), _ptr(S0), _ptr(o))
+    return o
+
+
+def gdr_backward(q, k, v, g, beta, dO, scale, seq_idx=None):
+    """(dq, dk, dv, dg, dbeta) of L = sum dO . o for gdr_forward (small inputs:
+    every state is stored)."""
+    q, k, v, g, be, dO, si = (_f64(q), _f64(k), _f64(v), _f64(g), _f64(beta), _f64(dO),
+                              _i32(seq_idx))
+    B, T, H, Dk, Dv = _dims(q, v)
+    dq, dk, dv = np.empty((B, T, H, Dk)), np.empty((B, T, H, Dk)), np.empty((B, T, H, Dv))
+    dg, db = np.empty((B, T, H)), np.empty((B, T, H))
+    lib().oracle_gdr_backward(B, T, H, Dk, Dv, float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                              _ptr(be), _ptr(si), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                              _ptr(db))
+    return dq, dk, dv, dg, db
+
+
+def gdr_forward_prepare(k, v, g, beta, seg_starts, seq_idx=None):
+    """(M [nseg,B,H,Dk,Dk], dS [nseg,B,H,Dk,Dv]): each segment's transition
+    (the ordered product of its A_t) and its end state from a zero state."""
+    k, v, g, be, si = _f64(k), _f64(v), _f64(g), _f64(beta), _i32(seq_idx)
+    B, T, H, Dk, Dv = _dims(k, v)
+    seg = _seg(seg_starts, T)
+    nseg = len(seg) - 1
+    M = np.empty((nseg, B, H, Dk, Dk))
+    dS = np.empty((nseg, B, H, Dk, Dv))
+    lib().oracle_gdr_forward_prepare(B, T, H, Dk, Dv, nseg, _ptr(seg), _ptr(k), _ptr(v), _ptr(g),
+                                     _ptr(be), _ptr(si), _ptr(M), _ptr(dS))
+    return M, dS
+
+
+def gdr_compose_prefix(M, dS):
+    """S_in[j]: segments [0, j) applied in order to a zero state, S <- M_i S + dS_i."""
+    S = np.zeros(dS.shape[1:])
+    out = np.empty_like(dS)
+    for j in range(dS.shape[0]):
+        out[j] = S
+        S = M[j] @ S + dS[j]
     return out

@@ -734,3 +734,175 @@ void oracle_vg_forward_prepare(int B, int T, int H, int Dk, int Dv, int nseg,
         }
     }
 }
+
+/* ----------------------------------------------------------------------- */
+/* Gated delta rule: the matrix-transition case of the summary algebra.     */
+/* Per row b and head h, with a scalar gate g_t, a write strength beta_t    */
+/* ([B,T,H] each) and A_t = alpha_t (I - beta_t k_t k_t^T), alpha_t =        */
+/* exp(g_t) (0 when token t starts a sequence):                              */
+/*   S_t = A_t S_{t-1} + beta_t k_t v_t^T,   o_t = scale S_t^T q_t.          */
+/* Every state is stored (memory O(T Dk Dv) per task): small inputs only.   */
+/* ----------------------------------------------------------------------- */
+
+/* S_out = alpha (S_in - beta k (k^T S_in)) + beta k v^T */
+static void gdr_step(double* S, double alpha, double beta, const double* k, const double* v,
+                     int Dk, int Dv, double* kS) {
+    for (int j = 0; j < Dv; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < Dk; ++i) acc += k[i] * S[(i64)i * Dv + j];
+        kS[j] = acc;
+    }
+    for (int i = 0; i < Dk; ++i)
+        for (int j = 0; j < Dv; ++j)
+            S[(i64)i * Dv + j] = alpha * (S[(i64)i * Dv + j] - beta * k[i] * kS[j]) + beta * k[i] * v[j];
+}
+
+void oracle_gdr_forward(int B, int T, int H, int Dk, int Dv, double scale, const double* q,
+                        const double* k, const double* v, const double* g, const double* beta,
+                        const int32_t* seq_idx, const double* S0, double* o) {
+    const i64 SZ = (i64)Dk * Dv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i64 bh = 0; bh < (i64)B * H; ++bh) {
+        const int b = (int)(bh / H), h = (int)(bh % H);
+        double* S = (double*)calloc((size_t)SZ, sizeof(double));
+        double* kS = (double*)malloc(sizeof(double) * (size_t)Dv);
+        if (S0) memcpy(S, S0 + bh * SZ, sizeof(double) * (size_t)SZ);
+        for (i64 t = 0; t < T; ++t) {
+            const int reset = starts_sequence(seq_idx, t) && (t > 0 || S0 == NULL);
+            const double a = reset ? 0.0 : exp(g[IDX_G(b, t, h)]);
+            gdr_step(S, a, beta[IDX_G(b, t, h)], k + IDX_QK(b, t, h), v + IDX_V(b, t, h), Dk, Dv, kS);
+            state_read(S, q + IDX_QK(b, t, h), scale, o + IDX_V(b, t, h), Dk, Dv);
+        }
+        free(kS);
+        free(S);
+    }
+}
+
+/* Backward of L = sum_t dO_t . o_t (zero initial state), from the stored
+ * states and the adjoint D_t = scale q_t dO_t^T + A_{t+1} D_{t+1} (A is
+ * symmetric; A_T = 0):
+ *   dq_t    = scale S_t dO_t
+ *   dv_t    = beta_t D_t^T k_t
+ *   dk_t    = beta_t D_t v_t - alpha_t beta_t (S_{t-1} D_t^T + D_t S_{t-1}^T) k_t
+ *   dbeta_t = k_t^T D_t v_t - alpha_t k_t^T D_t S_{t-1}^T k_t
+ *   dg_t    = alpha_t <D_t, (I - beta_t k_t k_t^T) S_{t-1}>   (0 at a start) */
+void oracle_gdr_backward(int B, int T, int H, int Dk, int Dv, double scale, const double* q,
+                         const double* k, const double* v, const double* g, const double* beta,
+                         const int32_t* seq_idx, const double* dO, double* dq, double* dk,
+                         double* dv, double* dg, double* dbeta) {
+    const i64 SZ = (i64)Dk * Dv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i64 bh = 0; bh < (i64)B * H; ++bh) {
+        const int b = (int)(bh / H), h = (int)(bh % H);
+        double* st = (double*)calloc((size_t)(T + 1) * SZ, sizeof(double)); /* st[t+1] = S_t */
+        double* kS = (double*)malloc(sizeof(double) * (size_t)Dv);
+        double* Dt = (double*)calloc((size_t)SZ, sizeof(double));
+        double* tmp = (double*)malloc(sizeof(double) * (size_t)SZ);
+        double* u = (double*)malloc(sizeof(double) * (size_t)Dk);
+        double* w = (double*)malloc(sizeof(double) * (size_t)Dv);
+        for (i64 t = 0; t < T; ++t) {
+            const double a = starts_sequence(seq_idx, t) ? 0.0 : exp(g[IDX_G(b, t, h)]);
+            memcpy(st + (t + 1) * SZ, st + t * SZ, sizeof(double) * (size_t)SZ);
+            gdr_step(st + (t + 1) * SZ, a, beta[IDX_G(b, t, h)], k + IDX_QK(b, t, h), v + IDX_V(b, t, h),
+                     Dk, Dv, kS);
+            state_apply(st + (t + 1) * SZ, dO + IDX_V(b, t, h), scale, dq + IDX_QK(b, t, h), Dk, Dv);
+        }
+        for (i64 t = T - 1; t >= 0; --t) {
+            /* D_t = scale q_t dO_t^T + A_{t+1} D_{t+1} */
+            if (t + 1 < T) {
+                const double an = starts_sequence(seq_idx, t + 1) ? 0.0 : exp(g[IDX_G(b, t + 1, h)]);
+                const double bn = beta[IDX_G(b, t + 1, h)];
+                const double* kn = k + IDX_QK(b, t + 1, h);
+                for (int j = 0; j < Dv; ++j) {
+                    double acc = 0.0;
+                    for (int i = 0; i < Dk; ++i) acc += kn[i] * Dt[(i64)i * Dv + j];
+                    w[j] = acc;
+                }
+                for (int i = 0; i < Dk; ++i)
+                    for (int j = 0; j < Dv; ++j)
+                        tmp[(i64)i * Dv + j] = an * (Dt[(i64)i * Dv + j] - bn * kn[i] * w[j]);
+            } else {
+                memset(tmp, 0, sizeof(double) * (size_t)SZ);
+            }
+            const double* qt = q + IDX_QK(b, t, h);
+            const double* dOt = dO + IDX_V(b, t, h);
+            for (int i = 0; i < Dk; ++i)
+                for (int j = 0; j < Dv; ++j) Dt[(i64)i * Dv + j] = scale * qt[i] * dOt[j] + tmp[(i64)i * Dv + j];
+            const double* kt = k + IDX_QK(b, t, h);
+            const double* vt = v + IDX_V(b, t, h);
+            const double* Sp = st + t * SZ; /* S_{t-1} */
+            const int start = starts_sequence(seq_idx, t);
+            const double a = start ? 0.0 : exp(g[IDX_G(b, t, h)]);
+            const double bt = beta[IDX_G(b, t, h)];
+            /* w = D_t^T k_t, u = D_t v_t */
+            for (int j = 0; j < Dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < Dk; ++i) acc += Dt[(i64)i * Dv + j] * kt[i];
+                w[j] = acc;
+                dv[IDX_V(b, t, h) + j] = bt * acc;
+            }
+            for (int i = 0; i < Dk; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < Dv; ++j) acc += Dt[(i64)i * Dv + j] * vt[j];
+                u[i] = acc;
+            }
+            /* kS = S_{t-1}^T k_t;  (S D^T + D S^T) k = S (D^T k) + D (S^T k) */
+            for (int j = 0; j < Dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < Dk; ++i) acc += Sp[(i64)i * Dv + j] * kt[i];
+                kS[j] = acc;
+            }
+            double kDv = 0.0, kDSk = 0.0, dgacc = 0.0;
+            for (int i = 0; i < Dk; ++i) {
+                double s1 = 0.0, s2 = 0.0;
+                for (int j = 0; j < Dv; ++j) {
+                    s1 += Sp[(i64)i * Dv + j] * w[j];
+                    s2 += Dt[(i64)i * Dv + j] * kS[j];
+                }
+                dk[IDX_QK(b, t, h) + i] = bt * u[i] - a * bt * (s1 + s2);
+                kDv += kt[i] * u[i];
+                kDSk += kt[i] * s2;
+            }
+            for (int i = 0; i < Dk; ++i)
+                for (int j = 0; j < Dv; ++j)
+                    dgacc += Dt[(i64)i * Dv + j] * (Sp[(i64)i * Dv + j] - bt * kt[i] * kS[j]);
+            dbeta[IDX_G(b, t, h)] = kDv - a * kDSk;
+            dg[IDX_G(b, t, h)] = start ? 0.0 : a * dgacc;
+        }
+        free(w);
+        free(u);
+        free(tmp);
+        free(Dt);
+        free(kS);
+        free(st);
+    }
+}
+
+/* Segment summaries with matrix transitions: M [nseg,B,H,Dk,Dk] = A_last ... A_first
+ * over the segment (A_t = 0 at a sequence start), dS the local end state. */
+void oracle_gdr_forward_prepare(int B, int T, int H, int Dk, int Dv, int nseg,
+                                const int32_t* seg_starts, const double* k, const double* v,
+                                const double* g, const double* beta, const int32_t* seq_idx,
+                                double* M, double* dS) {
+    const i64 SZ = (i64)Dk * Dv, MZ = (i64)Dk * Dk;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i64 task = 0; task < (i64)nseg * B * H; ++task) {
+        const int j = (int)(task / ((i64)B * H));
+        const int b = (int)((task / H) % B), h = (int)(task % H);
+        double* S = dS + task * SZ;
+        double* Mt = M + task * MZ;
+        double* kS = (double*)malloc(sizeof(double) * (size_t)(Dv > Dk ? Dv : Dk));
+        double* zero = (double*)calloc((size_t)Dk, sizeof(double));
+        memset(S, 0, sizeof(double) * (size_t)SZ);
+        memset(Mt, 0, sizeof(double) * (size_t)MZ);
+        for (int i = 0; i < Dk; ++i) Mt[(i64)i * Dk + i] = 1.0;
+        for (i64 t = seg_starts[j]; t < seg_starts[j + 1]; ++t) {
+            const double a = starts_sequence(seq_idx, t) ? 0.0 : exp(g[IDX_G(b, t, h)]);
+            const double bt = beta[IDX_G(b, t, h)];
+            gdr_step(S, a, bt, k + IDX_QK(b, t, h), v + IDX_V(b, t, h), Dk, Dv, kS);
+            gdr_step(Mt, a, bt, k + IDX_QK(b, t, h), zero, Dk, Dk, kS); /* M <- A_t M */
+        }
+        free(zero);
+        free(kS);
+    }
+}

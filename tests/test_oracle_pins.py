@@ -609,3 +609,104 @@ def test_vg_packed_equals_separate_runs():
         gs = oracle.vg_backward(q[:, sl], k[:, sl], v[:, sl], g[:, sl], dO[:, sl], 0.5)
         for a, b in zip(gr, gs):
             assert np.array_equal(a[:, sl], b)
+
+
+# ------------------------------------------------------------------ gated delta rule
+# S_t = exp(g_t)(I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T: the summary
+# algebra with matrix transitions.  Pins: reductions to causal linear attention
+# (orthonormal keys), to an overwrite (a repeated key), to pure decay (beta = 0),
+# finite differences of every gradient and the segmentation invariant with the
+# Dk x Dk transitions.
+
+def _gdr_inputs(rng, B, T, H, Dk, Dv):
+    q = rng.standard_normal((B, T, H, Dk))
+    k = rng.standard_normal((B, T, H, Dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, H, Dv))
+    g = -np.abs(rng.standard_normal((B, T, H))) * 0.5
+    beta = rng.uniform(0.1, 0.9, (B, T, H))
+    return q, k, v, g, beta
+
+
+def test_gdr_orthonormal_keys_is_linear_attention():
+    """alpha = beta = 1 with orthonormal keys: each write leaves the others'
+    values alone, so o_t = scale sum_{s<=t} (q_t . k_s) v_s."""
+    rng = np.random.default_rng(41)
+    T, Dk, Dv = 5, 6, 3
+    basis, _ = np.linalg.qr(rng.standard_normal((Dk, Dk)))
+    k = basis[:T][None, :, None, :]
+    q = rng.standard_normal((1, T, 1, Dk))
+    v = rng.standard_normal((1, T, 1, Dv))
+    o = oracle.gdr_forward(q, k, v, np.zeros((1, T, 1)), np.ones((1, T, 1)), 0.8)
+    ref = np.stack([0.8 * sum((q[0, t, 0] @ k[0, s, 0]) * v[0, s, 0] for s in range(t + 1))
+                    for t in range(T)])
+    np.testing.assert_allclose(o[0, :, 0], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gdr_repeated_key_overwrites():
+    rng = np.random.default_rng(42)
+    kk = rng.standard_normal(4)
+    kk /= np.linalg.norm(kk)
+    k = np.stack([kk, kk])[None, :, None, :]
+    v = rng.standard_normal((1, 2, 1, 3))
+    q = rng.standard_normal((1, 2, 1, 4))
+    o = oracle.gdr_forward(q, k, v, np.zeros((1, 2, 1)), np.ones((1, 2, 1)), 1.0)
+    np.testing.assert_allclose(o[0, 1, 0], (q[0, 1, 0] @ kk) * v[0, 1, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_gdr_zero_beta_is_pure_decay():
+    rng = np.random.default_rng(43)
+    q, k, v, g, _ = _gdr_inputs(rng, 1, 6, 2, 3, 2)
+    S0 = rng.standard_normal((1, 2, 3, 2))
+    o = oracle.gdr_forward(q, k, v, g, np.zeros((1, 6, 2)), 0.5, S0=S0)
+    decay = np.exp(np.cumsum(g, axis=1))
+    ref = 0.5 * decay[..., None] * np.einsum("bhij,bthi->bthj", S0, q)
+    np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("reset", [False, True])
+def test_gdr_gradients_match_finite_differences(reset):
+    rng = np.random.default_rng(44)
+    q, k, v, g, beta = _gdr_inputs(rng, 1, 8, 2, 3, 2)
+    dO = rng.standard_normal(v.shape)
+    si = np.array([0, 0, 0, 1, 1, 1, 1, 1], dtype=np.int32) if reset else None
+    grads = oracle.gdr_backward(q, k, v, g, beta, dO, 0.7, si)
+    base = dict(q=q, k=k, v=v, g=g, beta=beta)
+    eps = 1e-6
+    for name, gr in zip(("q", "k", "v", "g", "beta"), grads):
+        arr = base[name]
+        fd = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            a1, a2 = arr.copy(), arr.copy()
+            a1[i] += eps
+            a2[i] -= eps
+            fd[i] = (np.sum(dO * oracle.gdr_forward(**dict(base, **{name: a1}), scale=0.7, seq_idx=si))
+                     - np.sum(dO * oracle.gdr_forward(**dict(base, **{name: a2}), scale=0.7, seq_idx=si))) / (2 * eps)
+        assert np.max(np.abs(fd - gr)) <= 1e-7 * np.max(np.abs(fd)), name
+    if reset:
+        assert np.all(grads[3][:, [0, 3]] == 0.0)
+
+
+def test_gdr_segmented_equals_monolithic():
+    rng = np.random.default_rng(45)
+    q, k, v, g, beta = _gdr_inputs(rng, 2, 18, 2, 3, 2)
+    mono = oracle.gdr_forward(q, k, v, g, beta, 0.6)
+    for seg in ([0, 18], [0, 6, 12, 18], [0, 1, 5, 14, 18]):
+        seg = np.array(seg, dtype=np.int32)
+        M, dS = oracle.gdr_forward_prepare(k, v, g, beta, seg)
+        S_in = oracle.gdr_compose_prefix(M, dS)
+        out = np.empty_like(mono)
+        for j in range(len(seg) - 1):
+            sl = slice(seg[j], seg[j + 1])
+            out[:, sl] = oracle.gdr_forward(q[:, sl], k[:, sl], v[:, sl], g[:, sl], beta[:, sl], 0.6,
+                                            S0=S_in[j])
+        np.testing.assert_allclose(out, mono, rtol=1e-12, atol=1e-12)
+        assert np.all(M[0] == 0.0)  # the segment holding the row's first token
+        for j in range(1, len(seg) - 1):  # M_j = A_last ... A_first, built here in numpy
+            for b in range(2):
+                for h in range(2):
+                    P = np.eye(3)
+                    for t in range(seg[j], seg[j + 1]):
+                        kt = k[b, t, h]
+                        P = np.exp(g[b, t, h]) * (np.eye(3) - beta[b, t, h] * np.outer(kt, kt)) @ P
+                    np.testing.assert_allclose(M[j, b, h], P, rtol=1e-12, atol=1e-14)
