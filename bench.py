@@ -218,14 +218,20 @@ def replica_throughput(world: int, tokens_per_step: int, ms_per_step: float) -> 
 
 # ------------------------------------------------------------------ GPU arm
 
-def run_ours(args, rank, world, local_rank):
+# The headline is the largest single-GPU configuration (256k, fwd+bwd); the
+# other configurations of the metric are measured in the same run and
+# reported under "workloads".
+HEADLINE = "256k"
+SUB_WORKLOADS = ("32k", "packed64k", "fwd4k")
+
+
+def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_cpu):
+    """Times one workload: `steps` whole steps (fwd+bwd, or fwd for forward-only
+    workloads) with per-phase CUDA events, then `steps` forward-only steps.
+    Returns the workload's fields of the JSON line."""
     from state_summary_scan_gb300 import _capi as C
     from state_summary_scan_gb300 import api
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w = workload_of(args)
-    peaks, peak_src = load_peaks()
     inp = make_inputs(w)
     q, k, v, g = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.g))
     dO = inp.dO.to(dev) if w.backward else None
@@ -237,28 +243,24 @@ def run_ours(args, rank, world, local_rank):
     s = plan.spec
     stream = torch.cuda.current_stream(dev)
     phases = PHASES_FWD + (PHASES_BWD if w.backward else ())
+    fns = {
+        "forward_prepare": lambda: C.rm_cp_forward_prepare(s, k, v, g, plan.M, plan.dS, plan.ws, stream),
+        "compose_prefix": lambda: C.rm_cp_compose_prefix(s, plan.M, plan.dS, plan.S_in, stream),
+        "forward_apply": lambda: C.rm_cp_forward_apply(s, q, k, v, g, plan.S_in, o, plan.ws, stream),
+        "backward_prepare": lambda: C.rm_cp_backward_prepare(s, q, k, v, g, plan.S_in, dO, plan.gamma,
+                                                             dq, plan.ws, stream),
+        "compose_suffix": lambda: C.rm_cp_compose_suffix(s, plan.M, plan.gamma, plan.dS_out, stream),
+        "backward_apply": lambda: C.rm_cp_backward_apply(s, q, k, v, g, dO, plan.S_in, plan.dS_out,
+                                                         dk, dv, dg, plan.ws, stream),
+    }
 
-    def calls(q, k, v, g, dO, o, dq, dk, dv, dg):
-        return {
-            "forward_prepare": lambda: C.rm_cp_forward_prepare(s, k, v, g, plan.M, plan.dS, plan.ws, stream),
-            "compose_prefix": lambda: C.rm_cp_compose_prefix(s, plan.M, plan.dS, plan.S_in, stream),
-            "forward_apply": lambda: C.rm_cp_forward_apply(s, q, k, v, g, plan.S_in, o, plan.ws, stream),
-            "backward_prepare": lambda: C.rm_cp_backward_prepare(s, q, k, v, g, plan.S_in, dO, plan.gamma,
-                                                                 dq, plan.ws, stream),
-            "compose_suffix": lambda: C.rm_cp_compose_suffix(s, plan.M, plan.gamma, plan.dS_out, stream),
-            "backward_apply": lambda: C.rm_cp_backward_apply(s, q, k, v, g, dO, plan.S_in, plan.dS_out,
-                                                             dk, dv, dg, plan.ws, stream),
-        }
-
-    fns = calls(q, k, v, g, dO, o, dq, dk, dv, dg)
-
-    def step(events=None):
-        for i, ph in enumerate(phases):
+    def step(events=None, which=phases):
+        for i, ph in enumerate(which):
             if events is not None:
                 events[i].record(stream)
             fns[ph]()
         if events is not None:
-            events[len(phases)].record(stream)
+            events[len(which)].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -267,7 +269,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
 
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(local_rank_of(dev))
     clocks.start()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
           for _ in range(args.steps)]
@@ -280,24 +282,32 @@ def run_ours(args, rank, world, local_rank):
     end.record(stream)
     torch.cuda.synchronize(dev)
     launches = C.rm_cp_launch_count() - l0
+    # forward-only steps (the three forward calls), timed the same way
+    fstart = torch.cuda.Event(enable_timing=True)
+    fend = torch.cuda.Event(enable_timing=True)
+    fstart.record(stream)
+    for i in range(args.steps):
+        step(None, PHASES_FWD)
+    fend.record(stream)
+    torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    total_ms = replica_time(start.elapsed_time(end), world, dev)
-    ms_per_step = total_ms / args.steps
+    ms_per_step = replica_time(start.elapsed_time(end), world, dev) / args.steps
+    fwd_ms = replica_time(fstart.elapsed_time(fend), world, dev) / args.steps
     tok_per_step = w.B * w.T
     value = replica_throughput(world, tok_per_step, ms_per_step)
+    fwd_value = replica_throughput(world, tok_per_step, fwd_ms)
 
     phase_ms = {ph: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
                 for j, ph in enumerate(phases)}
     dom = max(phase_ms, key=phase_ms.get)
     dom_bytes = kernel_bytes(w, dom)
     achieved = dom_bytes / (phase_ms[dom] / 1e3) / 1e9
-    traffic = load_traffic(w.name, dom)
     roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-            "traffic": traffic, "algorithmic_bytes": dom_bytes, "launch_us": phase_ms[dom] * 1e3,
-            "peak_source": peak_src}
+            "traffic": load_traffic(w.name, dom), "algorithmic_bytes": dom_bytes,
+            "launch_us": phase_ms[dom] * 1e3, "peak_source": peak_src}
     pr = path_roofline(w, peaks)
     path = {"bound": pr["bound"], "t_roofline_us": pr["t_roofline_us"],
             "t_measured_us": ms_per_step * 1e3, "frac": pr["t_roofline_us"] / (ms_per_step * 1e3),
@@ -305,6 +315,9 @@ def run_ours(args, rank, world, local_rank):
             "phases_us": {ph: round(t * 1e3, 2) for ph, t in phase_ms.items()},
             "phase_frac_of_hbm": {ph: round(kernel_bytes(w, ph) / (phase_ms[ph] / 1e3) / 1e9
                                             / peaks["hbm_gbs"], 4) for ph in phases}}
+    fpr = path_roofline(w.replace(backward=False), peaks)
+    fwd_path = {"bound": fpr["bound"], "t_roofline_us": fpr["t_roofline_us"],
+                "t_measured_us": fwd_ms * 1e3, "frac": fpr["t_roofline_us"] / (fwd_ms * 1e3)}
 
     # ---- end to end through rm_cp_step_host: pinned host buffers in, results
     # out, every step.  Two device buffer sets and two copy streams: the
@@ -312,7 +325,7 @@ def run_ours(args, rank, world, local_rank):
     # while step i's kernels do, as a training loop that prefetches its next
     # batch would; every step's copies are inside the timed region.
     e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         names_in = ("q", "k", "v", "g") + (("dO",) if w.backward else ())
         host = {n: getattr(inp, n).pin_memory() for n in names_in}
         outs0 = {"o": o}
@@ -329,7 +342,7 @@ def run_ours(args, rank, world, local_rank):
 
         e2e_run(max(2, min(args.warmup, 3)))
         torch.cuda.synchronize(dev)
-        n_e2e = max(3, args.steps // 2)
+        n_e2e = max(3, min(args.steps // 2, 30))
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -341,30 +354,66 @@ def run_ours(args, rank, world, local_rank):
         e2e = {"value": replica_throughput(world, tok_per_step, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": sum(host[n].numel() * host[n].element_size() for n in names_in),
                "d2h_bytes_per_step": sum(host[n].numel() * host[n].element_size() for n in outs0),
-               "ms_per_step": e_ms, "call": "rm_cp_step_host",
+               "ms_per_step": e_ms, "steps": n_e2e, "call": "rm_cp_step_host",
                "pipeline": "2 device buffer sets; h2d of step i+1 and d2h of step i-1 overlap step i"}
+        del host, pipe
 
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, g) + ((dO,) if dO is not None else ()))
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, inp, args.cpu_seconds)
-
+    cpu = cpu_baseline(w, inp, args.cpu_seconds) if with_cpu else None
     path_kind = C.rm_cp_path(s)
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+    out = {
+        "value": value, "fwd_value": fwd_value, "unit": "tokens/s", "ms_per_step": ms_per_step,
+        "fwd_ms_per_step": fwd_ms, "mode": "fwd+bwd" if w.backward else "fwd",
         "dtype": "bf16" if (w.dtype == "bf16" and path_kind == 1) else "f32",
-        "data": "synthetic (seeded: q,k,v,dO ~ N(0,1), k L2-normalised, g = logsigmoid(N(0,1)+c))",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
                    "num_segments": w.num_segments, "chunk": w.chunk, "storage": w.dtype,
                    "mode": "fwd+bwd" if w.backward else "fwd", "packed": w.packed,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB > 129 MiB), no flush",
+                   "l2": (f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB > 129 MiB), no flush"
+                          if in_bytes > L2_BYTES else
+                          f"inputs ({in_bytes / 2**20:.0f} MiB) fit in L2: no flush, warm-L2 figure"),
                    "kernel_path": "tcgen05" if path_kind == 1 else "simt-fp32"},
-        "roofline": roof, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": int(launches), "clocks": clk,
+        "roofline": roof, "path_roofline": path, "fwd_path_roofline": fwd_path,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
     }
+    del q, k, v, g, dO, o, dq, dk, dv, dg, plan, inp
+    torch.cuda.empty_cache()
+    return out
+
+
+def local_rank_of(dev) -> int:
+    return dev.index if dev.index is not None else 0
+
+
+def run_ours(args, rank, world, local_rank):
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks, peak_src = load_peaks()
+    w = workload_of(args)
+    head = measure_workload(w, args, rank, world, dev, peaks, peak_src,
+                            with_e2e=not args.no_e2e,
+                            with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline)
+    line = {
+        "metric": METRIC, "value": head["value"], "fwd_value": head["fwd_value"], "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"], "fwd_ms_per_step": head["fwd_ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
+        "data": "synthetic (seeded: q,k,v,dO ~ N(0,1), k L2-normalised, g = logsigmoid(N(0,1)+c))",
+    }
+    for key in ("config", "roofline", "path_roofline", "fwd_path_roofline", "cpu_baseline", "e2e",
+                "gpu_launches", "clocks"):
+        line[key] = head[key]
+    if args.workload == HEADLINE and not args.T and not args.headline_only:
+        subs = {}
+        for name in SUB_WORKLOADS:
+            r = measure_workload(WORKLOADS[name], args, rank, world, dev, peaks, peak_src,
+                                 with_e2e=False, with_cpu=False)
+            subs[name] = {key: r[key] for key in ("value", "fwd_value", "unit", "mode", "ms_per_step",
+                                                 "fwd_ms_per_step", "dtype", "config", "roofline",
+                                                 "path_roofline", "fwd_path_roofline",
+                                                 "gpu_launches", "clocks")}
+        line["workloads"] = subs
+        line["gpu_launches"] = head["gpu_launches"]
     return line
 
 
@@ -534,12 +583,19 @@ def run_ssd(args, rank, world, local_rank):
     }
 
 
+def reference_budget(args) -> float:
+    """Seconds of oracle work per reference step: the whole --steps/--warmup
+    run stays near two and a half minutes of CPU time (at least 50 ms, the
+    smallest sample being 64 tokens of every row and head)."""
+    return max(0.05, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+
+
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm, timed per step on host cores."""
     if args.workload in SSD_WORKLOADS:
         w = SSD_WORKLOADS[args.workload]
         inp = make_ssd_inputs(w)
-        budget = max(2.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+        budget = reference_budget(args)
         runs = [ssd_cpu_baseline(w, inp, budget) for _ in range(args.steps)]
         value = statistics.mean(r["value"] for r in runs)
         return {
@@ -555,7 +611,7 @@ def run_reference(args):
         }
     w = workload_of(args)
     inp = make_inputs(w)
-    budget = max(2.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    budget = reference_budget(args)
     ntok = calibrate_oracle(w, inp, budget)
     for _ in range(args.warmup):
         oracle_sample_run(w, inp, ntok)
@@ -595,10 +651,12 @@ def load_traffic(workload, kernel):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="32k", choices=sorted(WORKLOADS) + sorted(SSD_WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + sorted(SSD_WORKLOADS))
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only the chosen workload (no 'workloads' object)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

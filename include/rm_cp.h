@@ -260,12 +260,17 @@ rm_status rm_cp_selftest_wait_timeout(uint32_t limit_us, rm_stream_t stream);
  *   replaces: q, k, v, dO (dtype), g fp32, S_in and M from the forward;
  *   gamma and dS_out [nseg,B,H,Dk,Dv] fp32 are written as by those calls;
  *   dq, dk, dv (dtype), dg fp32 out.
- *   Limit: B * T * H <= 4,194,304 (16 MiB of fp32 scratch, held on every
- *   device that loads the library until the process exits); larger
+ *   Limit: B * T * H <= 4,194,304 (16 MiB of fp32 scratch); larger
  *   problems get RM_ERR_SHAPE and must use the workspace form.
- *   The first call on a device looks the array's device address up (once
- *   per device, with that device current); make that first call before any
- *   stream capture.  Every call shares the one array: calls whose work
+ *   The array is placed on a device when the library's code for this call
+ *   is loaded there.  Under CUDA's default lazy module loading that happens
+ *   in the first call on the device, which looks the array's device address
+ *   up with that device current; the 16 MiB stay on the device until the
+ *   process exits.  A caller whose memory plan is fixed at start-up should
+ *   therefore make one call on each device during start-up, and before any
+ *   stream capture (a module cannot be loaded during capture).  A failed
+ *   lookup returns RM_ERR_CUDA, leaves no CUDA error pending, and is retried
+ *   by the next call.  Every call shares the one array: calls whose work
  *   overlaps on the GPU (other streams, other host threads) race on it and
  *   must be serialised by the caller.  Nothing in the array needs clearing:
  *   each call writes every entry it later reads.

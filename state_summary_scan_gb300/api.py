@@ -7,8 +7,10 @@ apply).  PyTorch only provides device memory and the stream.
 """
 from __future__ import annotations
 
+import collections
 import dataclasses
 import math
+import threading
 from typing import Optional
 
 import torch
@@ -21,7 +23,7 @@ class Plan:
     """Problem description plus every intermediate buffer of one step."""
     spec: C.ProblemSpec
     M: torch.Tensor          # [nseg,B,H] fp32
-    dS: torch.Tensor         # [nseg,B,H,Dk,Dv] fp32 (forward summaries)
+    dS: Optional[torch.Tensor]  # [nseg,B,H,Dk,Dv] fp32 (forward summaries)
     S_in: torch.Tensor       # [nseg,B,H,Dk,Dv] fp32
     gamma: torch.Tensor      # [nseg,B,H,Dk,Dv] fp32 (backward summaries)
     dS_out: torch.Tensor     # [nseg,B,H,Dk,Dv] fp32
@@ -29,30 +31,74 @@ class Plan:
     metadata: Optional[dict] = None   # host metadata of a packed problem
 
 
-def make_plan(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch.bfloat16,
-              cu_seqlens=None, device="cuda", backward=True, q_heads=0) -> Plan:
-    """q_heads > 0: q is [B,T,q_heads,Dk], shared by H / q_heads consecutive heads."""
+_SPEC_CACHE: "collections.OrderedDict" = collections.OrderedDict()
+_SPEC_CACHE_MAX = 64
+_SPEC_LOCK = threading.Lock()
+
+
+def cached_spec(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch.bfloat16,
+                cu_seqlens=None, device="cuda", q_heads=0):
+    """The problem description of a shape, built once: packed metadata is
+    computed on the host and copied to the device on the first call only.
+    Returns (spec, host metadata or None).  The spec holds no per-call
+    buffers, so any number of calls (layers, steps) may share it."""
     if scale is None:
         scale = 1.0 / math.sqrt(Dk)
+    cu_key = None if cu_seqlens is None else tuple(int(x) for x in cu_seqlens)
+    key = (int(B), int(T), int(H), int(Dk), int(Dv), int(num_segments), int(chunk), float(scale),
+           dtype, str(torch.device(device)), cu_key, int(q_heads))
+    with _SPEC_LOCK:
+        hit = _SPEC_CACHE.get(key)
+        if hit is not None:
+            _SPEC_CACHE.move_to_end(key)
+            return hit
     meta = None
     seq_idx = pre = fol = None
     if cu_seqlens is not None:
-        meta = C.rm_cp_build_packed_metadata(cu_seqlens, T, num_segments)
+        meta = C.rm_cp_build_packed_metadata(cu_key, T, num_segments)
         seq_idx = meta["seq_idx"].to(device)
         pre = meta["preceding_start"].to(device)
         fol = meta["following_stop"].to(device)
     spec = C.ProblemSpec(B, T, H, Dk, Dv, num_segments, chunk, scale, dtype, seq_idx, pre, fol,
                          q_heads=q_heads)
     C.rm_cp_validate(spec)
+    entry = (spec, meta)
+    with _SPEC_LOCK:
+        _SPEC_CACHE[key] = entry
+        while len(_SPEC_CACHE) > _SPEC_CACHE_MAX:
+            _SPEC_CACHE.popitem(last=False)
+    return entry
+
+
+def make_plan(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch.bfloat16,
+              cu_seqlens=None, device="cuda", backward=True, q_heads=0) -> Plan:
+    """q_heads > 0: q is [B,T,q_heads,Dk], shared by H / q_heads consecutive heads."""
+    spec, meta = cached_spec(B, T, H, Dk, Dv, num_segments, chunk, scale, dtype, cu_seqlens,
+                             device, q_heads)
     f32 = dict(dtype=torch.float32, device=device)
     ssz = (num_segments, B, H, Dk, Dv)
     M = torch.empty((num_segments, B, H), **f32)
     dS = torch.empty(ssz, **f32)
     S_in = torch.empty(ssz, **f32)
-    gamma = torch.empty(ssz if backward else (0,), **f32)
-    dS_out = torch.empty(ssz if backward else (0,), **f32)
-    ws = torch.empty(max(C.rm_cp_workspace_size(spec), 16), dtype=torch.uint8, device=device)
-    return Plan(spec, M, dS, S_in, gamma, dS_out, ws, meta)
+    plan = Plan(spec, M, dS, S_in, torch.empty((0,), **f32), torch.empty((0,), **f32),
+                torch.empty(16, dtype=torch.uint8, device=device), meta)
+    if backward:
+        backward_buffers(plan)
+    return plan
+
+
+def backward_buffers(plan: Plan) -> Plan:
+    """Allocates the backward's gamma, dS_out and workspace if the plan lacks them."""
+    s = plan.spec
+    ssz = (s.num_segments, s.B, s.H, s.Dk, s.Dv)
+    dev = plan.M.device
+    if tuple(plan.gamma.shape) != ssz:
+        plan.gamma = torch.empty(ssz, dtype=torch.float32, device=dev)
+        plan.dS_out = torch.empty(ssz, dtype=torch.float32, device=dev)
+    need = max(C.rm_cp_workspace_size(s), 16)
+    if plan.ws.numel() < need:
+        plan.ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    return plan
 
 
 def plan_like(q: torch.Tensor, v: torch.Tensor, num_segments: int, chunk: int = 64,
@@ -86,14 +132,20 @@ def backward(plan: Plan, q, k, v, g, dO, grads=None, stream=None):
 
 
 class ChunkwiseGatedLinearAttention(torch.autograd.Function):
-    """Autograd adapter; the saved context is (q, k, v, g) plus the plan, whose
-    S_in and M carry the forward's composed summaries into backward."""
+    """Autograd adapter.  The problem description (and a packed problem's
+    device metadata) comes from a cache keyed by shape and cu_seqlens, so a
+    training loop builds and uploads it once.  Between forward and backward
+    each call keeps only what the backward reads, M and S_in, beside the saved
+    (q, k, v, g); the forward summaries dS die with the forward, and gamma,
+    dS_out and the workspace are taken from PyTorch's caching allocator in the
+    backward."""
 
     @staticmethod
     def forward(ctx, q, k, v, g, num_segments, chunk, scale, cu_seqlens):
         q, k, v, g = (t.contiguous() for t in (q, k, v, g))
-        plan = plan_like(q, v, num_segments, chunk, scale, cu_seqlens)
+        plan = plan_like(q, v, num_segments, chunk, scale, cu_seqlens, backward=False)
         o = forward(plan, q, k, v, g)
+        plan.dS = None
         ctx.plan = plan
         ctx.save_for_backward(q, k, v, g)
         return o
@@ -101,7 +153,9 @@ class ChunkwiseGatedLinearAttention(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dO):
         q, k, v, g = ctx.saved_tensors
-        dq, dk, dv, dg = backward(ctx.plan, q, k, v, g, dO.contiguous())
+        plan = backward_buffers(ctx.plan)
+        dq, dk, dv, dg = backward(plan, q, k, v, g, dO.contiguous())
+        ctx.plan = None
         return dq, dk, dv, dg, None, None, None, None
 
 
@@ -197,8 +251,10 @@ def ssd_forward(sp: SsdPlan, x, dt, A, Bm, Cm, D=None, y=None, stream=None) -> t
     return y
 
 
-def ssd_backward(sp: SsdPlan, x, dt, A, Bm, Cm, dy, D=None, stream=None):
-    """(dx, ddt, dA, dB, dC, dD) of sum(dy * y); needs ssd_forward on sp first."""
+def ssd_backward(sp: SsdPlan, x, dt, A, Bm, Cm, dy, D=None, stream=None, core=None):
+    """(dx, ddt, dA, dB, dC, dD) of sum(dy * y); needs ssd_forward on sp first.
+    core: an optional dict that receives the gradients of the gated recurrence
+    the scan runs as (dq, dk, dv, dg of q = C, k = dt B, v = x, g = dt A)."""
     B, T, H, _ = x.shape
     grads = (torch.empty_like(sp.k), torch.empty_like(sp.k), torch.empty_like(x),
              torch.empty((B, T, H), dtype=torch.float32, device=x.device))
@@ -208,6 +264,9 @@ def ssd_backward(sp: SsdPlan, x, dt, A, Bm, Cm, dy, D=None, stream=None):
     dD = torch.empty(H, dtype=torch.float32, device=x.device)
     dB = torch.empty(Bm.shape, dtype=Bm.dtype, device=x.device)
     dC = torch.empty_like(dB)
+    if core is not None:
+        # dv becomes dx in place below; keep the recurrence's own copy
+        core.update(dq=dq, dk=dk, dv=dv.clone(), dg=dg)
     C.rm_ssd_finish_backward(sp.core.spec, sp.G, x, dt, A, Bm, dy, D, dq, dk, dv, dg, ddt, dA, dB,
                              dC, dD, sp.ws, stream)
     return dv, ddt, dA, dB, dC, dD

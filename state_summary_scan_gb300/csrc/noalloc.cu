@@ -6,6 +6,7 @@
 // sweeps (q.dq minus its same-token term, read by the gate-gradient scan).
 // The regular entry points take that as the caller's workspace; this one
 // keeps it in kScratchFloats floats of file-scope device memory instead.
+#include <cstdio>
 #include <mutex>
 
 #include "internal.h"
@@ -13,28 +14,44 @@
 namespace {
 
 // 4 Mi floats (16 MiB): enough for B * T * H <= 4,194,304, e.g. one row of
-// 262,144 tokens with 16 heads.  Every device that loads the library holds
-// this array until the process exits.
+// 262,144 tokens with 16 heads.  The array is placed on a device when this
+// file's module is loaded there; under CUDA's default lazy module loading
+// that is the first rm_cp_backward_noalloc call on the device (its address
+// lookup), after which the device holds it until the process exits.
 constexpr size_t kScratchFloats = size_t(1) << 22;
 static __device__ __align__(256) float g_backward_scratch[kScratchFloats];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
+std::mutex g_lock[kMaxDevices];
 float* g_scratch_ptr[kMaxDevices] = {};
-cudaError_t g_scratch_err[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  In host code
 // g_backward_scratch names a host-side shadow, never the device memory, so
-// the address is looked up once per device with that device current.
-rm_status scratch_for_current_device(float** out) {
+// the address is looked up with that device current.  Only a successful
+// lookup is kept: a failed one (e.g. attempted during stream capture, where
+// a module cannot be loaded) clears its error and is retried by the next call.
+rm_status scratch_for_current_device(float** out, cudaError_t* err) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RM_ERR_CUDA;
-    std::call_once(g_once[dev], [dev] {
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) {
+        cudaGetLastError();
+        return RM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return RM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> guard(g_lock[dev]);
+    if (g_scratch_ptr[dev] == nullptr) {
         void* p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_backward_scratch);
+        *err = cudaGetSymbolAddress(&p, g_backward_scratch);
+        if (*err != cudaSuccess || p == nullptr) {
+            cudaGetLastError();  // leave no error pending for later checks
+            if (*err == cudaSuccess) *err = cudaErrorInvalidSymbol;
+            return RM_ERR_CUDA;
+        }
         g_scratch_ptr[dev] = static_cast<float*>(p);
-    });
-    if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return RM_ERR_CUDA;
+    }
     *out = g_scratch_ptr[dev];
     return RM_OK;
 }
@@ -73,8 +90,15 @@ extern "C" rm_status rm_cp_backward_noalloc(const rm_cp_problem* p, const void* 
                               "rm_cp_backward_noalloc: B*T*H exceeds its fixed scratch of "
                               "4194304 entries; use rm_cp_backward_prepare/apply with a workspace");
     float* scratch = nullptr;
-    if (scratch_for_current_device(&scratch) != RM_OK)
-        return rmcp::api_fail(RM_ERR_CUDA, "rm_cp_backward_noalloc: scratch address lookup failed");
+    cudaError_t err = cudaSuccess;
+    if (scratch_for_current_device(&scratch, &err) != RM_OK) {
+        char msg[256];
+        std::snprintf(msg, sizeof(msg),
+                      "rm_cp_backward_noalloc: scratch address lookup failed (%s); the next "
+                      "call retries it",
+                      cudaGetErrorString(err));
+        return rmcp::api_fail(RM_ERR_CUDA, msg);
+    }
 
     // the per-token partials are fully written by the prepare sweep before the
     // apply sweep reads them, so the array needs no clearing between calls

@@ -9,10 +9,11 @@
 // (win = decay from the chunk's incoming state, wout = decay to its last
 // state, W = whole-chunk decay), and the backward mirrors it.  Every product
 // above is a tcgen05.mma with bf16 operands in 128-byte-swizzled shared memory
-// (loaded by TMA) and fp32 accumulators in tensor memory; the fp32 master
-// state lives in registers, one state row per thread (in tensor memory for
-// the Dv = 256 reverse sweep), and is re-quantised to a bf16 shared-memory
-// copy for the next chunk's products.
+// (loaded by TMA) and fp32 accumulators in tensor memory.  The fp32 master
+// state of a sweep lives in tensor memory in the forward sweep and in the
+// Dv = 256 dq and reverse sweeps, and in registers (one state row per pair of
+// threads) in the Dv = 128 dq and reverse sweeps; either way it is
+// re-quantised to a bf16 shared-memory copy for the next chunk's products.
 //
 // Kernels (one CTA per (segment, row, head[, value block])):
 //   tc_outer2_kernel    (Dv = 128, barrier-paced) and tc_outer_kernel (Dv = 256):

@@ -212,3 +212,26 @@ def test_ssd_calls_validate_before_any_launch():
     assert lib.rm_ssd_finish_forward(s.ref, ok, None, ok, None) == 0
     assert lib.rm_ssd_workspace_size(s.ref) == 4 * (256 * 4 + 2 * 1024 * 4)
     assert lib.rm_ssd_workspace_size(spec(T=250).ref) == 0
+
+
+def test_problem_spec_cache_builds_metadata_once_and_shares_no_buffers():
+    """The autograd adapter's problem description is built once per shape and
+    packing (metadata computed and copied once); every plan still gets its own
+    summary buffers, so layers of one shape never share an S_in."""
+    from state_summary_scan_gb300 import api
+    cu = [0, 100, 101, 256]
+    a = api.cached_spec(1, 256, 2, 32, 32, 4, 16, None, torch.float32, cu, "cpu")
+    b = api.cached_spec(1, 256, 2, 32, 32, 4, 16, None, torch.float32, tuple(cu), "cpu")
+    assert a is b
+    assert torch.equal(a[1]["seq_idx"], torch.as_tensor(oracle.packed_metadata(
+        cu, 256, oracle.equal_segments(256, 4))["seq_idx"]))
+    c = api.cached_spec(1, 256, 2, 32, 32, 4, 16, None, torch.float32, [0, 99, 256], "cpu")
+    assert c is not a
+    p1 = api.make_plan(1, 256, 2, 32, 32, 4, 16, None, torch.float32, cu, "cpu", backward=False)
+    p2 = api.make_plan(1, 256, 2, 32, 32, 4, 16, None, torch.float32, cu, "cpu", backward=False)
+    assert p1.spec is p2.spec
+    assert p1.S_in.data_ptr() != p2.S_in.data_ptr() and p1.M.data_ptr() != p2.M.data_ptr()
+    assert p1.gamma.numel() == 0
+    api.backward_buffers(p1)
+    assert tuple(p1.gamma.shape) == (4, 1, 2, 32, 32) and tuple(p1.dS_out.shape) == (4, 1, 2, 32, 32)
+    assert p1.ws.numel() >= C.rm_cp_workspace_size(p1.spec)

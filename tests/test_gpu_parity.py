@@ -282,8 +282,19 @@ def test_step_host_pipeline_matches_device_path(backward):
 def test_shared_queries(dtype, Dk, Dv, chunk):
     """q_heads = 2 of H = 4: heads 0, 1 read query row 0 and heads 2, 3 row 1;
     the oracle sees the same queries repeated per head.  dq stays per head."""
+    shared_queries_case(dtype, Dk, Dv, chunk, 1, 512, 4, 2, 4)
+
+
+@pytest.mark.parametrize("qh,Dv", [(1, 128), (2, 128), (2, 256)])
+def test_shared_queries_wide_grid(qh, Dv):
+    """16 segments x 16 heads = 256 (segment, head) sweeps (512 forward CTAs at
+    Dv = 256), more than the SMs: the forward sweep that runs two CTAs a SM
+    reads query row h / (H / q_heads), as a Mamba2 group's heads read C."""
+    shared_queries_case(torch.bfloat16, 128, Dv, 64, 1, 2048, 16, qh, 16)
+
+
+def shared_queries_case(dtype, Dk, Dv, chunk, B, T, H, qh, nseg):
     from state_summary_scan_gb300 import api
-    B, T, H, qh, nseg = 1, 512, 4, 2, 4
     gen = torch.Generator().manual_seed(21)
     q = torch.randn(B, T, qh, Dk, generator=gen)
     k = torch.randn(B, T, H, Dk, generator=gen)
