@@ -84,6 +84,21 @@ def test_noalloc_matches_workspace_backward_twice(dtype, Dk, Dv):
         assert_same(got, ref_out)
 
 
+def test_noalloc_matches_workspace_on_a_grid_wider_than_the_gpu():
+    """16 segments x 16 heads = 256 (segment, head) sweeps, more than the SMs,
+    so the sweeps run in more than one wave, with sequences starting inside
+    and across segments: the no-alloc form still equals the workspace form
+    bit for bit."""
+    q, k, v, g, dO = inputs(1, 4096, 16, 128, 128, torch.bfloat16, 31)
+    cu = [0, 1000, 1001, 2300, 4096]
+    plan = api.plan_like(q, v, 16, 64, 1.0 / math.sqrt(128), cu_seqlens=cu)
+    api.forward(plan, q, k, v, g)
+    ref_out = workspace_backward(plan, q, k, v, g, dO)
+    got = noalloc_backward(plan, q, k, v, g, dO)
+    torch.cuda.synchronize()
+    assert_same(got, ref_out)
+
+
 def test_noalloc_repeated_calls_agree():
     q, k, v, g, dO = inputs(2, 512, 2, 128, 128, torch.bfloat16, 21)
     plan = api.plan_like(q, v, 2, 64, 1.0 / math.sqrt(128))
