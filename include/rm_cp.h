@@ -21,8 +21,9 @@
  * Conventions for every call:
  *   - Layouts are contiguous row-major: q, k, dq, dk [B,T,H,Dk]; v, o, dO, dv
  *     [B,T,H,Dv]; g, dg [B,T,H] (fp32); summaries [nseg,B,H,Dk,Dv] (fp32);
- *     M [nseg,B,H] (fp32).  Segment j covers tokens [j*L, (j+1)*L) of every
- *     row, L = T / num_segments.
+ *     M [nseg,B,H] (fp32).  With vector gates (rm_cp_problem.vector_gates)
+ *     g, dg are [B,T,H,Dk] and M is [nseg,B,H,Dk].  Segment j covers tokens
+ *     [j*L, (j+1)*L) of every row, L = T / num_segments.
  *   - q, k, v, o, dO, dq, dk, dv have the problem's dtype (RM_F32 or RM_BF16;
  *     bf16 results are rounded to nearest even from fp32).  g, dg, M and all
  *     summaries are always fp32.
@@ -90,6 +91,17 @@ typedef enum { RM_F32 = 0, RM_BF16 = 1 } rm_dtype;
  *                    q row h / (H / q_heads), i.e. consecutive heads share
  *                    their queries (as the heads of a Mamba2 group share C).
  *                    dq stays [B,T,H,Dk]: one gradient per head.
+ *   vector_gates     0: one gate per (token, head) as above.  1: one gate per
+ *                    (token, head, key dimension): g, dg are [B,T,H,Dk]
+ *                    fp32 and S_t = diag(alpha_t) S_{t-1} + k_t v_t^T with
+ *                    alpha_t[i] = exp(g_t[i]) (all 0 at a sequence start).
+ *                    The segment transition is then the diagonal matrix
+ *                    M = diag(prod of alpha) -- the general M of the page's
+ *                    CPForwardUnpackedSummary (S_out = M S_in + delta_S),
+ *                    M^T = M -- stored as its diagonal, M [nseg,B,H,Dk]; the
+ *                    compositions apply it row by row, and the workspace
+ *                    holds one fp32 value per (row, token, head, key
+ *                    dimension).  Runs on the generic fp32-arithmetic kernels.
  * Out-of-range metadata values are clamped on the device to [0, j] and
  * [j+1, num_segments]; rm_cp_build_packed_metadata produces valid ones.
  */
@@ -103,6 +115,7 @@ typedef struct {
     const int32_t* preceding_start;
     const int32_t* following_stop;
     int32_t q_heads;
+    int32_t vector_gates;
 } rm_cp_problem;
 
 /*

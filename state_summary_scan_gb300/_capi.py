@@ -48,6 +48,7 @@ class Problem(ctypes.Structure):
         ("scale", ctypes.c_float), ("dtype", ctypes.c_int),
         ("seq_idx", ctypes.c_void_p), ("preceding_start", ctypes.c_void_p),
         ("following_stop", ctypes.c_void_p), ("q_heads", ctypes.c_int32),
+        ("vector_gates", ctypes.c_int32),
     ]
 
 
@@ -149,7 +150,8 @@ class ProblemSpec:
     def __init__(self, B, T, H, Dk, Dv, num_segments, chunk, scale, dtype,
                  seq_idx: Optional[torch.Tensor] = None,
                  preceding_start: Optional[torch.Tensor] = None,
-                 following_stop: Optional[torch.Tensor] = None, q_heads: int = 0):
+                 following_stop: Optional[torch.Tensor] = None, q_heads: int = 0,
+                 vector_gates: int = 0):
         if isinstance(dtype, torch.dtype):
             dtype = RM_F32 if dtype == torch.float32 else RM_BF16 if dtype == torch.bfloat16 else -1
         self._keep = (seq_idx, preceding_start, following_stop)
@@ -161,7 +163,7 @@ class ProblemSpec:
                          None if seq_idx is None else seq_idx.data_ptr(),
                          None if preceding_start is None else preceding_start.data_ptr(),
                          None if following_stop is None else following_stop.data_ptr(),
-                         int(q_heads))
+                         int(q_heads), int(vector_gates))
 
     @property
     def ref(self):

@@ -37,7 +37,7 @@ _SPEC_LOCK = threading.Lock()
 
 
 def cached_spec(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch.bfloat16,
-                cu_seqlens=None, device="cuda", q_heads=0):
+                cu_seqlens=None, device="cuda", q_heads=0, vector_gates=False):
     """The problem description of a shape, built once: packed metadata is
     computed on the host and copied to the device on the first call only.
     Returns (spec, host metadata or None).  The spec holds no per-call
@@ -46,7 +46,7 @@ def cached_spec(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch
         scale = 1.0 / math.sqrt(Dk)
     cu_key = None if cu_seqlens is None else tuple(int(x) for x in cu_seqlens)
     key = (int(B), int(T), int(H), int(Dk), int(Dv), int(num_segments), int(chunk), float(scale),
-           dtype, str(torch.device(device)), cu_key, int(q_heads))
+           dtype, str(torch.device(device)), cu_key, int(q_heads), bool(vector_gates))
     with _SPEC_LOCK:
         hit = _SPEC_CACHE.get(key)
         if hit is not None:
@@ -60,7 +60,7 @@ def cached_spec(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch
         pre = meta["preceding_start"].to(device)
         fol = meta["following_stop"].to(device)
     spec = C.ProblemSpec(B, T, H, Dk, Dv, num_segments, chunk, scale, dtype, seq_idx, pre, fol,
-                         q_heads=q_heads)
+                         q_heads=q_heads, vector_gates=int(bool(vector_gates)))
     C.rm_cp_validate(spec)
     entry = (spec, meta)
     with _SPEC_LOCK:
@@ -71,13 +71,14 @@ def cached_spec(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch
 
 
 def make_plan(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch.bfloat16,
-              cu_seqlens=None, device="cuda", backward=True, q_heads=0) -> Plan:
-    """q_heads > 0: q is [B,T,q_heads,Dk], shared by H / q_heads consecutive heads."""
+              cu_seqlens=None, device="cuda", backward=True, q_heads=0, vector_gates=False) -> Plan:
+    """q_heads > 0: q is [B,T,q_heads,Dk], shared by H / q_heads consecutive heads.
+    vector_gates: one gate per key dimension (g [B,T,H,Dk], M [nseg,B,H,Dk])."""
     spec, meta = cached_spec(B, T, H, Dk, Dv, num_segments, chunk, scale, dtype, cu_seqlens,
-                             device, q_heads)
+                             device, q_heads, vector_gates)
     f32 = dict(dtype=torch.float32, device=device)
     ssz = (num_segments, B, H, Dk, Dv)
-    M = torch.empty((num_segments, B, H), **f32)
+    M = torch.empty((num_segments, B, H) + ((Dk,) if vector_gates else ()), **f32)
     dS = torch.empty(ssz, **f32)
     S_in = torch.empty(ssz, **f32)
     plan = Plan(spec, M, dS, S_in, torch.empty((0,), **f32), torch.empty((0,), **f32),
@@ -102,10 +103,10 @@ def backward_buffers(plan: Plan) -> Plan:
 
 
 def plan_like(q: torch.Tensor, v: torch.Tensor, num_segments: int, chunk: int = 64,
-              scale=None, cu_seqlens=None, backward=True) -> Plan:
+              scale=None, cu_seqlens=None, backward=True, vector_gates=False) -> Plan:
     B, T, H, Dk = q.shape
     return make_plan(B, T, H, Dk, v.shape[-1], num_segments, chunk, scale, q.dtype, cu_seqlens,
-                     q.device, backward)
+                     q.device, backward, vector_gates=vector_gates)
 
 
 def forward(plan: Plan, q, k, v, g, o=None, stream=None) -> torch.Tensor:
@@ -143,7 +144,8 @@ class ChunkwiseGatedLinearAttention(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, g, num_segments, chunk, scale, cu_seqlens):
         q, k, v, g = (t.contiguous() for t in (q, k, v, g))
-        plan = plan_like(q, v, num_segments, chunk, scale, cu_seqlens, backward=False)
+        plan = plan_like(q, v, num_segments, chunk, scale, cu_seqlens, backward=False,
+                         vector_gates=g.dim() == 4)
         o = forward(plan, q, k, v, g)
         plan.dS = None
         ctx.plan = plan
@@ -162,7 +164,8 @@ class ChunkwiseGatedLinearAttention(torch.autograd.Function):
 def chunkwise_gla(q, k, v, g, num_segments: int, chunk: int = 64, scale=None, cu_seqlens=None):
     """Differentiable chunkwise gated linear attention.
 
-    q, k [B,T,H,Dk], v [B,T,H,Dv] (fp32 or bf16, CUDA), g [B,T,H] fp32 log-gates.
+    q, k [B,T,H,Dk], v [B,T,H,Dv] (fp32 or bf16, CUDA), g [B,T,H] fp32 log-gates
+    (or [B,T,H,Dk]: one gate per key dimension).
     cu_seqlens (host int32 [N+1]) packs several sequences along T."""
     return ChunkwiseGatedLinearAttention.apply(q, k, v, g, num_segments, chunk, scale, cu_seqlens)
 

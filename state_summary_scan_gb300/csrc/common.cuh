@@ -21,6 +21,7 @@ struct Dims {
     const int32_t* following_stop;   // device [nseg] or nullptr
     int qh;     // query heads (rows of q per token)
     int qdiv;   // H / qh: head h reads query row h / qdiv
+    int vg;     // 1: one gate per key dimension (g [B,T,H,Dk], M [nseg,B,H,Dk])
 };
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

@@ -96,7 +96,8 @@ extern "C" rm_status rm_cp_step_host(const rm_cp_problem* p, const rm_cp_host_io
 
     const size_t e = p->dtype == RM_BF16 ? 2 : 4;
     const size_t ntok = size_t(d.B) * size_t(d.T) * size_t(d.H);
-    const size_t bk = ntok * size_t(d.Dk) * e, bv = ntok * size_t(d.Dv) * e, bg = ntok * 4;
+    const size_t bk = ntok * size_t(d.Dk) * e, bv = ntok * size_t(d.Dv) * e;
+    const size_t bg = ntok * 4 * (d.vg ? size_t(d.Dk) : 1);  // g, dg: one per key dim with vector gates
     const size_t bq = size_t(d.B) * size_t(d.T) * size_t(d.qh) * size_t(d.Dk) * e;
     const Copy ins[5] = {{set->q, host->q, bq}, {set->k, host->k, bk}, {set->v, host->v, bv},
                          {set->g, host->g, bg}, {set->dO, host->dO, bv}};

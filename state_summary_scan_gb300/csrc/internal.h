@@ -33,6 +33,9 @@ void note_launch(int n);
 bool generic_supports(const Dims& d);
 rm_status launch_generic(Op op, const Dims& d, rm_dtype dt, const Ptrs& p, cudaStream_t s);
 
+// vector (per key dimension) gates on the generic path (vg_kernels.cu)
+rm_status launch_vg(Op op, const Dims& d, rm_dtype dt, const Ptrs& p, cudaStream_t s);
+
 // host-side checks and launches of rm_cp_host.cu, for other entry points
 rm_status api_check_problem(const rm_cp_problem* p, Dims* d);
 rm_status api_need(const void* ptr, const char* name);

@@ -85,10 +85,12 @@ extern "C" rm_status rm_cp_backward_noalloc(const rm_cp_problem* p, const void* 
     RM_NEED_NA(dk);
     RM_NEED_NA(dv);
     RM_NEED_NA(dg);
-    if (size_t(d.B) * size_t(d.T) * size_t(d.H) > kScratchFloats)
+    // one scratch value per (row, token, head), or per key dimension with vector gates
+    if (size_t(d.B) * size_t(d.T) * size_t(d.H) * (d.vg ? size_t(d.Dk) : 1) > kScratchFloats)
         return rmcp::api_fail(RM_ERR_SHAPE,
-                              "rm_cp_backward_noalloc: B*T*H exceeds its fixed scratch of "
-                              "4194304 entries; use rm_cp_backward_prepare/apply with a workspace");
+                              "rm_cp_backward_noalloc: B*T*H (times Dk with vector gates) exceeds "
+                              "its fixed scratch of 4194304 entries; use "
+                              "rm_cp_backward_prepare/apply with a workspace");
     float* scratch = nullptr;
     cudaError_t err = cudaSuccess;
     if (scratch_for_current_device(&scratch, &err) != RM_OK) {

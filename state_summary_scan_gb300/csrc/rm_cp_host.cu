@@ -71,6 +71,14 @@ rm_status check_problem(const rm_cp_problem* p, rmcp::Dims* d) {
         return fail(RM_ERR_INVALID_ARG, "q_heads=%d does not divide H=%d", p->q_heads, p->H);
     d->qh = p->q_heads > 0 ? p->q_heads : p->H;
     d->qdiv = p->H / d->qh;
+    if (p->vector_gates != 0 && p->vector_gates != 1)
+        return fail(RM_ERR_INVALID_ARG, "vector_gates=%d is neither 0 nor 1", p->vector_gates);
+    d->vg = p->vector_gates;
+    if (d->vg && !rmcp::generic_supports(*d))
+        return fail(RM_ERR_UNSUPPORTED,
+                    "vector gates: unsupported head dims Dk=%d Dv=%d (need Dk in {16,32,64,128}, Dv "
+                    "a multiple of 8 in [8,256], segment length a multiple of 16)",
+                    p->Dk, p->Dv);
     if (!rmcp::tc_supports(*d, p->dtype) && !rmcp::generic_supports(*d))
         return fail(RM_ERR_UNSUPPORTED,
                     "unsupported head dims Dk=%d Dv=%d (need Dk in {16,32,64,128}, Dv a multiple "
@@ -92,14 +100,16 @@ rm_status need(const void* ptr, const char* name) {
     } while (0)
 
 size_t workspace_bytes(const rmcp::Dims& d) {
-    const size_t per_tok = size_t(d.B) * d.T * d.H * sizeof(float);
+    // one fp32 per (row, token, head), or per key dimension with vector gates
+    const size_t per_tok = size_t(d.B) * d.T * d.H * sizeof(float) * (d.vg ? d.Dk : 1);
     return (per_tok + 255) / 256 * 256;
 }
 
 rm_status launch(rmcp::Op op, const rm_cp_problem* p, const rmcp::Dims& d, const rmcp::Ptrs& ptrs,
                  rm_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    rm_status st = rmcp::tc_supports_op(op, d, p->dtype)
+    rm_status st = d.vg ? rmcp::launch_vg(op, d, p->dtype, ptrs, s)
+                   : rmcp::tc_supports_op(op, d, p->dtype)
                        ? rmcp::launch_tc(op, d, ptrs, s)
                        : rmcp::launch_generic(op, d, p->dtype, ptrs, s);
     if (st == RM_ERR_CUDA) {

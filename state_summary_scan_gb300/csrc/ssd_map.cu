@@ -283,6 +283,7 @@ rm_status check_ssd(const rm_cp_problem* p, int G, Dims* d) {
     rm_status s = api_check_problem(p, d);
     if (s != RM_OK) return s;
     if (p->scale != 1.0f) return api_fail(RM_ERR_INVALID_ARG, "the SSD scan needs scale = 1");
+    if (d->vg) return api_fail(RM_ERR_INVALID_ARG, "the SSD scan has one gate per head (vector_gates = 0)");
     if (G < 1 || d->H % G != 0) return api_fail(RM_ERR_INVALID_ARG, "G must divide H");
     if (d->H > kThreads) return api_fail(RM_ERR_UNSUPPORTED, "the SSD reductions take H <= 256");
     // rows of N and P values split into 16-byte vectors over 1..32 lanes of a warp

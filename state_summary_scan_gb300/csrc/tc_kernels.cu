@@ -2672,7 +2672,7 @@ rm_status tc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cuda
 }
 
 bool tc_supports(const Dims& d, rm_dtype dt) {
-    return dt == RM_BF16 && d.Dk == 128 && (d.Dv == 128 || d.Dv == 256) && d.L % tc::kChunk == 0 &&
+    return !d.vg && dt == RM_BF16 && d.Dk == 128 && (d.Dv == 128 || d.Dv == 256) && d.L % tc::kChunk == 0 &&
            d.T >= tc::kChunk;
 }
 

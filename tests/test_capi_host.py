@@ -235,3 +235,26 @@ def test_problem_spec_cache_builds_metadata_once_and_shares_no_buffers():
     api.backward_buffers(p1)
     assert tuple(p1.gamma.shape) == (4, 1, 2, 32, 32) and tuple(p1.dS_out.shape) == (4, 1, 2, 32, 32)
     assert p1.ws.numel() >= C.rm_cp_workspace_size(p1.spec)
+
+
+def test_vector_gates_validation_and_sizes():
+    """vector_gates is 0 or 1; vector gates run on the generic kernels (path 0
+    even for shapes the tensor-core path serves), the workspace holds one value
+    per key dimension, and the SSD calls (one gate per head) refuse them."""
+    w = WORKLOADS["32k"]
+    base = dict(B=w.B, T=w.T, H=w.H, Dk=w.Dk, Dv=w.Dv, num_segments=w.num_segments,
+                chunk=w.chunk, scale=w.scale, dtype=1)
+    assert C.rm_cp_path(C.ProblemSpec(**base)) == 1
+    vg = C.ProblemSpec(**base, vector_gates=1)
+    assert C.rm_cp_path(vg) == 0
+    ntok = w.B * w.T * w.H
+    assert C.rm_cp_workspace_size(vg) >= ntok * w.Dk * 4
+    assert C.rm_cp_workspace_size(vg) < ntok * w.Dk * 4 + 256
+    with pytest.raises(C.RmCpError) as e:
+        C.rm_cp_validate(C.ProblemSpec(**base, vector_gates=2))
+    assert e.value.status == 1
+    ssd = C.ProblemSpec(1, 256, 4, 32, 16, 4, 16, 1.0, torch.float32, vector_gates=1)
+    ok = ctypes.c_void_p(0x1000)
+    lib = C.load()
+    assert lib.rm_ssd_finish_forward(ssd.ref, ok, ok, ok, None) == 1
+    assert b"vector_gates" in lib.rm_cp_last_error()

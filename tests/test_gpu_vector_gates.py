@@ -1,0 +1,120 @@
+"""GPU parity of vector (per key dimension) gates against the fp64 oracle.
+
+With g [B,T,H,Dk] the recurrence is S_t = diag(exp(g_t)) S_{t-1} + k_t v_t^T
+and each segment's transition is the diagonal M of the Megatron-Core page's
+general summary S_out = M S_in + delta_S.  The six calls run with
+rm_cp_problem.vector_gates = 1 (generic fp32-arithmetic kernels); outputs,
+gradients and the forward summaries (M, delta_S, S_in) are compared element
+by element with oracle.vg_forward / vg_backward / vg_forward_prepare /
+vg_compose_prefix: max|gpu - ref| <= tol * max|ref| per tensor, tol = 1e-4
+for fp32 storage and 2e-2 for bf16."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_summary_scan_gb300 import _capi as C
+from state_summary_scan_gb300 import api
+
+from _parity import compare, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    C.load()
+
+
+def vg_inputs(B, T, H, Dk, Dv, dtype, seed=0, shift=3.0, gate=None, qh=0):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, T, qh or H, Dk, generator=gen)
+    k = torch.randn(B, T, H, Dk, generator=gen)
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn(B, T, H, Dv, generator=gen)
+    g = torch.nn.functional.logsigmoid(torch.randn(B, T, H, Dk, generator=gen) + shift)
+    if gate is not None:
+        g = torch.full((B, T, H, Dk), float(gate))
+    dO = torch.randn(B, T, H, Dv, generator=gen)
+    return q.to(dtype), k.to(dtype), v.to(dtype), g.contiguous(), dO.to(dtype)
+
+
+def run_case(B, T, H, Dk, Dv, dtype, nseg, chunk=16, cu=None, qh=0, direct_dg=False, **kw):
+    q, k, v, g, dO = vg_inputs(B, T, H, Dk, Dv, dtype, qh=qh, **kw)
+    scale = 1.0 / math.sqrt(Dk)
+    dev = "cuda"
+    qd, kd, vd, gd, dOd = (t.to(dev).contiguous() for t in (q, k, v, g, dO))
+    plan = api.make_plan(B, T, H, Dk, Dv, nseg, chunk, scale, dtype, cu, dev, q_heads=qh,
+                         vector_gates=True)
+    o = api.forward(plan, qd, kd, vd, gd)
+    grads = (torch.empty_like(kd), torch.empty_like(kd), torch.empty_like(vd), torch.empty_like(gd))
+    dq, dk, dv, dg = api.backward(plan, qd, kd, vd, gd, dOd, grads=grads)
+    torch.cuda.synchronize()
+    gpu = {n: t.detach().to("cpu", torch.float64).numpy() for n, t in
+           dict(o=o, dq=dq, dk=dk, dv=dv, dg=dg, M=plan.M, dS=plan.dS, S_in=plan.S_in).items()}
+    si = None
+    seg = oracle.equal_segments(T, nseg)
+    if cu is not None:
+        si = oracle.packed_metadata(cu, T, seg)["seq_idx"]
+    qf = q.repeat_interleave(H // qh, dim=2) if qh else q
+    ref = dict(o=oracle.vg_forward(qf, k, v, g, scale, si))
+    ref.update(zip(("dq", "dk", "dv", "dg"), oracle.vg_backward(qf, k, v, g, dO, scale, si,
+                                                               direct=direct_dg)))
+    ref["M"], ref["dS"] = oracle.vg_forward_prepare(k, v, g, seg, si)
+    if cu is None:  # with resets the prefixes start at preceding_start (M = 0 makes them agree)
+        ref["S_in"] = oracle.vg_compose_prefix(ref["M"], ref["dS"])
+    keys = ("o", "dq", "dk", "dv", "dg", "M", "dS") + (("S_in",) if cu is None else ())
+    return compare(gpu, ref, tol_for(dtype), keys)
+
+
+DTYPES = [torch.float32, torch.bfloat16]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_vector_gates_small(dtype):
+    run_case(1, 256, 2, 32, 32, dtype, nseg=4)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_vector_gates_wide_heads(dtype):
+    # Dk = 128 and Dv = 256: two column blocks of the column-owner sweeps
+    run_case(1, 512, 2, 128, 256, dtype, nseg=4, seed=1)
+
+
+def test_vector_gates_narrow_values():
+    # Dv = 16 < Dk = 64: fewer column owners than key dimensions
+    run_case(2, 256, 3, 64, 16, torch.float32, nseg=8, seed=2)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_vector_gates_packed_resets(dtype):
+    cu = [0, 1, 2, 17, 31, 64, 65, 200, 255, 256]
+    run_case(1, 256, 2, 32, 32, dtype, nseg=4, cu=cu, seed=3)
+
+
+def test_vector_gates_strong_decay():
+    """alpha = e^-30 in every dimension: dg (~1e-13) is compared with the
+    oracle's direct form alpha_t[i] <S_{t-1}[i,:], D_t[i,:]>."""
+    run_case(1, 128, 2, 16, 16, torch.float32, nseg=4, gate=-30.0, direct_dg=True)
+
+
+def test_vector_gates_shared_queries():
+    run_case(1, 256, 4, 32, 32, torch.float32, nseg=4, qh=2, seed=4)
+
+
+def test_vector_gates_autograd():
+    """chunkwise_gla takes a [B,T,H,Dk] gate as vector gates."""
+    q, k, v, g, dO = vg_inputs(1, 128, 2, 32, 16, torch.float32, seed=5)
+    qd, kd, vd, gd = (t.cuda().requires_grad_() for t in (q, k, v, g))
+    o = api.chunkwise_gla(qd, kd, vd, gd, 4, 16, 0.2)
+    o.backward(dO.cuda())
+    torch.cuda.synchronize()
+    ref_o = oracle.vg_forward(q, k, v, g, 0.2)
+    ref = oracle.vg_backward(q, k, v, g, dO, 0.2)
+    for a, b in zip((o, qd.grad, kd.grad, vd.grad, gd.grad), (ref_o,) + tuple(ref)):
+        a = a.detach().double().cpu().numpy()
+        assert np.max(np.abs(a - b)) <= 1e-4 * np.max(np.abs(b))
