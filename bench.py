@@ -59,25 +59,44 @@ def load_peaks():
 
 def kernel_bytes(w, phase):
     """Algorithmic bytes of one launch: each input read once, each output
-    written once (tokens: [B,T,H] rows; summaries: [nseg,B,H] states)."""
+    written once (tokens: [B,T,H] rows; summaries: [nseg,B,H] states).  With
+    vector gates the gate, its gradient, M and the per-token workspace value
+    carry one fp32 per key dimension (f bytes)."""
     e = 4 if w.dtype == "f32" else 2
     ntok = w.B * w.T * w.H
     nsum = w.num_segments * w.B * w.H
     st = 4 * w.Dk * w.Dv
     Dk, Dv = w.Dk, w.Dv
+    f = 4 * (Dk if getattr(w, "vector_gates", False) else 1)
     if phase == "forward_prepare":
-        return ntok * (e * (Dk + Dv) + 4) + nsum * (st + 4)
+        return ntok * (e * (Dk + Dv) + f) + nsum * (st + f)
     if phase == "compose_prefix":
-        return nsum * (2 * st + 4)
+        return nsum * (2 * st + f)
     if phase == "forward_apply":
-        return ntok * (e * (2 * Dk + Dv) + 4 + e * Dv) + nsum * st
+        return ntok * (e * (2 * Dk + Dv) + f + e * Dv) + nsum * st
     if phase == "backward_prepare":
-        return ntok * (e * (2 * Dk + 2 * Dv) + 4 + e * Dk + 4) + nsum * 2 * st
+        return ntok * (e * (2 * Dk + 2 * Dv) + f + e * Dk + f) + nsum * 2 * st
     if phase == "compose_suffix":
-        return nsum * (2 * st + 4)
+        return nsum * (2 * st + f)
     if phase == "backward_apply":
-        return ntok * (e * (2 * Dk + 2 * Dv) + 4 + 4 + e * (Dk + Dv) + 4) + nsum * 2 * st
+        return ntok * (e * (2 * Dk + 2 * Dv) + f + f + e * (Dk + Dv) + f) + nsum * 2 * st
     raise KeyError(phase)
+
+
+# fp32 FMA throughput of the CUDA cores: 152 SMs x 128 FP32 lanes x 2 flops x
+# 2070 MHz (the generic kernels walk tokens one by one in fp32 and are bound by it)
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def kernel_alu_flops(w, phase):
+    """fp32 flops one launch of the generic token-walking kernels performs
+    (multiply-add = 2): the state update k v^T and the readouts, per token and
+    head, as the kernels run them."""
+    ntok = w.B * w.T * w.H
+    kd = w.Dk * w.Dv
+    per = {"forward_prepare": 2 * kd, "forward_apply": 4 * kd, "backward_prepare": 6 * kd,
+           "backward_apply": 6 * kd, "compose_prefix": 0, "compose_suffix": 0}[phase]
+    return ntok * per
 
 
 def path_roofline(w, peaks):
@@ -87,11 +106,12 @@ def path_roofline(w, peaks):
     C, Dk, Dv = w.chunk, w.Dk, w.Dv
     ntok = w.B * w.T * w.H
     nsum = w.num_segments * w.B * w.H
+    f = 4 * (Dk if getattr(w, "vector_gates", False) else 1)  # gate (and dg) bytes per token-head
     flops = ntok * (C * (Dk + Dv) + 4 * Dk * Dv)
-    byts = ntok * (e * (2 * Dk + Dv) + 4 + e * Dv) + nsum * (16 * Dk * Dv + 8)
+    byts = ntok * (e * (2 * Dk + Dv) + f + e * Dv) + nsum * (16 * Dk * Dv + 2 * f)
     if w.backward:
         flops += ntok * (C * (3 * Dk + 2 * Dv) + 8 * Dk * Dv)
-        byts += ntok * (2 * e * (2 * Dk + Dv) + e * Dv + 8) + nsum * (16 * Dk * Dv + 8)
+        byts += ntok * (2 * e * (2 * Dk + Dv) + e * Dv + 2 * f) + nsum * (16 * Dk * Dv + 2 * f)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
     return dict(flops=flops, bytes=byts, t_tc_us=t_tc * 1e6, t_hbm_us=t_hbm * 1e6,
@@ -161,10 +181,12 @@ def oracle_sample_run(w, inp, ntok, threads=0):
         si = md["seq_idx"][:ntok]
     args = [oracle._f64(x) for x in (q, k, v, g)]
     dO = oracle._f64(inp.dO[:, sl]) if w.backward else None
+    fwd, bwd = ((oracle.vg_forward, oracle.vg_backward) if getattr(w, "vector_gates", False)
+                else (oracle.forward, oracle.backward))
     t0 = time.perf_counter()
-    oracle.forward(*args, w.scale, si)
+    fwd(*args, w.scale, si)
     if w.backward:
-        oracle.backward(*args, dO, w.scale, si)
+        bwd(*args, dO, w.scale, si)
     return time.perf_counter() - t0, cores
 
 
@@ -222,7 +244,7 @@ def replica_throughput(world: int, tokens_per_step: int, ms_per_step: float) -> 
 # other configurations of the metric are measured in the same run and
 # reported under "workloads".
 HEADLINE = "256k"
-SUB_WORKLOADS = ("32k", "packed64k", "fwd4k")
+SUB_WORKLOADS = ("32k", "packed64k", "fwd4k", "vg32k")
 
 
 def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_cpu):
@@ -236,7 +258,7 @@ def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_
     q, k, v, g = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.g))
     dO = inp.dO.to(dev) if w.backward else None
     plan = api.make_plan(w.B, w.T, w.H, w.Dk, w.Dv, w.num_segments, w.chunk, w.scale,
-                         q.dtype, inp.cu_seqlens, dev, w.backward)
+                         q.dtype, inp.cu_seqlens, dev, w.backward, vector_gates=w.vector_gates)
     o = torch.empty_like(v)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dg = torch.empty_like(g)
@@ -308,6 +330,15 @@ def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_
             "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
             "traffic": load_traffic(w.name, dom), "algorithmic_bytes": dom_bytes,
             "launch_us": phase_ms[dom] * 1e3, "peak_source": peak_src}
+    if w.vector_gates:
+        # the generic kernels walk tokens one by one in fp32: bound by the CUDA cores
+        fl = kernel_alu_flops(w, dom)
+        ach = fl / (phase_ms[dom] / 1e3) / 1e12
+        roof = {"bound": "alu", "kernel": dom, "achieved": ach, "peak": FP32_ALU_TFLOPS,
+                "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS,
+                "traffic": load_traffic(w.name, dom), "alu_flops": fl,
+                "algorithmic_bytes": dom_bytes, "launch_us": phase_ms[dom] * 1e3,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2070 MHz"}
     pr = path_roofline(w, peaks)
     path = {"bound": pr["bound"], "t_roofline_us": pr["t_roofline_us"],
             "t_measured_us": ms_per_step * 1e3, "frac": pr["t_roofline_us"] / (ms_per_step * 1e3),
@@ -372,7 +403,8 @@ def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_
                    "l2": (f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB > 129 MiB), no flush"
                           if in_bytes > L2_BYTES else
                           f"inputs ({in_bytes / 2**20:.0f} MiB) fit in L2: no flush, warm-L2 figure"),
-                   "kernel_path": "tcgen05" if path_kind == 1 else "simt-fp32"},
+                   "kernel_path": "tcgen05" if path_kind == 1 else "simt-fp32",
+                   "gates": "per key dimension" if w.vector_gates else "per head"},
         "roofline": roof, "path_roofline": path, "fwd_path_roofline": fwd_path,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
     }

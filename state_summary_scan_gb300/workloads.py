@@ -11,7 +11,8 @@ Recipe (one torch CPU generator, seed 0, fixed draw order):
   2. q ~ N(0, 1)                                   [B, T, H, Dk]
   3. k ~ N(0, 1), L2-normalised per (token, head)  [B, T, H, Dk]
   4. v ~ N(0, 1)                                   [B, T, H, Dv]
-  5. g = logsigmoid(N(0, 1) + c), fp32             [B, T, H]
+  5. g = logsigmoid(N(0, 1) + c), fp32             [B, T, H] ([B, T, H, Dk] with
+     vector gates: one draw per key dimension)
   6. dO ~ N(0, 1)                                  [B, T, H, Dv]
 All draws are fp32; q, k, v and dO are then rounded to the workload dtype.
 The gate shift c is 3 for the tiny case, 4 for the 4k/32k/packed cases and 5
@@ -41,6 +42,7 @@ class Workload:
     packed: bool = False
     backward: bool = True
     seed: int = 0
+    vector_gates: bool = False  # one gate per key dimension: g [B, T, H, Dk]
 
     @property
     def seg_len(self) -> int:
@@ -69,6 +71,10 @@ WORKLOADS = {
                           num_segments=32, chunk=64, gate_shift=4.0, packed=True),
     "256k": Workload("256k", B=1, T=262144, H=16, Dk=128, Dv=256, dtype="bf16",
                      num_segments=64, chunk=64, gate_shift=5.0),
+    # The pages give no configuration for per-dimension gates; this one is the
+    # 32k configuration with g [B, T, H, Dk] drawn the same way per dimension.
+    "vg32k": Workload("vg32k", B=1, T=32768, H=16, Dk=128, Dv=128, dtype="bf16",
+                      num_segments=16, chunk=64, gate_shift=4.0, vector_gates=True),
 }
 
 
@@ -116,8 +122,9 @@ def make_inputs(w: Workload, with_grad: Optional[bool] = None,
     k = torch.randn(w.B, w.T, w.H, w.Dk, generator=gen, dtype=torch.float32)
     k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
     v = torch.randn(w.B, w.T, w.H, w.Dv, generator=gen, dtype=torch.float32)
+    gshape = (w.B, w.T, w.H) + ((w.Dk,) if w.vector_gates else ())
     g = torch.nn.functional.logsigmoid(
-        torch.randn(w.B, w.T, w.H, generator=gen, dtype=torch.float32) + c)
+        torch.randn(*gshape, generator=gen, dtype=torch.float32) + c)
     dO = None
     if with_grad:
         dO = torch.randn(w.B, w.T, w.H, w.Dv, generator=gen, dtype=torch.float32).to(dt)
