@@ -154,7 +154,8 @@ rm_status rm_cp_validate(const rm_cp_problem* p);
  * also for an invalid problem).  The SAME workspace must be passed, unchanged
  * in between, to rm_cp_backward_prepare and the rm_cp_backward_apply that
  * follows it: the first leaves per-token partial gate gradients there for the
- * second.  The forward calls accept NULL.
+ * second.  rm_cp_forward_fused uses it during its own call only.  The
+ * separate forward calls accept NULL.
  */
 size_t rm_cp_workspace_size(const rm_cp_problem* p);
 
@@ -191,6 +192,28 @@ rm_status rm_cp_compose_prefix(const rm_cp_problem* p, const float* M, const flo
 rm_status rm_cp_forward_apply(const rm_cp_problem* p, const void* q, const void* k,
                               const void* v, const float* g, const float* S_in, void* o,
                               void* ws, rm_stream_t stream);
+
+/*
+ * The whole forward in one call: rm_cp_forward_prepare, rm_cp_compose_prefix
+ * and rm_cp_forward_apply fused -- chunkwise_cp_forward's gather of the
+ * preceding summaries done by each segment itself, cp_forward_apply's
+ * "compose the preceding summaries and compute the local output".  Same
+ * inputs and outputs as the three calls (M, dS, S_in and o are all written,
+ * with the same values: the summaries are composed by the same chain of
+ * multiply-adds), plus a workspace.
+ *   On the tensor-core path (bf16, Dk = 128, Dv in {128, 256}) this is ONE
+ *   kernel launch (plus a clear of the workspace's flags): every CTA
+ *   prepares its segment's summary, then composes its own S_in from the
+ *   summaries and inclusive prefixes other CTAs of the launch have published
+ *   (a bounded look-back: CTAs start in segment order and wait, each wait
+ *   bounded, only for segments that started earlier), then applies.  On the
+ *   generic path it runs the three calls in order.
+ *   ws: device workspace of rm_cp_workspace_size bytes (its content is
+ *   overwritten; not needed across calls).
+ */
+rm_status rm_cp_forward_fused(const rm_cp_problem* p, const void* q, const void* k,
+                              const void* v, const float* g, float* M, float* dS, float* S_in,
+                              void* o, void* ws, rm_stream_t stream);
 
 /*
  * cp_backward_prepare ("compute local gamma with zero outgoing-state

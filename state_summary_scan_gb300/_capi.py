@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "RM_OK", 1: "RM_ERR_INVALID_ARG", 2: "RM_ERR_SHAPE", 3: "RM_E
 # every entry point declared in include/rm_cp.h
 EXPORTS = (
     "rm_cp_build_packed_metadata", "rm_cp_validate", "rm_cp_workspace_size",
-    "rm_cp_forward_prepare", "rm_cp_compose_prefix", "rm_cp_forward_apply",
+    "rm_cp_forward_prepare", "rm_cp_compose_prefix", "rm_cp_forward_apply", "rm_cp_forward_fused",
     "rm_cp_backward_prepare", "rm_cp_compose_suffix", "rm_cp_backward_apply",
     "rm_cp_status_string", "rm_cp_last_error", "rm_cp_path", "rm_cp_launch_count",
     "rm_cp_device_status", "rm_cp_selftest_wait_timeout", "rm_cp_backward_noalloc",
@@ -79,6 +79,7 @@ _SIGS = {
     "rm_cp_forward_prepare": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P]),
     "rm_cp_compose_prefix": (_S, [_PP, _P, _P, _P, _P]),
     "rm_cp_forward_apply": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "rm_cp_forward_fused": (_S, [_PP] + [_P] * 10),
     "rm_cp_backward_prepare": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "rm_cp_compose_suffix": (_S, [_PP, _P, _P, _P, _P]),
     "rm_cp_backward_apply": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -229,6 +230,12 @@ def rm_cp_compose_prefix(p, M, dS, S_in, stream=None):
 def rm_cp_forward_apply(p, q, k, v, g, S_in, o, ws=None, stream=None):
     _check(load().rm_cp_forward_apply(p.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S_in),
                                       _ptr(o), _ptr(ws), _stream(stream)))
+
+
+def rm_cp_forward_fused(p, q, k, v, g, M, dS, S_in, o, ws, stream=None):
+    """The three forward calls in one (one launch on the tensor-core path)."""
+    _check(load().rm_cp_forward_fused(p.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(M), _ptr(dS),
+                                      _ptr(S_in), _ptr(o), _ptr(ws), _stream(stream)))
 
 
 def rm_cp_backward_prepare(p, q, k, v, g, S_in, dO, gamma, dq, ws, stream=None):

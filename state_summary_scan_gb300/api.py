@@ -81,8 +81,8 @@ def make_plan(B, T, H, Dk, Dv, num_segments, chunk=64, scale=None, dtype=torch.b
     M = torch.empty((num_segments, B, H) + ((Dk,) if vector_gates else ()), **f32)
     dS = torch.empty(ssz, **f32)
     S_in = torch.empty(ssz, **f32)
-    plan = Plan(spec, M, dS, S_in, torch.empty((0,), **f32), torch.empty((0,), **f32),
-                torch.empty(16, dtype=torch.uint8, device=device), meta)
+    ws = torch.empty(max(C.rm_cp_workspace_size(spec), 16), dtype=torch.uint8, device=device)
+    plan = Plan(spec, M, dS, S_in, torch.empty((0,), **f32), torch.empty((0,), **f32), ws, meta)
     if backward:
         backward_buffers(plan)
     return plan
@@ -109,10 +109,16 @@ def plan_like(q: torch.Tensor, v: torch.Tensor, num_segments: int, chunk: int = 
                      q.device, backward, vector_gates=vector_gates)
 
 
-def forward(plan: Plan, q, k, v, g, o=None, stream=None) -> torch.Tensor:
-    """o = chunkwise gated linear attention; fills plan.M, plan.dS, plan.S_in."""
+def forward(plan: Plan, q, k, v, g, o=None, stream=None, fused=True) -> torch.Tensor:
+    """o = chunkwise gated linear attention; fills plan.M, plan.dS, plan.S_in.
+    fused=True: one rm_cp_forward_fused call (one launch on the tensor-core
+    path); fused=False: the three calls prepare -> compose_prefix -> apply.
+    Both give the same values."""
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    if fused:
+        C.rm_cp_forward_fused(plan.spec, q, k, v, g, plan.M, plan.dS, plan.S_in, o, plan.ws, stream)
+        return o
     C.rm_cp_forward_prepare(plan.spec, k, v, g, plan.M, plan.dS, plan.ws, stream)
     C.rm_cp_compose_prefix(plan.spec, plan.M, plan.dS, plan.S_in, stream)
     C.rm_cp_forward_apply(plan.spec, q, k, v, g, plan.S_in, o, plan.ws, stream)

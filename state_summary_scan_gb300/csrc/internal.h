@@ -24,6 +24,8 @@ struct Ptrs {
     void* out1 = nullptr;      // dv
     float* dg = nullptr;
     float* ws_f32 = nullptr;   // per-token q.dq [B,T,H]
+    void* ws = nullptr;        // the call's workspace (fused forward)
+    float* S_in_out = nullptr; // S_in written by the fused forward
 };
 
 // adds n to the process-wide launch counter (rm_cp_launch_count)
@@ -53,6 +55,9 @@ rm_status launch_compose_suffix(const Dims& d, const float* M, const float* gamm
 bool tc_supports(const Dims& d, rm_dtype dt);
 bool tc_supports_op(Op op, const Dims& d, rm_dtype dt);
 rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s);
+// the forward in one launch (prepare, composition, apply) and its workspace
+size_t tc_fused_bytes(const Dims& d, rm_dtype dt);
+rm_status tc_launch_fused_forward(const Dims& d, const Ptrs& p, cudaStream_t s);
 rm_status tc_selftest_wait(uint32_t limit_us, cudaStream_t s);
 rm_status tc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cudaStream_t s);
 

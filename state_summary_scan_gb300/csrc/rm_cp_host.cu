@@ -99,10 +99,14 @@ rm_status need(const void* ptr, const char* name) {
         if (s_ != RM_OK) return s_;                        \
     } while (0)
 
-size_t workspace_bytes(const rmcp::Dims& d) {
-    // one fp32 per (row, token, head), or per key dimension with vector gates
+size_t workspace_bytes(const rmcp::Dims& d, rm_dtype dt) {
+    // the backward: one fp32 per (row, token, head), or per key dimension with
+    // vector gates; the fused forward: its flags and inclusive prefixes (the
+    // two are never in use at the same time)
     const size_t per_tok = size_t(d.B) * d.T * d.H * sizeof(float) * (d.vg ? d.Dk : 1);
-    return (per_tok + 255) / 256 * 256;
+    const size_t bwd = (per_tok + 255) / 256 * 256;
+    const size_t fused = rmcp::tc_fused_bytes(d, dt);
+    return bwd > fused ? bwd : fused;
 }
 
 rm_status launch(rmcp::Op op, const rm_cp_problem* p, const rmcp::Dims& d, const rmcp::Ptrs& ptrs,
@@ -190,7 +194,7 @@ int32_t rm_cp_path(const rm_cp_problem* p) {
 size_t rm_cp_workspace_size(const rm_cp_problem* p) {
     rmcp::Dims d;
     if (check_problem(p, &d) != RM_OK) return 0;
-    return workspace_bytes(d);
+    return workspace_bytes(d, p->dtype);
 }
 
 rm_status rm_cp_build_packed_metadata(const int32_t* cu, int32_t num_seqs, int32_t T,
@@ -285,6 +289,44 @@ rm_status rm_cp_forward_apply(const rm_cp_problem* p, const void* q, const void*
     x.S_in = S_in;
     x.out0 = o;
     return launch(rmcp::Op::kForwardApply, p, d, x, stream);
+}
+
+rm_status rm_cp_forward_fused(const rm_cp_problem* p, const void* q, const void* k,
+                              const void* v, const float* g, float* M, float* dS, float* S_in,
+                              void* o, void* ws, rm_stream_t stream) {
+    rmcp::Dims d;
+    rm_status st = check_problem(p, &d);
+    if (st != RM_OK) return st;
+    RM_NEED(q);
+    RM_NEED(k);
+    RM_NEED(v);
+    RM_NEED(g);
+    RM_NEED(M);
+    RM_NEED(dS);
+    RM_NEED(S_in);
+    RM_NEED(o);
+    if (!rmcp::tc_supports(d, p->dtype)) {
+        // the generic kernels: the three calls in order
+        st = rm_cp_forward_prepare(p, k, v, g, M, dS, ws, stream);
+        if (st == RM_OK) st = rm_cp_compose_prefix(p, M, dS, S_in, stream);
+        if (st == RM_OK) st = rm_cp_forward_apply(p, q, k, v, g, S_in, o, ws, stream);
+        return st;
+    }
+    RM_NEED(ws);
+    rmcp::Ptrs x;
+    x.q = q;
+    x.k = k;
+    x.v = v;
+    x.g = g;
+    x.M = M;
+    x.sum_out = dS;
+    x.S_in_out = S_in;
+    x.out0 = o;
+    x.ws = ws;
+    st = rmcp::tc_launch_fused_forward(d, x, reinterpret_cast<cudaStream_t>(stream));
+    if (st == RM_ERR_CUDA)
+        return fail(RM_ERR_CUDA, "fused forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+    return st;
 }
 
 rm_status rm_cp_backward_prepare(const rm_cp_problem* p, const void* q, const void* k,

@@ -78,6 +78,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     return true;
 }
 
+// ------------------------------------------------------------------ flags
+// Flags in global memory between CTAs of one launch: a release store after
+// the data it publishes (written before a CTA barrier that the releasing
+// thread passed), an acquire load before the data is read.
+__device__ __forceinline__ void flag_release(int* f) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(1) : "memory");
+}
+__device__ __forceinline__ int flag_acquire(const int* f) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+// Waits until *f is set, for at most kWaitLimitNs; on a run-out sets
+// g_timeout_flag and returns false (the caller's outputs are then not valid).
+__device__ __forceinline__ bool flag_wait(const int* f) {
+    if (flag_acquire(f)) return true;
+    const uint64_t t0 = global_ns();
+    while (!flag_acquire(f)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicExch(&g_timeout_flag, 1);
+            return false;
+        }
+    }
+    return true;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint32_t bar) {

@@ -2090,12 +2090,15 @@ __global__ void __launch_bounds__(kRev3Threads, 1)
 //   warp 10 (one thread): loads (a stage refilled once its chunk is done)
 //              and the o stores.
 // ===========================================================================
+// The sweep as a device body: value block vb of segment seg, row b, head h,
+// from S_in.  tmem_slot holds the address of the tensor-memory columns
+// (256 with TWO, else 512) the caller allocated (read after the body's first
+// barrier).
 template <bool TWO>
-__global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
-    tc_fwd2_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
-                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                   const __grid_constant__ CUtensorMap mo, const float* __restrict__ g,
-                   const float* __restrict__ S_in) {
+__device__ __forceinline__ void fwd2_body(const Dims& d, const CUtensorMap* mq, const CUtensorMap* mk,
+                                          const CUtensorMap* mv, const CUtensorMap* mo,
+                                          const float* __restrict__ g, const float* __restrict__ S_in,
+                                          int seg, int vb, int b, int h, const uint32_t* tmem_slot) {
     constexpr uint32_t QKB = 4 * kTileBytes;  // Q | K
     constexpr uint32_t VB = 2 * kTileBytes;   // V block (128 columns)
     constexpr int NST = TWO ? 1 : 2;          // input stages
@@ -2103,7 +2106,7 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
     constexpr uint32_t OFF_O = OFF_S + 4 * kTileBytes;
     // tensor-memory columns of O and S; two CTAs a SM share the 512 columns,
     // so there O aliases the scores (issued after the scores were read)
-    constexpr uint32_t TO = TWO ? 0 : 64, TS = TWO ? 128 : 256, TCOLS = TWO ? 256 : 512;
+    constexpr uint32_t TO = TWO ? 0 : 64, TS = TWO ? 128 : 256;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint8_t* Ps = smem + OFF_P;
@@ -2115,15 +2118,12 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
     __shared__ __align__(8) uint64_t p_ready, s_ready, o_read, o_staged;   // epilogue -> warps 8, 10
     __shared__ __align__(8) uint64_t in_dead[NST], g_free[2], gate_ready[2];
     __shared__ __align__(8) uint64_t stg_free;                             // warp 10 -> epilogue
-    __shared__ uint32_t tmem_slot;
 
     const Geo G = geo();
     const bool epi = G.warp < 8;
     const bool ctl = G.warp == 8;
     const bool gat = G.warp == 9;
     const bool cpy = G.warp == 10;
-    const int nvb = d.Dv / 128;
-    const int seg = blockIdx.x / nvb, vb = blockIdx.x % nvb, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
 
@@ -2147,7 +2147,6 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
         mbar_init(smem_u32(&stg_free), 1);
         mbar_fence_init();
     }
-    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), TCOLS);
     GateRegs gr;
     if (gat) {  // gate tables of the first two chunks; registers for the third
         gr = gate_load(d, g, b, h, a0, G.lane);
@@ -2161,7 +2160,7 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tmem_slot;
+    const uint32_t tmem = *tmem_slot;
     if (epi) {  // S_in block into tensor memory and the bf16 tile: row srow, columns [64 grp, +64)
         const float* src = S_in + sum_off(d, seg, b, h) + int64_t(G.srow) * d.Dv + vb * 128 + 64 * G.grp;
         float f[64];
@@ -2265,10 +2264,10 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
                 uint8_t* st = smem + p * QKB;
                 const uint32_t qb = smem_u32(&qk_full[p]), vbar = smem_u32(&v_full[p]);
                 mbar_expect_tx(qb, QKB);
-                load_tile(st, &mq, 0, 128, h / d.qdiv, row, qb);
-                load_tile(st + 2 * kTileBytes, &mk, 0, 128, h, row, qb);
+                load_tile(st, mq, 0, 128, h / d.qdiv, row, qb);
+                load_tile(st + 2 * kTileBytes, mk, 0, 128, h, row, qb);
                 mbar_expect_tx(vbar, VB);
-                load_tile(smem + OFF_V + p * VB, &mv, vb * 128, 128, h, row, vbar);
+                load_tile(smem + OFF_V + p * VB, mv, vb * 128, 128, h, row, vbar);
             };
             load(0, 0);
             if (!TWO && nch > 1) load(1, 1);
@@ -2282,8 +2281,8 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
                     load(c + 1, 0);
                 }
                 mbar_wait(smem_u32(&o_staged), c & 1);
-                tma_store_3d(&mo, smem_u32(Os), vb * 128, h, row);
-                tma_store_3d(&mo, smem_u32(Os + kTileBytes), vb * 128 + 64, h, row);
+                tma_store_3d(mo, smem_u32(Os), vb * 128, h, row);
+                tma_store_3d(mo, smem_u32(Os + kTileBytes), vb * 128 + 64, h, row);
                 bulk_commit();
                 if (!TWO) {
                     mbar_wait(smem_u32(&in_dead[p]), (c >> 1) & 1);  // every read of the stage is done
@@ -2415,7 +2414,21 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (G.warp == 0) tmem_dealloc(tmem, TCOLS);
+}
+
+template <bool TWO>
+__global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
+    tc_fwd2_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                   const __grid_constant__ CUtensorMap mo, const float* __restrict__ g,
+                   const float* __restrict__ S_in) {
+    constexpr uint32_t TCOLS = TWO ? 256 : 512;
+    __shared__ uint32_t tmem_slot;
+    const int nvb = d.Dv / 128;
+    const int seg = blockIdx.x / nvb, vb = blockIdx.x % nvb, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    if (threadIdx.x < 32) tmem_alloc(smem_u32(&tmem_slot), TCOLS);
+    fwd2_body<TWO>(d, &mq, &mk, &mv, &mo, g, S_in, seg, vb, b, h, &tmem_slot);
+    if (threadIdx.x < 32) tmem_dealloc(tmem_slot, TCOLS);
 }
 
 // ===========================================================================
@@ -2427,11 +2440,18 @@ __global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
 // stage refills, warp 9 builds the gate tables two chunks ahead.  The scaling
 // of one chunk overlaps the products of the one before.
 // ===========================================================================
+// The sweep itself, as a device body: segment seg of row b and head h, value
+// columns [vcol0, vcol0 + DV) of y, written to out with row stride ostride.
+// Warps 0-9 take the roles above; any further warp only takes part in the
+// CTA barriers.  tmem_slot holds the address of DV tensor-memory columns the
+// caller allocated (read after the body's first barrier).  M (if not null)
+// receives exp(sum g) or 0 at (seg, b, h), and mval (if not null, shared
+// memory) the same value for the caller.
 template <int DV, bool GAMMA>
-__global__ void __launch_bounds__(kThreads + 64, 2)
-    tc_outer2_kernel(const Dims d, const __grid_constant__ CUtensorMap mx,
-                     const __grid_constant__ CUtensorMap my, const float* __restrict__ g,
-                     float* __restrict__ M, float* __restrict__ out) {
+__device__ __forceinline__ void outer2_body(const Dims& d, const CUtensorMap* mx, const CUtensorMap* my,
+                                            const float* __restrict__ g, float* __restrict__ M,
+                                            float* __restrict__ out, int seg, int b, int h, int vcol0,
+                                            int ostride, const uint32_t* tmem_slot, float* mval) {
     constexpr int NS = DV == 128 ? 3 : 2;
     constexpr uint32_t XBYTES = 2 * kTileBytes;
     constexpr uint32_t YBYTES = (DV / 64) * kTileBytes;
@@ -2441,12 +2461,10 @@ __global__ void __launch_bounds__(kThreads + 64, 2)
     __shared__ GateSmem gsb[2];
     __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS], xready[NS];
     __shared__ __align__(8) uint64_t done_bar, gate_ready[2], g_free[2];
-    __shared__ uint32_t tmem_slot;
 
     const Geo G = geo();
     const bool ctl = G.warp == 8;  // warps 0-7 scale, warp 8 issues, warp 9 prepares gates
     const bool gat = G.warp == 9;
-    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     // gamma walks forward from the segment start, delta_S backward from its end
@@ -2465,7 +2483,6 @@ __global__ void __launch_bounds__(kThreads + 64, 2)
         mbar_init(smem_u32(&done_bar), 1);
         mbar_fence_init();
     }
-    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), DV);
     GateRegs gr;
     if (gat) {
         gr = gate_load(d, g, b, h, a0 + chunk_of(0) * kChunk, G.lane);
@@ -2479,7 +2496,7 @@ __global__ void __launch_bounds__(kThreads + 64, 2)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tmem_slot;
+    const uint32_t tmem = *tmem_slot;
 
     if (ctl) {
         if (G.lane == 0) {
@@ -2488,8 +2505,8 @@ __global__ void __launch_bounds__(kThreads + 64, 2)
                 const uint32_t bar = smem_u32(&full_bar[s]);
                 uint8_t* st = smem + s * SBYTES;
                 mbar_expect_tx(bar, SBYTES);
-                load_tile(st, &mx, 0, 128, GAMMA ? h / d.qdiv : h, row, bar);  // x = q or k
-                load_tile(st + XBYTES, &my, 0, DV, h, row, bar);
+                load_tile(st, mx, 0, 128, GAMMA ? h / d.qdiv : h, row, bar);  // x = q or k
+                load_tile(st + XBYTES, my, vcol0, DV, h, row, bar);
             };
             for (int it = 0; it < NS && it < nch; ++it) issue(it, it);
             constexpr uint32_t idesc = idesc_bf16(128, DV, 1, 1);
@@ -2522,7 +2539,7 @@ __global__ void __launch_bounds__(kThreads + 64, 2)
             __syncwarp();
             if (G.lane == 0) mbar_arrive(smem_u32(&gate_ready[p]));
         }
-    } else {  // epilogue warps
+    } else if (G.warp < 8) {  // epilogue warps
         float run = 0.f;  // sum of the gates of the chunks already walked
         int seen = 0;     // a sequence starts in the chunks already walked
         for (int it = 0; it < nch; ++it) {
@@ -2553,7 +2570,7 @@ __global__ void __launch_bounds__(kThreads + 64, 2)
         }
         mbar_wait(smem_u32(&done_bar), 0);
         tc_fence_after();
-        float* dst = out + sum_off(d, seg, b, h) + int64_t(G.srow) * DV;
+        float* dst = out + sum_off(d, seg, b, h) + int64_t(G.srow) * ostride + vcol0;
 #pragma unroll 1
         for (int c = G.grp * (DV / 2); c < (G.grp + 1) * (DV / 2); c += 64) {
             float v[64];
@@ -2562,11 +2579,164 @@ __global__ void __launch_bounds__(kThreads + 64, 2)
             for (int i = 0; i < 64; i += 4)
                 *reinterpret_cast<float4*>(dst + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
         }
-        if (!GAMMA && G.tid == 0) M[(int64_t(seg) * d.B + b) * d.H + h] = seen ? 0.f : expf(run);
+        if (!GAMMA && G.tid == 0) {
+            const float m = seen ? 0.f : expf(run);
+            if (M != nullptr) M[(int64_t(seg) * d.B + b) * d.H + h] = m;
+            if (mval != nullptr) *mval = m;
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (G.warp == 0) tmem_dealloc(tmem, DV);
+}
+
+template <int DV, bool GAMMA>
+__global__ void __launch_bounds__(kThreads + 64, 2)
+    tc_outer2_kernel(const Dims d, const __grid_constant__ CUtensorMap mx,
+                     const __grid_constant__ CUtensorMap my, const float* __restrict__ g,
+                     float* __restrict__ M, float* __restrict__ out) {
+    __shared__ uint32_t tmem_slot;
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    if (threadIdx.x < 32) tmem_alloc(smem_u32(&tmem_slot), DV);
+    outer2_body<DV, GAMMA>(d, &mx, &my, g, M, out, seg, b, h, 0, DV, &tmem_slot, nullptr);
+    if (threadIdx.x < 32) tmem_dealloc(tmem_slot, DV);
+}
+
+// ===========================================================================
+// The forward in one launch: chunkwise_cp_forward's prepare, composition of
+// the preceding summaries and apply ("compose the preceding summaries and
+// compute the local output", cp_forward_apply), for one (segment j, row b,
+// head h, value block vb) per CTA.  CTAs take tickets in the order they
+// start; ticket t is (j, b H + h, vb) in segment-major order, so every CTA
+// whose results a CTA waits for started earlier, and none of them waits
+// before it has published what is waited for.
+//   1. prepare (outer2_body on the block's 128 value columns): dS_j, M_j;
+//      published with the block's "aggregate" flag.
+//   2. compose: S_in[j] = the fold S <- M_i S + dS_i over i in [p_j, j) from
+//      0, started instead after the last segment i in that range whose
+//      inclusive prefix (= S_in[i+1]) is already published (flags read
+//      without waiting); the aggregates folded after the start are waited
+//      for, each wait bounded.  Every start gives the same values: an
+//      inclusive prefix is the same chain of multiply-adds, and the chain
+//      from p_j equals the one through it because segment p_j holds a
+//      sequence start (M = 0).  The CTA writes S_in[j], then publishes its
+//      own inclusive prefix M_j S_in[j] + dS_j.
+//   3. apply (fwd2_body): o from S_in[j], with the same sweep variant the
+//      separate apply call picks (two CTAs a SM when there are more CTAs
+//      than SMs, else one with two stages).
+// The multiply-adds are those of compose_prefix_kernel, in the same order,
+// so M, dS, S_in and o equal those of the three separate calls.
+// ===========================================================================
+struct FusedWs {
+    int* ticket;     // one counter
+    int* agg;        // [n] aggregate published
+    int* inc;        // [n] inclusive prefix published
+    float* mval;     // [n] M_j of each CTA's segment
+    float* incl;     // [nseg,B,H,Dk,Dv] inclusive prefixes: incl[j] = S_in[j+1]
+};
+
+template <bool TWO>
+__global__ void __launch_bounds__(kRev3Threads, TWO ? 2 : 1)
+    tc_fused_fwd_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                        const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                        const __grid_constant__ CUtensorMap mo, const float* __restrict__ g,
+                        float* __restrict__ M, float* __restrict__ dS, float* __restrict__ S_in,
+                        const FusedWs w) {
+    constexpr uint32_t TCOLS = TWO ? 256 : 512;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int tk_s, start_s, from_inc_s;
+    __shared__ float m_self;
+    if (threadIdx.x == 0) tk_s = atomicAdd(w.ticket, 1);
+    if (threadIdx.x < 32) tmem_alloc(smem_u32(&tmem_slot), TCOLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const int nvb = d.Dv / 128, per = d.B * d.H * nvb;
+    const int tk = tk_s;
+    const int j = tk / per, bhv = tk % per, bh = bhv / nvb, vb = bhv % nvb;
+    const int b = bh / d.H, h = bh % d.H;
+    auto slot_of = [&](int i) { return (i * d.B * d.H + bh) * nvb + vb; };  // = ticket of (i, bh, vb)
+
+    // ---- 1. prepare
+    outer2_body<128, false>(d, &mk, &mv, g, vb == 0 ? M : nullptr, dS, j, b, h, vb * 128, d.Dv,
+                            &tmem_slot, &m_self);
+    const Geo G = geo();
+    if (G.tid == 0) {  // the body's closing barrier ordered every write of dS_j before this
+        w.mval[tk] = m_self;
+        flag_release(w.agg + tk);
+    }
+
+    // ---- 2. compose
+    if (G.warp == 0) {
+        const int pj = d.preceding_start ? min(max(__ldg(d.preceding_start + j), 0), j) : 0;
+        // the last i in [pj, j) with a published inclusive prefix, 32 at a time
+        int start = pj, from_inc = 0;
+        for (int top = j - 1; top >= pj; top -= 32) {
+            const int i = top - G.lane;
+            const bool ok = i >= pj && flag_acquire(w.inc + slot_of(i));
+            const unsigned m = __ballot_sync(kFull, ok);
+            if (m != 0u) {
+                start = top - (__ffs(m) - 1) + 1;
+                from_inc = 1;
+                break;
+            }
+        }
+        if (G.lane == 0) {
+            for (int l = start; l < j; ++l) flag_wait(w.agg + slot_of(l));
+            start_s = start;
+            from_inc_s = from_inc;
+        }
+    }
+    __syncthreads();
+    if (G.warp < 8) {
+        const int start = start_s;
+        const int64_t col = int64_t(G.srow) * d.Dv + vb * 128 + 64 * G.grp;
+        const float* dsj = dS + sum_off(d, j, b, h) + col;
+        const float mj = m_self;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+            float S[32];
+            if (from_inc_s) {
+                const float* src = w.incl + sum_off(d, start - 1, b, h) + col + 32 * hf;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4*>(src + e));
+                    S[e] = x.x; S[e + 1] = x.y; S[e + 2] = x.z; S[e + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) S[e] = 0.f;
+            }
+#pragma unroll 1
+            for (int l = start; l < j; ++l) {
+                const float m = __ldcg(w.mval + slot_of(l));
+                const float* src = dS + sum_off(d, l, b, h) + col + 32 * hf;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4*>(src + e));
+                    S[e] = fmaf(m, S[e], x.x);
+                    S[e + 1] = fmaf(m, S[e + 1], x.y);
+                    S[e + 2] = fmaf(m, S[e + 2], x.z);
+                    S[e + 3] = fmaf(m, S[e + 3], x.w);
+                }
+            }
+            float* so = S_in + sum_off(d, j, b, h) + col + 32 * hf;
+            float* io = w.incl + sum_off(d, j, b, h) + col + 32 * hf;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                *reinterpret_cast<float4*>(so + e) = make_float4(S[e], S[e + 1], S[e + 2], S[e + 3]);
+                const float4 x = *reinterpret_cast<const float4*>(dsj + 32 * hf + e);
+                *reinterpret_cast<float4*>(io + e) =
+                    make_float4(fmaf(mj, S[e], x.x), fmaf(mj, S[e + 1], x.y), fmaf(mj, S[e + 2], x.z),
+                                fmaf(mj, S[e + 3], x.w));
+            }
+        }
+    }
+    __syncthreads();  // every inclusive-prefix write is ordered before the release
+    if (G.tid == 0) flag_release(w.inc + tk);
+
+    // ---- 3. apply (reads S_in[j] back: each thread reads the elements it wrote)
+    fwd2_body<TWO>(d, &mq, &mk, &mv, &mo, g, S_in, j, vb, b, h, &tmem_slot);
+    if (threadIdx.x < 32) tmem_dealloc(tmem_slot, TCOLS);
 }
 
 // Failure-detection self test: waits on an mbarrier that nothing arrives on,
@@ -2650,9 +2820,52 @@ constexpr size_t rev_smem(int dv) {
     return size_t((dv == 128 ? 2 : 1) * (4 + 2 * (dv / 64)) + 6 + 2 * (dv / 64)) * kTileBytes + 1024;
 }
 
+// Workspace of the fused forward: ticket, the two flag arrays and the M
+// values (each in its own 256-byte-aligned block), then the inclusive prefixes.
+size_t fused_flags_bytes(const Dims& d) {
+    const size_t n = size_t(d.nseg) * d.B * d.H * (d.Dv / 128);
+    const size_t blk = (n * 4 + 255) / 256 * 256;
+    return 256 + 3 * blk;
+}
+size_t fused_bytes_for(const Dims& d) {
+    return fused_flags_bytes(d) + size_t(d.nseg) * d.B * d.H * d.Dk * d.Dv * sizeof(float);
+}
+
 }  // namespace
 
 }  // namespace tc
+
+size_t tc_fused_bytes(const Dims& d, rm_dtype dt) {
+    return tc_supports(d, dt) ? tc::fused_bytes_for(d) : 0;
+}
+
+rm_status tc_launch_fused_forward(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    using namespace tc;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, p.q, d, 128, d.qh) || !make_map(&mk, p.k, d, 128) ||
+        !make_map(&mv, p.v, d, d.Dv) || !make_map(&mo, p.out0, d, d.Dv))
+        return RM_ERR_CUDA;
+    const size_t n = size_t(d.nseg) * d.B * d.H * (d.Dv / 128);
+    const size_t blk = (n * 4 + 255) / 256 * 256;
+    char* base = static_cast<char*>(p.ws);
+    FusedWs w;
+    w.ticket = reinterpret_cast<int*>(base);
+    w.agg = reinterpret_cast<int*>(base + 256);
+    w.inc = reinterpret_cast<int*>(base + 256 + blk);
+    w.mval = reinterpret_cast<float*>(base + 256 + 2 * blk);
+    w.incl = reinterpret_cast<float*>(base + fused_flags_bytes(d));
+    // ticket and flags start at zero for every launch
+    if (cudaMemsetAsync(base, 0, 256 + 2 * blk, s) != cudaSuccess) return RM_ERR_CUDA;
+    // the apply variant of rm_cp_forward_apply for this grid (same arithmetic)
+    const bool two = int64_t(n) > sm_count();
+    auto fk = two ? tc_fused_fwd_kernel<true> : tc_fused_fwd_kernel<false>;
+    const size_t fsm = two ? kFwd2TwoSmem : kFwd2Smem;
+    if (!set_smem(fk, fsm)) return RM_ERR_CUDA;
+    fk<<<unsigned(n), kRev3Threads, fsm, s>>>(d, mq, mk, mv, mo, p.g, p.M, p.sum_out, p.S_in_out, w);
+    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    note_launch(1);
+    return RM_OK;
+}
 
 rm_status tc_selftest_wait(uint32_t limit_us, cudaStream_t s) {
     tc::selftest_wait_kernel<<<1, 1, 0, s>>>(uint64_t(limit_us) * 1000ull);

@@ -316,3 +316,48 @@ def shared_queries_case(dtype, Dk, Dv, chunk, B, T, H, qh, nseg):
     gpu = {key: val.detach().to("cpu", torch.float64).numpy() for key, val in gpu.items()}
     ref = run_oracle(q.repeat_interleave(H // qh, dim=2), k, v, g, dO, nseg, scale)
     compare(gpu, ref, tol_for(dtype), ALL_KEYS)
+
+
+# ------------------------------------------------------------------ fused forward
+
+@pytest.mark.parametrize("T,H,Dv,nseg,cu,qh", [
+    (2048, 16, 128, 16, None, 0),                                   # 256 CTAs (> SMs), one wave at two a SM
+    (2048, 16, 128, 16, [0, 1, 100, 128, 129, 700, 1024, 1025, 1500, 1999, 2048], 0),  # resets
+    (8192, 16, 256, 64, None, 0),                                   # 2048 CTAs: look-back across waves
+    (8192, 8, 256, 32, [0, 3000, 3001, 8192], 2),                   # Dv = 256 blocks, resets, shared queries
+    (512, 2, 128, 1, None, 0),                                      # one segment
+])
+def test_fused_forward_equals_three_calls(T, H, Dv, nseg, cu, qh):
+    """rm_cp_forward_fused (one launch: prepare, the bounded look-back over the
+    summaries the launch's other CTAs publish, apply) writes exactly what
+    rm_cp_forward_prepare + rm_cp_compose_prefix + rm_cp_forward_apply write:
+    the summaries are composed by the same chain of multiply-adds, whatever
+    point of the chain a CTA starts from."""
+    from state_summary_scan_gb300 import api
+    gen = torch.Generator().manual_seed(T + H + Dv + nseg)
+    q = torch.randn(1, T, qh or H, 128, generator=gen).to(torch.bfloat16).cuda()
+    k = torch.randn(1, T, H, 128, generator=gen)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16).cuda()
+    v = torch.randn(1, T, H, Dv, generator=gen).to(torch.bfloat16).cuda()
+    g = torch.nn.functional.logsigmoid(torch.randn(1, T, H, generator=gen) + 4).cuda()
+    outs = []
+    for fused in (True, False):
+        plan = api.make_plan(1, T, H, 128, Dv, nseg, 64, 128 ** -0.5, torch.bfloat16, cu,
+                             backward=False, q_heads=qh)
+        o = api.forward(plan, q, k, v, g, fused=fused)
+        torch.cuda.synchronize()
+        outs.append(dict(o=o, M=plan.M, dS=plan.dS, S_in=plan.S_in))
+    for key in outs[0]:
+        assert torch.equal(outs[0][key], outs[1][key]), key
+
+
+def test_fused_forward_generic_path_runs_the_three_calls():
+    from state_summary_scan_gb300 import api
+    q, k, v, g, _ = synth(1, 256, 2, 32, 32, torch.float32, seed=9)
+    q, k, v, g = (t.cuda() for t in (q, k, v, g))
+    outs = []
+    for fused in (True, False):
+        plan = api.make_plan(1, 256, 2, 32, 32, 4, 16, 0.2, torch.float32, backward=False)
+        outs.append(api.forward(plan, q, k, v, g, fused=fused).clone())
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
