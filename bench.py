@@ -4,7 +4,8 @@
 One step = the whole path on one batch of the workload: forward_prepare,
 compose_prefix, forward_apply, backward_prepare, compose_suffix,
 backward_apply (forward only for forward-only workloads), all through the
-C ABI on the current stream, inputs resident in HBM.
+C ABI on the current stream, inputs resident in HBM.  The forward is also
+timed as the one-launch rm_cp_forward_fused (fwd_path_roofline.fused_us).
 
 Prints ONE JSON line (rank 0).  Besides the step throughput it reports:
   roofline      the dominant kernel's algorithmic bytes per launch over its
@@ -43,6 +44,7 @@ METRIC = "fwd+bwd tokens/sec on 1 GB300; % of bf16 tensor/HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2 ** 20
 PHASES_FWD = ("forward_prepare", "compose_prefix", "forward_apply")
+PHASES_FUSED = ("forward_fused",)  # rm_cp_forward_fused: the same forward in one launch
 PHASES_BWD = ("backward_prepare", "compose_suffix", "backward_apply")
 
 
@@ -80,6 +82,8 @@ def kernel_bytes(w, phase):
         return nsum * (2 * st + f)
     if phase == "backward_apply":
         return ntok * (e * (2 * Dk + 2 * Dv) + f + f + e * (Dk + Dv) + f) + nsum * 2 * st
+    if phase == "forward_fused":  # the three forward calls' inputs and outputs
+        return sum(kernel_bytes(w, ph) for ph in PHASES_FWD)
     raise KeyError(phase)
 
 
@@ -95,7 +99,8 @@ def kernel_alu_flops(w, phase):
     ntok = w.B * w.T * w.H
     kd = w.Dk * w.Dv
     per = {"forward_prepare": 2 * kd, "forward_apply": 4 * kd, "backward_prepare": 6 * kd,
-           "backward_apply": 6 * kd, "compose_prefix": 0, "compose_suffix": 0}[phase]
+           "backward_apply": 6 * kd, "compose_prefix": 0, "compose_suffix": 0,
+           "forward_fused": 6 * kd}[phase]
     return ntok * per
 
 
@@ -266,6 +271,8 @@ def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_
     stream = torch.cuda.current_stream(dev)
     phases = PHASES_FWD + (PHASES_BWD if w.backward else ())
     fns = {
+        "forward_fused": lambda: C.rm_cp_forward_fused(s, q, k, v, g, plan.M, plan.dS, plan.S_in, o,
+                                                       plan.ws, stream),
         "forward_prepare": lambda: C.rm_cp_forward_prepare(s, k, v, g, plan.M, plan.dS, plan.ws, stream),
         "compose_prefix": lambda: C.rm_cp_compose_prefix(s, plan.M, plan.dS, plan.S_in, stream),
         "forward_apply": lambda: C.rm_cp_forward_apply(s, q, k, v, g, plan.S_in, o, plan.ws, stream),
@@ -304,19 +311,27 @@ def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_
     end.record(stream)
     torch.cuda.synchronize(dev)
     launches = C.rm_cp_launch_count() - l0
-    # forward-only steps (the three forward calls), timed the same way
+    # forward-only steps, timed the same way: the three calls, and the same
+    # forward as the one-launch rm_cp_forward_fused for comparison
     fstart = torch.cuda.Event(enable_timing=True)
     fend = torch.cuda.Event(enable_timing=True)
     fstart.record(stream)
     for i in range(args.steps):
         step(None, PHASES_FWD)
     fend.record(stream)
+    f3start = torch.cuda.Event(enable_timing=True)
+    f3end = torch.cuda.Event(enable_timing=True)
+    f3start.record(stream)
+    for i in range(args.steps):
+        step(None, PHASES_FUSED)
+    f3end.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
     ms_per_step = replica_time(start.elapsed_time(end), world, dev) / args.steps
     fwd_ms = replica_time(fstart.elapsed_time(fend), world, dev) / args.steps
+    fwd3_ms = replica_time(f3start.elapsed_time(f3end), world, dev) / args.steps
     tok_per_step = w.B * w.T
     value = replica_throughput(world, tok_per_step, ms_per_step)
     fwd_value = replica_throughput(world, tok_per_step, fwd_ms)
@@ -348,7 +363,10 @@ def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_
                                             / peaks["hbm_gbs"], 4) for ph in phases}}
     fpr = path_roofline(w.replace(backward=False), peaks)
     fwd_path = {"bound": fpr["bound"], "t_roofline_us": fpr["t_roofline_us"],
-                "t_measured_us": fwd_ms * 1e3, "frac": fpr["t_roofline_us"] / (fwd_ms * 1e3)}
+                "t_measured_us": fwd_ms * 1e3, "frac": fpr["t_roofline_us"] / (fwd_ms * 1e3),
+                "calls": "forward_prepare, compose_prefix, forward_apply",
+                "fused_us": fwd3_ms * 1e3,
+                "fused_frac": fpr["t_roofline_us"] / (fwd3_ms * 1e3)}
 
     # ---- end to end through rm_cp_step_host: pinned host buffers in, results
     # out, every step.  Two device buffer sets and two copy streams: the
@@ -539,6 +557,8 @@ def run_ssd(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     fns = {
         "ssd_map_inputs": lambda: C.rm_ssd_map_inputs(s, w.G, dt, A, Bm, None, None, sp.k, sp.g, stream),
+        "forward_fused": lambda: C.rm_cp_forward_fused(s, Cm, sp.k, x, sp.g, plan.M, plan.dS, plan.S_in, y,
+                                                       plan.ws, stream),
         "forward_prepare": lambda: C.rm_cp_forward_prepare(s, sp.k, x, sp.g, plan.M, plan.dS, plan.ws, stream),
         "compose_prefix": lambda: C.rm_cp_compose_prefix(s, plan.M, plan.dS, plan.S_in, stream),
         "forward_apply": lambda: C.rm_cp_forward_apply(s, Cm, sp.k, x, sp.g, plan.S_in, y, plan.ws, stream),

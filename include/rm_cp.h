@@ -210,6 +210,11 @@ rm_status rm_cp_forward_apply(const rm_cp_problem* p, const void* q, const void*
  *   generic path it runs the three calls in order.
  *   ws: device workspace of rm_cp_workspace_size bytes (its content is
  *   overwritten; not needed across calls).
+ *   Measured on GB300 this one launch is slower than the three calls on the
+ *   configurations here: all CTAs of a wave finish their summaries together,
+ *   so few find a predecessor's inclusive prefix already published, and each
+ *   then folds the summaries of the segments before it (more bytes and more
+ *   dependent loads than the separate, fully parallel composition).
  */
 rm_status rm_cp_forward_fused(const rm_cp_problem* p, const void* q, const void* k,
                               const void* v, const float* g, float* M, float* dS, float* S_in,

@@ -109,11 +109,11 @@ def plan_like(q: torch.Tensor, v: torch.Tensor, num_segments: int, chunk: int = 
                      q.device, backward, vector_gates=vector_gates)
 
 
-def forward(plan: Plan, q, k, v, g, o=None, stream=None, fused=True) -> torch.Tensor:
+def forward(plan: Plan, q, k, v, g, o=None, stream=None, fused=False) -> torch.Tensor:
     """o = chunkwise gated linear attention; fills plan.M, plan.dS, plan.S_in.
-    fused=True: one rm_cp_forward_fused call (one launch on the tensor-core
-    path); fused=False: the three calls prepare -> compose_prefix -> apply.
-    Both give the same values."""
+    fused=False: the three calls prepare -> compose_prefix -> apply (the
+    faster form on these shapes); fused=True: one rm_cp_forward_fused call
+    (one launch on the tensor-core path).  Both give the same values."""
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     if fused:

@@ -2799,10 +2799,14 @@ int sm_count() {
     return cache[dev];
 }
 
+// Dynamic shared memory of a kernel; the carveout is set to all shared memory,
+// so that kernels sized for two CTAs a SM get them.
 template <typename K>
 bool set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) ==
-           cudaSuccess;
+               cudaSuccess &&
+           cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                int(cudaSharedmemCarveoutMaxShared)) == cudaSuccess;
 }
 
 constexpr size_t kOuterSmem = 96 * 1024 + 1024;

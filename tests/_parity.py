@@ -33,7 +33,7 @@ def canary_empty(shape, dtype, device, pad=64):
 
 
 def run_gpu(q, k, v, g, dO, num_segments, chunk=64, scale=None, cu_seqlens=None,
-            use_metadata=True, canary=True):
+            use_metadata=True, canary=True, fused=False):
     """Run the CUDA path on host tensors; returns a dict of CPU float64 tensors."""
     dev = "cuda"
     qd, kd, vd, gd = (t.to(dev).contiguous() for t in (q, k, v, g))
@@ -49,7 +49,7 @@ def run_gpu(q, k, v, g, dO, num_segments, chunk=64, scale=None, cu_seqlens=None,
         fulls.append(f)
     else:
         o = None
-    o = api.forward(plan, qd, kd, vd, gd, o=o)
+    o = api.forward(plan, qd, kd, vd, gd, o=o, fused=fused)
     out = dict(o=o, M=plan.M, dS=plan.dS, S_in=plan.S_in)
     if dO is not None:
         dOd = dO.to(dev).contiguous()

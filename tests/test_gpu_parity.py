@@ -75,10 +75,10 @@ def synth(B, T, H, Dk, Dv, dtype, seed=0, gate_shift=3.0, gate=None):
     return q.to(dtype), k.to(dtype), v.to(dtype), g.contiguous(), dO.to(dtype)
 
 
-def check_case(B, T, H, Dk, Dv, dtype, nseg, chunk=16, cu=None, use_metadata=True, **kw):
+def check_case(B, T, H, Dk, Dv, dtype, nseg, chunk=16, cu=None, use_metadata=True, fused=False, **kw):
     q, k, v, g, dO = synth(B, T, H, Dk, Dv, dtype, **kw)
     scale = 1.0 / math.sqrt(Dk)
-    gpu = run_gpu(q, k, v, g, dO, nseg, chunk, scale, cu, use_metadata=use_metadata)
+    gpu = run_gpu(q, k, v, g, dO, nseg, chunk, scale, cu, use_metadata=use_metadata, fused=fused)
     ref = run_oracle(q, k, v, g, dO, nseg, scale, cu)
     keys = ALL_KEYS if use_metadata else ("o",) + GRAD_KEYS
     return compare(select_heads(gpu, None), ref, tol_for(dtype), keys)
@@ -349,6 +349,15 @@ def test_fused_forward_equals_three_calls(T, H, Dv, nseg, cu, qh):
         outs.append(dict(o=o, M=plan.M, dS=plan.dS, S_in=plan.S_in))
     for key in outs[0]:
         assert torch.equal(outs[0][key], outs[1][key]), key
+
+
+@pytest.mark.parametrize("Dv", [128, 256])
+def test_fused_forward_against_the_oracle(Dv):
+    """The one-launch forward (and the backward after it) against the fp64
+    oracle: packed sequences with starts at chunk positions 0, 1, 63, a
+    segment start and across three segments, on a grid wider than the GPU."""
+    cu = [0, 1, 2, 63, 64, 65, 129, 256, 257, 300, 511, 512, 700, 1024, 1500, 2048]
+    check_case(1, 2048, 16, 128, Dv, torch.bfloat16, nseg=16, chunk=64, cu=cu, fused=True)
 
 
 def test_fused_forward_generic_path_runs_the_three_calls():
