@@ -437,6 +437,54 @@ rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, const void* 
                                  void* dv, const float* dg, float* ddt, float* dA, void* dB,
                                  void* dC, float* dD, void* ws, rm_stream_t stream);
 
+/*
+ * Gated delta rule on the same segment-summary path.  Per row b and head h,
+ * with g_t and beta_t [B,T,H] fp32, alpha_t = exp(g_t) (0 when token t starts
+ * a sequence) and A_t = alpha_t (I - beta_t k_t k_t^T):
+ *     S_t = A_t S_{t-1} + beta_t k_t v_t^T,      o_t = scale S_t^T q_t.
+ * A segment's summary is the Megatron-Core page's general affine map
+ * S_out = M S_in + delta_S (CPForwardUnpackedSummary) with the Dk x Dk
+ * transition M = A_last ... A_first (0 when a token of the segment starts a
+ * sequence); the backward composes dS_in = M^T dS_out + gamma
+ * (CPBackwardUnpackedSummary).  The six calls mirror the scalar-gate ones:
+ *   rm_gdr_forward_prepare  M [nseg,B,H,Dk,Dk], dS [nseg,B,H,Dk,Dv] fp32 out
+ *   rm_gdr_compose_prefix   S_in[j] = fold over [pre_j, j) of S <- M_i S + dS_i
+ *   rm_gdr_forward_apply    o
+ *   rm_gdr_backward_prepare gamma [nseg,B,H,Dk,Dv] (the local adjoint at the
+ *                           segment start, zero outgoing gradient) and
+ *                           dq_t = scale S_t dO_t; saves the state before
+ *                           every 16-token block in ws for the apply
+ *   rm_gdr_compose_suffix   dS_out[j] = fold over (j, fol_j) of D <- M_i^T D + gamma_i
+ *   rm_gdr_backward_apply   from D = dS_out at each segment's end:
+ *                           dk, dv [B,T,H,*] (dtype), dg, dbeta [B,T,H] fp32
+ *                           (dg exactly 0 at sequence starts)
+ * The problem is an rm_cp_problem (vector_gates = 0, any q_heads); these run
+ * on generic fp32-arithmetic kernels for Dk in {16, 32, 64}, Dv a multiple of
+ * 8 up to 128, segment lengths a multiple of 16 (RM_ERR_UNSUPPORTED
+ * otherwise).  ws: rm_gdr_workspace_size bytes (B H (T / 16) Dk Dv fp32),
+ * passed unchanged from rm_gdr_backward_prepare to rm_gdr_backward_apply.
+ * Validation, ownership and errors as for the other calls.
+ */
+size_t rm_gdr_workspace_size(const rm_cp_problem* p);
+rm_status rm_gdr_forward_prepare(const rm_cp_problem* p, const void* k, const void* v,
+                                 const float* g, const float* beta, float* M, float* dS,
+                                 rm_stream_t stream);
+rm_status rm_gdr_compose_prefix(const rm_cp_problem* p, const float* M, const float* dS,
+                                float* S_in, rm_stream_t stream);
+rm_status rm_gdr_forward_apply(const rm_cp_problem* p, const void* q, const void* k, const void* v,
+                               const float* g, const float* beta, const float* S_in, void* o,
+                               rm_stream_t stream);
+rm_status rm_gdr_backward_prepare(const rm_cp_problem* p, const void* q, const void* k,
+                                  const void* v, const float* g, const float* beta,
+                                  const float* S_in, const void* dO, float* gamma, void* dq,
+                                  void* ws, rm_stream_t stream);
+rm_status rm_gdr_compose_suffix(const rm_cp_problem* p, const float* M, const float* gamma,
+                                float* dS_out, rm_stream_t stream);
+rm_status rm_gdr_backward_apply(const rm_cp_problem* p, const void* q, const void* k, const void* v,
+                                const float* g, const float* beta, const void* dO,
+                                const float* dS_out, void* dk, void* dv, float* dg, float* dbeta,
+                                void* ws, rm_stream_t stream);
+
 /* Name of a status code (static string). */
 const char* rm_cp_status_string(rm_status s);
 

@@ -30,6 +30,8 @@ EXPORTS = (
     "rm_cp_device_status", "rm_cp_selftest_wait_timeout", "rm_cp_backward_noalloc",
     "rm_cp_step_host", "rm_cp_event_create", "rm_cp_event_destroy",
     "rm_ssd_workspace_size", "rm_ssd_map_inputs", "rm_ssd_finish_forward", "rm_ssd_finish_backward",
+    "rm_gdr_workspace_size", "rm_gdr_forward_prepare", "rm_gdr_compose_prefix", "rm_gdr_forward_apply",
+    "rm_gdr_backward_prepare", "rm_gdr_compose_suffix", "rm_gdr_backward_apply",
 )
 
 
@@ -98,6 +100,13 @@ _SIGS = {
     "rm_ssd_map_inputs": (_S, [_PP, ctypes.c_int32] + [_P] * 8),
     "rm_ssd_finish_forward": (_S, [_PP, _P, _P, _P, _P]),
     "rm_ssd_finish_backward": (_S, [_PP, ctypes.c_int32] + [_P] * 17),
+    "rm_gdr_workspace_size": (ctypes.c_size_t, [_PP]),
+    "rm_gdr_forward_prepare": (_S, [_PP] + [_P] * 7),
+    "rm_gdr_compose_prefix": (_S, [_PP] + [_P] * 4),
+    "rm_gdr_forward_apply": (_S, [_PP] + [_P] * 8),
+    "rm_gdr_backward_prepare": (_S, [_PP] + [_P] * 11),
+    "rm_gdr_compose_suffix": (_S, [_PP] + [_P] * 4),
+    "rm_gdr_backward_apply": (_S, [_PP] + [_P] * 13),
 }
 
 _lock = threading.Lock()
@@ -314,3 +323,39 @@ def rm_ssd_finish_backward(p, G, x, dt, A, Bm, dy, D, dq, dk, dv, dg, ddt, dA, d
                                          _ptr(dy), _ptr(D), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
                                          _ptr(ddt), _ptr(dA), _ptr(dB), _ptr(dC), _ptr(dD),
                                          _ptr(ws), _stream(stream)))
+
+
+# ----------------------------------------------------------------- gated delta rule
+
+def rm_gdr_workspace_size(p: ProblemSpec) -> int:
+    return int(load().rm_gdr_workspace_size(p.ref))
+
+
+def rm_gdr_forward_prepare(p, k, v, g, beta, M, dS, stream=None):
+    _check(load().rm_gdr_forward_prepare(p.ref, _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(M),
+                                         _ptr(dS), _stream(stream)))
+
+
+def rm_gdr_compose_prefix(p, M, dS, S_in, stream=None):
+    _check(load().rm_gdr_compose_prefix(p.ref, _ptr(M), _ptr(dS), _ptr(S_in), _stream(stream)))
+
+
+def rm_gdr_forward_apply(p, q, k, v, g, beta, S_in, o, stream=None):
+    _check(load().rm_gdr_forward_apply(p.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                       _ptr(S_in), _ptr(o), _stream(stream)))
+
+
+def rm_gdr_backward_prepare(p, q, k, v, g, beta, S_in, dO, gamma, dq, ws, stream=None):
+    _check(load().rm_gdr_backward_prepare(p.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                          _ptr(S_in), _ptr(dO), _ptr(gamma), _ptr(dq), _ptr(ws),
+                                          _stream(stream)))
+
+
+def rm_gdr_compose_suffix(p, M, gamma, dS_out, stream=None):
+    _check(load().rm_gdr_compose_suffix(p.ref, _ptr(M), _ptr(gamma), _ptr(dS_out), _stream(stream)))
+
+
+def rm_gdr_backward_apply(p, q, k, v, g, beta, dO, dS_out, dk, dv, dg, dbeta, ws, stream=None):
+    _check(load().rm_gdr_backward_apply(p.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                        _ptr(dO), _ptr(dS_out), _ptr(dk), _ptr(dv), _ptr(dg),
+                                        _ptr(dbeta), _ptr(ws), _stream(stream)))

@@ -279,3 +279,50 @@ def ssd_backward(sp: SsdPlan, x, dt, A, Bm, Cm, dy, D=None, stream=None, core=No
     C.rm_ssd_finish_backward(sp.core.spec, sp.G, x, dt, A, Bm, dy, D, dq, dk, dv, dg, ddt, dA, dB,
                              dC, dD, sp.ws, stream)
     return dv, ddt, dA, dB, dC, dD
+
+
+# ------------------------------------------------------------------ gated delta rule
+
+@dataclasses.dataclass
+class GdrPlan:
+    """Summaries and workspace of the gated delta rule (Dk x Dk transitions)."""
+    spec: C.ProblemSpec
+    M: torch.Tensor        # [nseg,B,H,Dk,Dk] fp32
+    dS: torch.Tensor       # [nseg,B,H,Dk,Dv] fp32
+    S_in: torch.Tensor
+    gamma: torch.Tensor
+    dS_out: torch.Tensor
+    ws: torch.Tensor       # states saved by the backward prepare for the apply
+
+
+def make_gdr_plan(B, T, H, Dk, Dv, num_segments, chunk=16, scale=None, dtype=torch.float32,
+                  cu_seqlens=None, device="cuda", q_heads=0) -> GdrPlan:
+    spec, _ = cached_spec(B, T, H, Dk, Dv, num_segments, chunk, scale, dtype, cu_seqlens, device,
+                          q_heads)
+    f32 = dict(dtype=torch.float32, device=device)
+    ssz = (num_segments, B, H, Dk, Dv)
+    ws = torch.empty(max(C.rm_gdr_workspace_size(spec), 16), dtype=torch.uint8, device=device)
+    return GdrPlan(spec, torch.empty((num_segments, B, H, Dk, Dk), **f32), torch.empty(ssz, **f32),
+                   torch.empty(ssz, **f32), torch.empty(ssz, **f32), torch.empty(ssz, **f32), ws)
+
+
+def gdr_forward(plan: GdrPlan, q, k, v, g, beta, o=None, stream=None) -> torch.Tensor:
+    """o of the gated delta rule: prepare -> compose_prefix -> apply."""
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    C.rm_gdr_forward_prepare(plan.spec, k, v, g, beta, plan.M, plan.dS, stream)
+    C.rm_gdr_compose_prefix(plan.spec, plan.M, plan.dS, plan.S_in, stream)
+    C.rm_gdr_forward_apply(plan.spec, q, k, v, g, beta, plan.S_in, o, stream)
+    return o
+
+
+def gdr_backward(plan: GdrPlan, q, k, v, g, beta, dO, stream=None):
+    """(dq, dk, dv, dg, dbeta) of sum(dO * o); needs gdr_forward on plan first."""
+    dq, dk, dv = torch.empty_like(k), torch.empty_like(k), torch.empty_like(v)
+    dg, db = torch.empty_like(g), torch.empty_like(beta)
+    C.rm_gdr_backward_prepare(plan.spec, q, k, v, g, beta, plan.S_in, dO, plan.gamma, dq, plan.ws,
+                              stream)
+    C.rm_gdr_compose_suffix(plan.spec, plan.M, plan.gamma, plan.dS_out, stream)
+    C.rm_gdr_backward_apply(plan.spec, q, k, v, g, beta, dO, plan.dS_out, dk, dv, dg, db, plan.ws,
+                            stream)
+    return dq, dk, dv, dg, db

@@ -1,0 +1,613 @@
+// gdr_kernels.cu -- the gated delta rule on the segment-summary path.
+//
+// Per row b and head h, with a scalar gate g_t and write strength beta_t
+// ([B,T,H] fp32 each), alpha_t = exp(g_t) (0 when token t starts a sequence)
+// and A_t = alpha_t (I - beta_t k_t k_t^T):
+//     S_t = A_t S_{t-1} + beta_t k_t v_t^T,      o_t = scale S_t^T q_t.
+// A segment's summary is then the general affine map of the Megatron-Core
+// page "core.ssm.context_parallel.chunkwise": S_out = M S_in + delta_S
+// (CPForwardUnpackedSummary) with the Dk x Dk transition M = A_last ... A_first
+// (0 when a token of the segment starts a sequence), and the backward's
+// dS_in = M^T dS_out + gamma (CPBackwardUnpackedSummary); A_t is symmetric.
+//
+// Kernels (fp32 arithmetic, both storage types; one CTA per (segment, row,
+// head) unless noted):
+//   gdr_column_sweep  forward walks by column owners (thread = one column of
+//                     the state in registers: k^T S, the rank-one correction
+//                     and the readout are all column-local).  PREPARE also
+//                     walks M's columns as extra columns with v = 0 from the
+//                     identity; APPLY starts from S_in and writes o.
+//   gdr_gamma_sweep   gamma = A_a D_a of the local adjoint walked back from
+//                     the segment end with a zero outgoing gradient (column
+//                     owners of D, column-local for the same reason).
+//   gdr_compose       the prefix fold S <- M_i S + dS_i over [pre_j, j), or
+//                     the suffix fold D <- M_i^T D + gamma_i over (j, fol_j),
+//                     one CTA per (row, head, column block), M_i staged in
+//                     shared memory, a column per thread.
+//   gdr_dq_sweep      the state in shared memory from S_in (k^T S by column
+//                     owners, the update and dq_t = scale S_t dO_t by row
+//                     owners); writes the state before every 16-token block
+//                     to the workspace.
+//   gdr_reverse_sweep the adjoint D in shared memory from dS_out at the
+//                     segment end (D_t = scale q_t dO_t^T + A_{t+1} D_{t+1});
+//                     S_{t-1} is rebuilt in shared memory from the block's
+//                     saved state; dv, dk, dbeta and dg per token:
+//                       dv_t    = beta_t D_t^T k_t
+//                       dk_t    = beta_t D_t v_t - alpha_t beta_t (S_{t-1} D_t^T + D_t S_{t-1}^T) k_t
+//                       dbeta_t = k_t^T D_t v_t - alpha_t k_t^T D_t S_{t-1}^T k_t
+//                       dg_t    = alpha_t <D_t, (I - beta_t k_t k_t^T) S_{t-1}>  (0 at a start)
+#include "internal.h"
+
+namespace rmcp {
+
+namespace {
+
+constexpr int kBlk = 16;  // tokens per saved state of the dq sweep (and per rebuild)
+
+__device__ __forceinline__ float gdr_alpha(const Dims& d, const float* g, int b, int t, int h) {
+    return starts_sequence(d.seq_idx, t) ? 0.f : expf(__ldg(g + g_off(d, b, t, h)));
+}
+
+// ---------------------------------------------------------------------------
+// Forward column sweep.  Column c < Dv is column c of the state (value v_c);
+// PREPARE adds columns Dv + c' for column c' of M (value 0, start e_c').
+// grid (nseg, B*H, ceil(ncol / blockDim)); block 32..128 threads.
+// ---------------------------------------------------------------------------
+enum GdrMode { kGdrPrepare = 0, kGdrApply = 1 };
+
+template <int DK, int MODE, typename T>
+__global__ void __launch_bounds__(128) gdr_column_sweep(Dims d, const T* __restrict__ q,
+                                                        const T* __restrict__ k,
+                                                        const T* __restrict__ v,
+                                                        const float* __restrict__ g,
+                                                        const float* __restrict__ beta,
+                                                        const float* __restrict__ S_in,
+                                                        T* __restrict__ o, float* __restrict__ M,
+                                                        float* __restrict__ dS) {
+    constexpr int kTok = 16;
+    __shared__ float k_s[kTok][DK];
+    __shared__ float q_s[kTok][DK];
+    __shared__ float a_s[kTok], b_s[kTok];
+
+    const int seg = blockIdx.x;
+    const int b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int col = blockIdx.z * blockDim.x + threadIdx.x;
+    const int ncol = MODE == kGdrPrepare ? d.Dv + DK : d.Dv;
+    const bool active = col < ncol;
+    const bool is_m = MODE == kGdrPrepare && col >= d.Dv;  // a column of M
+    const int a0 = seg * d.L;
+
+    float st[DK];
+    if (MODE == kGdrApply && active) {
+        const float* src = S_in + sum_off(d, seg, b, h);
+#pragma unroll
+        for (int i = 0; i < DK; ++i) st[i] = src[int64_t(i) * d.Dv + col];
+    } else {
+#pragma unroll
+        for (int i = 0; i < DK; ++i) st[i] = (is_m && i == col - d.Dv) ? 1.f : 0.f;
+    }
+
+    for (int t0 = a0; t0 < a0 + d.L; t0 += kTok) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < kTok * DK; e += blockDim.x) {
+            const int tt = e / DK, i = e % DK;
+            k_s[tt][i] = to_f32(k[qk_off(d, b, t0 + tt, h) + i]);
+            if (MODE == kGdrApply) q_s[tt][i] = to_f32(q[q_off(d, b, t0 + tt, h) + i]);
+        }
+        if (threadIdx.x < kTok) {
+            const int t = t0 + threadIdx.x;
+            a_s[threadIdx.x] = gdr_alpha(d, g, b, t, h);
+            b_s[threadIdx.x] = __ldg(beta + g_off(d, b, t, h));
+        }
+        float vr[kTok];
+#pragma unroll
+        for (int tt = 0; tt < kTok; ++tt)
+            vr[tt] = (active && !is_m) ? to_f32(v[v_off(d, b, t0 + tt, h) + col]) : 0.f;
+        __syncthreads();
+#pragma unroll 1
+        for (int tt = 0; tt < kTok; ++tt) {
+            const float al = a_s[tt], be = b_s[tt];
+            float ks = 0.f;  // k_t^T S[:, col]
+#pragma unroll
+            for (int i = 0; i < DK; ++i) ks = fmaf(k_s[tt][i], st[i], ks);
+            // S = alpha (S - beta k (k^T S)) + beta k v^T, column col
+            const float c1 = be * ks, c2 = be * vr[tt];
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < DK; ++i) {
+                const float ki = k_s[tt][i];
+                st[i] = fmaf(al, fmaf(-c1, ki, st[i]), c2 * ki);
+                if (MODE == kGdrApply) acc = fmaf(st[i], q_s[tt][i], acc);
+            }
+            if (MODE == kGdrApply && active) o[v_off(d, b, t0 + tt, h) + col] = from_f32<T>(d.scale * acc);
+        }
+    }
+    if (MODE == kGdrPrepare && active) {
+        if (is_m) {
+            float* dst = M + ((int64_t(seg) * d.B + b) * d.H + h) * DK * DK + (col - d.Dv);
+#pragma unroll
+            for (int i = 0; i < DK; ++i) dst[int64_t(i) * DK] = st[i];
+        } else {
+            float* dst = dS + sum_off(d, seg, b, h) + col;
+#pragma unroll
+            for (int i = 0; i < DK; ++i) dst[int64_t(i) * d.Dv] = st[i];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// gamma: column owners of the local adjoint D, walked back from the segment
+// end with zero outgoing gradient: per token D += scale q_t dO_t[col] (now
+// D_t), then D <- A_t D (the carry into token t - 1); after the segment's
+// first token a, D = A_a D_a = gamma[:, col].
+// grid (nseg, B*H, ceil(Dv / blockDim)); block 32..128 threads.
+// ---------------------------------------------------------------------------
+template <int DK, typename T>
+__global__ void __launch_bounds__(128) gdr_gamma_sweep(Dims d, const T* __restrict__ q,
+                                                       const T* __restrict__ k,
+                                                       const float* __restrict__ g,
+                                                       const float* __restrict__ beta,
+                                                       const T* __restrict__ dO,
+                                                       float* __restrict__ gamma) {
+    constexpr int kTok = 16;
+    __shared__ float k_s[kTok][DK];  // k of the tile's tokens
+    __shared__ float q_s[kTok][DK];
+    __shared__ float a_s[kTok], b_s[kTok];
+
+    const int seg = blockIdx.x;
+    const int b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int col = blockIdx.z * blockDim.x + threadIdx.x;
+    const bool active = col < d.Dv;
+    const int a0 = seg * d.L, e0 = a0 + d.L;
+
+    float D[DK];
+#pragma unroll
+    for (int i = 0; i < DK; ++i) D[i] = 0.f;
+
+    for (int t0 = e0 - kTok; t0 >= a0; t0 -= kTok) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < kTok * DK; e += blockDim.x) {
+            const int tt = e / DK, i = e % DK;
+            k_s[tt][i] = to_f32(k[qk_off(d, b, t0 + tt, h) + i]);
+            q_s[tt][i] = to_f32(q[q_off(d, b, t0 + tt, h) + i]);
+        }
+        if (threadIdx.x < kTok) {
+            const int t = t0 + threadIdx.x;
+            a_s[threadIdx.x] = gdr_alpha(d, g, b, t, h);
+            b_s[threadIdx.x] = __ldg(beta + g_off(d, b, t, h));
+        }
+        float dor[kTok];
+#pragma unroll
+        for (int tt = 0; tt < kTok; ++tt) dor[tt] = active ? to_f32(dO[v_off(d, b, t0 + tt, h) + col]) : 0.f;
+        __syncthreads();
+#pragma unroll 1
+        for (int tt = kTok - 1; tt >= 0; --tt) {
+            // D holds A_{t+1} D_{t+1} (0 past the segment end): D_t = scale
+            // q_t dO_t + D, then the carry A_t D_t into token t - 1
+            const float w = d.scale * dor[tt];
+#pragma unroll
+            for (int i = 0; i < DK; ++i) D[i] = fmaf(w, q_s[tt][i], D[i]);
+            const float al = a_s[tt], be = b_s[tt];
+            float kd = 0.f;
+#pragma unroll
+            for (int i = 0; i < DK; ++i) kd = fmaf(k_s[tt][i], D[i], kd);
+            const float c1 = be * kd;
+#pragma unroll
+            for (int i = 0; i < DK; ++i) D[i] = al * fmaf(-c1, k_s[tt][i], D[i]);
+        }
+    }
+    // after the segment's first token: D = A_a D_a, i.e. gamma
+    if (active) {
+        float* dst = gamma + sum_off(d, seg, b, h) + col;
+#pragma unroll
+        for (int i = 0; i < DK; ++i) dst[int64_t(i) * d.Dv] = D[i];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Summary folds with matrix transitions.  One CTA per (row-head bh, column
+// block); thread = one column of the carried state (DK values in registers).
+//   prefix: S_in[j] = fold over [pre_j, j) of S <- M_i S + dS_i  (from 0)
+//   suffix: dS_out[j] = fold over (j, fol_j) of D <- M_i^T D + gamma_i,
+//           from the last segment down (from 0)
+// M_i [DK][DK] is staged in shared memory per step.
+// ---------------------------------------------------------------------------
+template <int DK, bool SUFFIX>
+__global__ void __launch_bounds__(128) gdr_compose(Dims d, const float* __restrict__ M,
+                                                   const float* __restrict__ X,
+                                                   const int32_t* __restrict__ range,
+                                                   float* __restrict__ out) {
+    __shared__ float m_s[DK][DK + 1];
+    const int bh = blockIdx.x;
+    const int b = bh / d.H, h = bh % d.H;
+    const int col = blockIdx.y * blockDim.x + threadIdx.x;
+    const bool active = col < d.Dv;
+    const int n = d.nseg;
+    float S[DK];
+    float nx[DK];
+    // the fold for segment j restarts whenever its range start (end) moves
+    int cur = SUFFIX ? n : 0;
+#pragma unroll
+    for (int i = 0; i < DK; ++i) S[i] = 0.f;
+    for (int u = 0; u < n; ++u) {
+        const int j = SUFFIX ? n - 1 - u : u;
+        int lim;
+        if (SUFFIX) {
+            lim = range ? __ldg(range + j) : n;
+            lim = lim < j + 1 ? j + 1 : (lim > n ? n : lim);
+        } else {
+            lim = range ? __ldg(range + j) : 0;
+            lim = lim < 0 ? 0 : (lim > j ? j : lim);
+        }
+        if (lim != cur) {  // rebuild the fold over the new range
+#pragma unroll
+            for (int i = 0; i < DK; ++i) S[i] = 0.f;
+            const int i0 = SUFFIX ? lim - 1 : lim;
+            const int i1 = SUFFIX ? j : j;  // exclusive bound in walking order
+            for (int i = i0; SUFFIX ? i > i1 : i < i1; i += SUFFIX ? -1 : 1) {
+                __syncthreads();
+                const float* mi = M + ((int64_t(i) * d.B + b) * d.H + h) * DK * DK;
+                for (int e = threadIdx.x; e < DK * DK; e += blockDim.x) m_s[e / DK][e % DK] = mi[e];
+                __syncthreads();
+                if (active) {
+                    const float* xi = X + sum_off(d, i, b, h) + col;
+#pragma unroll
+                    for (int r = 0; r < DK; ++r) {
+                        float acc = xi[int64_t(r) * d.Dv];
+#pragma unroll
+                        for (int c = 0; c < DK; ++c) acc = fmaf(SUFFIX ? m_s[c][r] : m_s[r][c], S[c], acc);
+                        nx[r] = acc;
+                    }
+#pragma unroll
+                    for (int r = 0; r < DK; ++r) S[r] = nx[r];
+                }
+            }
+            cur = lim;
+        }
+        if (active) {
+            float* dst = out + sum_off(d, j, b, h) + col;
+#pragma unroll
+            for (int r = 0; r < DK; ++r) dst[int64_t(r) * d.Dv] = S[r];
+        }
+        // extend the fold by segment j for the next segment's range
+        __syncthreads();
+        const float* mj = M + ((int64_t(j) * d.B + b) * d.H + h) * DK * DK;
+        for (int e = threadIdx.x; e < DK * DK; e += blockDim.x) m_s[e / DK][e % DK] = mj[e];
+        __syncthreads();
+        if (active) {
+            const float* xj = X + sum_off(d, j, b, h) + col;
+#pragma unroll
+            for (int r = 0; r < DK; ++r) {
+                float acc = xj[int64_t(r) * d.Dv];
+#pragma unroll
+                for (int c = 0; c < DK; ++c) acc = fmaf(SUFFIX ? m_s[c][r] : m_s[r][c], S[c], acc);
+                nx[r] = acc;
+            }
+#pragma unroll
+            for (int r = 0; r < DK; ++r) S[r] = nx[r];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// One step of the recurrence on a state in shared memory (pitch Dv + 1),
+// k, v, alpha, beta of the token given: column owners form k^T S into ks,
+// then row owners update.  All threads of the CTA take part (two barriers).
+// ---------------------------------------------------------------------------
+template <int DK>
+__device__ __forceinline__ void gdr_state_step(float* S, int pitch, int Dv, const float* kt,
+                                               const float* vt, float al, float be, float* ks) {
+    for (int j = threadIdx.x; j < Dv; j += blockDim.x) {
+        float acc = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < DK; ++i) acc = fmaf(kt[i], S[i * pitch + j], acc);
+        ks[j] = acc;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < DK; i += blockDim.x) {
+        const float c = be * kt[i];
+        float* row = S + i * pitch;
+        for (int j = 0; j < Dv; ++j) row[j] = fmaf(al, fmaf(-c, ks[j], row[j]), c * vt[j]);
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// dq sweep: S from S_in in shared memory; per token the state step, then
+// dq_t[i] = scale S_t[i,:] . dO_t by row owners.  Before every kBlk-token
+// block the state is saved to ckpt (the block's starting state).
+// grid (nseg, B*H); block 128 threads.
+// ---------------------------------------------------------------------------
+template <int DK, typename T>
+__global__ void __launch_bounds__(128) gdr_dq_sweep(Dims d, const T* __restrict__ q,
+                                                    const T* __restrict__ k,
+                                                    const T* __restrict__ v,
+                                                    const float* __restrict__ g,
+                                                    const float* __restrict__ beta,
+                                                    const T* __restrict__ dO,
+                                                    const float* __restrict__ S_in,
+                                                    T* __restrict__ dq, float* __restrict__ ckpt) {
+    extern __shared__ float smem[];
+    const int pitch = d.Dv + 1;
+    float* S = smem;                // [DK][pitch]
+    float* ks = S + DK * pitch;     // [Dv]
+    float* vt = ks + d.Dv;          // [Dv]
+    float* dot = vt + d.Dv;         // [Dv]
+    __shared__ float kt[DK];
+    __shared__ float ab[2];
+
+    const int seg = blockIdx.x;
+    const int b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int a0 = seg * d.L;
+    const int nblk = d.L / kBlk;
+    float* ck = ckpt + (((int64_t(seg) * d.B + b) * d.H + h) * nblk) * int64_t(DK) * d.Dv;
+
+    const float* src = S_in + sum_off(d, seg, b, h);
+    for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) S[(e / d.Dv) * pitch + e % d.Dv] = src[e];
+    __syncthreads();
+    for (int t = a0; t < a0 + d.L; ++t) {
+        if ((t - a0) % kBlk == 0) {
+            float* dst = ck + int64_t((t - a0) / kBlk) * DK * d.Dv;
+            for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) dst[e] = S[(e / d.Dv) * pitch + e % d.Dv];
+        }
+        for (int i = threadIdx.x; i < DK; i += blockDim.x) kt[i] = to_f32(k[qk_off(d, b, t, h) + i]);
+        for (int j = threadIdx.x; j < d.Dv; j += blockDim.x) {
+            vt[j] = to_f32(v[v_off(d, b, t, h) + j]);
+            dot[j] = to_f32(dO[v_off(d, b, t, h) + j]);
+        }
+        if (threadIdx.x == 0) {
+            ab[0] = gdr_alpha(d, g, b, t, h);
+            ab[1] = __ldg(beta + g_off(d, b, t, h));
+        }
+        __syncthreads();
+        gdr_state_step<DK>(S, pitch, d.Dv, kt, vt, ab[0], ab[1], ks);
+        for (int i = threadIdx.x; i < DK; i += blockDim.x) {
+            const float* row = S + i * pitch;
+            float acc = 0.f;
+            for (int j = 0; j < d.Dv; ++j) acc = fmaf(row[j], dot[j], acc);
+            dq[qk_off(d, b, t, h) + i] = from_f32<T>(d.scale * acc);
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Reverse sweep.  Shared memory: D and the rebuilt S_{t-1} (pitch Dv + 1),
+// and per-token vectors.  For each kBlk-token block (last first), then each
+// token t of it (last first): S_{t-1} is rebuilt from the block's saved state
+// (t - c steps), D_t = scale q_t dO_t^T + (t at the segment end ? dS_out :
+// A_{t+1} D_{t+1}), and the gradients follow.  grid (nseg, B*H); block 128.
+// ---------------------------------------------------------------------------
+template <int DK, typename T>
+__global__ void __launch_bounds__(128) gdr_reverse_sweep(Dims d, const T* __restrict__ q,
+                                                         const T* __restrict__ k,
+                                                         const T* __restrict__ v,
+                                                         const float* __restrict__ g,
+                                                         const float* __restrict__ beta,
+                                                         const T* __restrict__ dO,
+                                                         const float* __restrict__ dS_out,
+                                                         const float* __restrict__ ckpt,
+                                                         T* __restrict__ dk, T* __restrict__ dv,
+                                                         float* __restrict__ dg,
+                                                         float* __restrict__ dbeta) {
+    extern __shared__ float smem[];
+    const int pitch = d.Dv + 1;
+    float* D = smem;                 // [DK][pitch]
+    float* S = D + DK * pitch;       // [DK][pitch]
+    float* ks = S + DK * pitch;      // [Dv]  k^T S scratch / kS
+    float* w = ks + d.Dv;            // [Dv]  D^T k
+    float* vt = w + d.Dv;            // [Dv]
+    float* dot = vt + d.Dv;          // [Dv]
+    float* vv = dot + d.Dv;          // [Dv]  v of a rebuild step
+    __shared__ float kt[DK], qt[DK], kr[DK];
+    __shared__ float red[2][4];      // per-warp partials: k.u - alpha k.s2, <D, S>
+    __shared__ float ab[2];          // alpha_t, beta_t
+    __shared__ float abr[2];         // alpha, beta of a rebuild step
+
+    const int seg = blockIdx.x;
+    const int b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int a0 = seg * d.L, e0 = a0 + d.L;
+    const int nblk = d.L / kBlk;
+    const float* ck = ckpt + (((int64_t(seg) * d.B + b) * d.H + h) * nblk) * int64_t(DK) * d.Dv;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+
+    // D carries A_{t+1} D_{t+1} between tokens; it starts as dS_out
+    const float* dso = dS_out + sum_off(d, seg, b, h);
+    for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) D[(e / d.Dv) * pitch + e % d.Dv] = dso[e];
+    __syncthreads();
+
+    for (int c = e0 - kBlk; c >= a0; c -= kBlk) {
+        const float* cs = ck + int64_t((c - a0) / kBlk) * DK * d.Dv;
+        for (int t = c + kBlk - 1; t >= c; --t) {
+            // ---- S_{t-1}: the block's saved state advanced over tokens c .. t-1
+            for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) S[(e / d.Dv) * pitch + e % d.Dv] = cs[e];
+            __syncthreads();
+            for (int r = c; r < t; ++r) {
+                for (int i = threadIdx.x; i < DK; i += blockDim.x) kr[i] = to_f32(k[qk_off(d, b, r, h) + i]);
+                for (int j = threadIdx.x; j < d.Dv; j += blockDim.x) vv[j] = to_f32(v[v_off(d, b, r, h) + j]);
+                if (threadIdx.x == 0) {
+                    abr[0] = gdr_alpha(d, g, b, r, h);
+                    abr[1] = __ldg(beta + g_off(d, b, r, h));
+                }
+                __syncthreads();
+                gdr_state_step<DK>(S, pitch, d.Dv, kr, vv, abr[0], abr[1], ks);
+            }
+            // ---- token t's vectors
+            for (int i = threadIdx.x; i < DK; i += blockDim.x) {
+                kt[i] = to_f32(k[qk_off(d, b, t, h) + i]);
+                qt[i] = to_f32(q[q_off(d, b, t, h) + i]);
+            }
+            for (int j = threadIdx.x; j < d.Dv; j += blockDim.x) {
+                vt[j] = to_f32(v[v_off(d, b, t, h) + j]);
+                dot[j] = to_f32(dO[v_off(d, b, t, h) + j]);
+            }
+            if (threadIdx.x == 0) {
+                ab[0] = gdr_alpha(d, g, b, t, h);
+                ab[1] = __ldg(beta + g_off(d, b, t, h));
+            }
+            __syncthreads();
+            const float al = ab[0], be = ab[1];
+            // D_t = scale q_t dO_t^T + (A_{t+1} D_{t+1}, already in D)
+            for (int i = threadIdx.x; i < DK; i += blockDim.x) {
+                const float qi = d.scale * qt[i];
+                float* row = D + i * pitch;
+                for (int j = 0; j < d.Dv; ++j) row[j] = fmaf(qi, dot[j], row[j]);
+            }
+            __syncthreads();
+            // column owners: w = D_t^T k_t, kS = S_{t-1}^T k_t; dv = beta w
+            for (int j = threadIdx.x; j < d.Dv; j += blockDim.x) {
+                float a1 = 0.f, a2 = 0.f;
+#pragma unroll 8
+                for (int i = 0; i < DK; ++i) {
+                    a1 = fmaf(kt[i], D[i * pitch + j], a1);
+                    a2 = fmaf(kt[i], S[i * pitch + j], a2);
+                }
+                w[j] = a1;
+                ks[j] = a2;
+                dv[v_off(d, b, t, h) + j] = from_f32<T>(be * a1);
+            }
+            __syncthreads();
+            // row owners: u = D_t v_t, s1 = S_{t-1} w, s2 = D_t kS, <D, S> row part
+            float p_kb = 0.f, p_ds = 0.f;
+            for (int i = threadIdx.x; i < DK; i += blockDim.x) {
+                const float* dr = D + i * pitch;
+                const float* sr = S + i * pitch;
+                float u = 0.f, s1 = 0.f, s2 = 0.f, ds = 0.f;
+                for (int j = 0; j < d.Dv; ++j) {
+                    u = fmaf(dr[j], vt[j], u);
+                    s1 = fmaf(sr[j], w[j], s1);
+                    s2 = fmaf(dr[j], ks[j], s2);
+                    ds = fmaf(dr[j], sr[j], ds);
+                }
+                dk[qk_off(d, b, t, h) + i] = from_f32<T>(be * u - al * be * (s1 + s2));
+                p_kb = fmaf(kt[i], u - al * s2, p_kb);
+                p_ds += ds - be * kt[i] * s2;
+            }
+            p_kb = warp_sum(p_kb);
+            p_ds = warp_sum(p_ds);
+            if (lane == 0) {
+                red[0][wid] = p_kb;
+                red[1][wid] = p_ds;
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                float s_kb = 0.f, s_ds = 0.f;
+                for (int u2 = 0; u2 < int(blockDim.x >> 5); ++u2) {
+                    s_kb += red[0][u2];
+                    s_ds += red[1][u2];
+                }
+                dbeta[g_off(d, b, t, h)] = s_kb;
+                dg[g_off(d, b, t, h)] = starts_sequence(d.seq_idx, t) ? 0.f : al * s_ds;
+            }
+            // D <- A_t D_t = alpha (D - beta k w^T), the carry into token t-1
+            for (int i = threadIdx.x; i < DK; i += blockDim.x) {
+                const float cc = be * kt[i];
+                float* row = D + i * pitch;
+                for (int j = 0; j < d.Dv; ++j) row[j] = al * fmaf(-cc, w[j], row[j]);
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <typename T>
+rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s) {
+    const int BH = d.B * d.H;
+    const T* q = static_cast<const T*>(p.q);
+    const T* k = static_cast<const T*>(p.k);
+    const T* v = static_cast<const T*>(p.v);
+    const T* dO = static_cast<const T*>(p.dO);
+    int launches = 1;
+
+#define RMCP_GDR_DK_SWITCH(...)                                   \
+    switch (d.Dk) {                                               \
+        case 16: { constexpr int DK = 16; __VA_ARGS__; break; }   \
+        case 32: { constexpr int DK = 32; __VA_ARGS__; break; }   \
+        case 64: { constexpr int DK = 64; __VA_ARGS__; break; }   \
+        default: return RM_ERR_UNSUPPORTED;                       \
+    }
+
+    auto colgrid = [&](int ncol, int* threads) {
+        *threads = ncol >= 128 ? 128 : ((ncol + 31) / 32) * 32;
+        return dim3(d.nseg, BH, (ncol + *threads - 1) / *threads);
+    };
+    switch (op) {
+        case GdrOp::kPrepare: {
+            int th;
+            const dim3 grid = colgrid(d.Dv + d.Dk, &th);
+            RMCP_GDR_DK_SWITCH((gdr_column_sweep<DK, kGdrPrepare, T><<<grid, th, 0, s>>>(
+                d, nullptr, k, v, p.g, p.beta, nullptr, nullptr, p.M, p.dS)));
+            break;
+        }
+        case GdrOp::kApply: {
+            int th;
+            const dim3 grid = colgrid(d.Dv, &th);
+            RMCP_GDR_DK_SWITCH((gdr_column_sweep<DK, kGdrApply, T><<<grid, th, 0, s>>>(
+                d, q, k, v, p.g, p.beta, p.S_in, static_cast<T*>(p.o), nullptr, nullptr)));
+            break;
+        }
+        case GdrOp::kComposePrefix:
+        case GdrOp::kComposeSuffix: {
+            const int th = d.Dv >= 128 ? 128 : ((d.Dv + 31) / 32) * 32;
+            const dim3 grid(BH, (d.Dv + th - 1) / th);
+            if (op == GdrOp::kComposePrefix) {
+                RMCP_GDR_DK_SWITCH((gdr_compose<DK, false><<<grid, th, 0, s>>>(
+                    d, p.M, p.dS, d.preceding_start, p.S_in_out)));
+            } else {
+                RMCP_GDR_DK_SWITCH((gdr_compose<DK, true><<<grid, th, 0, s>>>(
+                    d, p.M, p.gamma, d.following_stop, p.dS_out_out)));
+            }
+            break;
+        }
+        case GdrOp::kBackwardPrepare: {
+            int th;
+            const dim3 grid = colgrid(d.Dv, &th);
+            RMCP_GDR_DK_SWITCH((gdr_gamma_sweep<DK, T><<<grid, th, 0, s>>>(d, q, k, p.g, p.beta, dO, p.gamma_out)));
+            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+            const size_t smem = sizeof(float) * (size_t(d.Dk) * (d.Dv + 1) + 3 * size_t(d.Dv));
+            RMCP_GDR_DK_SWITCH({
+                auto fn = gdr_dq_sweep<DK, T>;
+                if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+                    return RM_ERR_CUDA;
+                fn<<<dim3(d.nseg, BH), 128, smem, s>>>(d, q, k, v, p.g, p.beta, dO, p.S_in,
+                                                       static_cast<T*>(p.dq), p.ws);
+            });
+            launches = 2;
+            break;
+        }
+        case GdrOp::kBackwardApply: {
+            const size_t smem = sizeof(float) * (2 * size_t(d.Dk) * (d.Dv + 1) + 5 * size_t(d.Dv));
+            RMCP_GDR_DK_SWITCH({
+                auto fn = gdr_reverse_sweep<DK, T>;
+                if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+                    return RM_ERR_CUDA;
+                fn<<<dim3(d.nseg, BH), 128, smem, s>>>(d, q, k, v, p.g, p.beta, dO, p.dS_out, p.ws,
+                                                       static_cast<T*>(p.dk), static_cast<T*>(p.dv), p.dg,
+                                                       p.dbeta);
+            });
+            break;
+        }
+    }
+#undef RMCP_GDR_DK_SWITCH
+    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    note_launch(launches);
+    return RM_OK;
+}
+
+}  // namespace
+
+bool gdr_supports(const Dims& d) {
+    return (d.Dk == 16 || d.Dk == 32 || d.Dk == 64) && d.Dv % 8 == 0 && d.Dv >= 8 && d.Dv <= 128 &&
+           d.L % kBlk == 0 && !d.vg;
+}
+
+size_t gdr_workspace_bytes(const Dims& d) {
+    const size_t b = size_t(d.B) * d.H * (size_t(d.T) / kBlk) * d.Dk * d.Dv * sizeof(float);
+    return (b + 255) / 256 * 256;
+}
+
+rm_status launch_gdr(GdrOp op, const Dims& d, rm_dtype dt, const GdrPtrs& p, cudaStream_t s) {
+    return dt == RM_F32 ? launch_gdr_T<float>(op, d, p, s) : launch_gdr_T<__nv_bfloat16>(op, d, p, s);
+}
+
+}  // namespace rmcp

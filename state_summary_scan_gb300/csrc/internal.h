@@ -35,6 +35,35 @@ void note_launch(int n);
 bool generic_supports(const Dims& d);
 rm_status launch_generic(Op op, const Dims& d, rm_dtype dt, const Ptrs& p, cudaStream_t s);
 
+// gated delta rule (gdr_kernels.cu)
+enum class GdrOp { kPrepare, kComposePrefix, kApply, kBackwardPrepare, kComposeSuffix, kBackwardApply };
+struct GdrPtrs {
+    const void* q = nullptr;
+    const void* k = nullptr;
+    const void* v = nullptr;
+    const void* dO = nullptr;
+    const float* g = nullptr;
+    const float* beta = nullptr;
+    float* M = nullptr;           // [nseg,B,H,Dk,Dk]: written by kPrepare, read by the folds
+    float* dS = nullptr;          // written by kPrepare, read by kComposePrefix
+    const float* S_in = nullptr;  // read by kApply, kBackwardPrepare
+    float* S_in_out = nullptr;    // written by kComposePrefix
+    const float* gamma = nullptr; // read by kComposeSuffix
+    float* gamma_out = nullptr;   // written by kBackwardPrepare
+    const float* dS_out = nullptr;  // read by kBackwardApply
+    float* dS_out_out = nullptr;  // written by kComposeSuffix
+    void* o = nullptr;
+    void* dq = nullptr;
+    void* dk = nullptr;
+    void* dv = nullptr;
+    float* dg = nullptr;
+    float* dbeta = nullptr;
+    float* ws = nullptr;          // saved states: kBackwardPrepare -> kBackwardApply
+};
+bool gdr_supports(const Dims& d);
+size_t gdr_workspace_bytes(const Dims& d);
+rm_status launch_gdr(GdrOp op, const Dims& d, rm_dtype dt, const GdrPtrs& p, cudaStream_t s);
+
 // vector (per key dimension) gates on the generic path (vg_kernels.cu)
 rm_status launch_vg(Op op, const Dims& d, rm_dtype dt, const Ptrs& p, cudaStream_t s);
 

@@ -25,7 +25,7 @@ def declared_entry_points():
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names |= set(re.findall(r"\b(rm_(?:cp|ssd)_\w+)\s*\(", text))
+            names |= set(re.findall(r"\b(rm_(?:cp|ssd|gdr)_\w+)\s*\(", text))
     return sorted(names)
 
 

@@ -1,0 +1,100 @@
+"""GPU parity of the gated delta rule against the fp64 oracle.
+
+S_t = exp(g_t)(I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T, o_t = scale
+S_t^T q_t, run through the rm_gdr_* calls: each segment's summary is the
+general affine map S_out = M S_in + delta_S of the Megatron-Core page with a
+Dk x Dk transition M, composed as M S + dS forward and M^T D + gamma
+backward.  Outputs, gradients (q, k, v, g, beta) and the forward summaries
+(M, delta_S, S_in) are compared element by element with oracle.gdr_forward /
+gdr_backward / gdr_forward_prepare / gdr_compose_prefix: max|gpu - ref| <=
+tol * max|ref| per tensor, tol = 1e-4 for fp32 storage and 2e-2 for bf16."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_summary_scan_gb300 import _capi as C
+from state_summary_scan_gb300 import api
+
+from _parity import compare, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    C.load()
+
+
+def gdr_inputs(B, T, H, Dk, Dv, dtype, seed=0, qh=0):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, T, qh or H, Dk, generator=gen)
+    k = torch.randn(B, T, H, Dk, generator=gen)
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn(B, T, H, Dv, generator=gen)
+    g = torch.nn.functional.logsigmoid(torch.randn(B, T, H, generator=gen) + 3.0)
+    beta = torch.sigmoid(torch.randn(B, T, H, generator=gen))
+    dO = torch.randn(B, T, H, Dv, generator=gen)
+    return q.to(dtype), k.to(dtype), v.to(dtype), g, beta, dO.to(dtype)
+
+
+def run_case(B, T, H, Dk, Dv, dtype, nseg, cu=None, qh=0, seed=0):
+    q, k, v, g, beta, dO = gdr_inputs(B, T, H, Dk, Dv, dtype, seed, qh)
+    scale = 1.0 / math.sqrt(Dk)
+    dev = "cuda"
+    qd, kd, vd, gd, bd, dOd = (t.to(dev).contiguous() for t in (q, k, v, g, beta, dO))
+    plan = api.make_gdr_plan(B, T, H, Dk, Dv, nseg, 16, scale, dtype, cu, dev, q_heads=qh)
+    o = api.gdr_forward(plan, qd, kd, vd, gd, bd)
+    grads = api.gdr_backward(plan, qd, kd, vd, gd, bd, dOd)
+    torch.cuda.synchronize()
+    gpu = {n: t.detach().to("cpu", torch.float64).numpy() for n, t in
+           zip(("o", "dq", "dk", "dv", "dg", "dbeta", "M", "dS", "S_in"),
+               (o,) + tuple(grads) + (plan.M, plan.dS, plan.S_in))}
+    seg = oracle.equal_segments(T, nseg)
+    si = None
+    if cu is not None:
+        si = oracle.packed_metadata(cu, T, seg)["seq_idx"]
+    qf = q.repeat_interleave(H // qh, dim=2) if qh else q
+    ref = dict(o=oracle.gdr_forward(qf, k, v, g, beta, scale, si))
+    ref.update(zip(("dq", "dk", "dv", "dg", "dbeta"), oracle.gdr_backward(qf, k, v, g, beta, dO, scale, si)))
+    ref["M"], ref["dS"] = oracle.gdr_forward_prepare(k, v, g, beta, seg, si)
+    keys = ("o", "dq", "dk", "dv", "dg", "dbeta", "M", "dS")
+    if cu is None:  # with resets the prefixes start at preceding_start (M = 0 makes them agree)
+        ref["S_in"] = oracle.gdr_compose_prefix(ref["M"], ref["dS"])
+        keys += ("S_in",)
+    return compare(gpu, ref, tol_for(dtype), keys)
+
+
+def test_gdr_small_fp32():
+    run_case(1, 128, 2, 16, 16, torch.float32, nseg=4)
+
+
+def test_gdr_rectangular_heads_many_blocks():
+    # Dv != Dk, 64-token segments (four saved states each), two rows
+    run_case(2, 256, 2, 32, 48, torch.float32, nseg=4, seed=1)
+
+
+def test_gdr_packed_resets():
+    cu = [0, 1, 2, 17, 31, 64, 65, 100, 127, 128]
+    run_case(1, 128, 2, 16, 16, torch.float32, nseg=4, cu=cu, seed=2)
+
+
+def test_gdr_single_segment_and_shared_queries():
+    run_case(1, 64, 4, 16, 16, torch.float32, nseg=1, qh=2, seed=3)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_gdr_wide(dtype):
+    run_case(1, 256, 2, 64, 64, dtype, nseg=4, seed=4)
+
+
+def test_gdr_rejects_unsupported_shapes():
+    bad = C.ProblemSpec(1, 128, 2, 128, 16, 4, 16, 0.1, torch.float32)  # Dk = 128
+    t = torch.zeros(16, device="cuda")
+    with pytest.raises(C.RmCpError) as e:
+        C.rm_gdr_forward_prepare(bad, t, t, t, t, t, t)
+    assert e.value.status == 4
