@@ -37,8 +37,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from state_summary_scan_gb300.workloads import (SSD_WORKLOADS, WORKLOADS, make_inputs,  # noqa: E402
-                                                 make_ssd_inputs)
+from state_summary_scan_gb300.workloads import (GDR_WORKLOADS, SSD_WORKLOADS, WORKLOADS,  # noqa: E402
+                                                 make_gdr_inputs, make_inputs, make_ssd_inputs)
 
 METRIC = "fwd+bwd tokens/sec on 1 GB300; % of bf16 tensor/HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -455,9 +455,12 @@ def run_ours(args, rank, world, local_rank):
         line[key] = head[key]
     if args.workload == HEADLINE and not args.T and not args.headline_only:
         subs = {}
-        for name in SUB_WORKLOADS:
-            r = measure_workload(WORKLOADS[name], args, rank, world, dev, peaks, peak_src,
-                                 with_e2e=False, with_cpu=False)
+        for name in SUB_WORKLOADS + tuple(GDR_WORKLOADS):
+            if name in GDR_WORKLOADS:
+                r = measure_gdr(GDR_WORKLOADS[name], args, rank, world, dev, peaks, peak_src, False)
+            else:
+                r = measure_workload(WORKLOADS[name], args, rank, world, dev, peaks, peak_src,
+                                     with_e2e=False, with_cpu=False)
             subs[name] = {key: r[key] for key in ("value", "fwd_value", "unit", "mode", "ms_per_step",
                                                  "fwd_ms_per_step", "dtype", "config", "roofline",
                                                  "path_roofline", "fwd_path_roofline",
@@ -642,8 +645,182 @@ def reference_budget(args) -> float:
     return max(0.05, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
 
 
+# ------------------------------------------------------------------ gated delta rule
+
+GDR_PHASES_FWD = ("gdr_forward_prepare", "gdr_compose_prefix", "gdr_forward_apply")
+GDR_PHASES_BWD = ("gdr_backward_prepare", "gdr_compose_suffix", "gdr_backward_apply")
+
+
+def gdr_kernel_alu_flops(w, phase):
+    """fp32 flops one launch of the generic gated-delta-rule kernels performs,
+    per token and head as the kernels run them (multiply-add = 2): the state
+    step is k^T S then the rank-one correction (about 6 Dk Dv), the prepare
+    also walks M's Dk columns, the reverse sweep rebuilds S_{t-1} from the
+    state saved every 16 tokens (7.5 steps on average) before its gradients."""
+    ntok = w.B * w.T * w.H
+    kd = w.Dk * w.Dv
+    per = {"gdr_forward_prepare": 6 * w.Dk * (w.Dv + w.Dk), "gdr_forward_apply": 8 * kd,
+           "gdr_backward_prepare": 16 * kd, "gdr_backward_apply": 62 * kd,
+           "gdr_compose_prefix": 0, "gdr_compose_suffix": 0}[phase]
+    return ntok * per
+
+
+def gdr_path_roofline(w, peaks):
+    """The method's step: read q, k, v, g, beta (and dO), write o (and dq, dk,
+    dv, dg, dbeta); summaries M (Dk x Dk) and delta_S written, read by the
+    fold, S_in written and read (both directions).  Flops: the chunkwise form
+    of the scalar gate plus the per-chunk K K^T and triangular solve of the
+    delta rule (2 C Dk a token each way)."""
+    e = 4 if w.dtype == "f32" else 2
+    C, Dk, Dv = w.chunk, w.Dk, w.Dv
+    ntok = w.B * w.T * w.H
+    nsum = w.num_segments * w.B * w.H
+    summ = 16 * Dk * Dv + 8 * Dk * Dk
+    byts = (ntok * (e * (2 * Dk + Dv) + 8 + e * Dv) + nsum * summ
+            + ntok * (2 * e * (2 * Dk + Dv) + e * Dv + 16) + nsum * summ)
+    flops = ntok * (C * (3 * Dk + Dv) + 4 * Dk * Dv) + ntok * (C * (5 * Dk + 2 * Dv) + 8 * Dk * Dv)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    fwd_b = ntok * (e * (2 * Dk + Dv) + 8 + e * Dv) + nsum * summ
+    return dict(flops=flops, bytes=byts, bound="hbm" if t_hbm >= t_tc else "tensor",
+                t_roofline_us=max(t_tc, t_hbm) * 1e6, t_fwd_roofline_us=fwd_b / (peaks["hbm_gbs"] * 1e9) * 1e6)
+
+
+def gdr_cpu_baseline(w, inp, target_s=12.0):
+    import oracle
+    cores = oracle.set_threads(0)
+
+    def run(n):
+        sl = slice(0, n)
+        args = [oracle._f64(x[:, sl]) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)]
+        dO = oracle._f64(inp.dO[:, sl])
+        t0 = time.perf_counter()
+        oracle.gdr_forward(*args, w.scale)
+        oracle.gdr_backward(*args, dO, w.scale)
+        return time.perf_counter() - t0
+
+    per_tok = max(run(64) / 64, 1e-9)
+    n = max(64, min(w.T, int(target_s / per_tok) // 64 * 64))
+    dt = run(n)
+    return {"value": w.B * n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 gated-delta-rule oracle fwd+bwd on the first {n} of {w.T} tokens of all "
+                      f"{w.B} rows x {w.H} heads, {dt:.1f} s wall", "seconds": dt}
+
+
+def measure_gdr(w, args, rank, world, dev, peaks, peak_src, with_cpu):
+    from state_summary_scan_gb300 import _capi as C
+    from state_summary_scan_gb300 import api
+
+    inp = make_gdr_inputs(w)
+    q, k, v, g, beta, dO = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.g, inp.beta, inp.dO))
+    plan = api.make_gdr_plan(w.B, w.T, w.H, w.Dk, w.Dv, w.num_segments, w.chunk, w.scale,
+                             w.torch_dtype, device=dev)
+    s = plan.spec
+    o = torch.empty_like(v)
+    dq, dk, dv = torch.empty_like(k), torch.empty_like(k), torch.empty_like(v)
+    dg, db = torch.empty_like(g), torch.empty_like(beta)
+    stream = torch.cuda.current_stream(dev)
+    fns = {
+        "gdr_forward_prepare": lambda: C.rm_gdr_forward_prepare(s, k, v, g, beta, plan.M, plan.dS, stream),
+        "gdr_compose_prefix": lambda: C.rm_gdr_compose_prefix(s, plan.M, plan.dS, plan.S_in, stream),
+        "gdr_forward_apply": lambda: C.rm_gdr_forward_apply(s, q, k, v, g, beta, plan.S_in, o, stream),
+        "gdr_backward_prepare": lambda: C.rm_gdr_backward_prepare(s, q, k, v, g, beta, plan.S_in, dO,
+                                                                  plan.gamma, dq, plan.ws, stream),
+        "gdr_compose_suffix": lambda: C.rm_gdr_compose_suffix(s, plan.M, plan.gamma, plan.dS_out, stream),
+        "gdr_backward_apply": lambda: C.rm_gdr_backward_apply(s, q, k, v, g, beta, dO, plan.dS_out, dk, dv,
+                                                              dg, db, plan.ws, stream),
+    }
+    phases = GDR_PHASES_FWD + GDR_PHASES_BWD
+    steps = max(3, min(args.steps, 20))  # a step takes milliseconds on the generic kernels
+    for _ in range(args.warmup):
+        for ph in phases:
+            fns[ph]()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local_rank_of(dev))
+    clocks.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)] for _ in range(steps)]
+    l0 = C.rm_cp_launch_count()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        for j, ph in enumerate(phases):
+            ev[i][j].record(stream)
+            fns[ph]()
+        ev[i][len(phases)].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = C.rm_cp_launch_count() - l0
+    fs, fe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fs.record(stream)
+    for _ in range(steps):
+        for ph in GDR_PHASES_FWD:
+            fns[ph]()
+    fe.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = replica_time(start.elapsed_time(end), world, dev) / steps
+    fwd_ms = replica_time(fs.elapsed_time(fe), world, dev) / steps
+    phase_ms = {ph: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
+                for j, ph in enumerate(phases)}
+    dom = max(phase_ms, key=phase_ms.get)
+    fl = gdr_kernel_alu_flops(w, dom)
+    ach = fl / (phase_ms[dom] / 1e3) / 1e12
+    pr = gdr_path_roofline(w, peaks)
+    tok = w.B * w.T
+    return {
+        "value": replica_throughput(world, tok, ms), "fwd_value": replica_throughput(world, tok, fwd_ms),
+        "unit": "tokens/s", "mode": "fwd+bwd", "ms_per_step": ms, "fwd_ms_per_step": fwd_ms, "dtype": "f32",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
+                   "num_segments": w.num_segments, "storage": w.dtype, "mode": "fwd+bwd",
+                   "recurrence": "gated delta rule", "kernel_path": "simt-fp32", "steps": steps,
+                   "l2": "inputs larger than L2, no flush"},
+        "roofline": {"bound": "alu", "kernel": dom, "achieved": ach, "peak": FP32_ALU_TFLOPS,
+                     "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS, "alu_flops": fl,
+                     "launch_us": phase_ms[dom] * 1e3, "traffic": None,
+                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2070 MHz"},
+        "path_roofline": {"bound": pr["bound"], "t_roofline_us": pr["t_roofline_us"],
+                          "t_measured_us": ms * 1e3, "frac": pr["t_roofline_us"] / (ms * 1e3),
+                          "flops": pr["flops"], "bytes": pr["bytes"], "peak_source": peak_src,
+                          "phases_us": {ph: round(t * 1e3, 2) for ph, t in phase_ms.items()}},
+        "fwd_path_roofline": {"t_roofline_us": pr["t_fwd_roofline_us"], "t_measured_us": fwd_ms * 1e3,
+                              "frac": pr["t_fwd_roofline_us"] / (fwd_ms * 1e3)},
+        "cpu_baseline": gdr_cpu_baseline(w, inp, args.cpu_seconds) if with_cpu else None,
+        "e2e": None, "gpu_launches": int(launches), "clocks": clk,
+    }
+
+
+def run_gdr(args, rank, world, local_rank):
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks, peak_src = load_peaks()
+    r = measure_gdr(GDR_WORKLOADS[args.workload], args, rank, world, dev, peaks, peak_src,
+                    rank == 0 and world == 1 and not args.no_cpu_baseline)
+    line = {"metric": METRIC, "n_gpus": world, "steps": r["config"]["steps"], "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "data": "synthetic (seeded gated-delta-rule inputs)"}
+    line.update(r)
+    return line
+
+
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm, timed per step on host cores."""
+    if args.workload in GDR_WORKLOADS:
+        w = GDR_WORKLOADS[args.workload]
+        inp = make_gdr_inputs(w)
+        budget = reference_budget(args)
+        runs = [gdr_cpu_baseline(w, inp, budget) for _ in range(args.steps)]
+        value = statistics.mean(r["value"] for r in runs)
+        return {
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.B * w.T / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk,
+                                            "Dv": w.Dv, "num_segments": w.num_segments, "mode": "fwd+bwd",
+                                            "recurrence": "gated delta rule"},
+            "cpu_baseline": dict(runs[-1], value=value),
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0,
+        }
     if args.workload in SSD_WORKLOADS:
         w = SSD_WORKLOADS[args.workload]
         inp = make_ssd_inputs(w)
@@ -706,7 +883,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + sorted(SSD_WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=sorted(WORKLOADS) + sorted(SSD_WORKLOADS) + sorted(GDR_WORKLOADS))
     ap.add_argument("--headline-only", action="store_true",
                     help="time only the chosen workload (no 'workloads' object)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -726,13 +904,14 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
-    if args.workload in SSD_WORKLOADS and args.T:
+    if (args.workload in SSD_WORKLOADS or args.workload in GDR_WORKLOADS) and args.T:
         ap.error("--T applies to the gated-recurrence workloads only")
 
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        run = run_ssd if args.workload in SSD_WORKLOADS else run_ours
+        run = (run_ssd if args.workload in SSD_WORKLOADS
+               else run_gdr if args.workload in GDR_WORKLOADS else run_ours)
         line = run(args, rank, world, local_rank)
         if rank == 0:
             print(json.dumps(line), flush=True)

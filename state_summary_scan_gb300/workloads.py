@@ -201,3 +201,63 @@ def make_ssd_inputs(w: SsdWorkload) -> SsdInputs:
     dy = torch.randn(w.B, w.T, w.H, w.P, generator=gen)
     d = w.torch_dtype
     return SsdInputs(x.to(d), dt.contiguous(), A, Bm.to(d), Cm.to(d), D, dy.to(d))
+
+
+# ------------------------------------------------------------------ gated delta rule
+# The pages name the gated delta rule (its summaries carry a Dk x Dk
+# transition) but give no workload for it.  This one has 8192 tokens, 16
+# heads, Dk = Dv = 64 (the head size its generic kernels take) and 16
+# segments of 512 tokens.  Recipe (one torch CPU generator, seed 0, this draw
+# order): q ~ N(0,1); k ~ N(0,1) L2-normalised per (token, head); v ~ N(0,1);
+# g = logsigmoid(N(0,1) + 4); beta = sigmoid(N(0,1)); dO ~ N(0,1); q, k, v, dO
+# rounded to the dtype.
+
+@dataclasses.dataclass(frozen=True)
+class GdrWorkload:
+    name: str
+    B: int
+    T: int
+    H: int
+    Dk: int
+    Dv: int
+    dtype: str
+    num_segments: int
+    chunk: int = 16
+    gate_shift: float = 4.0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.Dk)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+
+GDR_WORKLOADS = {
+    "gdr8k": GdrWorkload("gdr8k", B=1, T=8192, H=16, Dk=64, Dv=64, dtype="bf16", num_segments=16),
+}
+
+
+@dataclasses.dataclass
+class GdrInputs:
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    g: torch.Tensor
+    beta: torch.Tensor
+    dO: torch.Tensor
+
+
+def make_gdr_inputs(w: GdrWorkload) -> GdrInputs:
+    gen = torch.Generator("cpu").manual_seed(w.seed)
+    q = torch.randn(w.B, w.T, w.H, w.Dk, generator=gen)
+    k = torch.randn(w.B, w.T, w.H, w.Dk, generator=gen)
+    k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+    v = torch.randn(w.B, w.T, w.H, w.Dv, generator=gen)
+    g = torch.nn.functional.logsigmoid(torch.randn(w.B, w.T, w.H, generator=gen) + w.gate_shift)
+    beta = torch.sigmoid(torch.randn(w.B, w.T, w.H, generator=gen))
+    dO = torch.randn(w.B, w.T, w.H, w.Dv, generator=gen)
+    d = w.torch_dtype
+    return GdrInputs(q.to(d), k.to(d), v.to(d), g.contiguous(), beta.contiguous(), dO.to(d))
