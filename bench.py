@@ -776,7 +776,7 @@ def measure_gdr(w, args, rank, world, dev, peaks, peak_src, with_cpu):
                    "l2": "inputs larger than L2, no flush"},
         "roofline": {"bound": "alu", "kernel": dom, "achieved": ach, "peak": FP32_ALU_TFLOPS,
                      "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS, "alu_flops": fl,
-                     "launch_us": phase_ms[dom] * 1e3, "traffic": None,
+                     "launch_us": phase_ms[dom] * 1e3, "traffic": load_traffic(w.name, dom),
                      "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2070 MHz"},
         "path_roofline": {"bound": pr["bound"], "t_roofline_us": pr["t_roofline_us"],
                           "t_measured_us": ms * 1e3, "frac": pr["t_roofline_us"] / (ms * 1e3),
