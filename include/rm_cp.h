@@ -101,7 +101,9 @@ typedef enum { RM_F32 = 0, RM_BF16 = 1 } rm_dtype;
  *                    M^T = M -- stored as its diagonal, M [nseg,B,H,Dk]; the
  *                    compositions apply it row by row, and the workspace
  *                    holds one fp32 value per (row, token, head, key
- *                    dimension).  Runs on the generic fp32-arithmetic kernels.
+ *                    dimension).  bf16 storage with Dk = Dv = 128 runs on
+ *                    the tensor cores; other shapes and fp32 storage on the
+ *                    generic fp32-arithmetic kernels.
  * Out-of-range metadata values are clamped on the device to [0, j] and
  * [j+1, num_segments]; rm_cp_build_packed_metadata produces valid ones.
  */
@@ -499,7 +501,9 @@ uint64_t rm_cp_launch_count(void);
  * every call, 1 = tensor-core (tcgen05) path for every call, 2 = tensor-core
  * path for some calls and the generic path for the others.  -1 for an
  * invalid problem.  The tensor-core path serves bf16 storage with Dk = 128,
- * Dv in {128, 256} and segment lengths that are multiples of 64. */
+ * Dv in {128, 256} and segment lengths that are multiples of 64; with vector
+ * gates, bf16 storage with Dk = Dv = 128 and segment lengths that are
+ * multiples of 64 (other vector-gate problems run on the generic path). */
 int32_t rm_cp_path(const rm_cp_problem* p);
 
 #ifdef __cplusplus

@@ -66,6 +66,10 @@ rm_status launch_gdr(GdrOp op, const Dims& d, rm_dtype dt, const GdrPtrs& p, cud
 
 // vector (per key dimension) gates on the generic path (vg_kernels.cu)
 rm_status launch_vg(Op op, const Dims& d, rm_dtype dt, const Ptrs& p, cudaStream_t s);
+// vector gates on the tensor-core path (vgtc_kernels.cu)
+bool vgtc_supports(const Dims& d, rm_dtype dt);
+rm_status launch_vgtc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s);
+rm_status vgtc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cudaStream_t s);
 
 // host-side checks and launches of rm_cp_host.cu, for other entry points
 rm_status api_check_problem(const rm_cp_problem* p, Dims* d);

@@ -112,7 +112,8 @@ size_t workspace_bytes(const rmcp::Dims& d, rm_dtype dt) {
 rm_status launch(rmcp::Op op, const rm_cp_problem* p, const rmcp::Dims& d, const rmcp::Ptrs& ptrs,
                  rm_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    rm_status st = d.vg ? rmcp::launch_vg(op, d, p->dtype, ptrs, s)
+    rm_status st = d.vg ? (rmcp::vgtc_supports(d, p->dtype) ? rmcp::launch_vgtc(op, d, ptrs, s)
+                                                            : rmcp::launch_vg(op, d, p->dtype, ptrs, s))
                    : rmcp::tc_supports_op(op, d, p->dtype)
                        ? rmcp::launch_tc(op, d, ptrs, s)
                        : rmcp::launch_generic(op, d, p->dtype, ptrs, s);
@@ -159,12 +160,15 @@ uint64_t rm_cp_launch_count(void) { return rmcp::g_launches.load(std::memory_ord
 
 rm_status rm_cp_device_status(int32_t* dev_scratch, int32_t clear, rm_stream_t stream) {
     RM_NEED(dev_scratch);
-    int flag = 0;
+    // each tensor-core translation unit keeps its own flag
+    int flag = 0, vflag = 0;
     rm_status st = rmcp::tc_read_timeout_flag(&flag, clear, dev_scratch,
                                               reinterpret_cast<cudaStream_t>(stream));
+    if (st == RM_OK)
+        st = rmcp::vgtc_read_timeout_flag(&vflag, clear, dev_scratch, reinterpret_cast<cudaStream_t>(stream));
     if (st != RM_OK)
         return fail(st, "device status read failed: %s", cudaGetErrorString(cudaGetLastError()));
-    if (flag) return fail(RM_ERR_TIMEOUT, "a bounded device-side wait ran out");
+    if (flag || vflag) return fail(RM_ERR_TIMEOUT, "a bounded device-side wait ran out");
     return RM_OK;
 }
 
@@ -184,6 +188,7 @@ rm_status rm_cp_validate(const rm_cp_problem* p) {
 int32_t rm_cp_path(const rm_cp_problem* p) {
     rmcp::Dims d;
     if (check_problem(p, &d) != RM_OK) return -1;
+    if (d.vg) return rmcp::vgtc_supports(d, p->dtype) ? 1 : 0;
     int n = 0;
     for (rmcp::Op op : {rmcp::Op::kForwardPrepare, rmcp::Op::kForwardApply,
                         rmcp::Op::kBackwardPrepare, rmcp::Op::kBackwardApply})

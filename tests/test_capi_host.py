@@ -238,15 +238,19 @@ def test_problem_spec_cache_builds_metadata_once_and_shares_no_buffers():
 
 
 def test_vector_gates_validation_and_sizes():
-    """vector_gates is 0 or 1; vector gates run on the generic kernels (path 0
-    even for shapes the tensor-core path serves), the workspace holds one value
-    per key dimension, and the SSD calls (one gate per head) refuse them."""
+    """vector_gates is 0 or 1; vector gates take the tensor-core path for bf16
+    with Dk = Dv = 128 and the generic kernels otherwise, the workspace holds
+    one value per key dimension, and the SSD calls (one gate per head) refuse
+    them."""
     w = WORKLOADS["32k"]
     base = dict(B=w.B, T=w.T, H=w.H, Dk=w.Dk, Dv=w.Dv, num_segments=w.num_segments,
                 chunk=w.chunk, scale=w.scale, dtype=1)
     assert C.rm_cp_path(C.ProblemSpec(**base)) == 1
     vg = C.ProblemSpec(**base, vector_gates=1)
-    assert C.rm_cp_path(vg) == 0
+    assert C.rm_cp_path(vg) == 1
+    assert C.rm_cp_path(C.ProblemSpec(**dict(base, dtype=0), vector_gates=1)) == 0
+    assert C.rm_cp_path(C.ProblemSpec(**dict(base, Dv=256), vector_gates=1)) == 0
+    assert C.rm_cp_path(C.ProblemSpec(**dict(base, T=w.T - 16 * 32, chunk=32), vector_gates=1)) == 0
     ntok = w.B * w.T * w.H
     assert C.rm_cp_workspace_size(vg) >= ntok * w.Dk * 4
     assert C.rm_cp_workspace_size(vg) < ntok * w.Dk * 4 + 256

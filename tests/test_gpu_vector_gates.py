@@ -3,7 +3,9 @@
 With g [B,T,H,Dk] the recurrence is S_t = diag(exp(g_t)) S_{t-1} + k_t v_t^T
 and each segment's transition is the diagonal M of the Megatron-Core page's
 general summary S_out = M S_in + delta_S.  The six calls run with
-rm_cp_problem.vector_gates = 1 (generic fp32-arithmetic kernels); outputs,
+rm_cp_problem.vector_gates = 1: on the tensor-core kernels for bf16 with
+Dk = Dv = 128 and segment lengths that are multiples of 64 (the cases named
+tc below), on the generic fp32-arithmetic kernels otherwise; outputs,
 gradients and the forward summaries (M, delta_S, S_in) are compared element
 by element with oracle.vg_forward / vg_backward / vg_forward_prepare /
 vg_compose_prefix: max|gpu - ref| <= tol * max|ref| per tensor, tol = 1e-4
@@ -30,7 +32,7 @@ def _cuda():
     C.load()
 
 
-def vg_inputs(B, T, H, Dk, Dv, dtype, seed=0, shift=3.0, gate=None, qh=0):
+def vg_inputs(B, T, H, Dk, Dv, dtype, seed=0, shift=3.0, gate=None, qh=0, gmod=None):
     gen = torch.Generator().manual_seed(seed)
     q = torch.randn(B, T, qh or H, Dk, generator=gen)
     k = torch.randn(B, T, H, Dk, generator=gen)
@@ -39,6 +41,8 @@ def vg_inputs(B, T, H, Dk, Dv, dtype, seed=0, shift=3.0, gate=None, qh=0):
     g = torch.nn.functional.logsigmoid(torch.randn(B, T, H, Dk, generator=gen) + shift)
     if gate is not None:
         g = torch.full((B, T, H, Dk), float(gate))
+    if gmod is not None:
+        gmod(g)
     dO = torch.randn(B, T, H, Dv, generator=gen)
     return q.to(dtype), k.to(dtype), v.to(dtype), g.contiguous(), dO.to(dtype)
 
@@ -65,6 +69,9 @@ def run_case(B, T, H, Dk, Dv, dtype, nseg, chunk=16, cu=None, qh=0, direct_dg=Fa
     ref.update(zip(("dq", "dk", "dv", "dg"), oracle.vg_backward(qf, k, v, g, dO, scale, si,
                                                                direct=direct_dg)))
     ref["M"], ref["dS"] = oracle.vg_forward_prepare(k, v, g, seg, si)
+    # M is an fp32 array: its reference is the fp64 value rounded to fp32
+    # (strong decays take a segment's product below fp32's range, to 0)
+    ref["M"] = ref["M"].astype(np.float32).astype(np.float64)
     if cu is None:  # with resets the prefixes start at preceding_start (M = 0 makes them agree)
         ref["S_in"] = oracle.vg_compose_prefix(ref["M"], ref["dS"])
     keys = ("o", "dq", "dk", "dv", "dg", "M", "dS") + (("S_in",) if cu is None else ())
@@ -118,3 +125,81 @@ def test_vector_gates_autograd():
     for a, b in zip((o, qd.grad, kd.grad, vd.grad, gd.grad), (ref_o,) + tuple(ref)):
         a = a.detach().double().cpu().numpy()
         assert np.max(np.abs(a - b)) <= 1e-4 * np.max(np.abs(b))
+
+
+# ------------------------------------------------------------ tensor-core path
+# bf16, Dk = Dv = 128, 64-token chunks.  A chunk is factored (its decays
+# folded into the operand tiles) when no sequence starts inside it and every
+# |b_t[i] - b_63[i]| < 60; other chunks take their intra-chunk terms directly.
+
+TC = dict(Dk=128, Dv=128, dtype=torch.bfloat16, chunk=64)
+
+
+def test_vector_gates_tc_path_selected():
+    spec = C.ProblemSpec(1, 1024, 2, 128, 128, 4, 64, 1 / math.sqrt(128), torch.bfloat16,
+                         vector_gates=1)
+    assert C.rm_cp_path(spec) == 1
+
+
+@pytest.mark.parametrize("B,T,H,nseg,shift,seed", [
+    (1, 1024, 2, 4, 3.0, 10),   # moderate decays: factored chunks (the first starts the row)
+    (2, 768, 3, 3, 4.0, 11),    # two rows, three heads, three chunks a segment
+    (1, 512, 2, 2, -1.0, 12),   # strong decays: every chunk's range exceeds 60, all direct
+    (1, 256, 1, 4, 3.0, 13),    # one chunk a segment
+])
+def test_vector_gates_tc(B, T, H, nseg, shift, seed):
+    run_case(B, T, H, nseg=nseg, seed=seed, shift=shift, **TC)
+
+
+def _strong_chunks(g):
+    # chunks 1 and 4 of every 256 tokens decay fast in 16 dimensions: those
+    # chunks are taken directly, their neighbours factored
+    for c0 in range(0, g.shape[1], 256):
+        for c in (1, 4):
+            a = c0 + 64 * c
+            if a < g.shape[1]:
+                g[:, a:a + 64, :, 40:56] = -2.5
+
+
+def test_vector_gates_tc_mixed_chunks():
+    run_case(1, 1024, 2, nseg=2, seed=14, gmod=_strong_chunks, **TC)
+
+
+def test_vector_gates_tc_packed_resets():
+    # starts at chunk boundaries (64, 512), inside chunks (100, 300, 301, 700)
+    # and at the last token (1023)
+    cu = [0, 64, 100, 300, 301, 512, 700, 1023, 1024]
+    run_case(1, 1024, 2, nseg=4, cu=cu, seed=15, **TC)
+
+
+def test_vector_gates_tc_shared_queries():
+    run_case(1, 512, 4, nseg=2, qh=2, seed=16, **TC)
+
+
+def test_vector_gates_tc_full_size_sampled_heads():
+    """vg32k (T = 32768, 16 heads, 16 segments; 256 CTAs, more than the SMs)
+    on the GPU; two heads against the oracle (heads are independent)."""
+    from state_summary_scan_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS["vg32k"]
+    inp = make_inputs(w)
+    dev = "cuda"
+    qd, kd, vd, gd, dOd = (t.to(dev).contiguous() for t in (inp.q, inp.k, inp.v, inp.g, inp.dO))
+    plan = api.make_plan(w.B, w.T, w.H, w.Dk, w.Dv, w.num_segments, w.chunk, w.scale, w.torch_dtype,
+                         None, dev, vector_gates=True)
+    assert C.rm_cp_path(plan.spec) == 1
+    o = api.forward(plan, qd, kd, vd, gd)
+    dq, dk, dv, dg = api.backward(plan, qd, kd, vd, gd, dOd)
+    torch.cuda.synchronize()
+    heads = [0, 11]
+    sl = lambda t: t[:, :, heads].contiguous()
+    gpu = {n: sl(t).detach().to("cpu", torch.float64).numpy()
+           for n, t in dict(o=o, dq=dq, dk=dk, dv=dv, dg=dg).items()}
+    for n, t in dict(M=plan.M, dS=plan.dS, S_in=plan.S_in).items():
+        gpu[n] = t[:, :, heads].detach().to("cpu", torch.float64).numpy()
+    q, k, v, g, dO = (sl(t) for t in (inp.q, inp.k, inp.v, inp.g, inp.dO))
+    ref = dict(o=oracle.vg_forward(q, k, v, g, w.scale))
+    ref.update(zip(("dq", "dk", "dv", "dg"), oracle.vg_backward(q, k, v, g, dO, w.scale)))
+    seg = oracle.equal_segments(w.T, w.num_segments)
+    ref["M"], ref["dS"] = oracle.vg_forward_prepare(k, v, g, seg)
+    ref["S_in"] = oracle.vg_compose_prefix(ref["M"], ref["dS"])
+    compare(gpu, ref, tol_for(w.torch_dtype), ("o", "dq", "dk", "dv", "dg", "M", "dS", "S_in"))
