@@ -25,13 +25,15 @@
 //                     one CTA per (row, head, column block), M_i staged in
 //                     shared memory, a column per thread.
 //   gdr_dq_sweep      the state in shared memory from S_in (k^T S by column
-//                     owners, the update and dq_t = scale S_t dO_t by row
-//                     owners); writes the state before every 16-token block
-//                     to the workspace.
+//                     partitions, the update over all elements, dq_t = scale
+//                     S_t dO_t by row owners); writes the state before every
+//                     16-token block to the workspace.  Each block's token
+//                     vectors are staged in shared memory by one coalesced load.
 //   gdr_reverse_sweep the adjoint D in shared memory from dS_out at the
 //                     segment end (D_t = scale q_t dO_t^T + A_{t+1} D_{t+1});
-//                     S_{t-1} is rebuilt in shared memory from the block's
-//                     saved state; dv, dk, dbeta and dg per token:
+//                     the states S_{t-1} of each group of four tokens are
+//                     rebuilt once, into a stack in shared memory, from the
+//                     block's saved state; dv, dk, dbeta and dg per token:
 //                       dv_t    = beta_t D_t^T k_t
 //                       dk_t    = beta_t D_t v_t - alpha_t beta_t (S_{t-1} D_t^T + D_t S_{t-1}^T) k_t
 //                       dbeta_t = k_t^T D_t v_t - alpha_t k_t^T D_t S_{t-1}^T k_t
@@ -290,32 +292,86 @@ __global__ void __launch_bounds__(128) gdr_compose(Dims d, const float* __restri
 }
 
 // ---------------------------------------------------------------------------
-// One step of the recurrence on a state in shared memory (pitch Dv + 1),
-// k, v, alpha, beta of the token given: column owners form k^T S into ks,
-// then row owners update.  All threads of the CTA take part (two barriers).
+// One step of the recurrence between states in shared memory (pitch Dv + 1):
+// dst = alpha (src - beta k (k^T src)) + beta k v^T; dst may equal src.  The
+// column sums k^T src are split over nprt = blockDim / Dv row partitions
+// (partial sums in ksp [nprt][Dv]); the update runs over all elements with
+// every thread.  Two CTA barriers; all threads of the CTA take part.
 // ---------------------------------------------------------------------------
 template <int DK>
-__device__ __forceinline__ void gdr_state_step(float* S, int pitch, int Dv, const float* kt,
-                                               const float* vt, float al, float be, float* ks) {
-    for (int j = threadIdx.x; j < Dv; j += blockDim.x) {
-        float acc = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < DK; ++i) acc = fmaf(kt[i], S[i * pitch + j], acc);
-        ks[j] = acc;
+__device__ __forceinline__ void gdr_step(const float* src, float* dst, int pitch, int Dv, const float* kt,
+                                         const float* vt, float al, float be, float* ksp, int nprt) {
+    const int tid = threadIdx.x;
+    const int j = tid % Dv, part = tid / Dv;
+    const bool act = tid < nprt * Dv;
+    if (act) {
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+        int i = part, u = 0;
+        for (; i < DK; i += nprt, u = (u + 1) & 3) a[u] = fmaf(kt[i], src[i * pitch + j], a[u]);
+        ksp[part * Dv + j] = (a[0] + a[1]) + (a[2] + a[3]);
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < DK; i += blockDim.x) {
-        const float c = be * kt[i];
-        float* row = S + i * pitch;
-        for (int j = 0; j < Dv; ++j) row[j] = fmaf(al, fmaf(-c, ks[j], row[j]), c * vt[j]);
+    if (act) {
+        float ks = 0.f;
+        for (int pp = 0; pp < nprt; ++pp) ks += ksp[pp * Dv + j];
+        const float bv = be * vt[j];
+        // rows i = part + nprt m: four loads ahead of four stores
+        for (int i0 = part; i0 < DK; i0 += 4 * nprt) {
+            float x[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int i = i0 + m * nprt;
+                x[m] = i < DK ? src[i * pitch + j] : 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int i = i0 + m * nprt;
+                if (i < DK) dst[i * pitch + j] = fmaf(al, fmaf(-be * kt[i], ks, x[m]), kt[i] * bv);
+            }
+        }
     }
     __syncthreads();
+}
+
+// X[i][j] = f(i, j, X[i][j]) over a [DK][Dv] state (pitch), every thread on
+// column j = tid % Dv and rows part, part + nprt, ... (part = tid / Dv), four
+// loads ahead of four stores.  No barrier.
+template <int DK, class F>
+__device__ __forceinline__ void gdr_map(float* X, int pitch, int Dv, int nprt, F f) {
+    const int tid = threadIdx.x;
+    if (tid >= nprt * Dv) return;
+    const int j = tid % Dv, part = tid / Dv;
+    for (int i0 = part; i0 < DK; i0 += 4 * nprt) {
+        float x[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int i = i0 + m * nprt;
+            x[m] = i < DK ? X[i * pitch + j] : 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int i = i0 + m * nprt;
+            if (i < DK) X[i * pitch + j] = f(i, j, x[m]);
+        }
+    }
+}
+
+// The kBlk tokens of a block starting at t0: the x rows ([B,T,heads,D], head
+// index hx) as fp32 in dst [kBlk][D]; a warp reads consecutive elements.
+template <typename T>
+__device__ __forceinline__ void stage_rows(const T* __restrict__ x, const Dims& d, int b, int t0, int heads,
+                                           int hx, int D, float* dst) {
+    for (int e = threadIdx.x; e < kBlk * D; e += blockDim.x) {
+        const int tt = e / D, c = e - tt * D;
+        dst[e] = to_f32(x[((int64_t(b) * d.T + t0 + tt) * heads + hx) * D + c]);
+    }
 }
 
 // ---------------------------------------------------------------------------
 // dq sweep: S from S_in in shared memory; per token the state step, then
 // dq_t[i] = scale S_t[i,:] . dO_t by row owners.  Before every kBlk-token
-// block the state is saved to ckpt (the block's starting state).
+// block the state is saved to ckpt (the block's starting state), and the
+// block's k, v, dO, alpha and beta are staged in shared memory.
 // grid (nseg, B*H); block 128 threads.
 // ---------------------------------------------------------------------------
 template <int DK, typename T>
@@ -329,12 +385,13 @@ __global__ void __launch_bounds__(128) gdr_dq_sweep(Dims d, const T* __restrict_
                                                     T* __restrict__ dq, float* __restrict__ ckpt) {
     extern __shared__ float smem[];
     const int pitch = d.Dv + 1;
-    float* S = smem;                // [DK][pitch]
-    float* ks = S + DK * pitch;     // [Dv]
-    float* vt = ks + d.Dv;          // [Dv]
-    float* dot = vt + d.Dv;         // [Dv]
-    __shared__ float kt[DK];
-    __shared__ float ab[2];
+    const int nprt = blockDim.x / d.Dv > 0 ? int(blockDim.x) / d.Dv : 1;
+    float* S = smem;                   // [DK][pitch]
+    float* kb = S + DK * pitch;        // [kBlk][DK]
+    float* vb = kb + kBlk * DK;        // [kBlk][Dv]
+    float* ob = vb + kBlk * d.Dv;      // [kBlk][Dv]
+    float* ksp = ob + kBlk * d.Dv;     // [nprt][Dv]
+    __shared__ float alb[kBlk], beb[kBlk];
 
     const int seg = blockIdx.x;
     const int b = blockIdx.y / d.H, h = blockIdx.y % d.H;
@@ -344,40 +401,47 @@ __global__ void __launch_bounds__(128) gdr_dq_sweep(Dims d, const T* __restrict_
 
     const float* src = S_in + sum_off(d, seg, b, h);
     for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) S[(e / d.Dv) * pitch + e % d.Dv] = src[e];
-    __syncthreads();
-    for (int t = a0; t < a0 + d.L; ++t) {
-        if ((t - a0) % kBlk == 0) {
-            float* dst = ck + int64_t((t - a0) / kBlk) * DK * d.Dv;
-            for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) dst[e] = S[(e / d.Dv) * pitch + e % d.Dv];
-        }
-        for (int i = threadIdx.x; i < DK; i += blockDim.x) kt[i] = to_f32(k[qk_off(d, b, t, h) + i]);
-        for (int j = threadIdx.x; j < d.Dv; j += blockDim.x) {
-            vt[j] = to_f32(v[v_off(d, b, t, h) + j]);
-            dot[j] = to_f32(dO[v_off(d, b, t, h) + j]);
-        }
-        if (threadIdx.x == 0) {
-            ab[0] = gdr_alpha(d, g, b, t, h);
-            ab[1] = __ldg(beta + g_off(d, b, t, h));
+    for (int c = a0; c < a0 + d.L; c += kBlk) {
+        __syncthreads();  // the state is complete and the last block's vectors are read
+        float* dst = ck + int64_t((c - a0) / kBlk) * DK * d.Dv;
+        for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) dst[e] = S[(e / d.Dv) * pitch + e % d.Dv];
+        stage_rows(k, d, b, c, d.H, h, DK, kb);
+        stage_rows(v, d, b, c, d.H, h, d.Dv, vb);
+        stage_rows(dO, d, b, c, d.H, h, d.Dv, ob);
+        if (threadIdx.x < kBlk) {
+            alb[threadIdx.x] = gdr_alpha(d, g, b, c + threadIdx.x, h);
+            beb[threadIdx.x] = __ldg(beta + g_off(d, b, c + threadIdx.x, h));
         }
         __syncthreads();
-        gdr_state_step<DK>(S, pitch, d.Dv, kt, vt, ab[0], ab[1], ks);
-        for (int i = threadIdx.x; i < DK; i += blockDim.x) {
-            const float* row = S + i * pitch;
-            float acc = 0.f;
-            for (int j = 0; j < d.Dv; ++j) acc = fmaf(row[j], dot[j], acc);
-            dq[qk_off(d, b, t, h) + i] = from_f32<T>(d.scale * acc);
+        for (int r = 0; r < kBlk; ++r) {
+            gdr_step<DK>(S, S, pitch, d.Dv, kb + r * DK, vb + r * d.Dv, alb[r], beb[r], ksp, nprt);
+            // the next step's first barrier orders these reads before its update
+            for (int i = threadIdx.x; i < DK; i += blockDim.x) {
+                const float* row = S + i * pitch;
+                const float* dr = ob + r * d.Dv;
+                float a0 = 0.f, a1 = 0.f;
+                for (int j = 0; j < d.Dv; j += 2) {
+                    a0 = fmaf(row[j], dr[j], a0);
+                    a1 = fmaf(row[j + 1], dr[j + 1], a1);
+                }
+                dq[qk_off(d, b, c + r, h) + i] = from_f32<T>(d.scale * (a0 + a1));
+            }
         }
-        __syncthreads();
     }
 }
 
 // ---------------------------------------------------------------------------
-// Reverse sweep.  Shared memory: D and the rebuilt S_{t-1} (pitch Dv + 1),
-// and per-token vectors.  For each kBlk-token block (last first), then each
-// token t of it (last first): S_{t-1} is rebuilt from the block's saved state
-// (t - c steps), D_t = scale q_t dO_t^T + (t at the segment end ? dS_out :
-// A_{t+1} D_{t+1}), and the gradients follow.  grid (nseg, B*H); block 128.
+// Reverse sweep.  Shared memory: D, a stack of kSlots states (pitch Dv + 1),
+// the block's staged vectors and scratch.  For each kBlk-token block (last
+// first) and each group of kSlots tokens of it (last first), the states
+// S_{t-1} of the group are rebuilt once from the block's saved state (the
+// first slot advanced in place to the group's start, the others one step
+// apart), then for each token t of the group (last first):
+// D_t = scale q_t dO_t^T + (t at the segment end ? dS_out : A_{t+1} D_{t+1}),
+// and the gradients follow.  grid (nseg, B*H); block 128.
 // ---------------------------------------------------------------------------
+constexpr int kSlots = 4;
+
 template <int DK, typename T>
 __global__ void __launch_bounds__(128) gdr_reverse_sweep(Dims d, const T* __restrict__ q,
                                                          const T* __restrict__ k,
@@ -392,17 +456,19 @@ __global__ void __launch_bounds__(128) gdr_reverse_sweep(Dims d, const T* __rest
                                                          float* __restrict__ dbeta) {
     extern __shared__ float smem[];
     const int pitch = d.Dv + 1;
-    float* D = smem;                 // [DK][pitch]
-    float* S = D + DK * pitch;       // [DK][pitch]
-    float* ks = S + DK * pitch;      // [Dv]  k^T S scratch / kS
-    float* w = ks + d.Dv;            // [Dv]  D^T k
-    float* vt = w + d.Dv;            // [Dv]
-    float* dot = vt + d.Dv;          // [Dv]
-    float* vv = dot + d.Dv;          // [Dv]  v of a rebuild step
-    __shared__ float kt[DK], qt[DK], kr[DK];
-    __shared__ float red[2][4];      // per-warp partials: k.u - alpha k.s2, <D, S>
-    __shared__ float ab[2];          // alpha_t, beta_t
-    __shared__ float abr[2];         // alpha, beta of a rebuild step
+    const int spitch = DK * pitch;     // floats per state
+    const int nprt = blockDim.x / d.Dv > 0 ? int(blockDim.x) / d.Dv : 1;
+    float* D = smem;                   // [DK][pitch]
+    float* St = D + spitch;            // [kSlots][DK][pitch]
+    float* kb = St + kSlots * spitch;  // [kBlk][DK]
+    float* qb = kb + kBlk * DK;        // [kBlk][DK]
+    float* vb = qb + kBlk * DK;        // [kBlk][Dv]
+    float* ob = vb + kBlk * d.Dv;      // [kBlk][Dv]
+    float* ksp = ob + kBlk * d.Dv;     // [nprt][Dv]
+    float* ks = ksp + nprt * d.Dv;     // [Dv]  S_{t-1}^T k
+    float* w = ks + d.Dv;              // [Dv]  D^T k
+    __shared__ float alb[kBlk], beb[kBlk];
+    __shared__ float red[2][4];        // per-warp partials: k.u - alpha k.s2, <D, S>
 
     const int seg = blockIdx.x;
     const int b = blockIdx.y / d.H, h = blockIdx.y % d.H;
@@ -414,98 +480,93 @@ __global__ void __launch_bounds__(128) gdr_reverse_sweep(Dims d, const T* __rest
     // D carries A_{t+1} D_{t+1} between tokens; it starts as dS_out
     const float* dso = dS_out + sum_off(d, seg, b, h);
     for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) D[(e / d.Dv) * pitch + e % d.Dv] = dso[e];
-    __syncthreads();
 
     for (int c = e0 - kBlk; c >= a0; c -= kBlk) {
         const float* cs = ck + int64_t((c - a0) / kBlk) * DK * d.Dv;
-        for (int t = c + kBlk - 1; t >= c; --t) {
-            // ---- S_{t-1}: the block's saved state advanced over tokens c .. t-1
-            for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) S[(e / d.Dv) * pitch + e % d.Dv] = cs[e];
+        __syncthreads();  // the previous block's vectors are read
+        stage_rows(k, d, b, c, d.H, h, DK, kb);
+        stage_rows(q, d, b, c, d.qh, h / d.qdiv, DK, qb);
+        stage_rows(v, d, b, c, d.H, h, d.Dv, vb);
+        stage_rows(dO, d, b, c, d.H, h, d.Dv, ob);
+        if (threadIdx.x < kBlk) {
+            alb[threadIdx.x] = gdr_alpha(d, g, b, c + threadIdx.x, h);
+            beb[threadIdx.x] = __ldg(beta + g_off(d, b, c + threadIdx.x, h));
+        }
+        for (int grp = kBlk / kSlots - 1; grp >= 0; --grp) {
+            const int r0 = grp * kSlots;  // block index of the group's first token
+            // slot 0 <- S_{c + r0 - 1}: the saved S_{c-1} advanced over tokens c .. c + r0 - 1
+            for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) St[(e / d.Dv) * pitch + e % d.Dv] = cs[e];
             __syncthreads();
-            for (int r = c; r < t; ++r) {
-                for (int i = threadIdx.x; i < DK; i += blockDim.x) kr[i] = to_f32(k[qk_off(d, b, r, h) + i]);
-                for (int j = threadIdx.x; j < d.Dv; j += blockDim.x) vv[j] = to_f32(v[v_off(d, b, r, h) + j]);
-                if (threadIdx.x == 0) {
-                    abr[0] = gdr_alpha(d, g, b, r, h);
-                    abr[1] = __ldg(beta + g_off(d, b, r, h));
+            for (int r = 0; r < r0; ++r)
+                gdr_step<DK>(St, St, pitch, d.Dv, kb + r * DK, vb + r * d.Dv, alb[r], beb[r], ksp, nprt);
+            // slot j <- S_{c + r0 + j - 1}
+            for (int j = 1; j < kSlots; ++j) {
+                const int r = r0 + j - 1;
+                gdr_step<DK>(St + (j - 1) * spitch, St + j * spitch, pitch, d.Dv, kb + r * DK, vb + r * d.Dv,
+                             alb[r], beb[r], ksp, nprt);
+            }
+            for (int j = kSlots - 1; j >= 0; --j) {
+                const int r = r0 + j, t = c + r;
+                const float* S = St + j * spitch;  // S_{t-1}
+                const float* kt = kb + r * DK;
+                const float* qt = qb + r * DK;
+                const float* vt = vb + r * d.Dv;
+                const float* dot = ob + r * d.Dv;
+                const float al = alb[r], be = beb[r];
+                // D_t = scale q_t dO_t^T + (A_{t+1} D_{t+1}, already in D)
+                gdr_map<DK>(D, pitch, d.Dv, nprt,
+                            [&](int i, int jj, float x) { return fmaf(d.scale * qt[i], dot[jj], x); });
+                __syncthreads();
+                // column owners: w = D_t^T k_t, kS = S_{t-1}^T k_t; dv = beta w
+                for (int jj = threadIdx.x; jj < d.Dv; jj += blockDim.x) {
+                    float a1 = 0.f, a2 = 0.f;
+#pragma unroll 8
+                    for (int i = 0; i < DK; ++i) {
+                        a1 = fmaf(kt[i], D[i * pitch + jj], a1);
+                        a2 = fmaf(kt[i], S[i * pitch + jj], a2);
+                    }
+                    w[jj] = a1;
+                    ks[jj] = a2;
+                    dv[v_off(d, b, t, h) + jj] = from_f32<T>(be * a1);
                 }
                 __syncthreads();
-                gdr_state_step<DK>(S, pitch, d.Dv, kr, vv, abr[0], abr[1], ks);
-            }
-            // ---- token t's vectors
-            for (int i = threadIdx.x; i < DK; i += blockDim.x) {
-                kt[i] = to_f32(k[qk_off(d, b, t, h) + i]);
-                qt[i] = to_f32(q[q_off(d, b, t, h) + i]);
-            }
-            for (int j = threadIdx.x; j < d.Dv; j += blockDim.x) {
-                vt[j] = to_f32(v[v_off(d, b, t, h) + j]);
-                dot[j] = to_f32(dO[v_off(d, b, t, h) + j]);
-            }
-            if (threadIdx.x == 0) {
-                ab[0] = gdr_alpha(d, g, b, t, h);
-                ab[1] = __ldg(beta + g_off(d, b, t, h));
-            }
-            __syncthreads();
-            const float al = ab[0], be = ab[1];
-            // D_t = scale q_t dO_t^T + (A_{t+1} D_{t+1}, already in D)
-            for (int i = threadIdx.x; i < DK; i += blockDim.x) {
-                const float qi = d.scale * qt[i];
-                float* row = D + i * pitch;
-                for (int j = 0; j < d.Dv; ++j) row[j] = fmaf(qi, dot[j], row[j]);
-            }
-            __syncthreads();
-            // column owners: w = D_t^T k_t, kS = S_{t-1}^T k_t; dv = beta w
-            for (int j = threadIdx.x; j < d.Dv; j += blockDim.x) {
-                float a1 = 0.f, a2 = 0.f;
-#pragma unroll 8
-                for (int i = 0; i < DK; ++i) {
-                    a1 = fmaf(kt[i], D[i * pitch + j], a1);
-                    a2 = fmaf(kt[i], S[i * pitch + j], a2);
+                // row owners: u = D_t v_t, s1 = S_{t-1} w, s2 = D_t kS, <D, S> row part
+                float p_kb = 0.f, p_ds = 0.f;
+                for (int i = threadIdx.x; i < DK; i += blockDim.x) {
+                    const float* dr = D + i * pitch;
+                    const float* sr = S + i * pitch;
+                    float u = 0.f, s1 = 0.f, s2 = 0.f, ds = 0.f;
+                    for (int jj = 0; jj < d.Dv; ++jj) {
+                        u = fmaf(dr[jj], vt[jj], u);
+                        s1 = fmaf(sr[jj], w[jj], s1);
+                        s2 = fmaf(dr[jj], ks[jj], s2);
+                        ds = fmaf(dr[jj], sr[jj], ds);
+                    }
+                    dk[qk_off(d, b, t, h) + i] = from_f32<T>(be * u - al * be * (s1 + s2));
+                    p_kb = fmaf(kt[i], u - al * s2, p_kb);
+                    p_ds += ds - be * kt[i] * s2;
                 }
-                w[j] = a1;
-                ks[j] = a2;
-                dv[v_off(d, b, t, h) + j] = from_f32<T>(be * a1);
-            }
-            __syncthreads();
-            // row owners: u = D_t v_t, s1 = S_{t-1} w, s2 = D_t kS, <D, S> row part
-            float p_kb = 0.f, p_ds = 0.f;
-            for (int i = threadIdx.x; i < DK; i += blockDim.x) {
-                const float* dr = D + i * pitch;
-                const float* sr = S + i * pitch;
-                float u = 0.f, s1 = 0.f, s2 = 0.f, ds = 0.f;
-                for (int j = 0; j < d.Dv; ++j) {
-                    u = fmaf(dr[j], vt[j], u);
-                    s1 = fmaf(sr[j], w[j], s1);
-                    s2 = fmaf(dr[j], ks[j], s2);
-                    ds = fmaf(dr[j], sr[j], ds);
+                p_kb = warp_sum(p_kb);
+                p_ds = warp_sum(p_ds);
+                if (lane == 0) {
+                    red[0][wid] = p_kb;
+                    red[1][wid] = p_ds;
                 }
-                dk[qk_off(d, b, t, h) + i] = from_f32<T>(be * u - al * be * (s1 + s2));
-                p_kb = fmaf(kt[i], u - al * s2, p_kb);
-                p_ds += ds - be * kt[i] * s2;
-            }
-            p_kb = warp_sum(p_kb);
-            p_ds = warp_sum(p_ds);
-            if (lane == 0) {
-                red[0][wid] = p_kb;
-                red[1][wid] = p_ds;
-            }
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                float s_kb = 0.f, s_ds = 0.f;
-                for (int u2 = 0; u2 < int(blockDim.x >> 5); ++u2) {
-                    s_kb += red[0][u2];
-                    s_ds += red[1][u2];
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    float s_kb = 0.f, s_ds = 0.f;
+                    for (int u2 = 0; u2 < int(blockDim.x >> 5); ++u2) {
+                        s_kb += red[0][u2];
+                        s_ds += red[1][u2];
+                    }
+                    dbeta[g_off(d, b, t, h)] = s_kb;
+                    dg[g_off(d, b, t, h)] = starts_sequence(d.seq_idx, t) ? 0.f : al * s_ds;
                 }
-                dbeta[g_off(d, b, t, h)] = s_kb;
-                dg[g_off(d, b, t, h)] = starts_sequence(d.seq_idx, t) ? 0.f : al * s_ds;
+                // D <- A_t D_t = alpha (D - beta k w^T), the carry into token t-1
+                gdr_map<DK>(D, pitch, d.Dv, nprt,
+                            [&](int i, int jj, float x) { return al * fmaf(-be * kt[i], w[jj], x); });
+                __syncthreads();
             }
-            // D <- A_t D_t = alpha (D - beta k w^T), the carry into token t-1
-            for (int i = threadIdx.x; i < DK; i += blockDim.x) {
-                const float cc = be * kt[i];
-                float* row = D + i * pitch;
-                for (int j = 0; j < d.Dv; ++j) row[j] = al * fmaf(-cc, w[j], row[j]);
-            }
-            __syncthreads();
         }
     }
 }
@@ -564,7 +625,9 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
             const dim3 grid = colgrid(d.Dv, &th);
             RMCP_GDR_DK_SWITCH((gdr_gamma_sweep<DK, T><<<grid, th, 0, s>>>(d, q, k, p.g, p.beta, dO, p.gamma_out)));
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
-            const size_t smem = sizeof(float) * (size_t(d.Dk) * (d.Dv + 1) + 3 * size_t(d.Dv));
+            const int nprt = 128 / d.Dv > 0 ? 128 / d.Dv : 1;
+            const size_t smem = sizeof(float) * (size_t(d.Dk) * (d.Dv + 1) + size_t(kBlk) * (d.Dk + 2 * d.Dv) +
+                                                 size_t(nprt) * d.Dv);
             RMCP_GDR_DK_SWITCH({
                 auto fn = gdr_dq_sweep<DK, T>;
                 if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
@@ -576,7 +639,9 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
             break;
         }
         case GdrOp::kBackwardApply: {
-            const size_t smem = sizeof(float) * (2 * size_t(d.Dk) * (d.Dv + 1) + 5 * size_t(d.Dv));
+            const int nprt = 128 / d.Dv > 0 ? 128 / d.Dv : 1;
+            const size_t smem = sizeof(float) * ((1 + kSlots) * size_t(d.Dk) * (d.Dv + 1) +
+                                                 size_t(kBlk) * (2 * d.Dk + 2 * d.Dv) + size_t(nprt + 2) * d.Dv);
             RMCP_GDR_DK_SWITCH({
                 auto fn = gdr_reverse_sweep<DK, T>;
                 if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
