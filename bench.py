@@ -345,7 +345,7 @@ def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_
             "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
             "traffic": load_traffic(w.name, dom), "algorithmic_bytes": dom_bytes,
             "launch_us": phase_ms[dom] * 1e3, "peak_source": peak_src}
-    if w.vector_gates:
+    if w.vector_gates and C.rm_cp_path(s) != 1:
         # the generic kernels walk tokens one by one in fp32: bound by the CUDA cores
         fl = kernel_alu_flops(w, dom)
         ach = fl / (phase_ms[dom] / 1e3) / 1e12

@@ -29,13 +29,14 @@
 // the TMA loads and stores and the tensor-core products, and the CTA steps
 // through each chunk together (two input stages, so the next chunk's tiles
 // load during this one):
-//   vgtc_outer_kernel<GAMMA>  sum_t diag(w_t) x_t y_t^T over the segment:
-//       delta_S and M of cp_forward_prepare (x = k, y = v, w = decay to the
-//       segment end) or gamma of cp_backward_prepare (x = q, y = dO,
-//       w = scale * decay from the segment start)
-//   vgtc_apply_kernel         o from S_in (cp_forward_apply)
-//   vgtc_dq_kernel            dq and, per key dimension, q_t[i] times dq_t[i]
-//                             without its same-token term (for dg)
+//   vgtc_prepare_kernel  delta_S = sum_t diag(w_t) k_t v_t^T over the
+//                        segment (w = decay to the segment end) and M
+//                        (cp_forward_prepare)
+//   vgtc_apply_kernel    o from S_in (cp_forward_apply)
+//   vgtc_dq_kernel       cp_backward_prepare in one sweep: dq, gamma =
+//                        sum_t diag(w_t) scale q_t dO_t^T (w = decay from the
+//                        segment start) and, per key dimension, q_t[i] times
+//                        dq_t[i] without its same-token term (for dg)
 //   vgtc_rev_kernel           dk, dv and dg from dS_out (cp_backward_apply);
 //                             dg is the reverse running sum, within a
 //                             sequence, of q.dq - k.dk per dimension, taken
@@ -55,8 +56,9 @@ constexpr int kDk = 128;
 constexpr uint32_t T8 = kTileBytes;   // one [64][64] bf16 block
 constexpr float kFactLimit = 60.f;
 
-// Per-chunk gate quantities shared by the CTA.
-struct VgGate {
+// Per-chunk gate quantities shared by the CTA (16-byte aligned: btot is
+// read as float4).
+struct alignas(16) VgGate {
     int lid[kChunk];    // number of sequence starts at chunk positions 1..tau
     float btot[kDk];    // B[i] = b_63[i]
     float tot0[kDk];    // g_0[i] + ... + g_31[i]
@@ -283,23 +285,19 @@ __device__ __forceinline__ void store_tile(const CUtensorMap* map, const uint8_t
 }
 
 // ===========================================================================
-// sum_t diag(w_t) x_t y_t^T over a segment (M = 128 key rows, N = 128).
-// prepare (GAMMA = false): x = k, y = v, chunks walked from the segment end,
-//   w_t[i] = exp(sum of g[i] over (t, end]) with no sequence start in (t, end];
-//   also M[i] = exp(sum of g[i] over the segment), 0 if a sequence starts in it.
-// gamma (GAMMA = true): x = q, y = dO, chunks walked from the segment start,
-//   w_t[i] = scale exp(sum of g[i] over [start, t]) with no sequence start in
-//   [start, t].
-// Shared memory: two stages of X|Y (32 KB each), the gate table (32 KB).
+// forward prepare: delta_S = sum_t diag(w_t) k_t v_t^T over a segment, chunks
+// walked from the segment end, w_t[i] = exp(sum of g[i] over (t, end]) with
+// no sequence start in (t, end]; M[i] = exp(sum of g[i] over the segment), 0
+// if a sequence starts in it.
+// Shared memory: two stages of K|V (32 KB each), the gate table (32 KB).
 // Tensor memory: the 128 x 128 accumulator.
 // ===========================================================================
 constexpr uint32_t O_STAGE = 4 * T8;
 constexpr uint32_t O_OFF_BT = 2 * O_STAGE;
-constexpr size_t kOuterSmem = O_OFF_BT + 4 * T8 + 1024;
+constexpr size_t kPrepSmem = O_OFF_BT + 4 * T8 + 1024;
 
-template <bool GAMMA>
 __global__ void __launch_bounds__(256, 2)
-    vgtc_outer_kernel(const Dims d, const __grid_constant__ CUtensorMap mx,
+    vgtc_prepare_kernel(const Dims d, const __grid_constant__ CUtensorMap mx,
                       const __grid_constant__ CUtensorMap my, const float* __restrict__ g,
                       float* __restrict__ M, float* __restrict__ out) {
     extern __shared__ uint8_t smem_raw[];
@@ -314,7 +312,7 @@ __global__ void __launch_bounds__(256, 2)
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     const int i = G.tid & 127, hf = G.tid >> 7;
-    auto chunk_of = [&](int it) { return GAMMA ? it : nch - 1 - it; };
+    auto chunk_of = [&](int it) { return nch - 1 - it; };
 
     if (G.tid == 0) {
         mbar_init(smem_u32(&full[0]), 1);
@@ -334,7 +332,7 @@ __global__ void __launch_bounds__(256, 2)
         const uint32_t bar = smem_u32(&full[s]);
         uint8_t* st = smem + s * O_STAGE;
         mbar_expect_tx(bar, O_STAGE);
-        load_tile(st, &mx, 0, 128, GAMMA ? h / d.qdiv : h, row, bar);
+        load_tile(st, &mx, 0, 128, h, row, bar);
         load_tile(st + 2 * T8, &my, 0, 128, h, row, bar);
     };
     if (G.tid == 0) {
@@ -354,12 +352,7 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
             const int t = 32 * hf + u;
-            float w;
-            if (GAMMA)
-                w = (!seen && !gs.first && gs.lid[t] == 0) ? d.scale * __expf(run + bl[u]) : 0.f;
-            else
-                w = (!seen && gs.lid[t] == lend) ? __expf(run + B - bl[u]) : 0.f;
-            bt[t * kDk + i] = w;
+            bt[t * kDk + i] = (!seen && gs.lid[t] == lend) ? __expf(run + B - bl[u]) : 0.f;
         }
         run += B;
         seen |= gs.any;
@@ -401,7 +394,7 @@ __global__ void __launch_bounds__(256, 2)
         for (int e = 0; e < 64; e += 4)
             *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
     }
-    if (!GAMMA && hf == 0) M[((int64_t(seg) * d.B + b) * d.H + h) * kDk + i] = seen ? 0.f : expf(run);
+    if (hf == 0) M[((int64_t(seg) * d.B + b) * d.H + h) * kDk + i] = seen ? 0.f : expf(run);
     tc_fence_before();
     __syncthreads();
     if (G.warp == 0) tmem_dealloc(tmem, 128);
@@ -616,7 +609,8 @@ __global__ void __launch_bounds__(256, 1)
     vgtc_dq_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                    const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                    const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdq,
-                   const float* __restrict__ g, const float* __restrict__ S_in, float* __restrict__ qdq) {
+                   const __nv_bfloat16* __restrict__ q, const float* __restrict__ g,
+                   const float* __restrict__ S_in, float* __restrict__ gamma, float* __restrict__ qdq) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint8_t* Kt = smem + Q_OFF_KT;
@@ -626,7 +620,8 @@ __global__ void __launch_bounds__(256, 1)
     __shared__ VgGate gs;
     __shared__ __align__(8) uint64_t full[2], abar, mbar;
     __shared__ uint32_t tmem_slot;
-    constexpr uint32_t TX = 128, TS = 256;
+    __shared__ __align__(16) float run_s[kDk];  // sum of g[i] over the segment's chunks before this one (read as float4)
+    constexpr uint32_t TX = 128, TS = 256, TG = 384;
 
     const Geo G = geo();
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
@@ -670,6 +665,8 @@ __global__ void __launch_bounds__(256, 1)
     constexpr uint32_t id_b = idesc_bf16(64, 128, 0, 0);
     constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
     const Fac fac{bt, &gs, d.scale};
+    if (G.tid < kDk) run_s[G.tid] = 0.f;
+    int seen = 0;  // a sequence starts in the segment's chunks before this one
     uint32_t aph = 0, mph = 0;
     for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
@@ -703,6 +700,17 @@ __global__ void __launch_bounds__(256, 1)
                 *reinterpret_cast<uint4*>(Kt + off) = *reinterpret_cast<const uint4*>(Ks + off);
             }
             scale_el(Kt, G.tid, [&](int r, int cc, float* x) { fac.k_wout(r, cc, x); });
+            // gamma's A operand in place of Q: scale exp(sum of g over [segment start, t])
+            // while no sequence starts in [segment start, t], else 0
+            const bool open = !seen && !gs.first;
+            scale_el(Qs, G.tid, [&](int r, int cc, float* x) {
+                const bool keep = open && gs.lid[r] == 0;
+                float bb[8], rr[8];
+                ld8(bt + r * kDk + cc, bb);
+                ld8(run_s + cc, rr);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = keep ? x[e] * d.scale * __expf(rr[e] + bb[e]) : 0.f;
+            });
         }
         state_pass(tmem, G, TS, gs.any ? 0.f : expf(gs.btot[G.srow]), fact, Sb);
         mbar_wait(smem_u32(&abar), aph);
@@ -735,7 +743,24 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k)  // S += K~^T V
                 mma_bf16(tmem + TS, desc_plus(ktm, k * 2048), desc_plus(vm, k * 2048), id_s, 1u);
+            const uint64_t qhm = desc_plus(DM, s * Q_STAGE), om = desc_plus(DM, s * Q_STAGE + 6 * T8);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // gamma += Qh^T dO
+                mma_bf16(tmem + TG, desc_plus(qhm, k * 2048), desc_plus(om, k * 2048), id_s,
+                         (c > 0 || k > 0) ? 1u : 0u);
             mma_commit(smem_u32(&mbar));
+        }
+        if (G.tid < kDk) run_s[G.tid] += gs.btot[G.tid];  // every scaling has read run_s
+        seen |= gs.any;
+        // this thread's raw q (the Q tile holds gamma's operand), loaded while the products run
+        uint4 q4[2][2];
+        {
+            const __nv_bfloat16* qp = q + q_off(d, b, a0 + c * kChunk + G.tau, h) + 64 * G.grp + 16 * G.hi;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                q4[k][0] = *reinterpret_cast<const uint4*>(qp + 32 * k);
+                q4[k][1] = *reinterpret_cast<const uint4*>(qp + 32 * k + 8);
+            }
         }
         mbar_wait(smem_u32(&mbar), mph);
         mph ^= 1;
@@ -752,7 +777,8 @@ __global__ void __launch_bounds__(256, 1)
                 const int cc = 64 * G.grp + 32 * k + 16 * G.hi;
                 float* x = xx[k];
                 float qv[16], bq[16], out[16];
-                tile_row_get16(Qs, G.tau, cc, qv);
+                unpack8(q4[k][0], qv);
+                unpack8(q4[k][1], qv + 8);
                 ld8(bt + G.tau * kDk + cc, bq);
                 ld8(bt + G.tau * kDk + cc + 8, bq + 8);
                 if (fact) {
@@ -790,6 +816,14 @@ __global__ void __launch_bounds__(256, 1)
             store_tile(&mdq, Vs, h, b * d.T + a0 + c * kChunk);
             bulk_commit();
         }
+    }
+    {   // gamma rows (every product has completed)
+        float* dst = gamma + sum_off(d, seg, b, h) + int64_t(G.srow) * kDk + 64 * G.grp;
+        float v[64];
+        state_cols64(tmem, G, TG, v);
+#pragma unroll
+        for (int e = 0; e < 64; e += 4)
+            *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
     }
     if (G.tid == 0) bulk_wait_all();
     tc_fence_before();
@@ -1050,12 +1084,21 @@ __global__ void __launch_bounds__(256, 1)
                 mma_bf16(tmem + TE, desc_plus(qm, kk * 2048), desc_plus(om, kk * 2048), id_e, 1u);
             mma_commit(smem_u32(&mbar));
         }
+        // this thread's q.dq values, loaded while the products run
+        float4 qd4[2][4];
+        {
+            const float* qrow = qdq + gv_off(d, b, t0 + G.tau, h);
+#pragma unroll
+            for (int kq = 0; kq < 2; ++kq)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    qd4[kq][u] = *reinterpret_cast<const float4*>(qrow + 64 * G.grp + 32 * kq + 16 * G.hi + 4 * u);
+        }
         mbar_wait(smem_u32(&mbar), mph);
         mph ^= 1;
         tc_fence_after();
         {   // dk rows (staged in V), the dg summands c (split into Q and K)
             const int t = t0 + G.tau;
-            const float* qrow = qdq + gv_off(d, b, t, h);
             const float att = tile_el(PD, G.tau, G.tau);  // as the products saw it
             const bool keep_out = gs.lid[G.tau] == gs.ltot;
             float xx[2][16];
@@ -1070,9 +1113,9 @@ __global__ void __launch_bounds__(256, 1)
                 ld8(gs.btot + cc, B);
                 ld8(gs.btot + cc + 8, B + 8);
 #pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    const float4 y = *reinterpret_cast<const float4*>(qrow + cc + u);
-                    qd[u] = y.x; qd[u + 1] = y.y; qd[u + 2] = y.z; qd[u + 3] = y.w;
+                for (int u = 0; u < 4; ++u) {
+                    const float4 y = qd4[kq][u];
+                    qd[4 * u] = y.x; qd[4 * u + 1] = y.y; qd[4 * u + 2] = y.z; qd[4 * u + 3] = y.w;
                 }
                 if (fact) {
                     float qt[16], kt[16];
@@ -1201,9 +1244,9 @@ rm_status launch_vgtc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
     switch (op) {
         case Op::kForwardPrepare: {
             if (!make_map(&mk, p.k, d, 128) || !make_map(&mv, p.v, d, 128)) return RM_ERR_CUDA;
-            auto fn = vgtc_outer_kernel<false>;
-            if (!set_smem(fn, kOuterSmem)) return RM_ERR_CUDA;
-            fn<<<grid, 256, kOuterSmem, s>>>(d, mk, mv, p.g, p.M, p.sum_out);
+            auto fn = vgtc_prepare_kernel;
+            if (!set_smem(fn, kPrepSmem)) return RM_ERR_CUDA;
+            fn<<<grid, 256, kPrepSmem, s>>>(d, mk, mv, p.g, p.M, p.sum_out);
             break;
         }
         case Op::kForwardApply: {
@@ -1221,15 +1264,11 @@ rm_status launch_vgtc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             if (!make_map(&mq, p.q, d, 128, d.qh) || !make_map(&mk, p.k, d, 128) ||
                 !make_map(&mv, p.v, d, 128) || !make_map(&mdo, p.dO, d, 128) || !make_map(&mdq, p.out0, d, 128))
                 return RM_ERR_CUDA;
-            auto fo = vgtc_outer_kernel<true>;
             auto fq = vgtc_dq_kernel;
-            if (!set_smem(fo, kOuterSmem) || !set_smem(fq, kDqSmem)) return RM_ERR_CUDA;
-            fo<<<grid, 256, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
-            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
-            fq<<<grid, 256, kDqSmem, s>>>(d, mq, mk, mv, mdo, mdq, p.g, p.S_in, p.ws_f32);
-            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
-            note_launch(2);
-            return RM_OK;
+            if (!set_smem(fq, kDqSmem)) return RM_ERR_CUDA;
+            fq<<<grid, 256, kDqSmem, s>>>(d, mq, mk, mv, mdo, mdq, static_cast<const __nv_bfloat16*>(p.q), p.g,
+                                          p.S_in, p.sum_out, p.ws_f32);
+            break;
         }
         case Op::kBackwardApply: {
             CUtensorMap mdk, mdv;
