@@ -655,12 +655,13 @@ def gdr_kernel_alu_flops(w, phase):
     """fp32 flops one launch of the generic gated-delta-rule kernels performs,
     per token and head as the kernels run them (multiply-add = 2): the state
     step is k^T S then the rank-one correction (about 6 Dk Dv), the prepare
-    also walks M's Dk columns, the reverse sweep rebuilds S_{t-1} from the
-    state saved every 16 tokens (7.5 steps on average) before its gradients."""
+    also walks M's Dk columns, the reverse sweep rebuilds the states S_{t-1} of
+    each group of four tokens once from the state saved every 16 tokens (2.25
+    steps a token) and forms its gradients (about 18 Dk Dv)."""
     ntok = w.B * w.T * w.H
     kd = w.Dk * w.Dv
     per = {"gdr_forward_prepare": 6 * w.Dk * (w.Dv + w.Dk), "gdr_forward_apply": 8 * kd,
-           "gdr_backward_prepare": 16 * kd, "gdr_backward_apply": 62 * kd,
+           "gdr_backward_prepare": 16 * kd, "gdr_backward_apply": 32 * kd,
            "gdr_compose_prefix": 0, "gdr_compose_suffix": 0}[phase]
     return ntok * per
 
