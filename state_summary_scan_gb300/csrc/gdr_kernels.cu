@@ -22,8 +22,8 @@
 //                     owners of D, column-local for the same reason).
 //   gdr_compose       the prefix fold S <- M_i S + dS_i over [pre_j, j), or
 //                     the suffix fold D <- M_i^T D + gamma_i over (j, fol_j),
-//                     one CTA per (row, head, column block), M_i staged in
-//                     shared memory, a column per thread.
+//                     one CTA per (row, head, block of 16 columns), M_i and
+//                     the carried block in shared memory, a row per thread.
 //   gdr_dq_sweep      the state in shared memory from S_in (k^T S by column
 //                     partitions, the update over all elements, dq_t = scale
 //                     S_t dO_t by row owners); writes the state before every
@@ -45,9 +45,30 @@ namespace rmcp {
 namespace {
 
 constexpr int kBlk = 16;  // tokens per saved state of the dq sweep (and per rebuild)
+constexpr int kSweepThreads = 256;  // threads of the backward sweeps' CTAs
 
 __device__ __forceinline__ float gdr_alpha(const Dims& d, const float* g, int b, int t, int h) {
     return starts_sequence(d.seq_idx, t) ? 0.f : expf(__ldg(g + g_off(d, b, t, h)));
+}
+
+// store(e, load(e)) for e in [0, n) over the CTA's threads, with eight loads
+// in flight ahead of their stores: a global load and a shared store in the
+// same step of a loop would otherwise wait out each load's latency in turn.
+template <class Load, class Store>
+__device__ __forceinline__ void batched_copy(int n, Load load, Store store) {
+    for (int e0 = threadIdx.x; e0 < n; e0 += 8 * blockDim.x) {
+        float x[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int e = e0 + m * blockDim.x;
+            x[m] = e < n ? load(e) : 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int e = e0 + m * blockDim.x;
+            if (e < n) store(e, x[m]);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -91,11 +112,11 @@ __global__ void __launch_bounds__(128) gdr_column_sweep(Dims d, const T* __restr
 
     for (int t0 = a0; t0 < a0 + d.L; t0 += kTok) {
         __syncthreads();
-        for (int e = threadIdx.x; e < kTok * DK; e += blockDim.x) {
-            const int tt = e / DK, i = e % DK;
-            k_s[tt][i] = to_f32(k[qk_off(d, b, t0 + tt, h) + i]);
-            if (MODE == kGdrApply) q_s[tt][i] = to_f32(q[q_off(d, b, t0 + tt, h) + i]);
-        }
+        batched_copy(kTok * DK, [&](int e) { return to_f32(k[qk_off(d, b, t0 + e / DK, h) + e % DK]); },
+                     [&](int e, float x) { k_s[e / DK][e % DK] = x; });
+        if (MODE == kGdrApply)
+            batched_copy(kTok * DK, [&](int e) { return to_f32(q[q_off(d, b, t0 + e / DK, h) + e % DK]); },
+                         [&](int e, float x) { q_s[e / DK][e % DK] = x; });
         if (threadIdx.x < kTok) {
             const int t = t0 + threadIdx.x;
             a_s[threadIdx.x] = gdr_alpha(d, g, b, t, h);
@@ -109,19 +130,21 @@ __global__ void __launch_bounds__(128) gdr_column_sweep(Dims d, const T* __restr
 #pragma unroll 1
         for (int tt = 0; tt < kTok; ++tt) {
             const float al = a_s[tt], be = b_s[tt];
-            float ks = 0.f;  // k_t^T S[:, col]
+            float ka[4] = {0.f, 0.f, 0.f, 0.f};  // k_t^T S[:, col], four sums
 #pragma unroll
-            for (int i = 0; i < DK; ++i) ks = fmaf(k_s[tt][i], st[i], ks);
+            for (int i = 0; i < DK; ++i) ka[i & 3] = fmaf(k_s[tt][i], st[i], ka[i & 3]);
+            const float ks = (ka[0] + ka[1]) + (ka[2] + ka[3]);
             // S = alpha (S - beta k (k^T S)) + beta k v^T, column col
             const float c1 = be * ks, c2 = be * vr[tt];
-            float acc = 0.f;
+            float oa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < DK; ++i) {
                 const float ki = k_s[tt][i];
                 st[i] = fmaf(al, fmaf(-c1, ki, st[i]), c2 * ki);
-                if (MODE == kGdrApply) acc = fmaf(st[i], q_s[tt][i], acc);
+                if (MODE == kGdrApply) oa[i & 3] = fmaf(st[i], q_s[tt][i], oa[i & 3]);
             }
-            if (MODE == kGdrApply && active) o[v_off(d, b, t0 + tt, h) + col] = from_f32<T>(d.scale * acc);
+            if (MODE == kGdrApply && active)
+                o[v_off(d, b, t0 + tt, h) + col] = from_f32<T>(d.scale * ((oa[0] + oa[1]) + (oa[2] + oa[3])));
         }
     }
     if (MODE == kGdrPrepare && active) {
@@ -168,11 +191,10 @@ __global__ void __launch_bounds__(128) gdr_gamma_sweep(Dims d, const T* __restri
 
     for (int t0 = e0 - kTok; t0 >= a0; t0 -= kTok) {
         __syncthreads();
-        for (int e = threadIdx.x; e < kTok * DK; e += blockDim.x) {
-            const int tt = e / DK, i = e % DK;
-            k_s[tt][i] = to_f32(k[qk_off(d, b, t0 + tt, h) + i]);
-            q_s[tt][i] = to_f32(q[q_off(d, b, t0 + tt, h) + i]);
-        }
+        batched_copy(kTok * DK, [&](int e) { return to_f32(k[qk_off(d, b, t0 + e / DK, h) + e % DK]); },
+                     [&](int e, float x) { k_s[e / DK][e % DK] = x; });
+        batched_copy(kTok * DK, [&](int e) { return to_f32(q[q_off(d, b, t0 + e / DK, h) + e % DK]); },
+                     [&](int e, float x) { q_s[e / DK][e % DK] = x; });
         if (threadIdx.x < kTok) {
             const int t = t0 + threadIdx.x;
             a_s[threadIdx.x] = gdr_alpha(d, g, b, t, h);
@@ -190,10 +212,10 @@ __global__ void __launch_bounds__(128) gdr_gamma_sweep(Dims d, const T* __restri
 #pragma unroll
             for (int i = 0; i < DK; ++i) D[i] = fmaf(w, q_s[tt][i], D[i]);
             const float al = a_s[tt], be = b_s[tt];
-            float kd = 0.f;
+            float ka[4] = {0.f, 0.f, 0.f, 0.f};  // k_t^T D, four sums
 #pragma unroll
-            for (int i = 0; i < DK; ++i) kd = fmaf(k_s[tt][i], D[i], kd);
-            const float c1 = be * kd;
+            for (int i = 0; i < DK; ++i) ka[i & 3] = fmaf(k_s[tt][i], D[i], ka[i & 3]);
+            const float c1 = be * ((ka[0] + ka[1]) + (ka[2] + ka[3]));
 #pragma unroll
             for (int i = 0; i < DK; ++i) D[i] = al * fmaf(-c1, k_s[tt][i], D[i]);
         }
@@ -207,30 +229,59 @@ __global__ void __launch_bounds__(128) gdr_gamma_sweep(Dims d, const T* __restri
 }
 
 // ---------------------------------------------------------------------------
-// Summary folds with matrix transitions.  One CTA per (row-head bh, column
-// block); thread = one column of the carried state (DK values in registers).
+// Summary folds with matrix transitions: each column of the carried state
+// folds on its own (S <- M S + X acts column by column), so one CTA takes
+// kFoldCols columns of one (row, head).  Thread (r, q): state row r and
+// columns q * CPT .. q * CPT + CPT - 1 of the block (CPT = kFoldCols * DK /
+// 256); the carried block and M_i [DK][DK] sit in shared memory.
 //   prefix: S_in[j] = fold over [pre_j, j) of S <- M_i S + dS_i  (from 0)
 //   suffix: dS_out[j] = fold over (j, fol_j) of D <- M_i^T D + gamma_i,
 //           from the last segment down (from 0)
-// M_i [DK][DK] is staged in shared memory per step.
+// grid (B*H, ceil(Dv / kFoldCols)); block 256.
 // ---------------------------------------------------------------------------
+constexpr int kFoldCols = 16;
+
 template <int DK, bool SUFFIX>
-__global__ void __launch_bounds__(128) gdr_compose(Dims d, const float* __restrict__ M,
+__global__ void __launch_bounds__(256) gdr_compose(Dims d, const float* __restrict__ M,
                                                    const float* __restrict__ X,
                                                    const int32_t* __restrict__ range,
                                                    float* __restrict__ out) {
+    constexpr int TPR = 256 / DK;            // threads per state row
+    constexpr int CPT = kFoldCols / TPR;     // columns per thread
+    static_assert(CPT >= 1, "fold block narrower than the threads of a row");
     __shared__ float m_s[DK][DK + 1];
+    __shared__ float s_s[2][DK][kFoldCols];
     const int bh = blockIdx.x;
     const int b = bh / d.H, h = bh % d.H;
-    const int col = blockIdx.y * blockDim.x + threadIdx.x;
-    const bool active = col < d.Dv;
+    const int r = threadIdx.x / TPR, q = threadIdx.x % TPR;
+    const int c0 = blockIdx.y * kFoldCols + q * CPT;  // this thread's first column
     const int n = d.nseg;
-    float S[DK];
-    float nx[DK];
+    int buf = 0;  // s_s[buf] holds the carried block
+    auto clear = [&]() {
+#pragma unroll
+        for (int u = 0; u < CPT; ++u) s_s[buf][r][q * CPT + u] = 0.f;
+    };
+    // s_s[buf ^ 1] = M_i s_s[buf] + X_i (M_i^T for the suffix); buf flips
+    auto fold = [&](int i) {
+        __syncthreads();  // earlier readers of m_s and s_s are done
+        const float* mi = M + ((int64_t(i) * d.B + b) * d.H + h) * DK * DK;
+        batched_copy(DK * DK, [&](int e) { return __ldg(mi + e); }, [&](int e, float x) { m_s[e / DK][e % DK] = x; });
+        __syncthreads();
+        const float* xi = X + sum_off(d, i, b, h) + int64_t(r) * d.Dv;
+#pragma unroll
+        for (int u = 0; u < CPT; ++u) {
+            const int col = c0 + u;
+            float acc = col < d.Dv ? xi[col] : 0.f;
+#pragma unroll 16
+            for (int c = 0; c < DK; ++c)
+                acc = fmaf(SUFFIX ? m_s[c][r] : m_s[r][c], s_s[buf][c][q * CPT + u], acc);
+            s_s[buf ^ 1][r][q * CPT + u] = acc;
+        }
+        buf ^= 1;
+    };
     // the fold for segment j restarts whenever its range start (end) moves
     int cur = SUFFIX ? n : 0;
-#pragma unroll
-    for (int i = 0; i < DK; ++i) S[i] = 0.f;
+    clear();
     for (int u = 0; u < n; ++u) {
         const int j = SUFFIX ? n - 1 - u : u;
         int lim;
@@ -242,52 +293,20 @@ __global__ void __launch_bounds__(128) gdr_compose(Dims d, const float* __restri
             lim = lim < 0 ? 0 : (lim > j ? j : lim);
         }
         if (lim != cur) {  // rebuild the fold over the new range
-#pragma unroll
-            for (int i = 0; i < DK; ++i) S[i] = 0.f;
+            __syncthreads();
+            clear();
             const int i0 = SUFFIX ? lim - 1 : lim;
-            const int i1 = SUFFIX ? j : j;  // exclusive bound in walking order
-            for (int i = i0; SUFFIX ? i > i1 : i < i1; i += SUFFIX ? -1 : 1) {
-                __syncthreads();
-                const float* mi = M + ((int64_t(i) * d.B + b) * d.H + h) * DK * DK;
-                for (int e = threadIdx.x; e < DK * DK; e += blockDim.x) m_s[e / DK][e % DK] = mi[e];
-                __syncthreads();
-                if (active) {
-                    const float* xi = X + sum_off(d, i, b, h) + col;
-#pragma unroll
-                    for (int r = 0; r < DK; ++r) {
-                        float acc = xi[int64_t(r) * d.Dv];
-#pragma unroll
-                        for (int c = 0; c < DK; ++c) acc = fmaf(SUFFIX ? m_s[c][r] : m_s[r][c], S[c], acc);
-                        nx[r] = acc;
-                    }
-#pragma unroll
-                    for (int r = 0; r < DK; ++r) S[r] = nx[r];
-                }
-            }
+            for (int i = i0; SUFFIX ? i > j : i < j; i += SUFFIX ? -1 : 1) fold(i);
             cur = lim;
         }
-        if (active) {
-            float* dst = out + sum_off(d, j, b, h) + col;
+        __syncthreads();  // the carried block is complete
+        {
+            float* dst = out + sum_off(d, j, b, h) + int64_t(r) * d.Dv;
 #pragma unroll
-            for (int r = 0; r < DK; ++r) dst[int64_t(r) * d.Dv] = S[r];
+            for (int uu = 0; uu < CPT; ++uu)
+                if (c0 + uu < d.Dv) dst[c0 + uu] = s_s[buf][r][q * CPT + uu];
         }
-        // extend the fold by segment j for the next segment's range
-        __syncthreads();
-        const float* mj = M + ((int64_t(j) * d.B + b) * d.H + h) * DK * DK;
-        for (int e = threadIdx.x; e < DK * DK; e += blockDim.x) m_s[e / DK][e % DK] = mj[e];
-        __syncthreads();
-        if (active) {
-            const float* xj = X + sum_off(d, j, b, h) + col;
-#pragma unroll
-            for (int r = 0; r < DK; ++r) {
-                float acc = xj[int64_t(r) * d.Dv];
-#pragma unroll
-                for (int c = 0; c < DK; ++c) acc = fmaf(SUFFIX ? m_s[c][r] : m_s[r][c], S[c], acc);
-                nx[r] = acc;
-            }
-#pragma unroll
-            for (int r = 0; r < DK; ++r) S[r] = nx[r];
-        }
+        fold(j);  // extend the fold by segment j for the next segment's range
     }
 }
 
@@ -305,10 +324,17 @@ __device__ __forceinline__ void gdr_step(const float* src, float* dst, int pitch
     const int j = tid % Dv, part = tid / Dv;
     const bool act = tid < nprt * Dv;
     if (act) {
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
-        int i = part, u = 0;
-        for (; i < DK; i += nprt, u = (u + 1) & 3) a[u] = fmaf(kt[i], src[i * pitch + j], a[u]);
-        ksp[part * Dv + j] = (a[0] + a[1]) + (a[2] + a[3]);
+        // four independent sums (named, so that they stay in registers)
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        int i = part;
+        for (; i + 3 * nprt < DK; i += 4 * nprt) {
+            a0 = fmaf(kt[i], src[i * pitch + j], a0);
+            a1 = fmaf(kt[i + nprt], src[(i + nprt) * pitch + j], a1);
+            a2 = fmaf(kt[i + 2 * nprt], src[(i + 2 * nprt) * pitch + j], a2);
+            a3 = fmaf(kt[i + 3 * nprt], src[(i + 3 * nprt) * pitch + j], a3);
+        }
+        for (; i < DK; i += nprt) a0 = fmaf(kt[i], src[i * pitch + j], a0);
+        ksp[part * Dv + j] = (a0 + a1) + (a2 + a3);
     }
     __syncthreads();
     if (act) {
@@ -361,10 +387,12 @@ __device__ __forceinline__ void gdr_map(float* X, int pitch, int Dv, int nprt, F
 template <typename T>
 __device__ __forceinline__ void stage_rows(const T* __restrict__ x, const Dims& d, int b, int t0, int heads,
                                            int hx, int D, float* dst) {
-    for (int e = threadIdx.x; e < kBlk * D; e += blockDim.x) {
-        const int tt = e / D, c = e - tt * D;
-        dst[e] = to_f32(x[((int64_t(b) * d.T + t0 + tt) * heads + hx) * D + c]);
-    }
+    batched_copy(kBlk * D,
+                 [&](int e) {
+                     const int tt = e / D, c = e - tt * D;
+                     return to_f32(x[((int64_t(b) * d.T + t0 + tt) * heads + hx) * D + c]);
+                 },
+                 [&](int e, float v) { dst[e] = v; });
 }
 
 // ---------------------------------------------------------------------------
@@ -372,10 +400,10 @@ __device__ __forceinline__ void stage_rows(const T* __restrict__ x, const Dims& 
 // dq_t[i] = scale S_t[i,:] . dO_t by row owners.  Before every kBlk-token
 // block the state is saved to ckpt (the block's starting state), and the
 // block's k, v, dO, alpha and beta are staged in shared memory.
-// grid (nseg, B*H); block 128 threads.
+// grid (nseg, B*H); block kSweepThreads.
 // ---------------------------------------------------------------------------
 template <int DK, typename T>
-__global__ void __launch_bounds__(128) gdr_dq_sweep(Dims d, const T* __restrict__ q,
+__global__ void __launch_bounds__(kSweepThreads) gdr_dq_sweep(Dims d, const T* __restrict__ q,
                                                     const T* __restrict__ k,
                                                     const T* __restrict__ v,
                                                     const float* __restrict__ g,
@@ -400,7 +428,8 @@ __global__ void __launch_bounds__(128) gdr_dq_sweep(Dims d, const T* __restrict_
     float* ck = ckpt + (((int64_t(seg) * d.B + b) * d.H + h) * nblk) * int64_t(DK) * d.Dv;
 
     const float* src = S_in + sum_off(d, seg, b, h);
-    for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) S[(e / d.Dv) * pitch + e % d.Dv] = src[e];
+    batched_copy(DK * d.Dv, [&](int e) { return __ldg(src + e); },
+                 [&](int e, float x) { S[(e / d.Dv) * pitch + e % d.Dv] = x; });
     for (int c = a0; c < a0 + d.L; c += kBlk) {
         __syncthreads();  // the state is complete and the last block's vectors are read
         float* dst = ck + int64_t((c - a0) / kBlk) * DK * d.Dv;
@@ -438,12 +467,12 @@ __global__ void __launch_bounds__(128) gdr_dq_sweep(Dims d, const T* __restrict_
 // first slot advanced in place to the group's start, the others one step
 // apart), then for each token t of the group (last first):
 // D_t = scale q_t dO_t^T + (t at the segment end ? dS_out : A_{t+1} D_{t+1}),
-// and the gradients follow.  grid (nseg, B*H); block 128.
+// and the gradients follow.  grid (nseg, B*H); block kSweepThreads.
 // ---------------------------------------------------------------------------
 constexpr int kSlots = 4;
 
 template <int DK, typename T>
-__global__ void __launch_bounds__(128) gdr_reverse_sweep(Dims d, const T* __restrict__ q,
+__global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const T* __restrict__ q,
                                                          const T* __restrict__ k,
                                                          const T* __restrict__ v,
                                                          const float* __restrict__ g,
@@ -468,7 +497,7 @@ __global__ void __launch_bounds__(128) gdr_reverse_sweep(Dims d, const T* __rest
     float* ks = ksp + nprt * d.Dv;     // [Dv]  S_{t-1}^T k
     float* w = ks + d.Dv;              // [Dv]  D^T k
     __shared__ float alb[kBlk], beb[kBlk];
-    __shared__ float red[2][4];        // per-warp partials: k.u - alpha k.s2, <D, S>
+    __shared__ float red[2][kSweepThreads / 32];  // per-warp partials: k.u - alpha k.s2, <D, S>
 
     const int seg = blockIdx.x;
     const int b = blockIdx.y / d.H, h = blockIdx.y % d.H;
@@ -479,7 +508,8 @@ __global__ void __launch_bounds__(128) gdr_reverse_sweep(Dims d, const T* __rest
 
     // D carries A_{t+1} D_{t+1} between tokens; it starts as dS_out
     const float* dso = dS_out + sum_off(d, seg, b, h);
-    for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) D[(e / d.Dv) * pitch + e % d.Dv] = dso[e];
+    batched_copy(DK * d.Dv, [&](int e) { return __ldg(dso + e); },
+                 [&](int e, float x) { D[(e / d.Dv) * pitch + e % d.Dv] = x; });
 
     for (int c = e0 - kBlk; c >= a0; c -= kBlk) {
         const float* cs = ck + int64_t((c - a0) / kBlk) * DK * d.Dv;
@@ -495,7 +525,8 @@ __global__ void __launch_bounds__(128) gdr_reverse_sweep(Dims d, const T* __rest
         for (int grp = kBlk / kSlots - 1; grp >= 0; --grp) {
             const int r0 = grp * kSlots;  // block index of the group's first token
             // slot 0 <- S_{c + r0 - 1}: the saved S_{c-1} advanced over tokens c .. c + r0 - 1
-            for (int e = threadIdx.x; e < DK * d.Dv; e += blockDim.x) St[(e / d.Dv) * pitch + e % d.Dv] = cs[e];
+            batched_copy(DK * d.Dv, [&](int e) { return __ldg(cs + e); },
+                         [&](int e, float x) { St[(e / d.Dv) * pitch + e % d.Dv] = x; });
             __syncthreads();
             for (int r = 0; r < r0; ++r)
                 gdr_step<DK>(St, St, pitch, d.Dv, kb + r * DK, vb + r * d.Dv, alb[r], beb[r], ksp, nprt);
@@ -609,13 +640,12 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
         }
         case GdrOp::kComposePrefix:
         case GdrOp::kComposeSuffix: {
-            const int th = d.Dv >= 128 ? 128 : ((d.Dv + 31) / 32) * 32;
-            const dim3 grid(BH, (d.Dv + th - 1) / th);
+            const dim3 grid(BH, (d.Dv + kFoldCols - 1) / kFoldCols);
             if (op == GdrOp::kComposePrefix) {
-                RMCP_GDR_DK_SWITCH((gdr_compose<DK, false><<<grid, th, 0, s>>>(
+                RMCP_GDR_DK_SWITCH((gdr_compose<DK, false><<<grid, 256, 0, s>>>(
                     d, p.M, p.dS, d.preceding_start, p.S_in_out)));
             } else {
-                RMCP_GDR_DK_SWITCH((gdr_compose<DK, true><<<grid, th, 0, s>>>(
+                RMCP_GDR_DK_SWITCH((gdr_compose<DK, true><<<grid, 256, 0, s>>>(
                     d, p.M, p.gamma, d.following_stop, p.dS_out_out)));
             }
             break;
@@ -625,28 +655,28 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
             const dim3 grid = colgrid(d.Dv, &th);
             RMCP_GDR_DK_SWITCH((gdr_gamma_sweep<DK, T><<<grid, th, 0, s>>>(d, q, k, p.g, p.beta, dO, p.gamma_out)));
             if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
-            const int nprt = 128 / d.Dv > 0 ? 128 / d.Dv : 1;
+            const int nprt = kSweepThreads / d.Dv > 0 ? kSweepThreads / d.Dv : 1;
             const size_t smem = sizeof(float) * (size_t(d.Dk) * (d.Dv + 1) + size_t(kBlk) * (d.Dk + 2 * d.Dv) +
                                                  size_t(nprt) * d.Dv);
             RMCP_GDR_DK_SWITCH({
                 auto fn = gdr_dq_sweep<DK, T>;
                 if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
                     return RM_ERR_CUDA;
-                fn<<<dim3(d.nseg, BH), 128, smem, s>>>(d, q, k, v, p.g, p.beta, dO, p.S_in,
+                fn<<<dim3(d.nseg, BH), kSweepThreads, smem, s>>>(d, q, k, v, p.g, p.beta, dO, p.S_in,
                                                        static_cast<T*>(p.dq), p.ws);
             });
             launches = 2;
             break;
         }
         case GdrOp::kBackwardApply: {
-            const int nprt = 128 / d.Dv > 0 ? 128 / d.Dv : 1;
+            const int nprt = kSweepThreads / d.Dv > 0 ? kSweepThreads / d.Dv : 1;
             const size_t smem = sizeof(float) * ((1 + kSlots) * size_t(d.Dk) * (d.Dv + 1) +
                                                  size_t(kBlk) * (2 * d.Dk + 2 * d.Dv) + size_t(nprt + 2) * d.Dv);
             RMCP_GDR_DK_SWITCH({
                 auto fn = gdr_reverse_sweep<DK, T>;
                 if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
                     return RM_ERR_CUDA;
-                fn<<<dim3(d.nseg, BH), 128, smem, s>>>(d, q, k, v, p.g, p.beta, dO, p.dS_out, p.ws,
+                fn<<<dim3(d.nseg, BH), kSweepThreads, smem, s>>>(d, q, k, v, p.g, p.beta, dO, p.dS_out, p.ws,
                                                        static_cast<T*>(p.dk), static_cast<T*>(p.dv), p.dg,
                                                        p.dbeta);
             });
