@@ -404,31 +404,42 @@ __global__ void __launch_bounds__(256, 2)
 // forward apply: o from S_in.
 // Shared memory: two stages of Q|K|V (48 KB each), P, S (bf16), the gate table.
 // Tensor memory: [0,64) scores, [64,192) O, [256,384) S.
+// With TWO (more CTAs than SMs): two CTAs a SM, each with one input stage,
+// the gate table in the S tile's bytes (the table's last reader, the
+// scaling, is done before the state pass writes the tile) and O over the
+// scores in 256 tensor-memory columns ([0,128) O, [128,256) S); a stage is
+// refilled once the chunk's o rows have left it.
 // Per chunk: gate tables; general chunks: exact scores into P; Q~, K~ in
 // place; S *= W (bf16 tile: W S in factored chunks, S otherwise); factored
 // chunks: scores = Q~ K~^T, causal mask into P; O = P V + Q~ S_tile,
 // S += K~^T V; o rows into the dead Q tile and out by TMA.
 // ===========================================================================
 constexpr uint32_t A_STAGE = 6 * T8;
-constexpr uint32_t A_OFF_P = 2 * A_STAGE;
-constexpr uint32_t A_OFF_S = A_OFF_P + T8;
-constexpr uint32_t A_OFF_BT = A_OFF_S + 4 * T8;
-constexpr size_t kApplySmem = A_OFF_BT + 4 * T8 + 1024;
+template <bool TWO> struct ApplyLayout {
+    static constexpr int NST = TWO ? 1 : 2;
+    static constexpr uint32_t OFF_P = NST * A_STAGE;
+    static constexpr uint32_t OFF_S = OFF_P + T8;
+    static constexpr uint32_t OFF_BT = TWO ? OFF_S : OFF_S + 4 * T8;
+    static constexpr size_t SMEM = OFF_BT + 4 * T8 + 1024;
+    static constexpr uint32_t TO = TWO ? 0 : 64, TS = TWO ? 128 : 256, TCOLS = TWO ? 256 : 512;
+};
 
-__global__ void __launch_bounds__(256, 1)
+template <bool TWO>
+__global__ void __launch_bounds__(256, TWO ? 2 : 1)
     vgtc_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                       const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                       const __grid_constant__ CUtensorMap mo, const float* __restrict__ g,
                       const float* __restrict__ S_in) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    uint8_t* Ps = smem + A_OFF_P;
-    uint8_t* Sb = smem + A_OFF_S;
-    float* bt = reinterpret_cast<float*>(smem + A_OFF_BT);
+    using LY = ApplyLayout<TWO>;
+    uint8_t* Ps = smem + LY::OFF_P;
+    uint8_t* Sb = smem + LY::OFF_S;
+    float* bt = reinterpret_cast<float*>(smem + LY::OFF_BT);
     __shared__ VgGate gs;
     __shared__ __align__(8) uint64_t full[2], mbar;
     __shared__ uint32_t tmem_slot;
-    constexpr uint32_t TO = 64, TS = 256;
+    constexpr uint32_t TO = LY::TO, TS = LY::TS;
 
     const Geo G = geo();
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
@@ -441,7 +452,7 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(smem_u32(&mbar), 1);
         mbar_fence_init();
     }
-    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), LY::TCOLS);
     float gp[32], bl[32];
     gate_fetch(d, g, b, h, a0, G.tid, gp);
     tc_fence_before();
@@ -460,27 +471,27 @@ __global__ void __launch_bounds__(256, 1)
     };
     if (G.tid == 0) {
         load(0, 0);
-        if (nch > 1) load(1, 1);
+        if (!TWO && nch > 1) load(1, 1);
     }
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
-    const uint64_t pa = desc_plus(DK, A_OFF_P), sa = desc_plus(sdesc(sb0, 2 * T8, 1024), A_OFF_S);
+    const uint64_t pa = desc_plus(DK, LY::OFF_P), sa = desc_plus(sdesc(sb0, 2 * T8, 1024), LY::OFF_S);
     constexpr uint32_t id1 = idesc_bf16(64, 64, 0, 0);
     constexpr uint32_t id_o = idesc_bf16(64, 128, 0, 1);
     constexpr uint32_t id_s = idesc_bf16(128, 128, 1, 1);
     const Fac fac{bt, &gs, d.scale};
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
-        const int s = c & 1;
+        const int s = TWO ? 0 : (c & 1);
         uint8_t* Qs = smem + s * A_STAGE;
         uint8_t* Ks = Qs + 2 * T8;
         const bool fact = gate_build(d, a0 + c * kChunk, gp, bt, gs, G.tid, bl);
         if (c + 1 < nch) gate_fetch(d, g, b, h, a0 + (c + 1) * kChunk, G.tid, gp);
-        if (G.tid == 0 && c >= 1 && c + 1 < nch) {
+        if (!TWO && G.tid == 0 && c >= 1 && c + 1 < nch) {
             bulk_wait_read();  // the o store of chunk c - 1 has read its stage
             load(c + 1, s ^ 1);
         }
-        mbar_wait(smem_u32(&full[s]), (c >> 1) & 1);
+        mbar_wait(smem_u32(&full[s]), TWO ? (c & 1) : ((c >> 1) & 1));
         if (!fact) {  // from the raw tiles, before any thread scales them
             exact_scores(Qs, Ks, bt, gs, G.tau, 32 * G.grp + 16 * G.hi, d.scale, Ps);
             __syncthreads();
@@ -490,6 +501,7 @@ __global__ void __launch_bounds__(256, 1)
         else
             scale_el(Qs, G.tid, [&](int r, int cc, float* x) { fac.q_win(r, cc, x); });
         scale_el(Ks, G.tid, [&](int r, int cc, float* x) { fac.k_wout(r, cc, x); });
+        if (TWO) __syncthreads();  // the gate table's last reads before the S tile takes its bytes
         state_pass(tmem, G, TS, gs.any ? 0.f : expf(gs.btot[G.srow]), fact, Sb);
         fence_async_smem();
         tc_fence_before();
@@ -549,12 +561,16 @@ __global__ void __launch_bounds__(256, 1)
         if (G.tid == 0) {
             store_tile(&mo, Qs, h, b * d.T + a0 + c * kChunk);
             bulk_commit();
+            if (TWO && c + 1 < nch) {
+                bulk_wait_read();  // the o store has read the stage
+                load(c + 1, 0);
+            }
         }
     }
     if (G.tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (G.warp == 0) tmem_dealloc(tmem, 512);
+    if (G.warp == 0) tmem_dealloc(tmem, LY::TCOLS);
 }
 
 // ===========================================================================
@@ -1254,9 +1270,13 @@ rm_status launch_vgtc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             if (!make_map(&mq, p.q, d, 128, d.qh) || !make_map(&mk, p.k, d, 128) ||
                 !make_map(&mv, p.v, d, 128) || !make_map(&mo, p.out0, d, 128))
                 return RM_ERR_CUDA;
-            auto fn = vgtc_apply_kernel;
-            if (!set_smem(fn, kApplySmem)) return RM_ERR_CUDA;
-            fn<<<grid, 256, kApplySmem, s>>>(d, mq, mk, mv, mo, p.g, p.S_in);
+            // more CTAs than SMs: two a SM (one input stage each), else one
+            // with two stages
+            const bool two = int64_t(grid.x) * grid.y > sm_count();
+            auto fn = two ? vgtc_apply_kernel<true> : vgtc_apply_kernel<false>;
+            const size_t sm = two ? ApplyLayout<true>::SMEM : ApplyLayout<false>::SMEM;
+            if (!set_smem(fn, sm)) return RM_ERR_CUDA;
+            fn<<<grid, 256, sm, s>>>(d, mq, mk, mv, mo, p.g, p.S_in);
             break;
         }
         case Op::kBackwardPrepare: {

@@ -203,3 +203,10 @@ def test_vector_gates_tc_full_size_sampled_heads():
     ref["M"], ref["dS"] = oracle.vg_forward_prepare(k, v, g, seg)
     ref["S_in"] = oracle.vg_compose_prefix(ref["M"], ref["dS"])
     compare(gpu, ref, tol_for(w.torch_dtype), ("o", "dq", "dk", "dv", "dg", "M", "dS", "S_in"))
+
+
+def test_vector_gates_tc_wide_grid():
+    """More (segment, head) CTAs than SMs (the forward then runs two CTAs a SM),
+    with sequence starts inside chunks and chunks of strong decay."""
+    cu = [0, 100, 1024, 1500, 2048, 2049, 3000, 4096]
+    run_case(1, 4096, 40, nseg=4, cu=cu, seed=17, gmod=_strong_chunks, **TC)
