@@ -486,7 +486,6 @@ __global__ void __launch_bounds__(256, TWO ? 2 : 1)
         uint8_t* Qs = smem + s * A_STAGE;
         uint8_t* Ks = Qs + 2 * T8;
         const bool fact = gate_build(d, a0 + c * kChunk, gp, bt, gs, G.tid, bl);
-        if (c + 1 < nch) gate_fetch(d, g, b, h, a0 + (c + 1) * kChunk, G.tid, gp);
         if (!TWO && G.tid == 0 && c >= 1 && c + 1 < nch) {
             bulk_wait_read();  // the o store of chunk c - 1 has read its stage
             load(c + 1, s ^ 1);
@@ -545,6 +544,8 @@ __global__ void __launch_bounds__(256, TWO ? 2 : 1)
                 mma_bf16(tmem + TS, desc_plus(km, k * 2048), desc_plus(vm, k * 2048), id_s, 1u);
             mma_commit(smem_u32(&mbar));
         }
+        // the next chunk's gates, loaded while the products run
+        if (c + 1 < nch) gate_fetch(d, g, b, h, a0 + (c + 1) * kChunk, G.tid, gp);
         mbar_wait(smem_u32(&mbar), mph);
         mph ^= 1;
         tc_fence_after();
@@ -690,7 +691,6 @@ __global__ void __launch_bounds__(256, 1)
         uint8_t* Ks = Qs + 2 * T8;
         uint8_t* Vs = Qs + 4 * T8;
         const bool fact = gate_build(d, a0 + c * kChunk, gp, bt, gs, G.tid, bl);
-        if (c + 1 < nch) gate_fetch(d, g, b, h, a0 + (c + 1) * kChunk, G.tid, gp);
         if (G.tid == 0) {
             if (c >= 1 && c + 1 < nch) {
                 bulk_wait_read();  // the dq store of chunk c - 1 has read its stage
@@ -768,7 +768,9 @@ __global__ void __launch_bounds__(256, 1)
         }
         if (G.tid < kDk) run_s[G.tid] += gs.btot[G.tid];  // every scaling has read run_s
         seen |= gs.any;
-        // this thread's raw q (the Q tile holds gamma's operand), loaded while the products run
+        // the next chunk's gates and this thread's raw q (the Q tile holds
+        // gamma's operand), loaded while the products run
+        if (c + 1 < nch) gate_fetch(d, g, b, h, a0 + (c + 1) * kChunk, G.tid, gp);
         uint4 q4[2][2];
         {
             const __nv_bfloat16* qp = q + q_off(d, b, a0 + c * kChunk + G.tau, h) + 64 * G.grp + 16 * G.hi;
@@ -994,7 +996,6 @@ __global__ void __launch_bounds__(256, 1)
         uint8_t* Vs = Qs + 4 * T8;
         uint8_t* Ds = Qs + 6 * T8;
         const bool fact = gate_build(d, t0, gp, bt, gs, G.tid, bl);
-        if (it + 1 < nch) gate_fetch(d, g, b, h, t0 - kChunk, G.tid, gp);
         if (G.tid == 0) {
             if (it >= 1 && it + 1 < nch) {
                 bulk_wait_read();  // the dk, dv stores of the previous chunk have read its stage
@@ -1100,7 +1101,9 @@ __global__ void __launch_bounds__(256, 1)
                 mma_bf16(tmem + TE, desc_plus(qm, kk * 2048), desc_plus(om, kk * 2048), id_e, 1u);
             mma_commit(smem_u32(&mbar));
         }
-        // this thread's q.dq values, loaded while the products run
+        // the previous chunk's gates and this thread's q.dq values, loaded
+        // while the products run
+        if (it + 1 < nch) gate_fetch(d, g, b, h, t0 - kChunk, G.tid, gp);
         float4 qd4[2][4];
         {
             const float* qrow = qdq + gv_off(d, b, t0 + G.tau, h);
