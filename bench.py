@@ -325,6 +325,23 @@ def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_
     for i in range(args.steps):
         step(None, PHASES_FUSED)
     f3end.record(stream)
+    # the same step and forward captured once as CUDA graphs (api.StepGraph)
+    # and replayed: one graph launch a step instead of one launch a call
+    g_step = api.StepGraph(plan, q, k, v, g, dO) if w.backward else None
+    g_fwd = api.StepGraph(plan, q, k, v, g)
+    gtimes = {}
+    for name, gr in (("step", g_step), ("fwd", g_fwd)):
+        if gr is None:
+            continue
+        for _ in range(3):
+            gr.replay()
+        a_ev = torch.cuda.Event(enable_timing=True)
+        b_ev = torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        for _ in range(args.steps):
+            gr.replay()
+        b_ev.record(stream)
+        gtimes[name] = (a_ev, b_ev)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
@@ -332,6 +349,10 @@ def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_
     ms_per_step = replica_time(start.elapsed_time(end), world, dev) / args.steps
     fwd_ms = replica_time(fstart.elapsed_time(fend), world, dev) / args.steps
     fwd3_ms = replica_time(f3start.elapsed_time(f3end), world, dev) / args.steps
+    g_fwd_ms = replica_time(gtimes["fwd"][0].elapsed_time(gtimes["fwd"][1]), world, dev) / args.steps
+    g_ms = (replica_time(gtimes["step"][0].elapsed_time(gtimes["step"][1]), world, dev) / args.steps
+            if "step" in gtimes else g_fwd_ms)
+    del g_step, g_fwd
     tok_per_step = w.B * w.T
     value = replica_throughput(world, tok_per_step, ms_per_step)
     fwd_value = replica_throughput(world, tok_per_step, fwd_ms)
@@ -424,6 +445,10 @@ def measure_workload(w, args, rank, world, dev, peaks, peak_src, with_e2e, with_
                    "kernel_path": "tcgen05" if path_kind == 1 else "simt-fp32",
                    "gates": "per key dimension" if w.vector_gates else "per head"},
         "roofline": roof, "path_roofline": path, "fwd_path_roofline": fwd_path,
+        "graph": {"value": replica_throughput(world, tok_per_step, g_ms), "ms_per_step": g_ms,
+                  "fwd_value": replica_throughput(world, tok_per_step, g_fwd_ms), "fwd_ms_per_step": g_fwd_ms,
+                  "frac": path["t_roofline_us"] / (g_ms * 1e3),
+                  "how": "the same calls captured once as a CUDA graph (api.StepGraph) and replayed"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
     }
     del q, k, v, g, dO, o, dq, dk, dv, dg, plan, inp
@@ -450,8 +475,8 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
         "data": "synthetic (seeded: q,k,v,dO ~ N(0,1), k L2-normalised, g = logsigmoid(N(0,1)+c))",
     }
-    for key in ("config", "roofline", "path_roofline", "fwd_path_roofline", "cpu_baseline", "e2e",
-                "gpu_launches", "clocks"):
+    for key in ("config", "roofline", "path_roofline", "fwd_path_roofline", "graph", "cpu_baseline",
+                "e2e", "gpu_launches", "clocks"):
         line[key] = head[key]
     if args.workload == HEADLINE and not args.T and not args.headline_only:
         subs = {}
@@ -463,8 +488,8 @@ def run_ours(args, rank, world, local_rank):
                                      with_e2e=False, with_cpu=False)
             subs[name] = {key: r[key] for key in ("value", "fwd_value", "unit", "mode", "ms_per_step",
                                                  "fwd_ms_per_step", "dtype", "config", "roofline",
-                                                 "path_roofline", "fwd_path_roofline",
-                                                 "gpu_launches", "clocks")}
+                                                 "path_roofline", "fwd_path_roofline", "graph",
+                                                 "gpu_launches", "clocks") if key in r}
         line["workloads"] = subs
         line["gpu_launches"] = head["gpu_launches"]
     return line

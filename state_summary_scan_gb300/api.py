@@ -138,6 +138,46 @@ def backward(plan: Plan, q, k, v, g, dO, grads=None, stream=None):
     return dq, dk, dv, dg
 
 
+class StepGraph:
+    """One step captured as a CUDA graph: the forward (the three calls, or the
+    one-launch forward with fused=True) and, given dO, the three backward
+    calls, on fixed buffers.  replay() re-runs the step on whatever those
+    buffers hold; results land in the same tensors (o, the gradients and the
+    plan's summaries).  The C calls neither allocate nor synchronise and only
+    enqueue on the stream they are given, so they capture as they are; one
+    uncaptured run first sets the kernels' launch attributes."""
+
+    def __init__(self, plan: Plan, q, k, v, g, dO=None, fused: bool = False):
+        self.plan = plan
+        self.q, self.k, self.v, self.g, self.dO = q, k, v, g, dO
+        self.fused = fused
+        self.o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+        self.grads = None
+        if dO is not None:
+            backward_buffers(plan)
+            self.grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                          torch.empty(g.shape, dtype=torch.float32, device=g.device))
+        dev = v.device
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            self._run()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=side):
+            self._run()
+
+    def _run(self):
+        forward(self.plan, self.q, self.k, self.v, self.g, o=self.o, fused=self.fused)
+        if self.dO is not None:
+            backward(self.plan, self.q, self.k, self.v, self.g, self.dO, grads=self.grads)
+
+    def replay(self):
+        """Runs the captured step on the current stream."""
+        self.graph.replay()
+        return (self.o,) + (self.grads if self.grads is not None else ())
+
+
 class ChunkwiseGatedLinearAttention(torch.autograd.Function):
     """Autograd adapter.  The problem description (and a packed problem's
     device metadata) comes from a cache keyed by shape and cu_seqlens, so a

@@ -1,0 +1,66 @@
+"""CUDA-graph capture of a step (api.StepGraph): the C calls neither allocate
+nor synchronise and only enqueue on the stream they are given, so the forward
+(three calls, or the one-launch forward) and the backward capture as they
+are.  Replaying the graph gives the direct calls' outputs, gradients and
+summaries bit for bit (same kernels, same launch shapes, same inputs), also
+after new values are written into the captured input buffers."""
+import math
+
+import pytest
+import torch
+
+from state_summary_scan_gb300 import _capi as C
+from state_summary_scan_gb300 import api
+from state_summary_scan_gb300.workloads import random_cu_seqlens
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    C.load()
+
+
+def _inputs(B, T, H, Dk, Dv, vg, seed):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, T, H, Dk, generator=gen)
+    k = torch.randn(B, T, H, Dk, generator=gen)
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn(B, T, H, Dv, generator=gen)
+    gshape = (B, T, H, Dk) if vg else (B, T, H)
+    g = torch.nn.functional.logsigmoid(torch.randn(*gshape, generator=gen) + 3.0)
+    dO = torch.randn(B, T, H, Dv, generator=gen)
+    bf = torch.bfloat16
+    return [t.to("cuda").contiguous() for t in (q.to(bf), k.to(bf), v.to(bf), g, dO.to(bf))]
+
+
+@pytest.mark.parametrize("case", ["scalar", "fused", "vector", "packed", "dv256"])
+def test_graph_replay_equals_direct_calls(case):
+    B, T, H, Dk, nseg = 1, 2048, 4, 128, 4
+    Dv = 256 if case == "dv256" else 128
+    vg = case == "vector"
+    fused = case == "fused"
+    cu = random_cu_seqlens(torch.Generator().manual_seed(5), T, 700) if case == "packed" else None
+
+    def plan():
+        return api.make_plan(B, T, H, Dk, Dv, nseg, 64, 1 / math.sqrt(Dk), torch.bfloat16, cu, "cuda",
+                             vector_gates=vg)
+
+    q, k, v, g, dO = _inputs(B, T, H, Dk, Dv, vg, seed=1)
+    pg = plan()
+    assert C.rm_cp_path(pg.spec) == 1
+    sg = api.StepGraph(pg, q, k, v, g, dO, fused=fused)
+    for seed in (1, 2):  # the captured values, then new ones in the same buffers
+        if seed == 2:
+            for dst, src in zip((q, k, v, g, dO), _inputs(B, T, H, Dk, Dv, vg, seed=2)):
+                dst.copy_(src)
+        got = list(sg.replay()) + [pg.M, pg.dS, pg.S_in, pg.gamma, pg.dS_out]
+        pd = plan()
+        o = api.forward(pd, q, k, v, g, fused=fused)
+        ref = [o, *api.backward(pd, q, k, v, g, dO), pd.M, pd.dS, pd.S_in, pd.gamma, pd.dS_out]
+        torch.cuda.synchronize()
+        names = ("o", "dq", "dk", "dv", "dg", "M", "dS", "S_in", "gamma", "dS_out")
+        for name, a, b in zip(names, got, ref):
+            assert torch.equal(a, b), (case, seed, name)
