@@ -210,3 +210,33 @@ def test_vector_gates_tc_wide_grid():
     with sequence starts inside chunks and chunks of strong decay."""
     cu = [0, 100, 1024, 1500, 2048, 2049, 3000, 4096]
     run_case(1, 4096, 40, nseg=4, cu=cu, seed=17, gmod=_strong_chunks, **TC)
+
+
+def test_vector_gates_tc_step_host_pipeline():
+    """rm_cp_step_host with vector gates (g and dg [B,T,H,Dk] copied in and
+    out): two steps from pinned host buffers equal the device-buffer calls
+    bit for bit (same kernels, same order)."""
+    B, T, H, D, nseg = 1, 512, 2, 128, 4
+    scale = 1.0 / math.sqrt(D)
+    q, k, v, g, dO = vg_inputs(B, T, H, D, D, torch.bfloat16, seed=18)
+    dev = "cuda"
+    qd, kd, vd, gd, dOd = (t.to(dev).contiguous() for t in (q, k, v, g, dO))
+    pd = api.make_plan(B, T, H, D, D, nseg, 64, scale, torch.bfloat16, None, dev, vector_gates=True)
+    o = api.forward(pd, qd, kd, vd, gd)
+    dq, dk, dv, dg = api.backward(pd, qd, kd, vd, gd, dOd)
+    torch.cuda.synchronize()
+    ref = {n: t.cpu() for n, t in dict(o=o, dq=dq, dk=dk, dv=dv, dg=dg).items()}
+    host = {n: t.contiguous().pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("g", g), ("dO", dO))}
+    plan = api.make_plan(B, T, H, D, D, nseg, 64, scale, torch.bfloat16, None, dev, vector_gates=True)
+    outs = [{n: torch.full(t.shape, 7.0, dtype=t.dtype).pin_memory() for n, t in ref.items()} for _ in range(2)]
+    pipe = api.HostPipeline(plan, dict(host, **outs[0]))
+    pipe.begin()
+    for i in range(2):
+        pipe.host = dict(host, **outs[i])
+        pipe.step()
+    pipe.join()
+    torch.cuda.synchronize()
+    pipe.close()
+    for i in range(2):
+        for n in ref:
+            assert torch.equal(outs[i][n], ref[n]), (i, n)

@@ -107,3 +107,24 @@ def test_noalloc_repeated_calls_agree():
     second = noalloc_backward(plan, q, k, v, g, dO)
     torch.cuda.synchronize()
     assert_same(second, first)
+
+
+@pytest.mark.parametrize("dtype,Dk,Dv", [
+    (torch.bfloat16, 128, 128),   # vector gates on the tensor-core kernels
+    (torch.float32, 32, 32),      # and on the generic kernels
+])
+def test_noalloc_vector_gates(dtype, Dk, Dv):
+    """One gate per key dimension: the shared scratch holds Dk values per
+    (row, token, head); the no-alloc form equals the workspace form."""
+    B, T, H, nseg = 1, 1024, 3, 4
+    cu = [0, 100, 101, 700, 1024]
+    q, k, v, _, dO = inputs(B, T, H, Dk, Dv, dtype, 41)
+    gen = torch.Generator().manual_seed(42)
+    g = torch.nn.functional.logsigmoid(torch.randn(B, T, H, Dk, generator=gen) + 3.0).cuda()
+    plan = api.plan_like(q, v, nseg, 64, 1.0 / math.sqrt(Dk), cu_seqlens=cu, vector_gates=True)
+    assert C.rm_cp_path(plan.spec) == (1 if dtype == torch.bfloat16 else 0)
+    api.forward(plan, q, k, v, g)
+    ref_out = workspace_backward(plan, q, k, v, g, dO)
+    got = noalloc_backward(plan, q, k, v, g, dO)
+    torch.cuda.synchronize()
+    assert_same(got, ref_out)
