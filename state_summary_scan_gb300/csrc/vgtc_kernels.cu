@@ -28,7 +28,8 @@
 // Kernels, one CTA of 256 threads per (segment, row, head); thread 0 issues
 // the TMA loads and stores and the tensor-core products, and the CTA steps
 // through each chunk together (two input stages, so the next chunk's tiles
-// load during this one):
+// load during this one; the apply on a grid wider than the GPU runs two CTAs
+// a SM with one stage each):
 //   vgtc_prepare_kernel  delta_S = sum_t diag(w_t) k_t v_t^T over the
 //                        segment (w = decay to the segment end) and M
 //                        (cp_forward_prepare)
@@ -37,12 +38,12 @@
 //                        sum_t diag(w_t) scale q_t dO_t^T (w = decay from the
 //                        segment start) and, per key dimension, q_t[i] times
 //                        dq_t[i] without its same-token term (for dg)
-//   vgtc_rev_kernel           dk, dv and dg from dS_out (cp_backward_apply);
-//                             dg is the reverse running sum, within a
-//                             sequence, of q.dq - k.dk per dimension, taken
-//                             as a product with a 0/1 upper-triangular
-//                             matrix on the tensor cores (the summands split
-//                             into two bf16 parts), plus <S_out, dS_out>.
+//   vgtc_rev_kernel      dk, dv and dg from dS_out (cp_backward_apply);
+//                        dg is the reverse running sum, within a sequence,
+//                        of q.dq - k.dk per dimension, taken as a product
+//                        with a 0/1 upper-triangular matrix on the tensor
+//                        cores (the summands split into two bf16 parts),
+//                        plus <S_out, dS_out>.
 #include "tc_tiles.cuh"
 
 namespace rmcp {
@@ -575,15 +576,18 @@ __global__ void __launch_bounds__(256, TWO ? 2 : 1)
 }
 
 // ===========================================================================
-// backward prepare, the dq sweep: dq and qdq[t][i] = q_t[i] (dq_t[i] minus
-// its same-token term scale (dO_t . v_t) k_t[i]), from S_in.
+// backward prepare in one sweep from S_in: dq, gamma and qdq[t][i] = q_t[i]
+// (dq_t[i] minus its same-token term scale (dO_t . v_t) k_t[i]).
 //   factored: X = mask(A) K~ + dO S'^T with A = dO V^T (s <= t), K~ and
 //             S' = W S_prev as in the forward; dq = scale exp(b_t - B) X
 //   general:  X = dO S_prev^T; dq = scale (win X + sum_{s <= t} A k_s
 //             exp(b_t - b_s)) with the sum taken directly
+//   gamma += Qh^T dO, Qh = Q scaled in place by scale exp(sum of g over
+//             [segment start, t]) (0 once a sequence starts there); the
+//             epilogue reads raw q from global memory
 // Shared memory: two stages of Q|K|V|dO (64 KB each), K~ (16 KB), A (bf16),
 // S (bf16), the gate table.  dq is staged in the dead V tile.
-// Tensor memory: [0,64) A, [128,256) X, [256,384) S.
+// Tensor memory: [0,64) A, [128,256) X, [256,384) S, [384,512) gamma.
 // ===========================================================================
 constexpr uint32_t Q_STAGE = 8 * T8;
 constexpr uint32_t Q_OFF_KT = 2 * Q_STAGE;
