@@ -21,7 +21,11 @@ rm_status check_gdr(const rm_cp_problem* p, rmcp::Dims* d) {
 
 rm_status run(rmcp::GdrOp op, const rm_cp_problem* p, const rmcp::Dims& d, const rmcp::GdrPtrs& x,
               rm_stream_t stream) {
-    rm_status st = rmcp::launch_gdr(op, d, p->dtype, x, reinterpret_cast<cudaStream_t>(stream));
+    // the forward's two sweeps take the tensor cores where they can
+    const bool tc = (op == rmcp::GdrOp::kPrepare || op == rmcp::GdrOp::kApply) &&
+                    rmcp::gdrtc_supports(d, p->dtype);
+    rm_status st = tc ? rmcp::launch_gdrtc(op, d, x, reinterpret_cast<cudaStream_t>(stream))
+                      : rmcp::launch_gdr(op, d, p->dtype, x, reinterpret_cast<cudaStream_t>(stream));
     if (st == RM_ERR_CUDA) {
         char msg[256];
         std::snprintf(msg, sizeof(msg), "gated delta rule launch failed: %s",

@@ -1,0 +1,533 @@
+// gdrtc_kernels.cu -- tensor-core forward (sm_103a, tcgen05 + TMA) of the
+// gated delta rule: bf16 storage, Dk = Dv = 64, segment lengths that are
+// multiples of 64.  Per row b and head h,
+//     S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
+//     o_t = scale S_t^T q_t,
+// alpha_t = exp(g_t) (0 when token t starts a sequence): the summary
+// S_out = M S_in + delta_S of CPForwardUnpackedSummary on the Megatron-Core
+// page "core.ssm.context_parallel.chunkwise" with a Dk x Dk transition M.
+//
+// Chunkwise (WY/UT) form.  In a chunk of 64 tokens with S_prev the state
+// before it, let b_t be the running sum of the gates, Gam[t][r] =
+// exp(b_t - b_r) for r <= t in one sequence (else 0), gam_t = exp(b_t) while
+// no sequence starts in [0, t] (else 0).  Unrolling the recurrence one token
+// at a time gives S_t = gam_t S_prev + sum_{r<=t} Gam[t][r] k_r D_r^T with
+//     D_t = beta_t (v_t - gam_t S_prev^T k_t - sum_{r<t} Gam[t][r] (k_r.k_t) D_r),
+// i.e. (I + A) D = diag(beta) (V - (K o gam) S_prev) with the strictly lower
+// A[t][r] = beta_t (k_t.k_r) Gam[t][r].  With T = (I + A)^{-1} diag(beta):
+//     D      = T V - T (K o gam) S_prev          (U = T V, W = T (K o gam))
+//     O      = scale ((Q o gam) S_prev + mask(Q K^T o Gam) D)
+//     S_next = gam_63 S_prev + (K o Gam[63][.])^T D
+// Every product is a tcgen05.mma of bf16 tiles in 128-byte-swizzled shared
+// memory with an fp32 accumulator in tensor memory; T is formed on the CUDA
+// cores in fp32 (the inverse of a unit lower-triangular matrix by 16 x 16
+// blocks), and the fp32 state lives in registers (16 values a thread).
+//
+// Kernels, one CTA of 256 threads per (segment, row, head); thread 0 issues
+// the TMA loads and stores and the products, and the CTA steps through each
+// chunk together (two input stages):
+//   gdrtc_prepare_kernel  the recurrence on [S | M] from [0 | I] with values
+//                         [V | 0]: delta_S and the transition M
+//   gdrtc_apply_kernel    o from S_in
+#include "tc_tiles.cuh"
+
+namespace rmcp {
+namespace gdrtc {
+
+using namespace tc;
+
+namespace {
+
+constexpr int kD = 64;                 // Dk = Dv
+constexpr uint32_t T8 = kTileBytes;    // one [64][64] bf16 tile
+constexpr int kP = kD + 1;             // pitch of the fp32 [64][64] work arrays
+
+// Row t of a [64][64] bf16 tile times w[t] (times mul), from src into dst:
+// 512 chunks of 16 bytes, two a thread (a row's scale does not depend on the
+// swizzle).
+__device__ __forceinline__ void rows_scaled(const uint8_t* src, uint8_t* dst, const float* w, float mul,
+                                            int tid) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int n = tid + 256 * k;
+        const int r = n >> 3;
+        const uint32_t off = uint32_t(r * 128 + (n & 7) * 16);
+        float x[8];
+        unpack8(*reinterpret_cast<const uint4*>(src + off), x);
+        const float f = mul * w[r];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= f;
+        *reinterpret_cast<uint4*>(dst + off) = pack8(x);
+    }
+}
+
+// Xs = (I + La)^{-1} for the strictly lower La (fp32, pitch kP): a unit lower
+// triangular inverse by 16 x 16 blocks.  The four diagonal blocks by forward
+// substitution (a column per thread), then the blocks below the diagonal by
+// their distance from it, X_ij = -X_ii sum_{k=j}^{i-1} A_ik X_kj (Ys holds the
+// sums).  Entries above the diagonal are 0.  Every thread of the CTA calls it.
+__device__ __noinline__ void tri_inverse(const float* La, float* Xs, float* Ys) {
+    const int tid = threadIdx.x;
+    for (int e = tid; e < kD * kD; e += blockDim.x) {
+        const int r = e >> 6, c = e & 63;
+        if ((c >> 4) > (r >> 4)) Xs[r * kP + c] = 0.f;
+    }
+    if (tid < kD) {
+        const int o = 16 * (tid >> 4), c = tid & 15;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < r; ++kk) acc = fmaf(La[(o + r) * kP + o + kk], x[kk], acc);
+            x[r] = r == c ? 1.f : (r > c ? -acc : 0.f);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Xs[(o + r) * kP + o + c] = x[r];
+    }
+    __syncthreads();
+    for (int dist = 1; dist < 4; ++dist) {
+        const int nb = 4 - dist;  // blocks (j + dist, j), j < nb
+        for (int e = tid; e < nb * 256; e += blockDim.x) {
+            const int j = e >> 8, i = j + dist, r = (e >> 4) & 15, c = e & 15;
+            float acc = 0.f;
+            for (int kb = j; kb < i; ++kb) {
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk)
+                    acc = fmaf(La[(16 * i + r) * kP + 16 * kb + kk], Xs[(16 * kb + kk) * kP + 16 * j + c], acc);
+            }
+            Ys[(16 * i + r) * kP + 16 * j + c] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < nb * 256; e += blockDim.x) {
+            const int j = e >> 8, i = j + dist, r = (e >> 4) & 15, c = e & 15;
+            float acc = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                acc = fmaf(Xs[(16 * i + r) * kP + 16 * i + kk], Ys[(16 * i + kk) * kP + 16 * j + c], acc);
+            Xs[(16 * i + r) * kP + 16 * j + c] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
+// The chunk's gate tables (warp 0) and write strengths (threads 0..63).
+__device__ __forceinline__ void chunk_gates(const Dims& d, const float* __restrict__ g,
+                                            const float* __restrict__ beta, int b, int h, int t0,
+                                            GateSmem& gs, float* beta_s, const Geo& G) {
+    if (G.warp == 0) {
+        const GateRegs gr = gate_load(d, g, b, h, t0, G.lane);
+        gate_prep(gr, &gs, G.lane);
+    }
+    if (G.tid < kChunk) beta_s[G.tid] = __ldg(beta + g_off(d, b, t0 + G.tid, h));
+}
+
+// A (strictly lower, fp32) from this thread's 16 columns r = c0..c0+15 of
+// row tau of K K^T: A[tau][r] = beta_tau (k_tau.k_r) Gam[tau][r], r < tau.
+__device__ __forceinline__ void a_row16(const GateSmem& gs, const float* beta_s, const float* kk, int tau,
+                                        int c0, float* La) {
+    const int lt = gs.lid[tau];
+    const float bt = gs.b[tau], be = beta_s[tau];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const int r = c0 + e;
+        La[tau * kP + r] = (r < tau && gs.lid[r] == lt) ? be * kk[e] * __expf(bt - gs.b[r]) : 0.f;
+    }
+}
+
+// T[tau][r] = Xs[tau][r] beta_r for this thread's 16 columns, as bf16.
+__device__ __forceinline__ void t_row16(const float* Xs, const float* beta_s, int tau, int c0, uint8_t* Tt) {
+    float x[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) x[e] = Xs[tau * kP + c0 + e] * beta_s[c0 + e];
+    store_row16(Tt, tau, c0, x);
+}
+
+// One synchronous step: fence shared-memory writes for the tensor core and
+// make every thread's tensor-memory reads and shared writes visible.
+__device__ __forceinline__ void cta_sync_tc() {
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// Commit the products issued so far (thread 0) and wait for them (everyone).
+__device__ __forceinline__ void commit_wait(uint64_t* mbar, uint32_t& mph, int tid) {
+    if (tid == 0) mma_commit(smem_u32(mbar));
+    mbar_wait(smem_u32(mbar), mph);
+    mph ^= 1;
+    tc_fence_after();
+}
+
+constexpr uint32_t idKK = idesc_bf16(64, 64, 0, 0);  // A K-major, B K-major
+constexpr uint32_t idKM = idesc_bf16(64, 64, 0, 1);  // A K-major, B MN-major
+constexpr uint32_t idMM = idesc_bf16(64, 64, 1, 1);  // A MN-major, B MN-major
+
+// D (+)= A B over K = 64 for [64][64] tiles (four K-steps of 16).
+__device__ __forceinline__ void mma_kk(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mma_bf16(d, desc_plus(a, k * 32), desc_plus(b, k * 32), idKK, (acc || k > 0) ? 1u : 0u);
+}
+__device__ __forceinline__ void mma_km(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mma_bf16(d, desc_plus(a, k * 32), desc_plus(b, k * 2048), idKM, (acc || k > 0) ? 1u : 0u);
+}
+__device__ __forceinline__ void mma_mm(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mma_bf16(d, desc_plus(a, k * 2048), desc_plus(b, k * 2048), idMM, (acc || k > 0) ? 1u : 0u);
+}
+
+// ===========================================================================
+// forward apply: o from S_in.
+// Shared memory (8 KB tiles): two stages of Q|K|V; Q o gam (scaled), K o gam,
+// K o Gam[63], P, T, -W, D, S (bf16), o staging; fp32 A, X, Y work arrays.
+// Tensor memory: [0,64) K K^T, then the state product; [64,128) Q K^T, then
+// O; [128,192) W; [192,256) U, then D.
+// ===========================================================================
+constexpr uint32_t AP_STAGE = 3 * T8;
+constexpr uint32_t AP_QG = 2 * AP_STAGE, AP_KG = AP_QG + T8, AP_KC = AP_KG + T8, AP_P = AP_KC + T8;
+constexpr uint32_t AP_T = AP_P + T8, AP_WN = AP_T + T8, AP_DL = AP_WN + T8, AP_S = AP_DL + T8, AP_O = AP_S + T8;
+constexpr uint32_t AP_F32 = AP_O + T8;
+constexpr size_t kApplySmem = AP_F32 + 3 * kD * kP * sizeof(float) + 1024;
+
+__global__ void __launch_bounds__(256, 1)
+    gdrtc_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                       const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                       const __grid_constant__ CUtensorMap mo, const float* __restrict__ g,
+                       const float* __restrict__ beta, const float* __restrict__ S_in) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    float* La = reinterpret_cast<float*>(smem + AP_F32);
+    float* Xs = La + kD * kP;
+    float* Ys = Xs + kD * kP;
+    __shared__ GateSmem gs;
+    __shared__ __align__(16) float beta_s[kChunk];
+    __shared__ __align__(8) uint64_t full[2], mbar;
+    __shared__ uint32_t tmem_slot;
+    constexpr uint32_t TKK = 0, TQK = 64, TW = 128, TD = 192;
+
+    const Geo G = geo();
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+    const int c0 = 32 * G.grp + 16 * G.hi;  // this thread's 16 columns of a [64][64] product
+
+    if (G.tid == 0) {
+        mbar_init(smem_u32(&full[0]), 1);
+        mbar_init(smem_u32(&full[1]), 1);
+        mbar_init(smem_u32(&mbar), 1);
+        mbar_fence_init();
+    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
+    // the state row tau, columns c0..c0+15, in registers; its bf16 copy in the S tile
+    float Sr[16];
+    {
+        const float* src = S_in + sum_off(d, seg, b, h) + G.tau * kD + c0;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src + e);
+            Sr[e] = x.x; Sr[e + 1] = x.y; Sr[e + 2] = x.z; Sr[e + 3] = x.w;
+        }
+        store_row16(smem + AP_S, G.tau, c0, Sr);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    auto load = [&](int c, int s) {
+        const int row = b * d.T + a0 + c * kChunk;
+        const uint32_t bar = smem_u32(&full[s]);
+        uint8_t* st = smem + s * AP_STAGE;
+        mbar_expect_tx(bar, AP_STAGE);
+        tma_load_3d(smem_u32(st), &mq, 0, h / d.qdiv, row, bar);
+        tma_load_3d(smem_u32(st + T8), &mk, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + 2 * T8), &mv, 0, h, row, bar);
+    };
+    if (G.tid == 0) {
+        load(0, 0);
+        if (nch > 1) load(1, 1);
+    }
+    const uint32_t sb0 = smem_u32(smem);
+    const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
+    uint32_t mph = 0;
+    for (int c = 0; c < nch; ++c) {
+        const int s = c & 1;
+        const int t0 = a0 + c * kChunk;
+        uint8_t* Qs = smem + s * AP_STAGE;
+        uint8_t* Ks = Qs + T8;
+        chunk_gates(d, g, beta, b, h, t0, gs, beta_s, G);
+        if (G.tid == 0) {
+            if (c >= 1 && c + 1 < nch) load(c + 1, s ^ 1);  // the previous chunk's products are done
+            if (c >= 1) bulk_wait_read();                    // the o store has read its staging tile
+        }
+        __syncthreads();
+        mbar_wait(smem_u32(&full[s]), (c >> 1) & 1);
+        tc_fence_after();
+        if (G.tid == 0) {  // K K^T and Q K^T
+            const uint64_t q = desc_plus(DK, s * AP_STAGE), k = desc_plus(q, T8);
+            mma_kk(tmem + TKK, k, k, 0);
+            mma_kk(tmem + TQK, q, k, 0);
+        }
+        rows_scaled(Qs, smem + AP_QG, gs.win, d.scale, G.tid);  // scale Q o gam
+        rows_scaled(Ks, smem + AP_KG, gs.win, 1.f, G.tid);      // K o gam
+        rows_scaled(Ks, smem + AP_KC, gs.wout, 1.f, G.tid);     // K o Gam[63]
+        commit_wait(&mbar, mph, G.tid);
+        {
+            float kk[16], qk[16];
+            tok16(tmem, G, TKK + 32 * G.grp, kk);
+            tok16(tmem, G, TQK + 32 * G.grp, qk);
+            a_row16(gs, beta_s, kk, G.tau, c0, La);
+            const int lt = gs.lid[G.tau];
+            const float bt = gs.b[G.tau];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {  // P = scale (Q K^T o Gam), r <= tau
+                const int r = c0 + e;
+                qk[e] = (r <= G.tau && gs.lid[r] == lt) ? d.scale * qk[e] * __expf(bt - gs.b[r]) : 0.f;
+            }
+            store_row16(smem + AP_P, G.tau, c0, qk);
+        }
+        __syncthreads();
+        tri_inverse(La, Xs, Ys);
+        t_row16(Xs, beta_s, G.tau, c0, smem + AP_T);
+        cta_sync_tc();
+        if (G.tid == 0) {  // W = T (K o gam), U = T V
+            const uint64_t t = desc_plus(DK, AP_T);
+            mma_km(tmem + TW, t, desc_plus(DM, AP_KG), 0);
+            mma_km(tmem + TD, t, desc_plus(DM, s * AP_STAGE + 2 * T8), 0);
+        }
+        commit_wait(&mbar, mph, G.tid);
+        {
+            float w[16];
+            tok16(tmem, G, TW + 32 * G.grp, w);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = -w[e];
+            store_row16(smem + AP_WN, G.tau, c0, w);
+        }
+        cta_sync_tc();
+        if (G.tid == 0)  // D = U - W S_prev
+            mma_km(tmem + TD, desc_plus(DK, AP_WN), desc_plus(DM, AP_S), 1);
+        commit_wait(&mbar, mph, G.tid);
+        {
+            float x[16];
+            tok16(tmem, G, TD + 32 * G.grp, x);
+            store_row16(smem + AP_DL, G.tau, c0, x);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) {
+            mma_km(tmem + TQK, desc_plus(DK, AP_QG), desc_plus(DM, AP_S), 0);  // O = (scale Q o gam) S_prev
+            mma_km(tmem + TQK, desc_plus(DK, AP_P), desc_plus(DM, AP_DL), 1);  //   + P D
+            mma_mm(tmem + TKK, desc_plus(DM, AP_KC), desc_plus(DM, AP_DL), 0); // (K o Gam[63])^T D
+        }
+        commit_wait(&mbar, mph, G.tid);
+        {
+            float x[16], y[16];
+            tok16(tmem, G, TQK + 32 * G.grp, x);
+            store_row16(smem + AP_O, G.tau, c0, x);
+            tok16(tmem, G, TKK + 32 * G.grp, y);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) Sr[e] = fmaf(gs.W, Sr[e], y[e]);
+            store_row16(smem + AP_S, G.tau, c0, Sr);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) {
+            tma_store_3d(&mo, smem_u32(smem + AP_O), 0, h, b * d.T + t0);
+            bulk_commit();
+        }
+    }
+    if (G.tid == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ===========================================================================
+// forward prepare: the recurrence on [S | M] from [0 | I] with values [V | 0]
+// over one segment: S_out = M S_in + delta_S with delta_S = S and M its last
+// state.  Per chunk: D_S = T V - W S, D_M = -W M, then S = gam_63 S +
+// (K o Gam[63])^T D_S and M likewise.
+// Shared memory: two stages of K|V; K o gam, K o Gam[63], T, -W, D_S, D_M,
+// S, M (bf16); fp32 A, X, Y.
+// Tensor memory: [0,64) K K^T, then the S product; [64,128) W, then the M
+// product; [128,192) U, then D_S; [192,256) D_M.
+// ===========================================================================
+constexpr uint32_t PR_STAGE = 2 * T8;
+constexpr uint32_t PR_KG = 2 * PR_STAGE, PR_KC = PR_KG + T8, PR_T = PR_KC + T8, PR_WN = PR_T + T8;
+constexpr uint32_t PR_DS = PR_WN + T8, PR_DM = PR_DS + T8, PR_S = PR_DM + T8, PR_M = PR_S + T8;
+constexpr uint32_t PR_F32 = PR_M + T8;
+constexpr size_t kPrepSmem = PR_F32 + 3 * kD * kP * sizeof(float) + 1024;
+
+__global__ void __launch_bounds__(256, 1)
+    gdrtc_prepare_kernel(const Dims d, const __grid_constant__ CUtensorMap mk,
+                         const __grid_constant__ CUtensorMap mv, const float* __restrict__ g,
+                         const float* __restrict__ beta, float* __restrict__ M, float* __restrict__ dS) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    float* La = reinterpret_cast<float*>(smem + PR_F32);
+    float* Xs = La + kD * kP;
+    float* Ys = Xs + kD * kP;
+    __shared__ GateSmem gs;
+    __shared__ __align__(16) float beta_s[kChunk];
+    __shared__ __align__(8) uint64_t full[2], mbar;
+    __shared__ uint32_t tmem_slot;
+    constexpr uint32_t TKK = 0, TW = 64, TU = 128, TDM = 192;
+
+    const Geo G = geo();
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+    const int c0 = 32 * G.grp + 16 * G.hi;
+
+    if (G.tid == 0) {
+        mbar_init(smem_u32(&full[0]), 1);
+        mbar_init(smem_u32(&full[1]), 1);
+        mbar_init(smem_u32(&mbar), 1);
+        mbar_fence_init();
+    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
+    float Sr[16], Mr[16];  // row tau, columns c0..c0+15 of S and of M
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        Sr[e] = 0.f;
+        Mr[e] = (c0 + e == G.tau) ? 1.f : 0.f;
+    }
+    store_row16(smem + PR_S, G.tau, c0, Sr);
+    store_row16(smem + PR_M, G.tau, c0, Mr);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    auto load = [&](int c, int s) {
+        const int row = b * d.T + a0 + c * kChunk;
+        const uint32_t bar = smem_u32(&full[s]);
+        uint8_t* st = smem + s * PR_STAGE;
+        mbar_expect_tx(bar, PR_STAGE);
+        tma_load_3d(smem_u32(st), &mk, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + T8), &mv, 0, h, row, bar);
+    };
+    if (G.tid == 0) {
+        load(0, 0);
+        if (nch > 1) load(1, 1);
+    }
+    const uint32_t sb0 = smem_u32(smem);
+    const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
+    uint32_t mph = 0;
+    for (int c = 0; c < nch; ++c) {
+        const int s = c & 1;
+        const int t0 = a0 + c * kChunk;
+        uint8_t* Ks = smem + s * PR_STAGE;
+        chunk_gates(d, g, beta, b, h, t0, gs, beta_s, G);
+        if (G.tid == 0 && c >= 1 && c + 1 < nch) load(c + 1, s ^ 1);  // the previous chunk's products are done
+        __syncthreads();
+        mbar_wait(smem_u32(&full[s]), (c >> 1) & 1);
+        tc_fence_after();
+        if (G.tid == 0) {
+            const uint64_t k = desc_plus(DK, s * PR_STAGE);
+            mma_kk(tmem + TKK, k, k, 0);  // K K^T
+        }
+        rows_scaled(Ks, smem + PR_KG, gs.win, 1.f, G.tid);   // K o gam
+        rows_scaled(Ks, smem + PR_KC, gs.wout, 1.f, G.tid);  // K o Gam[63]
+        commit_wait(&mbar, mph, G.tid);
+        {
+            float kk[16];
+            tok16(tmem, G, TKK + 32 * G.grp, kk);
+            a_row16(gs, beta_s, kk, G.tau, c0, La);
+        }
+        __syncthreads();
+        tri_inverse(La, Xs, Ys);
+        t_row16(Xs, beta_s, G.tau, c0, smem + PR_T);
+        cta_sync_tc();
+        if (G.tid == 0) {  // W = T (K o gam), U = T V
+            const uint64_t t = desc_plus(DK, PR_T);
+            mma_km(tmem + TW, t, desc_plus(DM, PR_KG), 0);
+            mma_km(tmem + TU, t, desc_plus(DM, s * PR_STAGE + T8), 0);
+        }
+        commit_wait(&mbar, mph, G.tid);
+        {
+            float w[16];
+            tok16(tmem, G, TW + 32 * G.grp, w);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = -w[e];
+            store_row16(smem + PR_WN, G.tau, c0, w);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) {
+            const uint64_t wn = desc_plus(DK, PR_WN);
+            mma_km(tmem + TU, wn, desc_plus(DM, PR_S), 1);   // D_S = U - W S
+            mma_km(tmem + TDM, wn, desc_plus(DM, PR_M), 0);  // D_M = -W M
+        }
+        commit_wait(&mbar, mph, G.tid);
+        {
+            float x[16], y[16];
+            tok16(tmem, G, TU + 32 * G.grp, x);
+            tok16(tmem, G, TDM + 32 * G.grp, y);
+            store_row16(smem + PR_DS, G.tau, c0, x);
+            store_row16(smem + PR_DM, G.tau, c0, y);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) {
+            const uint64_t kc = desc_plus(DM, PR_KC);
+            mma_mm(tmem + TKK, kc, desc_plus(DM, PR_DS), 0);  // (K o Gam[63])^T D_S
+            mma_mm(tmem + TW, kc, desc_plus(DM, PR_DM), 0);   // (K o Gam[63])^T D_M
+        }
+        commit_wait(&mbar, mph, G.tid);
+        {
+            float x[16], y[16];
+            tok16(tmem, G, TKK + 32 * G.grp, x);
+            tok16(tmem, G, TW + 32 * G.grp, y);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                Sr[e] = fmaf(gs.W, Sr[e], x[e]);
+                Mr[e] = fmaf(gs.W, Mr[e], y[e]);
+            }
+            store_row16(smem + PR_S, G.tau, c0, Sr);
+            store_row16(smem + PR_M, G.tau, c0, Mr);
+        }
+        cta_sync_tc();
+    }
+    {
+        float* ds = dS + sum_off(d, seg, b, h) + G.tau * kD + c0;
+        float* m = M + ((int64_t(seg) * d.B + b) * d.H + h) * kD * kD + G.tau * kD + c0;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            *reinterpret_cast<float4*>(ds + e) = make_float4(Sr[e], Sr[e + 1], Sr[e + 2], Sr[e + 3]);
+            *reinterpret_cast<float4*>(m + e) = make_float4(Mr[e], Mr[e + 1], Mr[e + 2], Mr[e + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 256);
+}
+
+}  // namespace
+}  // namespace gdrtc
+
+bool gdrtc_supports(const Dims& d, rm_dtype dt) {
+    return !d.vg && dt == RM_BF16 && d.Dk == gdrtc::kD && d.Dv == gdrtc::kD && d.L % tc::kChunk == 0 &&
+           d.T >= tc::kChunk;
+}
+
+rm_status launch_gdrtc(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s) {
+    using namespace gdrtc;
+    if (!gdrtc_supports(d, RM_BF16)) return RM_ERR_UNSUPPORTED;
+    const dim3 grid(d.nseg, d.B * d.H);
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mk, p.k, d, kD) || !make_map(&mv, p.v, d, kD)) return RM_ERR_CUDA;
+    if (op == GdrOp::kPrepare) {
+        auto fn = gdrtc_prepare_kernel;
+        if (!set_smem(fn, kPrepSmem)) return RM_ERR_CUDA;
+        fn<<<grid, 256, kPrepSmem, s>>>(d, mk, mv, p.g, p.beta, p.M, p.dS);
+    } else if (op == GdrOp::kApply) {
+        if (!make_map(&mq, p.q, d, kD, d.qh) || !make_map(&mo, p.o, d, kD)) return RM_ERR_CUDA;
+        auto fn = gdrtc_apply_kernel;
+        if (!set_smem(fn, kApplySmem)) return RM_ERR_CUDA;
+        fn<<<grid, 256, kApplySmem, s>>>(d, mq, mk, mv, mo, p.g, p.beta, p.S_in);
+    } else {
+        return RM_ERR_INVALID_ARG;
+    }
+    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    note_launch(1);
+    return RM_OK;
+}
+
+}  // namespace rmcp

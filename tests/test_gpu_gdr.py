@@ -98,3 +98,51 @@ def test_gdr_rejects_unsupported_shapes():
     with pytest.raises(C.RmCpError) as e:
         C.rm_gdr_forward_prepare(bad, t, t, t, t, t, t)
     assert e.value.status == 4
+
+
+# ------------------------------------------------------------ tensor-core forward
+# bf16, Dk = Dv = 64, segment lengths that are multiples of 64: the forward's
+# prepare and apply run the chunkwise WY/UT form on the tensor cores; the
+# backward (and its checks) stay on the generic kernels.
+
+def test_gdr_tc_several_chunks():
+    run_case(2, 1024, 3, 64, 64, torch.bfloat16, nseg=4, seed=5)
+
+
+def test_gdr_tc_packed_resets():
+    # starts at chunk boundaries (64, 512), inside chunks (100, 300, 301, 700)
+    # and at the last token (1023)
+    cu = [0, 64, 100, 300, 301, 512, 700, 1023, 1024]
+    run_case(1, 1024, 2, 64, 64, torch.bfloat16, nseg=4, cu=cu, seed=6)
+
+
+def test_gdr_tc_shared_queries():
+    run_case(1, 512, 4, 64, 64, torch.bfloat16, nseg=2, qh=2, seed=7)
+
+
+def test_gdr_tc_full_size_sampled_heads():
+    """gdr8k (T = 8192, 16 heads, 16 segments; 256 CTAs) on the GPU; two
+    heads against the oracle (heads are independent)."""
+    from state_summary_scan_gb300.workloads import GDR_WORKLOADS, make_gdr_inputs
+    w = GDR_WORKLOADS["gdr8k"]
+    inp = make_gdr_inputs(w)
+    dev = "cuda"
+    qd, kd, vd, gd, bd, dOd = (t.to(dev).contiguous() for t in (inp.q, inp.k, inp.v, inp.g, inp.beta, inp.dO))
+    plan = api.make_gdr_plan(w.B, w.T, w.H, w.Dk, w.Dv, w.num_segments, w.chunk, w.scale, w.torch_dtype,
+                             None, dev)
+    o = api.gdr_forward(plan, qd, kd, vd, gd, bd)
+    grads = api.gdr_backward(plan, qd, kd, vd, gd, bd, dOd)
+    torch.cuda.synchronize()
+    heads = [0, 9]
+    sl = lambda t: t[:, :, heads].contiguous()
+    gpu = {n: sl(t).detach().to("cpu", torch.float64).numpy()
+           for n, t in zip(("o", "dq", "dk", "dv", "dg", "dbeta"), (o,) + tuple(grads))}
+    for n, t in dict(M=plan.M, dS=plan.dS, S_in=plan.S_in).items():
+        gpu[n] = t[:, :, heads].detach().to("cpu", torch.float64).numpy()
+    q, k, v, g, beta, dO = (sl(t) for t in (inp.q, inp.k, inp.v, inp.g, inp.beta, inp.dO))
+    ref = dict(o=oracle.gdr_forward(q, k, v, g, beta, w.scale))
+    ref.update(zip(("dq", "dk", "dv", "dg", "dbeta"), oracle.gdr_backward(q, k, v, g, beta, dO, w.scale)))
+    seg = oracle.equal_segments(w.T, w.num_segments)
+    ref["M"], ref["dS"] = oracle.gdr_forward_prepare(k, v, g, beta, seg)
+    ref["S_in"] = oracle.gdr_compose_prefix(ref["M"], ref["dS"])
+    compare(gpu, ref, tol_for(w.torch_dtype), ("o", "dq", "dk", "dv", "dg", "dbeta", "M", "dS", "S_in"))
