@@ -691,6 +691,37 @@ def gdr_kernel_alu_flops(w, phase):
     return ntok * per
 
 
+def gdr_kernel_bytes(w, phase):
+    """Algorithmic bytes of one launch of a gated-delta-rule call: its inputs
+    read once and its outputs written once (token tensors, gates, summaries;
+    the backward prepare writes, and the apply reads, one fp32 state per
+    64-token chunk, the tensor-core sweeps' workspace)."""
+    e = 4 if w.dtype == "f32" else 2
+    Dk, Dv = w.Dk, w.Dv
+    ntok = w.B * w.T * w.H
+    nsum = w.num_segments * w.B * w.H
+    st, mt = 4 * Dk * Dv, 4 * Dk * Dk
+    ckpt = (ntok // 64) * st
+    return {
+        "gdr_forward_prepare": ntok * (e * (Dk + Dv) + 8) + nsum * (mt + st),
+        "gdr_compose_prefix": nsum * (mt + 2 * st),
+        "gdr_forward_apply": ntok * (e * (2 * Dk + Dv) + 8 + e * Dv) + nsum * st,
+        "gdr_backward_prepare": ntok * (e * (2 * Dk + 2 * Dv) + 8 + e * Dk) + 2 * nsum * st + ckpt,
+        "gdr_compose_suffix": nsum * (mt + 2 * st),
+        "gdr_backward_apply": ntok * (e * (2 * Dk + 2 * Dv) + 8 + e * (Dk + Dv) + 8) + nsum * st + ckpt,
+    }[phase]
+
+
+def gdr_kernel_tc_flops(w, phase):
+    """Tensor-core flops of one launch of the tensor-core sweeps: 64 x 64 x 64
+    products per 64-token chunk and head (7 in the forward prepare, 8 in the
+    apply, 8 + 7 in the backward prepare's dq and gamma walks, 16 in the
+    backward apply)."""
+    per = {"gdr_forward_prepare": 7, "gdr_forward_apply": 8, "gdr_backward_prepare": 15,
+           "gdr_backward_apply": 16}.get(phase, 0)
+    return (w.B * w.T * w.H // 64) * per * 2 * 64 ** 3
+
+
 def gdr_path_roofline(w, peaks):
     """The method's step: read q, k, v, g, beta (and dO), write o (and dq, dk,
     dv, dg, dbeta); summaries M (Dk x Dk) and delta_S written, read by the
@@ -757,7 +788,7 @@ def measure_gdr(w, args, rank, world, dev, peaks, peak_src, with_cpu):
                                                               dg, db, plan.ws, stream),
     }
     phases = GDR_PHASES_FWD + GDR_PHASES_BWD
-    steps = max(3, min(args.steps, 20))  # a step takes milliseconds on the generic kernels
+    steps = max(3, min(args.steps, 50))  # about a millisecond a step (several on the generic kernels)
     for _ in range(args.warmup):
         for ph in phases:
             fns[ph]()
@@ -789,21 +820,35 @@ def measure_gdr(w, args, rank, world, dev, peaks, peak_src, with_cpu):
     phase_ms = {ph: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
                 for j, ph in enumerate(phases)}
     dom = max(phase_ms, key=phase_ms.get)
-    fl = gdr_kernel_alu_flops(w, dom)
-    ach = fl / (phase_ms[dom] / 1e3) / 1e12
+    tc = C.rm_gdr_path(s) == 1
+    if tc:
+        # the tensor-core sweeps: bytes bound them (their flops take less time at peak)
+        kb, kf = gdr_kernel_bytes(w, dom), gdr_kernel_tc_flops(w, dom)
+        ach = kb / (phase_ms[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "kernel_bytes": kb, "tensor_flops": kf,
+                "tensor_frac": kf / (phase_ms[dom] / 1e3) / (peaks["bf16_tflops"] * 1e12),
+                "launch_us": phase_ms[dom] * 1e3, "traffic": load_traffic(w.name, dom),
+                "peak_source": peak_src}
+    else:
+        fl = gdr_kernel_alu_flops(w, dom)
+        ach = fl / (phase_ms[dom] / 1e3) / 1e12
+        roof = {"bound": "alu", "kernel": dom, "achieved": ach, "peak": FP32_ALU_TFLOPS,
+                "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS, "alu_flops": fl,
+                "launch_us": phase_ms[dom] * 1e3, "traffic": load_traffic(w.name, dom),
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2070 MHz"}
     pr = gdr_path_roofline(w, peaks)
     tok = w.B * w.T
     return {
         "value": replica_throughput(world, tok, ms), "fwd_value": replica_throughput(world, tok, fwd_ms),
-        "unit": "tokens/s", "mode": "fwd+bwd", "ms_per_step": ms, "fwd_ms_per_step": fwd_ms, "dtype": "f32",
+        "unit": "tokens/s", "mode": "fwd+bwd", "ms_per_step": ms, "fwd_ms_per_step": fwd_ms,
+        "dtype": "bf16" if tc else "f32",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
                    "num_segments": w.num_segments, "storage": w.dtype, "mode": "fwd+bwd",
-                   "recurrence": "gated delta rule", "kernel_path": "simt-fp32", "steps": steps,
+                   "recurrence": "gated delta rule",
+                   "kernel_path": "tcgen05 sweeps, fp32 folds" if tc else "simt-fp32", "steps": steps,
                    "l2": "inputs larger than L2, no flush"},
-        "roofline": {"bound": "alu", "kernel": dom, "achieved": ach, "peak": FP32_ALU_TFLOPS,
-                     "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS, "alu_flops": fl,
-                     "launch_us": phase_ms[dom] * 1e3, "traffic": load_traffic(w.name, dom),
-                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2070 MHz"},
+        "roofline": roof,
         "path_roofline": {"bound": pr["bound"], "t_roofline_us": pr["t_roofline_us"],
                           "t_measured_us": ms * 1e3, "frac": pr["t_roofline_us"] / (ms * 1e3),
                           "flops": pr["flops"], "bytes": pr["bytes"], "peak_source": peak_src,

@@ -454,19 +454,28 @@ rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, const void* 
  *   rm_gdr_forward_apply    o
  *   rm_gdr_backward_prepare gamma [nseg,B,H,Dk,Dv] (the local adjoint at the
  *                           segment start, zero outgoing gradient) and
- *                           dq_t = scale S_t dO_t; saves the state before
- *                           every 16-token block in ws for the apply
+ *                           dq_t = scale S_t dO_t; saves states (every 16
+ *                           tokens, every 64 on the tensor cores) in ws
  *   rm_gdr_compose_suffix   dS_out[j] = fold over (j, fol_j) of D <- M_i^T D + gamma_i
  *   rm_gdr_backward_apply   from D = dS_out at each segment's end:
  *                           dk, dv [B,T,H,*] (dtype), dg, dbeta [B,T,H] fp32
  *                           (dg exactly 0 at sequence starts)
- * The problem is an rm_cp_problem (vector_gates = 0, any q_heads); these run
- * on generic fp32-arithmetic kernels for Dk in {16, 32, 64}, Dv a multiple of
- * 8 up to 128, segment lengths a multiple of 16 (RM_ERR_UNSUPPORTED
- * otherwise).  ws: rm_gdr_workspace_size bytes (B H (T / 16) Dk Dv fp32),
- * passed unchanged from rm_gdr_backward_prepare to rm_gdr_backward_apply.
- * Validation, ownership and errors as for the other calls.
+ * The problem is an rm_cp_problem (vector_gates = 0, any q_heads): Dk in
+ * {16, 32, 64}, Dv a multiple of 8 up to 128, segment lengths a multiple of
+ * 16 (RM_ERR_UNSUPPORTED otherwise).  bf16 storage with Dk = Dv = 64 and
+ * segment lengths that are multiples of 64 runs the four sweeps on the
+ * tensor cores in the chunkwise WY/UT form (per 64-token chunk the products
+ * of the I - beta k k^T factors as one triangular solve); everything else,
+ * and the two folds, on generic fp32-arithmetic kernels.  ws:
+ * rm_gdr_workspace_size bytes (B H (T / 16) Dk Dv fp32; the states the
+ * backward prepare saves for the apply), passed unchanged from
+ * rm_gdr_backward_prepare to rm_gdr_backward_apply.  Validation, ownership
+ * and errors as for the other calls.
+ *
+ * rm_gdr_path: 1 when the problem's sweeps run on the tensor cores, 0 on the
+ * generic kernels, -1 for a problem these calls reject.
  */
+int32_t rm_gdr_path(const rm_cp_problem* p);
 size_t rm_gdr_workspace_size(const rm_cp_problem* p);
 rm_status rm_gdr_forward_prepare(const rm_cp_problem* p, const void* k, const void* v,
                                  const float* g, const float* beta, float* M, float* dS,

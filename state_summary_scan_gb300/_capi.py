@@ -30,7 +30,8 @@ EXPORTS = (
     "rm_cp_device_status", "rm_cp_selftest_wait_timeout", "rm_cp_backward_noalloc",
     "rm_cp_step_host", "rm_cp_event_create", "rm_cp_event_destroy",
     "rm_ssd_workspace_size", "rm_ssd_map_inputs", "rm_ssd_finish_forward", "rm_ssd_finish_backward",
-    "rm_gdr_workspace_size", "rm_gdr_forward_prepare", "rm_gdr_compose_prefix", "rm_gdr_forward_apply",
+    "rm_gdr_path", "rm_gdr_workspace_size", "rm_gdr_forward_prepare", "rm_gdr_compose_prefix",
+    "rm_gdr_forward_apply",
     "rm_gdr_backward_prepare", "rm_gdr_compose_suffix", "rm_gdr_backward_apply",
 )
 
@@ -100,6 +101,7 @@ _SIGS = {
     "rm_ssd_map_inputs": (_S, [_PP, ctypes.c_int32] + [_P] * 8),
     "rm_ssd_finish_forward": (_S, [_PP, _P, _P, _P, _P]),
     "rm_ssd_finish_backward": (_S, [_PP, ctypes.c_int32] + [_P] * 17),
+    "rm_gdr_path": (ctypes.c_int32, [_PP]),
     "rm_gdr_workspace_size": (ctypes.c_size_t, [_PP]),
     "rm_gdr_forward_prepare": (_S, [_PP] + [_P] * 7),
     "rm_gdr_compose_prefix": (_S, [_PP] + [_P] * 4),
@@ -326,6 +328,10 @@ def rm_ssd_finish_backward(p, G, x, dt, A, Bm, dy, D, dq, dk, dv, dg, ddt, dA, d
 
 
 # ----------------------------------------------------------------- gated delta rule
+
+def rm_gdr_path(p: ProblemSpec) -> int:
+    return int(load().rm_gdr_path(p.ref))
+
 
 def rm_gdr_workspace_size(p: ProblemSpec) -> int:
     return int(load().rm_gdr_workspace_size(p.ref))

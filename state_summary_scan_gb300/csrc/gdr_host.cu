@@ -21,8 +21,8 @@ rm_status check_gdr(const rm_cp_problem* p, rmcp::Dims* d) {
 
 rm_status run(rmcp::GdrOp op, const rm_cp_problem* p, const rmcp::Dims& d, const rmcp::GdrPtrs& x,
               rm_stream_t stream) {
-    // the forward's two sweeps take the tensor cores where they can
-    const bool tc = (op == rmcp::GdrOp::kPrepare || op == rmcp::GdrOp::kApply) &&
+    // the four sweeps take the tensor cores where they can (the folds stay generic)
+    const bool tc = op != rmcp::GdrOp::kComposePrefix && op != rmcp::GdrOp::kComposeSuffix &&
                     rmcp::gdrtc_supports(d, p->dtype);
     rm_status st = tc ? rmcp::launch_gdrtc(op, d, x, reinterpret_cast<cudaStream_t>(stream))
                       : rmcp::launch_gdr(op, d, p->dtype, x, reinterpret_cast<cudaStream_t>(stream));
@@ -45,6 +45,12 @@ rm_status run(rmcp::GdrOp op, const rm_cp_problem* p, const rmcp::Dims& d, const
     } while (0)
 
 extern "C" {
+
+int32_t rm_gdr_path(const rm_cp_problem* p) {
+    rmcp::Dims d;
+    if (rmcp::api_check_problem(p, &d) != RM_OK || d.vg || !rmcp::gdr_supports(d)) return -1;
+    return rmcp::gdrtc_supports(d, p->dtype) ? 1 : 0;
+}
 
 size_t rm_gdr_workspace_size(const rm_cp_problem* p) {
     rmcp::Dims d;

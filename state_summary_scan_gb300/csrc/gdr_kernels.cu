@@ -231,51 +231,80 @@ __global__ void __launch_bounds__(128) gdr_gamma_sweep(Dims d, const T* __restri
 // ---------------------------------------------------------------------------
 // Summary folds with matrix transitions: each column of the carried state
 // folds on its own (S <- M S + X acts column by column), so one CTA takes
-// kFoldCols columns of one (row, head).  Thread (r, q): state row r and
-// columns q * CPT .. q * CPT + CPT - 1 of the block (CPT = kFoldCols * DK /
-// 256); the carried block and M_i [DK][DK] sit in shared memory.
+// fold_cols(DK) columns of one (row, head): 4 for Dk = 64 (one column a
+// thread), the 256 / DK columns of one thread a row otherwise.  Thread (r, q):
+// state row r and columns q * CPT .. q * CPT + CPT - 1 of the block; the
+// carried block and M_i [DK][DK] sit in shared memory.  The next segment's
+// M_i and X_i are loaded into registers while the current one is folded, so
+// that the chain of folds waits on shared memory only.
 //   prefix: S_in[j] = fold over [pre_j, j) of S <- M_i S + dS_i  (from 0)
 //   suffix: dS_out[j] = fold over (j, fol_j) of D <- M_i^T D + gamma_i,
 //           from the last segment down (from 0)
-// grid (B*H, ceil(Dv / kFoldCols)); block 256.
+// grid (B*H, ceil(Dv / fold_cols(DK))); block 256.
 // ---------------------------------------------------------------------------
-constexpr int kFoldCols = 16;
+__host__ __device__ constexpr int fold_cols(int dk) { return 256 / dk > 4 ? 256 / dk : 4; }
 
 template <int DK, bool SUFFIX>
 __global__ void __launch_bounds__(256) gdr_compose(Dims d, const float* __restrict__ M,
                                                    const float* __restrict__ X,
                                                    const int32_t* __restrict__ range,
                                                    float* __restrict__ out) {
-    constexpr int TPR = 256 / DK;            // threads per state row
-    constexpr int CPT = kFoldCols / TPR;     // columns per thread
-    static_assert(CPT >= 1, "fold block narrower than the threads of a row");
+    constexpr int FC = fold_cols(DK);
+    constexpr int TPR = 256 / DK;       // threads per state row
+    constexpr int CPT = FC / TPR;       // columns per thread
+    constexpr int MPT = DK * DK / 256;  // entries of M_i a thread loads
+    static_assert(CPT >= 1 && MPT >= 1, "fold block narrower than the threads of a row");
     __shared__ float m_s[DK][DK + 1];
-    __shared__ float s_s[2][DK][kFoldCols];
+    __shared__ float s_s[2][DK][FC];
     const int bh = blockIdx.x;
     const int b = bh / d.H, h = bh % d.H;
     const int r = threadIdx.x / TPR, q = threadIdx.x % TPR;
-    const int c0 = blockIdx.y * kFoldCols + q * CPT;  // this thread's first column
+    const int c0 = blockIdx.y * FC + q * CPT;  // this thread's first column
     const int n = d.nseg;
     int buf = 0;  // s_s[buf] holds the carried block
+    float mp[MPT], xp[CPT];
+    int pf = -1;  // the segment whose M_i and X_i are in mp and xp (the same in every thread)
+    auto prefetch = [&](int i) {
+        const float* mi = M + ((int64_t(i) * d.B + b) * d.H + h) * DK * DK;
+#pragma unroll
+        for (int u = 0; u < MPT; ++u) mp[u] = __ldg(mi + threadIdx.x + 256 * u);
+        const float* xi = X + sum_off(d, i, b, h) + int64_t(r) * d.Dv;
+#pragma unroll
+        for (int u = 0; u < CPT; ++u) xp[u] = c0 + u < d.Dv ? __ldg(xi + c0 + u) : 0.f;
+        pf = i;
+    };
     auto clear = [&]() {
 #pragma unroll
         for (int u = 0; u < CPT; ++u) s_s[buf][r][q * CPT + u] = 0.f;
     };
     // s_s[buf ^ 1] = M_i s_s[buf] + X_i (M_i^T for the suffix); buf flips
     auto fold = [&](int i) {
+        if (pf != i) prefetch(i);
         __syncthreads();  // earlier readers of m_s and s_s are done
-        const float* mi = M + ((int64_t(i) * d.B + b) * d.H + h) * DK * DK;
-        batched_copy(DK * DK, [&](int e) { return __ldg(mi + e); }, [&](int e, float x) { m_s[e / DK][e % DK] = x; });
-        __syncthreads();
-        const float* xi = X + sum_off(d, i, b, h) + int64_t(r) * d.Dv;
+#pragma unroll
+        for (int u = 0; u < MPT; ++u) {
+            const int e = threadIdx.x + 256 * u;
+            m_s[e / DK][e % DK] = mp[u];
+        }
+        float acc[CPT][4];
 #pragma unroll
         for (int u = 0; u < CPT; ++u) {
-            const int col = c0 + u;
-            float acc = col < d.Dv ? xi[col] : 0.f;
-#pragma unroll 16
-            for (int c = 0; c < DK; ++c)
-                acc = fmaf(SUFFIX ? m_s[c][r] : m_s[r][c], s_s[buf][c][q * CPT + u], acc);
-            s_s[buf ^ 1][r][q * CPT + u] = acc;
+            acc[u][0] = xp[u];
+            acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+        }
+        const int nx = SUFFIX ? i - 1 : i + 1;  // the likely next fold
+        if (nx >= 0 && nx < n) prefetch(nx);
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < CPT; ++u) {
+#pragma unroll 4
+            for (int c = 0; c < DK; c += 4) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    acc[u][w] = fmaf(SUFFIX ? m_s[c + w][r] : m_s[r][c + w], s_s[buf][c + w][q * CPT + u],
+                                     acc[u][w]);
+            }
+            s_s[buf ^ 1][r][q * CPT + u] = (acc[u][0] + acc[u][1]) + (acc[u][2] + acc[u][3]);
         }
         buf ^= 1;
     };
@@ -640,7 +669,7 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
         }
         case GdrOp::kComposePrefix:
         case GdrOp::kComposeSuffix: {
-            const dim3 grid(BH, (d.Dv + kFoldCols - 1) / kFoldCols);
+            const dim3 grid(BH, (d.Dv + fold_cols(d.Dk) - 1) / fold_cols(d.Dk));
             if (op == GdrOp::kComposePrefix) {
                 RMCP_GDR_DK_SWITCH((gdr_compose<DK, false><<<grid, 256, 0, s>>>(
                     d, p.M, p.dS, d.preceding_start, p.S_in_out)));

@@ -499,6 +499,643 @@ __global__ void __launch_bounds__(256, 1)
     if (G.warp == 0) tmem_dealloc(tmem, 256);
 }
 
+
+// Row tau, columns c0..c0+15 of the within-sequence decay Gam[tau][r] =
+// exp(b_tau - b_r) for r < tau (strict) or r <= tau, 0 elsewhere.
+__device__ __forceinline__ void decay16(const GateSmem& gs, int tau, int c0, bool strict, float* m) {
+    const int lt = gs.lid[tau];
+    const float bt = gs.b[tau];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const int r = c0 + e;
+        m[e] = ((strict ? r < tau : r <= tau) && gs.lid[r] == lt) ? __expf(bt - gs.b[r]) : 0.f;
+    }
+}
+
+// The state row tau, columns c0..c0+15, of a [64][64] fp32 block at src.
+__device__ __forceinline__ void load_row16(const float* src, int tau, int c0, float* x) {
+    const float* p = src + tau * kD + c0;
+#pragma unroll
+    for (int e = 0; e < 16; e += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(p + e);
+        x[e] = v.x; x[e + 1] = v.y; x[e + 2] = v.z; x[e + 3] = v.w;
+    }
+}
+__device__ __forceinline__ void save_row16(float* dst, int tau, int c0, const float* x) {
+    float* p = dst + tau * kD + c0;
+#pragma unroll
+    for (int e = 0; e < 16; e += 4)
+        *reinterpret_cast<float4*>(p + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+}
+
+// Per-block state of the backward kernels (static shared memory).
+struct BwdShared {
+    GateSmem gs;
+    alignas(16) float beta_s[kChunk];
+    float red[3][2][kChunk];  // row partials of the gate, key-norm and beta terms, by column half
+    float dbm[kChunk];        // row sum minus column sum of the score-gradient products
+    float red_se[8];          // per-warp <S_prev, E>
+    alignas(8) uint64_t full[2];
+    alignas(8) uint64_t mbar;
+    uint32_t tmem_slot;
+};
+
+__device__ __forceinline__ void bwd_setup(BwdShared& sh, const Geo& G, int cols) {
+    if (G.tid == 0) {
+        mbar_init(smem_u32(&sh.full[0]), 1);
+        mbar_init(smem_u32(&sh.full[1]), 1);
+        mbar_init(smem_u32(&sh.mbar), 1);
+        mbar_fence_init();
+    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&sh.tmem_slot), cols);
+}
+
+// ===========================================================================
+// backward prepare, dq walk (blockIdx.z == 0): the forward recurrence again
+// from S_in with dO in place of the queries,
+//     dq = scale (gam o (dO S_prev^T) + mask(dO D^T o Gam) K),
+// (dq_t = scale S_t dO_t with S_t = gam_t S_prev + sum_{r<=t} Gam[t][r] k_r D_r^T)
+// and S_prev saved to the workspace before each chunk.
+// Shared memory: two stages of K|V|dO; K o gam, K o Gam[63], scale dO o gam,
+// T, -W, D, S, P, dq staging (bf16); fp32 A, X, Y.
+// Tensor memory: [0,64) K K^T, then dO D^T; [64,128) dq; [128,192) W, then
+// the state product; [192,256) U, then D.
+// ===========================================================================
+constexpr uint32_t DQ_STAGE = 3 * T8;
+constexpr uint32_t DQ_KG = 2 * DQ_STAGE, DQ_KC = DQ_KG + T8, DQ_OG = DQ_KC + T8, DQ_T = DQ_OG + T8;
+constexpr uint32_t DQ_WN = DQ_T + T8, DQ_DL = DQ_WN + T8, DQ_S = DQ_DL + T8, DQ_P = DQ_S + T8;
+constexpr uint32_t DQ_O = DQ_P + T8, DQ_F32 = DQ_O + T8;
+constexpr size_t kDqSmem = DQ_F32 + 3 * kD * kP * sizeof(float) + 1024;
+
+__device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, const CUtensorMap* mv,
+                                        const CUtensorMap* mo, const CUtensorMap* mdq,
+                                        const float* __restrict__ g, const float* __restrict__ beta,
+                                        const float* __restrict__ S_in, float* __restrict__ ws,
+                                        uint8_t* smem, BwdShared& sh, uint32_t tmem, const Geo& G) {
+    float* La = reinterpret_cast<float*>(smem + DQ_F32);
+    float* Xs = La + kD * kP;
+    float* Ys = Xs + kD * kP;
+    constexpr uint32_t TKK = 0, TQ = 64, TW = 128, TD = 192;
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+    const int c0 = 32 * G.grp + 16 * G.hi;
+    float* ck = ws + ((int64_t(seg) * d.B + b) * d.H + h) * nch * int64_t(kD * kD);
+
+    float Sr[16];
+    load_row16(S_in + sum_off(d, seg, b, h), G.tau, c0, Sr);
+    store_row16(smem + DQ_S, G.tau, c0, Sr);
+    auto load = [&](int c, int s) {
+        const int row = b * d.T + a0 + c * kChunk;
+        const uint32_t bar = smem_u32(&sh.full[s]);
+        uint8_t* st = smem + s * DQ_STAGE;
+        mbar_expect_tx(bar, DQ_STAGE);
+        tma_load_3d(smem_u32(st), mk, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + T8), mv, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + 2 * T8), mo, 0, h, row, bar);
+    };
+    if (G.tid == 0) {
+        load(0, 0);
+        if (nch > 1) load(1, 1);
+    }
+    const uint32_t sb0 = smem_u32(smem);
+    const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
+    uint32_t mph = 0;
+    for (int c = 0; c < nch; ++c) {
+        const int s = c & 1;
+        const int t0 = a0 + c * kChunk;
+        uint8_t* Ks = smem + s * DQ_STAGE;
+        uint8_t* Os = Ks + 2 * T8;
+        save_row16(ck + int64_t(c) * kD * kD, G.tau, c0, Sr);
+        chunk_gates(d, g, beta, b, h, t0, sh.gs, sh.beta_s, G);
+        if (G.tid == 0) {
+            if (c >= 1 && c + 1 < nch) load(c + 1, s ^ 1);  // the previous chunk's products are done
+            if (c >= 1) bulk_wait_read();                    // the dq store has read its staging tile
+        }
+        __syncthreads();
+        mbar_wait(smem_u32(&sh.full[s]), (c >> 1) & 1);
+        tc_fence_after();
+        if (G.tid == 0) {
+            const uint64_t k = desc_plus(DK, s * DQ_STAGE);
+            mma_kk(tmem + TKK, k, k, 0);  // K K^T
+        }
+        rows_scaled(Ks, smem + DQ_KG, sh.gs.win, 1.f, G.tid);      // K o gam
+        rows_scaled(Ks, smem + DQ_KC, sh.gs.wout, 1.f, G.tid);     // K o Gam[63]
+        rows_scaled(Os, smem + DQ_OG, sh.gs.win, d.scale, G.tid);  // scale dO o gam
+        cta_sync_tc();
+        if (G.tid == 0) mma_kk(tmem + TQ, desc_plus(DK, DQ_OG), desc_plus(DK, DQ_S), 0);  // (scale dO o gam) S^T
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float kk[16];
+            tok16(tmem, G, TKK + 32 * G.grp, kk);
+            a_row16(sh.gs, sh.beta_s, kk, G.tau, c0, La);
+        }
+        __syncthreads();
+        tri_inverse(La, Xs, Ys);
+        t_row16(Xs, sh.beta_s, G.tau, c0, smem + DQ_T);
+        cta_sync_tc();
+        if (G.tid == 0) {  // W = T (K o gam), U = T V
+            const uint64_t t = desc_plus(DK, DQ_T);
+            mma_km(tmem + TW, t, desc_plus(DM, DQ_KG), 0);
+            mma_km(tmem + TD, t, desc_plus(DM, s * DQ_STAGE + T8), 0);
+        }
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float w[16];
+            tok16(tmem, G, TW + 32 * G.grp, w);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = -w[e];
+            store_row16(smem + DQ_WN, G.tau, c0, w);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) mma_km(tmem + TD, desc_plus(DK, DQ_WN), desc_plus(DM, DQ_S), 1);  // D = U - W S_prev
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float x[16];
+            tok16(tmem, G, TD + 32 * G.grp, x);
+            store_row16(smem + DQ_DL, G.tau, c0, x);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) {
+            mma_kk(tmem + TKK, desc_plus(DK, s * DQ_STAGE + 2 * T8), desc_plus(DK, DQ_DL), 0);  // dO D^T
+            mma_mm(tmem + TW, desc_plus(DM, DQ_KC), desc_plus(DM, DQ_DL), 0);               // (K o Gam[63])^T D
+        }
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float p[16], m[16], y[16];
+            tok16(tmem, G, TKK + 32 * G.grp, p);
+            decay16(sh.gs, G.tau, c0, false, m);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) p[e] *= d.scale * m[e];
+            store_row16(smem + DQ_P, G.tau, c0, p);
+            tok16(tmem, G, TW + 32 * G.grp, y);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) Sr[e] = fmaf(sh.gs.W, Sr[e], y[e]);
+            store_row16(smem + DQ_S, G.tau, c0, Sr);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) mma_km(tmem + TQ, desc_plus(DK, DQ_P), desc_plus(DM, s * DQ_STAGE), 1);  // + P K
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float x[16];
+            tok16(tmem, G, TQ + 32 * G.grp, x);
+            store_row16(smem + DQ_O, G.tau, c0, x);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) {
+            tma_store_3d(mdq, smem_u32(smem + DQ_O), 0, h, b * d.T + t0);
+            bulk_commit();
+        }
+    }
+    if (G.tid == 0) bulk_wait_all();
+}
+
+// ===========================================================================
+// backward prepare, gamma walk (blockIdx.z == 1): the adjoint E of the state
+// walked back from the segment end with E = 0 there, chunk by chunk,
+//     dD = P^T dO + (K o Gam[63]) E,   dX = T^T dD,
+//     E <- scale (Q o gam)^T dO + gam_63 E - (K o gam)^T dX,
+// gamma = E at the segment start.  No state is needed.
+// Shared memory: two stages of Q|K|dO; K o gam, K o Gam[63], scale Q o gam,
+// P, T, dD, -dX, E (bf16); fp32 A, X, Y.
+// Tensor memory: [0,64) K K^T, then dX; [64,128) Q K^T; [128,192) dD;
+// [192,256) the E product.
+// ===========================================================================
+constexpr uint32_t GA_STAGE = 3 * T8;
+constexpr uint32_t GA_KG = 2 * GA_STAGE, GA_KC = GA_KG + T8, GA_QG = GA_KC + T8, GA_P = GA_QG + T8;
+constexpr uint32_t GA_T = GA_P + T8, GA_DD = GA_T + T8, GA_DX = GA_DD + T8, GA_E = GA_DX + T8;
+constexpr uint32_t GA_F32 = GA_E + T8;
+constexpr size_t kGaSmem = GA_F32 + 3 * kD * kP * sizeof(float) + 1024;
+constexpr size_t kBwdPrepSmem = kDqSmem > kGaSmem ? kDqSmem : kGaSmem;
+
+__device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq, const CUtensorMap* mk,
+                                           const CUtensorMap* mo, const float* __restrict__ g,
+                                           const float* __restrict__ beta, float* __restrict__ gamma,
+                                           uint8_t* smem, BwdShared& sh, uint32_t tmem, const Geo& G) {
+    float* La = reinterpret_cast<float*>(smem + GA_F32);
+    float* Xs = La + kD * kP;
+    float* Ys = Xs + kD * kP;
+    constexpr uint32_t TKK = 0, TQK = 64, TDD = 128, TE = 192;
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+    const int c0 = 32 * G.grp + 16 * G.hi;
+
+    float Er[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) Er[e] = 0.f;
+    store_row16(smem + GA_E, G.tau, c0, Er);
+    auto load = [&](int c, int s) {
+        const int row = b * d.T + a0 + c * kChunk;
+        const uint32_t bar = smem_u32(&sh.full[s]);
+        uint8_t* st = smem + s * GA_STAGE;
+        mbar_expect_tx(bar, GA_STAGE);
+        tma_load_3d(smem_u32(st), mq, 0, h / d.qdiv, row, bar);
+        tma_load_3d(smem_u32(st + T8), mk, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + 2 * T8), mo, 0, h, row, bar);
+    };
+    if (G.tid == 0) {
+        load(nch - 1, 0);
+        if (nch > 1) load(nch - 2, 1);
+    }
+    const uint32_t sb0 = smem_u32(smem);
+    const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
+    uint32_t mph = 0;
+    for (int it = 0; it < nch; ++it) {
+        const int c = nch - 1 - it, s = it & 1;
+        const int t0 = a0 + c * kChunk;
+        uint8_t* Qs = smem + s * GA_STAGE;
+        uint8_t* Ks = Qs + T8;
+        chunk_gates(d, g, beta, b, h, t0, sh.gs, sh.beta_s, G);
+        if (G.tid == 0 && it >= 1 && it + 1 < nch) load(c - 1, s ^ 1);  // the previous chunk's products are done
+        __syncthreads();
+        mbar_wait(smem_u32(&sh.full[s]), (it >> 1) & 1);
+        tc_fence_after();
+        if (G.tid == 0) {  // K K^T and Q K^T
+            const uint64_t q = desc_plus(DK, s * GA_STAGE), k = desc_plus(q, T8);
+            mma_kk(tmem + TKK, k, k, 0);
+            mma_kk(tmem + TQK, q, k, 0);
+        }
+        rows_scaled(Ks, smem + GA_KG, sh.gs.win, 1.f, G.tid);      // K o gam
+        rows_scaled(Ks, smem + GA_KC, sh.gs.wout, 1.f, G.tid);     // K o Gam[63]
+        rows_scaled(Qs, smem + GA_QG, sh.gs.win, d.scale, G.tid);  // scale Q o gam
+        cta_sync_tc();
+        if (G.tid == 0) {
+            mma_km(tmem + TDD, desc_plus(DK, GA_KC), desc_plus(DM, GA_E), 0);                // (K o Gam[63]) E
+            mma_mm(tmem + TE, desc_plus(DM, GA_QG), desc_plus(DM, s * GA_STAGE + 2 * T8), 0);  // (scale Q o gam)^T dO
+        }
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float kk[16], qk[16], m[16];
+            tok16(tmem, G, TKK + 32 * G.grp, kk);
+            a_row16(sh.gs, sh.beta_s, kk, G.tau, c0, La);
+            tok16(tmem, G, TQK + 32 * G.grp, qk);
+            decay16(sh.gs, G.tau, c0, false, m);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) qk[e] *= d.scale * m[e];
+            store_row16(smem + GA_P, G.tau, c0, qk);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) mma_mm(tmem + TDD, desc_plus(DM, GA_P), desc_plus(DM, s * GA_STAGE + 2 * T8), 1);  // + P^T dO
+        tri_inverse(La, Xs, Ys);
+        t_row16(Xs, sh.beta_s, G.tau, c0, smem + GA_T);
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float x[16];
+            tok16(tmem, G, TDD + 32 * G.grp, x);
+            store_row16(smem + GA_DD, G.tau, c0, x);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) mma_mm(tmem + TKK, desc_plus(DM, GA_T), desc_plus(DM, GA_DD), 0);  // dX = T^T dD
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float x[16];
+            tok16(tmem, G, TKK + 32 * G.grp, x);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = -x[e];
+            store_row16(smem + GA_DX, G.tau, c0, x);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) mma_mm(tmem + TE, desc_plus(DM, GA_KG), desc_plus(DM, GA_DX), 1);  // - (K o gam)^T dX
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float x[16];
+            tok16(tmem, G, TE + 32 * G.grp, x);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) Er[e] = fmaf(sh.gs.W, Er[e], x[e]);
+            store_row16(smem + GA_E, G.tau, c0, Er);
+        }
+        cta_sync_tc();
+    }
+    save_row16(gamma + sum_off(d, seg, b, h), G.tau, c0, Er);
+}
+
+__global__ void __launch_bounds__(256, 1)
+    gdrtc_bwd_prepare_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                             const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                             const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mdq,
+                             const float* __restrict__ g, const float* __restrict__ beta,
+                             const float* __restrict__ S_in, float* __restrict__ gamma, float* __restrict__ ws) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    __shared__ BwdShared sh;
+    const Geo G = geo();
+    bwd_setup(sh, G, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_slot;
+    if (blockIdx.z == 0)
+        dq_walk(d, &mk, &mv, &mo, &mdq, g, beta, S_in, ws, smem, sh, tmem, G);
+    else
+        gamma_walk(d, &mq, &mk, &mo, g, beta, gamma, smem, sh, tmem, G);
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ===========================================================================
+// backward apply: one CTA per (segment, row, head), chunks last to first,
+// E = dS_out at the segment end and S_prev of each chunk from the workspace.
+// With L = I + A, P = scale mask(Q K^T o Gam), X = V - (K o gam) S_prev and
+// D = T X as in the forward, and G = K K^T:
+//     dD  = P^T dO + (K o Gam[63]) E,   dZ = L^{-T} dD,   dv = dX = beta o dZ
+//     dA  = -strict_lower(dZ D^T),     dG = dA o beta_t o Gam
+//     dk  = scale mask(dO D^T o Gam)^T Q + (dG + dG^T) K
+//           + Gam[63] o (D E^T) - gam o (dX S_prev^T)
+//     dbeta_t = dZ_t . X_t + sum_r dA[t][r] G[t][r] Gam[t][r]
+//     E  <- scale (Q o gam)^T dO + gam_63 E - (K o gam)^T dX
+// and, through the running gate sums b_t (Gam, gam, Gam[63] and gam_63 are
+// exponentials of their differences), the gradient db_t:
+//     row sum minus column sum of M1 + M2 with M1 = P o (dO D^T), M2 = dA o A,
+//     + scale gam_t q_t . (S_prev dO_t) - gam_t k_t . (S_prev dX_t) - w_t,
+//     w_t = Gam[63][t] k_t . (E D_t), and at t = 63 + gam_63 <S_prev, E> + sum_r w_r;
+// dg_u = sum_{t >= u} db_t inside the chunk (0 where a sequence starts).
+// Shared memory (8 KB tiles): two stages of Q|K|V|dO; K o gam, K o Gam[63]
+// (then dZ), scale Q o gam (then scale mask(dO D^T o Gam)), S, E, P (then
+// -dX), T (then dG + dG^T), L^{-1}, X (then dD), D, dv and dk staging; fp32
+// A (then dG), X, Y (then M1 + M2) work arrays.
+// Tensor memory (64 columns each): K K^T then dZ; Q K^T then the dk
+// product; (K o gam) S_prev, D, then dZ D^T; dD, dO D^T, then -dX S_prev^T;
+// the E product; dO S_prev^T; D E^T.
+// ===========================================================================
+constexpr uint32_t BA_STAGE = 4 * T8;
+constexpr uint32_t BA_KG = 2 * BA_STAGE, BA_KC = BA_KG + T8, BA_QG = BA_KC + T8, BA_S = BA_QG + T8;
+constexpr uint32_t BA_E = BA_S + T8, BA_P = BA_E + T8, BA_T = BA_P + T8, BA_LI = BA_T + T8;
+constexpr uint32_t BA_X = BA_LI + T8, BA_D = BA_X + T8, BA_SV = BA_D + T8, BA_SK = BA_SV + T8;
+constexpr uint32_t BA_F32 = BA_SK + T8;
+constexpr size_t kBwdApplySmem = BA_F32 + 3 * kD * kP * sizeof(float) + 1024;
+
+__global__ void __launch_bounds__(256, 1)
+    gdrtc_bwd_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                           const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                           const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mdk,
+                           const __grid_constant__ CUtensorMap mdv, const float* __restrict__ g,
+                           const float* __restrict__ beta, const float* __restrict__ dS_out,
+                           const float* __restrict__ ws, float* __restrict__ dg, float* __restrict__ dbeta) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    float* La = reinterpret_cast<float*>(smem + BA_F32);
+    float* Xs = La + kD * kP;
+    float* Ys = Xs + kD * kP;
+    __shared__ BwdShared sh;
+    constexpr uint32_t TKK = 0, TQK = 64, TX = 128, TDD = 192, TE = 256, TOS = 320, TDE = 384;
+    constexpr uint32_t TZ = TKK, TK = TQK, TD = TX, TDA = TX, TOD = TDD, TXS = TDD;
+
+    const Geo G = geo();
+    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int nch = d.L / kChunk;
+    const int a0 = seg * d.L;
+    const int c0 = 32 * G.grp + 16 * G.hi;
+    const float* ck = ws + ((int64_t(seg) * d.B + b) * d.H + h) * nch * int64_t(kD * kD);
+
+    bwd_setup(sh, G, 512);
+    float Er[16];
+    load_row16(dS_out + sum_off(d, seg, b, h), G.tau, c0, Er);
+    store_row16(smem + BA_E, G.tau, c0, Er);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_slot;
+    auto load = [&](int c, int s) {
+        const int row = b * d.T + a0 + c * kChunk;
+        const uint32_t bar = smem_u32(&sh.full[s]);
+        uint8_t* st = smem + s * BA_STAGE;
+        mbar_expect_tx(bar, BA_STAGE);
+        tma_load_3d(smem_u32(st), &mq, 0, h / d.qdiv, row, bar);
+        tma_load_3d(smem_u32(st + T8), &mk, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + 2 * T8), &mv, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + 3 * T8), &mo, 0, h, row, bar);
+    };
+    if (G.tid == 0) {
+        load(nch - 1, 0);
+        if (nch > 1) load(nch - 2, 1);
+    }
+    const uint32_t sb0 = smem_u32(smem);
+    const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
+    uint32_t mph = 0;
+    for (int it = 0; it < nch; ++it) {
+        const int c = nch - 1 - it, s = it & 1;
+        const int t0 = a0 + c * kChunk;
+        uint8_t* Qs = smem + s * BA_STAGE;
+        uint8_t* Ks = Qs + T8;
+        uint8_t* Vs = Ks + T8;
+        const uint32_t sq = s * BA_STAGE, sk = sq + T8, so = sq + 3 * T8;
+        float Sr[16];
+        load_row16(ck + int64_t(c) * kD * kD, G.tau, c0, Sr);
+        store_row16(smem + BA_S, G.tau, c0, Sr);
+        chunk_gates(d, g, beta, b, h, t0, sh.gs, sh.beta_s, G);
+        if (G.tid == 0) {
+            if (it >= 1 && it + 1 < nch) load(c - 1, s ^ 1);  // the previous chunk's products are done
+            if (it >= 1) bulk_wait_read();                     // the dv and dk stores have read their tiles
+        }
+        __syncthreads();
+        mbar_wait(smem_u32(&sh.full[s]), (it >> 1) & 1);
+        tc_fence_after();
+        if (G.tid == 0) {  // K K^T and Q K^T
+            mma_kk(tmem + TKK, desc_plus(DK, sk), desc_plus(DK, sk), 0);
+            mma_kk(tmem + TQK, desc_plus(DK, sq), desc_plus(DK, sk), 0);
+        }
+        rows_scaled(Ks, smem + BA_KG, sh.gs.win, 1.f, G.tid);      // K o gam
+        rows_scaled(Ks, smem + BA_KC, sh.gs.wout, 1.f, G.tid);     // K o Gam[63]
+        rows_scaled(Qs, smem + BA_QG, sh.gs.win, d.scale, G.tid);  // scale Q o gam
+        cta_sync_tc();
+        if (G.tid == 0) {
+            mma_km(tmem + TX, desc_plus(DK, BA_KG), desc_plus(DM, BA_S), 0);   // (K o gam) S_prev
+            mma_km(tmem + TDD, desc_plus(DK, BA_KC), desc_plus(DM, BA_E), 0);  // (K o Gam[63]) E
+            mma_mm(tmem + TE, desc_plus(DM, BA_QG), desc_plus(DM, so), 0);     // (scale Q o gam)^T dO
+            mma_kk(tmem + TOS, desc_plus(DK, so), desc_plus(DK, BA_S), 0);     // dO S_prev^T
+        }
+        commit_wait(&sh.mbar, mph, G.tid);
+        // kg = G o Gam (strict, within a sequence) and X stay in registers
+        float kg[16], Xr[16];
+        {
+            float kk[16], qk[16], tx[16], m[16];
+            tok16(tmem, G, TKK + 32 * G.grp, kk);
+            tok16(tmem, G, TQK + 32 * G.grp, qk);
+            tok16(tmem, G, TX + 32 * G.grp, tx);
+            tile_row_get16(Vs, G.tau, c0, Xr);
+            decay16(sh.gs, G.tau, c0, false, m);
+            const float be = sh.beta_s[G.tau];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int r = c0 + e;
+                kg[e] = r < G.tau ? kk[e] * m[e] : 0.f;
+                La[G.tau * kP + r] = be * kg[e];
+                qk[e] *= d.scale * m[e];
+                Xr[e] -= tx[e];
+            }
+            store_row16(smem + BA_P, G.tau, c0, qk);
+            store_row16(smem + BA_X, G.tau, c0, Xr);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) mma_mm(tmem + TDD, desc_plus(DM, BA_P), desc_plus(DM, so), 1);  // + P^T dO
+        tri_inverse(La, Xs, Ys);
+        {
+            float x[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = Xs[G.tau * kP + c0 + e];
+            store_row16(smem + BA_LI, G.tau, c0, x);
+            t_row16(Xs, sh.beta_s, G.tau, c0, smem + BA_T);
+        }
+        cta_sync_tc();
+        if (G.tid == 0) mma_km(tmem + TD, desc_plus(DK, BA_T), desc_plus(DM, BA_X), 0);  // D = T X
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float x[16], y[16];
+            tok16(tmem, G, TD + 32 * G.grp, x);
+            store_row16(smem + BA_D, G.tau, c0, x);
+            tok16(tmem, G, TDD + 32 * G.grp, y);
+            store_row16(smem + BA_X, G.tau, c0, y);  // dD
+        }
+        cta_sync_tc();
+        if (G.tid == 0) {
+            mma_mm(tmem + TZ, desc_plus(DM, BA_LI), desc_plus(DM, BA_X), 0);  // dZ = L^{-T} dD
+            mma_kk(tmem + TOD, desc_plus(DK, so), desc_plus(DK, BA_D), 0);    // dO D^T
+            mma_kk(tmem + TDE, desc_plus(DK, BA_D), desc_plus(DK, BA_E), 0);  // D E^T
+        }
+        commit_wait(&sh.mbar, mph, G.tid);
+        float pb = 0.f, pw = 0.f;  // this thread's parts of dbeta_t and of k_t . (E D_t)
+        {
+            float z[16], od[16], qk[16], de[16], kv[16], m[16], x[16];
+            tok16(tmem, G, TZ + 32 * G.grp, z);
+            tok16(tmem, G, TOD + 32 * G.grp, od);
+            tok16(tmem, G, TQK + 32 * G.grp, qk);
+            tok16(tmem, G, TDE + 32 * G.grp, de);
+            tile_row_get16(Ks, G.tau, c0, kv);
+            decay16(sh.gs, G.tau, c0, false, m);
+            const float be = sh.beta_s[G.tau];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                pb = fmaf(z[e], Xr[e], pb);
+                pw = fmaf(kv[e], de[e], pw);
+                x[e] = be * z[e];
+            }
+            store_row16(smem + BA_KC, G.tau, c0, z);  // dZ
+            store_row16(smem + BA_SV, G.tau, c0, x);  // dv = dX
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = -x[e];
+            store_row16(smem + BA_P, G.tau, c0, x);   // -dX
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float p2 = d.scale * m[e] * od[e];
+                Ys[G.tau * kP + c0 + e] = p2 * qk[e];  // M1 = P o (dO D^T)
+                od[e] = p2;
+            }
+            store_row16(smem + BA_QG, G.tau, c0, od);  // scale mask(dO D^T o Gam)
+        }
+        cta_sync_tc();
+        if (G.tid == 0) {
+            tma_store_3d(&mdv, smem_u32(smem + BA_SV), 0, h, b * d.T + t0);
+            bulk_commit();
+            mma_mm(tmem + TE, desc_plus(DM, BA_KG), desc_plus(DM, BA_P), 1);   // - (K o gam)^T dX
+            mma_kk(tmem + TDA, desc_plus(DK, BA_KC), desc_plus(DK, BA_D), 0);  // dZ D^T
+            mma_kk(tmem + TXS, desc_plus(DK, BA_P), desc_plus(DK, BA_S), 0);   // -dX S_prev^T
+            mma_mm(tmem + TK, desc_plus(DM, BA_QG), desc_plus(DM, sq), 0);     // scale mask(dO D^T o Gam)^T Q
+        }
+        commit_wait(&sh.mbar, mph, G.tid);
+        float pse = 0.f;  // this thread's part of <S_prev, E>
+        {
+            float da[16], ee[16], m[16];
+            tok16(tmem, G, TDA + 32 * G.grp, da);
+            tok16(tmem, G, TE + 32 * G.grp, ee);
+            decay16(sh.gs, G.tau, c0, true, m);
+            const float be = sh.beta_s[G.tau];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int r = c0 + e;
+                const float a = r < G.tau ? -da[e] : 0.f;  // dA
+                pb = fmaf(a, kg[e], pb);
+                Ys[G.tau * kP + r] += a * be * kg[e];  // M2 = dA o A
+                La[G.tau * kP + r] = a * be * m[e];    // dG
+                pse = fmaf(Sr[e], Er[e], pse);
+                Er[e] = fmaf(sh.gs.W, Er[e], ee[e]);
+            }
+            store_row16(smem + BA_E, G.tau, c0, Er);
+        }
+        __syncthreads();
+        {
+            float x[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = La[G.tau * kP + c0 + e] + La[(c0 + e) * kP + G.tau];
+            store_row16(smem + BA_T, G.tau, c0, x);  // dG + dG^T
+            const int t = G.tid >> 2, part = G.tid & 3;
+            float rs = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) rs += Ys[t * kP + 16 * part + e] - Ys[(16 * part + e) * kP + t];
+            rs += __shfl_xor_sync(kFull, rs, 1);
+            rs += __shfl_xor_sync(kFull, rs, 2);
+            if (part == 0) sh.dbm[t] = rs;
+        }
+        cta_sync_tc();
+        if (G.tid == 0) mma_km(tmem + TK, desc_plus(DK, BA_T), desc_plus(DM, sk), 1);  // + (dG + dG^T) K
+        commit_wait(&sh.mbar, mph, G.tid);
+        {
+            float ka[16], de[16], xs[16], os[16], qv[16], kv[16];
+            tok16(tmem, G, TK + 32 * G.grp, ka);
+            tok16(tmem, G, TDE + 32 * G.grp, de);
+            tok16(tmem, G, TXS + 32 * G.grp, xs);
+            tok16(tmem, G, TOS + 32 * G.grp, os);
+            tile_row_get16(Qs, G.tau, c0, qv);
+            tile_row_get16(Ks, G.tau, c0, kv);
+            const float wo = sh.gs.wout[G.tau], gm = sh.gs.win[G.tau];
+            float pq = 0.f, pk = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                ka[e] += wo * de[e] + gm * xs[e];
+                pq = fmaf(qv[e], os[e], pq);
+                pk = fmaf(kv[e], xs[e], pk);
+            }
+            store_row16(smem + BA_SK, G.tau, c0, ka);
+            float rw = wo * pw;
+            float rdb = d.scale * gm * pq + gm * pk - rw;
+            rdb += __shfl_xor_sync(kFull, rdb, 16);
+            rw += __shfl_xor_sync(kFull, rw, 16);
+            pb += __shfl_xor_sync(kFull, pb, 16);
+            if (!G.hi) {
+                sh.red[0][G.grp][G.tau] = rdb;
+                sh.red[1][G.grp][G.tau] = rw;
+                sh.red[2][G.grp][G.tau] = pb;
+            }
+            pse = warp_sum(pse);
+            if (G.lane == 0) sh.red_se[G.warp] = pse;
+        }
+        cta_sync_tc();
+        if (G.tid == 0) {
+            tma_store_3d(&mdk, smem_u32(smem + BA_SK), 0, h, b * d.T + t0);
+            bulk_commit();
+        }
+        if (G.warp == 0) {  // tokens 2 lane and 2 lane + 1: db, the in-chunk suffix sums, dbeta
+            const int u0 = 2 * G.lane, u1 = u0 + 1;
+            float db0 = sh.red[0][0][u0] + sh.red[0][1][u0] + sh.dbm[u0];
+            float db1 = sh.red[0][0][u1] + sh.red[0][1][u1] + sh.dbm[u1];
+            const float wsum = warp_sum(sh.red[1][0][u0] + sh.red[1][1][u0] + sh.red[1][0][u1] + sh.red[1][1][u1]);
+            const float se = warp_sum(G.lane < 8 ? sh.red_se[G.lane] : 0.f);
+            if (u1 == kChunk - 1) db1 += sh.gs.W * se + wsum;
+            float suf = db0 + db1;  // inclusive suffix sum over lanes >= lane
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float x = __shfl_down_sync(kFull, suf, o);
+                if (G.lane + o < 32) suf += x;
+            }
+            const int ta = t0 + u0, tb = t0 + u1;
+            dg[g_off(d, b, ta, h)] = starts_sequence(d.seq_idx, ta) ? 0.f : suf;
+            dg[g_off(d, b, tb, h)] = starts_sequence(d.seq_idx, tb) ? 0.f : suf - db0;
+            dbeta[g_off(d, b, ta, h)] = sh.red[2][0][u0] + sh.red[2][1][u0];
+            dbeta[g_off(d, b, tb, h)] = sh.red[2][0][u1] + sh.red[2][1][u1];
+        }
+    }
+    if (G.tid == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 512);
+}
+
+__global__ void read_flag_kernel(int* out, int clear) {
+    *out = g_timeout_flag;
+    if (clear) g_timeout_flag = 0;
+}
+
 }  // namespace
 }  // namespace gdrtc
 
@@ -511,22 +1148,49 @@ rm_status launch_gdrtc(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
     using namespace gdrtc;
     if (!gdrtc_supports(d, RM_BF16)) return RM_ERR_UNSUPPORTED;
     const dim3 grid(d.nseg, d.B * d.H);
-    CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mk, p.k, d, kD) || !make_map(&mv, p.v, d, kD)) return RM_ERR_CUDA;
+    CUtensorMap mq, mk, mv, mo, mx, my;
+    if (!make_map(&mk, p.k, d, kD)) return RM_ERR_CUDA;
+    if (op != GdrOp::kBackwardPrepare && !make_map(&mv, p.v, d, kD)) return RM_ERR_CUDA;
+    if (op != GdrOp::kPrepare && !make_map(&mq, p.q, d, kD, d.qh)) return RM_ERR_CUDA;
     if (op == GdrOp::kPrepare) {
         auto fn = gdrtc_prepare_kernel;
         if (!set_smem(fn, kPrepSmem)) return RM_ERR_CUDA;
         fn<<<grid, 256, kPrepSmem, s>>>(d, mk, mv, p.g, p.beta, p.M, p.dS);
     } else if (op == GdrOp::kApply) {
-        if (!make_map(&mq, p.q, d, kD, d.qh) || !make_map(&mo, p.o, d, kD)) return RM_ERR_CUDA;
+        if (!make_map(&mo, p.o, d, kD)) return RM_ERR_CUDA;
         auto fn = gdrtc_apply_kernel;
         if (!set_smem(fn, kApplySmem)) return RM_ERR_CUDA;
         fn<<<grid, 256, kApplySmem, s>>>(d, mq, mk, mv, mo, p.g, p.beta, p.S_in);
+    } else if (op == GdrOp::kBackwardPrepare) {
+        // z = 0: the dq walk (which also needs v); z = 1: the gamma walk
+        if (!make_map(&mv, p.v, d, kD) || !make_map(&mo, p.dO, d, kD) || !make_map(&mx, p.dq, d, kD))
+            return RM_ERR_CUDA;
+        auto fn = gdrtc_bwd_prepare_kernel;
+        if (!set_smem(fn, kBwdPrepSmem)) return RM_ERR_CUDA;
+        fn<<<dim3(d.nseg, d.B * d.H, 2), 256, kBwdPrepSmem, s>>>(d, mq, mk, mv, mo, mx, p.g, p.beta, p.S_in,
+                                                                p.gamma_out, p.ws);
+    } else if (op == GdrOp::kBackwardApply) {
+        if (!make_map(&mo, p.dO, d, kD) || !make_map(&mx, p.dk, d, kD) || !make_map(&my, p.dv, d, kD))
+            return RM_ERR_CUDA;
+        auto fn = gdrtc_bwd_apply_kernel;
+        if (!set_smem(fn, kBwdApplySmem)) return RM_ERR_CUDA;
+        fn<<<grid, 256, kBwdApplySmem, s>>>(d, mq, mk, mv, mo, mx, my, p.g, p.beta, p.dS_out, p.ws, p.dg,
+                                            p.dbeta);
     } else {
         return RM_ERR_INVALID_ARG;
     }
     if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
     note_launch(1);
+    return RM_OK;
+}
+
+rm_status gdrtc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cudaStream_t s) {
+    gdrtc::read_flag_kernel<<<1, 1, 0, s>>>(dev_scratch, clear);
+    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    note_launch(1);
+    if (cudaMemcpyAsync(host_flag, dev_scratch, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return RM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RM_ERR_CUDA;
     return RM_OK;
 }
 

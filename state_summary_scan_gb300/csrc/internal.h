@@ -63,9 +63,10 @@ struct GdrPtrs {
 bool gdr_supports(const Dims& d);
 size_t gdr_workspace_bytes(const Dims& d);
 rm_status launch_gdr(GdrOp op, const Dims& d, rm_dtype dt, const GdrPtrs& p, cudaStream_t s);
-// its forward prepare and apply on the tensor cores (gdrtc_kernels.cu)
+// its forward and backward sweeps on the tensor cores (gdrtc_kernels.cu)
 bool gdrtc_supports(const Dims& d, rm_dtype dt);
 rm_status launch_gdrtc(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s);
+rm_status gdrtc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cudaStream_t s);
 
 // vector (per key dimension) gates on the generic path (vg_kernels.cu)
 rm_status launch_vg(Op op, const Dims& d, rm_dtype dt, const Ptrs& p, cudaStream_t s);

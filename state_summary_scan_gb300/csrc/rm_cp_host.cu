@@ -161,14 +161,14 @@ uint64_t rm_cp_launch_count(void) { return rmcp::g_launches.load(std::memory_ord
 rm_status rm_cp_device_status(int32_t* dev_scratch, int32_t clear, rm_stream_t stream) {
     RM_NEED(dev_scratch);
     // each tensor-core translation unit keeps its own flag
-    int flag = 0, vflag = 0;
-    rm_status st = rmcp::tc_read_timeout_flag(&flag, clear, dev_scratch,
-                                              reinterpret_cast<cudaStream_t>(stream));
-    if (st == RM_OK)
-        st = rmcp::vgtc_read_timeout_flag(&vflag, clear, dev_scratch, reinterpret_cast<cudaStream_t>(stream));
+    int flag = 0, vflag = 0, gflag = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    rm_status st = rmcp::tc_read_timeout_flag(&flag, clear, dev_scratch, s);
+    if (st == RM_OK) st = rmcp::vgtc_read_timeout_flag(&vflag, clear, dev_scratch, s);
+    if (st == RM_OK) st = rmcp::gdrtc_read_timeout_flag(&gflag, clear, dev_scratch, s);
     if (st != RM_OK)
         return fail(st, "device status read failed: %s", cudaGetErrorString(cudaGetLastError()));
-    if (flag || vflag) return fail(RM_ERR_TIMEOUT, "a bounded device-side wait ran out");
+    if (flag || vflag || gflag) return fail(RM_ERR_TIMEOUT, "a bounded device-side wait ran out");
     return RM_OK;
 }
 

@@ -262,3 +262,27 @@ def test_vector_gates_validation_and_sizes():
     lib = C.load()
     assert lib.rm_ssd_finish_forward(ssd.ref, ok, ok, ok, None) == 1
     assert b"vector_gates" in lib.rm_cp_last_error()
+
+
+def test_gdr_path_and_workspace():
+    """The gated delta rule's sweeps take the tensor cores for bf16 with
+    Dk = Dv = 64 and segment lengths that are multiples of 64, the generic
+    kernels for the other supported shapes; unsupported problems are -1.  The
+    workspace (one fp32 state every 16 tokens) also holds the tensor-core
+    sweeps' state every 64 tokens."""
+    from state_summary_scan_gb300.workloads import GDR_WORKLOADS
+    w = GDR_WORKLOADS["gdr8k"]
+    base = dict(B=w.B, T=w.T, H=w.H, Dk=w.Dk, Dv=w.Dv, num_segments=w.num_segments,
+                chunk=w.chunk, scale=w.scale, dtype=1)
+    tc = C.ProblemSpec(**base)
+    assert C.rm_gdr_path(tc) == 1
+    assert C.rm_gdr_path(C.ProblemSpec(**dict(base, dtype=0))) == 0                   # fp32 storage
+    assert C.rm_gdr_path(C.ProblemSpec(**dict(base, Dk=32))) == 0                     # Dk != 64
+    assert C.rm_gdr_path(C.ProblemSpec(**dict(base, Dv=48))) == 0                     # Dv != 64
+    assert C.rm_gdr_path(C.ProblemSpec(**dict(base, T=w.T - 32 * 16, chunk=16))) == 0  # L % 64 != 0
+    assert C.rm_gdr_path(C.ProblemSpec(**dict(base, Dk=128))) == -1
+    assert C.rm_gdr_path(C.ProblemSpec(**base, vector_gates=1)) == -1
+    ntok = w.B * w.T * w.H
+    ws = C.rm_gdr_workspace_size(tc)
+    assert ws >= (ntok // 16) * w.Dk * w.Dv * 4 >= (ntok // 64) * w.Dk * w.Dv * 4
+    assert C.rm_gdr_workspace_size(C.ProblemSpec(**dict(base, Dk=128))) == 0
