@@ -40,7 +40,9 @@ namespace {
 
 constexpr int kD = 64;                 // Dk = Dv
 constexpr uint32_t T8 = kTileBytes;    // one [64][64] bf16 tile
-constexpr int kP = kD + 1;             // pitch of the fp32 [64][64] work arrays
+constexpr int kP = kD + 1;             // pitch of the fp32 [64][64] A (and scratch) arrays
+constexpr int kQ = kD + 4;             // pitch of the fp32 inverse and its partial sums (16-byte rows)
+constexpr size_t kF32Bytes = (kD * kP + 2 * kD * kQ) * sizeof(float);  // A, X, Y
 
 // Row t of a [64][64] bf16 tile times w[t] (times mul), from src into dst:
 // 512 chunks of 16 bytes, two a thread (a row's scale does not depend on the
@@ -61,85 +63,148 @@ __device__ __forceinline__ void rows_scaled(const uint8_t* src, uint8_t* dst, co
     }
 }
 
-// Xs = (I + La)^{-1} for the strictly lower La (fp32, pitch kP): a unit lower
-// triangular inverse by 16 x 16 blocks.  The four diagonal blocks by forward
-// substitution (a column per thread), then the blocks below the diagonal by
-// their distance from it, X_ij = -X_ii sum_{k=j}^{i-1} A_ik X_kj (Ys holds the
-// sums).  Entries above the diagonal are 0.  Every thread of the CTA calls it.
+// Xs = (I + La)^{-1} for the strictly lower La (fp32, pitch kP; Xs and the
+// scratch Ys pitch kQ): a unit lower triangular inverse by 16 x 16 blocks.
+// The four diagonal blocks by forward substitution with the 16 rows of a
+// column in 16 lanes (x_k reaches the rows below it by a shuffle; four columns
+// a thread, every thread of the CTA busy), then the blocks below the diagonal
+// by their distance from it, X_ij = -X_ii sum_{k=j}^{i-1} A_ik X_kj (Ys holds
+// the sums), four adjacent columns a thread so that each loaded A or X entry
+// serves four products.  Entries above the diagonal are 0.  All 256 threads of
+// the CTA call it.
 __device__ __noinline__ void tri_inverse(const float* La, float* Xs, float* Ys) {
     const int tid = threadIdx.x;
-    for (int e = tid; e < kD * kD; e += blockDim.x) {
-        const int r = e >> 6, c = e & 63;
-        if ((c >> 4) > (r >> 4)) Xs[r * kP + c] = 0.f;
+    for (int e = tid; e < kD * kD / 4; e += blockDim.x) {  // the six blocks above the diagonal
+        const int r = e >> 4, c = (e & 15) * 4;
+        if ((c >> 4) > (r >> 4)) *reinterpret_cast<float4*>(Xs + r * kQ + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (tid < kD) {
-        const int o = 16 * (tid >> 4), c = tid & 15;
-        float x[16];
+    {
+        // warp w: diagonal block w / 2; lane: row r, column group (w % 2, lane / 16)
+        const int w = tid >> 5, lane = tid & 31;
+        const int o = 16 * (w >> 1), r = lane & 15, grp = ((w & 1) << 1) | (lane >> 4);
+        float x[4];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = 0.f;
+        for (int m = 0; m < 4; ++m) x[m] = r == 4 * grp + m ? 1.f : 0.f;
+        const float* lrow = La + (o + r) * kP + o;
 #pragma unroll
-            for (int kk = 0; kk < r; ++kk) acc = fmaf(La[(o + r) * kP + o + kk], x[kk], acc);
-            x[r] = r == c ? 1.f : (r > c ? -acc : 0.f);
+        for (int k = 0; k < 15; ++k) {
+            const float l = lrow[k];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float xk = __shfl_sync(kFull, x[m], (lane & 16) | k);
+                if (r > k) x[m] = fmaf(-l, xk, x[m]);
+            }
         }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Xs[(o + r) * kP + o + c] = x[r];
+        *reinterpret_cast<float4*>(Xs + (o + r) * kQ + o + 4 * grp) = make_float4(x[0], x[1], x[2], x[3]);
     }
     __syncthreads();
     for (int dist = 1; dist < 4; ++dist) {
-        const int nb = 4 - dist;  // blocks (j + dist, j), j < nb
-        for (int e = tid; e < nb * 256; e += blockDim.x) {
-            const int j = e >> 8, i = j + dist, r = (e >> 4) & 15, c = e & 15;
-            float acc = 0.f;
-            for (int kb = j; kb < i; ++kb) {
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk)
-                    acc = fmaf(La[(16 * i + r) * kP + 16 * kb + kk], Xs[(16 * kb + kk) * kP + 16 * j + c], acc);
+        // thread: block (j + dist, j), row r, columns 4 q .. 4 q + 3 of the block
+        const bool act = tid < 64 * (4 - dist);
+        const int j = tid >> 6, r = (tid >> 2) & 15, q = tid & 3, i = j + dist;
+        if (act) {
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            const float* arow = La + (16 * i + r) * kP;
+            const float* xc = Xs + 16 * j + 4 * q;
+#pragma unroll 16
+            for (int kk = 16 * j; kk < 16 * i; ++kk) {
+                const float a = arow[kk];
+                const float4 xv = *reinterpret_cast<const float4*>(xc + kk * kQ);
+                a0 = fmaf(a, xv.x, a0);
+                a1 = fmaf(a, xv.y, a1);
+                a2 = fmaf(a, xv.z, a2);
+                a3 = fmaf(a, xv.w, a3);
             }
-            Ys[(16 * i + r) * kP + 16 * j + c] = acc;
+            *reinterpret_cast<float4*>(Ys + (16 * i + r) * kQ + 16 * j + 4 * q) = make_float4(a0, a1, a2, a3);
         }
         __syncthreads();
-        for (int e = tid; e < nb * 256; e += blockDim.x) {
-            const int j = e >> 8, i = j + dist, r = (e >> 4) & 15, c = e & 15;
-            float acc = 0.f;
+        if (act) {
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            const float* xrow = Xs + (16 * i + r) * kQ + 16 * i;
+            const float* yc = Ys + 16 * i * kQ + 16 * j + 4 * q;
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk)
-                acc = fmaf(Xs[(16 * i + r) * kP + 16 * i + kk], Ys[(16 * i + kk) * kP + 16 * j + c], acc);
-            Xs[(16 * i + r) * kP + 16 * j + c] = -acc;
+            for (int kk = 0; kk < 16; ++kk) {
+                const float a = xrow[kk];
+                const float4 yv = *reinterpret_cast<const float4*>(yc + kk * kQ);
+                a0 = fmaf(a, yv.x, a0);
+                a1 = fmaf(a, yv.y, a1);
+                a2 = fmaf(a, yv.z, a2);
+                a3 = fmaf(a, yv.w, a3);
+            }
+            *reinterpret_cast<float4*>(Xs + (16 * i + r) * kQ + 16 * j + 4 * q) = make_float4(-a0, -a1, -a2, -a3);
         }
         __syncthreads();
     }
 }
 
-// The chunk's gate tables (warp 0) and write strengths (threads 0..63).
-__device__ __forceinline__ void chunk_gates(const Dims& d, const float* __restrict__ g,
-                                            const float* __restrict__ beta, int b, int h, int t0,
-                                            GateSmem& gs, float* beta_s, const Geo& G) {
-    if (G.warp == 0) {
-        const GateRegs gr = gate_load(d, g, b, h, t0, G.lane);
-        gate_prep(gr, &gs, G.lane);
+// Columns c0..c0+15 of row tau of the inverse (pitch kQ).
+__device__ __forceinline__ void xs_row16(const float* Xs, int tau, int c0, float* x) {
+    const float* row = Xs + tau * kQ + c0;
+#pragma unroll
+    for (int e = 0; e < 16; e += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(row + e);
+        x[e] = v.x; x[e + 1] = v.y; x[e + 2] = v.z; x[e + 3] = v.w;
     }
-    if (G.tid < kChunk) beta_s[G.tid] = __ldg(beta + g_off(d, b, t0 + G.tid, h));
+}
+
+// The next chunk's gates (warp 0) and write strengths (threads 0..63), loaded
+// into registers while the current chunk runs, then published to shared
+// memory at the top of the chunk that uses them.
+struct GateFetch {
+    GateRegs gr;
+    float be;
+};
+__device__ __forceinline__ GateFetch gates_fetch(const Dims& d, const float* __restrict__ g,
+                                                 const float* __restrict__ beta, int b, int h, int t0,
+                                                 const Geo& G) {
+    GateFetch f{};
+    if (G.warp == 0) f.gr = gate_load(d, g, b, h, t0, G.lane);
+    if (G.tid < kChunk) f.be = __ldg(beta + g_off(d, b, t0 + G.tid, h));
+    return f;
+}
+__device__ __forceinline__ void gates_commit(const GateFetch& f, GateSmem& gs, float* beta_s, const Geo& G) {
+    if (G.warp == 0) gate_prep(f.gr, &gs, G.lane);
+    if (G.tid < kChunk) beta_s[G.tid] = f.be;
+}
+
+// Row tau, columns c0..c0+15 of the within-sequence decay Gam[tau][r] =
+// exp(b_tau - b_r) for r < tau (strict) or r <= tau, 0 elsewhere.  Branch
+// free: the gate table is read by 16-byte loads and every exponential is
+// taken (those outside the mask may overflow; the select drops them).
+__device__ __forceinline__ void decay16(const GateSmem& gs, int tau, int c0, bool strict, float* m) {
+    const int lt = gs.lid[tau];
+    const float bt = gs.b[tau];
+#pragma unroll
+    for (int e = 0; e < 16; e += 4) {
+        const float4 bv = *reinterpret_cast<const float4*>(gs.b + c0 + e);
+        const int4 lv = *reinterpret_cast<const int4*>(gs.lid + c0 + e);
+        const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
+        const int ll[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = c0 + e + u;
+            const float x = __expf(bt - bb[u]);
+            m[e + u] = ((strict ? r < tau : r <= tau) && ll[u] == lt) ? x : 0.f;
+        }
+    }
 }
 
 // A (strictly lower, fp32) from this thread's 16 columns r = c0..c0+15 of
-// row tau of K K^T: A[tau][r] = beta_tau (k_tau.k_r) Gam[tau][r], r < tau.
-__device__ __forceinline__ void a_row16(const GateSmem& gs, const float* beta_s, const float* kk, int tau,
-                                        int c0, float* La) {
-    const int lt = gs.lid[tau];
-    const float bt = gs.b[tau], be = beta_s[tau];
+// row tau of K K^T and of the inclusive decay m: A[tau][r] = beta_tau
+// (k_tau.k_r) Gam[tau][r], r < tau.
+__device__ __forceinline__ void a_row16(const float* beta_s, const float* kk, const float* m, int tau, int c0,
+                                        float* La) {
+    const float be = beta_s[tau];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        const int r = c0 + e;
-        La[tau * kP + r] = (r < tau && gs.lid[r] == lt) ? be * kk[e] * __expf(bt - gs.b[r]) : 0.f;
-    }
+    for (int e = 0; e < 16; ++e) La[tau * kP + c0 + e] = c0 + e < tau ? be * kk[e] * m[e] : 0.f;
 }
 
 // T[tau][r] = Xs[tau][r] beta_r for this thread's 16 columns, as bf16.
 __device__ __forceinline__ void t_row16(const float* Xs, const float* beta_s, int tau, int c0, uint8_t* Tt) {
     float x[16];
+    xs_row16(Xs, tau, c0, x);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) x[e] = Xs[tau * kP + c0 + e] * beta_s[c0 + e];
+    for (int e = 0; e < 16; ++e) x[e] *= beta_s[c0 + e];
     store_row16(Tt, tau, c0, x);
 }
 
@@ -189,7 +254,7 @@ constexpr uint32_t AP_STAGE = 3 * T8;
 constexpr uint32_t AP_QG = 2 * AP_STAGE, AP_KG = AP_QG + T8, AP_KC = AP_KG + T8, AP_P = AP_KC + T8;
 constexpr uint32_t AP_T = AP_P + T8, AP_WN = AP_T + T8, AP_DL = AP_WN + T8, AP_S = AP_DL + T8, AP_O = AP_S + T8;
 constexpr uint32_t AP_F32 = AP_O + T8;
-constexpr size_t kApplySmem = AP_F32 + 3 * kD * kP * sizeof(float) + 1024;
+constexpr size_t kApplySmem = AP_F32 + kF32Bytes + 1024;
 
 __global__ void __launch_bounds__(256, 1)
     gdrtc_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
@@ -200,7 +265,7 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t* smem = align1024(smem_raw);
     float* La = reinterpret_cast<float*>(smem + AP_F32);
     float* Xs = La + kD * kP;
-    float* Ys = Xs + kD * kP;
+    float* Ys = Xs + kD * kQ;
     __shared__ GateSmem gs;
     __shared__ __align__(16) float beta_s[kChunk];
     __shared__ __align__(8) uint64_t full[2], mbar;
@@ -250,13 +315,15 @@ __global__ void __launch_bounds__(256, 1)
     }
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
+    GateFetch gf = gates_fetch(d, g, beta, b, h, a0, G);
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const int t0 = a0 + c * kChunk;
         uint8_t* Qs = smem + s * AP_STAGE;
         uint8_t* Ks = Qs + T8;
-        chunk_gates(d, g, beta, b, h, t0, gs, beta_s, G);
+        gates_commit(gf, gs, beta_s, G);
+        if (c + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + kChunk, G);
         if (G.tid == 0) {
             if (c >= 1 && c + 1 < nch) load(c + 1, s ^ 1);  // the previous chunk's products are done
             if (c >= 1) bulk_wait_read();                    // the o store has read its staging tile
@@ -274,17 +341,12 @@ __global__ void __launch_bounds__(256, 1)
         rows_scaled(Ks, smem + AP_KC, gs.wout, 1.f, G.tid);     // K o Gam[63]
         commit_wait(&mbar, mph, G.tid);
         {
-            float kk[16], qk[16];
-            tok16(tmem, G, TKK + 32 * G.grp, kk);
-            tok16(tmem, G, TQK + 32 * G.grp, qk);
-            a_row16(gs, beta_s, kk, G.tau, c0, La);
-            const int lt = gs.lid[G.tau];
-            const float bt = gs.b[G.tau];
+            float kk[16], qk[16], m[16];
+            tok16x2(tmem, G, TKK + 32 * G.grp, TQK + 32 * G.grp, kk, qk);
+            decay16(gs, G.tau, c0, false, m);
+            a_row16(beta_s, kk, m, G.tau, c0, La);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {  // P = scale (Q K^T o Gam), r <= tau
-                const int r = c0 + e;
-                qk[e] = (r <= G.tau && gs.lid[r] == lt) ? d.scale * qk[e] * __expf(bt - gs.b[r]) : 0.f;
-            }
+            for (int e = 0; e < 16; ++e) qk[e] *= d.scale * m[e];  // P = scale (Q K^T o Gam), r <= tau
             store_row16(smem + AP_P, G.tau, c0, qk);
         }
         __syncthreads();
@@ -355,7 +417,7 @@ constexpr uint32_t PR_STAGE = 2 * T8;
 constexpr uint32_t PR_KG = 2 * PR_STAGE, PR_KC = PR_KG + T8, PR_T = PR_KC + T8, PR_WN = PR_T + T8;
 constexpr uint32_t PR_DS = PR_WN + T8, PR_DM = PR_DS + T8, PR_S = PR_DM + T8, PR_M = PR_S + T8;
 constexpr uint32_t PR_F32 = PR_M + T8;
-constexpr size_t kPrepSmem = PR_F32 + 3 * kD * kP * sizeof(float) + 1024;
+constexpr size_t kPrepSmem = PR_F32 + kF32Bytes + 1024;
 
 __global__ void __launch_bounds__(256, 1)
     gdrtc_prepare_kernel(const Dims d, const __grid_constant__ CUtensorMap mk,
@@ -365,7 +427,7 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t* smem = align1024(smem_raw);
     float* La = reinterpret_cast<float*>(smem + PR_F32);
     float* Xs = La + kD * kP;
-    float* Ys = Xs + kD * kP;
+    float* Ys = Xs + kD * kQ;
     __shared__ GateSmem gs;
     __shared__ __align__(16) float beta_s[kChunk];
     __shared__ __align__(8) uint64_t full[2], mbar;
@@ -411,12 +473,14 @@ __global__ void __launch_bounds__(256, 1)
     }
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
+    GateFetch gf = gates_fetch(d, g, beta, b, h, a0, G);
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const int t0 = a0 + c * kChunk;
         uint8_t* Ks = smem + s * PR_STAGE;
-        chunk_gates(d, g, beta, b, h, t0, gs, beta_s, G);
+        gates_commit(gf, gs, beta_s, G);
+        if (c + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + kChunk, G);
         if (G.tid == 0 && c >= 1 && c + 1 < nch) load(c + 1, s ^ 1);  // the previous chunk's products are done
         __syncthreads();
         mbar_wait(smem_u32(&full[s]), (c >> 1) & 1);
@@ -429,9 +493,10 @@ __global__ void __launch_bounds__(256, 1)
         rows_scaled(Ks, smem + PR_KC, gs.wout, 1.f, G.tid);  // K o Gam[63]
         commit_wait(&mbar, mph, G.tid);
         {
-            float kk[16];
+            float kk[16], m[16];
             tok16(tmem, G, TKK + 32 * G.grp, kk);
-            a_row16(gs, beta_s, kk, G.tau, c0, La);
+            decay16(gs, G.tau, c0, false, m);
+            a_row16(beta_s, kk, m, G.tau, c0, La);
         }
         __syncthreads();
         tri_inverse(La, Xs, Ys);
@@ -500,18 +565,6 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 
-// Row tau, columns c0..c0+15 of the within-sequence decay Gam[tau][r] =
-// exp(b_tau - b_r) for r < tau (strict) or r <= tau, 0 elsewhere.
-__device__ __forceinline__ void decay16(const GateSmem& gs, int tau, int c0, bool strict, float* m) {
-    const int lt = gs.lid[tau];
-    const float bt = gs.b[tau];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        const int r = c0 + e;
-        m[e] = ((strict ? r < tau : r <= tau) && gs.lid[r] == lt) ? __expf(bt - gs.b[r]) : 0.f;
-    }
-}
-
 // The state row tau, columns c0..c0+15, of a [64][64] fp32 block at src.
 __device__ __forceinline__ void load_row16(const float* src, int tau, int c0, float* x) {
     const float* p = src + tau * kD + c0;
@@ -565,7 +618,7 @@ constexpr uint32_t DQ_STAGE = 3 * T8;
 constexpr uint32_t DQ_KG = 2 * DQ_STAGE, DQ_KC = DQ_KG + T8, DQ_OG = DQ_KC + T8, DQ_T = DQ_OG + T8;
 constexpr uint32_t DQ_WN = DQ_T + T8, DQ_DL = DQ_WN + T8, DQ_S = DQ_DL + T8, DQ_P = DQ_S + T8;
 constexpr uint32_t DQ_O = DQ_P + T8, DQ_F32 = DQ_O + T8;
-constexpr size_t kDqSmem = DQ_F32 + 3 * kD * kP * sizeof(float) + 1024;
+constexpr size_t kDqSmem = DQ_F32 + kF32Bytes + 1024;
 
 __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, const CUtensorMap* mv,
                                         const CUtensorMap* mo, const CUtensorMap* mdq,
@@ -574,7 +627,7 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
                                         uint8_t* smem, BwdShared& sh, uint32_t tmem, const Geo& G) {
     float* La = reinterpret_cast<float*>(smem + DQ_F32);
     float* Xs = La + kD * kP;
-    float* Ys = Xs + kD * kP;
+    float* Ys = Xs + kD * kQ;
     constexpr uint32_t TKK = 0, TQ = 64, TW = 128, TD = 192;
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
     const int nch = d.L / kChunk;
@@ -600,6 +653,7 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
     }
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
+    GateFetch gf = gates_fetch(d, g, beta, b, h, a0, G);
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
@@ -607,7 +661,8 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
         uint8_t* Ks = smem + s * DQ_STAGE;
         uint8_t* Os = Ks + 2 * T8;
         save_row16(ck + int64_t(c) * kD * kD, G.tau, c0, Sr);
-        chunk_gates(d, g, beta, b, h, t0, sh.gs, sh.beta_s, G);
+        gates_commit(gf, sh.gs, sh.beta_s, G);
+        if (c + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + kChunk, G);
         if (G.tid == 0) {
             if (c >= 1 && c + 1 < nch) load(c + 1, s ^ 1);  // the previous chunk's products are done
             if (c >= 1) bulk_wait_read();                    // the dq store has read its staging tile
@@ -626,9 +681,10 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
         if (G.tid == 0) mma_kk(tmem + TQ, desc_plus(DK, DQ_OG), desc_plus(DK, DQ_S), 0);  // (scale dO o gam) S^T
         commit_wait(&sh.mbar, mph, G.tid);
         {
-            float kk[16];
+            float kk[16], m[16];
             tok16(tmem, G, TKK + 32 * G.grp, kk);
-            a_row16(sh.gs, sh.beta_s, kk, G.tau, c0, La);
+            decay16(sh.gs, G.tau, c0, false, m);
+            a_row16(sh.beta_s, kk, m, G.tau, c0, La);
         }
         __syncthreads();
         tri_inverse(La, Xs, Ys);
@@ -705,7 +761,7 @@ constexpr uint32_t GA_STAGE = 3 * T8;
 constexpr uint32_t GA_KG = 2 * GA_STAGE, GA_KC = GA_KG + T8, GA_QG = GA_KC + T8, GA_P = GA_QG + T8;
 constexpr uint32_t GA_T = GA_P + T8, GA_DD = GA_T + T8, GA_DX = GA_DD + T8, GA_E = GA_DX + T8;
 constexpr uint32_t GA_F32 = GA_E + T8;
-constexpr size_t kGaSmem = GA_F32 + 3 * kD * kP * sizeof(float) + 1024;
+constexpr size_t kGaSmem = GA_F32 + kF32Bytes + 1024;
 constexpr size_t kBwdPrepSmem = kDqSmem > kGaSmem ? kDqSmem : kGaSmem;
 
 __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq, const CUtensorMap* mk,
@@ -714,7 +770,7 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
                                            uint8_t* smem, BwdShared& sh, uint32_t tmem, const Geo& G) {
     float* La = reinterpret_cast<float*>(smem + GA_F32);
     float* Xs = La + kD * kP;
-    float* Ys = Xs + kD * kP;
+    float* Ys = Xs + kD * kQ;
     constexpr uint32_t TKK = 0, TQK = 64, TDD = 128, TE = 192;
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
     const int nch = d.L / kChunk;
@@ -740,13 +796,15 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
     }
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
+    GateFetch gf = gates_fetch(d, g, beta, b, h, a0 + (nch - 1) * kChunk, G);
     uint32_t mph = 0;
     for (int it = 0; it < nch; ++it) {
         const int c = nch - 1 - it, s = it & 1;
         const int t0 = a0 + c * kChunk;
         uint8_t* Qs = smem + s * GA_STAGE;
         uint8_t* Ks = Qs + T8;
-        chunk_gates(d, g, beta, b, h, t0, sh.gs, sh.beta_s, G);
+        gates_commit(gf, sh.gs, sh.beta_s, G);
+        if (it + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 - kChunk, G);
         if (G.tid == 0 && it >= 1 && it + 1 < nch) load(c - 1, s ^ 1);  // the previous chunk's products are done
         __syncthreads();
         mbar_wait(smem_u32(&sh.full[s]), (it >> 1) & 1);
@@ -767,10 +825,9 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
         commit_wait(&sh.mbar, mph, G.tid);
         {
             float kk[16], qk[16], m[16];
-            tok16(tmem, G, TKK + 32 * G.grp, kk);
-            a_row16(sh.gs, sh.beta_s, kk, G.tau, c0, La);
-            tok16(tmem, G, TQK + 32 * G.grp, qk);
+            tok16x2(tmem, G, TKK + 32 * G.grp, TQK + 32 * G.grp, kk, qk);
             decay16(sh.gs, G.tau, c0, false, m);
+            a_row16(sh.beta_s, kk, m, G.tau, c0, La);
 #pragma unroll
             for (int e = 0; e < 16; ++e) qk[e] *= d.scale * m[e];
             store_row16(smem + GA_P, G.tau, c0, qk);
@@ -864,7 +921,7 @@ constexpr uint32_t BA_KG = 2 * BA_STAGE, BA_KC = BA_KG + T8, BA_QG = BA_KC + T8,
 constexpr uint32_t BA_E = BA_S + T8, BA_P = BA_E + T8, BA_T = BA_P + T8, BA_LI = BA_T + T8;
 constexpr uint32_t BA_X = BA_LI + T8, BA_D = BA_X + T8, BA_SV = BA_D + T8, BA_SK = BA_SV + T8;
 constexpr uint32_t BA_F32 = BA_SK + T8;
-constexpr size_t kBwdApplySmem = BA_F32 + 3 * kD * kP * sizeof(float) + 1024;
+constexpr size_t kBwdApplySmem = BA_F32 + kF32Bytes + 1024;
 
 __global__ void __launch_bounds__(256, 1)
     gdrtc_bwd_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
@@ -877,7 +934,7 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t* smem = align1024(smem_raw);
     float* La = reinterpret_cast<float*>(smem + BA_F32);
     float* Xs = La + kD * kP;
-    float* Ys = Xs + kD * kP;
+    float* Ys = Xs + kD * kQ;
     __shared__ BwdShared sh;
     constexpr uint32_t TKK = 0, TQK = 64, TX = 128, TDD = 192, TE = 256, TOS = 320, TDE = 384;
     constexpr uint32_t TZ = TKK, TK = TQK, TD = TX, TDA = TX, TOD = TDD, TXS = TDD;
@@ -913,6 +970,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
+    GateFetch gf = gates_fetch(d, g, beta, b, h, a0 + (nch - 1) * kChunk, G);
     uint32_t mph = 0;
     for (int it = 0; it < nch; ++it) {
         const int c = nch - 1 - it, s = it & 1;
@@ -924,7 +982,8 @@ __global__ void __launch_bounds__(256, 1)
         float Sr[16];
         load_row16(ck + int64_t(c) * kD * kD, G.tau, c0, Sr);
         store_row16(smem + BA_S, G.tau, c0, Sr);
-        chunk_gates(d, g, beta, b, h, t0, sh.gs, sh.beta_s, G);
+        gates_commit(gf, sh.gs, sh.beta_s, G);
+        if (it + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 - kChunk, G);
         if (G.tid == 0) {
             if (it >= 1 && it + 1 < nch) load(c - 1, s ^ 1);  // the previous chunk's products are done
             if (it >= 1) bulk_wait_read();                     // the dv and dk stores have read their tiles
@@ -973,8 +1032,7 @@ __global__ void __launch_bounds__(256, 1)
         tri_inverse(La, Xs, Ys);
         {
             float x[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] = Xs[G.tau * kP + c0 + e];
+            xs_row16(Xs, G.tau, c0, x);
             store_row16(smem + BA_LI, G.tau, c0, x);
             t_row16(Xs, sh.beta_s, G.tau, c0, smem + BA_T);
         }
