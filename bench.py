@@ -712,6 +712,19 @@ def gdr_kernel_bytes(w, phase):
     }[phase]
 
 
+def gdr_step_bytes(w, tc):
+    """Device bytes one gated-delta-rule step touches: q, k, v, dO, g, beta;
+    o, dq, dk, dv, dg, dbeta; M, delta_S, S_in, gamma, dS_out; the saved
+    states (one every 64 tokens on the tensor cores, every 16 otherwise)."""
+    e = 4 if w.dtype == "f32" else 2
+    ntok = w.B * w.T * w.H
+    nsum = w.num_segments * w.B * w.H
+    qk = ntok * w.Dk * e
+    vv = ntok * w.Dv * e
+    return (2 * (2 * qk + 2 * vv) + 4 * ntok * 4 + nsum * (w.Dk * w.Dk + 4 * w.Dk * w.Dv) * 4
+            + (ntok // (64 if tc else 16)) * w.Dk * w.Dv * 4)
+
+
 def gdr_kernel_tc_flops(w, phase):
     """Tensor-core flops of one launch of the tensor-core sweeps: 64 x 64 x 64
     products per 64-token chunk and head (7 in the forward prepare, 8 in the
@@ -847,7 +860,8 @@ def measure_gdr(w, args, rank, world, dev, peaks, peak_src, with_cpu):
                    "num_segments": w.num_segments, "storage": w.dtype, "mode": "fwd+bwd",
                    "recurrence": "gated delta rule",
                    "kernel_path": "tcgen05 sweeps, fp32 folds" if tc else "simt-fp32", "steps": steps,
-                   "l2": "inputs larger than L2, no flush"},
+                   "l2": f"a step touches {gdr_step_bytes(w, tc) / 1e6:.0f} MB (inputs, outputs, summaries, saved "
+                         f"states), more than the 129 MB L2; no flush"},
         "roofline": roof,
         "path_roofline": {"bound": pr["bound"], "t_roofline_us": pr["t_roofline_us"],
                           "t_measured_us": ms * 1e3, "frac": pr["t_roofline_us"] / (ms * 1e3),
