@@ -791,9 +791,10 @@ def measure_gdr(w, args, rank, world, dev, peaks, peak_src, with_cpu):
     dg, db = torch.empty_like(g), torch.empty_like(beta)
     stream = torch.cuda.current_stream(dev)
     fns = {
-        "gdr_forward_prepare": lambda: C.rm_gdr_forward_prepare(s, k, v, g, beta, plan.M, plan.dS, stream),
+        "gdr_forward_prepare": lambda: C.rm_gdr_forward_prepare(s, k, v, g, beta, plan.M, plan.dS, plan.ws,
+                                                                stream),
         "gdr_compose_prefix": lambda: C.rm_gdr_compose_prefix(s, plan.M, plan.dS, plan.S_in, stream),
-        "gdr_forward_apply": lambda: C.rm_gdr_forward_apply(s, q, k, v, g, beta, plan.S_in, o, stream),
+        "gdr_forward_apply": lambda: C.rm_gdr_forward_apply(s, q, k, v, g, beta, plan.S_in, o, plan.ws, stream),
         "gdr_backward_prepare": lambda: C.rm_gdr_backward_prepare(s, q, k, v, g, beta, plan.S_in, dO,
                                                                   plan.gamma, dq, plan.ws, stream),
         "gdr_compose_suffix": lambda: C.rm_gdr_compose_suffix(s, plan.M, plan.gamma, plan.dS_out, stream),

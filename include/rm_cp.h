@@ -450,6 +450,7 @@ rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, const void* 
  * sequence); the backward composes dS_in = M^T dS_out + gamma
  * (CPBackwardUnpackedSummary).  The six calls mirror the scalar-gate ones:
  *   rm_gdr_forward_prepare  M [nseg,B,H,Dk,Dk], dS [nseg,B,H,Dk,Dv] fp32 out
+ *                           (and the per-chunk factors in ws, tensor cores)
  *   rm_gdr_compose_prefix   S_in[j] = fold over [pre_j, j) of S <- M_i S + dS_i
  *   rm_gdr_forward_apply    o
  *   rm_gdr_backward_prepare gamma [nseg,B,H,Dk,Dv] (the local adjoint at the
@@ -467,10 +468,16 @@ rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, const void* 
  * tensor cores in the chunkwise WY/UT form (per 64-token chunk the products
  * of the I - beta k k^T factors as one triangular solve); everything else,
  * and the two folds, on generic fp32-arithmetic kernels.  ws:
- * rm_gdr_workspace_size bytes (B H (T / 16) Dk Dv fp32; the states the
- * backward prepare saves for the apply), passed unchanged from
- * rm_gdr_backward_prepare to rm_gdr_backward_apply.  Validation, ownership
- * and errors as for the other calls.
+ * rm_gdr_workspace_size bytes (B H (T / 16) Dk Dv fp32), one workspace for
+ * the whole step, passed unchanged to every call that takes it: the backward
+ * prepare saves states there for the backward apply (every 16 tokens, every
+ * 64 on the tensor cores), and on the tensor cores the forward prepare also
+ * leaves there each chunk's triangular factors T = (I + A)^-1 diag(beta) and
+ * (I + A)^-1 (bf16; they depend on k, g and beta only), which the forward
+ * apply and the two backward calls read, so the forward prepare must have run
+ * on the same k, g, beta and ws before them (the generic kernels do not use
+ * ws in the forward).  Validation, ownership and errors as for the other
+ * calls.
  *
  * rm_gdr_path: 1 when the problem's sweeps run on the tensor cores, 0 on the
  * generic kernels, -1 for a problem these calls reject.
@@ -478,12 +485,12 @@ rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, const void* 
 int32_t rm_gdr_path(const rm_cp_problem* p);
 size_t rm_gdr_workspace_size(const rm_cp_problem* p);
 rm_status rm_gdr_forward_prepare(const rm_cp_problem* p, const void* k, const void* v,
-                                 const float* g, const float* beta, float* M, float* dS,
+                                 const float* g, const float* beta, float* M, float* dS, void* ws,
                                  rm_stream_t stream);
 rm_status rm_gdr_compose_prefix(const rm_cp_problem* p, const float* M, const float* dS,
                                 float* S_in, rm_stream_t stream);
 rm_status rm_gdr_forward_apply(const rm_cp_problem* p, const void* q, const void* k, const void* v,
-                               const float* g, const float* beta, const float* S_in, void* o,
+                               const float* g, const float* beta, const float* S_in, void* o, void* ws,
                                rm_stream_t stream);
 rm_status rm_gdr_backward_prepare(const rm_cp_problem* p, const void* q, const void* k,
                                   const void* v, const float* g, const float* beta,

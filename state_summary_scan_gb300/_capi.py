@@ -103,9 +103,9 @@ _SIGS = {
     "rm_ssd_finish_backward": (_S, [_PP, ctypes.c_int32] + [_P] * 17),
     "rm_gdr_path": (ctypes.c_int32, [_PP]),
     "rm_gdr_workspace_size": (ctypes.c_size_t, [_PP]),
-    "rm_gdr_forward_prepare": (_S, [_PP] + [_P] * 7),
+    "rm_gdr_forward_prepare": (_S, [_PP] + [_P] * 8),
     "rm_gdr_compose_prefix": (_S, [_PP] + [_P] * 4),
-    "rm_gdr_forward_apply": (_S, [_PP] + [_P] * 8),
+    "rm_gdr_forward_apply": (_S, [_PP] + [_P] * 9),
     "rm_gdr_backward_prepare": (_S, [_PP] + [_P] * 11),
     "rm_gdr_compose_suffix": (_S, [_PP] + [_P] * 4),
     "rm_gdr_backward_apply": (_S, [_PP] + [_P] * 13),
@@ -337,18 +337,18 @@ def rm_gdr_workspace_size(p: ProblemSpec) -> int:
     return int(load().rm_gdr_workspace_size(p.ref))
 
 
-def rm_gdr_forward_prepare(p, k, v, g, beta, M, dS, stream=None):
+def rm_gdr_forward_prepare(p, k, v, g, beta, M, dS, ws, stream=None):
     _check(load().rm_gdr_forward_prepare(p.ref, _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(M),
-                                         _ptr(dS), _stream(stream)))
+                                         _ptr(dS), _ptr(ws), _stream(stream)))
 
 
 def rm_gdr_compose_prefix(p, M, dS, S_in, stream=None):
     _check(load().rm_gdr_compose_prefix(p.ref, _ptr(M), _ptr(dS), _ptr(S_in), _stream(stream)))
 
 
-def rm_gdr_forward_apply(p, q, k, v, g, beta, S_in, o, stream=None):
+def rm_gdr_forward_apply(p, q, k, v, g, beta, S_in, o, ws, stream=None):
     _check(load().rm_gdr_forward_apply(p.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                                       _ptr(S_in), _ptr(o), _stream(stream)))
+                                       _ptr(S_in), _ptr(o), _ptr(ws), _stream(stream)))
 
 
 def rm_gdr_backward_prepare(p, q, k, v, g, beta, S_in, dO, gamma, dq, ws, stream=None):

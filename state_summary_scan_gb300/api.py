@@ -350,9 +350,9 @@ def gdr_forward(plan: GdrPlan, q, k, v, g, beta, o=None, stream=None) -> torch.T
     """o of the gated delta rule: prepare -> compose_prefix -> apply."""
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
-    C.rm_gdr_forward_prepare(plan.spec, k, v, g, beta, plan.M, plan.dS, stream)
+    C.rm_gdr_forward_prepare(plan.spec, k, v, g, beta, plan.M, plan.dS, plan.ws, stream)
     C.rm_gdr_compose_prefix(plan.spec, plan.M, plan.dS, plan.S_in, stream)
-    C.rm_gdr_forward_apply(plan.spec, q, k, v, g, beta, plan.S_in, o, stream)
+    C.rm_gdr_forward_apply(plan.spec, q, k, v, g, beta, plan.S_in, o, plan.ws, stream)
     return o
 
 

@@ -59,7 +59,7 @@ size_t rm_gdr_workspace_size(const rm_cp_problem* p) {
 }
 
 rm_status rm_gdr_forward_prepare(const rm_cp_problem* p, const void* k, const void* v,
-                                 const float* g, const float* beta, float* M, float* dS,
+                                 const float* g, const float* beta, float* M, float* dS, void* ws,
                                  rm_stream_t stream) {
     rmcp::Dims d;
     rm_status s = check_gdr(p, &d);
@@ -70,6 +70,7 @@ rm_status rm_gdr_forward_prepare(const rm_cp_problem* p, const void* k, const vo
     RM_NEED_GDR(beta);
     RM_NEED_GDR(M);
     RM_NEED_GDR(dS);
+    RM_NEED_GDR(ws);
     rmcp::GdrPtrs x;
     x.k = k;
     x.v = v;
@@ -77,6 +78,7 @@ rm_status rm_gdr_forward_prepare(const rm_cp_problem* p, const void* k, const vo
     x.beta = beta;
     x.M = M;
     x.dS = dS;
+    x.ws = static_cast<float*>(ws);
     return run(rmcp::GdrOp::kPrepare, p, d, x, stream);
 }
 
@@ -96,7 +98,7 @@ rm_status rm_gdr_compose_prefix(const rm_cp_problem* p, const float* M, const fl
 }
 
 rm_status rm_gdr_forward_apply(const rm_cp_problem* p, const void* q, const void* k, const void* v,
-                               const float* g, const float* beta, const float* S_in, void* o,
+                               const float* g, const float* beta, const float* S_in, void* o, void* ws,
                                rm_stream_t stream) {
     rmcp::Dims d;
     rm_status s = check_gdr(p, &d);
@@ -108,6 +110,7 @@ rm_status rm_gdr_forward_apply(const rm_cp_problem* p, const void* q, const void
     RM_NEED_GDR(beta);
     RM_NEED_GDR(S_in);
     RM_NEED_GDR(o);
+    RM_NEED_GDR(ws);
     rmcp::GdrPtrs x;
     x.q = q;
     x.k = k;
@@ -116,6 +119,7 @@ rm_status rm_gdr_forward_apply(const rm_cp_problem* p, const void* q, const void
     x.beta = beta;
     x.S_in = S_in;
     x.o = o;
+    x.ws = static_cast<float*>(ws);
     return run(rmcp::GdrOp::kApply, p, d, x, stream);
 }
 

@@ -1,4 +1,4 @@
-// gdrtc_kernels.cu -- tensor-core forward (sm_103a, tcgen05 + TMA) of the
+// gdrtc_kernels.cu -- tensor-core sweeps (sm_103a, tcgen05 + TMA) of the
 // gated delta rule: bf16 storage, Dk = Dv = 64, segment lengths that are
 // multiples of 64.  Per row b and head h,
 //     S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
@@ -26,9 +26,15 @@
 // Kernels, one CTA of 256 threads per (segment, row, head); thread 0 issues
 // the TMA loads and stores and the products, and the CTA steps through each
 // chunk together (two input stages):
-//   gdrtc_prepare_kernel  the recurrence on [S | M] from [0 | I] with values
-//                         [V | 0]: delta_S and the transition M
-//   gdrtc_apply_kernel    o from S_in
+//   gdrtc_prepare_kernel      the recurrence on [S | M] from [0 | I] with
+//                             values [V | 0]: delta_S and the transition M; it
+//                             also leaves each chunk's T and (I + A)^{-1} in
+//                             the workspace
+//   gdrtc_apply_kernel        o from S_in (T from the workspace)
+//   gdrtc_bwd_prepare_kernel  dq by a forward walk that saves each chunk's
+//                             incoming state, and gamma by a reverse walk of
+//                             the state adjoint (two CTA roles, one launch)
+//   gdrtc_bwd_apply_kernel    dk, dv, dbeta and dg by a reverse walk
 #include "tc_tiles.cuh"
 
 namespace rmcp {
@@ -199,13 +205,20 @@ __device__ __forceinline__ void a_row16(const float* beta_s, const float* kk, co
     for (int e = 0; e < 16; ++e) La[tau * kP + c0 + e] = c0 + e < tau ? be * kk[e] * m[e] : 0.f;
 }
 
-// T[tau][r] = Xs[tau][r] beta_r for this thread's 16 columns, as bf16.
-__device__ __forceinline__ void t_row16(const float* Xs, const float* beta_s, int tau, int c0, uint8_t* Tt) {
-    float x[16];
-    xs_row16(Xs, tau, c0, x);
+// The state row tau, columns c0..c0+15, of a [64][64] fp32 block at src.
+__device__ __forceinline__ void load_row16(const float* src, int tau, int c0, float* x) {
+    const float* p = src + tau * kD + c0;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) x[e] *= beta_s[c0 + e];
-    store_row16(Tt, tau, c0, x);
+    for (int e = 0; e < 16; e += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(p + e);
+        x[e] = v.x; x[e + 1] = v.y; x[e + 2] = v.z; x[e + 3] = v.w;
+    }
+}
+__device__ __forceinline__ void save_row16(float* dst, int tau, int c0, const float* x) {
+    float* p = dst + tau * kD + c0;
+#pragma unroll
+    for (int e = 0; e < 16; e += 4)
+        *reinterpret_cast<float4*>(p + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
 }
 
 // One synchronous step: fence shared-memory writes for the tensor core and
@@ -244,28 +257,40 @@ __device__ __forceinline__ void mma_mm(uint32_t d, uint64_t a, uint64_t b, uint3
 }
 
 // ===========================================================================
-// forward apply: o from S_in.
-// Shared memory (8 KB tiles): two stages of Q|K|V; Q o gam (scaled), K o gam,
-// K o Gam[63], P, T, -W, D, S (bf16), o staging; fp32 A, X, Y work arrays.
-// Tensor memory: [0,64) K K^T, then the state product; [64,128) Q K^T, then
-// O; [128,192) W; [192,256) U, then D.
+// The per-chunk factors.  The forward prepare forms, for every chunk, T =
+// (I + A)^{-1} diag(beta) and (I + A)^{-1} (they depend on k, beta and the
+// gates only) and leaves them in the workspace after the saved states: a
+// bf16 table of [chunks][2][64][64] rows, chunk index ((seg B + b) H + h)
+// (L / 64) + c.  The apply and the backward load them by TMA instead of
+// forming them again.
 // ===========================================================================
-constexpr uint32_t AP_STAGE = 3 * T8;
+__device__ __forceinline__ int64_t chunk_base(const Dims& d, int seg, int b, int h) {
+    return ((int64_t(seg) * d.B + b) * d.H + h) * (d.L / kChunk);
+}
+// first row of factor f (0: T, 1: the inverse) of chunk ci in the factor table
+__device__ __forceinline__ int fac_row(int64_t ci, int f) { return int((2 * ci + f) * kD); }
+
+// ===========================================================================
+// forward apply: o from S_in.
+// Shared memory (8 KB tiles): two stages of Q|K|V|T; scale Q o gam, K o gam
+// (then -W), K o Gam[63], P, D, S (bf16), o staging.
+// Tensor memory: [0,64) the state product; [64,128) Q K^T, then O; [128,192)
+// W; [192,256) U, then D.
+// ===========================================================================
+constexpr uint32_t AP_STAGE = 4 * T8;
 constexpr uint32_t AP_QG = 2 * AP_STAGE, AP_KG = AP_QG + T8, AP_KC = AP_KG + T8, AP_P = AP_KC + T8;
-constexpr uint32_t AP_T = AP_P + T8, AP_WN = AP_T + T8, AP_DL = AP_WN + T8, AP_S = AP_DL + T8, AP_O = AP_S + T8;
-constexpr uint32_t AP_F32 = AP_O + T8;
-constexpr size_t kApplySmem = AP_F32 + kF32Bytes + 1024;
+constexpr uint32_t AP_DL = AP_P + T8, AP_S = AP_DL + T8, AP_O = AP_S + T8;
+constexpr uint32_t AP_WN = AP_KG;  // -W over K o gam, which dies with W
+constexpr size_t kApplySmem = AP_O + T8 + 1024;
 
 __global__ void __launch_bounds__(256, 1)
     gdrtc_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                        const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                       const __grid_constant__ CUtensorMap mo, const float* __restrict__ g,
-                       const float* __restrict__ beta, const float* __restrict__ S_in) {
+                       const __grid_constant__ CUtensorMap mf, const __grid_constant__ CUtensorMap mo,
+                       const float* __restrict__ g, const float* __restrict__ beta,
+                       const float* __restrict__ S_in) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    float* La = reinterpret_cast<float*>(smem + AP_F32);
-    float* Xs = La + kD * kP;
-    float* Ys = Xs + kD * kQ;
     __shared__ GateSmem gs;
     __shared__ __align__(16) float beta_s[kChunk];
     __shared__ __align__(8) uint64_t full[2], mbar;
@@ -277,6 +302,7 @@ __global__ void __launch_bounds__(256, 1)
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     const int c0 = 32 * G.grp + 16 * G.hi;  // this thread's 16 columns of a [64][64] product
+    const int64_t cb = chunk_base(d, seg, b, h);
 
     if (G.tid == 0) {
         mbar_init(smem_u32(&full[0]), 1);
@@ -287,15 +313,8 @@ __global__ void __launch_bounds__(256, 1)
     if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
     // the state row tau, columns c0..c0+15, in registers; its bf16 copy in the S tile
     float Sr[16];
-    {
-        const float* src = S_in + sum_off(d, seg, b, h) + G.tau * kD + c0;
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(src + e);
-            Sr[e] = x.x; Sr[e + 1] = x.y; Sr[e + 2] = x.z; Sr[e + 3] = x.w;
-        }
-        store_row16(smem + AP_S, G.tau, c0, Sr);
-    }
+    load_row16(S_in + sum_off(d, seg, b, h), G.tau, c0, Sr);
+    store_row16(smem + AP_S, G.tau, c0, Sr);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -308,6 +327,7 @@ __global__ void __launch_bounds__(256, 1)
         tma_load_3d(smem_u32(st), &mq, 0, h / d.qdiv, row, bar);
         tma_load_3d(smem_u32(st + T8), &mk, 0, h, row, bar);
         tma_load_3d(smem_u32(st + 2 * T8), &mv, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + 3 * T8), &mf, 0, 0, fac_row(cb + c, 0), bar);
     };
     if (G.tid == 0) {
         load(0, 0);
@@ -320,8 +340,7 @@ __global__ void __launch_bounds__(256, 1)
     for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const int t0 = a0 + c * kChunk;
-        uint8_t* Qs = smem + s * AP_STAGE;
-        uint8_t* Ks = Qs + T8;
+        const uint32_t sq = s * AP_STAGE, sk = sq + T8, sv = sq + 2 * T8, st = sq + 3 * T8;
         gates_commit(gf, gs, beta_s, G);
         if (c + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + kChunk, G);
         if (G.tid == 0) {
@@ -331,39 +350,26 @@ __global__ void __launch_bounds__(256, 1)
         __syncthreads();
         mbar_wait(smem_u32(&full[s]), (c >> 1) & 1);
         tc_fence_after();
-        if (G.tid == 0) {  // K K^T and Q K^T
-            const uint64_t q = desc_plus(DK, s * AP_STAGE), k = desc_plus(q, T8);
-            mma_kk(tmem + TKK, k, k, 0);
-            mma_kk(tmem + TQK, q, k, 0);
-        }
-        rows_scaled(Qs, smem + AP_QG, gs.win, d.scale, G.tid);  // scale Q o gam
-        rows_scaled(Ks, smem + AP_KG, gs.win, 1.f, G.tid);      // K o gam
-        rows_scaled(Ks, smem + AP_KC, gs.wout, 1.f, G.tid);     // K o Gam[63]
-        commit_wait(&mbar, mph, G.tid);
-        {
-            float kk[16], qk[16], m[16];
-            tok16x2(tmem, G, TKK + 32 * G.grp, TQK + 32 * G.grp, kk, qk);
-            decay16(gs, G.tau, c0, false, m);
-            a_row16(beta_s, kk, m, G.tau, c0, La);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) qk[e] *= d.scale * m[e];  // P = scale (Q K^T o Gam), r <= tau
-            store_row16(smem + AP_P, G.tau, c0, qk);
-        }
-        __syncthreads();
-        tri_inverse(La, Xs, Ys);
-        t_row16(Xs, beta_s, G.tau, c0, smem + AP_T);
+        if (G.tid == 0) mma_kk(tmem + TQK, desc_plus(DK, sq), desc_plus(DK, sk), 0);  // Q K^T
+        rows_scaled(smem + sq, smem + AP_QG, gs.win, d.scale, G.tid);  // scale Q o gam
+        rows_scaled(smem + sk, smem + AP_KG, gs.win, 1.f, G.tid);      // K o gam
+        rows_scaled(smem + sk, smem + AP_KC, gs.wout, 1.f, G.tid);     // K o Gam[63]
         cta_sync_tc();
         if (G.tid == 0) {  // W = T (K o gam), U = T V
-            const uint64_t t = desc_plus(DK, AP_T);
-            mma_km(tmem + TW, t, desc_plus(DM, AP_KG), 0);
-            mma_km(tmem + TD, t, desc_plus(DM, s * AP_STAGE + 2 * T8), 0);
+            mma_km(tmem + TW, desc_plus(DK, st), desc_plus(DM, AP_KG), 0);
+            mma_km(tmem + TD, desc_plus(DK, st), desc_plus(DM, sv), 0);
         }
         commit_wait(&mbar, mph, G.tid);
         {
-            float w[16];
-            tok16(tmem, G, TW + 32 * G.grp, w);
+            float qk[16], w[16], m[16];
+            tok16x2(tmem, G, TQK + 32 * G.grp, TW + 32 * G.grp, qk, w);
+            decay16(gs, G.tau, c0, false, m);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) w[e] = -w[e];
+            for (int e = 0; e < 16; ++e) {
+                qk[e] *= d.scale * m[e];  // P = scale (Q K^T o Gam), r <= tau
+                w[e] = -w[e];
+            }
+            store_row16(smem + AP_P, G.tau, c0, qk);
             store_row16(smem + AP_WN, G.tau, c0, w);
         }
         cta_sync_tc();
@@ -384,9 +390,8 @@ __global__ void __launch_bounds__(256, 1)
         commit_wait(&mbar, mph, G.tid);
         {
             float x[16], y[16];
-            tok16(tmem, G, TQK + 32 * G.grp, x);
+            tok16x2(tmem, G, TQK + 32 * G.grp, TKK + 32 * G.grp, x, y);
             store_row16(smem + AP_O, G.tau, c0, x);
-            tok16(tmem, G, TKK + 32 * G.grp, y);
 #pragma unroll
             for (int e = 0; e < 16; ++e) Sr[e] = fmaf(gs.W, Sr[e], y[e]);
             store_row16(smem + AP_S, G.tau, c0, Sr);
@@ -407,7 +412,8 @@ __global__ void __launch_bounds__(256, 1)
 // forward prepare: the recurrence on [S | M] from [0 | I] with values [V | 0]
 // over one segment: S_out = M S_in + delta_S with delta_S = S and M its last
 // state.  Per chunk: D_S = T V - W S, D_M = -W M, then S = gam_63 S +
-// (K o Gam[63])^T D_S and M likewise.
+// (K o Gam[63])^T D_S and M likewise; T and (I + A)^{-1} go to the factor
+// table for the apply and the backward.
 // Shared memory: two stages of K|V; K o gam, K o Gam[63], T, -W, D_S, D_M,
 // S, M (bf16); fp32 A, X, Y.
 // Tensor memory: [0,64) K K^T, then the S product; [64,128) W, then the M
@@ -422,7 +428,8 @@ constexpr size_t kPrepSmem = PR_F32 + kF32Bytes + 1024;
 __global__ void __launch_bounds__(256, 1)
     gdrtc_prepare_kernel(const Dims d, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const float* __restrict__ g,
-                         const float* __restrict__ beta, float* __restrict__ M, float* __restrict__ dS) {
+                         const float* __restrict__ beta, float* __restrict__ M, float* __restrict__ dS,
+                         __nv_bfloat16* __restrict__ fac) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     float* La = reinterpret_cast<float*>(smem + PR_F32);
@@ -439,6 +446,7 @@ __global__ void __launch_bounds__(256, 1)
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     const int c0 = 32 * G.grp + 16 * G.hi;
+    const int64_t cb = chunk_base(d, seg, b, h);
 
     if (G.tid == 0) {
         mbar_init(smem_u32(&full[0]), 1);
@@ -500,7 +508,17 @@ __global__ void __launch_bounds__(256, 1)
         }
         __syncthreads();
         tri_inverse(La, Xs, Ys);
-        t_row16(Xs, beta_s, G.tau, c0, smem + PR_T);
+        {
+            // T into its tile, and T and (I + A)^{-1} into the factor table
+            float x[16], t[16];
+            xs_row16(Xs, G.tau, c0, x);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) t[e] = x[e] * beta_s[c0 + e];
+            store_row16(smem + PR_T, G.tau, c0, t);
+            __nv_bfloat16* f = fac + (int64_t(fac_row(cb + c, 0)) + G.tau) * kD + c0;
+            store_bf16x16(f, t);
+            store_bf16x16(f + kD * kD, x);
+        }
         cta_sync_tc();
         if (G.tid == 0) {  // W = T (K o gam), U = T V
             const uint64_t t = desc_plus(DK, PR_T);
@@ -565,22 +583,6 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 
-// The state row tau, columns c0..c0+15, of a [64][64] fp32 block at src.
-__device__ __forceinline__ void load_row16(const float* src, int tau, int c0, float* x) {
-    const float* p = src + tau * kD + c0;
-#pragma unroll
-    for (int e = 0; e < 16; e += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(p + e);
-        x[e] = v.x; x[e + 1] = v.y; x[e + 2] = v.z; x[e + 3] = v.w;
-    }
-}
-__device__ __forceinline__ void save_row16(float* dst, int tau, int c0, const float* x) {
-    float* p = dst + tau * kD + c0;
-#pragma unroll
-    for (int e = 0; e < 16; e += 4)
-        *reinterpret_cast<float4*>(p + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-}
-
 // Per-block state of the backward kernels (static shared memory).
 struct BwdShared {
     GateSmem gs;
@@ -609,31 +611,29 @@ __device__ __forceinline__ void bwd_setup(BwdShared& sh, const Geo& G, int cols)
 //     dq = scale (gam o (dO S_prev^T) + mask(dO D^T o Gam) K),
 // (dq_t = scale S_t dO_t with S_t = gam_t S_prev + sum_{r<=t} Gam[t][r] k_r D_r^T)
 // and S_prev saved to the workspace before each chunk.
-// Shared memory: two stages of K|V|dO; K o gam, K o Gam[63], scale dO o gam,
-// T, -W, D, S, P, dq staging (bf16); fp32 A, X, Y.
-// Tensor memory: [0,64) K K^T, then dO D^T; [64,128) dq; [128,192) W, then
-// the state product; [192,256) U, then D.
+// Shared memory: two stages of K|V|dO|T; K o gam (then -W), K o Gam[63],
+// scale dO o gam, D, S, P, dq staging (bf16).
+// Tensor memory: [0,64) dO D^T; [64,128) dq; [128,192) W, then the state
+// product; [192,256) U, then D.
 // ===========================================================================
-constexpr uint32_t DQ_STAGE = 3 * T8;
-constexpr uint32_t DQ_KG = 2 * DQ_STAGE, DQ_KC = DQ_KG + T8, DQ_OG = DQ_KC + T8, DQ_T = DQ_OG + T8;
-constexpr uint32_t DQ_WN = DQ_T + T8, DQ_DL = DQ_WN + T8, DQ_S = DQ_DL + T8, DQ_P = DQ_S + T8;
-constexpr uint32_t DQ_O = DQ_P + T8, DQ_F32 = DQ_O + T8;
-constexpr size_t kDqSmem = DQ_F32 + kF32Bytes + 1024;
+constexpr uint32_t DQ_STAGE = 4 * T8;
+constexpr uint32_t DQ_KG = 2 * DQ_STAGE, DQ_KC = DQ_KG + T8, DQ_OG = DQ_KC + T8, DQ_DL = DQ_OG + T8;
+constexpr uint32_t DQ_S = DQ_DL + T8, DQ_P = DQ_S + T8, DQ_O = DQ_P + T8;
+constexpr uint32_t DQ_WN = DQ_KG;  // -W over K o gam, which dies with W
+constexpr size_t kDqSmem = DQ_O + T8 + 1024;
 
 __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, const CUtensorMap* mv,
-                                        const CUtensorMap* mo, const CUtensorMap* mdq,
+                                        const CUtensorMap* mo, const CUtensorMap* mf, const CUtensorMap* mdq,
                                         const float* __restrict__ g, const float* __restrict__ beta,
                                         const float* __restrict__ S_in, float* __restrict__ ws,
                                         uint8_t* smem, BwdShared& sh, uint32_t tmem, const Geo& G) {
-    float* La = reinterpret_cast<float*>(smem + DQ_F32);
-    float* Xs = La + kD * kP;
-    float* Ys = Xs + kD * kQ;
     constexpr uint32_t TKK = 0, TQ = 64, TW = 128, TD = 192;
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     const int c0 = 32 * G.grp + 16 * G.hi;
-    float* ck = ws + ((int64_t(seg) * d.B + b) * d.H + h) * nch * int64_t(kD * kD);
+    const int64_t cb = chunk_base(d, seg, b, h);
+    float* ck = ws + cb * int64_t(kD * kD);
 
     float Sr[16];
     load_row16(S_in + sum_off(d, seg, b, h), G.tau, c0, Sr);
@@ -646,6 +646,7 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
         tma_load_3d(smem_u32(st), mk, 0, h, row, bar);
         tma_load_3d(smem_u32(st + T8), mv, 0, h, row, bar);
         tma_load_3d(smem_u32(st + 2 * T8), mo, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + 3 * T8), mf, 0, 0, fac_row(cb + c, 0), bar);
     };
     if (G.tid == 0) {
         load(0, 0);
@@ -658,8 +659,7 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
     for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const int t0 = a0 + c * kChunk;
-        uint8_t* Ks = smem + s * DQ_STAGE;
-        uint8_t* Os = Ks + 2 * T8;
+        const uint32_t sk = s * DQ_STAGE, sv = sk + T8, so = sk + 2 * T8, st = sk + 3 * T8;
         save_row16(ck + int64_t(c) * kD * kD, G.tau, c0, Sr);
         gates_commit(gf, sh.gs, sh.beta_s, G);
         if (c + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + kChunk, G);
@@ -670,30 +670,14 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
         __syncthreads();
         mbar_wait(smem_u32(&sh.full[s]), (c >> 1) & 1);
         tc_fence_after();
+        rows_scaled(smem + sk, smem + DQ_KG, sh.gs.win, 1.f, G.tid);      // K o gam
+        rows_scaled(smem + sk, smem + DQ_KC, sh.gs.wout, 1.f, G.tid);     // K o Gam[63]
+        rows_scaled(smem + so, smem + DQ_OG, sh.gs.win, d.scale, G.tid);  // scale dO o gam
+        cta_sync_tc();
         if (G.tid == 0) {
-            const uint64_t k = desc_plus(DK, s * DQ_STAGE);
-            mma_kk(tmem + TKK, k, k, 0);  // K K^T
-        }
-        rows_scaled(Ks, smem + DQ_KG, sh.gs.win, 1.f, G.tid);      // K o gam
-        rows_scaled(Ks, smem + DQ_KC, sh.gs.wout, 1.f, G.tid);     // K o Gam[63]
-        rows_scaled(Os, smem + DQ_OG, sh.gs.win, d.scale, G.tid);  // scale dO o gam
-        cta_sync_tc();
-        if (G.tid == 0) mma_kk(tmem + TQ, desc_plus(DK, DQ_OG), desc_plus(DK, DQ_S), 0);  // (scale dO o gam) S^T
-        commit_wait(&sh.mbar, mph, G.tid);
-        {
-            float kk[16], m[16];
-            tok16(tmem, G, TKK + 32 * G.grp, kk);
-            decay16(sh.gs, G.tau, c0, false, m);
-            a_row16(sh.beta_s, kk, m, G.tau, c0, La);
-        }
-        __syncthreads();
-        tri_inverse(La, Xs, Ys);
-        t_row16(Xs, sh.beta_s, G.tau, c0, smem + DQ_T);
-        cta_sync_tc();
-        if (G.tid == 0) {  // W = T (K o gam), U = T V
-            const uint64_t t = desc_plus(DK, DQ_T);
-            mma_km(tmem + TW, t, desc_plus(DM, DQ_KG), 0);
-            mma_km(tmem + TD, t, desc_plus(DM, s * DQ_STAGE + T8), 0);
+            mma_kk(tmem + TQ, desc_plus(DK, DQ_OG), desc_plus(DK, DQ_S), 0);  // (scale dO o gam) S^T
+            mma_km(tmem + TW, desc_plus(DK, st), desc_plus(DM, DQ_KG), 0);    // W = T (K o gam)
+            mma_km(tmem + TD, desc_plus(DK, st), desc_plus(DM, sv), 0);       // U = T V
         }
         commit_wait(&sh.mbar, mph, G.tid);
         {
@@ -713,24 +697,23 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
         }
         cta_sync_tc();
         if (G.tid == 0) {
-            mma_kk(tmem + TKK, desc_plus(DK, s * DQ_STAGE + 2 * T8), desc_plus(DK, DQ_DL), 0);  // dO D^T
-            mma_mm(tmem + TW, desc_plus(DM, DQ_KC), desc_plus(DM, DQ_DL), 0);               // (K o Gam[63])^T D
+            mma_kk(tmem + TKK, desc_plus(DK, so), desc_plus(DK, DQ_DL), 0);     // dO D^T
+            mma_mm(tmem + TW, desc_plus(DM, DQ_KC), desc_plus(DM, DQ_DL), 0);  // (K o Gam[63])^T D
         }
         commit_wait(&sh.mbar, mph, G.tid);
         {
             float p[16], m[16], y[16];
-            tok16(tmem, G, TKK + 32 * G.grp, p);
+            tok16x2(tmem, G, TKK + 32 * G.grp, TW + 32 * G.grp, p, y);
             decay16(sh.gs, G.tau, c0, false, m);
 #pragma unroll
             for (int e = 0; e < 16; ++e) p[e] *= d.scale * m[e];
             store_row16(smem + DQ_P, G.tau, c0, p);
-            tok16(tmem, G, TW + 32 * G.grp, y);
 #pragma unroll
             for (int e = 0; e < 16; ++e) Sr[e] = fmaf(sh.gs.W, Sr[e], y[e]);
             store_row16(smem + DQ_S, G.tau, c0, Sr);
         }
         cta_sync_tc();
-        if (G.tid == 0) mma_km(tmem + TQ, desc_plus(DK, DQ_P), desc_plus(DM, s * DQ_STAGE), 1);  // + P K
+        if (G.tid == 0) mma_km(tmem + TQ, desc_plus(DK, DQ_P), desc_plus(DM, sk), 1);  // + P K
         commit_wait(&sh.mbar, mph, G.tid);
         {
             float x[16];
@@ -752,30 +735,28 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
 //     dD = P^T dO + (K o Gam[63]) E,   dX = T^T dD,
 //     E <- scale (Q o gam)^T dO + gam_63 E - (K o gam)^T dX,
 // gamma = E at the segment start.  No state is needed.
-// Shared memory: two stages of Q|K|dO; K o gam, K o Gam[63], scale Q o gam,
-// P, T, dD, -dX, E (bf16); fp32 A, X, Y.
-// Tensor memory: [0,64) K K^T, then dX; [64,128) Q K^T; [128,192) dD;
-// [192,256) the E product.
+// Shared memory: two stages of Q|K|dO|T; K o gam, K o Gam[63], scale Q o gam,
+// P, dD, -dX, E (bf16).
+// Tensor memory: [0,64) dX; [64,128) Q K^T; [128,192) dD; [192,256) the E
+// product.
 // ===========================================================================
-constexpr uint32_t GA_STAGE = 3 * T8;
+constexpr uint32_t GA_STAGE = 4 * T8;
 constexpr uint32_t GA_KG = 2 * GA_STAGE, GA_KC = GA_KG + T8, GA_QG = GA_KC + T8, GA_P = GA_QG + T8;
-constexpr uint32_t GA_T = GA_P + T8, GA_DD = GA_T + T8, GA_DX = GA_DD + T8, GA_E = GA_DX + T8;
-constexpr uint32_t GA_F32 = GA_E + T8;
-constexpr size_t kGaSmem = GA_F32 + kF32Bytes + 1024;
+constexpr uint32_t GA_DD = GA_P + T8, GA_DX = GA_DD + T8, GA_E = GA_DX + T8;
+constexpr size_t kGaSmem = GA_E + T8 + 1024;
 constexpr size_t kBwdPrepSmem = kDqSmem > kGaSmem ? kDqSmem : kGaSmem;
 
 __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq, const CUtensorMap* mk,
-                                           const CUtensorMap* mo, const float* __restrict__ g,
-                                           const float* __restrict__ beta, float* __restrict__ gamma,
-                                           uint8_t* smem, BwdShared& sh, uint32_t tmem, const Geo& G) {
-    float* La = reinterpret_cast<float*>(smem + GA_F32);
-    float* Xs = La + kD * kP;
-    float* Ys = Xs + kD * kQ;
-    constexpr uint32_t TKK = 0, TQK = 64, TDD = 128, TE = 192;
+                                           const CUtensorMap* mo, const CUtensorMap* mf,
+                                           const float* __restrict__ g, const float* __restrict__ beta,
+                                           float* __restrict__ gamma, uint8_t* smem, BwdShared& sh,
+                                           uint32_t tmem, const Geo& G) {
+    constexpr uint32_t TX = 0, TQK = 64, TDD = 128, TE = 192;
     const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     const int c0 = 32 * G.grp + 16 * G.hi;
+    const int64_t cb = chunk_base(d, seg, b, h);
 
     float Er[16];
 #pragma unroll
@@ -789,6 +770,7 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
         tma_load_3d(smem_u32(st), mq, 0, h / d.qdiv, row, bar);
         tma_load_3d(smem_u32(st + T8), mk, 0, h, row, bar);
         tma_load_3d(smem_u32(st + 2 * T8), mo, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + 3 * T8), mf, 0, 0, fac_row(cb + c, 0), bar);
     };
     if (G.tid == 0) {
         load(nch - 1, 0);
@@ -801,41 +783,33 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
     for (int it = 0; it < nch; ++it) {
         const int c = nch - 1 - it, s = it & 1;
         const int t0 = a0 + c * kChunk;
-        uint8_t* Qs = smem + s * GA_STAGE;
-        uint8_t* Ks = Qs + T8;
+        const uint32_t sq = s * GA_STAGE, sk = sq + T8, so = sq + 2 * T8, st = sq + 3 * T8;
         gates_commit(gf, sh.gs, sh.beta_s, G);
         if (it + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 - kChunk, G);
         if (G.tid == 0 && it >= 1 && it + 1 < nch) load(c - 1, s ^ 1);  // the previous chunk's products are done
         __syncthreads();
         mbar_wait(smem_u32(&sh.full[s]), (it >> 1) & 1);
         tc_fence_after();
-        if (G.tid == 0) {  // K K^T and Q K^T
-            const uint64_t q = desc_plus(DK, s * GA_STAGE), k = desc_plus(q, T8);
-            mma_kk(tmem + TKK, k, k, 0);
-            mma_kk(tmem + TQK, q, k, 0);
-        }
-        rows_scaled(Ks, smem + GA_KG, sh.gs.win, 1.f, G.tid);      // K o gam
-        rows_scaled(Ks, smem + GA_KC, sh.gs.wout, 1.f, G.tid);     // K o Gam[63]
-        rows_scaled(Qs, smem + GA_QG, sh.gs.win, d.scale, G.tid);  // scale Q o gam
+        if (G.tid == 0) mma_kk(tmem + TQK, desc_plus(DK, sq), desc_plus(DK, sk), 0);  // Q K^T
+        rows_scaled(smem + sk, smem + GA_KG, sh.gs.win, 1.f, G.tid);      // K o gam
+        rows_scaled(smem + sk, smem + GA_KC, sh.gs.wout, 1.f, G.tid);     // K o Gam[63]
+        rows_scaled(smem + sq, smem + GA_QG, sh.gs.win, d.scale, G.tid);  // scale Q o gam
         cta_sync_tc();
         if (G.tid == 0) {
-            mma_km(tmem + TDD, desc_plus(DK, GA_KC), desc_plus(DM, GA_E), 0);                // (K o Gam[63]) E
-            mma_mm(tmem + TE, desc_plus(DM, GA_QG), desc_plus(DM, s * GA_STAGE + 2 * T8), 0);  // (scale Q o gam)^T dO
+            mma_km(tmem + TDD, desc_plus(DK, GA_KC), desc_plus(DM, GA_E), 0);  // (K o Gam[63]) E
+            mma_mm(tmem + TE, desc_plus(DM, GA_QG), desc_plus(DM, so), 0);     // (scale Q o gam)^T dO
         }
         commit_wait(&sh.mbar, mph, G.tid);
         {
-            float kk[16], qk[16], m[16];
-            tok16x2(tmem, G, TKK + 32 * G.grp, TQK + 32 * G.grp, kk, qk);
+            float qk[16], m[16];
+            tok16(tmem, G, TQK + 32 * G.grp, qk);
             decay16(sh.gs, G.tau, c0, false, m);
-            a_row16(sh.beta_s, kk, m, G.tau, c0, La);
 #pragma unroll
             for (int e = 0; e < 16; ++e) qk[e] *= d.scale * m[e];
             store_row16(smem + GA_P, G.tau, c0, qk);
         }
         cta_sync_tc();
-        if (G.tid == 0) mma_mm(tmem + TDD, desc_plus(DM, GA_P), desc_plus(DM, s * GA_STAGE + 2 * T8), 1);  // + P^T dO
-        tri_inverse(La, Xs, Ys);
-        t_row16(Xs, sh.beta_s, G.tau, c0, smem + GA_T);
+        if (G.tid == 0) mma_mm(tmem + TDD, desc_plus(DM, GA_P), desc_plus(DM, so), 1);  // + P^T dO
         commit_wait(&sh.mbar, mph, G.tid);
         {
             float x[16];
@@ -843,11 +817,11 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
             store_row16(smem + GA_DD, G.tau, c0, x);
         }
         cta_sync_tc();
-        if (G.tid == 0) mma_mm(tmem + TKK, desc_plus(DM, GA_T), desc_plus(DM, GA_DD), 0);  // dX = T^T dD
+        if (G.tid == 0) mma_mm(tmem + TX, desc_plus(DM, st), desc_plus(DM, GA_DD), 0);  // dX = T^T dD
         commit_wait(&sh.mbar, mph, G.tid);
         {
             float x[16];
-            tok16(tmem, G, TKK + 32 * G.grp, x);
+            tok16(tmem, G, TX + 32 * G.grp, x);
 #pragma unroll
             for (int e = 0; e < 16; ++e) x[e] = -x[e];
             store_row16(smem + GA_DX, G.tau, c0, x);
@@ -870,7 +844,8 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
 __global__ void __launch_bounds__(256, 1)
     gdrtc_bwd_prepare_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                              const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                             const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mdq,
+                             const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mf,
+                             const __grid_constant__ CUtensorMap mdq,
                              const float* __restrict__ g, const float* __restrict__ beta,
                              const float* __restrict__ S_in, float* __restrict__ gamma, float* __restrict__ ws) {
     extern __shared__ uint8_t smem_raw[];
@@ -883,9 +858,9 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after();
     const uint32_t tmem = sh.tmem_slot;
     if (blockIdx.z == 0)
-        dq_walk(d, &mk, &mv, &mo, &mdq, g, beta, S_in, ws, smem, sh, tmem, G);
+        dq_walk(d, &mk, &mv, &mo, &mf, &mdq, g, beta, S_in, ws, smem, sh, tmem, G);
     else
-        gamma_walk(d, &mq, &mk, &mo, g, beta, gamma, smem, sh, tmem, G);
+        gamma_walk(d, &mq, &mk, &mo, &mf, g, beta, gamma, smem, sh, tmem, G);
     tc_fence_before();
     __syncthreads();
     if (G.warp == 0) tmem_dealloc(tmem, 256);
@@ -908,33 +883,33 @@ __global__ void __launch_bounds__(256, 1)
 //     + scale gam_t q_t . (S_prev dO_t) - gam_t k_t . (S_prev dX_t) - w_t,
 //     w_t = Gam[63][t] k_t . (E D_t), and at t = 63 + gam_63 <S_prev, E> + sum_r w_r;
 // dg_u = sum_{t >= u} db_t inside the chunk (0 where a sequence starts).
-// Shared memory (8 KB tiles): two stages of Q|K|V|dO; K o gam, K o Gam[63]
-// (then dZ), scale Q o gam (then scale mask(dO D^T o Gam)), S, E, P (then
-// -dX), T (then dG + dG^T), L^{-1}, X (then dD), D, dv and dk staging; fp32
-// A (then dG), X, Y (then M1 + M2) work arrays.
+// Shared memory (8 KB tiles): two stages of Q|K|V|dO|T|L^{-1}; K o gam,
+// K o Gam[63] (then dZ), scale Q o gam (then scale mask(dO D^T o Gam)), S, E,
+// P (then -dX), X (then dD, then dG + dG^T), D, dv and dk staging; fp32 dG
+// and M1 + M2 work arrays.
 // Tensor memory (64 columns each): K K^T then dZ; Q K^T then the dk
 // product; (K o gam) S_prev, D, then dZ D^T; dD, dO D^T, then -dX S_prev^T;
 // the E product; dO S_prev^T; D E^T.
 // ===========================================================================
-constexpr uint32_t BA_STAGE = 4 * T8;
+constexpr uint32_t BA_STAGE = 6 * T8;
 constexpr uint32_t BA_KG = 2 * BA_STAGE, BA_KC = BA_KG + T8, BA_QG = BA_KC + T8, BA_S = BA_QG + T8;
-constexpr uint32_t BA_E = BA_S + T8, BA_P = BA_E + T8, BA_T = BA_P + T8, BA_LI = BA_T + T8;
-constexpr uint32_t BA_X = BA_LI + T8, BA_D = BA_X + T8, BA_SV = BA_D + T8, BA_SK = BA_SV + T8;
-constexpr uint32_t BA_F32 = BA_SK + T8;
-constexpr size_t kBwdApplySmem = BA_F32 + kF32Bytes + 1024;
+constexpr uint32_t BA_E = BA_S + T8, BA_P = BA_E + T8, BA_X = BA_P + T8, BA_D = BA_X + T8;
+constexpr uint32_t BA_SV = BA_D + T8, BA_SK = BA_SV + T8, BA_F32 = BA_SK + T8;
+constexpr uint32_t BA_GS = BA_X;  // dG + dG^T over dD, which dies with dZ
+constexpr size_t kBwdApplySmem = BA_F32 + 2 * kD * kP * sizeof(float) + 1024;
 
 __global__ void __launch_bounds__(256, 1)
     gdrtc_bwd_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                            const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                           const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mdk,
-                           const __grid_constant__ CUtensorMap mdv, const float* __restrict__ g,
-                           const float* __restrict__ beta, const float* __restrict__ dS_out,
-                           const float* __restrict__ ws, float* __restrict__ dg, float* __restrict__ dbeta) {
+                           const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mf,
+                           const __grid_constant__ CUtensorMap mdk, const __grid_constant__ CUtensorMap mdv,
+                           const float* __restrict__ g, const float* __restrict__ beta,
+                           const float* __restrict__ dS_out, const float* __restrict__ ws,
+                           float* __restrict__ dg, float* __restrict__ dbeta) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    float* La = reinterpret_cast<float*>(smem + BA_F32);
-    float* Xs = La + kD * kP;
-    float* Ys = Xs + kD * kQ;
+    float* La = reinterpret_cast<float*>(smem + BA_F32);  // dG
+    float* Ys = La + kD * kP;                               // M1 + M2
     __shared__ BwdShared sh;
     constexpr uint32_t TKK = 0, TQK = 64, TX = 128, TDD = 192, TE = 256, TOS = 320, TDE = 384;
     constexpr uint32_t TZ = TKK, TK = TQK, TD = TX, TDA = TX, TOD = TDD, TXS = TDD;
@@ -944,7 +919,8 @@ __global__ void __launch_bounds__(256, 1)
     const int nch = d.L / kChunk;
     const int a0 = seg * d.L;
     const int c0 = 32 * G.grp + 16 * G.hi;
-    const float* ck = ws + ((int64_t(seg) * d.B + b) * d.H + h) * nch * int64_t(kD * kD);
+    const int64_t cb = chunk_base(d, seg, b, h);
+    const float* ck = ws + cb * int64_t(kD * kD);
 
     bwd_setup(sh, G, 512);
     float Er[16];
@@ -963,6 +939,8 @@ __global__ void __launch_bounds__(256, 1)
         tma_load_3d(smem_u32(st + T8), &mk, 0, h, row, bar);
         tma_load_3d(smem_u32(st + 2 * T8), &mv, 0, h, row, bar);
         tma_load_3d(smem_u32(st + 3 * T8), &mo, 0, h, row, bar);
+        tma_load_3d(smem_u32(st + 4 * T8), &mf, 0, 0, fac_row(cb + c, 0), bar);
+        tma_load_3d(smem_u32(st + 5 * T8), &mf, 0, 0, fac_row(cb + c, 1), bar);
     };
     if (G.tid == 0) {
         load(nch - 1, 0);
@@ -978,7 +956,7 @@ __global__ void __launch_bounds__(256, 1)
         uint8_t* Qs = smem + s * BA_STAGE;
         uint8_t* Ks = Qs + T8;
         uint8_t* Vs = Ks + T8;
-        const uint32_t sq = s * BA_STAGE, sk = sq + T8, so = sq + 3 * T8;
+        const uint32_t sq = s * BA_STAGE, sk = sq + T8, so = sq + 3 * T8, st = sq + 4 * T8, sl = sq + 5 * T8;
         float Sr[16];
         load_row16(ck + int64_t(c) * kD * kD, G.tau, c0, Sr);
         store_row16(smem + BA_S, G.tau, c0, Sr);
@@ -1015,12 +993,9 @@ __global__ void __launch_bounds__(256, 1)
             tok16(tmem, G, TX + 32 * G.grp, tx);
             tile_row_get16(Vs, G.tau, c0, Xr);
             decay16(sh.gs, G.tau, c0, false, m);
-            const float be = sh.beta_s[G.tau];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                const int r = c0 + e;
-                kg[e] = r < G.tau ? kk[e] * m[e] : 0.f;
-                La[G.tau * kP + r] = be * kg[e];
+                kg[e] = c0 + e < G.tau ? kk[e] * m[e] : 0.f;
                 qk[e] *= d.scale * m[e];
                 Xr[e] -= tx[e];
             }
@@ -1028,16 +1003,10 @@ __global__ void __launch_bounds__(256, 1)
             store_row16(smem + BA_X, G.tau, c0, Xr);
         }
         cta_sync_tc();
-        if (G.tid == 0) mma_mm(tmem + TDD, desc_plus(DM, BA_P), desc_plus(DM, so), 1);  // + P^T dO
-        tri_inverse(La, Xs, Ys);
-        {
-            float x[16];
-            xs_row16(Xs, G.tau, c0, x);
-            store_row16(smem + BA_LI, G.tau, c0, x);
-            t_row16(Xs, sh.beta_s, G.tau, c0, smem + BA_T);
+        if (G.tid == 0) {
+            mma_mm(tmem + TDD, desc_plus(DM, BA_P), desc_plus(DM, so), 1);  // + P^T dO
+            mma_km(tmem + TD, desc_plus(DK, st), desc_plus(DM, BA_X), 0);   // D = T X
         }
-        cta_sync_tc();
-        if (G.tid == 0) mma_km(tmem + TD, desc_plus(DK, BA_T), desc_plus(DM, BA_X), 0);  // D = T X
         commit_wait(&sh.mbar, mph, G.tid);
         {
             float x[16], y[16];
@@ -1048,7 +1017,7 @@ __global__ void __launch_bounds__(256, 1)
         }
         cta_sync_tc();
         if (G.tid == 0) {
-            mma_mm(tmem + TZ, desc_plus(DM, BA_LI), desc_plus(DM, BA_X), 0);  // dZ = L^{-T} dD
+            mma_mm(tmem + TZ, desc_plus(DM, sl), desc_plus(DM, BA_X), 0);     // dZ = L^{-T} dD
             mma_kk(tmem + TOD, desc_plus(DK, so), desc_plus(DK, BA_D), 0);    // dO D^T
             mma_kk(tmem + TDE, desc_plus(DK, BA_D), desc_plus(DK, BA_E), 0);  // D E^T
         }
@@ -1116,7 +1085,7 @@ __global__ void __launch_bounds__(256, 1)
             float x[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) x[e] = La[G.tau * kP + c0 + e] + La[(c0 + e) * kP + G.tau];
-            store_row16(smem + BA_T, G.tau, c0, x);  // dG + dG^T
+            store_row16(smem + BA_GS, G.tau, c0, x);  // dG + dG^T
             const int t = G.tid >> 2, part = G.tid & 3;
             float rs = 0.f;
 #pragma unroll
@@ -1126,7 +1095,7 @@ __global__ void __launch_bounds__(256, 1)
             if (part == 0) sh.dbm[t] = rs;
         }
         cta_sync_tc();
-        if (G.tid == 0) mma_km(tmem + TK, desc_plus(DK, BA_T), desc_plus(DM, sk), 1);  // + (dG + dG^T) K
+        if (G.tid == 0) mma_km(tmem + TK, desc_plus(DK, BA_GS), desc_plus(DM, sk), 1);  // + (dG + dG^T) K
         commit_wait(&sh.mbar, mph, G.tid);
         {
             float ka[16], de[16], xs[16], os[16], qv[16], kv[16];
@@ -1206,33 +1175,40 @@ rm_status launch_gdrtc(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
     using namespace gdrtc;
     if (!gdrtc_supports(d, RM_BF16)) return RM_ERR_UNSUPPORTED;
     const dim3 grid(d.nseg, d.B * d.H);
-    CUtensorMap mq, mk, mv, mo, mx, my;
+    // the factor table follows the saved states (one fp32 state per chunk) in the workspace
+    const int64_t nchunks = int64_t(d.B) * d.H * (d.T / kChunk);
+    __nv_bfloat16* fac = reinterpret_cast<__nv_bfloat16*>(p.ws + nchunks * kD * kD);
+    Dims fd = d;  // the factor table as a [2 nchunks 64][64] bf16 matrix
+    fd.B = 1;
+    fd.T = int(2 * nchunks * kD);
+    CUtensorMap mq, mk, mv, mo, mf, mx, my;
     if (!make_map(&mk, p.k, d, kD)) return RM_ERR_CUDA;
     if (op != GdrOp::kBackwardPrepare && !make_map(&mv, p.v, d, kD)) return RM_ERR_CUDA;
-    if (op != GdrOp::kPrepare && !make_map(&mq, p.q, d, kD, d.qh)) return RM_ERR_CUDA;
+    if (op != GdrOp::kPrepare && (!make_map(&mq, p.q, d, kD, d.qh) || !make_map(&mf, fac, fd, kD, 1)))
+        return RM_ERR_CUDA;
     if (op == GdrOp::kPrepare) {
         auto fn = gdrtc_prepare_kernel;
         if (!set_smem(fn, kPrepSmem)) return RM_ERR_CUDA;
-        fn<<<grid, 256, kPrepSmem, s>>>(d, mk, mv, p.g, p.beta, p.M, p.dS);
+        fn<<<grid, 256, kPrepSmem, s>>>(d, mk, mv, p.g, p.beta, p.M, p.dS, fac);
     } else if (op == GdrOp::kApply) {
         if (!make_map(&mo, p.o, d, kD)) return RM_ERR_CUDA;
         auto fn = gdrtc_apply_kernel;
         if (!set_smem(fn, kApplySmem)) return RM_ERR_CUDA;
-        fn<<<grid, 256, kApplySmem, s>>>(d, mq, mk, mv, mo, p.g, p.beta, p.S_in);
+        fn<<<grid, 256, kApplySmem, s>>>(d, mq, mk, mv, mf, mo, p.g, p.beta, p.S_in);
     } else if (op == GdrOp::kBackwardPrepare) {
         // z = 0: the dq walk (which also needs v); z = 1: the gamma walk
         if (!make_map(&mv, p.v, d, kD) || !make_map(&mo, p.dO, d, kD) || !make_map(&mx, p.dq, d, kD))
             return RM_ERR_CUDA;
         auto fn = gdrtc_bwd_prepare_kernel;
         if (!set_smem(fn, kBwdPrepSmem)) return RM_ERR_CUDA;
-        fn<<<dim3(d.nseg, d.B * d.H, 2), 256, kBwdPrepSmem, s>>>(d, mq, mk, mv, mo, mx, p.g, p.beta, p.S_in,
+        fn<<<dim3(d.nseg, d.B * d.H, 2), 256, kBwdPrepSmem, s>>>(d, mq, mk, mv, mo, mf, mx, p.g, p.beta, p.S_in,
                                                                 p.gamma_out, p.ws);
     } else if (op == GdrOp::kBackwardApply) {
         if (!make_map(&mo, p.dO, d, kD) || !make_map(&mx, p.dk, d, kD) || !make_map(&my, p.dv, d, kD))
             return RM_ERR_CUDA;
         auto fn = gdrtc_bwd_apply_kernel;
         if (!set_smem(fn, kBwdApplySmem)) return RM_ERR_CUDA;
-        fn<<<grid, 256, kBwdApplySmem, s>>>(d, mq, mk, mv, mo, mx, my, p.g, p.beta, p.dS_out, p.ws, p.dg,
+        fn<<<grid, 256, kBwdApplySmem, s>>>(d, mq, mk, mv, mo, mf, mx, my, p.g, p.beta, p.dS_out, p.ws, p.dg,
                                             p.dbeta);
     } else {
         return RM_ERR_INVALID_ARG;

@@ -58,7 +58,9 @@ struct GdrPtrs {
     void* dv = nullptr;
     float* dg = nullptr;
     float* dbeta = nullptr;
-    float* ws = nullptr;          // saved states: kBackwardPrepare -> kBackwardApply
+    float* ws = nullptr;          // the step's workspace: saved states (kBackwardPrepare ->
+                                  // kBackwardApply) and, on the tensor cores, the per-chunk
+                                  // factors (kPrepare -> the other sweeps)
 };
 bool gdr_supports(const Dims& d);
 size_t gdr_workspace_bytes(const Dims& d);

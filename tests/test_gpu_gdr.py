@@ -99,7 +99,7 @@ def test_gdr_rejects_unsupported_shapes():
     bad = C.ProblemSpec(1, 128, 2, 128, 16, 4, 16, 0.1, torch.float32)  # Dk = 128
     t = torch.zeros(16, device="cuda")
     with pytest.raises(C.RmCpError) as e:
-        C.rm_gdr_forward_prepare(bad, t, t, t, t, t, t)
+        C.rm_gdr_forward_prepare(bad, t, t, t, t, t, t, t)
     assert e.value.status == 4
 
 
