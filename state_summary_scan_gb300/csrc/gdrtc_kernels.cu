@@ -271,19 +271,22 @@ __device__ __forceinline__ int64_t chunk_base(const Dims& d, int seg, int b, int
 __device__ __forceinline__ int fac_row(int64_t ci, int f) { return int((2 * ci + f) * kD); }
 
 // ===========================================================================
-// forward apply: o from S_in.
-// Shared memory (8 KB tiles): two stages of Q|K|V|T; scale Q o gam, K o gam
-// (then -W), K o Gam[63], P, D, S (bf16), o staging.
+// forward apply: o from S_in.  Two CTAs a SM: one input stage, refilled with
+// the next chunk as soon as the chunk's first products (the last readers of
+// Q, K, V and T) are done.
+// Shared memory (8 KB tiles): Q|K|V|T; scale Q o gam (then o staging), K o gam
+// (then -W), K o Gam[63], P, D, S (bf16).
 // Tensor memory: [0,64) the state product; [64,128) Q K^T, then O; [128,192)
 // W; [192,256) U, then D.
 // ===========================================================================
 constexpr uint32_t AP_STAGE = 4 * T8;
-constexpr uint32_t AP_QG = 2 * AP_STAGE, AP_KG = AP_QG + T8, AP_KC = AP_KG + T8, AP_P = AP_KC + T8;
-constexpr uint32_t AP_DL = AP_P + T8, AP_S = AP_DL + T8, AP_O = AP_S + T8;
+constexpr uint32_t AP_QG = AP_STAGE, AP_KG = AP_QG + T8, AP_KC = AP_KG + T8, AP_P = AP_KC + T8;
+constexpr uint32_t AP_DL = AP_P + T8, AP_S = AP_DL + T8;
 constexpr uint32_t AP_WN = AP_KG;  // -W over K o gam, which dies with W
-constexpr size_t kApplySmem = AP_O + T8 + 1024;
+constexpr uint32_t AP_O = AP_QG;   // o over scale Q o gam, which dies with O
+constexpr size_t kApplySmem = AP_S + T8 + 1024;
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
     gdrtc_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                        const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                        const __grid_constant__ CUtensorMap mf, const __grid_constant__ CUtensorMap mo,
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t* smem = align1024(smem_raw);
     __shared__ GateSmem gs;
     __shared__ __align__(16) float beta_s[kChunk];
-    __shared__ __align__(8) uint64_t full[2], mbar;
+    __shared__ __align__(8) uint64_t full, mbar;
     __shared__ uint32_t tmem_slot;
     constexpr uint32_t TKK = 0, TQK = 64, TW = 128, TD = 192;
 
@@ -305,8 +308,7 @@ __global__ void __launch_bounds__(256, 1)
     const int64_t cb = chunk_base(d, seg, b, h);
 
     if (G.tid == 0) {
-        mbar_init(smem_u32(&full[0]), 1);
-        mbar_init(smem_u32(&full[1]), 1);
+        mbar_init(smem_u32(&full), 1);
         mbar_init(smem_u32(&mbar), 1);
         mbar_fence_init();
     }
@@ -319,36 +321,29 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    auto load = [&](int c, int s) {
+    auto load = [&](int c) {
         const int row = b * d.T + a0 + c * kChunk;
-        const uint32_t bar = smem_u32(&full[s]);
-        uint8_t* st = smem + s * AP_STAGE;
+        const uint32_t bar = smem_u32(&full);
+        uint8_t* st = smem;
         mbar_expect_tx(bar, AP_STAGE);
         tma_load_3d(smem_u32(st), &mq, 0, h / d.qdiv, row, bar);
         tma_load_3d(smem_u32(st + T8), &mk, 0, h, row, bar);
         tma_load_3d(smem_u32(st + 2 * T8), &mv, 0, h, row, bar);
         tma_load_3d(smem_u32(st + 3 * T8), &mf, 0, 0, fac_row(cb + c, 0), bar);
     };
-    if (G.tid == 0) {
-        load(0, 0);
-        if (nch > 1) load(1, 1);
-    }
+    if (G.tid == 0) load(0);
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
     GateFetch gf = gates_fetch(d, g, beta, b, h, a0, G);
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
-        const int s = c & 1;
         const int t0 = a0 + c * kChunk;
-        const uint32_t sq = s * AP_STAGE, sk = sq + T8, sv = sq + 2 * T8, st = sq + 3 * T8;
+        constexpr uint32_t sq = 0, sk = T8, sv = 2 * T8, st = 3 * T8;
         gates_commit(gf, gs, beta_s, G);
         if (c + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + kChunk, G);
-        if (G.tid == 0) {
-            if (c >= 1 && c + 1 < nch) load(c + 1, s ^ 1);  // the previous chunk's products are done
-            if (c >= 1) bulk_wait_read();                    // the o store has read its staging tile
-        }
+        if (G.tid == 0 && c >= 1) bulk_wait_read();  // the o store has read its staging tile
         __syncthreads();
-        mbar_wait(smem_u32(&full[s]), (c >> 1) & 1);
+        mbar_wait(smem_u32(&full), c & 1);
         tc_fence_after();
         if (G.tid == 0) mma_kk(tmem + TQK, desc_plus(DK, sq), desc_plus(DK, sk), 0);  // Q K^T
         rows_scaled(smem + sq, smem + AP_QG, gs.win, d.scale, G.tid);  // scale Q o gam
@@ -360,6 +355,7 @@ __global__ void __launch_bounds__(256, 1)
             mma_km(tmem + TD, desc_plus(DK, st), desc_plus(DM, sv), 0);
         }
         commit_wait(&mbar, mph, G.tid);
+        if (G.tid == 0 && c + 1 < nch) load(c + 1);  // Q, K, V and T are read
         {
             float qk[16], w[16], m[16];
             tok16x2(tmem, G, TQK + 32 * G.grp, TW + 32 * G.grp, qk, w);
@@ -612,15 +608,17 @@ __device__ __forceinline__ void bwd_setup(BwdShared& sh, const Geo& G, int cols)
 // (dq_t = scale S_t dO_t with S_t = gam_t S_prev + sum_{r<=t} Gam[t][r] k_r D_r^T)
 // and S_prev saved to the workspace before each chunk.
 // Shared memory: two stages of K|V|dO|T; K o gam (then -W), K o Gam[63],
-// scale dO o gam, D, S, P, dq staging (bf16).
+// scale dO o gam (then dq staging), D (then P), S (bf16).
 // Tensor memory: [0,64) dO D^T; [64,128) dq; [128,192) W, then the state
 // product; [192,256) U, then D.
 // ===========================================================================
 constexpr uint32_t DQ_STAGE = 4 * T8;
 constexpr uint32_t DQ_KG = 2 * DQ_STAGE, DQ_KC = DQ_KG + T8, DQ_OG = DQ_KC + T8, DQ_DL = DQ_OG + T8;
-constexpr uint32_t DQ_S = DQ_DL + T8, DQ_P = DQ_S + T8, DQ_O = DQ_P + T8;
+constexpr uint32_t DQ_S = DQ_DL + T8;
 constexpr uint32_t DQ_WN = DQ_KG;  // -W over K o gam, which dies with W
-constexpr size_t kDqSmem = DQ_O + T8 + 1024;
+constexpr uint32_t DQ_P = DQ_DL;   // P over D, which dies with dO D^T and the state product
+constexpr uint32_t DQ_O = DQ_OG;   // dq over scale dO o gam, which dies with dO S^T
+constexpr size_t kDqSmem = DQ_S + T8 + 1024;
 
 __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, const CUtensorMap* mv,
                                         const CUtensorMap* mo, const CUtensorMap* mf, const CUtensorMap* mdq,
@@ -735,14 +733,16 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
 //     dD = P^T dO + (K o Gam[63]) E,   dX = T^T dD,
 //     E <- scale (Q o gam)^T dO + gam_63 E - (K o gam)^T dX,
 // gamma = E at the segment start.  No state is needed.
-// Shared memory: two stages of Q|K|dO|T; K o gam, K o Gam[63], scale Q o gam,
-// P, dD, -dX, E (bf16).
+// Shared memory: two stages of Q|K|dO|T; K o gam, K o Gam[63] (then dD),
+// scale Q o gam (then P, then -dX), E (bf16).
 // Tensor memory: [0,64) dX; [64,128) Q K^T; [128,192) dD; [192,256) the E
 // product.
 // ===========================================================================
 constexpr uint32_t GA_STAGE = 4 * T8;
-constexpr uint32_t GA_KG = 2 * GA_STAGE, GA_KC = GA_KG + T8, GA_QG = GA_KC + T8, GA_P = GA_QG + T8;
-constexpr uint32_t GA_DD = GA_P + T8, GA_DX = GA_DD + T8, GA_E = GA_DX + T8;
+constexpr uint32_t GA_KG = 2 * GA_STAGE, GA_KC = GA_KG + T8, GA_QG = GA_KC + T8, GA_E = GA_QG + T8;
+constexpr uint32_t GA_P = GA_QG;   // P over scale Q o gam, which dies with its E product
+constexpr uint32_t GA_DD = GA_KC;  // dD over K o Gam[63], which dies with its dD product
+constexpr uint32_t GA_DX = GA_QG;  // -dX over P, which dies with P^T dO
 constexpr size_t kGaSmem = GA_E + T8 + 1024;
 constexpr size_t kBwdPrepSmem = kDqSmem > kGaSmem ? kDqSmem : kGaSmem;
 
@@ -841,7 +841,7 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
     save_row16(gamma + sum_off(d, seg, b, h), G.tau, c0, Er);
 }
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
     gdrtc_bwd_prepare_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
                              const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                              const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mf,
