@@ -26,10 +26,10 @@
 // Kernels, one CTA of 256 threads per (segment, row, head); thread 0 issues
 // the TMA loads and stores and the products, and the CTA steps through each
 // chunk together (two input stages):
+//   gdrtc_factor_kernel       each chunk's T and (I + A)^{-1}, every chunk at
+//                             once, into the workspace (forward prepare, first)
 //   gdrtc_prepare_kernel      the recurrence on [S | M] from [0 | I] with
-//                             values [V | 0]: delta_S and the transition M; it
-//                             also leaves each chunk's T and (I + A)^{-1} in
-//                             the workspace
+//                             values [V | 0]: delta_S and the transition M
 //   gdrtc_apply_kernel        o from S_in (T from the workspace)
 //   gdrtc_bwd_prepare_kernel  dq by a forward walk that saves each chunk's
 //                             incoming state, and gamma by a reverse walk of
@@ -405,35 +405,107 @@ __global__ void __launch_bounds__(256, 2)
 }
 
 // ===========================================================================
-// forward prepare: the recurrence on [S | M] from [0 | I] with values [V | 0]
-// over one segment: S_out = M S_in + delta_S with delta_S = S and M its last
-// state.  Per chunk: D_S = T V - W S, D_M = -W M, then S = gam_63 S +
-// (K o Gam[63])^T D_S and M likewise; T and (I + A)^{-1} go to the factor
-// table for the apply and the backward.
-// Shared memory: two stages of K|V; K o gam, K o Gam[63], T, -W, D_S, D_M,
-// S, M (bf16); fp32 A, X, Y.
-// Tensor memory: [0,64) K K^T, then the S product; [64,128) W, then the M
-// product; [128,192) U, then D_S; [192,256) D_M.
+// per-chunk factors (the first launch of the forward prepare): one CTA per
+// (chunk, row, head), every chunk at once (they do not depend on the state).
+// K K^T on the tensor cores, A from it and the chunk's gates, the fp32
+// inverse, then T = (I + A)^{-1} diag(beta) and (I + A)^{-1} (bf16) to the
+// factor table.
+// Shared memory: K (bf16); fp32 A, X, Y.  Tensor memory: K K^T.
 // ===========================================================================
-constexpr uint32_t PR_STAGE = 2 * T8;
-constexpr uint32_t PR_KG = 2 * PR_STAGE, PR_KC = PR_KG + T8, PR_T = PR_KC + T8, PR_WN = PR_T + T8;
-constexpr uint32_t PR_DS = PR_WN + T8, PR_DM = PR_DS + T8, PR_S = PR_DM + T8, PR_M = PR_S + T8;
-constexpr uint32_t PR_F32 = PR_M + T8;
-constexpr size_t kPrepSmem = PR_F32 + kF32Bytes + 1024;
+constexpr uint32_t FA_F32 = T8;
+constexpr size_t kFactorSmem = FA_F32 + kF32Bytes + 1024;
 
-__global__ void __launch_bounds__(256, 1)
-    gdrtc_prepare_kernel(const Dims d, const __grid_constant__ CUtensorMap mk,
-                         const __grid_constant__ CUtensorMap mv, const float* __restrict__ g,
-                         const float* __restrict__ beta, float* __restrict__ M, float* __restrict__ dS,
-                         __nv_bfloat16* __restrict__ fac) {
+__global__ void __launch_bounds__(256, 3)
+    gdrtc_factor_kernel(const Dims d, const __grid_constant__ CUtensorMap mk, const float* __restrict__ g,
+                        const float* __restrict__ beta, __nv_bfloat16* __restrict__ fac) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    float* La = reinterpret_cast<float*>(smem + PR_F32);
+    float* La = reinterpret_cast<float*>(smem + FA_F32);
     float* Xs = La + kD * kP;
     float* Ys = Xs + kD * kQ;
     __shared__ GateSmem gs;
     __shared__ __align__(16) float beta_s[kChunk];
-    __shared__ __align__(8) uint64_t full[2], mbar;
+    __shared__ __align__(8) uint64_t full, mbar;
+    __shared__ uint32_t tmem_slot;
+
+    const Geo G = geo();
+    const int b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int t0 = blockIdx.x * kChunk;
+    const int seg = t0 / d.L, c = (t0 % d.L) / kChunk;
+    const int64_t ci = chunk_base(d, seg, b, h) + c;
+    const int c0 = 32 * G.grp + 16 * G.hi;
+
+    if (G.tid == 0) {
+        mbar_init(smem_u32(&full), 1);
+        mbar_init(smem_u32(&mbar), 1);
+        mbar_fence_init();
+    }
+    if (G.warp == 0) tmem_alloc(smem_u32(&tmem_slot), 64);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (G.tid == 0) {
+        mbar_expect_tx(smem_u32(&full), T8);
+        tma_load_3d(smem_u32(smem), &mk, 0, h, b * d.T + t0, smem_u32(&full));
+    }
+    gates_commit(gates_fetch(d, g, beta, b, h, t0, G), gs, beta_s, G);
+    mbar_wait(smem_u32(&full), 0);
+    tc_fence_after();
+    const uint64_t DK = sdesc(smem_u32(smem), 16, 1024);
+    if (G.tid == 0) mma_kk(tmem, DK, DK, 0);  // K K^T
+    uint32_t mph = 0;
+    commit_wait(&mbar, mph, G.tid);
+    __syncthreads();  // the gate tables are complete
+    {
+        float kk[16], m[16];
+        tok16(tmem, G, 32 * G.grp, kk);
+        decay16(gs, G.tau, c0, false, m);
+        a_row16(beta_s, kk, m, G.tau, c0, La);
+    }
+    __syncthreads();
+    tri_inverse(La, Xs, Ys);
+    {
+        float x[16], t[16];
+        xs_row16(Xs, G.tau, c0, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) t[e] = x[e] * beta_s[c0 + e];
+        __nv_bfloat16* f = fac + (int64_t(fac_row(ci, 0)) + G.tau) * kD + c0;
+        store_bf16x16(f, t);
+        store_bf16x16(f + kD * kD, x);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 64);
+}
+
+// ===========================================================================
+// forward prepare walk (the second launch): the recurrence on [S | M] from
+// [0 | I] with values [V | 0] over one segment: S_out = M S_in + delta_S
+// with delta_S = S and M its last state.  Per chunk, with T from the factor
+// table: D_S = T V - W S, D_M = -W M, then S = gam_63 S + (K o Gam[63])^T D_S
+// and M likewise.  Two CTAs a SM: one input stage, refilled once the
+// chunk's first products are done.
+// Shared memory: K|V|T; K o gam (then -W), K o Gam[63], D_S, D_M, S, M (bf16).
+// Tensor memory: [0,64) the S product; [64,128) W, then the M product;
+// [128,192) U, then D_S; [192,256) D_M.
+// ===========================================================================
+constexpr uint32_t PR_STAGE = 3 * T8;
+constexpr uint32_t PR_KG = PR_STAGE, PR_KC = PR_KG + T8, PR_DS = PR_KC + T8, PR_DM = PR_DS + T8;
+constexpr uint32_t PR_S = PR_DM + T8, PR_M = PR_S + T8;
+constexpr uint32_t PR_WN = PR_KG;  // -W over K o gam, which dies with W
+constexpr size_t kPrepSmem = PR_M + T8 + 1024;
+
+__global__ void __launch_bounds__(256, 2)
+    gdrtc_prepare_kernel(const Dims d, const __grid_constant__ CUtensorMap mk,
+                         const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mf,
+                         const float* __restrict__ g, const float* __restrict__ beta, float* __restrict__ M,
+                         float* __restrict__ dS) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    __shared__ GateSmem gs;
+    __shared__ __align__(16) float beta_s[kChunk];
+    __shared__ __align__(8) uint64_t full, mbar;
     __shared__ uint32_t tmem_slot;
     constexpr uint32_t TKK = 0, TW = 64, TU = 128, TDM = 192;
 
@@ -445,8 +517,7 @@ __global__ void __launch_bounds__(256, 1)
     const int64_t cb = chunk_base(d, seg, b, h);
 
     if (G.tid == 0) {
-        mbar_init(smem_u32(&full[0]), 1);
-        mbar_init(smem_u32(&full[1]), 1);
+        mbar_init(smem_u32(&full), 1);
         mbar_init(smem_u32(&mbar), 1);
         mbar_fence_init();
     }
@@ -463,65 +534,36 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    auto load = [&](int c, int s) {
+    auto load = [&](int c) {
         const int row = b * d.T + a0 + c * kChunk;
-        const uint32_t bar = smem_u32(&full[s]);
-        uint8_t* st = smem + s * PR_STAGE;
+        const uint32_t bar = smem_u32(&full);
         mbar_expect_tx(bar, PR_STAGE);
-        tma_load_3d(smem_u32(st), &mk, 0, h, row, bar);
-        tma_load_3d(smem_u32(st + T8), &mv, 0, h, row, bar);
+        tma_load_3d(smem_u32(smem), &mk, 0, h, row, bar);
+        tma_load_3d(smem_u32(smem + T8), &mv, 0, h, row, bar);
+        tma_load_3d(smem_u32(smem + 2 * T8), &mf, 0, 0, fac_row(cb + c, 0), bar);
     };
-    if (G.tid == 0) {
-        load(0, 0);
-        if (nch > 1) load(1, 1);
-    }
+    if (G.tid == 0) load(0);
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
     GateFetch gf = gates_fetch(d, g, beta, b, h, a0, G);
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
-        const int s = c & 1;
         const int t0 = a0 + c * kChunk;
-        uint8_t* Ks = smem + s * PR_STAGE;
         gates_commit(gf, gs, beta_s, G);
         if (c + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + kChunk, G);
-        if (G.tid == 0 && c >= 1 && c + 1 < nch) load(c + 1, s ^ 1);  // the previous chunk's products are done
         __syncthreads();
-        mbar_wait(smem_u32(&full[s]), (c >> 1) & 1);
+        mbar_wait(smem_u32(&full), c & 1);
         tc_fence_after();
-        if (G.tid == 0) {
-            const uint64_t k = desc_plus(DK, s * PR_STAGE);
-            mma_kk(tmem + TKK, k, k, 0);  // K K^T
-        }
-        rows_scaled(Ks, smem + PR_KG, gs.win, 1.f, G.tid);   // K o gam
-        rows_scaled(Ks, smem + PR_KC, gs.wout, 1.f, G.tid);  // K o Gam[63]
-        commit_wait(&mbar, mph, G.tid);
-        {
-            float kk[16], m[16];
-            tok16(tmem, G, TKK + 32 * G.grp, kk);
-            decay16(gs, G.tau, c0, false, m);
-            a_row16(beta_s, kk, m, G.tau, c0, La);
-        }
-        __syncthreads();
-        tri_inverse(La, Xs, Ys);
-        {
-            // T into its tile, and T and (I + A)^{-1} into the factor table
-            float x[16], t[16];
-            xs_row16(Xs, G.tau, c0, x);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) t[e] = x[e] * beta_s[c0 + e];
-            store_row16(smem + PR_T, G.tau, c0, t);
-            __nv_bfloat16* f = fac + (int64_t(fac_row(cb + c, 0)) + G.tau) * kD + c0;
-            store_bf16x16(f, t);
-            store_bf16x16(f + kD * kD, x);
-        }
+        rows_scaled(smem, smem + PR_KG, gs.win, 1.f, G.tid);   // K o gam
+        rows_scaled(smem, smem + PR_KC, gs.wout, 1.f, G.tid);  // K o Gam[63]
         cta_sync_tc();
         if (G.tid == 0) {  // W = T (K o gam), U = T V
-            const uint64_t t = desc_plus(DK, PR_T);
+            const uint64_t t = desc_plus(DK, 2 * T8);
             mma_km(tmem + TW, t, desc_plus(DM, PR_KG), 0);
-            mma_km(tmem + TU, t, desc_plus(DM, s * PR_STAGE + T8), 0);
+            mma_km(tmem + TU, t, desc_plus(DM, T8), 0);
         }
         commit_wait(&mbar, mph, G.tid);
+        if (G.tid == 0 && c + 1 < nch) load(c + 1);  // K, V and T are read
         {
             float w[16];
             tok16(tmem, G, TW + 32 * G.grp, w);
@@ -538,8 +580,7 @@ __global__ void __launch_bounds__(256, 1)
         commit_wait(&mbar, mph, G.tid);
         {
             float x[16], y[16];
-            tok16(tmem, G, TU + 32 * G.grp, x);
-            tok16(tmem, G, TDM + 32 * G.grp, y);
+            tok16x2(tmem, G, TU + 32 * G.grp, TDM + 32 * G.grp, x, y);
             store_row16(smem + PR_DS, G.tau, c0, x);
             store_row16(smem + PR_DM, G.tau, c0, y);
         }
@@ -552,8 +593,7 @@ __global__ void __launch_bounds__(256, 1)
         commit_wait(&mbar, mph, G.tid);
         {
             float x[16], y[16];
-            tok16(tmem, G, TKK + 32 * G.grp, x);
-            tok16(tmem, G, TW + 32 * G.grp, y);
+            tok16x2(tmem, G, TKK + 32 * G.grp, TW + 32 * G.grp, x, y);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 Sr[e] = fmaf(gs.W, Sr[e], x[e]);
@@ -564,15 +604,8 @@ __global__ void __launch_bounds__(256, 1)
         }
         cta_sync_tc();
     }
-    {
-        float* ds = dS + sum_off(d, seg, b, h) + G.tau * kD + c0;
-        float* m = M + ((int64_t(seg) * d.B + b) * d.H + h) * kD * kD + G.tau * kD + c0;
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-            *reinterpret_cast<float4*>(ds + e) = make_float4(Sr[e], Sr[e + 1], Sr[e + 2], Sr[e + 3]);
-            *reinterpret_cast<float4*>(m + e) = make_float4(Mr[e], Mr[e + 1], Mr[e + 2], Mr[e + 3]);
-        }
-    }
+    save_row16(dS + sum_off(d, seg, b, h), G.tau, c0, Sr);
+    save_row16(M + ((int64_t(seg) * d.B + b) * d.H + h) * kD * kD, G.tau, c0, Mr);
     tc_fence_before();
     __syncthreads();
     if (G.warp == 0) tmem_dealloc(tmem, 256);
@@ -1187,9 +1220,16 @@ rm_status launch_gdrtc(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
     if (op != GdrOp::kPrepare && (!make_map(&mq, p.q, d, kD, d.qh) || !make_map(&mf, fac, fd, kD, 1)))
         return RM_ERR_CUDA;
     if (op == GdrOp::kPrepare) {
+        // every chunk's factors at once, then the walk over each segment's chunks
+        if (!make_map(&mf, fac, fd, kD, 1)) return RM_ERR_CUDA;
+        auto ff = gdrtc_factor_kernel;
+        if (!set_smem(ff, kFactorSmem)) return RM_ERR_CUDA;
+        ff<<<dim3(d.T / kChunk, d.B * d.H), 256, kFactorSmem, s>>>(d, mk, p.g, p.beta, fac);
+        if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+        note_launch(1);
         auto fn = gdrtc_prepare_kernel;
         if (!set_smem(fn, kPrepSmem)) return RM_ERR_CUDA;
-        fn<<<grid, 256, kPrepSmem, s>>>(d, mk, mv, p.g, p.beta, p.M, p.dS, fac);
+        fn<<<grid, 256, kPrepSmem, s>>>(d, mk, mv, mf, p.g, p.beta, p.M, p.dS);
     } else if (op == GdrOp::kApply) {
         if (!make_map(&mo, p.o, d, kD)) return RM_ERR_CUDA;
         auto fn = gdrtc_apply_kernel;
