@@ -274,8 +274,8 @@ __device__ __forceinline__ int fac_row(int64_t ci, int f) { return int((2 * ci +
 // forward apply: o from S_in.  Two CTAs a SM: one input stage, refilled with
 // the next chunk as soon as the chunk's first products (the last readers of
 // Q, K, V and T) are done.
-// Shared memory (8 KB tiles): Q|K|V|T; scale Q o gam (then o staging), K o gam
-// (then -W), K o Gam[63], P, D, S (bf16).
+// Shared memory (8 KB tiles): Q|K|V|T; scale Q o gam, K o gam (then -W),
+// K o Gam[63], P, D (then o staging), S (bf16).
 // Tensor memory: [0,64) the state product; [64,128) Q K^T, then O; [128,192)
 // W; [192,256) U, then D.
 // ===========================================================================
@@ -283,7 +283,7 @@ constexpr uint32_t AP_STAGE = 4 * T8;
 constexpr uint32_t AP_QG = AP_STAGE, AP_KG = AP_QG + T8, AP_KC = AP_KG + T8, AP_P = AP_KC + T8;
 constexpr uint32_t AP_DL = AP_P + T8, AP_S = AP_DL + T8;
 constexpr uint32_t AP_WN = AP_KG;  // -W over K o gam, which dies with W
-constexpr uint32_t AP_O = AP_QG;   // o over scale Q o gam, which dies with O
+constexpr uint32_t AP_O = AP_DL;   // o over D, which dies with O and the state product
 constexpr size_t kApplySmem = AP_S + T8 + 1024;
 
 __global__ void __launch_bounds__(256, 2)
@@ -294,8 +294,8 @@ __global__ void __launch_bounds__(256, 2)
                        const float* __restrict__ S_in) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    __shared__ GateSmem gs;
-    __shared__ __align__(16) float beta_s[kChunk];
+    __shared__ GateSmem gsb[2];
+    __shared__ __align__(16) float bsb[2][kChunk];
     __shared__ __align__(8) uint64_t full, mbar;
     __shared__ uint32_t tmem_slot;
     constexpr uint32_t TKK = 0, TQK = 64, TW = 128, TD = 192;
@@ -335,13 +335,13 @@ __global__ void __launch_bounds__(256, 2)
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
     GateFetch gf = gates_fetch(d, g, beta, b, h, a0, G);
+    gates_commit(gf, gsb[0], bsb[0], G);
+    if (nch > 1) gf = gates_fetch(d, g, beta, b, h, a0 + kChunk, G);
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
         const int t0 = a0 + c * kChunk;
         constexpr uint32_t sq = 0, sk = T8, sv = 2 * T8, st = 3 * T8;
-        gates_commit(gf, gs, beta_s, G);
-        if (c + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + kChunk, G);
-        if (G.tid == 0 && c >= 1) bulk_wait_read();  // the o store has read its staging tile
+        GateSmem& gs = gsb[c & 1];
         __syncthreads();
         mbar_wait(smem_u32(&full), c & 1);
         tc_fence_after();
@@ -353,6 +353,10 @@ __global__ void __launch_bounds__(256, 2)
         if (G.tid == 0) {  // W = T (K o gam), U = T V
             mma_km(tmem + TW, desc_plus(DK, st), desc_plus(DM, AP_KG), 0);
             mma_km(tmem + TD, desc_plus(DK, st), desc_plus(DM, sv), 0);
+        }
+        if (c + 1 < nch) {  // the next chunk's gate tables, while the products run
+            gates_commit(gf, gsb[(c + 1) & 1], bsb[(c + 1) & 1], G);
+            if (c + 2 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + 2 * kChunk, G);
         }
         commit_wait(&mbar, mph, G.tid);
         if (G.tid == 0 && c + 1 < nch) load(c + 1);  // Q, K, V and T are read
@@ -368,6 +372,7 @@ __global__ void __launch_bounds__(256, 2)
             store_row16(smem + AP_P, G.tau, c0, qk);
             store_row16(smem + AP_WN, G.tau, c0, w);
         }
+        if (G.tid == 0) bulk_wait_read();  // the previous o store has read its tile (over D)
         cta_sync_tc();
         if (G.tid == 0)  // D = U - W S_prev
             mma_km(tmem + TD, desc_plus(DK, AP_WN), desc_plus(DM, AP_S), 1);
@@ -503,8 +508,8 @@ __global__ void __launch_bounds__(256, 2)
                          float* __restrict__ dS) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    __shared__ GateSmem gs;
-    __shared__ __align__(16) float beta_s[kChunk];
+    __shared__ GateSmem gsb[2];
+    __shared__ __align__(16) float bsb[2][kChunk];
     __shared__ __align__(8) uint64_t full, mbar;
     __shared__ uint32_t tmem_slot;
     constexpr uint32_t TKK = 0, TW = 64, TU = 128, TDM = 192;
@@ -546,11 +551,12 @@ __global__ void __launch_bounds__(256, 2)
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
     GateFetch gf = gates_fetch(d, g, beta, b, h, a0, G);
+    gates_commit(gf, gsb[0], bsb[0], G);
+    if (nch > 1) gf = gates_fetch(d, g, beta, b, h, a0 + kChunk, G);
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
         const int t0 = a0 + c * kChunk;
-        gates_commit(gf, gs, beta_s, G);
-        if (c + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + kChunk, G);
+        GateSmem& gs = gsb[c & 1];
         __syncthreads();
         mbar_wait(smem_u32(&full), c & 1);
         tc_fence_after();
@@ -561,6 +567,10 @@ __global__ void __launch_bounds__(256, 2)
             const uint64_t t = desc_plus(DK, 2 * T8);
             mma_km(tmem + TW, t, desc_plus(DM, PR_KG), 0);
             mma_km(tmem + TU, t, desc_plus(DM, T8), 0);
+        }
+        if (c + 1 < nch) {  // the next chunk's gate tables, while the products run
+            gates_commit(gf, gsb[(c + 1) & 1], bsb[(c + 1) & 1], G);
+            if (c + 2 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + 2 * kChunk, G);
         }
         commit_wait(&mbar, mph, G.tid);
         if (G.tid == 0 && c + 1 < nch) load(c + 1);  // K, V and T are read
@@ -614,8 +624,8 @@ __global__ void __launch_bounds__(256, 2)
 
 // Per-block state of the backward kernels (static shared memory).
 struct BwdShared {
-    GateSmem gs;
-    alignas(16) float beta_s[kChunk];
+    GateSmem gsb[2];                   // gate tables, by chunk parity
+    alignas(16) float bsb[2][kChunk];  // write strengths, by chunk parity
     float red[3][2][kChunk];  // row partials of the gate, key-norm and beta terms, by column half
     float dbm[kChunk];        // row sum minus column sum of the score-gradient products
     float red_se[8];          // per-warp <S_prev, E>
@@ -641,7 +651,7 @@ __device__ __forceinline__ void bwd_setup(BwdShared& sh, const Geo& G, int cols)
 // (dq_t = scale S_t dO_t with S_t = gam_t S_prev + sum_{r<=t} Gam[t][r] k_r D_r^T)
 // and S_prev saved to the workspace before each chunk.
 // Shared memory: two stages of K|V|dO|T; K o gam (then -W), K o Gam[63],
-// scale dO o gam (then dq staging), D (then P), S (bf16).
+// scale dO o gam, D (then P, then dq staging), S (bf16).
 // Tensor memory: [0,64) dO D^T; [64,128) dq; [128,192) W, then the state
 // product; [192,256) U, then D.
 // ===========================================================================
@@ -650,7 +660,7 @@ constexpr uint32_t DQ_KG = 2 * DQ_STAGE, DQ_KC = DQ_KG + T8, DQ_OG = DQ_KC + T8,
 constexpr uint32_t DQ_S = DQ_DL + T8;
 constexpr uint32_t DQ_WN = DQ_KG;  // -W over K o gam, which dies with W
 constexpr uint32_t DQ_P = DQ_DL;   // P over D, which dies with dO D^T and the state product
-constexpr uint32_t DQ_O = DQ_OG;   // dq over scale dO o gam, which dies with dO S^T
+constexpr uint32_t DQ_O = DQ_DL;   // dq over P, which dies with P K
 constexpr size_t kDqSmem = DQ_S + T8 + 1024;
 
 __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, const CUtensorMap* mv,
@@ -686,29 +696,31 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
     GateFetch gf = gates_fetch(d, g, beta, b, h, a0, G);
+    gates_commit(gf, sh.gsb[0], sh.bsb[0], G);
+    if (nch > 1) gf = gates_fetch(d, g, beta, b, h, a0 + kChunk, G);
     uint32_t mph = 0;
     for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const int t0 = a0 + c * kChunk;
         const uint32_t sk = s * DQ_STAGE, sv = sk + T8, so = sk + 2 * T8, st = sk + 3 * T8;
         save_row16(ck + int64_t(c) * kD * kD, G.tau, c0, Sr);
-        gates_commit(gf, sh.gs, sh.beta_s, G);
-        if (c + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + kChunk, G);
-        if (G.tid == 0) {
-            if (c >= 1 && c + 1 < nch) load(c + 1, s ^ 1);  // the previous chunk's products are done
-            if (c >= 1) bulk_wait_read();                    // the dq store has read its staging tile
-        }
+        GateSmem& gs = sh.gsb[c & 1];
+        if (G.tid == 0 && c >= 1 && c + 1 < nch) load(c + 1, s ^ 1);  // the previous chunk's products are done
         __syncthreads();
         mbar_wait(smem_u32(&sh.full[s]), (c >> 1) & 1);
         tc_fence_after();
-        rows_scaled(smem + sk, smem + DQ_KG, sh.gs.win, 1.f, G.tid);      // K o gam
-        rows_scaled(smem + sk, smem + DQ_KC, sh.gs.wout, 1.f, G.tid);     // K o Gam[63]
-        rows_scaled(smem + so, smem + DQ_OG, sh.gs.win, d.scale, G.tid);  // scale dO o gam
+        rows_scaled(smem + sk, smem + DQ_KG, gs.win, 1.f, G.tid);      // K o gam
+        rows_scaled(smem + sk, smem + DQ_KC, gs.wout, 1.f, G.tid);     // K o Gam[63]
+        rows_scaled(smem + so, smem + DQ_OG, gs.win, d.scale, G.tid);  // scale dO o gam
         cta_sync_tc();
         if (G.tid == 0) {
             mma_kk(tmem + TQ, desc_plus(DK, DQ_OG), desc_plus(DK, DQ_S), 0);  // (scale dO o gam) S^T
             mma_km(tmem + TW, desc_plus(DK, st), desc_plus(DM, DQ_KG), 0);    // W = T (K o gam)
             mma_km(tmem + TD, desc_plus(DK, st), desc_plus(DM, sv), 0);       // U = T V
+        }
+        if (c + 1 < nch) {  // the next chunk's gate tables, while the products run
+            gates_commit(gf, sh.gsb[(c + 1) & 1], sh.bsb[(c + 1) & 1], G);
+            if (c + 2 < nch) gf = gates_fetch(d, g, beta, b, h, t0 + 2 * kChunk, G);
         }
         commit_wait(&sh.mbar, mph, G.tid);
         {
@@ -718,6 +730,7 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
             for (int e = 0; e < 16; ++e) w[e] = -w[e];
             store_row16(smem + DQ_WN, G.tau, c0, w);
         }
+        if (G.tid == 0) bulk_wait_read();  // the previous dq store has read its tile (over D)
         cta_sync_tc();
         if (G.tid == 0) mma_km(tmem + TD, desc_plus(DK, DQ_WN), desc_plus(DM, DQ_S), 1);  // D = U - W S_prev
         commit_wait(&sh.mbar, mph, G.tid);
@@ -735,12 +748,12 @@ __device__ __forceinline__ void dq_walk(const Dims& d, const CUtensorMap* mk, co
         {
             float p[16], m[16], y[16];
             tok16x2(tmem, G, TKK + 32 * G.grp, TW + 32 * G.grp, p, y);
-            decay16(sh.gs, G.tau, c0, false, m);
+            decay16(gs, G.tau, c0, false, m);
 #pragma unroll
             for (int e = 0; e < 16; ++e) p[e] *= d.scale * m[e];
             store_row16(smem + DQ_P, G.tau, c0, p);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) Sr[e] = fmaf(sh.gs.W, Sr[e], y[e]);
+            for (int e = 0; e < 16; ++e) Sr[e] = fmaf(gs.W, Sr[e], y[e]);
             store_row16(smem + DQ_S, G.tau, c0, Sr);
         }
         cta_sync_tc();
@@ -812,31 +825,36 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
     GateFetch gf = gates_fetch(d, g, beta, b, h, a0 + (nch - 1) * kChunk, G);
+    gates_commit(gf, sh.gsb[0], sh.bsb[0], G);
+    if (nch > 1) gf = gates_fetch(d, g, beta, b, h, a0 + (nch - 2) * kChunk, G);
     uint32_t mph = 0;
     for (int it = 0; it < nch; ++it) {
         const int c = nch - 1 - it, s = it & 1;
         const int t0 = a0 + c * kChunk;
         const uint32_t sq = s * GA_STAGE, sk = sq + T8, so = sq + 2 * T8, st = sq + 3 * T8;
-        gates_commit(gf, sh.gs, sh.beta_s, G);
-        if (it + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 - kChunk, G);
+        GateSmem& gs = sh.gsb[it & 1];
         if (G.tid == 0 && it >= 1 && it + 1 < nch) load(c - 1, s ^ 1);  // the previous chunk's products are done
         __syncthreads();
         mbar_wait(smem_u32(&sh.full[s]), (it >> 1) & 1);
         tc_fence_after();
         if (G.tid == 0) mma_kk(tmem + TQK, desc_plus(DK, sq), desc_plus(DK, sk), 0);  // Q K^T
-        rows_scaled(smem + sk, smem + GA_KG, sh.gs.win, 1.f, G.tid);      // K o gam
-        rows_scaled(smem + sk, smem + GA_KC, sh.gs.wout, 1.f, G.tid);     // K o Gam[63]
-        rows_scaled(smem + sq, smem + GA_QG, sh.gs.win, d.scale, G.tid);  // scale Q o gam
+        rows_scaled(smem + sk, smem + GA_KG, gs.win, 1.f, G.tid);      // K o gam
+        rows_scaled(smem + sk, smem + GA_KC, gs.wout, 1.f, G.tid);     // K o Gam[63]
+        rows_scaled(smem + sq, smem + GA_QG, gs.win, d.scale, G.tid);  // scale Q o gam
         cta_sync_tc();
         if (G.tid == 0) {
             mma_km(tmem + TDD, desc_plus(DK, GA_KC), desc_plus(DM, GA_E), 0);  // (K o Gam[63]) E
             mma_mm(tmem + TE, desc_plus(DM, GA_QG), desc_plus(DM, so), 0);     // (scale Q o gam)^T dO
         }
+        if (it + 1 < nch) {  // the next chunk's gate tables, while the products run
+            gates_commit(gf, sh.gsb[(it + 1) & 1], sh.bsb[(it + 1) & 1], G);
+            if (it + 2 < nch) gf = gates_fetch(d, g, beta, b, h, t0 - 2 * kChunk, G);
+        }
         commit_wait(&sh.mbar, mph, G.tid);
         {
             float qk[16], m[16];
             tok16(tmem, G, TQK + 32 * G.grp, qk);
-            decay16(sh.gs, G.tau, c0, false, m);
+            decay16(gs, G.tau, c0, false, m);
 #pragma unroll
             for (int e = 0; e < 16; ++e) qk[e] *= d.scale * m[e];
             store_row16(smem + GA_P, G.tau, c0, qk);
@@ -866,7 +884,7 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
             float x[16];
             tok16(tmem, G, TE + 32 * G.grp, x);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) Er[e] = fmaf(sh.gs.W, Er[e], x[e]);
+            for (int e = 0; e < 16; ++e) Er[e] = fmaf(gs.W, Er[e], x[e]);
             store_row16(smem + GA_E, G.tau, c0, Er);
         }
         cta_sync_tc();
@@ -982,6 +1000,10 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
     GateFetch gf = gates_fetch(d, g, beta, b, h, a0 + (nch - 1) * kChunk, G);
+    gates_commit(gf, sh.gsb[0], sh.bsb[0], G);
+    if (nch > 1) gf = gates_fetch(d, g, beta, b, h, a0 + (nch - 2) * kChunk, G);
+    float Sn[16];  // S_prev of the chunk about to start, loaded during the one before
+    load_row16(ck + int64_t(nch - 1) * kD * kD, G.tau, c0, Sn);
     uint32_t mph = 0;
     for (int it = 0; it < nch; ++it) {
         const int c = nch - 1 - it, s = it & 1;
@@ -991,14 +1013,12 @@ __global__ void __launch_bounds__(256, 1)
         uint8_t* Vs = Ks + T8;
         const uint32_t sq = s * BA_STAGE, sk = sq + T8, so = sq + 3 * T8, st = sq + 4 * T8, sl = sq + 5 * T8;
         float Sr[16];
-        load_row16(ck + int64_t(c) * kD * kD, G.tau, c0, Sr);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) Sr[e] = Sn[e];
         store_row16(smem + BA_S, G.tau, c0, Sr);
-        gates_commit(gf, sh.gs, sh.beta_s, G);
-        if (it + 1 < nch) gf = gates_fetch(d, g, beta, b, h, t0 - kChunk, G);
-        if (G.tid == 0) {
-            if (it >= 1 && it + 1 < nch) load(c - 1, s ^ 1);  // the previous chunk's products are done
-            if (it >= 1) bulk_wait_read();                     // the dv and dk stores have read their tiles
-        }
+        GateSmem& gs = sh.gsb[it & 1];
+        const float* beta_s = sh.bsb[it & 1];
+        if (G.tid == 0 && it >= 1 && it + 1 < nch) load(c - 1, s ^ 1);  // the previous chunk's products are done
         __syncthreads();
         mbar_wait(smem_u32(&sh.full[s]), (it >> 1) & 1);
         tc_fence_after();
@@ -1006,15 +1026,20 @@ __global__ void __launch_bounds__(256, 1)
             mma_kk(tmem + TKK, desc_plus(DK, sk), desc_plus(DK, sk), 0);
             mma_kk(tmem + TQK, desc_plus(DK, sq), desc_plus(DK, sk), 0);
         }
-        rows_scaled(Ks, smem + BA_KG, sh.gs.win, 1.f, G.tid);      // K o gam
-        rows_scaled(Ks, smem + BA_KC, sh.gs.wout, 1.f, G.tid);     // K o Gam[63]
-        rows_scaled(Qs, smem + BA_QG, sh.gs.win, d.scale, G.tid);  // scale Q o gam
+        rows_scaled(Ks, smem + BA_KG, gs.win, 1.f, G.tid);      // K o gam
+        rows_scaled(Ks, smem + BA_KC, gs.wout, 1.f, G.tid);     // K o Gam[63]
+        rows_scaled(Qs, smem + BA_QG, gs.win, d.scale, G.tid);  // scale Q o gam
         cta_sync_tc();
         if (G.tid == 0) {
             mma_km(tmem + TX, desc_plus(DK, BA_KG), desc_plus(DM, BA_S), 0);   // (K o gam) S_prev
             mma_km(tmem + TDD, desc_plus(DK, BA_KC), desc_plus(DM, BA_E), 0);  // (K o Gam[63]) E
             mma_mm(tmem + TE, desc_plus(DM, BA_QG), desc_plus(DM, so), 0);     // (scale Q o gam)^T dO
             mma_kk(tmem + TOS, desc_plus(DK, so), desc_plus(DK, BA_S), 0);     // dO S_prev^T
+        }
+        if (it + 1 < nch) {  // the next chunk's gate tables, while the products run
+            gates_commit(gf, sh.gsb[(it + 1) & 1], sh.bsb[(it + 1) & 1], G);
+            if (it + 2 < nch) gf = gates_fetch(d, g, beta, b, h, t0 - 2 * kChunk, G);
+            load_row16(ck + int64_t(c - 1) * kD * kD, G.tau, c0, Sn);  // the next chunk's S_prev
         }
         commit_wait(&sh.mbar, mph, G.tid);
         // kg = G o Gam (strict, within a sequence) and X stay in registers
@@ -1025,7 +1050,7 @@ __global__ void __launch_bounds__(256, 1)
             tok16(tmem, G, TQK + 32 * G.grp, qk);
             tok16(tmem, G, TX + 32 * G.grp, tx);
             tile_row_get16(Vs, G.tau, c0, Xr);
-            decay16(sh.gs, G.tau, c0, false, m);
+            decay16(gs, G.tau, c0, false, m);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 kg[e] = c0 + e < G.tau ? kk[e] * m[e] : 0.f;
@@ -1048,6 +1073,7 @@ __global__ void __launch_bounds__(256, 1)
             tok16(tmem, G, TDD + 32 * G.grp, y);
             store_row16(smem + BA_X, G.tau, c0, y);  // dD
         }
+        if (G.tid == 0) bulk_wait_read();  // the previous dv and dk stores have read their tiles
         cta_sync_tc();
         if (G.tid == 0) {
             mma_mm(tmem + TZ, desc_plus(DM, sl), desc_plus(DM, BA_X), 0);     // dZ = L^{-T} dD
@@ -1063,8 +1089,8 @@ __global__ void __launch_bounds__(256, 1)
             tok16(tmem, G, TQK + 32 * G.grp, qk);
             tok16(tmem, G, TDE + 32 * G.grp, de);
             tile_row_get16(Ks, G.tau, c0, kv);
-            decay16(sh.gs, G.tau, c0, false, m);
-            const float be = sh.beta_s[G.tau];
+            decay16(gs, G.tau, c0, false, m);
+            const float be = beta_s[G.tau];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 pb = fmaf(z[e], Xr[e], pb);
@@ -1099,8 +1125,8 @@ __global__ void __launch_bounds__(256, 1)
             float da[16], ee[16], m[16];
             tok16(tmem, G, TDA + 32 * G.grp, da);
             tok16(tmem, G, TE + 32 * G.grp, ee);
-            decay16(sh.gs, G.tau, c0, true, m);
-            const float be = sh.beta_s[G.tau];
+            decay16(gs, G.tau, c0, true, m);
+            const float be = beta_s[G.tau];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int r = c0 + e;
@@ -1109,7 +1135,7 @@ __global__ void __launch_bounds__(256, 1)
                 Ys[G.tau * kP + r] += a * be * kg[e];  // M2 = dA o A
                 La[G.tau * kP + r] = a * be * m[e];    // dG
                 pse = fmaf(Sr[e], Er[e], pse);
-                Er[e] = fmaf(sh.gs.W, Er[e], ee[e]);
+                Er[e] = fmaf(gs.W, Er[e], ee[e]);
             }
             store_row16(smem + BA_E, G.tau, c0, Er);
         }
@@ -1138,7 +1164,7 @@ __global__ void __launch_bounds__(256, 1)
             tok16(tmem, G, TOS + 32 * G.grp, os);
             tile_row_get16(Qs, G.tau, c0, qv);
             tile_row_get16(Ks, G.tau, c0, kv);
-            const float wo = sh.gs.wout[G.tau], gm = sh.gs.win[G.tau];
+            const float wo = gs.wout[G.tau], gm = gs.win[G.tau];
             float pq = 0.f, pk = 0.f;
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -1171,7 +1197,7 @@ __global__ void __launch_bounds__(256, 1)
             float db1 = sh.red[0][0][u1] + sh.red[0][1][u1] + sh.dbm[u1];
             const float wsum = warp_sum(sh.red[1][0][u0] + sh.red[1][1][u0] + sh.red[1][0][u1] + sh.red[1][1][u1]);
             const float se = warp_sum(G.lane < 8 ? sh.red_se[G.lane] : 0.f);
-            if (u1 == kChunk - 1) db1 += sh.gs.W * se + wsum;
+            if (u1 == kChunk - 1) db1 += gs.W * se + wsum;
             float suf = db0 + db1;  // inclusive suffix sum over lanes >= lane
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
