@@ -231,110 +231,108 @@ __global__ void __launch_bounds__(128) gdr_gamma_sweep(Dims d, const T* __restri
 // ---------------------------------------------------------------------------
 // Summary folds with matrix transitions: each column of the carried state
 // folds on its own (S <- M S + X acts column by column), so one CTA takes
-// fold_cols(DK) columns of one (row, head): 4 for Dk = 64 (one column a
-// thread), the 256 / DK columns of one thread a row otherwise.  Thread (r, q):
-// state row r and columns q * CPT .. q * CPT + CPT - 1 of the block; the
-// carried block and M_i [DK][DK] sit in shared memory.  The next segment's
-// M_i and X_i are loaded into registers while the current one is folded, so
-// that the chain of folds waits on shared memory only.
+// kFoldCols = 4 columns of one (row, head), one thread per state row r (DK
+// threads).  The thread holds row r of M_i (column r for the suffix's M_i^T)
+// in registers, loaded two segments ahead, and reads the
+// carried block's rows as 16-byte vectors from shared memory, so each loaded
+// entry serves four multiply-adds; it writes its own row of the result.
 //   prefix: S_in[j] = fold over [pre_j, j) of S <- M_i S + dS_i  (from 0)
 //   suffix: dS_out[j] = fold over (j, fol_j) of D <- M_i^T D + gamma_i,
 //           from the last segment down (from 0)
-// grid (B*H, ceil(Dv / fold_cols(DK))); block 256.
+// grid (B*H, Dv / kFoldCols); block DK.
 // ---------------------------------------------------------------------------
-__host__ __device__ constexpr int fold_cols(int dk) { return 256 / dk > 4 ? 256 / dk : 4; }
+constexpr int kFoldCols = 4;
 
 template <int DK, bool SUFFIX>
-__global__ void __launch_bounds__(256) gdr_compose(Dims d, const float* __restrict__ M,
-                                                   const float* __restrict__ X,
-                                                   const int32_t* __restrict__ range,
-                                                   float* __restrict__ out) {
-    constexpr int FC = fold_cols(DK);
-    constexpr int TPR = 256 / DK;       // threads per state row
-    constexpr int CPT = FC / TPR;       // columns per thread
-    constexpr int MPT = DK * DK / 256;  // entries of M_i a thread loads
-    static_assert(CPT >= 1 && MPT >= 1, "fold block narrower than the threads of a row");
-    __shared__ float m_s[DK][DK + 1];
-    __shared__ float s_s[2][DK][FC];
+__global__ void __launch_bounds__(64) gdr_compose(Dims d, const float* __restrict__ M,
+                                                  const float* __restrict__ X,
+                                                  const int32_t* __restrict__ range,
+                                                  float* __restrict__ out) {
+    __shared__ float4 s_s[2][DK];  // the carried block: row c, the CTA's four columns
     const int bh = blockIdx.x;
     const int b = bh / d.H, h = bh % d.H;
-    const int r = threadIdx.x / TPR, q = threadIdx.x % TPR;
-    const int c0 = blockIdx.y * FC + q * CPT;  // this thread's first column
+    const int r = threadIdx.x;                // state row
+    const int c0 = blockIdx.y * kFoldCols;    // first column (Dv is a multiple of 8)
     const int n = d.nseg;
     int buf = 0;  // s_s[buf] holds the carried block
-    float mp[MPT], xp[CPT];
-    int pf = -1;  // the segment whose M_i and X_i are in mp and xp (the same in every thread)
-    auto prefetch = [&](int i) {
+    // two segments in flight: slot i & 1 holds segment i's row of M_i and X_i
+    // (the folds walk the segments in order, so i + 2 refills the slot i frees)
+    float mpa[DK], mpb[DK];
+    float4 xpa, xpb;
+    int pfa = -1, pfb = -1;  // the segment in each slot (the same in every thread)
+    auto fetch = [&](int i, float (&mp)[DK], float4& xp) {
         const float* mi = M + ((int64_t(i) * d.B + b) * d.H + h) * DK * DK;
+        if (SUFFIX) {
 #pragma unroll
-        for (int u = 0; u < MPT; ++u) mp[u] = __ldg(mi + threadIdx.x + 256 * u);
-        const float* xi = X + sum_off(d, i, b, h) + int64_t(r) * d.Dv;
+            for (int c = 0; c < DK; ++c) mp[c] = __ldg(mi + c * DK + r);
+        } else {
 #pragma unroll
-        for (int u = 0; u < CPT; ++u) xp[u] = c0 + u < d.Dv ? __ldg(xi + c0 + u) : 0.f;
-        pf = i;
+            for (int c = 0; c < DK; c += 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(mi + r * DK + c));
+                mp[c] = v.x; mp[c + 1] = v.y; mp[c + 2] = v.z; mp[c + 3] = v.w;
+            }
+        }
+        xp = __ldg(reinterpret_cast<const float4*>(X + sum_off(d, i, b, h) + int64_t(r) * d.Dv + c0));
     };
-    auto clear = [&]() {
+    auto prefetch = [&](int i) {
+        if (i < 0 || i >= n) return;
+        if (i & 1) {
+            fetch(i, mpb, xpb);
+            pfb = i;
+        } else {
+            fetch(i, mpa, xpa);
+            pfa = i;
+        }
+    };
+    auto clear = [&]() { s_s[buf][r] = make_float4(0.f, 0.f, 0.f, 0.f); };
+    auto step = [&](const float (&m)[DK], float4 a0) {
+        float4 a1 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < CPT; ++u) s_s[buf][r][q * CPT + u] = 0.f;
+        for (int c = 0; c < DK; c += 2) {
+            const float4 s0 = s_s[buf][c], s1 = s_s[buf][c + 1];
+            a0.x = fmaf(m[c], s0.x, a0.x); a0.y = fmaf(m[c], s0.y, a0.y);
+            a0.z = fmaf(m[c], s0.z, a0.z); a0.w = fmaf(m[c], s0.w, a0.w);
+            a1.x = fmaf(m[c + 1], s1.x, a1.x); a1.y = fmaf(m[c + 1], s1.y, a1.y);
+            a1.z = fmaf(m[c + 1], s1.z, a1.z); a1.w = fmaf(m[c + 1], s1.w, a1.w);
+        }
+        s_s[buf ^ 1][r] = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
     };
     // s_s[buf ^ 1] = M_i s_s[buf] + X_i (M_i^T for the suffix); buf flips
     auto fold = [&](int i) {
-        if (pf != i) prefetch(i);
-        __syncthreads();  // earlier readers of m_s and s_s are done
-#pragma unroll
-        for (int u = 0; u < MPT; ++u) {
-            const int e = threadIdx.x + 256 * u;
-            m_s[e / DK][e % DK] = mp[u];
-        }
-        float acc[CPT][4];
-#pragma unroll
-        for (int u = 0; u < CPT; ++u) {
-            acc[u][0] = xp[u];
-            acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
-        }
-        const int nx = SUFFIX ? i - 1 : i + 1;  // the likely next fold
-        if (nx >= 0 && nx < n) prefetch(nx);
-        __syncthreads();
-#pragma unroll
-        for (int u = 0; u < CPT; ++u) {
-#pragma unroll 4
-            for (int c = 0; c < DK; c += 4) {
-#pragma unroll
-                for (int w = 0; w < 4; ++w)
-                    acc[u][w] = fmaf(SUFFIX ? m_s[c + w][r] : m_s[r][c + w], s_s[buf][c + w][q * CPT + u],
-                                     acc[u][w]);
-            }
-            s_s[buf ^ 1][r][q * CPT + u] = (acc[u][0] + acc[u][1]) + (acc[u][2] + acc[u][3]);
-        }
+        const bool odd = i & 1;
+        if ((odd ? pfb : pfa) != i) prefetch(i);
+        __syncthreads();  // the carried block is complete
+        if (odd)
+            step(mpb, xpb);
+        else
+            step(mpa, xpa);
         buf ^= 1;
+        prefetch(SUFFIX ? i - 2 : i + 2);  // into the slot just read
     };
-    // the fold for segment j restarts whenever its range start (end) moves
+    // the fold for segment j restarts whenever its range start (end) moves;
+    // the next segment's bound is loaded a segment ahead
     int cur = SUFFIX ? n : 0;
     clear();
+    prefetch(SUFFIX ? n - 1 : 0);
+    prefetch(SUFFIX ? n - 2 : 1);
+    int rnext = range ? __ldg(range + (SUFFIX ? n - 1 : 0)) : (SUFFIX ? n : 0);
     for (int u = 0; u < n; ++u) {
         const int j = SUFFIX ? n - 1 - u : u;
-        int lim;
-        if (SUFFIX) {
-            lim = range ? __ldg(range + j) : n;
+        int lim = rnext;
+        if (range && u + 1 < n) rnext = __ldg(range + (SUFFIX ? j - 1 : j + 1));
+        if (SUFFIX)
             lim = lim < j + 1 ? j + 1 : (lim > n ? n : lim);
-        } else {
-            lim = range ? __ldg(range + j) : 0;
+        else
             lim = lim < 0 ? 0 : (lim > j ? j : lim);
-        }
         if (lim != cur) {  // rebuild the fold over the new range
-            __syncthreads();
+            __syncthreads();  // every thread has read the old carried block
             clear();
             const int i0 = SUFFIX ? lim - 1 : lim;
             for (int i = i0; SUFFIX ? i > j : i < j; i += SUFFIX ? -1 : 1) fold(i);
             cur = lim;
         }
-        __syncthreads();  // the carried block is complete
-        {
-            float* dst = out + sum_off(d, j, b, h) + int64_t(r) * d.Dv;
-#pragma unroll
-            for (int uu = 0; uu < CPT; ++uu)
-                if (c0 + uu < d.Dv) dst[c0 + uu] = s_s[buf][r][q * CPT + uu];
-        }
+        // this thread's row of the carried block is its own last write
+        *reinterpret_cast<float4*>(out + sum_off(d, j, b, h) + int64_t(r) * d.Dv + c0) = s_s[buf][r];
         fold(j);  // extend the fold by segment j for the next segment's range
     }
 }
@@ -669,12 +667,12 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
         }
         case GdrOp::kComposePrefix:
         case GdrOp::kComposeSuffix: {
-            const dim3 grid(BH, (d.Dv + fold_cols(d.Dk) - 1) / fold_cols(d.Dk));
+            const dim3 grid(BH, d.Dv / kFoldCols);
             if (op == GdrOp::kComposePrefix) {
-                RMCP_GDR_DK_SWITCH((gdr_compose<DK, false><<<grid, 256, 0, s>>>(
+                RMCP_GDR_DK_SWITCH((gdr_compose<DK, false><<<grid, DK, 0, s>>>(
                     d, p.M, p.dS, d.preceding_start, p.S_in_out)));
             } else {
-                RMCP_GDR_DK_SWITCH((gdr_compose<DK, true><<<grid, 256, 0, s>>>(
+                RMCP_GDR_DK_SWITCH((gdr_compose<DK, true><<<grid, DK, 0, s>>>(
                     d, p.M, p.gamma, d.following_stop, p.dS_out_out)));
             }
             break;
