@@ -692,23 +692,27 @@ def gdr_kernel_alu_flops(w, phase):
 
 
 def gdr_kernel_bytes(w, phase):
-    """Algorithmic bytes of one launch of a gated-delta-rule call: its inputs
-    read once and its outputs written once (token tensors, gates, summaries;
-    the backward prepare writes, and the apply reads, one fp32 state per
-    64-token chunk, the tensor-core sweeps' workspace)."""
+    """Algorithmic bytes of one gated-delta-rule call on the tensor-core
+    sweeps: its inputs read once and its outputs written once (token tensors,
+    gates, summaries) plus its share of the workspace: the forward prepare
+    writes each 64-token chunk's two bf16 [64][64] factors, the apply and
+    the backward prepare read T, the backward apply reads both; the backward
+    prepare writes, and the apply reads, one fp32 state per chunk."""
     e = 4 if w.dtype == "f32" else 2
     Dk, Dv = w.Dk, w.Dv
     ntok = w.B * w.T * w.H
     nsum = w.num_segments * w.B * w.H
     st, mt = 4 * Dk * Dv, 4 * Dk * Dk
-    ckpt = (ntok // 64) * st
+    nch = ntok // 64
+    ckpt = nch * st
+    tf = nch * 64 * 64 * 2  # one bf16 factor tile a chunk
     return {
-        "gdr_forward_prepare": ntok * (e * (Dk + Dv) + 8) + nsum * (mt + st),
+        "gdr_forward_prepare": ntok * (e * (Dk + Dv) + 8) + nsum * (mt + st) + 2 * tf,
         "gdr_compose_prefix": nsum * (mt + 2 * st),
-        "gdr_forward_apply": ntok * (e * (2 * Dk + Dv) + 8 + e * Dv) + nsum * st,
-        "gdr_backward_prepare": ntok * (e * (2 * Dk + 2 * Dv) + 8 + e * Dk) + 2 * nsum * st + ckpt,
+        "gdr_forward_apply": ntok * (e * (2 * Dk + Dv) + 8 + e * Dv) + nsum * st + tf,
+        "gdr_backward_prepare": ntok * (e * (2 * Dk + 2 * Dv) + 8 + e * Dk) + 2 * nsum * st + ckpt + tf,
         "gdr_compose_suffix": nsum * (mt + 2 * st),
-        "gdr_backward_apply": ntok * (e * (2 * Dk + 2 * Dv) + 8 + e * (Dk + Dv) + 8) + nsum * st + ckpt,
+        "gdr_backward_apply": ntok * (e * (2 * Dk + 2 * Dv) + 8 + e * (Dk + Dv) + 8) + nsum * st + ckpt + 2 * tf,
     }[phase]
 
 
@@ -726,11 +730,11 @@ def gdr_step_bytes(w, tc):
 
 
 def gdr_kernel_tc_flops(w, phase):
-    """Tensor-core flops of one launch of the tensor-core sweeps: 64 x 64 x 64
-    products per 64-token chunk and head (7 in the forward prepare, 8 in the
-    apply, 8 + 7 in the backward prepare's dq and gamma walks, 16 in the
-    backward apply)."""
-    per = {"gdr_forward_prepare": 7, "gdr_forward_apply": 8, "gdr_backward_prepare": 15,
+    """Tensor-core flops of one call on the tensor-core sweeps: 64 x 64 x 64
+    products per 64-token chunk and head (K K^T and the walk's 6 in the
+    forward prepare, 7 in the apply, 7 + 6 in the backward prepare's dq and
+    gamma walks, 16 in the backward apply)."""
+    per = {"gdr_forward_prepare": 7, "gdr_forward_apply": 7, "gdr_backward_prepare": 13,
            "gdr_backward_apply": 16}.get(phase, 0)
     return (w.B * w.T * w.H // 64) * per * 2 * 64 ** 3
 
