@@ -831,10 +831,26 @@ def measure_gdr(w, args, rank, world, dev, peaks, peak_src, with_cpu):
         for ph in GDR_PHASES_FWD:
             fns[ph]()
     fe.record(stream)
+    # the same step and forward captured once as CUDA graphs and replayed
+    g_step = api.GdrStepGraph(plan, q, k, v, g, beta, dO)
+    g_fwd = api.GdrStepGraph(plan, q, k, v, g, beta)
+    gtimes = {}
+    for name, gr in (("step", g_step), ("fwd", g_fwd)):
+        for _ in range(3):
+            gr.replay()
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        for _ in range(steps):
+            gr.replay()
+        b_ev.record(stream)
+        gtimes[name] = (a_ev, b_ev)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     ms = replica_time(start.elapsed_time(end), world, dev) / steps
     fwd_ms = replica_time(fs.elapsed_time(fe), world, dev) / steps
+    g_ms = replica_time(gtimes["step"][0].elapsed_time(gtimes["step"][1]), world, dev) / steps
+    g_fwd_ms = replica_time(gtimes["fwd"][0].elapsed_time(gtimes["fwd"][1]), world, dev) / steps
+    del g_step, g_fwd
     phase_ms = {ph: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
                 for j, ph in enumerate(phases)}
     dom = max(phase_ms, key=phase_ms.get)
@@ -874,6 +890,10 @@ def measure_gdr(w, args, rank, world, dev, peaks, peak_src, with_cpu):
                           "phases_us": {ph: round(t * 1e3, 2) for ph, t in phase_ms.items()}},
         "fwd_path_roofline": {"t_roofline_us": pr["t_fwd_roofline_us"], "t_measured_us": fwd_ms * 1e3,
                               "frac": pr["t_fwd_roofline_us"] / (fwd_ms * 1e3)},
+        "graph": {"value": replica_throughput(world, tok, g_ms), "ms_per_step": g_ms,
+                  "fwd_value": replica_throughput(world, tok, g_fwd_ms), "fwd_ms_per_step": g_fwd_ms,
+                  "frac": pr["t_roofline_us"] / (g_ms * 1e3),
+                  "how": "the same calls captured once as a CUDA graph (api.GdrStepGraph) and replayed"},
         "cpu_baseline": gdr_cpu_baseline(w, inp, args.cpu_seconds) if with_cpu else None,
         "e2e": None, "gpu_launches": int(launches), "clocks": clk,
     }

@@ -332,7 +332,7 @@ class GdrPlan:
     S_in: torch.Tensor
     gamma: torch.Tensor
     dS_out: torch.Tensor
-    ws: torch.Tensor       # states saved by the backward prepare for the apply
+    ws: torch.Tensor       # the step's workspace: per-chunk factors (tensor cores) and saved states
 
 
 def make_gdr_plan(B, T, H, Dk, Dv, num_segments, chunk=16, scale=None, dtype=torch.float32,
@@ -356,13 +356,52 @@ def gdr_forward(plan: GdrPlan, q, k, v, g, beta, o=None, stream=None) -> torch.T
     return o
 
 
-def gdr_backward(plan: GdrPlan, q, k, v, g, beta, dO, stream=None):
-    """(dq, dk, dv, dg, dbeta) of sum(dO * o); needs gdr_forward on plan first."""
-    dq, dk, dv = torch.empty_like(k), torch.empty_like(k), torch.empty_like(v)
-    dg, db = torch.empty_like(g), torch.empty_like(beta)
+def gdr_backward(plan: GdrPlan, q, k, v, g, beta, dO, stream=None, grads=None):
+    """(dq, dk, dv, dg, dbeta) of sum(dO * o); needs gdr_forward on plan first.
+    grads: optional preallocated (dq, dk, dv, dg, dbeta) to write into."""
+    if grads is None:
+        grads = (torch.empty_like(k), torch.empty_like(k), torch.empty_like(v), torch.empty_like(g),
+                 torch.empty_like(beta))
+    dq, dk, dv, dg, db = grads
     C.rm_gdr_backward_prepare(plan.spec, q, k, v, g, beta, plan.S_in, dO, plan.gamma, dq, plan.ws,
                               stream)
     C.rm_gdr_compose_suffix(plan.spec, plan.M, plan.gamma, plan.dS_out, stream)
     C.rm_gdr_backward_apply(plan.spec, q, k, v, g, beta, dO, plan.dS_out, dk, dv, dg, db, plan.ws,
                             stream)
     return dq, dk, dv, dg, db
+
+
+class GdrStepGraph:
+    """One gated-delta-rule step captured as a CUDA graph: the three forward
+    calls and, given dO, the three backward calls, on fixed buffers (as
+    StepGraph does for the scalar and vector gates).  replay() returns
+    (o,) + (dq, dk, dv, dg, dbeta)."""
+
+    def __init__(self, plan: GdrPlan, q, k, v, g, beta, dO=None):
+        self.plan = plan
+        self.args = (q, k, v, g, beta)
+        self.dO = dO
+        self.o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+        self.grads = None
+        if dO is not None:
+            self.grads = (torch.empty_like(k), torch.empty_like(k), torch.empty_like(v), torch.empty_like(g),
+                          torch.empty_like(beta))
+        dev = v.device
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            self._run()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=side):
+            self._run()
+
+    def _run(self):
+        gdr_forward(self.plan, *self.args, o=self.o)
+        if self.dO is not None:
+            gdr_backward(self.plan, *self.args, self.dO, grads=self.grads)
+
+    def replay(self):
+        """Runs the captured step on the current stream."""
+        self.graph.replay()
+        return (self.o,) + (self.grads if self.grads is not None else ())

@@ -64,3 +64,43 @@ def test_graph_replay_equals_direct_calls(case):
         names = ("o", "dq", "dk", "dv", "dg", "M", "dS", "S_in", "gamma", "dS_out")
         for name, a, b in zip(names, got, ref):
             assert torch.equal(a, b), (case, seed, name)
+
+
+def test_gdr_graph_replay_equals_direct_calls():
+    """The gated delta rule's six calls (tensor-core sweeps: the forward
+    prepare's two launches, the apply, the backward's two walks and the
+    reverse walk) captured as one graph give the direct calls' results bit for
+    bit, also after new inputs are written into the captured buffers."""
+    B, T, H, D, nseg = 1, 1024, 4, 64, 4
+    gen = torch.Generator().manual_seed(11)
+
+    def inputs():
+        q = torch.randn(B, T, H, D, generator=gen)
+        k = torch.randn(B, T, H, D, generator=gen)
+        k = k / k.norm(dim=-1, keepdim=True)
+        v = torch.randn(B, T, H, D, generator=gen)
+        g = torch.nn.functional.logsigmoid(torch.randn(B, T, H, generator=gen) + 3.0)
+        beta = torch.sigmoid(torch.randn(B, T, H, generator=gen))
+        dO = torch.randn(B, T, H, D, generator=gen)
+        bf = torch.bfloat16
+        return [t.to("cuda").contiguous() for t in (q.to(bf), k.to(bf), v.to(bf), g, beta, dO.to(bf))]
+
+    def plan():
+        return api.make_gdr_plan(B, T, H, D, D, nseg, 64, 1 / math.sqrt(D), torch.bfloat16, None, "cuda")
+
+    q, k, v, g, beta, dO = inputs()
+    pg = plan()
+    assert C.rm_gdr_path(pg.spec) == 1
+    sg = api.GdrStepGraph(pg, q, k, v, g, beta, dO)
+    for it in range(2):  # the captured values, then new ones in the same buffers
+        if it == 1:
+            for dst, src in zip((q, k, v, g, beta, dO), inputs()):
+                dst.copy_(src)
+        got = list(sg.replay()) + [pg.M, pg.dS, pg.S_in, pg.gamma, pg.dS_out]
+        pd = plan()
+        o = api.gdr_forward(pd, q, k, v, g, beta)
+        want = [o] + list(api.gdr_backward(pd, q, k, v, g, beta, dO)) + [pd.M, pd.dS, pd.S_in, pd.gamma,
+                                                                           pd.dS_out]
+        torch.cuda.synchronize()
+        for a, b_ in zip(got, want):
+            assert torch.equal(a, b_)
