@@ -1046,8 +1046,7 @@ __global__ void __launch_bounds__(256, 1)
         float kg[16], Xr[16];
         {
             float kk[16], qk[16], tx[16], m[16];
-            tok16(tmem, G, TKK + 32 * G.grp, kk);
-            tok16(tmem, G, TQK + 32 * G.grp, qk);
+            tok16x2(tmem, G, TKK + 32 * G.grp, TQK + 32 * G.grp, kk, qk);
             tok16(tmem, G, TX + 32 * G.grp, tx);
             tile_row_get16(Vs, G.tau, c0, Xr);
             decay16(gs, G.tau, c0, false, m);
@@ -1068,9 +1067,8 @@ __global__ void __launch_bounds__(256, 1)
         commit_wait(&sh.mbar, mph, G.tid);
         {
             float x[16], y[16];
-            tok16(tmem, G, TD + 32 * G.grp, x);
+            tok16x2(tmem, G, TD + 32 * G.grp, TDD + 32 * G.grp, x, y);
             store_row16(smem + BA_D, G.tau, c0, x);
-            tok16(tmem, G, TDD + 32 * G.grp, y);
             store_row16(smem + BA_X, G.tau, c0, y);  // dD
         }
         if (G.tid == 0) bulk_wait_read();  // the previous dv and dk stores have read their tiles
@@ -1084,10 +1082,8 @@ __global__ void __launch_bounds__(256, 1)
         float pb = 0.f, pw = 0.f;  // this thread's parts of dbeta_t and of k_t . (E D_t)
         {
             float z[16], od[16], qk[16], de[16], kv[16], m[16], x[16];
-            tok16(tmem, G, TZ + 32 * G.grp, z);
-            tok16(tmem, G, TOD + 32 * G.grp, od);
-            tok16(tmem, G, TQK + 32 * G.grp, qk);
-            tok16(tmem, G, TDE + 32 * G.grp, de);
+            tok16x2(tmem, G, TZ + 32 * G.grp, TOD + 32 * G.grp, z, od);
+            tok16x2(tmem, G, TQK + 32 * G.grp, TDE + 32 * G.grp, qk, de);
             tile_row_get16(Ks, G.tau, c0, kv);
             decay16(gs, G.tau, c0, false, m);
             const float be = beta_s[G.tau];
@@ -1123,8 +1119,7 @@ __global__ void __launch_bounds__(256, 1)
         float pse = 0.f;  // this thread's part of <S_prev, E>
         {
             float da[16], ee[16], m[16];
-            tok16(tmem, G, TDA + 32 * G.grp, da);
-            tok16(tmem, G, TE + 32 * G.grp, ee);
+            tok16x2(tmem, G, TDA + 32 * G.grp, TE + 32 * G.grp, da, ee);
             decay16(gs, G.tau, c0, true, m);
             const float be = beta_s[G.tau];
 #pragma unroll
@@ -1158,10 +1153,8 @@ __global__ void __launch_bounds__(256, 1)
         commit_wait(&sh.mbar, mph, G.tid);
         {
             float ka[16], de[16], xs[16], os[16], qv[16], kv[16];
-            tok16(tmem, G, TK + 32 * G.grp, ka);
-            tok16(tmem, G, TDE + 32 * G.grp, de);
-            tok16(tmem, G, TXS + 32 * G.grp, xs);
-            tok16(tmem, G, TOS + 32 * G.grp, os);
+            tok16x2(tmem, G, TK + 32 * G.grp, TDE + 32 * G.grp, ka, de);
+            tok16x2(tmem, G, TXS + 32 * G.grp, TOS + 32 * G.grp, xs, os);
             tile_row_get16(Qs, G.tau, c0, qv);
             tile_row_get16(Ks, G.tau, c0, kv);
             const float wo = gs.wout[G.tau], gm = gs.win[G.tau];
