@@ -21,13 +21,15 @@
 // Every product is a tcgen05.mma of bf16 tiles in 128-byte-swizzled shared
 // memory with an fp32 accumulator in tensor memory; T is formed on the CUDA
 // cores in fp32 (the inverse of a unit lower-triangular matrix by 16 x 16
-// blocks), and the fp32 state lives in registers (16 values a thread).
+// blocks) once per chunk, for every chunk at once, and the walks read it from
+// the workspace; the fp32 state lives in registers (16 values a thread).
 //
-// Kernels, one CTA of 256 threads per (segment, row, head); thread 0 issues
-// the TMA loads and stores and the products, and the CTA steps through each
-// chunk together (two input stages):
-//   gdrtc_factor_kernel       each chunk's T and (I + A)^{-1}, every chunk at
-//                             once, into the workspace (forward prepare, first)
+// Kernels (256 threads a CTA; thread 0 issues the TMA loads and stores and
+// the products, and the CTA steps through each chunk together):
+//   gdrtc_factor_kernel       one CTA per (chunk, row, head): the chunk's T
+//                             and (I + A)^{-1} into the workspace (the forward
+//                             prepare's first launch)
+// and the walks, one CTA per (segment, row, head):
 //   gdrtc_prepare_kernel      the recurrence on [S | M] from [0 | I] with
 //                             values [V | 0]: delta_S and the transition M
 //   gdrtc_apply_kernel        o from S_in (T from the workspace)
