@@ -647,6 +647,12 @@ def run_ssd(args, rank, world, local_rank):
             "peak_source": peak_src, "phases_us": {ph: round(t * 1e3, 2) for ph, t in phase_ms.items()},
             "phase_frac_of_hbm": {ph: round(ssd_kernel_bytes(w, ph) / (phase_ms[ph] / 1e3) / 1e9
                                             / peaks["hbm_gbs"], 4) for ph in SSD_PHASES}}
+    e2e = None
+    if not args.no_e2e:
+        e2e = host_e2e(stream, dev, dict(x=x, dt=dt, A=A, B=Bm, C=Cm, D=D, dy=dy),
+                       dict(y=y, dx=dv, ddt=ddt, dA=dA, dB=dB, dC=dC, dD=dD), step,
+                       max(3, min(args.steps // 2, 20)), tok_per_step, world,
+                       "rm_ssd_map_inputs, the six calls and the two finish calls (bench.run_ssd's step)")
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = ssd_cpu_baseline(w, inp, args.cpu_seconds)
@@ -659,7 +665,7 @@ def run_ssd(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2, no flush", "kernel_path": "tcgen05"},
         "roofline": roof, "path_roofline": path, "cpu_baseline": cpu,
-        "e2e": None, "gpu_launches": int(launches), "clocks": clk,
+        "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
     }
 
 
@@ -854,6 +860,14 @@ def measure_gdr(w, args, rank, world, dev, peaks, peak_src, with_cpu):
     phase_ms = {ph: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
                 for j, ph in enumerate(phases)}
     dom = max(phase_ms, key=phase_ms.get)
+    e2e = None
+    if not args.no_e2e:
+        def gdr_step():
+            for ph in phases:
+                fns[ph]()
+        e2e = host_e2e(stream, dev, dict(q=q, k=k, v=v, g=g, beta=beta, dO=dO),
+                       dict(o=o, dq=dq, dk=dk, dv=dv, dg=dg, dbeta=db), gdr_step, steps, w.B * w.T, world,
+                       "the six rm_gdr_* calls")
     tc = C.rm_gdr_path(s) == 1
     if tc:
         # the tensor-core sweeps: bytes bound them (their flops take less time at peak)
@@ -895,7 +909,7 @@ def measure_gdr(w, args, rank, world, dev, peaks, peak_src, with_cpu):
                   "frac": pr["t_roofline_us"] / (g_ms * 1e3),
                   "how": "the same calls captured once as a CUDA graph (api.GdrStepGraph) and replayed"},
         "cpu_baseline": gdr_cpu_baseline(w, inp, args.cpu_seconds) if with_cpu else None,
-        "e2e": None, "gpu_launches": int(launches), "clocks": clk,
+        "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
     }
 
 
@@ -974,6 +988,38 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
+
+
+def host_e2e(stream, dev, dev_in, dev_out, step_fn, steps, tok_per_step, world, call):
+    """End to end through the calls with host buffers: every step copies its
+    inputs from pinned host memory into the device buffers the calls read,
+    runs the calls, and copies the outputs back into pinned host memory, all
+    on one stream and inside the timed region (no overlap between steps)."""
+    host_in = {n: t.detach().to("cpu").pin_memory() for n, t in dev_in.items()}
+    host_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in dev_out.items()}
+
+    def one():
+        for n, t in dev_in.items():
+            t.copy_(host_in[n], non_blocking=True)
+        step_fn()
+        for n, t in dev_out.items():
+            host_out[n].copy_(t, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = replica_time(a.elapsed_time(b) / steps, world, dev)
+    return {"value": replica_throughput(world, tok_per_step, e_ms), "unit": "tokens/s",
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out.values()),
+            "ms_per_step": e_ms, "steps": steps, "call": call,
+            "pipeline": "one stream: h2d, the calls, d2h, step after step"}
 
 
 def load_traffic(workload, kernel):
