@@ -136,6 +136,20 @@ def test_gdr_tc_strong_decay_saturated_writes():
     run_case(1, 512, 2, 64, 64, torch.bfloat16, nseg=4, seed=9, gshift=-1.0, bshift=3.0)
 
 
+def test_gdr_tc_many_segments_long_sequences():
+    # 32 segments of 64 tokens; sequences spanning up to 20 segments, so the
+    # folds start far back (preceding_start, following_stop) and restart
+    # their chains several times, in both directions
+    cu = [0, 5, 1300, 1301, 1990, 2048]
+    run_case(1, 2048, 2, 64, 64, torch.bfloat16, nseg=32, cu=cu, seed=12)
+
+
+def test_gdr_many_segments_generic():
+    # the same on the generic kernels (fp32, Dk = 32, Dv = 24): 64 segments of 16
+    cu = [0, 300, 301, 700, 1024]
+    run_case(1, 1024, 2, 32, 24, torch.float32, nseg=64, cu=cu, seed=13)
+
+
 def test_gdr_tc_weak_writes():
     # beta ~ 0.05: T = (I + A)^{-1} diag(beta) near 0, dbeta from dZ . X
     run_case(1, 512, 2, 64, 64, torch.bfloat16, nseg=2, seed=10, bshift=-3.0)
