@@ -739,9 +739,9 @@ def gdr_kernel_tc_flops(w, phase):
     """Tensor-core flops of one call on the tensor-core sweeps: 64 x 64 x 64
     products per 64-token chunk and head (K K^T and the walk's 6 in the
     forward prepare, 7 in the apply, 7 + 6 in the backward prepare's dq and
-    gamma walks, 16 in the backward apply)."""
+    gamma walks, 6 + 15 in the backward apply's adjoint walk and chunk pass)."""
     per = {"gdr_forward_prepare": 7, "gdr_forward_apply": 7, "gdr_backward_prepare": 13,
-           "gdr_backward_apply": 16}.get(phase, 0)
+           "gdr_backward_apply": 21}.get(phase, 0)
     return (w.B * w.T * w.H // 64) * per * 2 * 64 ** 3
 
 

@@ -476,8 +476,9 @@ rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, const void* 
  * (I + A)^-1 (bf16; they depend on k, g and beta only), which the forward
  * apply and the two backward calls read, so the forward prepare must have run
  * on the same k, g, beta and ws before them (the generic kernels do not use
- * ws in the forward).  Validation, ownership and errors as for the other
- * calls.
+ * ws in the forward); the tensor-core backward apply also keeps each chunk's
+ * state adjoint there between its two launches.  Validation, ownership and
+ * errors as for the other calls.
  *
  * rm_gdr_path: 1 when the problem's sweeps run on the tensor cores, 0 on the
  * generic kernels, -1 for a problem these calls reject.

@@ -36,7 +36,11 @@
 //   gdrtc_bwd_prepare_kernel  dq by a forward walk that saves each chunk's
 //                             incoming state, and gamma by a reverse walk of
 //                             the state adjoint (two CTA roles, one launch)
-//   gdrtc_bwd_apply_kernel    dk, dv, dbeta and dg by a reverse walk
+//   gdrtc_adjoint_kernel      the state adjoint E of each chunk by a reverse
+//                             walk from dS_out (the backward apply's first launch)
+// and, one CTA per (chunk, row, head), every chunk at once:
+//   gdrtc_chunk_grad_kernel   dk, dv, dbeta and dg of the chunk from its
+//                             saved S_prev and E (the backward apply's second)
 #include "tc_tiles.cuh"
 
 namespace rmcp {
@@ -794,9 +798,13 @@ constexpr uint32_t GA_DX = GA_QG;  // -dX over P, which dies with P^T dO
 constexpr size_t kGaSmem = GA_E + T8 + 1024;
 constexpr size_t kBwdPrepSmem = kDqSmem > kGaSmem ? kDqSmem : kGaSmem;
 
+// E0 (the segments' dS_out, or NULL for 0) starts the walk; Esave (or NULL)
+// receives each chunk's E, the adjoint of the state after the chunk, before the
+// chunk updates it; gamma (or NULL) receives E at the segment start.
 __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq, const CUtensorMap* mk,
                                            const CUtensorMap* mo, const CUtensorMap* mf,
                                            const float* __restrict__ g, const float* __restrict__ beta,
+                                           const float* __restrict__ E0, float* __restrict__ Esave,
                                            float* __restrict__ gamma, uint8_t* smem, BwdShared& sh,
                                            uint32_t tmem, const Geo& G) {
     constexpr uint32_t TX = 0, TQK = 64, TDD = 128, TE = 192;
@@ -807,8 +815,12 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
     const int64_t cb = chunk_base(d, seg, b, h);
 
     float Er[16];
+    if (E0 != nullptr) {
+        load_row16(E0 + sum_off(d, seg, b, h), G.tau, c0, Er);
+    } else {
 #pragma unroll
-    for (int e = 0; e < 16; ++e) Er[e] = 0.f;
+        for (int e = 0; e < 16; ++e) Er[e] = 0.f;
+    }
     store_row16(smem + GA_E, G.tau, c0, Er);
     auto load = [&](int c, int s) {
         const int row = b * d.T + a0 + c * kChunk;
@@ -835,6 +847,7 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
         const int t0 = a0 + c * kChunk;
         const uint32_t sq = s * GA_STAGE, sk = sq + T8, so = sq + 2 * T8, st = sq + 3 * T8;
         GateSmem& gs = sh.gsb[it & 1];
+        if (Esave != nullptr) save_row16(Esave + (cb + c) * int64_t(kD * kD), G.tau, c0, Er);
         if (G.tid == 0 && it >= 1 && it + 1 < nch) load(c - 1, s ^ 1);  // the previous chunk's products are done
         __syncthreads();
         mbar_wait(smem_u32(&sh.full[s]), (it >> 1) & 1);
@@ -891,7 +904,7 @@ __device__ __forceinline__ void gamma_walk(const Dims& d, const CUtensorMap* mq,
         }
         cta_sync_tc();
     }
-    save_row16(gamma + sum_off(d, seg, b, h), G.tau, c0, Er);
+    if (gamma != nullptr) save_row16(gamma + sum_off(d, seg, b, h), G.tau, c0, Er);
 }
 
 __global__ void __launch_bounds__(256, 2)
@@ -913,303 +926,307 @@ __global__ void __launch_bounds__(256, 2)
     if (blockIdx.z == 0)
         dq_walk(d, &mk, &mv, &mo, &mf, &mdq, g, beta, S_in, ws, smem, sh, tmem, G);
     else
-        gamma_walk(d, &mq, &mk, &mo, &mf, g, beta, gamma, smem, sh, tmem, G);
+        gamma_walk(d, &mq, &mk, &mo, &mf, g, beta, nullptr, nullptr, gamma, smem, sh, tmem, G);
     tc_fence_before();
     __syncthreads();
     if (G.warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ===========================================================================
-// backward apply: one CTA per (segment, row, head), chunks last to first,
-// E = dS_out at the segment end and S_prev of each chunk from the workspace.
-// With L = I + A, P = scale mask(Q K^T o Gam), X = V - (K o gam) S_prev and
-// D = T X as in the forward, and G = K K^T:
-//     dD  = P^T dO + (K o Gam[63]) E,   dZ = L^{-T} dD,   dv = dX = beta o dZ
-//     dA  = -strict_lower(dZ D^T),     dG = dA o beta_t o Gam
-//     dk  = scale mask(dO D^T o Gam)^T Q + (dG + dG^T) K
-//           + Gam[63] o (D E^T) - gam o (dX S_prev^T)
-//     dbeta_t = dZ_t . X_t + sum_r dA[t][r] G[t][r] Gam[t][r]
-//     E  <- scale (Q o gam)^T dO + gam_63 E - (K o gam)^T dX
-// and, through the running gate sums b_t (Gam, gam, Gam[63] and gam_63 are
-// exponentials of their differences), the gradient db_t:
-//     row sum minus column sum of M1 + M2 with M1 = P o (dO D^T), M2 = dA o A,
-//     + scale gam_t q_t . (S_prev dO_t) - gam_t k_t . (S_prev dX_t) - w_t,
-//     w_t = Gam[63][t] k_t . (E D_t), and at t = 63 + gam_63 <S_prev, E> + sum_r w_r;
-// dg_u = sum_{t >= u} db_t inside the chunk (0 where a sequence starts).
-// Shared memory (8 KB tiles): two stages of Q|K|V|dO|T|L^{-1}; K o gam,
-// K o Gam[63] (then dZ), scale Q o gam (then scale mask(dO D^T o Gam)), S, E,
-// P (then -dX), X (then dD, then dG + dG^T), D, dv and dk staging; fp32 dG
-// and M1 + M2 work arrays.
-// Tensor memory (64 columns each): K K^T then dZ; Q K^T then the dk
-// product; (K o gam) S_prev, D, then dZ D^T; dD, dO D^T, then -dX S_prev^T;
-// the E product; dO S_prev^T; D E^T.
+// backward apply, first launch: the adjoint walk of gamma_walk from dS_out,
+// saving each chunk's E (the adjoint of the state after the chunk) to the
+// workspace.  Two CTAs a SM.
 // ===========================================================================
-constexpr uint32_t BA_STAGE = 6 * T8;
-constexpr uint32_t BA_KG = 2 * BA_STAGE, BA_KC = BA_KG + T8, BA_QG = BA_KC + T8, BA_S = BA_QG + T8;
-constexpr uint32_t BA_E = BA_S + T8, BA_P = BA_E + T8, BA_X = BA_P + T8, BA_D = BA_X + T8;
-constexpr uint32_t BA_SV = BA_D + T8, BA_SK = BA_SV + T8, BA_F32 = BA_SK + T8;
-constexpr uint32_t BA_GS = BA_X;  // dG + dG^T over dD, which dies with dZ
-constexpr size_t kBwdApplySmem = BA_F32 + 2 * kD * kP * sizeof(float) + 1024;
-
-__global__ void __launch_bounds__(256, 1)
-    gdrtc_bwd_apply_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
-                           const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                           const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mf,
-                           const __grid_constant__ CUtensorMap mdk, const __grid_constant__ CUtensorMap mdv,
-                           const float* __restrict__ g, const float* __restrict__ beta,
-                           const float* __restrict__ dS_out, const float* __restrict__ ws,
-                           float* __restrict__ dg, float* __restrict__ dbeta) {
+__global__ void __launch_bounds__(256, 2)
+    gdrtc_adjoint_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                         const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mo,
+                         const __grid_constant__ CUtensorMap mf, const float* __restrict__ g,
+                         const float* __restrict__ beta, const float* __restrict__ dS_out,
+                         float* __restrict__ Esave) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    float* La = reinterpret_cast<float*>(smem + BA_F32);  // dG
-    float* Ys = La + kD * kP;                               // M1 + M2
     __shared__ BwdShared sh;
-    constexpr uint32_t TKK = 0, TQK = 64, TX = 128, TDD = 192, TE = 256, TOS = 320, TDE = 384;
-    constexpr uint32_t TZ = TKK, TK = TQK, TD = TX, TDA = TX, TOD = TDD, TXS = TDD;
-
     const Geo G = geo();
-    const int seg = blockIdx.x, b = blockIdx.y / d.H, h = blockIdx.y % d.H;
-    const int nch = d.L / kChunk;
-    const int a0 = seg * d.L;
-    const int c0 = 32 * G.grp + 16 * G.hi;
-    const int64_t cb = chunk_base(d, seg, b, h);
-    const float* ck = ws + cb * int64_t(kD * kD);
-
-    bwd_setup(sh, G, 512);
-    float Er[16];
-    load_row16(dS_out + sum_off(d, seg, b, h), G.tau, c0, Er);
-    store_row16(smem + BA_E, G.tau, c0, Er);
+    bwd_setup(sh, G, 256);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_slot;
-    auto load = [&](int c, int s) {
-        const int row = b * d.T + a0 + c * kChunk;
-        const uint32_t bar = smem_u32(&sh.full[s]);
-        uint8_t* st = smem + s * BA_STAGE;
-        mbar_expect_tx(bar, BA_STAGE);
-        tma_load_3d(smem_u32(st), &mq, 0, h / d.qdiv, row, bar);
-        tma_load_3d(smem_u32(st + T8), &mk, 0, h, row, bar);
-        tma_load_3d(smem_u32(st + 2 * T8), &mv, 0, h, row, bar);
-        tma_load_3d(smem_u32(st + 3 * T8), &mo, 0, h, row, bar);
-        tma_load_3d(smem_u32(st + 4 * T8), &mf, 0, 0, fac_row(cb + c, 0), bar);
-        tma_load_3d(smem_u32(st + 5 * T8), &mf, 0, 0, fac_row(cb + c, 1), bar);
-    };
+    gamma_walk(d, &mq, &mk, &mo, &mf, g, beta, dS_out, Esave, nullptr, smem, sh, tmem, G);
+    tc_fence_before();
+    __syncthreads();
+    if (G.warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ===========================================================================
+// backward apply, second launch: the gradients of every chunk at once, one
+// CTA per (chunk, row, head), from the chunk's S_prev (saved by the dq walk),
+// its E (saved by the adjoint walk) and its factors T and L^{-1} = (I + A)^-1.
+// With L = I + A, P = scale mask(Q K^T o Gam), X = V - (K o gam) S_prev,
+// D = T X and G = K K^T:
+//     dD  = P^T dO + (K o Gam[63]) E,   dZ = L^{-T} dD,   dv = dX = beta o dZ
+//     dA  = -strict_lower(dZ D^T),     dG = dA o beta_t o Gam
+//     dk  = DW E^T + XG S_prev^T + P2^T Q + (dG + dG^T) K,  with
+//           DW = Gam[63] o D, XG = -gam o dX, P2 = scale mask(dO D^T o Gam)
+//     dbeta_t = dZ_t . X_t + sum_r dA[t][r] G[t][r] Gam[t][r]
+// and the gradient db_t of the running gate sums: the row sum minus the
+// column sum of M1 + M2 (M1 = P o (dO D^T), M2 = dA o A), + scale gam_t
+// q_t . (S_prev dO_t) + k_t . (XG S_prev^T)_t - w_t, w_t = k_t . (DW E^T)_t,
+// and at t = 63 + gam_63 <S_prev, E> + sum_r w_r; dg_u = sum_{t >= u} db_t
+// inside the chunk (0 where a sequence starts).
+// Two CTAs a SM.  Shared memory (8 KB tiles): Q|K|V|dO|T|L^{-1} (dk staged in
+// Q and dv in V once they are dead), and seven work tiles reused by lifetime:
+//   W0 S_prev, then dG + dG^T      W1 E, then P2
+//   W2 K o gam, then dD            W3 K o Gam[63], then DW
+//   W4 P, then dZ                  W5 X, then XG          W6 D
+// with the fp32 M1 + M2 over W2|W3 from the third products on and the fp32
+// dG over W4|W5 from the fourth (rows of 64 values, the column index
+// swizzled by the row so that row and column walks avoid bank conflicts).
+// Tensor memory, four 64-column slots: Q K^T, then dD, then dZ, then dZ D^T;
+// (K o gam) S_prev, then D, then dO D^T, then XG S_prev^T; dO S_prev^T,
+// then the dk product; Q K^T again, then K K^T.
+// ===========================================================================
+constexpr uint32_t CG_Q = 0, CG_K = T8, CG_V = 2 * T8, CG_O = 3 * T8, CG_T = 4 * T8, CG_L = 5 * T8;
+constexpr uint32_t CG_W0 = 6 * T8, CG_W1 = 7 * T8, CG_W2 = 8 * T8, CG_W3 = 9 * T8;
+constexpr uint32_t CG_W4 = 10 * T8, CG_W5 = 11 * T8, CG_W6 = 12 * T8;
+constexpr size_t kChunkGradSmem = 13 * T8 + 1024;
+
+// element (t, c) of a [64][64] fp32 array of unpadded rows, column swizzled by the row
+__device__ __forceinline__ int swz(int t, int c) { return t * kD + (c ^ (t & 31)); }
+
+__global__ void __launch_bounds__(256, 2)
+    gdrtc_chunk_grad_kernel(const Dims d, const __grid_constant__ CUtensorMap mq,
+                            const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                            const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mf,
+                            const __grid_constant__ CUtensorMap mdk, const __grid_constant__ CUtensorMap mdv,
+                            const float* __restrict__ g, const float* __restrict__ beta,
+                            const float* __restrict__ Ssave, const float* __restrict__ Esave,
+                            float* __restrict__ dg, float* __restrict__ dbeta) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    float* Mm = reinterpret_cast<float*>(smem + CG_W2);  // M1 + M2
+    float* dG = reinterpret_cast<float*>(smem + CG_W4);
+    __shared__ BwdShared sh;
+    constexpr uint32_t SA = 0, SB = 64, SC = 128, SD = 192;
+    GateSmem& gs = sh.gsb[0];
+    const float* beta_s = sh.bsb[0];
+
+    const Geo G = geo();
+    const int b = blockIdx.y / d.H, h = blockIdx.y % d.H;
+    const int t0 = blockIdx.x * kChunk;
+    const int seg = t0 / d.L, c = (t0 % d.L) / kChunk;
+    const int64_t ci = chunk_base(d, seg, b, h) + c;
+    const int c0 = 32 * G.grp + 16 * G.hi;
+
+    // every load of the chunk in flight at once: the TMA tiles (thread 0, as
+    // soon as its barrier exists), the fp32 S_prev and E rows, the gates
     if (G.tid == 0) {
-        load(nch - 1, 0);
-        if (nch > 1) load(nch - 2, 1);
+        mbar_init(smem_u32(&sh.full[0]), 1);
+        mbar_init(smem_u32(&sh.mbar), 1);
+        mbar_fence_init();
+        const uint32_t bar = smem_u32(&sh.full[0]);
+        const int row = b * d.T + t0;
+        mbar_expect_tx(bar, 6 * T8);
+        tma_load_3d(smem_u32(smem + CG_Q), &mq, 0, h / d.qdiv, row, bar);
+        tma_load_3d(smem_u32(smem + CG_K), &mk, 0, h, row, bar);
+        tma_load_3d(smem_u32(smem + CG_V), &mv, 0, h, row, bar);
+        tma_load_3d(smem_u32(smem + CG_O), &mo, 0, h, row, bar);
+        tma_load_3d(smem_u32(smem + CG_T), &mf, 0, 0, fac_row(ci, 0), bar);
+        tma_load_3d(smem_u32(smem + CG_L), &mf, 0, 0, fac_row(ci, 1), bar);
     }
+    if (G.warp == 0) tmem_alloc(smem_u32(&sh.tmem_slot), 256);
+    const GateFetch gf = gates_fetch(d, g, beta, b, h, t0, G);
+    float pse = 0.f;  // this thread's part of <S_prev, E>
+    {
+        float Sr[16], Er[16];
+        load_row16(Ssave + ci * int64_t(kD * kD), G.tau, c0, Sr);
+        load_row16(Esave + ci * int64_t(kD * kD), G.tau, c0, Er);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pse = fmaf(Sr[e], Er[e], pse);
+        store_row16(smem + CG_W0, G.tau, c0, Sr);
+        store_row16(smem + CG_W1, G.tau, c0, Er);
+    }
+    gates_commit(gf, gs, sh.bsb[0], G);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_slot;
+    mbar_wait(smem_u32(&sh.full[0]), 0);
+    tc_fence_after();
     const uint32_t sb0 = smem_u32(smem);
     const uint64_t DK = sdesc(sb0, 16, 1024), DM = sdesc(sb0, T8, 1024);
-    GateFetch gf = gates_fetch(d, g, beta, b, h, a0 + (nch - 1) * kChunk, G);
-    gates_commit(gf, sh.gsb[0], sh.bsb[0], G);
-    if (nch > 1) gf = gates_fetch(d, g, beta, b, h, a0 + (nch - 2) * kChunk, G);
-    float Sn[16];  // S_prev of the chunk about to start, loaded during the one before
-    load_row16(ck + int64_t(nch - 1) * kD * kD, G.tau, c0, Sn);
     uint32_t mph = 0;
-    for (int it = 0; it < nch; ++it) {
-        const int c = nch - 1 - it, s = it & 1;
-        const int t0 = a0 + c * kChunk;
-        uint8_t* Qs = smem + s * BA_STAGE;
-        uint8_t* Ks = Qs + T8;
-        uint8_t* Vs = Ks + T8;
-        const uint32_t sq = s * BA_STAGE, sk = sq + T8, so = sq + 3 * T8, st = sq + 4 * T8, sl = sq + 5 * T8;
-        float Sr[16];
+    if (G.tid == 0) mma_kk(tmem + SA, desc_plus(DK, CG_Q), desc_plus(DK, CG_K), 0);  // Q K^T
+    rows_scaled(smem + CG_K, smem + CG_W2, gs.win, 1.f, G.tid);   // K o gam
+    rows_scaled(smem + CG_K, smem + CG_W3, gs.wout, 1.f, G.tid);  // K o Gam[63]
+    cta_sync_tc();
+    if (G.tid == 0) {
+        mma_km(tmem + SB, desc_plus(DK, CG_W2), desc_plus(DM, CG_W0), 0);  // (K o gam) S_prev
+        mma_kk(tmem + SC, desc_plus(DK, CG_O), desc_plus(DK, CG_W0), 0);   // dO S_prev^T
+    }
+    commit_wait(&sh.mbar, mph, G.tid);
+    float Xr[16], pq = 0.f;  // X (fp32) and this thread's part of q_t . (dO S_prev^T)_t
+    {
+        float qk[16], tx[16], os[16], qv[16], m[16];
+        tok16x2(tmem, G, SA + 32 * G.grp, SB + 32 * G.grp, qk, tx);
+        tok16(tmem, G, SC + 32 * G.grp, os);
+        tile_row_get16(smem + CG_V, G.tau, c0, Xr);
+        tile_row_get16(smem + CG_Q, G.tau, c0, qv);
+        decay16(gs, G.tau, c0, false, m);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) Sr[e] = Sn[e];
-        store_row16(smem + BA_S, G.tau, c0, Sr);
-        GateSmem& gs = sh.gsb[it & 1];
-        const float* beta_s = sh.bsb[it & 1];
-        if (G.tid == 0 && it >= 1 && it + 1 < nch) load(c - 1, s ^ 1);  // the previous chunk's products are done
-        __syncthreads();
-        mbar_wait(smem_u32(&sh.full[s]), (it >> 1) & 1);
-        tc_fence_after();
-        if (G.tid == 0) {  // K K^T and Q K^T
-            mma_kk(tmem + TKK, desc_plus(DK, sk), desc_plus(DK, sk), 0);
-            mma_kk(tmem + TQK, desc_plus(DK, sq), desc_plus(DK, sk), 0);
+        for (int e = 0; e < 16; ++e) {
+            qk[e] *= d.scale * m[e];
+            Xr[e] -= tx[e];
+            pq = fmaf(qv[e], os[e], pq);
         }
-        rows_scaled(Ks, smem + BA_KG, gs.win, 1.f, G.tid);      // K o gam
-        rows_scaled(Ks, smem + BA_KC, gs.wout, 1.f, G.tid);     // K o Gam[63]
-        rows_scaled(Qs, smem + BA_QG, gs.win, d.scale, G.tid);  // scale Q o gam
-        cta_sync_tc();
-        if (G.tid == 0) {
-            mma_km(tmem + TX, desc_plus(DK, BA_KG), desc_plus(DM, BA_S), 0);   // (K o gam) S_prev
-            mma_km(tmem + TDD, desc_plus(DK, BA_KC), desc_plus(DM, BA_E), 0);  // (K o Gam[63]) E
-            mma_mm(tmem + TE, desc_plus(DM, BA_QG), desc_plus(DM, so), 0);     // (scale Q o gam)^T dO
-            mma_kk(tmem + TOS, desc_plus(DK, so), desc_plus(DK, BA_S), 0);     // dO S_prev^T
-        }
-        if (it + 1 < nch) {  // the next chunk's gate tables, while the products run
-            gates_commit(gf, sh.gsb[(it + 1) & 1], sh.bsb[(it + 1) & 1], G);
-            if (it + 2 < nch) gf = gates_fetch(d, g, beta, b, h, t0 - 2 * kChunk, G);
-            load_row16(ck + int64_t(c - 1) * kD * kD, G.tau, c0, Sn);  // the next chunk's S_prev
-        }
-        commit_wait(&sh.mbar, mph, G.tid);
-        // kg = G o Gam (strict, within a sequence) and X stay in registers
-        float kg[16], Xr[16];
-        {
-            float kk[16], qk[16], tx[16], m[16];
-            tok16x2(tmem, G, TKK + 32 * G.grp, TQK + 32 * G.grp, kk, qk);
-            tok16(tmem, G, TX + 32 * G.grp, tx);
-            tile_row_get16(Vs, G.tau, c0, Xr);
-            decay16(gs, G.tau, c0, false, m);
+        store_row16(smem + CG_W4, G.tau, c0, qk);  // P
+        store_row16(smem + CG_W5, G.tau, c0, Xr);  // X
+    }
+    cta_sync_tc();
+    if (G.tid == 0) {
+        mma_km(tmem + SA, desc_plus(DK, CG_W3), desc_plus(DM, CG_W1), 0);  // (K o Gam[63]) E
+        mma_mm(tmem + SA, desc_plus(DM, CG_W4), desc_plus(DM, CG_O), 1);   //   + P^T dO = dD
+        mma_km(tmem + SB, desc_plus(DK, CG_T), desc_plus(DM, CG_W5), 0);   // D = T X
+    }
+    commit_wait(&sh.mbar, mph, G.tid);
+    {
+        float x[16], y[16];
+        tok16x2(tmem, G, SA + 32 * G.grp, SB + 32 * G.grp, x, y);
+        store_row16(smem + CG_W2, G.tau, c0, x);  // dD
+        store_row16(smem + CG_W6, G.tau, c0, y);  // D
+        const float wo = gs.wout[G.tau];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                kg[e] = c0 + e < G.tau ? kk[e] * m[e] : 0.f;
-                qk[e] *= d.scale * m[e];
-                Xr[e] -= tx[e];
-            }
-            store_row16(smem + BA_P, G.tau, c0, qk);
-            store_row16(smem + BA_X, G.tau, c0, Xr);
-        }
-        cta_sync_tc();
-        if (G.tid == 0) {
-            mma_mm(tmem + TDD, desc_plus(DM, BA_P), desc_plus(DM, so), 1);  // + P^T dO
-            mma_km(tmem + TD, desc_plus(DK, st), desc_plus(DM, BA_X), 0);   // D = T X
-        }
-        commit_wait(&sh.mbar, mph, G.tid);
-        {
-            float x[16], y[16];
-            tok16x2(tmem, G, TD + 32 * G.grp, TDD + 32 * G.grp, x, y);
-            store_row16(smem + BA_D, G.tau, c0, x);
-            store_row16(smem + BA_X, G.tau, c0, y);  // dD
-        }
-        if (G.tid == 0) bulk_wait_read();  // the previous dv and dk stores have read their tiles
-        cta_sync_tc();
-        if (G.tid == 0) {
-            mma_mm(tmem + TZ, desc_plus(DM, sl), desc_plus(DM, BA_X), 0);     // dZ = L^{-T} dD
-            mma_kk(tmem + TOD, desc_plus(DK, so), desc_plus(DK, BA_D), 0);    // dO D^T
-            mma_kk(tmem + TDE, desc_plus(DK, BA_D), desc_plus(DK, BA_E), 0);  // D E^T
-        }
-        commit_wait(&sh.mbar, mph, G.tid);
-        float pb = 0.f, pw = 0.f;  // this thread's parts of dbeta_t and of k_t . (E D_t)
-        {
-            float z[16], od[16], qk[16], de[16], kv[16], m[16], x[16];
-            tok16x2(tmem, G, TZ + 32 * G.grp, TOD + 32 * G.grp, z, od);
-            tok16x2(tmem, G, TQK + 32 * G.grp, TDE + 32 * G.grp, qk, de);
-            tile_row_get16(Ks, G.tau, c0, kv);
-            decay16(gs, G.tau, c0, false, m);
-            const float be = beta_s[G.tau];
+        for (int e = 0; e < 16; ++e) y[e] *= wo;
+        store_row16(smem + CG_W3, G.tau, c0, y);  // DW = Gam[63] o D
+    }
+    cta_sync_tc();
+    if (G.tid == 0) {
+        mma_mm(tmem + SA, desc_plus(DM, CG_L), desc_plus(DM, CG_W2), 0);   // dZ = L^{-T} dD
+        mma_kk(tmem + SB, desc_plus(DK, CG_O), desc_plus(DK, CG_W6), 0);   // dO D^T
+        mma_kk(tmem + SC, desc_plus(DK, CG_W3), desc_plus(DK, CG_W1), 0);  // DW E^T (the dk product)
+        mma_kk(tmem + SD, desc_plus(DK, CG_Q), desc_plus(DK, CG_K), 0);    // Q K^T again
+    }
+    commit_wait(&sh.mbar, mph, G.tid);
+    float pb = 0.f, pw = 0.f;  // this thread's parts of dbeta_t and of w_t
+    {
+        float z[16], od[16], qk[16], kw[16], kv[16], m[16], x[16];
+        tok16x2(tmem, G, SA + 32 * G.grp, SB + 32 * G.grp, z, od);
+        tok16x2(tmem, G, SC + 32 * G.grp, SD + 32 * G.grp, kw, qk);
+        tile_row_get16(smem + CG_K, G.tau, c0, kv);
+        decay16(gs, G.tau, c0, false, m);
+        const float be = beta_s[G.tau], gm = gs.win[G.tau];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                pb = fmaf(z[e], Xr[e], pb);
-                pw = fmaf(kv[e], de[e], pw);
-                x[e] = be * z[e];
-            }
-            store_row16(smem + BA_KC, G.tau, c0, z);  // dZ
-            store_row16(smem + BA_SV, G.tau, c0, x);  // dv = dX
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] = -x[e];
-            store_row16(smem + BA_P, G.tau, c0, x);   // -dX
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float p2 = d.scale * m[e] * od[e];
-                Ys[G.tau * kP + c0 + e] = p2 * qk[e];  // M1 = P o (dO D^T)
-                od[e] = p2;
-            }
-            store_row16(smem + BA_QG, G.tau, c0, od);  // scale mask(dO D^T o Gam)
+        for (int e = 0; e < 16; ++e) {
+            pb = fmaf(z[e], Xr[e], pb);
+            pw = fmaf(kv[e], kw[e], pw);
+            x[e] = be * z[e];
         }
-        cta_sync_tc();
-        if (G.tid == 0) {
-            tma_store_3d(&mdv, smem_u32(smem + BA_SV), 0, h, b * d.T + t0);
-            bulk_commit();
-            mma_mm(tmem + TE, desc_plus(DM, BA_KG), desc_plus(DM, BA_P), 1);   // - (K o gam)^T dX
-            mma_kk(tmem + TDA, desc_plus(DK, BA_KC), desc_plus(DK, BA_D), 0);  // dZ D^T
-            mma_kk(tmem + TXS, desc_plus(DK, BA_P), desc_plus(DK, BA_S), 0);   // -dX S_prev^T
-            mma_mm(tmem + TK, desc_plus(DM, BA_QG), desc_plus(DM, sq), 0);     // scale mask(dO D^T o Gam)^T Q
-        }
-        commit_wait(&sh.mbar, mph, G.tid);
-        float pse = 0.f;  // this thread's part of <S_prev, E>
-        {
-            float da[16], ee[16], m[16];
-            tok16x2(tmem, G, TDA + 32 * G.grp, TE + 32 * G.grp, da, ee);
-            decay16(gs, G.tau, c0, true, m);
-            const float be = beta_s[G.tau];
+        store_row16(smem + CG_W4, G.tau, c0, z);  // dZ
+        store_row16(smem + CG_V, G.tau, c0, x);   // dv = dX, staged over V
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int r = c0 + e;
-                const float a = r < G.tau ? -da[e] : 0.f;  // dA
-                pb = fmaf(a, kg[e], pb);
-                Ys[G.tau * kP + r] += a * be * kg[e];  // M2 = dA o A
-                La[G.tau * kP + r] = a * be * m[e];    // dG
-                pse = fmaf(Sr[e], Er[e], pse);
-                Er[e] = fmaf(gs.W, Er[e], ee[e]);
-            }
-            store_row16(smem + BA_E, G.tau, c0, Er);
-        }
-        __syncthreads();
-        {
-            float x[16];
+        for (int e = 0; e < 16; ++e) x[e] *= -gm;
+        store_row16(smem + CG_W5, G.tau, c0, x);  // XG = -gam o dX
 #pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] = La[G.tau * kP + c0 + e] + La[(c0 + e) * kP + G.tau];
-            store_row16(smem + BA_GS, G.tau, c0, x);  // dG + dG^T
-            const int t = G.tid >> 2, part = G.tid & 3;
-            float rs = 0.f;
+        for (int e = 0; e < 16; ++e) {
+            const float p2 = d.scale * m[e] * od[e];
+            Mm[swz(G.tau, c0 + e)] = p2 * qk[e];  // M1 = P o (dO D^T)
+            od[e] = p2;
+        }
+        store_row16(smem + CG_W1, G.tau, c0, od);  // P2 = scale mask(dO D^T o Gam)
+    }
+    cta_sync_tc();
+    if (G.tid == 0) {
+        tma_store_3d(&mdv, smem_u32(smem + CG_V), 0, h, b * d.T + t0);
+        bulk_commit();
+        mma_kk(tmem + SA, desc_plus(DK, CG_W4), desc_plus(DK, CG_W6), 0);  // dZ D^T
+        mma_kk(tmem + SB, desc_plus(DK, CG_W5), desc_plus(DK, CG_W0), 0);  // XG S_prev^T
+        mma_kk(tmem + SC, desc_plus(DK, CG_W5), desc_plus(DK, CG_W0), 1);  // dk += XG S_prev^T
+        mma_mm(tmem + SC, desc_plus(DM, CG_W1), desc_plus(DM, CG_Q), 1);   // dk += P2^T Q
+        mma_kk(tmem + SD, desc_plus(DK, CG_K), desc_plus(DK, CG_K), 0);    // K K^T
+    }
+    commit_wait(&sh.mbar, mph, G.tid);
+    float pk = 0.f;  // this thread's part of k_t . (XG S_prev^T)_t
+    {
+        float da[16], kk[16], xs[16], kv[16], m[16];
+        tok16x2(tmem, G, SA + 32 * G.grp, SD + 32 * G.grp, da, kk);
+        tok16(tmem, G, SB + 32 * G.grp, xs);
+        tile_row_get16(smem + CG_K, G.tau, c0, kv);
+        decay16(gs, G.tau, c0, true, m);
+        const float be = beta_s[G.tau];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) rs += Ys[t * kP + 16 * part + e] - Ys[(16 * part + e) * kP + t];
-            rs += __shfl_xor_sync(kFull, rs, 1);
-            rs += __shfl_xor_sync(kFull, rs, 2);
-            if (part == 0) sh.dbm[t] = rs;
+        for (int e = 0; e < 16; ++e) {
+            const int r = c0 + e;
+            const float a = r < G.tau ? -da[e] : 0.f;  // dA
+            const float kg = kk[e] * m[e];           // G o Gam, strictly lower within a sequence
+            pb = fmaf(a, kg, pb);
+            Mm[swz(G.tau, r)] += a * be * kg;        // M2 = dA o A
+            dG[swz(G.tau, r)] = a * be * m[e];
+            pk = fmaf(kv[e], xs[e], pk);
         }
-        cta_sync_tc();
-        if (G.tid == 0) mma_km(tmem + TK, desc_plus(DK, BA_GS), desc_plus(DM, sk), 1);  // + (dG + dG^T) K
-        commit_wait(&sh.mbar, mph, G.tid);
-        {
-            float ka[16], de[16], xs[16], os[16], qv[16], kv[16];
-            tok16x2(tmem, G, TK + 32 * G.grp, TDE + 32 * G.grp, ka, de);
-            tok16x2(tmem, G, TXS + 32 * G.grp, TOS + 32 * G.grp, xs, os);
-            tile_row_get16(Qs, G.tau, c0, qv);
-            tile_row_get16(Ks, G.tau, c0, kv);
-            const float wo = gs.wout[G.tau], gm = gs.win[G.tau];
-            float pq = 0.f, pk = 0.f;
+    }
+    __syncthreads();
+    {
+        float x[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                ka[e] += wo * de[e] + gm * xs[e];
-                pq = fmaf(qv[e], os[e], pq);
-                pk = fmaf(kv[e], xs[e], pk);
-            }
-            store_row16(smem + BA_SK, G.tau, c0, ka);
-            float rw = wo * pw;
-            float rdb = d.scale * gm * pq + gm * pk - rw;
-            rdb += __shfl_xor_sync(kFull, rdb, 16);
-            rw += __shfl_xor_sync(kFull, rw, 16);
-            pb += __shfl_xor_sync(kFull, pb, 16);
-            if (!G.hi) {
-                sh.red[0][G.grp][G.tau] = rdb;
-                sh.red[1][G.grp][G.tau] = rw;
-                sh.red[2][G.grp][G.tau] = pb;
-            }
-            pse = warp_sum(pse);
-            if (G.lane == 0) sh.red_se[G.warp] = pse;
-        }
-        cta_sync_tc();
-        if (G.tid == 0) {
-            tma_store_3d(&mdk, smem_u32(smem + BA_SK), 0, h, b * d.T + t0);
-            bulk_commit();
-        }
-        if (G.warp == 0) {  // tokens 2 lane and 2 lane + 1: db, the in-chunk suffix sums, dbeta
-            const int u0 = 2 * G.lane, u1 = u0 + 1;
-            float db0 = sh.red[0][0][u0] + sh.red[0][1][u0] + sh.dbm[u0];
-            float db1 = sh.red[0][0][u1] + sh.red[0][1][u1] + sh.dbm[u1];
-            const float wsum = warp_sum(sh.red[1][0][u0] + sh.red[1][1][u0] + sh.red[1][0][u1] + sh.red[1][1][u1]);
-            const float se = warp_sum(G.lane < 8 ? sh.red_se[G.lane] : 0.f);
-            if (u1 == kChunk - 1) db1 += gs.W * se + wsum;
-            float suf = db0 + db1;  // inclusive suffix sum over lanes >= lane
+        for (int e = 0; e < 16; ++e) x[e] = dG[swz(G.tau, c0 + e)] + dG[swz(c0 + e, G.tau)];
+        store_row16(smem + CG_W0, G.tau, c0, x);  // dG + dG^T
+        const int t = G.tid >> 2, part = G.tid & 3;
+        float rs = 0.f;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float x = __shfl_down_sync(kFull, suf, o);
-                if (G.lane + o < 32) suf += x;
-            }
-            const int ta = t0 + u0, tb = t0 + u1;
-            dg[g_off(d, b, ta, h)] = starts_sequence(d.seq_idx, ta) ? 0.f : suf;
-            dg[g_off(d, b, tb, h)] = starts_sequence(d.seq_idx, tb) ? 0.f : suf - db0;
-            dbeta[g_off(d, b, ta, h)] = sh.red[2][0][u0] + sh.red[2][1][u0];
-            dbeta[g_off(d, b, tb, h)] = sh.red[2][0][u1] + sh.red[2][1][u1];
+        for (int e = 0; e < 16; ++e) rs += Mm[swz(t, 16 * part + e)] - Mm[swz(16 * part + e, t)];
+        rs += __shfl_xor_sync(kFull, rs, 1);
+        rs += __shfl_xor_sync(kFull, rs, 2);
+        if (part == 0) sh.dbm[t] = rs;
+    }
+    cta_sync_tc();
+    if (G.tid == 0) mma_km(tmem + SC, desc_plus(DK, CG_W0), desc_plus(DM, CG_K), 1);  // dk += (dG + dG^T) K
+    commit_wait(&sh.mbar, mph, G.tid);
+    {
+        float ka[16];
+        tok16(tmem, G, SC + 32 * G.grp, ka);
+        store_row16(smem + CG_Q, G.tau, c0, ka);  // dk, staged over Q
+        const float gm = gs.win[G.tau];
+        float rw = pw;
+        float rdb = d.scale * gm * pq + pk - rw;
+        rdb += __shfl_xor_sync(kFull, rdb, 16);
+        rw += __shfl_xor_sync(kFull, rw, 16);
+        pb += __shfl_xor_sync(kFull, pb, 16);
+        if (!G.hi) {
+            sh.red[0][G.grp][G.tau] = rdb;
+            sh.red[1][G.grp][G.tau] = rw;
+            sh.red[2][G.grp][G.tau] = pb;
         }
+        pse = warp_sum(pse);
+        if (G.lane == 0) sh.red_se[G.warp] = pse;
+    }
+    cta_sync_tc();
+    if (G.tid == 0) {
+        tma_store_3d(&mdk, smem_u32(smem + CG_Q), 0, h, b * d.T + t0);
+        bulk_commit();
+    }
+    if (G.warp == 0) {  // tokens 2 lane and 2 lane + 1: db, the in-chunk suffix sums, dbeta
+        const int u0 = 2 * G.lane, u1 = u0 + 1;
+        float db0 = sh.red[0][0][u0] + sh.red[0][1][u0] + sh.dbm[u0];
+        float db1 = sh.red[0][0][u1] + sh.red[0][1][u1] + sh.dbm[u1];
+        const float wsum = warp_sum(sh.red[1][0][u0] + sh.red[1][1][u0] + sh.red[1][0][u1] + sh.red[1][1][u1]);
+        const float se = warp_sum(G.lane < 8 ? sh.red_se[G.lane] : 0.f);
+        if (u1 == kChunk - 1) db1 += gs.W * se + wsum;
+        float suf = db0 + db1;  // inclusive suffix sum over lanes >= lane
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float x = __shfl_down_sync(kFull, suf, o);
+            if (G.lane + o < 32) suf += x;
+        }
+        const int ta = t0 + u0, tb = t0 + u1;
+        dg[g_off(d, b, ta, h)] = starts_sequence(d.seq_idx, ta) ? 0.f : suf;
+        dg[g_off(d, b, tb, h)] = starts_sequence(d.seq_idx, tb) ? 0.f : suf - db0;
+        dbeta[g_off(d, b, ta, h)] = sh.red[2][0][u0] + sh.red[2][1][u0];
+        dbeta[g_off(d, b, tb, h)] = sh.red[2][0][u1] + sh.red[2][1][u1];
     }
     if (G.tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (G.warp == 0) tmem_dealloc(tmem, 512);
+    if (G.warp == 0) tmem_dealloc(tmem, 256);
 }
 
 __global__ void read_flag_kernel(int* out, int clear) {
@@ -1265,12 +1282,20 @@ rm_status launch_gdrtc(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
         fn<<<dim3(d.nseg, d.B * d.H, 2), 256, kBwdPrepSmem, s>>>(d, mq, mk, mv, mo, mf, mx, p.g, p.beta, p.S_in,
                                                                 p.gamma_out, p.ws);
     } else if (op == GdrOp::kBackwardApply) {
+        // the adjoint walk saves each chunk's E after the states and the factors,
+        // then the gradients of every chunk at once
         if (!make_map(&mo, p.dO, d, kD) || !make_map(&mx, p.dk, d, kD) || !make_map(&my, p.dv, d, kD))
             return RM_ERR_CUDA;
-        auto fn = gdrtc_bwd_apply_kernel;
-        if (!set_smem(fn, kBwdApplySmem)) return RM_ERR_CUDA;
-        fn<<<grid, 256, kBwdApplySmem, s>>>(d, mq, mk, mv, mo, mf, mx, my, p.g, p.beta, p.dS_out, p.ws, p.dg,
-                                            p.dbeta);
+        float* Esave = p.ws + 2 * nchunks * kD * kD;
+        auto fa = gdrtc_adjoint_kernel;
+        if (!set_smem(fa, kGaSmem)) return RM_ERR_CUDA;
+        fa<<<grid, 256, kGaSmem, s>>>(d, mq, mk, mo, mf, p.g, p.beta, p.dS_out, Esave);
+        if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+        note_launch(1);
+        auto fc = gdrtc_chunk_grad_kernel;
+        if (!set_smem(fc, kChunkGradSmem)) return RM_ERR_CUDA;
+        fc<<<dim3(d.T / kChunk, d.B * d.H), 256, kChunkGradSmem, s>>>(d, mq, mk, mv, mo, mf, mx, my, p.g, p.beta,
+                                                                     p.ws, Esave, p.dg, p.dbeta);
     } else {
         return RM_ERR_INVALID_ARG;
     }
