@@ -488,7 +488,7 @@ def run_ours(args, rank, world, local_rank):
                                      with_e2e=False, with_cpu=False)
             subs[name] = {key: r[key] for key in ("value", "fwd_value", "unit", "mode", "ms_per_step",
                                                  "fwd_ms_per_step", "dtype", "config", "roofline",
-                                                 "path_roofline", "fwd_path_roofline", "graph",
+                                                 "path_roofline", "fwd_path_roofline", "graph", "e2e",
                                                  "gpu_launches", "clocks") if key in r}
         line["workloads"] = subs
         line["gpu_launches"] = head["gpu_launches"]
