@@ -181,3 +181,24 @@ def test_gdr_tc_full_size_sampled_heads():
     ref["M"], ref["dS"] = oracle.gdr_forward_prepare(k, v, g, beta, seg)
     ref["S_in"] = oracle.gdr_compose_prefix(ref["M"], ref["dS"])
     compare(gpu, ref, tol_for(w.torch_dtype), ("o", "dq", "dk", "dv", "dg", "dbeta", "M", "dS", "S_in"))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_gdr_tc_random_shapes(seed):
+    """Seeded random problems on the tensor-core sweeps: rows, heads, segment
+    count and length (multiples of 64), packed sequences (one row) with
+    starts anywhere, shared query rows, gate and write-strength shifts."""
+    rng = np.random.default_rng(100 + seed)
+    nseg = int(rng.choice([1, 2, 4, 8]))
+    L = 64 * int(rng.integers(1, 4))
+    T = nseg * L
+    packed = bool(rng.integers(0, 2))
+    B = 1 if packed else int(rng.integers(1, 3))
+    H = int(rng.choice([1, 2, 4]))
+    qh = int(rng.choice([0, 1])) if H > 1 else 0
+    cu = None
+    if packed:
+        cuts = sorted(set(int(x) for x in rng.integers(1, T, size=int(rng.integers(1, 6)))))
+        cu = [0] + cuts + [T]
+    run_case(B, T, H, 64, 64, torch.bfloat16, nseg=nseg, cu=cu, qh=qh, seed=200 + seed,
+             gshift=float(rng.uniform(-1.0, 4.0)), bshift=float(rng.uniform(-2.0, 2.0)))
