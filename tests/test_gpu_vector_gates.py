@@ -240,3 +240,24 @@ def test_vector_gates_tc_step_host_pipeline():
     for i in range(2):
         for n in ref:
             assert torch.equal(outs[i][n], ref[n]), (i, n)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_vector_gates_tc_random_shapes(seed):
+    """Seeded random problems on the tensor-core path: rows, heads, segment
+    count and length (multiples of 64), packed sequences (one row) with
+    starts anywhere, shared query rows, gate shifts from strong to weak decay
+    (so that factored and directly taken chunks mix)."""
+    rng = np.random.default_rng(300 + seed)
+    nseg = int(rng.choice([1, 2, 4]))
+    L = 64 * int(rng.integers(1, 4))
+    T = nseg * L
+    packed = bool(rng.integers(0, 2))
+    B = 1 if packed else int(rng.integers(1, 3))
+    H = int(rng.choice([1, 2, 4]))
+    qh = int(rng.choice([0, 1])) if H > 1 else 0
+    cu = None
+    if packed:
+        cuts = sorted(set(int(x) for x in rng.integers(1, T, size=int(rng.integers(1, 6)))))
+        cu = [0] + cuts + [T]
+    run_case(B, T, H, nseg=nseg, cu=cu, qh=qh, seed=400 + seed, shift=float(rng.uniform(-1.0, 4.0)), **TC)
