@@ -33,8 +33,14 @@
  *     legacy default stream).  Outputs are fully overwritten.
  *   - All validation happens on the host before anything is launched.  On a
  *     non-OK status nothing was enqueued; rm_cp_last_error() returns a
- *     thread-local description.  Launch failures map to RM_ERR_CUDA.  Kernels
- *     contain no traps and no inter-block waits.
+ *     thread-local description.  Launch failures map to RM_ERR_CUDA, and the
+ *     description names the CUDA error of the launch that failed.  A compute
+ *     call first makes the current device's primary context current on the
+ *     calling thread (a thread that has made no CUDA call yet may have none)
+ *     and clears a non-sticky CUDA error that an earlier runtime call left
+ *     pending on that thread (cudaGetLastError is per thread), so that only
+ *     its own launches decide its status.  Kernels contain no traps and no
+ *     inter-block waits.
  *   - Calls are thread-safe; concurrent calls on different streams may not
  *     share output buffers.
  */

@@ -11,8 +11,10 @@ Layers:
 from . import _capi  # noqa: F401
 from ._capi import RmCpError, ProblemSpec, load  # noqa: F401
 from .api import (Plan, make_plan, plan_like, forward, backward,  # noqa: F401
-                  chunkwise_gla, ChunkwiseGatedLinearAttention)
+                  chunkwise_gla, ChunkwiseGatedLinearAttention, GdrPlan, make_gdr_plan,
+                  gdr_forward, gdr_backward, gated_delta_rule, GatedDeltaRule)
 from .build import build as build_library  # noqa: F401
 
 __all__ = ["RmCpError", "ProblemSpec", "load", "Plan", "make_plan", "plan_like", "forward",
-           "backward", "chunkwise_gla", "ChunkwiseGatedLinearAttention", "build_library"]
+           "backward", "chunkwise_gla", "ChunkwiseGatedLinearAttention", "GdrPlan", "make_gdr_plan",
+           "gdr_forward", "gdr_backward", "gated_delta_rule", "GatedDeltaRule", "build_library"]

@@ -371,6 +371,43 @@ def gdr_backward(plan: GdrPlan, q, k, v, g, beta, dO, stream=None, grads=None):
     return dq, dk, dv, dg, db
 
 
+class GatedDeltaRule(torch.autograd.Function):
+    """Autograd adapter of the gated delta rule (the six rm_gdr_* calls).  The
+    plan (summaries and the step's workspace) lives from the forward to the
+    backward: the backward reads M, S_in and the workspace the forward filled
+    (on the tensor cores, each chunk's triangular factors).  q has one row per
+    head (shared query rows are a plan option of the direct calls only)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, num_segments, chunk, scale, cu_seqlens):
+        q, k, v, g, beta = (t.contiguous() for t in (q, k, v, g, beta))
+        if q.shape != k.shape:
+            raise ValueError("gated_delta_rule: q and k must have the same shape [B,T,H,Dk]")
+        B, T, H, Dk = k.shape
+        plan = make_gdr_plan(B, T, H, Dk, v.shape[-1], num_segments, chunk, scale, v.dtype, cu_seqlens,
+                             v.device)
+        o = gdr_forward(plan, q, k, v, g, beta)
+        ctx.plan = plan
+        ctx.save_for_backward(q, k, v, g, beta)
+        return o
+
+    @staticmethod
+    def backward(ctx, dO):
+        q, k, v, g, beta = ctx.saved_tensors
+        grads = gdr_backward(ctx.plan, q, k, v, g, beta, dO.contiguous())
+        ctx.plan = None
+        return grads + (None, None, None, None)
+
+
+def gated_delta_rule(q, k, v, g, beta, num_segments: int, chunk: int = 16, scale=None, cu_seqlens=None):
+    """Differentiable gated delta rule: S_t = exp(g_t)(I - beta_t k_t k_t^T) S_{t-1}
+    + beta_t k_t v_t^T, o_t = scale S_t^T q_t.
+
+    q, k [B,T,H,Dk], v [B,T,H,Dv] (fp32 or bf16, CUDA), g and beta [B,T,H] fp32.
+    cu_seqlens (host int32 [N+1]) packs several sequences along T."""
+    return GatedDeltaRule.apply(q, k, v, g, beta, num_segments, chunk, scale, cu_seqlens)
+
+
 class GdrStepGraph:
     """One gated-delta-rule step captured as a CUDA graph: the three forward
     calls and, given dO, the three backward calls, on fixed buffers (as

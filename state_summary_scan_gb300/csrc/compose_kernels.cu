@@ -131,7 +131,7 @@ rm_status launch_compose_prefix(const Dims& d, const float* M, const float* dS, 
     const int blocks = int((n + kThreads - 1) / kThreads);
     compose_prefix_kernel<<<blocks, kThreads, 0, s>>>(d.nseg, d.B * d.H, vps, d.Dv, d.vg ? d.Dk : 1,
                                                       M, dS, d.preceding_start, S_in);
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(1);
     return RM_OK;
 }
@@ -143,7 +143,7 @@ rm_status launch_compose_suffix(const Dims& d, const float* M, const float* gamm
     const int blocks = int((n + kThreads - 1) / kThreads);
     compose_suffix_kernel<<<blocks, kThreads, 0, s>>>(d.nseg, d.B * d.H, vps, d.Dv, d.vg ? d.Dk : 1,
                                                       M, gamma, d.following_stop, dS_out);
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(1);
     return RM_OK;
 }

@@ -24,12 +24,13 @@ rm_status run(rmcp::GdrOp op, const rm_cp_problem* p, const rmcp::Dims& d, const
     // the four sweeps take the tensor cores where they can (the folds stay generic)
     const bool tc = op != rmcp::GdrOp::kComposePrefix && op != rmcp::GdrOp::kComposeSuffix &&
                     rmcp::gdrtc_supports(d, p->dtype);
-    rm_status st = tc ? rmcp::launch_gdrtc(op, d, x, reinterpret_cast<cudaStream_t>(stream))
-                      : rmcp::launch_gdr(op, d, p->dtype, x, reinterpret_cast<cudaStream_t>(stream));
+    rmcp::begin_launches();
+    if (tc) return rmcp::launch_gdrtc(op, d, x, reinterpret_cast<cudaStream_t>(stream));  // reports its own failures
+    rm_status st = rmcp::launch_gdr(op, d, p->dtype, x, reinterpret_cast<cudaStream_t>(stream));
     if (st == RM_ERR_CUDA) {
         char msg[256];
         std::snprintf(msg, sizeof(msg), "gated delta rule launch failed: %s",
-                      cudaGetErrorString(cudaGetLastError()));
+                      rmcp::cuda_error_text());
         return api_fail(RM_ERR_CUDA, msg);
     }
     if (st != RM_OK) return api_fail(st, "gated delta rule launch refused");

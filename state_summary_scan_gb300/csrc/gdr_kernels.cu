@@ -681,7 +681,7 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
             int th;
             const dim3 grid = colgrid(d.Dv, &th);
             RMCP_GDR_DK_SWITCH((gdr_gamma_sweep<DK, T><<<grid, th, 0, s>>>(d, q, k, p.g, p.beta, dO, p.gamma_out)));
-            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+            if (!rmcp::launch_ok()) return RM_ERR_CUDA;
             const int nprt = kSweepThreads / d.Dv > 0 ? kSweepThreads / d.Dv : 1;
             const size_t smem = sizeof(float) * (size_t(d.Dk) * (d.Dv + 1) + size_t(kBlk) * (d.Dk + 2 * d.Dv) +
                                                  size_t(nprt) * d.Dv);
@@ -711,7 +711,7 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
         }
     }
 #undef RMCP_GDR_DK_SWITCH
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(launches);
     return RM_OK;
 }

@@ -41,6 +41,8 @@
 // and, one CTA per (chunk, row, head), every chunk at once:
 //   gdrtc_chunk_grad_kernel   dk, dv, dbeta and dg of the chunk from its
 //                             saved S_prev and E (the backward apply's second)
+#include <cstdio>
+
 #include "tc_tiles.cuh"
 
 namespace rmcp {
@@ -1242,6 +1244,25 @@ bool gdrtc_supports(const Dims& d, rm_dtype dt) {
            d.T >= tc::kChunk;
 }
 
+namespace {
+
+// Failures of launch_gdrtc, reported with the step that failed.
+rm_status map_fail(const char* what) {
+    char msg[192];
+    std::snprintf(msg, sizeof(msg), "gated delta rule (tensor cores): no tensor map for %s (CUresult %d)", what,
+                  tc::last_map_result());
+    return api_fail(RM_ERR_CUDA, msg);
+}
+
+rm_status cuda_fail(const char* what) {
+    char msg[256];
+    std::snprintf(msg, sizeof(msg), "gated delta rule (tensor cores): %s failed: %s", what,
+                  cuda_error_text());
+    return api_fail(RM_ERR_CUDA, msg);
+}
+
+}  // namespace
+
 rm_status launch_gdrtc(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s) {
     using namespace gdrtc;
     if (!gdrtc_supports(d, RM_BF16)) return RM_ERR_UNSUPPORTED;
@@ -1253,60 +1274,62 @@ rm_status launch_gdrtc(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
     fd.B = 1;
     fd.T = int(2 * nchunks * kD);
     CUtensorMap mq, mk, mv, mo, mf, mx, my;
-    if (!make_map(&mk, p.k, d, kD)) return RM_ERR_CUDA;
-    if (op != GdrOp::kBackwardPrepare && !make_map(&mv, p.v, d, kD)) return RM_ERR_CUDA;
-    if (op != GdrOp::kPrepare && (!make_map(&mq, p.q, d, kD, d.qh) || !make_map(&mf, fac, fd, kD, 1)))
-        return RM_ERR_CUDA;
+    if (!make_map(&mk, p.k, d, kD)) return map_fail("k");
+    if (op != GdrOp::kBackwardPrepare && !make_map(&mv, p.v, d, kD)) return map_fail("v");
+    if (op != GdrOp::kPrepare && !make_map(&mq, p.q, d, kD, d.qh)) return map_fail("q");
+    if (op != GdrOp::kPrepare && !make_map(&mf, fac, fd, kD, 1)) return map_fail("the factor table");
     if (op == GdrOp::kPrepare) {
         // every chunk's factors at once, then the walk over each segment's chunks
-        if (!make_map(&mf, fac, fd, kD, 1)) return RM_ERR_CUDA;
+        if (!make_map(&mf, fac, fd, kD, 1)) return map_fail("the factor table");
         auto ff = gdrtc_factor_kernel;
-        if (!set_smem(ff, kFactorSmem)) return RM_ERR_CUDA;
+        if (!set_smem(ff, kFactorSmem)) return cuda_fail("shared-memory attribute of the factor kernel");
         ff<<<dim3(d.T / kChunk, d.B * d.H), 256, kFactorSmem, s>>>(d, mk, p.g, p.beta, fac);
-        if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+        if (!launch_ok()) return cuda_fail("launch of the factor kernel");
         note_launch(1);
         auto fn = gdrtc_prepare_kernel;
-        if (!set_smem(fn, kPrepSmem)) return RM_ERR_CUDA;
+        if (!set_smem(fn, kPrepSmem)) return cuda_fail("shared-memory attribute of the prepare kernel");
         fn<<<grid, 256, kPrepSmem, s>>>(d, mk, mv, mf, p.g, p.beta, p.M, p.dS);
     } else if (op == GdrOp::kApply) {
-        if (!make_map(&mo, p.o, d, kD)) return RM_ERR_CUDA;
+        if (!make_map(&mo, p.o, d, kD)) return map_fail("o");
         auto fn = gdrtc_apply_kernel;
-        if (!set_smem(fn, kApplySmem)) return RM_ERR_CUDA;
+        if (!set_smem(fn, kApplySmem)) return cuda_fail("shared-memory attribute of the apply kernel");
         fn<<<grid, 256, kApplySmem, s>>>(d, mq, mk, mv, mf, mo, p.g, p.beta, p.S_in);
     } else if (op == GdrOp::kBackwardPrepare) {
         // z = 0: the dq walk (which also needs v); z = 1: the gamma walk
-        if (!make_map(&mv, p.v, d, kD) || !make_map(&mo, p.dO, d, kD) || !make_map(&mx, p.dq, d, kD))
-            return RM_ERR_CUDA;
+        if (!make_map(&mv, p.v, d, kD)) return map_fail("v");
+        if (!make_map(&mo, p.dO, d, kD)) return map_fail("dO");
+        if (!make_map(&mx, p.dq, d, kD)) return map_fail("dq");
         auto fn = gdrtc_bwd_prepare_kernel;
-        if (!set_smem(fn, kBwdPrepSmem)) return RM_ERR_CUDA;
+        if (!set_smem(fn, kBwdPrepSmem)) return cuda_fail("shared-memory attribute of the backward prepare kernel");
         fn<<<dim3(d.nseg, d.B * d.H, 2), 256, kBwdPrepSmem, s>>>(d, mq, mk, mv, mo, mf, mx, p.g, p.beta, p.S_in,
                                                                 p.gamma_out, p.ws);
     } else if (op == GdrOp::kBackwardApply) {
         // the adjoint walk saves each chunk's E after the states and the factors,
         // then the gradients of every chunk at once
-        if (!make_map(&mo, p.dO, d, kD) || !make_map(&mx, p.dk, d, kD) || !make_map(&my, p.dv, d, kD))
-            return RM_ERR_CUDA;
+        if (!make_map(&mo, p.dO, d, kD)) return map_fail("dO");
+        if (!make_map(&mx, p.dk, d, kD)) return map_fail("dk");
+        if (!make_map(&my, p.dv, d, kD)) return map_fail("dv");
         float* Esave = p.ws + 2 * nchunks * kD * kD;
         auto fa = gdrtc_adjoint_kernel;
-        if (!set_smem(fa, kGaSmem)) return RM_ERR_CUDA;
+        if (!set_smem(fa, kGaSmem)) return cuda_fail("shared-memory attribute of the adjoint kernel");
         fa<<<grid, 256, kGaSmem, s>>>(d, mq, mk, mo, mf, p.g, p.beta, p.dS_out, Esave);
-        if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+        if (!launch_ok()) return cuda_fail("launch of the adjoint kernel");
         note_launch(1);
         auto fc = gdrtc_chunk_grad_kernel;
-        if (!set_smem(fc, kChunkGradSmem)) return RM_ERR_CUDA;
+        if (!set_smem(fc, kChunkGradSmem)) return cuda_fail("shared-memory attribute of the chunk-gradient kernel");
         fc<<<dim3(d.T / kChunk, d.B * d.H), 256, kChunkGradSmem, s>>>(d, mq, mk, mv, mo, mf, mx, my, p.g, p.beta,
                                                                      p.ws, Esave, p.dg, p.dbeta);
     } else {
         return RM_ERR_INVALID_ARG;
     }
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!launch_ok()) return cuda_fail("kernel launch");
     note_launch(1);
     return RM_OK;
 }
 
 rm_status gdrtc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cudaStream_t s) {
     gdrtc::read_flag_kernel<<<1, 1, 0, s>>>(dev_scratch, clear);
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(1);
     if (cudaMemcpyAsync(host_flag, dev_scratch, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return RM_ERR_CUDA;

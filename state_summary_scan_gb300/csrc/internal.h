@@ -81,6 +81,18 @@ rm_status vgtc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cu
 rm_status api_check_problem(const rm_cp_problem* p, Dims* d);
 rm_status api_need(const void* ptr, const char* name);
 rm_status api_fail(rm_status s, const char* msg);
+// Every compute entry point calls begin_launches() before its first CUDA
+// call.  It makes the current device's primary context current on the calling
+// thread (a thread that has made no runtime call yet, such as the thread
+// PyTorch's autograd runs backward calls on, may have none, and the tensor-map
+// encoder is a driver call that needs one) and clears a non-sticky error that
+// an earlier, unrelated runtime call on the thread left pending
+// (cudaGetLastError is per thread); a faulted context still fails the launches
+// themselves.  launch_ok() checks the launch just made and keeps its error for
+// the message cuda_error_text() gives.
+void begin_launches();
+bool launch_ok();
+const char* cuda_error_text();
 rm_status api_launch(Op op, const rm_cp_problem* p, const Dims& d, const Ptrs& ptrs,
                      rm_stream_t stream);
 

@@ -117,7 +117,11 @@ extern "C" rm_status rm_cp_backward_noalloc(const rm_cp_problem* p, const void* 
     st = rmcp::api_launch(rmcp::Op::kBackwardPrepare, p, d, a, stream);
     if (st != RM_OK) return st;
     st = rmcp::launch_compose_suffix(d, M, gamma, dS_out, reinterpret_cast<cudaStream_t>(stream));
-    if (st != RM_OK) return rmcp::api_fail(st, "rm_cp_backward_noalloc: suffix launch failed");
+    if (st != RM_OK) {
+        char msg[192];
+        std::snprintf(msg, sizeof(msg), "rm_cp_backward_noalloc: suffix launch failed: %s", rmcp::cuda_error_text());
+        return rmcp::api_fail(st, msg);
+    }
     rmcp::Ptrs b;
     b.q = q;
     b.k = k;

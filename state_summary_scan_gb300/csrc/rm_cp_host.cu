@@ -18,6 +18,30 @@ std::atomic<uint64_t> g_launches{0};
 void note_launch(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed); }
 }  // namespace rmcp
 
+namespace rmcp {
+namespace {
+thread_local cudaError_t g_launch_error = cudaSuccess;
+}
+void begin_launches() {
+    g_launch_error = cudaSuccess;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) (void)cudaSetDevice(dev);  // initialises and binds the context
+    (void)cudaGetLastError();
+}
+bool launch_ok() {
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) return true;
+    g_launch_error = e;
+    return false;
+}
+const char* cuda_error_text() {
+    cudaError_t e = g_launch_error;
+    g_launch_error = cudaSuccess;
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cudaGetErrorString(e);
+}
+}  // namespace rmcp
+
 namespace {
 
 thread_local char g_last_error[512] = "";
@@ -112,15 +136,13 @@ size_t workspace_bytes(const rmcp::Dims& d, rm_dtype dt) {
 rm_status launch(rmcp::Op op, const rm_cp_problem* p, const rmcp::Dims& d, const rmcp::Ptrs& ptrs,
                  rm_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    rmcp::begin_launches();
     rm_status st = d.vg ? (rmcp::vgtc_supports(d, p->dtype) ? rmcp::launch_vgtc(op, d, ptrs, s)
                                                             : rmcp::launch_vg(op, d, p->dtype, ptrs, s))
                    : rmcp::tc_supports_op(op, d, p->dtype)
                        ? rmcp::launch_tc(op, d, ptrs, s)
                        : rmcp::launch_generic(op, d, p->dtype, ptrs, s);
-    if (st == RM_ERR_CUDA) {
-        cudaError_t e = cudaGetLastError();
-        return fail(RM_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
-    }
+    if (st == RM_ERR_CUDA) return fail(RM_ERR_CUDA, "kernel launch failed: %s", rmcp::cuda_error_text());
     if (st != RM_OK) return fail(st, "launch refused");
     return RM_OK;
 }
@@ -167,7 +189,7 @@ rm_status rm_cp_device_status(int32_t* dev_scratch, int32_t clear, rm_stream_t s
     if (st == RM_OK) st = rmcp::vgtc_read_timeout_flag(&vflag, clear, dev_scratch, s);
     if (st == RM_OK) st = rmcp::gdrtc_read_timeout_flag(&gflag, clear, dev_scratch, s);
     if (st != RM_OK)
-        return fail(st, "device status read failed: %s", cudaGetErrorString(cudaGetLastError()));
+        return fail(st, "device status read failed: %s", rmcp::cuda_error_text());
     if (flag || vflag || gflag) return fail(RM_ERR_TIMEOUT, "a bounded device-side wait ran out");
     return RM_OK;
 }
@@ -267,9 +289,10 @@ rm_status rm_cp_compose_prefix(const rm_cp_problem* p, const float* M, const flo
     RM_NEED(M);
     RM_NEED(dS);
     RM_NEED(S_in);
+    rmcp::begin_launches();
     st = rmcp::launch_compose_prefix(d, M, dS, S_in, reinterpret_cast<cudaStream_t>(stream));
     if (st != RM_OK) return fail(st, "compose_prefix launch failed: %s",
-                                 cudaGetErrorString(cudaGetLastError()));
+                                 rmcp::cuda_error_text());
     return RM_OK;
 }
 
@@ -328,9 +351,10 @@ rm_status rm_cp_forward_fused(const rm_cp_problem* p, const void* q, const void*
     x.S_in_out = S_in;
     x.out0 = o;
     x.ws = ws;
+    rmcp::begin_launches();
     st = rmcp::tc_launch_fused_forward(d, x, reinterpret_cast<cudaStream_t>(stream));
     if (st == RM_ERR_CUDA)
-        return fail(RM_ERR_CUDA, "fused forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+        return fail(RM_ERR_CUDA, "fused forward launch failed: %s", rmcp::cuda_error_text());
     return st;
 }
 
@@ -371,9 +395,10 @@ rm_status rm_cp_compose_suffix(const rm_cp_problem* p, const float* M, const flo
     RM_NEED(M);
     RM_NEED(gamma);
     RM_NEED(dS_out);
+    rmcp::begin_launches();
     st = rmcp::launch_compose_suffix(d, M, gamma, dS_out, reinterpret_cast<cudaStream_t>(stream));
     if (st != RM_OK) return fail(st, "compose_suffix launch failed: %s",
-                                 cudaGetErrorString(cudaGetLastError()));
+                                 rmcp::cuda_error_text());
     return RM_OK;
 }
 

@@ -386,7 +386,7 @@ rm_status launch_generic_T(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) 
         case Op::kBackwardPrepare: {
             RMCP_DK_SWITCH((simt_column_sweep<DK, kGamma, T><<<cgrid, colthreads, 0, s>>>(
                 d, q, nullptr, nullptr, p.g, dO, nullptr, nullptr, nullptr, p.sum_out)));
-            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+            if (!rmcp::launch_ok()) return RM_ERR_CUDA;
             const int threads = d.Dk < 32 ? 32 : d.Dk;
             const size_t smem = sizeof(float) * (size_t(d.Dk) * (d.Dv + 1) + 2 * kTok * d.Dv);
             RMCP_DK_SWITCH({
@@ -417,7 +417,7 @@ rm_status launch_generic_T(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) 
             return RM_ERR_INVALID_ARG;
     }
 #undef RMCP_DK_SWITCH
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(op == Op::kBackwardPrepare ? 2 : 1);
     return RM_OK;
 }

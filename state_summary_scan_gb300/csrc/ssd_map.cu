@@ -335,6 +335,7 @@ extern "C" rm_status rm_ssd_map_inputs(const rm_cp_problem* p, int32_t G, const 
     RM_NEED_SSD(k);
     RM_NEED_SSD(g);
     auto st = reinterpret_cast<cudaStream_t>(stream);
+    rmcp::begin_launches();
     const int64_t bt = int64_t(d.B) * d.T;
     if (p->dtype == RM_BF16) {
         rmcp::ssd_map_inputs_kernel<__nv_bfloat16><<<unsigned(bt), rmcp::kThreads, 0, st>>>(
@@ -346,7 +347,11 @@ extern "C" rm_status rm_ssd_map_inputs(const rm_cp_problem* p, int32_t G, const 
             d.H, G, d.Dk, rmcp::log2i(d.Dk / 4), dt, A, static_cast<const float*>(Bm), static_cast<const float*>(Cm),
             static_cast<float*>(q), static_cast<float*>(k), g);
     }
-    if (cudaGetLastError() != cudaSuccess) return api_fail(RM_ERR_CUDA, "rm_ssd_map_inputs: launch failed");
+    if (!rmcp::launch_ok()) {
+        char msg[192];
+        std::snprintf(msg, sizeof(msg), "rm_ssd_map_inputs: launch failed: %s", rmcp::cuda_error_text());
+        return api_fail(RM_ERR_CUDA, msg);
+    }
     rmcp::note_launch(1);
     return RM_OK;
 }
@@ -361,6 +366,7 @@ extern "C" rm_status rm_ssd_finish_forward(const rm_cp_problem* p, const void* x
     if (D == nullptr) return RM_OK;
     RM_NEED_SSD(D);
     auto st = reinterpret_cast<cudaStream_t>(stream);
+    rmcp::begin_launches();
     const unsigned bt = unsigned(int64_t(d.B) * d.T);
     if (p->dtype == RM_BF16) {
         rmcp::ssd_finish_forward_kernel<__nv_bfloat16><<<bt, rmcp::kThreads, 0, st>>>(
@@ -369,7 +375,11 @@ extern "C" rm_status rm_ssd_finish_forward(const rm_cp_problem* p, const void* x
         rmcp::ssd_finish_forward_kernel<float><<<bt, rmcp::kThreads, 0, st>>>(
             d.H, rmcp::log2i(d.Dv / 4), static_cast<const float*>(x), D, static_cast<float*>(o));
     }
-    if (cudaGetLastError() != cudaSuccess) return api_fail(RM_ERR_CUDA, "rm_ssd_finish_forward: launch failed");
+    if (!rmcp::launch_ok()) {
+        char msg[192];
+        std::snprintf(msg, sizeof(msg), "rm_ssd_finish_forward: launch failed: %s", rmcp::cuda_error_text());
+        return api_fail(RM_ERR_CUDA, msg);
+    }
     rmcp::note_launch(1);
     return RM_OK;
 }
@@ -400,6 +410,7 @@ extern "C" rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, c
     RM_NEED_SSD(ws);
     if (D != nullptr) RM_NEED_SSD(D);
     auto st = reinterpret_cast<cudaStream_t>(stream);
+    rmcp::begin_launches();
     const int64_t bt = int64_t(d.B) * d.T, rows = bt * d.H;
     float* part = static_cast<float*>(ws);
     float* pa = part + rows;
@@ -432,7 +443,11 @@ extern "C" rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, c
         bt, d.H, dt, dg, part, pa, pd);
     rmcp::ssd_reduce_final_kernel<<<d.H, rmcp::kThreads, 0, st>>>(d.H, pa, pd, dA, dD);
     launches += 2;
-    if (cudaGetLastError() != cudaSuccess) return api_fail(RM_ERR_CUDA, "rm_ssd_finish_backward: launch failed");
+    if (!rmcp::launch_ok()) {
+        char msg[192];
+        std::snprintf(msg, sizeof(msg), "rm_ssd_finish_backward: launch failed: %s", rmcp::cuda_error_text());
+        return api_fail(RM_ERR_CUDA, msg);
+    }
     rmcp::note_launch(launches);
     return RM_OK;
 }

@@ -2656,17 +2656,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 // [B*T rows][H][D] bf16 viewed as a 3-D tensor; boxes of 64 tokens x 64 columns.
+namespace {
+thread_local int g_map_result = 0;
+}
+int last_map_result() { return g_map_result; }
+
 bool make_map(CUtensorMap* m, const void* base, const Dims& d, int D, int heads) {
     auto fn = encode_fn();
+    g_map_result = -1;  // no encoder
     if (!fn) return false;
     if (heads <= 0) heads = d.H;
     cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(heads), cuuint64_t(d.B) * cuuint64_t(d.T)};
     cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(heads) * D * 2};
     cuuint32_t box[3] = {64, 1, uint32_t(kChunk)};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    g_map_result = int(fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+    return g_map_result == int(CUDA_SUCCESS);
 }
 
 // multiprocessors of the current device (cached per device)
@@ -2741,21 +2748,21 @@ rm_status tc_launch_fused_forward(const Dims& d, const Ptrs& p, cudaStream_t s) 
     const size_t fsm = two ? kFwd2TwoSmem : kFwd2Smem;
     if (!set_smem(fk, fsm)) return RM_ERR_CUDA;
     fk<<<unsigned(n), kRev3Threads, fsm, s>>>(d, mq, mk, mv, mo, p.g, p.M, p.sum_out, p.S_in_out, w);
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(1);
     return RM_OK;
 }
 
 rm_status tc_selftest_wait(uint32_t limit_us, cudaStream_t s) {
     tc::selftest_wait_kernel<<<1, 1, 0, s>>>(uint64_t(limit_us) * 1000ull);
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(1);
     return RM_OK;
 }
 
 rm_status tc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cudaStream_t s) {
     tc::read_flag_kernel<<<1, 1, 0, s>>>(dev_scratch, clear);
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(1);
     if (cudaMemcpyAsync(host_flag, dev_scratch, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return RM_ERR_CUDA;
@@ -2792,7 +2799,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 if (!set_smem(fn, kOuterSmem)) return RM_ERR_CUDA;
                 fn<<<grid, kThreads, kOuterSmem, s>>>(d, mk, mv, p.g, p.M, p.sum_out);
             }
-            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+            if (!rmcp::launch_ok()) return RM_ERR_CUDA;
             note_launch(1);
             return RM_OK;
         }
@@ -2811,7 +2818,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             if (!set_smem(ff, fsm)) return RM_ERR_CUDA;
             ff<<<fgrid, kRev3Threads, fsm, s>>>(
                 d, mq, mk, mv, mo, p.g, p.S_in);
-            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+            if (!rmcp::launch_ok()) return RM_ERR_CUDA;
             note_launch(1);
             return RM_OK;
         }
@@ -2826,7 +2833,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 if (!set_smem(fq, kDqg128Smem)) return RM_ERR_CUDA;
                 fq<<<grid, kRev3Threads, kDqg128Smem, s>>>(d, mq, mk, mv, mdo, mdq, p.g, p.S_in, p.sum_out,
                                                           p.ws_f32);
-                if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+                if (!rmcp::launch_ok()) return RM_ERR_CUDA;
                 note_launch(1);
                 return RM_OK;
             } else {
@@ -2834,11 +2841,11 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 auto fq = tc_dq256_kernel;
                 if (!set_smem(fo, kOuterSmem) || !set_smem(fq, kDq256Smem)) return RM_ERR_CUDA;
                 fo<<<grid, kThreads, kOuterSmem, s>>>(d, mq, mdo, p.g, nullptr, p.sum_out);
-                if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+                if (!rmcp::launch_ok()) return RM_ERR_CUDA;
                 fq<<<grid, kRev3Threads, kDq256Smem, s>>>(d, mq, mk, mv, mdo, p.g, p.S_in,
                                                           static_cast<__nv_bfloat16*>(p.out0), p.ws_f32);
             }
-            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+            if (!rmcp::launch_ok()) return RM_ERR_CUDA;
             note_launch(2);
             return RM_OK;
         }
@@ -2861,7 +2868,7 @@ rm_status launch_tc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
                 fr<<<grid, kRev3Threads, rev_smem(256), s>>>(d, mq, mk, mv, mdo, p.g, p.S_in, p.dS_out,
                                                              p.ws_f32, dko, dvo, p.dg);
             }
-            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+            if (!rmcp::launch_ok()) return RM_ERR_CUDA;
             note_launch(1);
             return RM_OK;
         }

@@ -334,7 +334,7 @@ rm_status launch_vg_T(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
         case Op::kBackwardPrepare: {
             RMCP_VG_DK_SWITCH((vg_column_sweep<DK, kVgGamma, T><<<cgrid, colthreads, 0, s>>>(
                 d, q, nullptr, nullptr, p.g, dO, nullptr, nullptr, nullptr, p.sum_out)));
-            if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+            if (!rmcp::launch_ok()) return RM_ERR_CUDA;
             const int threads = d.Dk < 32 ? 32 : d.Dk;
             const size_t smem = sizeof(float) * (size_t(d.Dk) * (d.Dv + 1) + 2 * kTok * d.Dv);
             RMCP_VG_DK_SWITCH({
@@ -365,7 +365,7 @@ rm_status launch_vg_T(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
             return RM_ERR_INVALID_ARG;
     }
 #undef RMCP_VG_DK_SWITCH
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(op == Op::kBackwardPrepare ? 2 : 1);
     return RM_OK;
 }

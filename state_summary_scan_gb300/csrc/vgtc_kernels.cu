@@ -1314,14 +1314,14 @@ rm_status launch_vgtc(Op op, const Dims& d, const Ptrs& p, cudaStream_t s) {
         default:
             return RM_ERR_INVALID_ARG;
     }
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(1);
     return RM_OK;
 }
 
 rm_status vgtc_read_timeout_flag(int* host_flag, int clear, int* dev_scratch, cudaStream_t s) {
     vgtc::read_flag_kernel<<<1, 1, 0, s>>>(dev_scratch, clear);
-    if (cudaGetLastError() != cudaSuccess) return RM_ERR_CUDA;
+    if (!rmcp::launch_ok()) return RM_ERR_CUDA;
     note_launch(1);
     if (cudaMemcpyAsync(host_flag, dev_scratch, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return RM_ERR_CUDA;

@@ -104,3 +104,72 @@ def test_gdr_graph_replay_equals_direct_calls():
         torch.cuda.synchronize()
         for a, b_ in zip(got, want):
             assert torch.equal(a, b_)
+
+
+@pytest.mark.parametrize("case", ["scalar", "vector"])
+def test_autograd_equals_direct_calls_tensor_cores(case):
+    """torch.autograd through chunkwise_gla runs its backward on autograd's
+    device thread; on the tensor-core path it gives the direct calls' o and
+    gradients bit for bit."""
+    B, T, H, Dk, Dv, nseg = 1, 1024, 2, 128, 128, 4
+    vg = case == "vector"
+    q, k, v, g, dO = _inputs(B, T, H, Dk, Dv, vg, seed=3)
+    scale = 1 / math.sqrt(Dk)
+    pd = api.make_plan(B, T, H, Dk, Dv, nseg, 64, scale, torch.bfloat16, None, "cuda", vector_gates=vg)
+    assert C.rm_cp_path(pd.spec) == 1
+    o_ref = api.forward(pd, q, k, v, g)
+    g_ref = api.backward(pd, q, k, v, g, dO)
+    leaves = [t.clone().requires_grad_(True) for t in (q, k, v, g)]
+    o = api.chunkwise_gla(*leaves, nseg, 64, scale)
+    o.backward(dO)
+    torch.cuda.synchronize()
+    assert torch.equal(o.detach(), o_ref)
+    for name, leaf, ref in zip(("dq", "dk", "dv", "dg"), leaves, g_ref):
+        assert torch.equal(leaf.grad, ref), name
+
+
+@pytest.mark.parametrize("case", ["scalar", "gdr"])
+def test_calls_from_a_thread_without_cuda_context(case):
+    """A backward called from a thread that has made no CUDA call (buffers
+    preallocated, the stream passed in: autograd's device thread with a warm
+    caching allocator is such a thread) gives the same gradients as from the
+    main thread: the entry points bind the device's context themselves before
+    encoding their tensor maps."""
+    import threading
+
+    stream = torch.cuda.current_stream()
+    if case == "scalar":
+        B, T, H, D, nseg = 1, 1024, 2, 128, 4
+        q, k, v, g, dO = _inputs(B, T, H, D, D, False, seed=4)
+        plan = api.make_plan(B, T, H, D, D, nseg, 64, 1 / math.sqrt(D), torch.bfloat16, None, "cuda")
+        assert C.rm_cp_path(plan.spec) == 1
+        api.forward(plan, q, k, v, g)
+        call = lambda out: api.backward(plan, q, k, v, g, dO, stream=stream, grads=out)
+        out = [torch.empty_like(t) for t in (q, k, v, g)]
+    else:
+        B, T, H, D, nseg = 1, 512, 2, 64, 4
+        q, k, v, g, dO = _inputs(B, T, H, D, D, False, seed=4)
+        beta = torch.sigmoid(g)
+        plan = api.make_gdr_plan(B, T, H, D, D, nseg, 16, 1 / math.sqrt(D), torch.bfloat16, None, "cuda")
+        assert C.rm_gdr_path(plan.spec) == 1
+        api.gdr_forward(plan, q, k, v, g, beta)
+        call = lambda out: api.gdr_backward(plan, q, k, v, g, beta, dO, stream=stream, grads=out)
+        out = [torch.empty_like(t) for t in (q, k, v, g, beta)]
+    ref = [torch.empty_like(t) for t in out]
+    call(ref)
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker():
+        try:
+            call(out)
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for a, b in zip(out, ref):
+        assert torch.equal(a, b)
