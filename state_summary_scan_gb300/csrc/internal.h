@@ -93,6 +93,10 @@ rm_status api_fail(rm_status s, const char* msg);
 void begin_launches();
 bool launch_ok();
 const char* cuda_error_text();
+namespace tc {
+int last_map_result();   // CUresult of the thread's last tensor-map encode
+void clear_map_result();
+}  // namespace tc
 rm_status api_launch(Op op, const rm_cp_problem* p, const Dims& d, const Ptrs& ptrs,
                      rm_stream_t stream);
 

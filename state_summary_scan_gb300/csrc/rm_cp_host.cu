@@ -24,6 +24,7 @@ thread_local cudaError_t g_launch_error = cudaSuccess;
 }
 void begin_launches() {
     g_launch_error = cudaSuccess;
+    tc::clear_map_result();
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) (void)cudaSetDevice(dev);  // initialises and binds the context
     (void)cudaGetLastError();
@@ -142,7 +143,12 @@ rm_status launch(rmcp::Op op, const rm_cp_problem* p, const rmcp::Dims& d, const
                    : rmcp::tc_supports_op(op, d, p->dtype)
                        ? rmcp::launch_tc(op, d, ptrs, s)
                        : rmcp::launch_generic(op, d, p->dtype, ptrs, s);
-    if (st == RM_ERR_CUDA) return fail(RM_ERR_CUDA, "kernel launch failed: %s", rmcp::cuda_error_text());
+    if (st == RM_ERR_CUDA) {
+        const int mr = rmcp::tc::last_map_result();
+        if (mr != 0)
+            return fail(RM_ERR_CUDA, "kernel launch failed: no tensor map (CUresult %d; bases 16-byte aligned?)", mr);
+        return fail(RM_ERR_CUDA, "kernel launch failed: %s", rmcp::cuda_error_text());
+    }
     if (st != RM_OK) return fail(st, "launch refused");
     return RM_OK;
 }
@@ -353,8 +359,12 @@ rm_status rm_cp_forward_fused(const rm_cp_problem* p, const void* q, const void*
     x.ws = ws;
     rmcp::begin_launches();
     st = rmcp::tc_launch_fused_forward(d, x, reinterpret_cast<cudaStream_t>(stream));
-    if (st == RM_ERR_CUDA)
+    if (st == RM_ERR_CUDA) {
+        const int mr = rmcp::tc::last_map_result();
+        if (mr != 0)
+            return fail(RM_ERR_CUDA, "fused forward launch failed: no tensor map (CUresult %d)", mr);
         return fail(RM_ERR_CUDA, "fused forward launch failed: %s", rmcp::cuda_error_text());
+    }
     return st;
 }
 

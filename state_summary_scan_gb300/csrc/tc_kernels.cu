@@ -2655,12 +2655,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// [B*T rows][H][D] bf16 viewed as a 3-D tensor; boxes of 64 tokens x 64 columns.
 namespace {
-thread_local int g_map_result = 0;
+thread_local int g_map_result = 0;  // CUresult of the calling thread's last make_map
 }
 int last_map_result() { return g_map_result; }
+void clear_map_result() { g_map_result = 0; }
 
+// [B*T rows][H][D] bf16 viewed as a 3-D tensor; boxes of 64 tokens x 64 columns.
 bool make_map(CUtensorMap* m, const void* base, const Dims& d, int D, int heads) {
     auto fn = encode_fn();
     g_map_result = -1;  // no encoder

@@ -146,8 +146,10 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v
 // [B*T rows][heads][D] bf16 viewed as a 3-D tensor; boxes of 64 tokens x 64
 // columns, 128-byte swizzle (heads <= 0: d.H).
 bool make_map(CUtensorMap* m, const void* base, const Dims& d, int D, int heads = 0);
-// the CUresult of the calling thread's last make_map (-1: no encoder found)
+// the CUresult of the calling thread's last make_map (-1: no encoder found;
+// 0 after clear_map_result)
 int last_map_result();
+void clear_map_result();
 // multiprocessors of the current device (cached per device)
 int sm_count();
 
