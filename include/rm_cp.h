@@ -468,7 +468,7 @@ rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, const void* 
  *                           dk, dv [B,T,H,*] (dtype), dg, dbeta [B,T,H] fp32
  *                           (dg exactly 0 at sequence starts)
  * The problem is an rm_cp_problem (vector_gates = 0, any q_heads): Dk in
- * {16, 32, 64}, Dv a multiple of 8 up to 128, segment lengths a multiple of
+ * {16, 32, 64, 128}, Dv a multiple of 8 up to 128, segment lengths a multiple of
  * 16 (RM_ERR_UNSUPPORTED otherwise).  bf16 storage with Dk = Dv = 64 and
  * segment lengths that are multiples of 64 runs the four sweeps on the
  * tensor cores in the chunkwise WY/UT form (per 64-token chunk the products

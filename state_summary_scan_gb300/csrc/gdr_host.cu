@@ -14,7 +14,7 @@ rm_status check_gdr(const rm_cp_problem* p, rmcp::Dims* d) {
     if (d->vg) return api_fail(RM_ERR_INVALID_ARG, "the gated delta rule takes one gate per head");
     if (!rmcp::gdr_supports(*d))
         return api_fail(RM_ERR_UNSUPPORTED,
-                        "the gated delta rule takes Dk in {16, 32, 64}, Dv a multiple of 8 in "
+                        "the gated delta rule takes Dk in {16, 32, 64, 128}, Dv a multiple of 8 in "
                         "[8, 128] and segment lengths that are multiples of 16");
     return RM_OK;
 }

@@ -231,48 +231,59 @@ __global__ void __launch_bounds__(128) gdr_gamma_sweep(Dims d, const T* __restri
 // ---------------------------------------------------------------------------
 // Summary folds with matrix transitions: each column of the carried state
 // folds on its own (S <- M S + X acts column by column), so one CTA takes
-// kFoldCols = 4 columns of one (row, head), one thread per state row r (DK
-// threads).  The thread holds row r of M_i (column r for the suffix's M_i^T)
-// in registers, loaded two segments ahead, and reads the
-// carried block's rows as 16-byte vectors from shared memory, so each loaded
-// entry serves four multiply-adds; it writes its own row of the result.
+// kFoldCols = 4 columns of one (row, head), fold_parts(DK) consecutive lanes
+// per state row r.  Lane part p holds the entries [NT p, NT p + NT) of row r
+// of M_i (of column r for the suffix's M_i^T; NT = DK / parts) in registers,
+// loaded two segments ahead, and reads those rows of the carried block as
+// 16-byte vectors from shared memory, so each loaded entry serves four
+// multiply-adds; the parts' sums meet by lane exchanges and part 0 writes row
+// r of the result.  Up to DK = 64 a lane takes the whole row; at DK = 128 two
+// lanes share it, so that the two segments' entries stay in registers.
 //   prefix: S_in[j] = fold over [pre_j, j) of S <- M_i S + dS_i  (from 0)
 //   suffix: dS_out[j] = fold over (j, fol_j) of D <- M_i^T D + gamma_i,
 //           from the last segment down (from 0)
-// grid (B*H, Dv / kFoldCols); block DK.
+// grid (B*H, Dv / kFoldCols); block DK * fold_parts(DK).
 // ---------------------------------------------------------------------------
 constexpr int kFoldCols = 4;
+__host__ __device__ constexpr int fold_parts(int dk) { return dk > 64 ? 2 : 1; }
 
 template <int DK, bool SUFFIX>
-__global__ void __launch_bounds__(64) gdr_compose(Dims d, const float* __restrict__ M,
+__global__ void __launch_bounds__(DK * fold_parts(DK)) gdr_compose(Dims d, const float* __restrict__ M,
                                                   const float* __restrict__ X,
                                                   const int32_t* __restrict__ range,
                                                   float* __restrict__ out) {
-    __shared__ float4 s_s[2][DK];  // the carried block: row c, the CTA's four columns
+    constexpr int PARTS = fold_parts(DK);
+    constexpr int NT = DK / PARTS;  // entries of a row a lane multiplies
+    // the carried block: row c, the CTA's four columns, at c + c / NT (one
+    // vector of padding per part, so that the parts read distinct banks)
+    __shared__ float4 s_s[2][DK + PARTS];
     const int bh = blockIdx.x;
     const int b = bh / d.H, h = bh % d.H;
-    const int r = threadIdx.x;                // state row
+    const int r = threadIdx.x / PARTS;        // state row
+    const int part = threadIdx.x % PARTS;     // rows [NT part, +NT) of the product
+    const int rs = r + r / NT;                // padded slot of row r
     const int c0 = blockIdx.y * kFoldCols;    // first column (Dv is a multiple of 8)
     const int n = d.nseg;
     int buf = 0;  // s_s[buf] holds the carried block
     // two segments in flight: slot i & 1 holds segment i's row of M_i and X_i
     // (the folds walk the segments in order, so i + 2 refills the slot i frees)
-    float mpa[DK], mpb[DK];
-    float4 xpa, xpb;
+    float mpa[NT], mpb[NT];
+    float4 xpa = make_float4(0.f, 0.f, 0.f, 0.f), xpb = xpa;  // X_i's row (part 0)
     int pfa = -1, pfb = -1;  // the segment in each slot (the same in every thread)
-    auto fetch = [&](int i, float (&mp)[DK], float4& xp) {
+    auto fetch = [&](int i, float (&mp)[NT], float4& xp) {
         const float* mi = M + ((int64_t(i) * d.B + b) * d.H + h) * DK * DK;
         if (SUFFIX) {
 #pragma unroll
-            for (int c = 0; c < DK; ++c) mp[c] = __ldg(mi + c * DK + r);
+            for (int c = 0; c < NT; ++c) mp[c] = __ldg(mi + (NT * part + c) * DK + r);
         } else {
 #pragma unroll
-            for (int c = 0; c < DK; c += 4) {
-                const float4 v = __ldg(reinterpret_cast<const float4*>(mi + r * DK + c));
+            for (int c = 0; c < NT; c += 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(mi + r * DK + NT * part + c));
                 mp[c] = v.x; mp[c + 1] = v.y; mp[c + 2] = v.z; mp[c + 3] = v.w;
             }
         }
-        xp = __ldg(reinterpret_cast<const float4*>(X + sum_off(d, i, b, h) + int64_t(r) * d.Dv + c0));
+        if (part == 0)
+            xp = __ldg(reinterpret_cast<const float4*>(X + sum_off(d, i, b, h) + int64_t(r) * d.Dv + c0));
     };
     auto prefetch = [&](int i) {
         if (i < 0 || i >= n) return;
@@ -284,18 +295,29 @@ __global__ void __launch_bounds__(64) gdr_compose(Dims d, const float* __restric
             pfa = i;
         }
     };
-    auto clear = [&]() { s_s[buf][r] = make_float4(0.f, 0.f, 0.f, 0.f); };
-    auto step = [&](const float (&m)[DK], float4 a0) {
+    auto clear = [&]() {
+        if (part == 0) s_s[buf][rs] = make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto step = [&](const float (&m)[NT], float4 a0) {
         float4 a1 = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4* src = &s_s[buf][(NT + 1) * part];
 #pragma unroll
-        for (int c = 0; c < DK; c += 2) {
-            const float4 s0 = s_s[buf][c], s1 = s_s[buf][c + 1];
+        for (int c = 0; c < NT; c += 2) {
+            const float4 s0 = src[c], s1 = src[c + 1];
             a0.x = fmaf(m[c], s0.x, a0.x); a0.y = fmaf(m[c], s0.y, a0.y);
             a0.z = fmaf(m[c], s0.z, a0.z); a0.w = fmaf(m[c], s0.w, a0.w);
             a1.x = fmaf(m[c + 1], s1.x, a1.x); a1.y = fmaf(m[c + 1], s1.y, a1.y);
             a1.z = fmaf(m[c + 1], s1.z, a1.z); a1.w = fmaf(m[c + 1], s1.w, a1.w);
         }
-        s_s[buf ^ 1][r] = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
+        float4 a = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
+#pragma unroll
+        for (int o = 1; o < PARTS; o <<= 1) {  // the parts of row r
+            a.x += __shfl_xor_sync(0xffffffffu, a.x, o);
+            a.y += __shfl_xor_sync(0xffffffffu, a.y, o);
+            a.z += __shfl_xor_sync(0xffffffffu, a.z, o);
+            a.w += __shfl_xor_sync(0xffffffffu, a.w, o);
+        }
+        if (part == 0) s_s[buf ^ 1][rs] = a;
     };
     // s_s[buf ^ 1] = M_i s_s[buf] + X_i (M_i^T for the suffix); buf flips
     auto fold = [&](int i) {
@@ -331,8 +353,8 @@ __global__ void __launch_bounds__(64) gdr_compose(Dims d, const float* __restric
             for (int i = i0; SUFFIX ? i > j : i < j; i += SUFFIX ? -1 : 1) fold(i);
             cur = lim;
         }
-        // this thread's row of the carried block is its own last write
-        *reinterpret_cast<float4*>(out + sum_off(d, j, b, h) + int64_t(r) * d.Dv + c0) = s_s[buf][r];
+        // row r of the carried block is part 0's own last write
+        if (part == 0) *reinterpret_cast<float4*>(out + sum_off(d, j, b, h) + int64_t(r) * d.Dv + c0) = s_s[buf][rs];
         fold(j);  // extend the fold by segment j for the next segment's range
     }
 }
@@ -494,9 +516,23 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_dq_sweep(Dims d, const T* _
 // first slot advanced in place to the group's start, the others one step
 // apart), then for each token t of the group (last first):
 // D_t = scale q_t dO_t^T + (t at the segment end ? dS_out : A_{t+1} D_{t+1}),
-// and the gradients follow.  grid (nseg, B*H); block kSweepThreads.
+// and the gradients follow.  The stack holds rev_slots(Dk, Dv) states (four,
+// or fewer where four do not fit in shared memory, e.g. one at Dk = Dv = 128).
+// grid (nseg, B*H); block kSweepThreads.
 // ---------------------------------------------------------------------------
 constexpr int kSlots = 4;
+constexpr size_t kRevSmemLimit = 227 * 1024;
+
+size_t rev_smem_bytes(const Dims& d, int slots) {
+    const int nprt = kSweepThreads / d.Dv > 0 ? kSweepThreads / d.Dv : 1;
+    return sizeof(float) * ((1 + size_t(slots)) * size_t(d.Dk) * (d.Dv + 1) +
+                            size_t(kBlk) * (2 * d.Dk + 2 * d.Dv) + size_t(nprt + 2) * d.Dv);
+}
+int rev_slots(const Dims& d) {
+    int s = kSlots;
+    while (s > 1 && rev_smem_bytes(d, s) > kRevSmemLimit) s /= 2;  // kBlk stays a multiple
+    return s;
+}
 
 template <int DK, typename T>
 __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const T* __restrict__ q,
@@ -509,14 +545,14 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
                                                          const float* __restrict__ ckpt,
                                                          T* __restrict__ dk, T* __restrict__ dv,
                                                          float* __restrict__ dg,
-                                                         float* __restrict__ dbeta) {
+                                                         float* __restrict__ dbeta, int nslots) {
     extern __shared__ float smem[];
     const int pitch = d.Dv + 1;
     const int spitch = DK * pitch;     // floats per state
     const int nprt = blockDim.x / d.Dv > 0 ? int(blockDim.x) / d.Dv : 1;
     float* D = smem;                   // [DK][pitch]
-    float* St = D + spitch;            // [kSlots][DK][pitch]
-    float* kb = St + kSlots * spitch;  // [kBlk][DK]
+    float* St = D + spitch;            // [nslots][DK][pitch]
+    float* kb = St + nslots * spitch;  // [kBlk][DK]
     float* qb = kb + kBlk * DK;        // [kBlk][DK]
     float* vb = qb + kBlk * DK;        // [kBlk][Dv]
     float* ob = vb + kBlk * d.Dv;      // [kBlk][Dv]
@@ -549,8 +585,8 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
             alb[threadIdx.x] = gdr_alpha(d, g, b, c + threadIdx.x, h);
             beb[threadIdx.x] = __ldg(beta + g_off(d, b, c + threadIdx.x, h));
         }
-        for (int grp = kBlk / kSlots - 1; grp >= 0; --grp) {
-            const int r0 = grp * kSlots;  // block index of the group's first token
+        for (int grp = kBlk / nslots - 1; grp >= 0; --grp) {
+            const int r0 = grp * nslots;  // block index of the group's first token
             // slot 0 <- S_{c + r0 - 1}: the saved S_{c-1} advanced over tokens c .. c + r0 - 1
             batched_copy(DK * d.Dv, [&](int e) { return __ldg(cs + e); },
                          [&](int e, float x) { St[(e / d.Dv) * pitch + e % d.Dv] = x; });
@@ -558,12 +594,12 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
             for (int r = 0; r < r0; ++r)
                 gdr_step<DK>(St, St, pitch, d.Dv, kb + r * DK, vb + r * d.Dv, alb[r], beb[r], ksp, nprt);
             // slot j <- S_{c + r0 + j - 1}
-            for (int j = 1; j < kSlots; ++j) {
+            for (int j = 1; j < nslots; ++j) {
                 const int r = r0 + j - 1;
                 gdr_step<DK>(St + (j - 1) * spitch, St + j * spitch, pitch, d.Dv, kb + r * DK, vb + r * d.Dv,
                              alb[r], beb[r], ksp, nprt);
             }
-            for (int j = kSlots - 1; j >= 0; --j) {
+            for (int j = nslots - 1; j >= 0; --j) {
                 const int r = r0 + j, t = c + r;
                 const float* S = St + j * spitch;  // S_{t-1}
                 const float* kt = kb + r * DK;
@@ -643,6 +679,7 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
         case 16: { constexpr int DK = 16; __VA_ARGS__; break; }   \
         case 32: { constexpr int DK = 32; __VA_ARGS__; break; }   \
         case 64: { constexpr int DK = 64; __VA_ARGS__; break; }   \
+        case 128: { constexpr int DK = 128; __VA_ARGS__; break; } \
         default: return RM_ERR_UNSUPPORTED;                       \
     }
 
@@ -669,10 +706,10 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
         case GdrOp::kComposeSuffix: {
             const dim3 grid(BH, d.Dv / kFoldCols);
             if (op == GdrOp::kComposePrefix) {
-                RMCP_GDR_DK_SWITCH((gdr_compose<DK, false><<<grid, DK, 0, s>>>(
+                RMCP_GDR_DK_SWITCH((gdr_compose<DK, false><<<grid, DK * fold_parts(DK), 0, s>>>(
                     d, p.M, p.dS, d.preceding_start, p.S_in_out)));
             } else {
-                RMCP_GDR_DK_SWITCH((gdr_compose<DK, true><<<grid, DK, 0, s>>>(
+                RMCP_GDR_DK_SWITCH((gdr_compose<DK, true><<<grid, DK * fold_parts(DK), 0, s>>>(
                     d, p.M, p.gamma, d.following_stop, p.dS_out_out)));
             }
             break;
@@ -696,16 +733,15 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
             break;
         }
         case GdrOp::kBackwardApply: {
-            const int nprt = kSweepThreads / d.Dv > 0 ? kSweepThreads / d.Dv : 1;
-            const size_t smem = sizeof(float) * ((1 + kSlots) * size_t(d.Dk) * (d.Dv + 1) +
-                                                 size_t(kBlk) * (2 * d.Dk + 2 * d.Dv) + size_t(nprt + 2) * d.Dv);
+            const int nslots = rev_slots(d);
+            const size_t smem = rev_smem_bytes(d, nslots);
             RMCP_GDR_DK_SWITCH({
                 auto fn = gdr_reverse_sweep<DK, T>;
                 if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
                     return RM_ERR_CUDA;
                 fn<<<dim3(d.nseg, BH), kSweepThreads, smem, s>>>(d, q, k, v, p.g, p.beta, dO, p.dS_out, p.ws,
                                                        static_cast<T*>(p.dk), static_cast<T*>(p.dv), p.dg,
-                                                       p.dbeta);
+                                                       p.dbeta, nslots);
             });
             break;
         }
@@ -719,7 +755,8 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
 }  // namespace
 
 bool gdr_supports(const Dims& d) {
-    return (d.Dk == 16 || d.Dk == 32 || d.Dk == 64) && d.Dv % 8 == 0 && d.Dv >= 8 && d.Dv <= 128 &&
+    return (d.Dk == 16 || d.Dk == 32 || d.Dk == 64 || d.Dk == 128) && d.Dv % 8 == 0 && d.Dv >= 8 &&
+           d.Dv <= 128 &&
            d.L % kBlk == 0 && !d.vg;
 }
 

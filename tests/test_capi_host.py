@@ -280,9 +280,10 @@ def test_gdr_path_and_workspace():
     assert C.rm_gdr_path(C.ProblemSpec(**dict(base, Dk=32))) == 0                     # Dk != 64
     assert C.rm_gdr_path(C.ProblemSpec(**dict(base, Dv=48))) == 0                     # Dv != 64
     assert C.rm_gdr_path(C.ProblemSpec(**dict(base, T=w.T - 32 * 16, chunk=16))) == 0  # L % 64 != 0
-    assert C.rm_gdr_path(C.ProblemSpec(**dict(base, Dk=128))) == -1
+    assert C.rm_gdr_path(C.ProblemSpec(**dict(base, Dk=128))) == 0                    # generic kernels
+    assert C.rm_gdr_path(C.ProblemSpec(**dict(base, Dk=128, Dv=136))) == -1           # Dv > 128
     assert C.rm_gdr_path(C.ProblemSpec(**base, vector_gates=1)) == -1
     ntok = w.B * w.T * w.H
     ws = C.rm_gdr_workspace_size(tc)
     assert ws >= (ntok // 16) * w.Dk * w.Dv * 4 >= (ntok // 64) * w.Dk * w.Dv * 4
-    assert C.rm_gdr_workspace_size(C.ProblemSpec(**dict(base, Dk=128))) == 0
+    assert C.rm_gdr_workspace_size(C.ProblemSpec(**dict(base, Dk=128, Dv=136))) == 0

@@ -95,8 +95,20 @@ def test_gdr_wide(dtype):
     run_case(1, 256, 2, 64, 64, dtype, nseg=4, seed=4)
 
 
+@pytest.mark.parametrize("dtype,Dv", [(torch.float32, 128), (torch.bfloat16, 64)])
+def test_gdr_dk128(dtype, Dv):
+    # Dk = 128 on the generic kernels: the fold splits a state row over two
+    # lanes, the reverse sweep rebuilds one state at a time (Dv = 128)
+    run_case(1, 256, 2, 128, Dv, dtype, nseg=4, seed=14)
+
+
+def test_gdr_dk128_packed_shared_queries():
+    cu = [0, 40, 41, 130, 256]
+    run_case(1, 256, 4, 128, 32, torch.float32, nseg=8, cu=cu, qh=2, seed=15)
+
+
 def test_gdr_rejects_unsupported_shapes():
-    bad = C.ProblemSpec(1, 128, 2, 128, 16, 4, 16, 0.1, torch.float32)  # Dk = 128
+    bad = C.ProblemSpec(1, 128, 2, 48, 16, 4, 16, 0.1, torch.float32)  # Dk = 48
     t = torch.zeros(16, device="cuda")
     with pytest.raises(C.RmCpError) as e:
         C.rm_gdr_forward_prepare(bad, t, t, t, t, t, t, t)
