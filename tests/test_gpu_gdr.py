@@ -239,3 +239,31 @@ def test_gated_delta_rule_autograd_equals_direct_calls(case):
     for name, leaf, ref in zip(("dq", "dk", "dv", "dg", "dbeta"), leaves, g_ref):
         assert leaf.grad.dtype == leaf.dtype, name
         assert torch.equal(leaf.grad, ref), name
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_gdr_generic_random_shapes(seed):
+    """Seeded random problems on the generic kernels: Dk in {16, 32, 64, 128},
+    Dv a multiple of 8 up to 128, fp32 or bf16 storage (bf16 with Dk = Dv =
+    64 and 64-token segments would take the tensor cores, so those pick
+    16-token segments), segment lengths multiples of 16, packed sequences with
+    starts anywhere, shared query rows, gate and write-strength shifts."""
+    rng = np.random.default_rng(300 + seed)
+    Dk = int(rng.choice([16, 32, 64, 128]))
+    Dv = 8 * int(rng.integers(1, 17))
+    dtype = torch.float32 if rng.integers(0, 2) else torch.bfloat16
+    nseg = int(rng.choice([1, 2, 4, 8]))
+    L = 16 * int(rng.integers(1, 5))
+    if L % 64 == 0:
+        L += 16
+    T = nseg * L
+    packed = bool(rng.integers(0, 2))
+    B = 1 if packed else int(rng.integers(1, 3))
+    H = int(rng.choice([1, 2, 4]))
+    qh = int(rng.choice([0, 1])) if H > 1 else 0
+    cu = None
+    if packed:
+        cuts = sorted(set(int(x) for x in rng.integers(1, T, size=int(rng.integers(1, 6)))))
+        cu = [0] + cuts + [T]
+    run_case(B, T, H, Dk, Dv, dtype, nseg=nseg, cu=cu, qh=qh, seed=400 + seed,
+             gshift=float(rng.uniform(-1.0, 4.0)), bshift=float(rng.uniform(-2.0, 2.0)))
