@@ -22,8 +22,10 @@
 //                     owners of D, column-local for the same reason).
 //   gdr_compose       the prefix fold S <- M_i S + dS_i over [pre_j, j), or
 //                     the suffix fold D <- M_i^T D + gamma_i over (j, fol_j),
-//                     one CTA per (row, head, block of 16 columns), M_i and
-//                     the carried block in shared memory, a row per thread.
+//                     one CTA per (row, head, block of 4 columns), the
+//                     carried block in shared memory, each lane's part of a
+//                     row of M_i in registers (a row per lane up to Dk = 64,
+//                     half a row at Dk = 128).
 //   gdr_dq_sweep      the state in shared memory from S_in (k^T S by column
 //                     partitions, the update over all elements, dq_t = scale
 //                     S_t dO_t by row owners); writes the state before every
