@@ -236,6 +236,29 @@ def test_tc_wide_grid_value_blocks():
     check_case(1, 1024, 16, 128, 256, torch.bfloat16, nseg=16, chunk=64, seed=5)
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_tc_random_shapes(seed):
+    """Seeded random problems on the tensor-core sweeps: rows, heads, Dv in
+    {128, 256}, segment count (not only powers of two) and length (multiples
+    of 64), packed sequences (one row) with starts anywhere, and gate shifts
+    from strong to weak decay (the wide-grid cases above cover more CTAs than
+    SMs)."""
+    rng = np.random.default_rng(500 + seed)
+    nseg = int(rng.choice([1, 2, 3, 4, 8]))
+    L = 64 * int(rng.integers(1, 5))
+    T = nseg * L
+    packed = bool(rng.integers(0, 2))
+    B = 1 if packed else int(rng.integers(1, 3))
+    H = int(rng.choice([1, 2, 4, 8, 16]))
+    Dv = int(rng.choice([128, 256]))
+    cu = None
+    if packed:
+        cuts = sorted(set(int(x) for x in rng.integers(1, T, size=int(rng.integers(1, 7)))))
+        cu = [0] + cuts + [T]
+    check_case(B, T, H, 128, Dv, torch.bfloat16, nseg=nseg, chunk=64, cu=cu, seed=600 + seed,
+               gate_shift=float(rng.uniform(-1.0, 5.0)))
+
+
 # ------------------------------------------------------------------ from host memory
 
 @pytest.mark.parametrize("backward", [True, False])
