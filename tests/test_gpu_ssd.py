@@ -105,6 +105,33 @@ def test_ssd_generic_fp32_one_group_per_head():
     check(2, 256, 4, 4, 32, 16, torch.float32, nseg=4, seed=3)
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_ssd_random_shapes(seed):
+    """Seeded random SSD problems: heads and groups (G divides H), the
+    tensor-core shapes (bf16, N = 128, P in {128, 256}, 64-token segments) or
+    generic ones (fp32, N and P smaller powers of two), with or without D,
+    packed sequences (one row) with starts anywhere."""
+    rng = np.random.default_rng(700 + seed)
+    tc = seed % 2 == 0
+    H = int(rng.choice([2, 4, 8]))
+    G = int(rng.choice([g for g in (1, 2, 4) if H % g == 0]))
+    if tc:
+        N, P, dtype, L = 128, int(rng.choice([128, 256])), torch.bfloat16, 64 * int(rng.integers(1, 4))
+    else:
+        # the maps take N / 4 and P / 4 powers of two for fp32
+        N, P, dtype, L = int(rng.choice([16, 32, 64])), int(rng.choice([8, 16, 32, 64])), torch.float32, \
+            16 * int(rng.integers(1, 5))
+    nseg = int(rng.choice([1, 2, 4]))
+    T = nseg * L
+    packed = bool(rng.integers(0, 2))
+    B = 1 if packed else int(rng.integers(1, 3))
+    cu = None
+    if packed:
+        cuts = sorted(set(int(x) for x in rng.integers(1, T, size=int(rng.integers(1, 5)))))
+        cu = [0] + cuts + [T]
+    check(B, T, H, G, N, P, dtype, nseg, cu=cu, with_D=bool(rng.integers(0, 2)), seed=800 + seed)
+
+
 @pytest.mark.slow
 def test_ssd32k_full_size():
     """The benchmarked ssd32k configuration at full size (16 heads in one
