@@ -474,8 +474,9 @@ rm_status rm_ssd_finish_backward(const rm_cp_problem* p, int32_t G, const void* 
  * tensor cores in the chunkwise WY/UT form (per 64-token chunk the products
  * of the I - beta k k^T factors as one triangular solve); everything else,
  * and the two folds, on generic fp32-arithmetic kernels (at Dk = 128 a slow
- * fallback: the reverse sweep keeps one state in shared memory and rebuilds
- * each token's incoming state from its 16-token checkpoint).  ws:
+ * fallback; with Dv > 64 there the backward apply runs its reverse sweep on
+ * each half of the value columns in turn, and the workspace also holds the
+ * first half's partial dk, dbeta and dg: B T H (Dk + 2) fp32 more).  ws:
  * rm_gdr_workspace_size bytes (B H (T / 16) Dk Dv fp32), one workspace for
  * the whole step, passed unchanged to every call that takes it: the backward
  * prepare saves states there for the backward apply (every 16 tokens, every

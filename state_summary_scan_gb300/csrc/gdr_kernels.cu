@@ -518,22 +518,36 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_dq_sweep(Dims d, const T* _
 // first slot advanced in place to the group's start, the others one step
 // apart), then for each token t of the group (last first):
 // D_t = scale q_t dO_t^T + (t at the segment end ? dS_out : A_{t+1} D_{t+1}),
-// and the gradients follow.  The stack holds rev_slots(Dk, Dv) states (four,
-// or fewer where four do not fit in shared memory, e.g. one at Dk = Dv = 128).
-// grid (nseg, B*H); block kSweepThreads.
+// and the gradients follow.  The stack holds four states, or fewer where
+// four do not fit in shared memory.  The value columns are independent given
+// k, so where four states of all Dv columns do not fit (Dk = 128, Dv > 64)
+// the sweep runs twice, on columns [0, Dv/2) and then [Dv/2, Dv): dv is
+// written per half, and the first launch leaves its partial dk, dbeta and dg
+// (sums over the columns) in fp32 in the workspace, where the second adds
+// its own before writing them.  grid (nseg, B*H); block kSweepThreads.
 // ---------------------------------------------------------------------------
 constexpr int kSlots = 4;
 constexpr size_t kRevSmemLimit = 227 * 1024;
 
-size_t rev_smem_bytes(const Dims& d, int slots) {
-    const int nprt = kSweepThreads / d.Dv > 0 ? kSweepThreads / d.Dv : 1;
-    return sizeof(float) * ((1 + size_t(slots)) * size_t(d.Dk) * (d.Dv + 1) +
-                            size_t(kBlk) * (2 * d.Dk + 2 * d.Dv) + size_t(nprt + 2) * d.Dv);
+size_t rev_smem_bytes(int Dk, int ncol, int slots) {
+    const int nprt = kSweepThreads / ncol > 0 ? kSweepThreads / ncol : 1;
+    return sizeof(float) * ((1 + size_t(slots)) * size_t(Dk) * (ncol + 1) +
+                            size_t(kBlk) * (2 * Dk + 2 * ncol) + size_t(nprt + 2) * ncol);
 }
-int rev_slots(const Dims& d) {
+int rev_slots(int Dk, int ncol) {
     int s = kSlots;
-    while (s > 1 && rev_smem_bytes(d, s) > kRevSmemLimit) s /= 2;  // kBlk stays a multiple
+    while (s > 1 && rev_smem_bytes(Dk, ncol, s) > kRevSmemLimit) s /= 2;  // kBlk stays a multiple
     return s;
+}
+// column parts of the reverse sweep: 2 where four states of all columns do
+// not fit but four of half of them do
+int rev_parts(const Dims& d) {
+    return rev_slots(d.Dk, d.Dv) < kSlots && d.Dv % 16 == 0 && rev_slots(d.Dk, d.Dv / 2) == kSlots ? 2 : 1;
+}
+// bytes of the partial sums a two-part reverse sweep keeps: per (row, token,
+// head) Dk values of dk, then dbeta's and dg's sums
+size_t rev_part_bytes(const Dims& d) {
+    return rev_parts(d) > 1 ? size_t(d.B) * d.T * d.H * (d.Dk + 2) * sizeof(float) : 0;
 }
 
 template <int DK, typename T>
@@ -547,20 +561,24 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
                                                          const float* __restrict__ ckpt,
                                                          T* __restrict__ dk, T* __restrict__ dv,
                                                          float* __restrict__ dg,
-                                                         float* __restrict__ dbeta, int nslots) {
+                                                         float* __restrict__ dbeta, int nslots, int col0,
+                                                         int ncol, int mode, float* __restrict__ part) {
+    // columns [col0, col0 + ncol) of the state (d.Dv is the storage stride);
+    // mode 0: every column, 1: the first part (partial sums to part), 2: the
+    // last part (adds part's partial sums)
     extern __shared__ float smem[];
-    const int pitch = d.Dv + 1;
+    const int pitch = ncol + 1;
     const int spitch = DK * pitch;     // floats per state
-    const int nprt = blockDim.x / d.Dv > 0 ? int(blockDim.x) / d.Dv : 1;
+    const int nprt = blockDim.x / ncol > 0 ? int(blockDim.x) / ncol : 1;
     float* D = smem;                   // [DK][pitch]
     float* St = D + spitch;            // [nslots][DK][pitch]
     float* kb = St + nslots * spitch;  // [kBlk][DK]
     float* qb = kb + kBlk * DK;        // [kBlk][DK]
-    float* vb = qb + kBlk * DK;        // [kBlk][Dv]
-    float* ob = vb + kBlk * d.Dv;      // [kBlk][Dv]
-    float* ksp = ob + kBlk * d.Dv;     // [nprt][Dv]
-    float* ks = ksp + nprt * d.Dv;     // [Dv]  S_{t-1}^T k
-    float* w = ks + d.Dv;              // [Dv]  D^T k
+    float* vb = qb + kBlk * DK;        // [kBlk][ncol]
+    float* ob = vb + kBlk * ncol;      // [kBlk][ncol]
+    float* ksp = ob + kBlk * ncol;     // [nprt][ncol]
+    float* ks = ksp + nprt * ncol;     // [ncol]  S_{t-1}^T k
+    float* w = ks + ncol;              // [ncol]  D^T k
     __shared__ float alb[kBlk], beb[kBlk];
     __shared__ float red[2][kSweepThreads / 32];  // per-warp partials: k.u - alpha k.s2, <D, S>
 
@@ -572,17 +590,26 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 
     // D carries A_{t+1} D_{t+1} between tokens; it starts as dS_out
-    const float* dso = dS_out + sum_off(d, seg, b, h);
-    batched_copy(DK * d.Dv, [&](int e) { return __ldg(dso + e); },
-                 [&](int e, float x) { D[(e / d.Dv) * pitch + e % d.Dv] = x; });
+    const float* dso = dS_out + sum_off(d, seg, b, h) + col0;
+    batched_copy(DK * ncol, [&](int e) { return __ldg(dso + (e / ncol) * d.Dv + e % ncol); },
+                 [&](int e, float x) { D[(e / ncol) * pitch + e % ncol] = x; });
+    // the block's value-side rows, columns [col0, col0 + ncol)
+    auto stage_cols = [&](const T* __restrict__ x, int t0, float* dst) {
+        batched_copy(kBlk * ncol,
+                     [&](int e) {
+                         const int tt = e / ncol, cc = e - tt * ncol;
+                         return to_f32(x[v_off(d, b, t0 + tt, h) + col0 + cc]);
+                     },
+                     [&](int e, float val) { dst[e] = val; });
+    };
 
     for (int c = e0 - kBlk; c >= a0; c -= kBlk) {
         const float* cs = ck + int64_t((c - a0) / kBlk) * DK * d.Dv;
         __syncthreads();  // the previous block's vectors are read
         stage_rows(k, d, b, c, d.H, h, DK, kb);
         stage_rows(q, d, b, c, d.qh, h / d.qdiv, DK, qb);
-        stage_rows(v, d, b, c, d.H, h, d.Dv, vb);
-        stage_rows(dO, d, b, c, d.H, h, d.Dv, ob);
+        stage_cols(v, c, vb);
+        stage_cols(dO, c, ob);
         if (threadIdx.x < kBlk) {
             alb[threadIdx.x] = gdr_alpha(d, g, b, c + threadIdx.x, h);
             beb[threadIdx.x] = __ldg(beta + g_off(d, b, c + threadIdx.x, h));
@@ -590,15 +617,15 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
         for (int grp = kBlk / nslots - 1; grp >= 0; --grp) {
             const int r0 = grp * nslots;  // block index of the group's first token
             // slot 0 <- S_{c + r0 - 1}: the saved S_{c-1} advanced over tokens c .. c + r0 - 1
-            batched_copy(DK * d.Dv, [&](int e) { return __ldg(cs + e); },
-                         [&](int e, float x) { St[(e / d.Dv) * pitch + e % d.Dv] = x; });
+            batched_copy(DK * ncol, [&](int e) { return __ldg(cs + (e / ncol) * d.Dv + col0 + e % ncol); },
+                         [&](int e, float x) { St[(e / ncol) * pitch + e % ncol] = x; });
             __syncthreads();
             for (int r = 0; r < r0; ++r)
-                gdr_step<DK>(St, St, pitch, d.Dv, kb + r * DK, vb + r * d.Dv, alb[r], beb[r], ksp, nprt);
+                gdr_step<DK>(St, St, pitch, ncol, kb + r * DK, vb + r * ncol, alb[r], beb[r], ksp, nprt);
             // slot j <- S_{c + r0 + j - 1}
             for (int j = 1; j < nslots; ++j) {
                 const int r = r0 + j - 1;
-                gdr_step<DK>(St + (j - 1) * spitch, St + j * spitch, pitch, d.Dv, kb + r * DK, vb + r * d.Dv,
+                gdr_step<DK>(St + (j - 1) * spitch, St + j * spitch, pitch, ncol, kb + r * DK, vb + r * ncol,
                              alb[r], beb[r], ksp, nprt);
             }
             for (int j = nslots - 1; j >= 0; --j) {
@@ -606,15 +633,15 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
                 const float* S = St + j * spitch;  // S_{t-1}
                 const float* kt = kb + r * DK;
                 const float* qt = qb + r * DK;
-                const float* vt = vb + r * d.Dv;
-                const float* dot = ob + r * d.Dv;
+                const float* vt = vb + r * ncol;
+                const float* dot = ob + r * ncol;
                 const float al = alb[r], be = beb[r];
                 // D_t = scale q_t dO_t^T + (A_{t+1} D_{t+1}, already in D)
-                gdr_map<DK>(D, pitch, d.Dv, nprt,
+                gdr_map<DK>(D, pitch, ncol, nprt,
                             [&](int i, int jj, float x) { return fmaf(d.scale * qt[i], dot[jj], x); });
                 __syncthreads();
                 // column owners: w = D_t^T k_t, kS = S_{t-1}^T k_t; dv = beta w
-                for (int jj = threadIdx.x; jj < d.Dv; jj += blockDim.x) {
+                for (int jj = threadIdx.x; jj < ncol; jj += blockDim.x) {
                     float a1 = 0.f, a2 = 0.f;
 #pragma unroll 8
                     for (int i = 0; i < DK; ++i) {
@@ -623,22 +650,27 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
                     }
                     w[jj] = a1;
                     ks[jj] = a2;
-                    dv[v_off(d, b, t, h) + jj] = from_f32<T>(be * a1);
+                    dv[v_off(d, b, t, h) + col0 + jj] = from_f32<T>(be * a1);
                 }
                 __syncthreads();
                 // row owners: u = D_t v_t, s1 = S_{t-1} w, s2 = D_t kS, <D, S> row part
                 float p_kb = 0.f, p_ds = 0.f;
+                float* prow = part + ((int64_t(b) * d.T + t) * d.H + h) * (DK + 2);  // modes 1, 2
                 for (int i = threadIdx.x; i < DK; i += blockDim.x) {
                     const float* dr = D + i * pitch;
                     const float* sr = S + i * pitch;
                     float u = 0.f, s1 = 0.f, s2 = 0.f, ds = 0.f;
-                    for (int jj = 0; jj < d.Dv; ++jj) {
+                    for (int jj = 0; jj < ncol; ++jj) {
                         u = fmaf(dr[jj], vt[jj], u);
                         s1 = fmaf(sr[jj], w[jj], s1);
                         s2 = fmaf(dr[jj], ks[jj], s2);
                         ds = fmaf(dr[jj], sr[jj], ds);
                     }
-                    dk[qk_off(d, b, t, h) + i] = from_f32<T>(be * u - al * be * (s1 + s2));
+                    const float dki = be * u - al * be * (s1 + s2);
+                    if (mode == 1)
+                        prow[i] = dki;
+                    else
+                        dk[qk_off(d, b, t, h) + i] = from_f32<T>(mode == 2 ? prow[i] + dki : dki);
                     p_kb = fmaf(kt[i], u - al * s2, p_kb);
                     p_ds += ds - be * kt[i] * s2;
                 }
@@ -655,11 +687,20 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
                         s_kb += red[0][u2];
                         s_ds += red[1][u2];
                     }
-                    dbeta[g_off(d, b, t, h)] = s_kb;
-                    dg[g_off(d, b, t, h)] = starts_sequence(d.seq_idx, t) ? 0.f : al * s_ds;
+                    if (mode == 1) {
+                        prow[DK] = s_kb;
+                        prow[DK + 1] = s_ds;
+                    } else {
+                        if (mode == 2) {
+                            s_kb += prow[DK];
+                            s_ds += prow[DK + 1];
+                        }
+                        dbeta[g_off(d, b, t, h)] = s_kb;
+                        dg[g_off(d, b, t, h)] = starts_sequence(d.seq_idx, t) ? 0.f : al * s_ds;
+                    }
                 }
                 // D <- A_t D_t = alpha (D - beta k w^T), the carry into token t-1
-                gdr_map<DK>(D, pitch, d.Dv, nprt,
+                gdr_map<DK>(D, pitch, ncol, nprt,
                             [&](int i, int jj, float x) { return al * fmaf(-be * kt[i], w[jj], x); });
                 __syncthreads();
             }
@@ -735,16 +776,24 @@ rm_status launch_gdr_T(GdrOp op, const Dims& d, const GdrPtrs& p, cudaStream_t s
             break;
         }
         case GdrOp::kBackwardApply: {
-            const int nslots = rev_slots(d);
-            const size_t smem = rev_smem_bytes(d, nslots);
+            const int parts = rev_parts(d), ncol = d.Dv / parts;
+            const int nslots = rev_slots(d.Dk, ncol);
+            const size_t smem = rev_smem_bytes(d.Dk, ncol, nslots);
+            // the partial sums follow the saved states in the workspace
+            float* part = p.ws + (gdr_workspace_bytes(d) - rev_part_bytes(d)) / sizeof(float);
             RMCP_GDR_DK_SWITCH({
                 auto fn = gdr_reverse_sweep<DK, T>;
                 if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
                     return RM_ERR_CUDA;
-                fn<<<dim3(d.nseg, BH), kSweepThreads, smem, s>>>(d, q, k, v, p.g, p.beta, dO, p.dS_out, p.ws,
-                                                       static_cast<T*>(p.dk), static_cast<T*>(p.dv), p.dg,
-                                                       p.dbeta, nslots);
+                for (int pt = 0; pt < parts; ++pt) {
+                    const int mode = parts == 1 ? 0 : (pt == 0 ? 1 : 2);
+                    fn<<<dim3(d.nseg, BH), kSweepThreads, smem, s>>>(
+                        d, q, k, v, p.g, p.beta, dO, p.dS_out, p.ws, static_cast<T*>(p.dk),
+                        static_cast<T*>(p.dv), p.dg, p.dbeta, nslots, pt * ncol, ncol, mode, part);
+                    if (pt + 1 < parts && !rmcp::launch_ok()) return RM_ERR_CUDA;
+                }
             });
+            launches = parts;
             break;
         }
     }
@@ -763,8 +812,10 @@ bool gdr_supports(const Dims& d) {
 }
 
 size_t gdr_workspace_bytes(const Dims& d) {
+    // the saved states (every kBlk tokens), then the two-part reverse sweep's
+    // partial sums (where it runs in two parts)
     const size_t b = size_t(d.B) * d.H * (size_t(d.T) / kBlk) * d.Dk * d.Dv * sizeof(float);
-    return (b + 255) / 256 * 256;
+    return (b + 255) / 256 * 256 + rev_part_bytes(d);
 }
 
 rm_status launch_gdr(GdrOp op, const Dims& d, rm_dtype dt, const GdrPtrs& p, cudaStream_t s) {
