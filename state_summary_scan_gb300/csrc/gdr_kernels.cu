@@ -593,6 +593,16 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
     const float* dso = dS_out + sum_off(d, seg, b, h) + col0;
     batched_copy(DK * ncol, [&](int e) { return __ldg(dso + (e / ncol) * d.Dv + e % ncol); },
                  [&](int e, float x) { D[(e / ncol) * pitch + e % ncol] = x; });
+    // lanes per column (cp) and per row (rp) of the per-token phases: the
+    // largest power of two up to 32 that keeps all kSweepThreads busy
+    auto lanes_per = [](int n) {
+        int l = 1;
+        while (l < 32 && 2 * l * n <= kSweepThreads) l *= 2;
+        return l;
+    };
+    const int cp = lanes_per(ncol), rp = lanes_per(DK);
+    const int col_iters = (ncol + kSweepThreads / cp - 1) / (kSweepThreads / cp);
+    const int row_iters = (DK + kSweepThreads / rp - 1) / (kSweepThreads / rp);
     // the block's value-side rows, columns [col0, col0 + ncol)
     auto stage_cols = [&](const T* __restrict__ x, int t0, float* dst) {
         batched_copy(kBlk * ncol,
@@ -640,39 +650,65 @@ __global__ void __launch_bounds__(kSweepThreads) gdr_reverse_sweep(Dims d, const
                 gdr_map<DK>(D, pitch, ncol, nprt,
                             [&](int i, int jj, float x) { return fmaf(d.scale * qt[i], dot[jj], x); });
                 __syncthreads();
-                // column owners: w = D_t^T k_t, kS = S_{t-1}^T k_t; dv = beta w
-                for (int jj = threadIdx.x; jj < ncol; jj += blockDim.x) {
+                // column owners: w = D_t^T k_t, kS = S_{t-1}^T k_t; dv = beta w.
+                // cp consecutive lanes share a column (rows p, p + cp, ...) and
+                // meet by lane exchanges; every lane of a warp runs the same
+                // iterations
+                for (int it = 0; it < col_iters; ++it) {
+                    const int jj = threadIdx.x / cp + it * (kSweepThreads / cp), pp = threadIdx.x % cp;
+                    const bool live = jj < ncol;
                     float a1 = 0.f, a2 = 0.f;
-#pragma unroll 8
-                    for (int i = 0; i < DK; ++i) {
-                        a1 = fmaf(kt[i], D[i * pitch + jj], a1);
-                        a2 = fmaf(kt[i], S[i * pitch + jj], a2);
+                    if (live) {
+#pragma unroll 4
+                        for (int i = pp; i < DK; i += cp) {
+                            a1 = fmaf(kt[i], D[i * pitch + jj], a1);
+                            a2 = fmaf(kt[i], S[i * pitch + jj], a2);
+                        }
                     }
-                    w[jj] = a1;
-                    ks[jj] = a2;
-                    dv[v_off(d, b, t, h) + col0 + jj] = from_f32<T>(be * a1);
+                    for (int o = 1; o < cp; o <<= 1) {
+                        a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+                        a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+                    }
+                    if (live && pp == 0) {
+                        w[jj] = a1;
+                        ks[jj] = a2;
+                        dv[v_off(d, b, t, h) + col0 + jj] = from_f32<T>(be * a1);
+                    }
                 }
                 __syncthreads();
-                // row owners: u = D_t v_t, s1 = S_{t-1} w, s2 = D_t kS, <D, S> row part
+                // row owners: u = D_t v_t, s1 = S_{t-1} w, s2 = D_t kS, <D, S> row
+                // part; rp consecutive lanes share a row (columns p, p + rp, ...)
                 float p_kb = 0.f, p_ds = 0.f;
                 float* prow = part + ((int64_t(b) * d.T + t) * d.H + h) * (DK + 2);  // modes 1, 2
-                for (int i = threadIdx.x; i < DK; i += blockDim.x) {
-                    const float* dr = D + i * pitch;
-                    const float* sr = S + i * pitch;
+                for (int it = 0; it < row_iters; ++it) {
+                    const int i = threadIdx.x / rp + it * (kSweepThreads / rp), pp = threadIdx.x % rp;
+                    const bool live = i < DK;
                     float u = 0.f, s1 = 0.f, s2 = 0.f, ds = 0.f;
-                    for (int jj = 0; jj < ncol; ++jj) {
-                        u = fmaf(dr[jj], vt[jj], u);
-                        s1 = fmaf(sr[jj], w[jj], s1);
-                        s2 = fmaf(dr[jj], ks[jj], s2);
-                        ds = fmaf(dr[jj], sr[jj], ds);
+                    if (live) {
+                        const float* dr = D + i * pitch;
+                        const float* sr = S + i * pitch;
+                        for (int jj = pp; jj < ncol; jj += rp) {
+                            u = fmaf(dr[jj], vt[jj], u);
+                            s1 = fmaf(sr[jj], w[jj], s1);
+                            s2 = fmaf(dr[jj], ks[jj], s2);
+                            ds = fmaf(dr[jj], sr[jj], ds);
+                        }
                     }
-                    const float dki = be * u - al * be * (s1 + s2);
-                    if (mode == 1)
-                        prow[i] = dki;
-                    else
-                        dk[qk_off(d, b, t, h) + i] = from_f32<T>(mode == 2 ? prow[i] + dki : dki);
-                    p_kb = fmaf(kt[i], u - al * s2, p_kb);
-                    p_ds += ds - be * kt[i] * s2;
+                    for (int o = 1; o < rp; o <<= 1) {
+                        u += __shfl_xor_sync(0xffffffffu, u, o);
+                        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+                        s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+                        ds += __shfl_xor_sync(0xffffffffu, ds, o);
+                    }
+                    if (live && pp == 0) {
+                        const float dki = be * u - al * be * (s1 + s2);
+                        if (mode == 1)
+                            prow[i] = dki;
+                        else
+                            dk[qk_off(d, b, t, h) + i] = from_f32<T>(mode == 2 ? prow[i] + dki : dki);
+                        p_kb = fmaf(kt[i], u - al * s2, p_kb);
+                        p_ds += ds - be * kt[i] * s2;
+                    }
                 }
                 p_kb = warp_sum(p_kb);
                 p_ds = warp_sum(p_ds);
